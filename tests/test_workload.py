@@ -1,0 +1,47 @@
+"""Host generator: exactness, determinism, statistics and structure."""
+import numpy as np
+
+from block_sparse_kv_pred_gb300 import workload as W
+
+
+def test_irwin_hall_exact_in_fp32_and_deterministic():
+    idx = np.arange(0, 50000, dtype=np.uint64)
+    z = W.irwin_hall(0, W.STREAM_K, idx)
+    # every value is an integer multiple of 2^-16 in [-6, 6)
+    scaled = (z.astype(np.float64) + 6.0) * 65536.0
+    assert np.all(scaled == np.round(scaled)) and z.min() >= -6 and z.max() < 6
+    assert np.array_equal(z, W.irwin_hall(0, W.STREAM_K, idx))
+    # random access: any slice equals the matching part of the full draw
+    assert np.array_equal(z[1234:1300], W.irwin_hall(0, W.STREAM_K, idx[1234:1300]))
+    # streams and seeds differ
+    assert not np.array_equal(z[:100], W.irwin_hall(0, W.STREAM_V, idx[:100]))
+    assert not np.array_equal(z[:100], W.irwin_hall(1, W.STREAM_K, idx[:100]))
+
+
+def test_irwin_hall_moments():
+    z = W.irwin_hall(3, W.STREAM_Q, np.arange(400000, dtype=np.uint64)).astype(np.float64)
+    assert abs(z.mean()) < 0.01
+    assert abs(z.var() - 1.0) < 0.01
+
+
+def test_workload_structure():
+    s = W.Shape("t", B=2, Hq=8, Hkv=2, T=1000, P=32, k=8, resident_frac=0.25, seq_lens=(1000, 777))
+    wl = W.Workload(s)
+    nb = s.nblk
+    assert sorted(wl.page_table.ravel().tolist()) == list(range(s.units * nb))
+    for u in range(s.units):
+        nv = int(wl.nvalid[u // s.Hkv])
+        assert wl.resident[u].sum() == round(0.25 * nv)
+        assert wl.heavy[u].sum() == round(0.05 * nv)
+        assert wl.resident[u, nv:].sum() == 0 and wl.heavy[u, nv:].sum() == 0
+    bits = wl.resident_bits().reshape(s.units, s.words)
+    for u in range(s.units):
+        for j in range(nb):
+            assert ((int(bits[u, j // 32]) >> (j % 32)) & 1) == wl.resident[u, j]
+    K = wl.unit_kv(1)
+    assert K.shape == (nb * s.P, s.D) and K.dtype == np.uint16
+    # outlier channels carry about outlier_scale times the spread
+    Kf = W.bf16_to_f32(K).astype(np.float64)
+    non_heavy = ~np.repeat(wl.heavy[1].astype(bool), s.P)
+    sd = Kf[non_heavy].std(axis=0)
+    assert np.all(sd[wl.outliers] > 6.0) and np.median(sd) < 1.2
