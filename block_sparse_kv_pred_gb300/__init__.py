@@ -1,0 +1,227 @@
+"""Python binding of libscout (block-sparse decode attention for GB300, sm_103a).
+
+Argument marshalling only: every entry point forwards device pointers of torch
+tensors, sizes and the current CUDA stream to the C ABI declared in
+``include/scout.h``; all arithmetic runs in the library's CUDA kernels.  There is
+no fallback: if ``libscout.so`` is missing or fails to load, every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+__all__ = [
+    "ScoutError", "lib", "MINMAX", "MEAN", "predict_q", "build_digest", "score_topk", "score_topk_workspace",
+    "sparse_attn", "sparse_attn_workspace", "merge", "recall_async", "commit_residency", "RecallOp",
+]
+
+MINMAX = 0
+MEAN = 1
+_KIND = {"minmax": MINMAX, "mean": MEAN, MINMAX: MINMAX, MEAN: MEAN}
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+_LIB = None
+
+_p = ctypes.c_void_p
+_i = ctypes.c_int
+_i64 = ctypes.c_int64
+_f = ctypes.c_float
+_sz = ctypes.c_size_t
+
+
+class ScoutError(RuntimeError):
+    pass
+
+
+class RecallOp(ctypes.Structure):
+    _fields_ = [("unit", ctypes.c_int32), ("block", ctypes.c_int32), ("slot", ctypes.c_int32),
+                ("evict_block", ctypes.c_int32)]
+
+
+_SIGS = {
+    "scout_status_string": ([_i], ctypes.c_char_p),
+    "scout_version": ([], _i),
+    "scout_predict_q": ([_p, _p, _p, _i, _i, _i, _p], _i),
+    "scout_build_digest": ([_i, _p, _i64, _p, _p, _i, _i, _i, _i, _i, _p, _i, _p, _p, _p], _i),
+    "scout_score_topk_workspace_bytes": ([_i, _i, _i], _sz),
+    "scout_score_topk": ([_i, _p, _p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _i, _p, _p, _p, _p, _p, _p, _p, _p,
+                          _p, _p, _sz, _p], _i),
+    "scout_sparse_attn_workspace_bytes": ([_i, _i, _i, _i, _i], _sz),
+    "scout_sparse_attn": ([_p, _p, _p, _i64, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _i, _f, _p, _p, _p, _sz, _p,
+                           _p], _i),
+    "scout_merge": ([_p, _p, _p, _p, _i, _i, _p, _p, _p], _i),
+    "scout_recall_async": ([_p, _i, _p, _p, _p, _p, _i64, _i, _i, _i, _i, _i, _p, _p, _p], _i),
+    "scout_commit_residency": ([_p, _i, _p, _p, _i64, _i, _i, _i, _p, _p], _i),
+}
+
+
+def lib_path() -> str:
+    return os.path.join(_PKG, "libscout.so")
+
+
+def lib():
+    """The loaded libscout (raises ScoutError when it is not built)."""
+    global _LIB
+    if _LIB is None:
+        path = lib_path()
+        if not os.path.exists(path):
+            raise ScoutError(f"{path} is missing: run `python -m block_sparse_kv_pred_gb300.build`")
+        L = ctypes.CDLL(path)
+        for name, (args, res) in _SIGS.items():
+            fn = getattr(L, name)
+            fn.argtypes = args
+            fn.restype = res
+        _LIB = L
+    return _LIB
+
+
+def _check(rc: int, what: str):
+    if rc != 0:
+        raise ScoutError(f"{what}: {lib().scout_status_string(rc).decode()}")
+
+
+def _stream(stream) -> int:
+    s = torch.cuda.current_stream() if stream is None else stream
+    return s.cuda_stream
+
+
+def _dev(t: torch.Tensor, dtype, name: str) -> int:
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise ScoutError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise ScoutError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ScoutError(f"{name} must be contiguous")
+    return t.data_ptr()
+
+
+def _opt(t, dtype, name):
+    return None if t is None else _dev(t, dtype, name)
+
+
+# ---------------------------------------------------------------------------
+def predict_q(X: torch.Tensor, W: torch.Tensor, Q: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Q_pred = X W^T (bf16 in, fp32 accumulate, bf16 out)."""
+    M, K = X.shape
+    N = W.shape[0]
+    if Q is None:
+        Q = torch.empty((M, N), dtype=torch.bfloat16, device=X.device)
+    _check(lib().scout_predict_q(_dev(X, torch.bfloat16, "X"), _dev(W, torch.bfloat16, "W"),
+                                 _dev(Q, torch.bfloat16, "Q"), M, N, K, _stream(stream)), "scout_predict_q")
+    return Q
+
+
+def build_digest(kind, K_pool, page_table, seq_len, B, Hkv, P, digest, block_list=None, status=None,
+                 stream=None):
+    kind = _KIND[kind]
+    nblk_cap = page_table.shape[-1]
+    n_slots = K_pool.shape[0]
+    ddt = torch.bfloat16 if kind == MINMAX else torch.float32
+    n_list = 0 if block_list is None else block_list.shape[0]
+    _check(lib().scout_build_digest(kind, _dev(K_pool, torch.bfloat16, "K_pool"), n_slots,
+                                    _dev(page_table, torch.int32, "page_table"), _dev(seq_len, torch.int32, "seq_len"),
+                                    B, Hkv, K_pool.shape[-1], P, nblk_cap, _opt(block_list, torch.int32, "block_list"),
+                                    n_list, _dev(digest, ddt, "digest"), _opt(status, torch.int32, "status"),
+                                    _stream(stream)), "scout_build_digest")
+    return digest
+
+
+def score_topk_workspace(B, Hkv, nblk_cap, device="cuda") -> torch.Tensor:
+    n = lib().scout_score_topk_workspace_bytes(B, Hkv, nblk_cap)
+    return torch.zeros(n, dtype=torch.uint8, device=device)
+
+
+def score_topk(kind, q, digest, seq_len, resident_bits, B, Hq, Hkv, P, nblk_cap, k, workspace, out=None,
+               prev_cpu=None, scores=None, stream=None) -> dict:
+    """Score digests, select top-k per unit, split by residency.
+
+    ``out`` (optional) is a dict of preallocated outputs with the keys returned.
+    ``prev_cpu`` is an optional (list, count) pair from the previous step.
+    """
+    kind = _KIND[kind]
+    dev = q.device
+    U = B * Hkv
+    if out is None:
+        out = {}
+        for name in ("topk", "res", "cpu", "delta"):
+            out[name] = torch.empty((B, Hkv, k), dtype=torch.int32, device=dev)
+            out[name + "_count"] = torch.empty((B, Hkv), dtype=torch.int32, device=dev)
+    pl, pc = (None, None) if prev_cpu is None else prev_cpu
+    ddt = torch.bfloat16 if kind == MINMAX else torch.float32
+    _check(lib().scout_score_topk(
+        kind, _dev(q, torch.bfloat16, "q"), _dev(digest, ddt, "digest"), _dev(seq_len, torch.int32, "seq_len"),
+        _dev(resident_bits, torch.int32, "resident_bits"), _opt(pl, torch.int32, "prev_cpu_list"),
+        _opt(pc, torch.int32, "prev_cpu_count"), B, Hq, Hkv, q.shape[-1], P, nblk_cap, k,
+        _opt(scores, torch.float32, "scores"),
+        _dev(out["topk"], torch.int32, "topk"), _dev(out["topk_count"], torch.int32, "topk_count"),
+        _dev(out["res"], torch.int32, "res"), _dev(out["res_count"], torch.int32, "res_count"),
+        _dev(out["cpu"], torch.int32, "cpu"), _dev(out["cpu_count"], torch.int32, "cpu_count"),
+        _dev(out["delta"], torch.int32, "delta"), _dev(out["delta_count"], torch.int32, "delta_count"),
+        _dev(workspace, torch.uint8, "workspace"), workspace.numel(), _stream(stream)), "scout_score_topk")
+    if scores is not None:
+        out["scores"] = scores
+    del U
+    return out
+
+
+def sparse_attn_workspace(B, Hq, Hkv, P, D=128, device="cuda") -> torch.Tensor:
+    n = lib().scout_sparse_attn_workspace_bytes(B, Hq, Hkv, D, P)
+    return torch.zeros(n, dtype=torch.uint8, device=device)
+
+
+def sparse_attn(q, K_pool, V_pool, page_table, seq_len, res_list, res_count, B, Hq, Hkv, P, k, scale, workspace,
+                O=None, lse=None, status=None, stream=None):
+    """GPU partial attention over the resident selected blocks -> (O fp32 [B][Hq][D], lse fp32 [B][Hq])."""
+    D = q.shape[-1]
+    if O is None:
+        O = torch.empty((B, Hq, D), dtype=torch.float32, device=q.device)
+    if lse is None:
+        lse = torch.empty((B, Hq), dtype=torch.float32, device=q.device)
+    _check(lib().scout_sparse_attn(
+        _dev(q, torch.bfloat16, "q"), _dev(K_pool, torch.bfloat16, "K_pool"), _dev(V_pool, torch.bfloat16, "V_pool"),
+        K_pool.shape[0], _dev(page_table, torch.int32, "page_table"), _dev(seq_len, torch.int32, "seq_len"),
+        _dev(res_list, torch.int32, "res_list"), _dev(res_count, torch.int32, "res_count"), B, Hq, Hkv, D, P,
+        page_table.shape[-1], k, float(scale), _dev(O, torch.float32, "O"), _dev(lse, torch.float32, "lse"),
+        _dev(workspace, torch.uint8, "workspace"), workspace.numel(), _opt(status, torch.int32, "status"),
+        _stream(stream)), "scout_sparse_attn")
+    return O, lse
+
+
+def merge(O_a, lse_a, O_b, lse_b, O_out=None, lse_out=None, stream=None):
+    """LSE merge of two partials -> (O bf16, lse fp32)."""
+    D = O_a.shape[-1]
+    rows = O_a.numel() // D
+    if O_out is None:
+        O_out = torch.empty(O_a.shape, dtype=torch.bfloat16, device=O_a.device)
+    if lse_out is None:
+        lse_out = torch.empty(lse_a.shape, dtype=torch.float32, device=O_a.device)
+    _check(lib().scout_merge(_dev(O_a, torch.float32, "O_a"), _dev(lse_a, torch.float32, "lse_a"),
+                             _dev(O_b, torch.float32, "O_b"), _dev(lse_b, torch.float32, "lse_b"), rows, D,
+                             _dev(O_out, torch.bfloat16, "O_out"), _dev(lse_out, torch.float32, "lse_out"),
+                             _stream(stream)), "scout_merge")
+    return O_out, lse_out
+
+
+def recall_async(ops, host_K, host_V, K_pool, V_pool, B, Hkv, P, nblk_cap, side_stream, wait_event=None,
+                 done_event=None):
+    """Queue host->pool copies of recalled blocks on side_stream. ``ops``: list of (unit, block, slot, evict)."""
+    arr = (RecallOp * max(1, len(ops)))(*[RecallOp(*o) for o in ops])
+    for t, n in ((host_K, "host_K"), (host_V, "host_V")):
+        if t.is_cuda or not t.is_contiguous() or t.dtype != torch.bfloat16:
+            raise ScoutError(f"{n} must be a contiguous bf16 host tensor")
+    _check(lib().scout_recall_async(arr, len(ops), host_K.data_ptr(), host_V.data_ptr(),
+                                    _dev(K_pool, torch.bfloat16, "K_pool"), _dev(V_pool, torch.bfloat16, "V_pool"),
+                                    K_pool.shape[0], B, Hkv, K_pool.shape[-1], P, nblk_cap,
+                                    None if wait_event is None else wait_event.cuda_event, side_stream.cuda_stream,
+                                    None if done_event is None else done_event.cuda_event), "scout_recall_async")
+
+
+def commit_residency(d_ops, page_table, resident_bits, n_slots, B, Hkv, wait_event=None, stream=None):
+    """Apply recall ops (device int32 [n][4]) to the page table and residency bits after wait_event."""
+    n = 0 if d_ops is None else d_ops.shape[0]
+    _check(lib().scout_commit_residency(_opt(d_ops, torch.int32, "ops"), n, _dev(page_table, torch.int32, "page_table"),
+                                        _dev(resident_bits, torch.int32, "resident_bits"), n_slots, B, Hkv,
+                                        page_table.shape[-1], None if wait_event is None else wait_event.cuda_event,
+                                        _stream(stream)), "scout_commit_residency")

@@ -1,0 +1,90 @@
+// Asynchronous periodic recall (host side) and the residency commit.
+// ScoutAttention (arXiv HTML), section 3.4: important blocks are copied back from
+// host memory into GPU memory after a layer's attention, on a path that does not
+// block inference; they are first needed at the same layer of the next step.
+//
+// The copies run on a side stream as plain cudaMemcpyAsync calls (one per run of
+// consecutive blocks landing in consecutive slots).  Page table and residency
+// bits change only in scout_commit_residency, which the caller orders after the
+// copies' event, so a block never looks resident before its bytes have landed.
+#include "common.cuh"
+
+namespace scout {
+namespace {
+
+__global__ void commit_kernel(const scout_recall_op* __restrict__ ops, int n, int32_t* __restrict__ page_table,
+                              uint32_t* __restrict__ bits, int64_t n_slots, int units, int nblk_cap, int words) {
+  // a single CTA: evictions first, then insertions, so a slot handed over
+  // within one recall ends up owned by its new block
+  for (int i = threadIdx.x; i < n; i += blockDim.x) {
+    const scout_recall_op op = ops[i];
+    if (op.unit < 0 || op.unit >= units || op.evict_block < 0 || op.evict_block >= nblk_cap) continue;
+    page_table[(int64_t)op.unit * nblk_cap + op.evict_block] = -1;
+    atomicAnd(&bits[(int64_t)op.unit * words + (op.evict_block >> 5)], ~(1u << (op.evict_block & 31)));
+  }
+  __syncthreads();
+  for (int i = threadIdx.x; i < n; i += blockDim.x) {
+    const scout_recall_op op = ops[i];
+    if (op.unit < 0 || op.unit >= units || op.block < 0 || op.block >= nblk_cap || op.slot < 0 || op.slot >= n_slots)
+      continue;
+    page_table[(int64_t)op.unit * nblk_cap + op.block] = op.slot;
+    atomicOr(&bits[(int64_t)op.unit * words + (op.block >> 5)], 1u << (op.block & 31));
+  }
+}
+
+}  // namespace
+}  // namespace scout
+
+extern "C" int scout_recall_async(const scout_recall_op* ops, int n_ops, const void* host_K, const void* host_V,
+                                  void* K_pool, void* V_pool, int64_t n_slots, int B, int Hkv, int D, int P,
+                                  int nblk_cap, cudaEvent_t wait_event, cudaStream_t side_stream,
+                                  cudaEvent_t done_event) {
+  using namespace scout;
+  if (n_ops < 0 || (n_ops > 0 && ops == nullptr) || host_K == nullptr || host_V == nullptr || K_pool == nullptr ||
+      V_pool == nullptr || B <= 0 || Hkv <= 0 || nblk_cap <= 0 || n_slots <= 0)
+    return SCOUT_ERR_INVALID_ARG;
+  if (D != kD || !valid_P(P)) return SCOUT_ERR_UNSUPPORTED;
+  const int64_t units = (int64_t)B * Hkv;
+  for (int i = 0; i < n_ops; ++i) {
+    const scout_recall_op& op = ops[i];
+    if (op.unit < 0 || op.unit >= units || op.block < 0 || op.block >= nblk_cap || op.slot < 0 || op.slot >= n_slots ||
+        op.evict_block < -1 || op.evict_block >= nblk_cap)
+      return SCOUT_ERR_INVALID_ARG;
+  }
+  if (wait_event != nullptr && cudaStreamWaitEvent(side_stream, wait_event, 0) != cudaSuccess) return SCOUT_ERR_CUDA;
+  const size_t page = (size_t)P * kD * 2;
+  const auto* hK = static_cast<const uint8_t*>(host_K);
+  const auto* hV = static_cast<const uint8_t*>(host_V);
+  auto* dK = static_cast<uint8_t*>(K_pool);
+  auto* dV = static_cast<uint8_t*>(V_pool);
+  int i = 0;
+  while (i < n_ops) {
+    // extend the run while source blocks and destination slots are both consecutive
+    int r = 1;
+    while (i + r < n_ops && ops[i + r].unit == ops[i].unit && ops[i + r].block == ops[i].block + r &&
+           ops[i + r].slot == ops[i].slot + r)
+      ++r;
+    const size_t src = ((size_t)ops[i].unit * nblk_cap + ops[i].block) * page;
+    const size_t dst = (size_t)ops[i].slot * page;
+    if (cudaMemcpyAsync(dK + dst, hK + src, page * r, cudaMemcpyHostToDevice, side_stream) != cudaSuccess ||
+        cudaMemcpyAsync(dV + dst, hV + src, page * r, cudaMemcpyHostToDevice, side_stream) != cudaSuccess)
+      return SCOUT_ERR_CUDA;
+    i += r;
+  }
+  if (done_event != nullptr && cudaEventRecord(done_event, side_stream) != cudaSuccess) return SCOUT_ERR_CUDA;
+  return SCOUT_OK;
+}
+
+extern "C" int scout_commit_residency(const scout_recall_op* d_ops, int n_ops, int32_t* page_table,
+                                      uint32_t* resident_bits, int64_t n_slots, int B, int Hkv, int nblk_cap,
+                                      cudaEvent_t wait_event, cudaStream_t stream) {
+  using namespace scout;
+  if (n_ops < 0 || (n_ops > 0 && d_ops == nullptr) || page_table == nullptr || resident_bits == nullptr || B <= 0 ||
+      Hkv <= 0 || nblk_cap <= 0 || n_slots <= 0)
+    return SCOUT_ERR_INVALID_ARG;
+  if (wait_event != nullptr && cudaStreamWaitEvent(stream, wait_event, 0) != cudaSuccess) return SCOUT_ERR_CUDA;
+  if (n_ops == 0) return SCOUT_OK;
+  commit_kernel<<<1, 1024, 0, stream>>>(d_ops, n_ops, page_table, resident_bits, n_slots, B * Hkv, nblk_cap,
+                                        (nblk_cap + 31) / 32);
+  return launch_status();
+}

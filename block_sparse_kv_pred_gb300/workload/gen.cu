@@ -76,10 +76,12 @@ int grid_for(int64_t n) {
 
 }  // namespace
 
+#define GEN_API __attribute__((visibility("default")))
+
 extern "C" {
 
 // Fill dst[0..n) with bf16(z * sigma), z the Irwin-Hall variate of counter offset + i.
-int scoutgen_fill_normal_bf16(void* dst, int64_t n, uint64_t seed, uint64_t stream, float sigma, int64_t offset,
+GEN_API int scoutgen_fill_normal_bf16(void* dst, int64_t n, uint64_t seed, uint64_t stream, float sigma, int64_t offset,
                               cudaStream_t st) {
   if (n <= 0) return 0;
   fill_normal_bf16<<<grid_for(n), 256, 0, st>>>((__nv_bfloat16*)dst, n, key_of(seed, stream), sigma, offset);
@@ -87,7 +89,7 @@ int scoutgen_fill_normal_bf16(void* dst, int64_t n, uint64_t seed, uint64_t stre
 }
 
 // Fill a paged K or V pool from the logical per-unit tensors (see Workload.unit_kv).
-int scoutgen_fill_pool_bf16(void* pool, int64_t n_slots, int P, int D, const int32_t* owner, int nblk, uint64_t seed,
+GEN_API int scoutgen_fill_pool_bf16(void* pool, int64_t n_slots, int P, int D, const int32_t* owner, int nblk, uint64_t seed,
                             uint64_t stream, const float* chan_scale, const uint8_t* heavy, const float* hdir,
                             cudaStream_t st) {
   if (n_slots <= 0) return 0;

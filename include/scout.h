@@ -1,0 +1,217 @@
+/*
+ * libscout: the GPU side of GPU-CPU collaborative block-sparse decode attention
+ * (ScoutAttention, arXiv 2603.27138), for NVIDIA GB300 (sm_103a).
+ *
+ * Conventions for every entry point
+ * ---------------------------------
+ * - Pointers are DEVICE memory owned by the caller unless the comment says host.
+ *   The library never allocates or frees device memory and never synchronises
+ *   the device; scratch space is a caller-provided workspace.
+ * - Every call is asynchronous on the given stream and returns SCOUT_OK once
+ *   the work is enqueued.  Arguments are checked on the host before any launch;
+ *   a rejected call launches nothing.  A launch failure reported by the CUDA
+ *   runtime returns SCOUT_ERR_CUDA.
+ * - bf16 tensors are IEEE bfloat16 (2 bytes); fp32 are IEEE binary32.
+ * - Shapes: B sequences, Hq query heads, Hkv KV heads (G = Hq / Hkv query heads
+ *   per KV head, 1 <= G <= 8), D = 128 head dims, P tokens per KV block
+ *   (16, 32 or 64), nblk_cap blocks per (sequence, KV head) in the tables.
+ *   A "unit" is one (sequence b, KV head h): u = b * Hkv + h.
+ * - Device-side bounds problems (a page-table slot outside the pool, a block
+ *   index outside the table) never fault: the offending block is skipped and,
+ *   when dev_status is not NULL, bit SCOUT_DEV_BAD_INDEX is OR-ed into
+ *   *dev_status.  Bounded waits that expire set SCOUT_DEV_TIMEOUT.
+ * - No C++ exception crosses this interface and the library keeps no mutable
+ *   global state: calls on different streams with different buffers are
+ *   independent.
+ */
+#ifndef SCOUT_H_
+#define SCOUT_H_
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime.h>
+
+#if defined(__GNUC__)
+#pragma GCC visibility push(default)
+#endif
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum scout_status {
+  SCOUT_OK = 0,
+  SCOUT_ERR_INVALID_ARG = 1,  /* null pointer, negative or inconsistent size */
+  SCOUT_ERR_UNSUPPORTED = 2,  /* D != 128, P not in {16,32,64}, G > 8, misaligned pointer */
+  SCOUT_ERR_WORKSPACE = 3,    /* workspace missing or smaller than *_workspace_bytes() */
+  SCOUT_ERR_CUDA = 4,         /* the CUDA runtime rejected a launch or copy */
+  SCOUT_ERR_TIMEOUT = 5       /* a bounded host-side wait expired */
+} scout_status;
+
+/* bits OR-ed into the optional device status word */
+#define SCOUT_DEV_BAD_INDEX 1
+#define SCOUT_DEV_TIMEOUT 2
+
+typedef enum scout_digest_kind {
+  SCOUT_DIGEST_MINMAX = 0, /* Quest: channel-wise min and max of K over a block */
+  SCOUT_DIGEST_MEAN = 1    /* MoBA: channel-wise mean of K over a block */
+} scout_digest_kind;
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char* scout_status_string(int status);
+
+/* Library version: major * 10000 + minor * 100 + patch. */
+int scout_version(void);
+
+/* ------------------------------------------------------------------------ *
+ * Layer-ahead query prediction.
+ * ScoutAttention (arXiv HTML), section 3.3 and Algorithm 1: the next layer's
+ * query is predicted from the current layer's input, Q_pred^{i+1} = W_Q^{i+1} X^i.
+ *
+ * X  bf16 [M][K] row-major (one row per sequence), W bf16 [N][K] row-major
+ * (linear-layer layout, N = Hq * D), Q bf16 [M][N] row-major; Q = X W^T with
+ * fp32 accumulation, rounded to nearest bf16.  Requires 1 <= M <= 256,
+ * N % 128 == 0, K % 64 == 0, and 16-byte-aligned X, W, Q.
+ * Runs on the tensor cores (tcgen05, TMA-fed).  No workspace.
+ * ------------------------------------------------------------------------ */
+int scout_predict_q(const void* X, const void* W, void* Q, int M, int N, int K, cudaStream_t stream);
+
+/* ------------------------------------------------------------------------ *
+ * Block digests.
+ * ScoutAttention (arXiv HTML), section 2.2: each fixed-size KV block is
+ * summarised by a digest; Quest uses channel-wise min/max pooling of K, MoBA
+ * mean pooling.  The digest of block j covers its valid tokens
+ * t in [jP, min((j+1)P, seq_len[b])).
+ *
+ * K_pool     bf16 [n_slots][P][D]: block j of unit u lives in slot page_table[u][j]
+ * page_table int32 [B][Hkv][nblk_cap]
+ * seq_len    int32 [B]
+ * block_list int32 [n_list][2] of (u, j) pairs to (re)build, or NULL for every
+ *            valid block of every unit (prefill).  Blocks without valid tokens
+ *            are left untouched.
+ * digest     MINMAX: bf16 [B][Hkv][nblk_cap][2][D] (min row, then max row)
+ *            MEAN:   fp32 [B][Hkv][nblk_cap][D]
+ * Min/max are exact.  The mean is a compensated fp32 sum divided by the count.
+ * ------------------------------------------------------------------------ */
+int scout_build_digest(int kind, const void* K_pool, int64_t n_slots, const int32_t* page_table,
+                       const int32_t* seq_len, int B, int Hkv, int D, int P, int nblk_cap,
+                       const int32_t* block_list, int n_list, void* digest, int32_t* dev_status,
+                       cudaStream_t stream);
+
+/* ------------------------------------------------------------------------ *
+ * Digest scoring, top-k selection and residency split.
+ * ScoutAttention (arXiv HTML), section 3.2 and Algorithm 1: the GPU takes the
+ * top-k blocks by query-digest dot product (B_pred), compares them with the
+ * blocks resident in GPU memory (B_gpu) and marks the rest for the CPU
+ * (B_cpu = B_pred \ B_gpu).
+ *
+ * Score of block j for query head h:  MINMAX  sum_c max(q_hc min_jc, q_hc max_jc)
+ *                                     MEAN    sum_c q_hc mean_jc
+ * One selection per unit: the block score is the maximum over the G query
+ * heads of the unit.  Valid blocks are j < ceil(seq_len[b] / P).
+ * Top-k: k_eff = min(k, valid blocks) blocks by (score desc, index asc).
+ *
+ * q            bf16 [B][Hq][D]   (query head hq belongs to KV head hq / G)
+ * digest       as written by scout_build_digest for the same kind
+ * resident_bits uint32 [B][Hkv][ceil(nblk_cap/32)]: bit j%32 of word j/32 set
+ *              when block j is in GPU memory
+ * prev_cpu_list int32 [B][Hkv][k] / prev_cpu_count int32 [B][Hkv]: the previous
+ *              step's CPU list, or both NULL (then delta = cpu list).  They may
+ *              alias cpu_list / cpu_count.
+ * Outputs (all [B][Hkv][k] int32 lists in ascending block order, entries past
+ * the count set to -1; counts int32 [B][Hkv]):
+ *   scores     fp32 [B][Hkv][nblk_cap] pooled scores (-inf past the valid
+ *              blocks), or NULL
+ *   topk_idx/topk_count  B_pred;  res_list/res_count  B_pred with bit set;
+ *   cpu_list/cpu_count   B_pred with bit clear;  delta_list/delta_count
+ *   cpu list minus the previous cpu list.
+ * workspace    scout_score_topk_workspace_bytes() bytes; its first
+ *              4 * B * Hkv bytes must be zero before the first use and are
+ *              left zero by every call.
+ * Requires k >= 1, nblk_cap <= 8192, G <= 8.
+ * ------------------------------------------------------------------------ */
+size_t scout_score_topk_workspace_bytes(int B, int Hkv, int nblk_cap);
+int scout_score_topk(int kind, const void* q, const void* digest, const int32_t* seq_len,
+                     const uint32_t* resident_bits, const int32_t* prev_cpu_list,
+                     const int32_t* prev_cpu_count, int B, int Hq, int Hkv, int D, int P, int nblk_cap,
+                     int k, float* scores, int32_t* topk_idx, int32_t* topk_count, int32_t* res_list,
+                     int32_t* res_count, int32_t* cpu_list, int32_t* cpu_count, int32_t* delta_list,
+                     int32_t* delta_count, void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/* ------------------------------------------------------------------------ *
+ * GPU partial attention over the resident selected blocks.
+ * ScoutAttention (arXiv HTML), section 3.2 and Algorithm 1 (A_gpu): the GPU
+ * attends the top-k blocks that reside in its memory.
+ *
+ * For query head hq of sequence b (unit u = b * Hkv + hq / G): the tokens of
+ * blocks res_list[u][0 .. res_count[u]) with t < seq_len[b];
+ * s_t = scale * q . k_t;  O_part = sum_t softmax(s)_t v_t (normalised, fp32
+ * [B][Hq][D]);  lse_part = ln sum_t exp(s_t) (fp32 [B][Hq]).  An empty set
+ * gives O = 0 and lse = -inf.  The work is balanced over the SMs by splitting
+ * the total block count evenly; split units are combined by LSE.
+ * workspace: scout_sparse_attn_workspace_bytes() bytes; its first 4 * B * Hkv
+ * bytes must be zero before the first use and are left zero by every call.
+ * K_pool / V_pool must be 16-byte aligned.  Requires G <= 8, res_count <= k.
+ * ------------------------------------------------------------------------ */
+size_t scout_sparse_attn_workspace_bytes(int B, int Hq, int Hkv, int D, int P);
+int scout_sparse_attn(const void* q, const void* K_pool, const void* V_pool, int64_t n_slots,
+                      const int32_t* page_table, const int32_t* seq_len, const int32_t* res_list,
+                      const int32_t* res_count, int B, int Hq, int Hkv, int D, int P, int nblk_cap, int k,
+                      float scale, float* O_part, float* lse_part, void* workspace, size_t workspace_bytes,
+                      int32_t* dev_status, cudaStream_t stream);
+
+/* ------------------------------------------------------------------------ *
+ * Merge of the GPU and CPU partial results.
+ * ScoutAttention (arXiv HTML), section 3.2 (FlashAttention / online-softmax
+ * combination of the two devices' intermediate results) and Algorithm 1 (MERGE).
+ *
+ * For each of rows = B * Hq query heads:  m = max(lse_a, lse_b),
+ * O = (e^{lse_a - m} O_a + e^{lse_b - m} O_b) / (e^{lse_a - m} + e^{lse_b - m}),
+ * lse = m + ln(e^{lse_a - m} + e^{lse_b - m}); two empty partials give O = 0,
+ * lse = -inf.  O_a, O_b fp32 [rows][D]; lse_a, lse_b fp32 [rows];
+ * O_out bf16 [rows][D]; lse_out fp32 [rows] (may be NULL).
+ * ------------------------------------------------------------------------ */
+int scout_merge(const float* O_a, const float* lse_a, const float* O_b, const float* lse_b, int rows, int D,
+                void* O_out, float* lse_out, cudaStream_t stream);
+
+/* ------------------------------------------------------------------------ *
+ * Asynchronous periodic recall (host side).
+ * ScoutAttention (arXiv HTML), section 3.4: important blocks are periodically
+ * copied from host memory back into GPU memory, off the critical path; the
+ * copy is started after a layer's attention and only needed one step later.
+ *
+ * One op moves block `block` of unit `unit` from the host copy of the cache
+ * into pool slot `slot`; `evict_block` (or -1) is the block that held the slot
+ * before.  host_K / host_V: host memory (pinned for asynchronous copies),
+ * layout bf16 [B][Hkv][nblk_cap][P][D].  ops is a HOST array.
+ *
+ * scout_recall_async: on side_stream, waits for wait_event (may be NULL), copies
+ * K and V of every op (adjacent ops with consecutive blocks and slots become one
+ * copy), then records done_event (may be NULL).
+ * scout_commit_residency: on stream, waits for wait_event (normally the recall's
+ * done_event), then for every op clears evict_block's page-table entry (-1) and
+ * residency bit, and afterwards sets block's entry to slot and its bit.
+ * d_ops is a DEVICE copy of the same ops.  Until the commit runs, the tables
+ * still describe the old residency, so a failed or unfinished copy never makes a
+ * block look resident.
+ * ------------------------------------------------------------------------ */
+typedef struct scout_recall_op {
+  int32_t unit;
+  int32_t block;
+  int32_t slot;
+  int32_t evict_block;
+} scout_recall_op;
+
+int scout_recall_async(const scout_recall_op* ops, int n_ops, const void* host_K, const void* host_V,
+                       void* K_pool, void* V_pool, int64_t n_slots, int B, int Hkv, int D, int P,
+                       int nblk_cap, cudaEvent_t wait_event, cudaStream_t side_stream, cudaEvent_t done_event);
+int scout_commit_residency(const scout_recall_op* d_ops, int n_ops, int32_t* page_table, uint32_t* resident_bits,
+                           int64_t n_slots, int B, int Hkv, int nblk_cap, cudaEvent_t wait_event,
+                           cudaStream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+#if defined(__GNUC__)
+#pragma GCC visibility pop
+#endif
+#endif /* SCOUT_H_ */

@@ -1,0 +1,78 @@
+"""The C-ABI library loads, exports every declared entry point, and rejects bad
+arguments on the host before any launch (no GPU needed)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import block_sparse_kv_pred_gb300 as bs
+from block_sparse_kv_pred_gb300 import build as B
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    if not os.path.exists(bs.lib_path()):
+        B.build()
+    return bs.lib()
+
+
+def declared_functions():
+    src = open(os.path.join(ROOT, "include", "scout.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(scout_[a-z_0-9]+)\s*\(", src)))
+
+
+def test_every_declared_symbol_is_exported(L):
+    names = declared_functions()
+    assert len(names) >= 11
+    for n in names:
+        assert hasattr(L, n), n
+
+
+def test_status_strings_and_version(L):
+    for code in range(6):
+        assert L.scout_status_string(code).decode().startswith("SCOUT_")
+    assert L.scout_status_string(99) == b"unknown scout status"
+    assert L.scout_version() == 10000
+
+
+def test_workspace_sizes(L):
+    assert L.scout_score_topk_workspace_bytes(40, 8, 1024) == 1280 + 40 * 8 * 1024 * 4
+    assert L.scout_score_topk_workspace_bytes(0, 8, 1024) == 0
+    assert L.scout_sparse_attn_workspace_bytes(40, 40, 8, 128, 32) > 1024 * 2 * 8 * 128 * 4
+
+
+def test_host_validation_rejects_without_launch(L):
+    # null pointers, bad shapes and unsupported sizes come back before any CUDA call
+    fake = ctypes.c_void_p(4096)
+    assert L.scout_merge(None, None, None, None, 4, 128, None, None, None) == 1
+    assert L.scout_merge(fake, fake, fake, fake, 4, 64, fake, fake, None) == 2  # D != 128
+    assert L.scout_predict_q(fake, fake, fake, 8, 100, 64, None) == 2  # N % 128
+    assert L.scout_predict_q(fake, fake, fake, 0, 128, 64, None) == 1
+    assert L.scout_build_digest(0, fake, 10, fake, fake, 1, 1, 128, 48, 4, None, 0, fake, None, None) == 2  # P
+    assert L.scout_build_digest(7, fake, 10, fake, fake, 1, 1, 128, 32, 4, None, 0, fake, None, None) == 1  # kind
+    args = [0, fake, fake, fake, fake, None, None, 1, 18, 2, 128, 32, 64, 8, None] + [fake] * 8 + [fake, 1 << 20, None]
+    assert L.scout_score_topk(*args) == 2  # G = 9 > 8
+    args[7:10] = [1, 8, 2]
+    args[-2] = 16
+    assert L.scout_score_topk(*args) == 3  # workspace too small
+    args[5] = fake  # prev list without prev count
+    assert L.scout_score_topk(*args) == 1
+    assert L.scout_sparse_attn(fake, fake, fake, 100, fake, fake, fake, fake, 1, 8, 2, 128, 32, 8, 4, 0.0, fake,
+                               fake, fake, 1 << 24, None, None) == 1  # scale <= 0
+    assert L.scout_sparse_attn(fake, ctypes.c_void_p(4097), fake, 100, fake, fake, fake, fake, 1, 8, 2, 128, 32, 8,
+                               4, 0.1, fake, fake, fake, 1 << 24, None, None) == 2  # misaligned pool
+    ops = (bs.RecallOp * 1)(bs.RecallOp(0, 5, 3, -1))
+    assert L.scout_recall_async(ops, 1, fake, fake, fake, fake, 2, 1, 1, 128, 32, 8, None, None, None) == 1  # slot 3 >= 2
+
+
+def test_generator_library_exports():
+    import block_sparse_kv_pred_gb300.workload.device as WD
+
+    if not os.path.exists(os.path.join(os.path.dirname(bs.lib_path()), "libscoutgen.so")):
+        B.build()
+    L = WD.gen_lib()
+    assert hasattr(L, "scoutgen_fill_normal_bf16") and hasattr(L, "scoutgen_fill_pool_bf16")
