@@ -225,3 +225,21 @@ def commit_residency(d_ops, page_table, resident_bits, n_slots, B, Hkv, wait_eve
                                         _dev(resident_bits, torch.int32, "resident_bits"), n_slots, B, Hkv,
                                         page_table.shape[-1], None if wait_event is None else wait_event.cuda_event,
                                         _stream(stream)), "scout_commit_residency")
+
+
+class Prepared:
+    """One C-ABI call with its arguments converted once; calling it re-issues the call.
+
+    Used by timing loops so that per-step host work is a single foreign call.
+    Buffers named by the arguments must outlive the object.
+    """
+
+    def __init__(self, name: str, *args):
+        self.name = name
+        self.fn = getattr(lib(), name)
+        self.args = tuple(args)
+
+    def __call__(self):
+        rc = self.fn(*self.args)
+        if rc != 0:
+            raise ScoutError(f"{self.name}: {lib().scout_status_string(rc).decode()}")
