@@ -48,6 +48,9 @@ _SIGS = {
     "scout_score_topk_workspace_bytes": ([_i, _i, _i], _sz),
     "scout_score_topk": ([_i, _p, _p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _i, _p, _p, _p, _p, _p, _p, _p, _p,
                           _p, _p, _sz, _p], _i),
+    "scout_score_topk_noalloc_max_bytes": ([], _sz),
+    "scout_score_topk_noalloc": ([_i, _p, _p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _i, _p, _p, _p, _p, _p, _p, _p,
+                                  _p, _p, _p], _i),
     "scout_sparse_attn_workspace_bytes": ([_i, _i, _i, _i, _i], _sz),
     "scout_sparse_attn": ([_p, _p, _p, _i64, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _i, _f, _p, _p, _p, _sz, _p,
                            _p], _i),

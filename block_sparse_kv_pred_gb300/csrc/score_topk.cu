@@ -418,3 +418,67 @@ extern "C" int scout_score_topk(int kind, const void* q, const void* digest, con
     score_topk_kernel<SCOUT_DIGEST_MEAN><<<grid, kThreads, smem, stream>>>(a);
   return launch_status();
 }
+
+// ---------------------------------------------------------------------------
+// Allocation-free variant of scout_score_topk.
+//
+// Some callers cannot allocate device memory at the point where they select
+// blocks: engines that reserve all GPU memory in one pool at start-up and forbid
+// later cudaMalloc calls (a cudaMalloc can stall other streams and fragment the
+// pool), or hosts that load this library as a plugin and hand it no allocator.
+// For them the scratch lives in one file-scope device array of fixed size that
+// every GPU loading the library keeps until the process exits.
+// ---------------------------------------------------------------------------
+#include <mutex>
+
+namespace scout {
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = 4u << 20;  // 4 MiB: counters + fp32 scores
+constexpr int kNoAllocMaxDevices = 64;
+
+static __device__ __align__(256) uint8_t g_topk_scratch[kNoAllocScratchBytes];
+
+std::mutex g_scratch_mu;
+void* g_scratch_addr[kNoAllocMaxDevices] = {};
+
+// Device address of g_topk_scratch on the current device, looked up once per
+// device (the host-side symbol is only a stand-in and must never reach a kernel).
+int scratch_address(void** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return SCOUT_ERR_CUDA;
+  if (dev < 0 || dev >= kNoAllocMaxDevices) return SCOUT_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lock(g_scratch_mu);
+  if (g_scratch_addr[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_topk_scratch) != cudaSuccess || p == nullptr) return SCOUT_ERR_CUDA;
+    g_scratch_addr[dev] = p;
+  }
+  *out = g_scratch_addr[dev];
+  return SCOUT_OK;
+}
+
+}  // namespace
+}  // namespace scout
+
+extern "C" size_t scout_score_topk_noalloc_max_bytes(void) { return scout::kNoAllocScratchBytes; }
+
+extern "C" int scout_score_topk_noalloc(int kind, const void* q, const void* digest, const int32_t* seq_len,
+                                        const uint32_t* resident_bits, const int32_t* prev_cpu_list,
+                                        const int32_t* prev_cpu_count, int B, int Hq, int Hkv, int D, int P,
+                                        int nblk_cap, int k, float* scores, int32_t* topk_idx, int32_t* topk_count,
+                                        int32_t* res_list, int32_t* res_count, int32_t* cpu_list, int32_t* cpu_count,
+                                        int32_t* delta_list, int32_t* delta_count, cudaStream_t stream) {
+  using namespace scout;
+  const size_t need = scout_score_topk_workspace_bytes(B, Hkv, nblk_cap);
+  if (need == 0) return SCOUT_ERR_INVALID_ARG;
+  if (need > kNoAllocScratchBytes) return SCOUT_ERR_WORKSPACE;  // beyond the fixed scratch
+  void* scratch = nullptr;
+  const int rc = scratch_address(&scratch);
+  if (rc != SCOUT_OK) return rc;
+  // the array keeps whatever the previous call left: zero the per-unit counters
+  if (cudaMemsetAsync(scratch, 0, counters_bytes((int64_t)B * Hkv), stream) != cudaSuccess) return SCOUT_ERR_CUDA;
+  return scout_score_topk(kind, q, digest, seq_len, resident_bits, prev_cpu_list, prev_cpu_count, B, Hq, Hkv, D, P,
+                          nblk_cap, k, scores, topk_idx, topk_count, res_list, res_count, cpu_list, cpu_count,
+                          delta_list, delta_count, scratch, kNoAllocScratchBytes, stream);
+}

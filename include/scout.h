@@ -138,6 +138,32 @@ int scout_score_topk(int kind, const void* q, const void* digest, const int32_t*
                      int32_t* delta_count, void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
 /* ------------------------------------------------------------------------ *
+ * scout_score_topk without a caller workspace (no counterpart in the paper).
+ *
+ * For callers that cannot allocate device memory when they select blocks: an
+ * engine that reserves all GPU memory in one pool at start-up and forbids later
+ * cudaMalloc calls, or a host that loads this library as a plugin without giving
+ * it an allocator.  Same arguments and results as scout_score_topk, minus the
+ * workspace.  The scratch is one fixed device array of
+ * scout_score_topk_noalloc_max_bytes() bytes (4 MiB) inside the library, held by
+ * every GPU that loads it until the process exits; a call whose
+ * scout_score_topk_workspace_bytes(B, Hkv, nblk_cap) exceeds that returns
+ * SCOUT_ERR_WORKSPACE and launches nothing.  It never calls cudaMalloc or
+ * cudaFree.  The first call on a device looks up the array's device address
+ * (once per device, with that device current); make that first call before any
+ * stream capture.  Each call zeroes the array's counters on `stream` before its
+ * kernel.  All calls share the one array, so calls whose kernels overlap on the
+ * GPU (different streams, or different host threads) race: serialise them.
+ * ------------------------------------------------------------------------ */
+size_t scout_score_topk_noalloc_max_bytes(void);
+int scout_score_topk_noalloc(int kind, const void* q, const void* digest, const int32_t* seq_len,
+                             const uint32_t* resident_bits, const int32_t* prev_cpu_list,
+                             const int32_t* prev_cpu_count, int B, int Hq, int Hkv, int D, int P, int nblk_cap,
+                             int k, float* scores, int32_t* topk_idx, int32_t* topk_count, int32_t* res_list,
+                             int32_t* res_count, int32_t* cpu_list, int32_t* cpu_count, int32_t* delta_list,
+                             int32_t* delta_count, cudaStream_t stream);
+
+/* ------------------------------------------------------------------------ *
  * GPU partial attention over the resident selected blocks.
  * ScoutAttention (arXiv HTML), section 3.2 and Algorithm 1 (A_gpu): the GPU
  * attends the top-k blocks that reside in its memory.
