@@ -151,7 +151,7 @@ def setup_step(shape, device):
     calls = [
         bs.Prepared("scout_build_digest", bs.MINMAX, p("K_pool"), wl.n_slots, p("page_table"), p("seq_len"), s.B,
                     s.Hkv, D, s.P, nb, p("tail"), U, p("digest"), p("status"), st),
-        bs.Prepared("scout_predict_q", p("X"), p("W"), p("Qp"), s.B, s.Hq * D, s.hidden, st),
+        bs.Prepared("scout_predict_q", p("X"), p("W"), p("Qp"), s.B, s.Hq * D, s.hidden, p("status"), st),
         # the previous step's CPU list is this step's prev list (in place), so delta = newly offloaded blocks
         bs.Prepared("scout_score_topk", bs.MINMAX, p("Qp"), p("digest"), p("seq_len"), p("resident_bits"), p("cpu"),
                     p("cpu_count"), s.B, s.Hq, s.Hkv, D, s.P, nb, s.k, None, p("topk"), p("topk_count"), p("res"),

@@ -43,7 +43,7 @@ class RecallOp(ctypes.Structure):
 _SIGS = {
     "scout_status_string": ([_i], ctypes.c_char_p),
     "scout_version": ([], _i),
-    "scout_predict_q": ([_p, _p, _p, _i, _i, _i, _p], _i),
+    "scout_predict_q": ([_p, _p, _p, _i, _i, _i, _p, _p], _i),
     "scout_build_digest": ([_i, _p, _i64, _p, _p, _i, _i, _i, _i, _i, _p, _i, _p, _p, _p], _i),
     "scout_score_topk_workspace_bytes": ([_i, _i, _i], _sz),
     "scout_score_topk": ([_i, _p, _p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _i, _p, _p, _p, _p, _p, _p, _p, _p,
@@ -105,14 +105,16 @@ def _opt(t, dtype, name):
 
 
 # ---------------------------------------------------------------------------
-def predict_q(X: torch.Tensor, W: torch.Tensor, Q: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+def predict_q(X: torch.Tensor, W: torch.Tensor, Q: torch.Tensor | None = None, status=None,
+              stream=None) -> torch.Tensor:
     """Q_pred = X W^T (bf16 in, fp32 accumulate, bf16 out)."""
     M, K = X.shape
     N = W.shape[0]
     if Q is None:
         Q = torch.empty((M, N), dtype=torch.bfloat16, device=X.device)
     _check(lib().scout_predict_q(_dev(X, torch.bfloat16, "X"), _dev(W, torch.bfloat16, "W"),
-                                 _dev(Q, torch.bfloat16, "Q"), M, N, K, _stream(stream)), "scout_predict_q")
+                                 _dev(Q, torch.bfloat16, "Q"), M, N, K, _opt(status, torch.int32, "status"),
+                                 _stream(stream)), "scout_predict_q")
     return Q
 
 

@@ -1,56 +1,264 @@
-// scout_predict_q: layer-ahead query prediction Q_pred = X W_Q^T.
-// ScoutAttention (arXiv HTML), section 3.3 and Algorithm 1 (query prediction):
-// the next layer's query projection applied to the current layer's input.
+// scout_predict_q: layer-ahead query prediction Q_pred = X W_Q^T on the 5th-generation
+// tensor cores.  ScoutAttention (arXiv HTML), section 3.3 and Algorithm 1 (query
+// prediction): the next layer's query projection applied to the current layer's input.
 //
-// Shared-memory tiled GEMM on the CUDA cores: a CTA computes a 32 x 32 tile of
-// Q (rows of X x rows of W), fp32 accumulation, bf16 output.
+// Decode batches are small (M = 1..256 rows of X) while W_Q is large, so the GEMM is
+// computed swapped: D[n][m] = sum_k W[n][k] X[m][k].  A CTA owns 128 rows of W (the
+// MMA's M = 128 TMEM lanes); the batch, padded to a multiple of 16, is the MMA's N.
+// W and X tiles (64 k-columns, 128-byte swizzle) stream in by TMA through a ring of
+// shared-memory stages guarded by mbarriers; one thread issues tcgen05.mma into a
+// TMEM accumulator and frees each stage with tcgen05.commit.  The K dimension is
+// split over the CTAs of a thread-block cluster so that about one CTA runs per SM;
+// the partial accumulators are summed through distributed shared memory by the
+// cluster's first CTA, which writes bf16 Q.  No global scratch is used.
 #include "common.cuh"
 
 namespace scout {
 namespace {
 
-constexpr int kTile = 32, kKt = 64;
+constexpr int kBM = 128;      // W rows per CTA (MMA M)
+constexpr int kBK = 64;       // k columns per stage (one 128-byte swizzle atom of bf16)
+constexpr int kStages = 6;
+constexpr int kThreadsQ = 128;
+constexpr int kMaxN = 256;    // padded batch (MMA N) limit
+constexpr int kWTileBytes = kBM * kBK * 2;  // 16 KiB
 
-__global__ void __launch_bounds__(256) predict_q_simple(const __nv_bfloat16* __restrict__ X,
-                                                        const __nv_bfloat16* __restrict__ W,
-                                                        __nv_bfloat16* __restrict__ Q, int M, int N, int K) {
-  __shared__ float xs[kTile][kKt + 1], ws[kTile][kKt + 1];
-  const int n0 = blockIdx.x * kTile, m0 = blockIdx.y * kTile;
-  const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;  // ty: 0..7
-  float acc[4] = {0.f, 0.f, 0.f, 0.f};
-  for (int k0 = 0; k0 < K; k0 += kKt) {
-    for (int e = threadIdx.x; e < kTile * kKt; e += 256) {
-      const int r = e / kKt, c = e - r * kKt;
-      xs[r][c] = (m0 + r < M && k0 + c < K) ? __bfloat162float(X[(int64_t)(m0 + r) * K + k0 + c]) : 0.f;
-      ws[r][c] = (n0 + r < N && k0 + c < K) ? __bfloat162float(W[(int64_t)(n0 + r) * K + k0 + c]) : 0.f;
-    }
-    __syncthreads();
-#pragma unroll 8
-    for (int c = 0; c < kKt; ++c) {
-      const float w = ws[tx][c];
+// --- tcgen05 / cluster PTX ----------------------------------------------------
+__device__ __forceinline__ void tmem_alloc(uint32_t* slot, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(slot)),
+               "r"(ncols)
+               : "memory");
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// D(tmem) (+)= A(smem desc) * B(smem desc), bf16 inputs, fp32 accumulators.
+__device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                          uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// Arrive on an mbarrier once every tcgen05 operation issued so far by this thread completes.
+__device__ __forceinline__ void umma_commit(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
+               : "memory");
+}
+// 32 lanes x 32 bits, 8 consecutive columns per thread.
+__device__ __forceinline__ void tmem_ld8(uint32_t taddr, float (&v)[8]) {
+  uint32_t r[8];
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+               : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 #pragma unroll
-      for (int i = 0; i < 4; ++i) acc[i] = fmaf(xs[ty + 8 * i][c], w, acc[i]);
+  for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\nbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+__device__ __forceinline__ uint32_t map_peer(uint32_t addr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ float ld_peer(uint32_t addr) {
+  float v;
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+  return v;
+}
+
+// Shared-memory matrix descriptor: K-major operand, 128-byte swizzle, rows of 128 bytes,
+// 8-row core-matrix groups 1024 bytes apart (the layout a 64-column TMA box writes).
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
+  uint64_t d = (uint64_t)((saddr >> 4) & 0x3FFFu);
+  d |= (uint64_t)1 << 16;             // leading byte offset (unused for swizzled K-major)
+  d |= (uint64_t)(1024 >> 4) << 32;   // stride byte offset between 8-row groups
+  d |= (uint64_t)1 << 46;             // descriptor version for this architecture family
+  d |= (uint64_t)2 << 61;             // 128-byte swizzle
+  return d;
+}
+// Instruction descriptor: fp32 accumulate, bf16 A and B, both K-major, M = 128, N = n.
+__host__ __device__ constexpr uint32_t idesc_bf16(int n) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(kBM >> 4) << 24);
+}
+
+struct GemmArgs {
+  __nv_bfloat16* Q;
+  int M, N, n_pad, tmem_cols, kblocks, stages, x_tile_bytes;
+  int32_t* status;
+};
+
+__global__ void __launch_bounds__(kThreadsQ, 1) predict_q_kernel(const __grid_constant__ CUtensorMap tmW,
+                                                                 const __grid_constant__ CUtensorMap tmX,
+                                                                 const GemmArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ uint64_t full_bar[kStages], empty_bar[kStages], done_bar;
+  __shared__ uint32_t tmem_slot;
+  const uint32_t raw = smem_u32(smem_raw);
+  uint8_t* base = smem_raw + (((raw + 1023u) & ~1023u) - raw);
+  const int stage_bytes = kWTileBytes + a.x_tile_bytes;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int tile = blockIdx.x;
+  const uint32_t S = gridDim.y, rank = cluster_rank();
+  const int kb0 = (int)(rank * a.kblocks / S), kb1 = (int)((rank + 1) * a.kblocks / S);
+  const int nkb = kb1 - kb0;
+
+  if (tid == 0) {
+    for (int i = 0; i < a.stages; ++i) {
+      mbar_init(&full_bar[i], 1);
+      mbar_init(&empty_bar[i], 1);
     }
-    __syncthreads();
+    mbar_init(&done_bar, 1);
+    fence_mbar_init();
   }
+  if (warp == 2) tmem_alloc(&tmem_slot, (uint32_t)a.tmem_cols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_slot;
+
+  if (warp == 0 && lane == 0) {
+    // TMA producer
+    prefetch_tmap(&tmW);
+    prefetch_tmap(&tmX);
+    int issued = 0;
+    for (int i = 0; i < nkb; ++i) {
+      const int st = i % a.stages;
+      if (!mbar_wait(&empty_bar[st], ((i / a.stages) & 1) ^ 1)) {
+        report(a.status, SCOUT_DEV_TIMEOUT);
+        break;
+      }
+      uint8_t* sW = base + st * stage_bytes;
+      mbar_arrive_tx(&full_bar[st], (uint32_t)stage_bytes);
+      const int kx = (kb0 + i) * kBK;
+      tma_load_2d(sW, &tmW, kx, tile * kBM, &full_bar[st]);
+      tma_load_2d(sW + kWTileBytes, &tmX, kx, 0, &full_bar[st]);
+      issued = i + 1;
+    }
+    // every issued copy lands before the CTA can retire
+    for (int r = 0; r < a.stages && r < issued; ++r) {
+      const int last = issued - 1 - r;
+      if (!mbar_wait(&full_bar[last % a.stages], (last / a.stages) & 1)) report(a.status, SCOUT_DEV_TIMEOUT);
+    }
+  } else if (warp == 1 && lane == 0) {
+    // MMA issuer
+    const uint32_t idesc = idesc_bf16(a.n_pad);
+    for (int i = 0; i < nkb; ++i) {
+      const int st = i % a.stages;
+      if (!mbar_wait(&full_bar[st], (i / a.stages) & 1)) {
+        report(a.status, SCOUT_DEV_TIMEOUT);
+        break;
+      }
+      tc_fence_after();
+      const uint32_t sW = smem_u32(base + st * stage_bytes), sX = sW + kWTileBytes;
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const int m = m0 + ty + 8 * i, n = n0 + tx;
-    if (m < M && n < N) Q[(int64_t)m * N + n] = __float2bfloat16_rn(acc[i]);
+      for (int kk = 0; kk < kBK / 16; ++kk)
+        umma_bf16(tmem, sw128_desc(sW + kk * 32), sw128_desc(sX + kk * 32), idesc, (i > 0 || kk > 0) ? 1u : 0u);
+      umma_commit(&empty_bar[st]);
+    }
+    umma_commit(&done_bar);
   }
+  __syncwarp();
+
+  // ---- epilogue: thread (warp w, lane l) owns W row tile*128 + 32w + l (TMEM lane) ----
+  if (!mbar_wait(&done_bar, 0)) report(a.status, SCOUT_DEV_TIMEOUT);
+  tc_fence_after();
+  const int r_local = warp * 32 + lane;
+  const int row = tile * kBM + r_local;
+  const uint32_t trow = tmem + ((uint32_t)(warp * 32) << 16);
+  float* part = reinterpret_cast<float*>(base);  // [n_pad][128]: the stage ring is idle now
+  float v[8];
+  if (S > 1 && rank != 0) {
+    for (int c = 0; c < a.n_pad; c += 8) {
+      tmem_ld8(trow + (uint32_t)c, v);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) part[(c + e) * kBM + r_local] = v[e];
+    }
+  }
+  if (S > 1) cluster_sync();
+  if (rank == 0) {
+    for (int c = 0; c < a.n_pad; c += 8) {
+      tmem_ld8(trow + (uint32_t)c, v);
+      for (uint32_t r = 1; r < S; ++r) {
+        const uint32_t pa = map_peer(smem_u32(part + c * kBM + r_local), r);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) v[e] += ld_peer(pa + (uint32_t)(e * kBM * 4));
+      }
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const int m = c + e;
+        if (m < a.M && row < a.N) a.Q[(int64_t)m * a.N + row] = __float2bfloat16_rn(v[e]);
+      }
+    }
+  }
+  if (S > 1) cluster_sync();  // peers keep their shared memory until the first CTA has read it
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 2) tmem_dealloc(tmem, (uint32_t)a.tmem_cols);
+}
+
+bool make_map(CUtensorMap* map, const void* ptr, int rows, int cols, int box_rows) {
+  const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
+  const cuuint32_t box[2] = {(cuuint32_t)kBK, (cuuint32_t)box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  return encode_tiled(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, estr,
+                      CU_TENSOR_MAP_SWIZZLE_128B) == CUDA_SUCCESS;
 }
 
 }  // namespace
 }  // namespace scout
 
-extern "C" int scout_predict_q(const void* X, const void* W, void* Q, int M, int N, int K, cudaStream_t stream) {
+extern "C" int scout_predict_q(const void* X, const void* W, void* Q, int M, int N, int K, int32_t* dev_status,
+                               cudaStream_t stream) {
   using namespace scout;
   if (X == nullptr || W == nullptr || Q == nullptr || M <= 0 || N <= 0 || K <= 0) return SCOUT_ERR_INVALID_ARG;
-  if (M > 256 || N % 128 != 0 || K % 64 != 0 || !aligned16(X) || !aligned16(W) || !aligned16(Q))
+  if (M > kMaxN || N % kBM != 0 || K % kBK != 0 || !aligned16(X) || !aligned16(W) || !aligned16(Q))
     return SCOUT_ERR_UNSUPPORTED;
-  const dim3 grid((unsigned)(N / kTile), (unsigned)((M + kTile - 1) / kTile));
-  predict_q_simple<<<grid, 256, 0, stream>>>(static_cast<const __nv_bfloat16*>(X),
-                                             static_cast<const __nv_bfloat16*>(W), static_cast<__nv_bfloat16*>(Q), M,
-                                             N, K);
+  GemmArgs a;
+  a.Q = static_cast<__nv_bfloat16*>(Q);
+  a.M = M;
+  a.N = N;
+  a.n_pad = (M + 15) / 16 * 16;
+  a.tmem_cols = 32;
+  while (a.tmem_cols < a.n_pad) a.tmem_cols <<= 1;
+  a.kblocks = K / kBK;
+  a.x_tile_bytes = (a.n_pad * 128 + 1023) / 1024 * 1024;
+  const int stage_bytes = kWTileBytes + a.x_tile_bytes;
+  a.stages = min(kStages, (200 * 1024) / stage_bytes);
+  a.status = dev_status;
+  const int tiles = N / kBM;
+  const int S = max(1, min(min(8, a.kblocks), sm_count() / tiles));
+  const size_t smem = 1024 + (size_t)max(a.stages * stage_bytes, a.n_pad * kBM * 4);
+  CUtensorMap tmW, tmX;
+  if (!make_map(&tmW, W, N, K, kBM) || !make_map(&tmX, X, M, K, a.n_pad)) return SCOUT_ERR_UNSUPPORTED;
+  if (cudaFuncSetAttribute(predict_q_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+    return SCOUT_ERR_CUDA;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)tiles, (unsigned)S, 1);
+  cfg.blockDim = dim3(kThreadsQ, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 1;
+  attr[0].val.clusterDim.y = (unsigned)S;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, predict_q_kernel, tmW, tmX, a) != cudaSuccess) return SCOUT_ERR_CUDA;
   return launch_status();
 }

@@ -71,9 +71,13 @@ int scout_version(void);
  * (linear-layer layout, N = Hq * D), Q bf16 [M][N] row-major; Q = X W^T with
  * fp32 accumulation, rounded to nearest bf16.  Requires 1 <= M <= 256,
  * N % 128 == 0, K % 64 == 0, and 16-byte-aligned X, W, Q.
- * Runs on the tensor cores (tcgen05, TMA-fed).  No workspace.
+ * Runs on the tensor cores (tcgen05, TMA-fed), with K split over the CTAs of a
+ * thread-block cluster and reduced through distributed shared memory.  No
+ * workspace.  dev_status (may be NULL) receives SCOUT_DEV_TIMEOUT if a bounded
+ * pipeline wait expires.
  * ------------------------------------------------------------------------ */
-int scout_predict_q(const void* X, const void* W, void* Q, int M, int N, int K, cudaStream_t stream);
+int scout_predict_q(const void* X, const void* W, void* Q, int M, int N, int K, int32_t* dev_status,
+                    cudaStream_t stream);
 
 /* ------------------------------------------------------------------------ *
  * Block digests.

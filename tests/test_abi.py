@@ -50,8 +50,9 @@ def test_host_validation_rejects_without_launch(L):
     fake = ctypes.c_void_p(4096)
     assert L.scout_merge(None, None, None, None, 4, 128, None, None, None) == 1
     assert L.scout_merge(fake, fake, fake, fake, 4, 64, fake, fake, None) == 2  # D != 128
-    assert L.scout_predict_q(fake, fake, fake, 8, 100, 64, None) == 2  # N % 128
-    assert L.scout_predict_q(fake, fake, fake, 0, 128, 64, None) == 1
+    assert L.scout_predict_q(fake, fake, fake, 8, 100, 64, None, None) == 2  # N % 128
+    assert L.scout_predict_q(fake, fake, fake, 0, 128, 64, None, None) == 1
+    assert L.scout_predict_q(fake, fake, fake, 257, 128, 64, None, None) == 2  # M > 256
     assert L.scout_build_digest(0, fake, 10, fake, fake, 1, 1, 128, 48, 4, None, 0, fake, None, None) == 2  # P
     assert L.scout_build_digest(7, fake, 10, fake, fake, 1, 1, 128, 32, 4, None, 0, fake, None, None) == 1  # kind
     args = [0, fake, fake, fake, fake, None, None, 1, 18, 2, 128, 32, 64, 8, None] + [fake] * 8 + [fake, 1 << 20, None]

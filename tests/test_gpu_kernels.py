@@ -347,7 +347,8 @@ def test_merge_parity_including_empty_partials():
         check_attention(Og[r], Lg[r], o, l, what=r)
 
 
-@pytest.mark.parametrize("M,N,K", [(1, 1024, 1024), (8, 256, 512), (40, 640, 5120), (130, 384, 192)])
+@pytest.mark.parametrize("M,N,K", [(1, 1024, 1024), (8, 256, 512), (40, 640, 5120), (130, 384, 192), (256, 256, 128),
+                                   (40, 5120, 5120), (8, 4096, 4096)])
 def test_predict_q_parity(M, N, K):
     X = W.normal_bf16(1, W.STREAM_X, (M, K))
     Wq = W.normal_bf16(1, W.STREAM_W, (N, K), sigma=0.02)
