@@ -29,7 +29,7 @@ import time
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
-L2_FLUSH_BYTES = 256 << 20
+L2_BYTES = 129 << 20  # GB300 L2
 FALLBACK_HBM_GBS = 6800.0
 
 
@@ -115,74 +115,7 @@ class ClockSampler:
 # ---------------------------------------------------------------------------
 # libscout arm
 # ---------------------------------------------------------------------------
-KERNELS = ("build_digest", "predict_q", "score_topk", "sparse_attn", "merge")
-
-
-def setup_step(shape, device):
-    """Device inputs, prefill digests and the five prepared C-ABI calls of one step."""
-    import torch
-
-    import block_sparse_kv_pred_gb300 as bs
-    from block_sparse_kv_pred_gb300 import workload as W
-    from block_sparse_kv_pred_gb300.workload import device as WD
-
-    s = shape
-    wl = W.Workload(s)
-    d = WD.materialize(wl, device=device)
-    U, nb, D = s.units, s.nblk, s.D
-    t = {k: v for k, v in d.items()}
-    t["digest"] = torch.empty((s.B, s.Hkv, nb, 2, D), dtype=torch.bfloat16, device=device)
-    bs.build_digest("minmax", d["K_pool"], d["page_table"], d["seq_len"], s.B, s.Hkv, s.P, t["digest"])
-    tail = [[u, int(wl.nvalid[u // s.Hkv]) - 1] for u in range(U)]
-    t["tail"] = torch.tensor(tail, dtype=torch.int32, device=device)
-    t["Qp"] = torch.empty((s.B, s.Hq * D), dtype=torch.bfloat16, device=device)
-    t["ws_t"] = bs.score_topk_workspace(s.B, s.Hkv, nb, device=device)
-    for name in ("topk", "res", "cpu", "delta"):
-        t[name] = torch.full((s.B, s.Hkv, s.k), -1, dtype=torch.int32, device=device)
-        t[name + "_count"] = torch.zeros((s.B, s.Hkv), dtype=torch.int32, device=device)
-    t["ws_a"] = bs.sparse_attn_workspace(s.B, s.Hq, s.Hkv, s.P, device=device)
-    t["O_gpu"] = torch.empty((s.B, s.Hq, D), dtype=torch.float32, device=device)
-    t["lse_gpu"] = torch.empty((s.B, s.Hq), dtype=torch.float32, device=device)
-    t["O"] = torch.empty((s.B, s.Hq, D), dtype=torch.bfloat16, device=device)
-    t["lse"] = torch.empty((s.B, s.Hq), dtype=torch.float32, device=device)
-    t["status"] = torch.zeros(1, dtype=torch.int32, device=device)
-    st = torch.cuda.current_stream(device).cuda_stream
-    p = lambda name: t[name].data_ptr()  # noqa: E731
-    calls = [
-        bs.Prepared("scout_build_digest", bs.MINMAX, p("K_pool"), wl.n_slots, p("page_table"), p("seq_len"), s.B,
-                    s.Hkv, D, s.P, nb, p("tail"), U, p("digest"), p("status"), st),
-        bs.Prepared("scout_predict_q", p("X"), p("W"), p("Qp"), s.B, s.Hq * D, s.hidden, p("status"), st),
-        # the previous step's CPU list is this step's prev list (in place), so delta = newly offloaded blocks
-        bs.Prepared("scout_score_topk", bs.MINMAX, p("Qp"), p("digest"), p("seq_len"), p("resident_bits"), p("cpu"),
-                    p("cpu_count"), s.B, s.Hq, s.Hkv, D, s.P, nb, s.k, None, p("topk"), p("topk_count"), p("res"),
-                    p("res_count"), p("cpu"), p("cpu_count"), p("delta"), p("delta_count"), p("ws_t"),
-                    t["ws_t"].numel(), st),
-        bs.Prepared("scout_sparse_attn", p("q"), p("K_pool"), p("V_pool"), wl.n_slots, p("page_table"),
-                    p("seq_len"), p("res"), p("res_count"), s.B, s.Hq, s.Hkv, D, s.P, nb, s.k, s.scale, p("O_gpu"),
-                    p("lse_gpu"), p("ws_a"), t["ws_a"].numel(), p("status"), st),
-        bs.Prepared("scout_merge", p("O_gpu"), p("lse_gpu"), p("O_cpu"), p("lse_cpu"), s.B * s.Hq, D, p("O"),
-                    p("lse"), st),
-    ]
-    return wl, t, calls
-
-
-def algorithmic_bytes(s, wl, t):
-    """Bytes each kernel must move per launch (inputs read once, outputs written once)."""
-    U, D, P, k = s.units, s.D, s.P, s.k
-    nvalid = int(sum(int(wl.nvalid[u // s.Hkv]) for u in range(U)))
-    res_total = int(t["res_count"].sum().item())
-    cpu_total = int(t["cpu_count"].sum().item())
-    q_bytes = s.B * s.Hq * D * 2
-    part = s.B * s.Hq * (D * 4 + 4)
-    return {
-        "build_digest": U * (P * D * 2 + 2 * D * 2 + 8) + s.B * 4,
-        "predict_q": s.Hq * D * s.hidden * 2 + s.B * s.hidden * 2 + s.B * s.Hq * D * 2,
-        "score_topk": nvalid * 2 * D * 2 + q_bytes + U * s.words * 4 + s.B * 4 + cpu_total * 4 + U * 4
-        + 4 * (U * k * 4 + U * 4),
-        "sparse_attn": res_total * (2 * P * D * 2 + 8) + q_bytes + part + U * 4 + s.B * 4,
-        "merge": 2 * part + s.B * s.Hq * (D * 2 + 4),
-        "_res_blocks": res_total,
-    }
+from block_sparse_kv_pred_gb300.step import KERNELS, algorithmic_bytes, setup_step  # noqa: E402
 
 
 def run_scout(args, rank, world, local):
@@ -196,14 +129,12 @@ def run_scout(args, rank, world, local):
     shape = W.CONFIGS[args.config]()
     wl, t, calls = setup_step(shape, device)
     s = shape
-    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
 
     def barrier():
         if world > 1:
             dist.barrier()
 
     for i in range(args.warmup):
-        flush.fill_(i & 255)
         for c in calls:
             c()
     torch.cuda.synchronize()
@@ -217,7 +148,6 @@ def run_scout(args, rank, world, local):
     torch.cuda.synchronize()
     wall0 = time.perf_counter()
     for i in range(args.steps):
-        flush.fill_(i & 255)  # evict L2 between steps; outside the step's events
         e = ev[i]
         e[0].record()
         for j, c in enumerate(calls):
@@ -237,12 +167,12 @@ def run_scout(args, rank, world, local):
         ms = float(m.item())
     value = world * s.B * s.Hq / (ms / 1e3)
 
-    e2e = run_e2e(args, t, calls, s, flush, world, device)
+    e2e = run_e2e(args, t, calls, s, world, device)
     return s, wl, t, dict(ms=ms, value=value, kern_ms=kern_ms, clocks=clocks, wall=wall, e2e=e2e,
                           launches=len(calls) * args.steps)
 
 
-def run_e2e(args, t, calls, s, flush, world, device):
+def run_e2e(args, t, calls, s, world, device):
     """Same metric with the step's inputs copied from pinned host memory and its results read back."""
     import torch
     import torch.distributed as dist
@@ -259,7 +189,6 @@ def run_e2e(args, t, calls, s, flush, world, device):
         dist.barrier()
     torch.cuda.synchronize()
     for i in range(steps):
-        flush.fill_(i & 255)
         ev[i][0].record()
         for n, h in h_in.items():
             t[n].copy_(h, non_blocking=True)
@@ -380,7 +309,8 @@ def config_of(s, world):
     return {"workload": s.name, "batch": s.B, "q_heads": s.Hq, "kv_heads": s.Hkv, "head_dim": s.D,
             "context": s.T, "page": s.P, "budget_tokens": s.k * s.P, "resident_frac": s.resident_frac,
             "digest": s.kind, "gemm_mnk": [s.B, s.Hq * s.D, s.hidden],
-            "l2": "flushed between steps by a 256 MiB write outside the timed events",
+            "l2": "not flushed: one step reads inputs larger than L2 (see step_input_bytes), in an order "
+                  "that evicts each input before its next use",
             "parallelism": f"independent replicas x{world} (one batch of sequences per GPU)"}
 
 
@@ -455,6 +385,7 @@ def main():
                            "note": "score_topk + sparse_attn + merge only"},
         "kv_tokens_per_s": nbytes["_res_blocks"] * s.P / (r["kern_ms"]["sparse_attn"] / 1e3),
         "step_GB_s": sum(nbytes[k] for k in KERNELS) / (r["ms"] / 1e3) / 1e9,
+        "step_input_bytes": sum(nbytes[k] for k in KERNELS),
         "wall_s_timed": r["wall"],
     }
     if world == 1 and not args.no_cpu_baseline:

@@ -22,16 +22,23 @@ namespace scout {
 namespace {
 
 constexpr int kConsumerWarps = 4;
-constexpr int kThreads = (kConsumerWarps + 1) * 32;
+constexpr int kProducerWarp = kConsumerWarps;      // streams pages with TMA
+constexpr int kEpilogueWarp = kConsumerWarps + 1;  // combines, writes, fixes up split units
+constexpr int kThreads = (kConsumerWarps + 2) * 32;
 constexpr int kMaxUnits = 4096;
+constexpr int kSlots = 1;  // combine slots between the consumer warps and the epilogue warp
 constexpr int kMaxGrid = 1024;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
+// A stage holds K and V of one sub-page of PS tokens (a 64-token block streams as two
+// 32-token sub-pages); every consumer warp owns kStages / 4 stages (3 in flight).
 template <int P>
 struct Cfg {
-  static constexpr int kStages = P == 16 ? 8 : 4;
-  static constexpr int kHalfBytes = P * 128;        // one 64-column half of a page
+  static constexpr int PS = P < 32 ? P : 32;         // tokens per stage
+  static constexpr int kSub = P / PS;                // stages per block
+  static constexpr int kStages = P == 16 ? 24 : 12;  // a multiple of the consumer warps
+  static constexpr int kHalfBytes = PS * 128;        // one 64-column half of a sub-page
   static constexpr int kStageBytes = 4 * kHalfBytes; // K (2 halves) + V (2 halves)
   static constexpr int kRingBytes = kStages * kStageBytes;
 };
@@ -78,96 +85,170 @@ __device__ __forceinline__ uint32_t page_addr(uint32_t base, int r, int C) {
   return base + (uint32_t)((C >> 3) * Cfg<P>::kHalfBytes + r * 128 + ((((C & 7) ^ (r & 7))) << 4));
 }
 
-__device__ __forceinline__ void consumer_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
-
 struct WarpState {
-  float m;       // running max of scaled scores (log2 units), row g
-  float l;       // running sum of exp2(s - m), this lane's columns only
-  float o[16][4];
+  float m[2];  // running max of scaled scores (log2 units) of heads 2t, 2t+1
+  float l[2];  // running sum of exp2(s - m) over this lane's tokens, heads 2t, 2t+1
+  float o[8][4];  // O^T accumulators: dims 16md + g (+8) x heads 2t, 2t+1
 };
 
-// One page: S = Q K^T, online softmax, O += P V.
+__device__ __forceinline__ uint32_t movmatrix_t(uint32_t x) {
+  uint32_t y;
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
+  return y;
+}
+
+// One page, computed transposed so that tokens and head dims fill the MMA's M:
+//   S^T = K Q^T (tokens x heads), online softmax per head (column),
+//   O^T += V^T P^T (dims x heads); P^T reaches the B-operand layout by movmatrix.
+// qb holds Q^T fragments: qb[s] = heads g, dims 16s + 2t (+8).
 template <int P>
-__device__ __forceinline__ void attend_page(uint32_t kbase, uint32_t vbase, int ntok, const uint32_t (&qa)[8][2],
+__device__ __forceinline__ void attend_page(uint32_t kbase, uint32_t vbase, int ntok, const uint32_t (&qb)[8][2],
                                             float scale_log2, WarpState& st, int lane) {
-  constexpr int NT = P / 8;
-  const int t = lane & 3;
-  float s[NT][4];
+  constexpr int MT = Cfg<P>::PS / 16;  // 16-token tiles per stage
+  const int g = lane >> 2;
+  float s[MT][4];
 #pragma unroll
-  for (int nt = 0; nt < NT; ++nt) {
-    s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
-    const int r = nt * 8 + (lane & 7);
+  for (int mt = 0; mt < MT; ++mt) {
+    float s2[4] = {0.f, 0.f, 0.f, 0.f};  // second accumulator: halves the dependent MMA chain
+    s[mt][0] = s[mt][1] = s[mt][2] = s[mt][3] = 0.f;
+    const int r = mt * 16 + ((lane >> 3) & 1) * 8 + (lane & 7);
 #pragma unroll
-    for (int kp = 0; kp < 4; ++kp) {
-      uint32_t b0, b1, b2, b3;
-      ldsm_x4(page_addr<P>(kbase, r, 4 * kp + (lane >> 3)), b0, b1, b2, b3);
-      mma_bf16(s[nt], qa[2 * kp][0], 0u, qa[2 * kp][1], 0u, b0, b1);
-      mma_bf16(s[nt], qa[2 * kp + 1][0], 0u, qa[2 * kp + 1][1], 0u, b2, b3);
+    for (int ks = 0; ks < 8; ks += 2) {
+      uint32_t a0, a1, a2, a3, c0, c1, c2, c3;
+      ldsm_x4(page_addr<P>(kbase, r, 2 * ks + (lane >> 4)), a0, a1, a2, a3);
+      ldsm_x4(page_addr<P>(kbase, r, 2 * ks + 2 + (lane >> 4)), c0, c1, c2, c3);
+      mma_bf16(s[mt], a0, a1, a2, a3, qb[ks][0], qb[ks][1]);
+      mma_bf16(s2, c0, c1, c2, c3, qb[ks + 1][0], qb[ks + 1][1]);
     }
+#pragma unroll
+    for (int e = 0; e < 4; ++e) s[mt][e] += s2[e];
   }
-  float bmax = -INFINITY;
+  // per-head (column) max over this page's tokens
+  float bm0 = -INFINITY, bm1 = -INFINITY;
 #pragma unroll
-  for (int nt = 0; nt < NT; ++nt) {
-#pragma unroll
-    for (int e = 0; e < 2; ++e) {
-      const int tok = nt * 8 + 2 * t + e;
-      s[nt][e] = tok < ntok ? s[nt][e] * scale_log2 : -INFINITY;
-      bmax = fmaxf(bmax, s[nt][e]);
-    }
-  }
-  bmax = fmaxf(bmax, __shfl_xor_sync(0xffffffffu, bmax, 1));
-  bmax = fmaxf(bmax, __shfl_xor_sync(0xffffffffu, bmax, 2));
-  const float m_new = fmaxf(st.m, bmax);
-  const float alpha = exp2f(st.m - m_new);  // 0 on the first page (m = -inf)
-  st.m = m_new;
-  float psum = 0.f;
-#pragma unroll
-  for (int nt = 0; nt < NT; ++nt) {
-    s[nt][0] = exp2f(s[nt][0] - m_new);
-    s[nt][1] = exp2f(s[nt][1] - m_new);
-    psum += s[nt][0] + s[nt][1];
-  }
-  st.l = st.l * alpha + psum;
-#pragma unroll
-  for (int d = 0; d < 16; ++d) {
-    st.o[d][0] *= alpha;
-    st.o[d][1] *= alpha;
+  for (int mt = 0; mt < MT; ++mt) {
+    const int t0 = mt * 16 + g, t1 = t0 + 8;
+    s[mt][0] = t0 < ntok ? s[mt][0] * scale_log2 : -INFINITY;
+    s[mt][1] = t0 < ntok ? s[mt][1] * scale_log2 : -INFINITY;
+    s[mt][2] = t1 < ntok ? s[mt][2] * scale_log2 : -INFINITY;
+    s[mt][3] = t1 < ntok ? s[mt][3] * scale_log2 : -INFINITY;
+    bm0 = fmaxf(bm0, fmaxf(s[mt][0], s[mt][2]));
+    bm1 = fmaxf(bm1, fmaxf(s[mt][1], s[mt][3]));
   }
 #pragma unroll
-  for (int kk = 0; kk < P / 16; ++kk) {
-    const uint32_t h0 = pack_bf16(s[2 * kk][0], s[2 * kk][1]);
-    const uint32_t h2 = pack_bf16(s[2 * kk + 1][0], s[2 * kk + 1][1]);
-    const uint32_t l0 = pack_bf16(s[2 * kk][0] - bf16_lo(h0), s[2 * kk][1] - bf16_hi(h0));
-    const uint32_t l2 = pack_bf16(s[2 * kk + 1][0] - bf16_lo(h2), s[2 * kk + 1][1] - bf16_hi(h2));
-    const int r = kk * 16 + ((lane >> 3) & 1) * 8 + (lane & 7);
+  for (int o = 4; o < 32; o <<= 1) {
+    bm0 = fmaxf(bm0, __shfl_xor_sync(0xffffffffu, bm0, o));
+    bm1 = fmaxf(bm1, __shfl_xor_sync(0xffffffffu, bm1, o));
+  }
+  const float n0 = fmaxf(st.m[0], bm0), n1 = fmaxf(st.m[1], bm1);
+  const float al0 = exp2f(st.m[0] - n0), al1 = exp2f(st.m[1] - n1);  // 0 on the first page
+  st.m[0] = n0;
+  st.m[1] = n1;
+  float ps0 = 0.f, ps1 = 0.f;
 #pragma unroll
-    for (int dp = 0; dp < 8; ++dp) {
-      uint32_t b0, b1, b2, b3;
-      ldsm_x4_t(page_addr<P>(vbase, r, 2 * dp + (lane >> 4)), b0, b1, b2, b3);
-      mma_bf16(st.o[2 * dp], h0, 0u, h2, 0u, b0, b1);
-      mma_bf16(st.o[2 * dp], l0, 0u, l2, 0u, b0, b1);
-      mma_bf16(st.o[2 * dp + 1], h0, 0u, h2, 0u, b2, b3);
-      mma_bf16(st.o[2 * dp + 1], l0, 0u, l2, 0u, b2, b3);
+  for (int mt = 0; mt < MT; ++mt) {
+    s[mt][0] = exp2f(s[mt][0] - n0);
+    s[mt][1] = exp2f(s[mt][1] - n1);
+    s[mt][2] = exp2f(s[mt][2] - n0);
+    s[mt][3] = exp2f(s[mt][3] - n1);
+    ps0 += s[mt][0] + s[mt][2];
+    ps1 += s[mt][1] + s[mt][3];
+  }
+  st.l[0] = st.l[0] * al0 + ps0;
+  st.l[1] = st.l[1] * al1 + ps1;
+#pragma unroll
+  for (int md = 0; md < 8; ++md) {
+    st.o[md][0] *= al0;
+    st.o[md][1] *= al1;
+    st.o[md][2] *= al0;
+    st.o[md][3] *= al1;
+  }
+#pragma unroll
+  for (int kk = 0; kk < MT; ++kk) {
+    // P^T as B operand (k = tokens, n = heads), split into bf16 high and low parts
+    const uint32_t ht = pack_bf16(s[kk][0], s[kk][1]), hb = pack_bf16(s[kk][2], s[kk][3]);
+    const uint32_t lt = pack_bf16(s[kk][0] - bf16_lo(ht), s[kk][1] - bf16_hi(ht));
+    const uint32_t lb = pack_bf16(s[kk][2] - bf16_lo(hb), s[kk][3] - bf16_hi(hb));
+    const uint32_t bh0 = movmatrix_t(ht), bh1 = movmatrix_t(hb);
+    const uint32_t bl0 = movmatrix_t(lt), bl1 = movmatrix_t(lb);
+    const int r = kk * 16 + (lane >> 4) * 8 + (lane & 7);
+#pragma unroll
+    for (int md = 0; md < 8; ++md) {
+      uint32_t a0, a1, a2, a3;
+      ldsm_x4_t(page_addr<P>(vbase, r, 2 * md + ((lane >> 3) & 1)), a0, a1, a2, a3);
+      mma_bf16(st.o[md], a0, a1, a2, a3, bh0, bh1);
+      mma_bf16(st.o[md], a0, a1, a2, a3, bl0, bl1);
     }
   }
 }
 
+// One segment's per-warp softmax states, handed from the consumer warps to the
+// epilogue warp through shared memory.
+struct CombineSlot {
+  float m[kConsumerWarps][kMaxG];
+  float l[kConsumerWarps][kMaxG];
+  float o[kConsumerWarps][kMaxG][kD];
+};
+
+// Walks the unit segments of one CTA's flattened block range [pos, end).
+struct SegIter {
+  const int* prefix;
+  int64_t pos, end;
+  int u;
+  __device__ __forceinline__ bool next(int& uu, int64_t& lo, int64_t& hi) {
+    while (pos < end) {
+      const int64_t h = min(end, (int64_t)prefix[u + 1]);
+      if (h > pos) {
+        uu = u;
+        lo = pos;
+        hi = h;
+        pos = h;
+        ++u;
+        return true;
+      }
+      ++u;
+    }
+    return false;
+  }
+};
+
+__device__ __forceinline__ int unit_of(const int* prefix, int units, int64_t x, int lo = 0) {
+  int hi = units - 1;  // last unit with prefix[u] <= x: the unit holding x
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (prefix[mid] <= x) lo = mid; else hi = mid - 1;
+  }
+  return lo;
+}
+
+// Q^T fragments (B operand) of unit u: head g, dims 16 ks + 2t (+8); zero for g >= G.
+__device__ __forceinline__ void load_q(const AttnArgs& a, int u, int lane, uint32_t (&qf)[8][2]) {
+  const int g = lane >> 2, t = lane & 3;
+  const int b = u / a.Hkv, kvh = u - b * a.Hkv;
+  const __nv_bfloat16* qrow = a.q + ((int64_t)b * a.Hq + (int64_t)kvh * a.G + g) * kD;
+#pragma unroll
+  for (int ks = 0; ks < 8; ++ks) {
+    qf[ks][0] = g < a.G ? *reinterpret_cast<const uint32_t*>(qrow + ks * 16 + 2 * t) : 0u;
+    qf[ks][1] = g < a.G ? *reinterpret_cast<const uint32_t*>(qrow + ks * 16 + 8 + 2 * t) : 0u;
+  }
+}
+
 template <int P>
-__global__ void __launch_bounds__(kThreads) sparse_attn_kernel(const __grid_constant__ CUtensorMap tmK,
-                                                               const __grid_constant__ CUtensorMap tmV,
-                                                               const AttnArgs a) {
+__global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const __grid_constant__ CUtensorMap tmK,
+                                                                  const __grid_constant__ CUtensorMap tmV,
+                                                                  const AttnArgs a) {
   using C = Cfg<P>;
   extern __shared__ uint8_t smem_raw[];
-  __shared__ uint64_t full_bar[C::kStages], empty_bar[C::kStages];
-  __shared__ float cm[kConsumerWarps][kMaxG], cl[kConsumerWarps][kMaxG];
+  __shared__ uint64_t full_bar[C::kStages], empty_bar[C::kStages], cfull[kSlots], cempty[kSlots];
   __shared__ int wtot[kThreads / 32];
-  __shared__ int s_last;
+  __shared__ int meta[C::kStages];  // valid tokens of the block in each stage (0: skipped)
+  __shared__ float ew[kMaxG][kConsumerWarps], ehm[kMaxG], ehl[kMaxG];  // epilogue weights
 
-  // dynamic shared memory: [ring (1024-aligned)][combine O][unit prefix]
+  // dynamic shared memory: [ring (1024-aligned)][combine slots][unit prefix]
   const uint32_t raw = smem_u32(smem_raw);
   uint8_t* ring = smem_raw + (((raw + 1023u) & ~1023u) - raw);
-  float* co = reinterpret_cast<float*>(ring + C::kRingBytes);          // [4][kMaxG][kD]
-  int* prefix = reinterpret_cast<int*>(co + kConsumerWarps * kMaxG * kD);  // [units + 1]
+  CombineSlot* cb = reinterpret_cast<CombineSlot*>(ring + C::kRingBytes);
+  int* prefix = reinterpret_cast<int*>(cb + kSlots);  // [units + 1]
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   if (tid == 0) {
@@ -175,9 +256,13 @@ __global__ void __launch_bounds__(kThreads) sparse_attn_kernel(const __grid_cons
       mbar_init(&full_bar[i], 1);
       mbar_init(&empty_bar[i], 1);
     }
+    for (int i = 0; i < kSlots; ++i) {
+      mbar_init(&cfull[i], kConsumerWarps);
+      mbar_init(&cempty[i], 1);
+    }
     fence_mbar_init();
   }
-  if (warp == kConsumerWarps && lane == 0) {
+  if (warp == kProducerWarp && lane == 0) {
     prefetch_tmap(&tmK);
     prefetch_tmap(&tmV);
   }
@@ -206,104 +291,229 @@ __global__ void __launch_bounds__(kThreads) sparse_attn_kernel(const __grid_cons
     __syncthreads();
   }
   const int64_t N = prefix[a.units];
-  const int Gp = (int)min((int64_t)((int64_t)gridDim.x), (int64_t)(N));
+  const int Gp = (int)min((int64_t)gridDim.x, N);
   const int c = blockIdx.x;
 
-  if (warp == kConsumerWarps) {
-    // ---------------- producer: one thread streams pages -----------------
-    if (lane != 0 || c >= Gp) return;
+  if (warp == kProducerWarp) {
+    // ---------------- producer warp -------------------------------------------
+    // The 32 lanes resolve the next 32 blocks of the range at once (unit, list
+    // entry, page-table slot, valid tokens); lane 0 then streams them in order.
+    if (c >= Gp) return;
     const int64_t start = range_start(c, N, Gp), end = range_start(c + 1, N, Gp);
-    int u = 0;
+    int ucur = 0;
     {
-      int lo = 0, hi = a.units - 1;  // last unit with prefix[u] <= start
+      int lo = 0, hi = a.units - 1;  // last unit with prefix[u] <= start: the unit holding start
       while (lo < hi) {
         const int mid = (lo + hi + 1) >> 1;
         if (prefix[mid] <= start) lo = mid; else hi = mid - 1;
       }
-      u = lo;
+      ucur = lo;
     }
     uint32_t i = 0;
     bool ok = true;
-    for (int64_t pos = start; pos < end && ok; ++u) {
-      const int64_t seg_hi = min((int64_t)(end), (int64_t)(prefix[u + 1]));
-      for (; pos < seg_hi; ++pos, ++i) {
-        const int stage = (int)(i % C::kStages);
-        if (!mbar_wait(&empty_bar[stage], ((i / C::kStages) & 1u) ^ 1u)) {
-          report(a.status, SCOUT_DEV_TIMEOUT);
-          ok = false;
-          break;
+    for (int64_t pos = start; pos < end && ok; pos += 32) {
+      const int64_t x = pos + lane;
+      int64_t slot = -1;
+      int ntok = 0;
+      if (x < end) {
+        int lo = ucur, hi = a.units - 1;
+        while (lo < hi) {
+          const int mid = (lo + hi + 1) >> 1;
+          if (prefix[mid] <= x) lo = mid; else hi = mid - 1;
         }
-        const int j = a.res_list[(int64_t)u * a.k + (pos - prefix[u])];
-        int ntok = 0;
-        const int64_t slot = block_slot(a, u, j, P, &ntok);
-        if (slot < 0) {
-          report(a.status, SCOUT_DEV_BAD_INDEX);
-          mbar_arrive(&full_bar[stage]);
-          continue;
-        }
-        uint8_t* st = ring + stage * C::kStageBytes;
-        mbar_arrive_tx(&full_bar[stage], C::kStageBytes);
-        const int y = (int)(slot * P);
-        tma_load_2d(st, &tmK, 0, y, &full_bar[stage]);
-        tma_load_2d(st + C::kHalfBytes, &tmK, 64, y, &full_bar[stage]);
-        tma_load_2d(st + 2 * C::kHalfBytes, &tmV, 0, y, &full_bar[stage]);
-        tma_load_2d(st + 3 * C::kHalfBytes, &tmV, 64, y, &full_bar[stage]);
+        const int j = a.res_list[(int64_t)lo * a.k + (x - prefix[lo])];
+        slot = block_slot(a, lo, j, P, &ntok);
+        if (slot < 0) ntok = 0;
       }
+      {
+        // the unit of the last position of this batch is where the next batch starts
+        int lo = ucur, hi = a.units - 1;
+        const int64_t xl = min(pos + 31, end - 1);
+        while (lo < hi) {
+          const int mid = (lo + hi + 1) >> 1;
+          if (prefix[mid] <= xl) lo = mid; else hi = mid - 1;
+        }
+        ucur = lo;
+      }
+      const int nb = (int)min((int64_t)32, end - pos);
+      for (int t = 0; t < nb; ++t) {
+        const int64_t slot_t = __shfl_sync(0xffffffffu, slot, t);
+        const int ntok_t = __shfl_sync(0xffffffffu, ntok, t);
+        if (lane == 0 && ok) {
+          if (ntok_t == 0) report(a.status, SCOUT_DEV_BAD_INDEX);
+          for (int h = 0; h < C::kSub && ok; ++h) {
+            const int stage = (int)(i % C::kStages);
+            if (!mbar_wait(&empty_bar[stage], ((i / C::kStages) & 1u) ^ 1u)) {
+              report(a.status, SCOUT_DEV_TIMEOUT);
+              ok = false;
+              break;
+            }
+            const int nt = min(max(ntok_t - h * C::PS, 0), C::PS);
+            meta[stage] = nt;  // published to the consumer by the arrive below
+            if (nt == 0) {
+              mbar_arrive(&full_bar[stage]);
+            } else {
+              uint8_t* st = ring + stage * C::kStageBytes;
+              mbar_arrive_tx(&full_bar[stage], C::kStageBytes);
+              const int y = (int)(slot_t * P) + h * C::PS;
+              tma_load_2d(st, &tmK, 0, y, &full_bar[stage]);
+              tma_load_2d(st + C::kHalfBytes, &tmK, 64, y, &full_bar[stage]);
+              tma_load_2d(st + 2 * C::kHalfBytes, &tmV, 0, y, &full_bar[stage]);
+              tma_load_2d(st + 3 * C::kHalfBytes, &tmV, 64, y, &full_bar[stage]);
+            }
+            ++i;
+          }
+        }
+        __syncwarp();
+      }
+      ok = __shfl_sync(0xffffffffu, ok, 0);
     }
     // drain: wait until every copy issued into a stage has landed
-    for (uint32_t r = 0; r < C::kStages && r < i; ++r) {
-      const uint32_t last = i - 1 - r;
-      if (!mbar_wait(&full_bar[last % C::kStages], (last / C::kStages) & 1u)) report(a.status, SCOUT_DEV_TIMEOUT);
+    if (lane == 0) {
+      for (uint32_t r = 0; r < C::kStages && r < i; ++r) {
+        const uint32_t last = i - 1 - r;
+        if (!mbar_wait(&full_bar[last % C::kStages], (last / C::kStages) & 1u)) report(a.status, SCOUT_DEV_TIMEOUT);
+      }
     }
     return;
   }
 
-  // ---------------- consumers (warps 0..3) ---------------------------------
-  const int g = lane >> 2, t = lane & 3;
-  // units with no resident selected block: O = 0, lse = -inf
-  for (int u = c; u < a.units; u += gridDim.x) {
-    if (prefix[u + 1] != prefix[u]) continue;
-    for (int idx = tid; idx < a.G * kD; idx += kConsumerWarps * 32) a.O_part[(int64_t)u * a.G * kD + idx] = 0.f;
-    if (tid < a.G) a.lse_part[(int64_t)u * a.G + tid] = -INFINITY;
+  if (warp == kEpilogueWarp) {
+    // ---------------- epilogue warp ------------------------------------------
+    // units with no resident selected block: O = 0, lse = -inf
+    for (int u = c; u < a.units; u += gridDim.x) {
+      if (prefix[u + 1] != prefix[u]) continue;
+      for (int idx = lane; idx < a.G * kD; idx += 32) a.O_part[(int64_t)u * a.G * kD + idx] = 0.f;
+      if (lane < a.G) a.lse_part[(int64_t)u * a.G + lane] = -INFINITY;
+    }
+    if (c >= Gp) return;
+    const int64_t start = range_start(c, N, Gp), end = range_start(c + 1, N, Gp);
+    SegIter it{prefix, start, end, unit_of(prefix, a.units, start)};
+    int u;
+    int64_t lo, hi;
+    for (int sg = 0; it.next(u, lo, hi); ++sg) {
+      const int slot = sg % kSlots;
+      if (!mbar_wait(&cfull[slot], (uint32_t)(sg / kSlots) & 1u) && lane == 0) report(a.status, SCOUT_DEV_TIMEOUT);
+      const CombineSlot& cs = cb[slot];
+      const bool whole = lo == prefix[u] && hi == prefix[u + 1];
+      const int which = prefix[u] <= start ? 0 : 1;
+      // per-head weights of the four warps' states (normalised), and the head's LSE
+      if (lane < a.G) {
+        float M = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, cs.m[w][lane]);
+        float f[kConsumerWarps], L = 0.f;
+#pragma unroll
+        for (int w = 0; w < kConsumerWarps; ++w) {
+          f[w] = M == -INFINITY ? 0.f : exp2f(cs.m[w][lane] - M);
+          L += cs.l[w][lane] * f[w];
+        }
+#pragma unroll
+        for (int w = 0; w < kConsumerWarps; ++w) ew[lane][w] = L > 0.f ? f[w] / L : 0.f;
+        const float lse = L > 0.f ? (M + log2f(L)) * kLn2 : -INFINITY;
+        if (whole) a.lse_part[(int64_t)u * a.G + lane] = lse;
+        else a.slot_lse[((int64_t)c * 2 + which) * kMaxG + lane] = lse;
+      }
+      __syncwarp();
+      float* dst = whole ? a.O_part + (int64_t)u * a.G * kD : a.slot_O + ((int64_t)c * 2 + which) * kMaxG * kD;
+      for (int i4 = lane; i4 < a.G * (kD / 4); i4 += 32) {
+        const int h = i4 / (kD / 4), d = (i4 % (kD / 4)) * 4;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int w = 0; w < kConsumerWarps; ++w) {
+          const float4 o = *reinterpret_cast<const float4*>(&cs.o[w][h][d]);
+          const float f = ew[h][w];
+          acc.x += f * o.x;
+          acc.y += f * o.y;
+          acc.z += f * o.z;
+          acc.w += f * o.w;
+        }
+        reinterpret_cast<float4*>(dst + h * kD + d)[0] = acc;
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&cempty[slot]);  // the combine slot may be refilled
+      if (!whole) {
+        __threadfence();
+        __syncwarp();
+        const int c0 = cta_of(prefix[u], N, Gp), c1 = cta_of(prefix[u + 1] - 1, N, Gp);
+        int last = 0;
+        if (lane == 0) last = atomicAdd(&a.counters[u], 1) == c1 - c0;
+        last = __shfl_sync(0xffffffffu, last, 0);
+        if (last) {
+          __threadfence();
+          // per head: max and sum of the pieces' LSE weights
+          if (lane < a.G) {
+            float M = -INFINITY;
+            for (int cc = c0; cc <= c1; ++cc) {
+              const int64_t sl = (int64_t)cc * 2 + (prefix[u] <= range_start(cc, N, Gp) ? 0 : 1);
+              M = fmaxf(M, __ldcg(a.slot_lse + sl * kMaxG + lane));
+            }
+            float L = 0.f;
+            if (M != -INFINITY)
+              for (int cc = c0; cc <= c1; ++cc) {
+                const int64_t sl = (int64_t)cc * 2 + (prefix[u] <= range_start(cc, N, Gp) ? 0 : 1);
+                L += expf(__ldcg(a.slot_lse + sl * kMaxG + lane) - M);
+              }
+            ehm[lane] = M;
+            ehl[lane] = L;
+            a.lse_part[(int64_t)u * a.G + lane] = L > 0.f ? M + logf(L) : -INFINITY;
+          }
+          __syncwarp();
+          for (int i4 = lane; i4 < a.G * (kD / 4); i4 += 32) {
+            const int h = i4 / (kD / 4), d = (i4 % (kD / 4)) * 4;
+            const float M = ehm[h], L = ehl[h];
+            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (L > 0.f)
+              for (int cc = c0; cc <= c1; ++cc) {
+                const int64_t sl = (int64_t)cc * 2 + (prefix[u] <= range_start(cc, N, Gp) ? 0 : 1);
+                const float f = expf(__ldcg(a.slot_lse + sl * kMaxG + h) - M) / L;
+                const float4 o = __ldcg(reinterpret_cast<const float4*>(a.slot_O + (sl * kMaxG + h) * kD + d));
+                acc.x += f * o.x;
+                acc.y += f * o.y;
+                acc.z += f * o.z;
+                acc.w += f * o.w;
+              }
+            reinterpret_cast<float4*>(a.O_part + ((int64_t)u * a.G + h) * kD + d)[0] = acc;
+          }
+          if (lane == 0) a.counters[u] = 0;  // ready for the next call
+        }
+      }
+    }
+    return;
   }
+
+  // ---------------- consumer warps 0..3 ----------------------------------------
   if (c >= Gp) return;
+  const int g = lane >> 2, t = lane & 3;
   const int64_t start = range_start(c, N, Gp), end = range_start(c + 1, N, Gp);
-  int u0 = 0;
-  {
-    int lo = 0, hi = a.units - 1;
-    while (lo < hi) {
-      const int mid = (lo + hi + 1) >> 1;
-      if (prefix[mid] <= start) lo = mid; else hi = mid - 1;
-    }
-    u0 = lo;
-  }
+  SegIter it{prefix, start, end, unit_of(prefix, a.units, start)};
   const uint32_t ring_s = smem_u32(ring);
+  int u;
+  int64_t lo, hi;
+  bool have = it.next(u, lo, hi);
+  uint32_t qa[8][2], qn[8][2];
+  if (have) load_q(a, u, lane, qa);
   uint32_t i = 0;
-  for (int64_t pos = start, u = u0; pos < end; ++u) {
-    const int64_t seg_lo = pos, seg_hi = min((int64_t)(end), (int64_t)(prefix[u + 1]));
-    if (seg_hi <= seg_lo) continue;
-    const int b = (int)(u / a.Hkv), kvh = (int)(u - (int64_t)b * a.Hkv);
-    uint32_t qa[8][2];
-    const __nv_bfloat16* qrow = a.q + ((int64_t)b * a.Hq + (int64_t)kvh * a.G + g) * kD;
-#pragma unroll
-    for (int ks = 0; ks < 8; ++ks) {
-      qa[ks][0] = g < a.G ? *reinterpret_cast<const uint32_t*>(qrow + ks * 16 + 2 * t) : 0u;
-      qa[ks][1] = g < a.G ? *reinterpret_cast<const uint32_t*>(qrow + ks * 16 + 8 + 2 * t) : 0u;
-    }
+  for (int sg = 0; have; ++sg) {
+    // prefetch the next segment's query while this one streams
+    SegIter peek = it;
+    int un;
+    int64_t lo2, hi2;
+    const bool have2 = peek.next(un, lo2, hi2);
+    if (have2) load_q(a, un, lane, qn);
     WarpState st;
-    st.m = -INFINITY;
-    st.l = 0.f;
+    st.m[0] = st.m[1] = -INFINITY;
+    st.l[0] = st.l[1] = 0.f;
 #pragma unroll
-    for (int d = 0; d < 16; ++d) st.o[d][0] = st.o[d][1] = st.o[d][2] = st.o[d][3] = 0.f;
-    for (int64_t p = seg_lo; p < seg_hi; ++p, ++i) {
+    for (int d = 0; d < 8; ++d) st.o[d][0] = st.o[d][1] = st.o[d][2] = st.o[d][3] = 0.f;
+    for (int64_t p = lo * C::kSub; p < hi * C::kSub; ++p, ++i) {  // sub-pages of the segment's blocks
       if ((int)(i % kConsumerWarps) != warp) continue;
       const int stage = (int)(i % C::kStages);
       if (!mbar_wait(&full_bar[stage], (i / C::kStages) & 1u)) {
         if (lane == 0) report(a.status, SCOUT_DEV_TIMEOUT);
       } else {
-        const int j = a.res_list[u * a.k + (p - prefix[u])];
-        int ntok = 0;
-        if (block_slot(a, (int)u, j, P, &ntok) >= 0) {
+        const int ntok = meta[stage];
+        if (ntok > 0) {
           const uint32_t kb = ring_s + stage * C::kStageBytes;
           attend_page<P>(kb, kb + 2 * C::kHalfBytes, ntok, qa, a.scale_log2, st, lane);
         }
@@ -311,82 +521,46 @@ __global__ void __launch_bounds__(kThreads) sparse_attn_kernel(const __grid_cons
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty_bar[stage]);
     }
-    pos = seg_hi;
-
-    // combine the four warps of this CTA
-    float lsum = st.l + __shfl_xor_sync(0xffffffffu, st.l, 1);
-    lsum += __shfl_xor_sync(0xffffffffu, lsum, 2);
-    if (g < a.G) {
-      if (t == 0) {
-        cm[warp][g] = st.m;
-        cl[warp][g] = lsum;
-      }
-      float* dst = co + (warp * kMaxG + g) * kD;
+    // hand this warp's state for the segment to the epilogue warp
+    float l0 = st.l[0], l1 = st.l[1];
 #pragma unroll
-      for (int d = 0; d < 16; ++d) {
-        dst[d * 8 + 2 * t] = st.o[d][0];
-        dst[d * 8 + 2 * t + 1] = st.o[d][1];
+    for (int o = 4; o < 32; o <<= 1) {
+      l0 += __shfl_xor_sync(0xffffffffu, l0, o);
+      l1 += __shfl_xor_sync(0xffffffffu, l1, o);
+    }
+    const int slot = sg % kSlots;
+    if (!mbar_wait(&cempty[slot], ((uint32_t)(sg / kSlots) & 1u) ^ 1u) && lane == 0) report(a.status, SCOUT_DEV_TIMEOUT);
+    CombineSlot& cs = cb[slot];
+    if (g == 0) {
+      if (2 * t < a.G) {
+        cs.m[warp][2 * t] = st.m[0];
+        cs.l[warp][2 * t] = l0;
+      }
+      if (2 * t + 1 < a.G) {
+        cs.m[warp][2 * t + 1] = st.m[1];
+        cs.l[warp][2 * t + 1] = l1;
       }
     }
-    consumer_sync();
-    const bool whole = seg_lo == prefix[u] && seg_hi == prefix[u + 1];
-    const int which = prefix[u] <= start ? 0 : 1;
-    for (int idx = tid; idx < a.G * kD; idx += kConsumerWarps * 32) {
-      const int h = idx / kD, d = idx - h * kD;
-      float M = -INFINITY;
 #pragma unroll
-      for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, cm[w][h]);
-      float L = 0.f, acc = 0.f;
-      if (M != -INFINITY) {
-#pragma unroll
-        for (int w = 0; w < kConsumerWarps; ++w) {
-          const float f = exp2f(cm[w][h] - M);
-          L += cl[w][h] * f;
-          acc += co[(w * kMaxG + h) * kD + d] * f;
-        }
+    for (int md = 0; md < 8; ++md) {
+      const int d0 = md * 16 + g;
+      if (2 * t < a.G) {
+        cs.o[warp][2 * t][d0] = st.o[md][0];
+        cs.o[warp][2 * t][d0 + 8] = st.o[md][2];
       }
-      const float O = L > 0.f ? acc / L : 0.f;
-      const float lse = L > 0.f ? (M + log2f(L)) * kLn2 : -INFINITY;
-      if (whole) {
-        a.O_part[(u * a.G + h) * kD + d] = O;
-        if (d == 0) a.lse_part[u * a.G + h] = lse;
-      } else {
-        const int64_t sl = (int64_t)c * 2 + which;
-        a.slot_O[(sl * kMaxG + h) * kD + d] = O;
-        if (d == 0) a.slot_lse[sl * kMaxG + h] = lse;
+      if (2 * t + 1 < a.G) {
+        cs.o[warp][2 * t + 1][d0] = st.o[md][1];
+        cs.o[warp][2 * t + 1][d0 + 8] = st.o[md][3];
       }
     }
-    if (!whole) {
-      __threadfence();
-      consumer_sync();
-      const int c0 = cta_of(prefix[u], N, Gp), c1 = cta_of(prefix[u + 1] - 1, N, Gp);
-      if (tid == 0) s_last = atomicAdd(&a.counters[u], 1) == c1 - c0;
-      consumer_sync();
-      if (s_last) {
-        __threadfence();
-        for (int idx = tid; idx < a.G * kD; idx += kConsumerWarps * 32) {
-          const int h = idx / kD, d = idx - h * kD;
-          float M = -INFINITY;
-          for (int cc = c0; cc <= c1; ++cc) {
-            const int64_t sl = (int64_t)cc * 2 + (prefix[u] <= range_start(cc, N, Gp) ? 0 : 1);
-            M = fmaxf(M, __ldcg(a.slot_lse + sl * kMaxG + h));
-          }
-          float L = 0.f, acc = 0.f;
-          if (M != -INFINITY) {
-            for (int cc = c0; cc <= c1; ++cc) {
-              const int64_t sl = (int64_t)cc * 2 + (prefix[u] <= range_start(cc, N, Gp) ? 0 : 1);
-              const float f = expf(__ldcg(a.slot_lse + sl * kMaxG + h) - M);
-              L += f;
-              acc += f * __ldcg(a.slot_O + (sl * kMaxG + h) * kD + d);
-            }
-          }
-          a.O_part[(u * a.G + h) * kD + d] = L > 0.f ? acc / L : 0.f;
-          if (d == 0) a.lse_part[u * a.G + h] = L > 0.f ? M + logf(L) : -INFINITY;
-        }
-        if (tid == 0) a.counters[u] = 0;  // ready for the next call
-      }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&cfull[slot]);
+    have = it.next(u, lo, hi);
+#pragma unroll
+    for (int ks = 0; ks < 8; ++ks) {
+      qa[ks][0] = qn[ks][0];
+      qa[ks][1] = qn[ks][1];
     }
-    consumer_sync();  // the combine scratch is reused by the next segment
   }
 }
 
@@ -396,13 +570,15 @@ constexpr size_t kSlotOBytes = (size_t)kMaxGrid * 2 * kMaxG * kD * sizeof(float)
 
 template <int P>
 size_t dyn_smem(int units) {
-  return 1024 + Cfg<P>::kRingBytes + (size_t)kConsumerWarps * kMaxG * kD * sizeof(float) + (size_t)(units + 1) * 4;
+  return 1024 + Cfg<P>::kRingBytes + kSlots * sizeof(CombineSlot) + (size_t)(units + 1) * 4;
 }
 
-bool make_page_map(CUtensorMap* map, const void* pool, int64_t n_slots, int P) {
+// The pool as a 2-D bf16 tensor [n_slots * P rows][128 columns]; boxes of 64 columns
+// x box_rows tokens (one sub-page) with the 128-byte swizzle.
+bool make_page_map(CUtensorMap* map, const void* pool, int64_t n_slots, int P, int box_rows) {
   const cuuint64_t dims[2] = {(cuuint64_t)kD, (cuuint64_t)(n_slots * P)};
   const cuuint64_t strides[1] = {(cuuint64_t)kD * 2};
-  const cuuint32_t box[2] = {64, (cuuint32_t)P};
+  const cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
   const cuuint32_t estr[2] = {1, 1};
   return encode_tiled(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(pool), dims, strides, box, estr,
                       CU_TENSOR_MAP_SWIZZLE_128B) == CUDA_SUCCESS;
@@ -411,11 +587,12 @@ bool make_page_map(CUtensorMap* map, const void* pool, int64_t n_slots, int P) {
 template <int P>
 int launch_attn(const void* K_pool, const void* V_pool, const AttnArgs& a, cudaStream_t stream) {
   CUtensorMap tmK, tmV;
-  if (!make_page_map(&tmK, K_pool, a.n_slots, P) || !make_page_map(&tmV, V_pool, a.n_slots, P))
+  if (!make_page_map(&tmK, K_pool, a.n_slots, P, Cfg<P>::PS) || !make_page_map(&tmV, V_pool, a.n_slots, P, Cfg<P>::PS))
     return SCOUT_ERR_UNSUPPORTED;
   const size_t smem = dyn_smem<P>(a.units);
   if (cudaFuncSetAttribute(sparse_attn_kernel<P>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
-      cudaSuccess)
+          cudaSuccess ||
+      cudaFuncSetAttribute(sparse_attn_kernel<P>, cudaFuncAttributePreferredSharedMemoryCarveout, 100) != cudaSuccess)
     return SCOUT_ERR_CUDA;
   int occ = 0;
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, sparse_attn_kernel<P>, kThreads, smem) != cudaSuccess ||

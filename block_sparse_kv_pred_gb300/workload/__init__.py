@@ -207,7 +207,9 @@ class Workload:
       page_table[u][j] slot of block j of unit u in the K/V pool (a seeded permutation)
     """
 
-    def __init__(self, shape: Shape):
+    def __init__(self, shape: Shape, pool_slots: int | None = None):
+        """``pool_slots`` (profiling only) shrinks the K/V pool: blocks share slots, so
+        the pool no longer holds each block's own keys and parity does not apply."""
         self.s = s = shape
         rng = np.random.Generator(np.random.PCG64(s.seed))
         self.seq_len = s.lens()
@@ -242,11 +244,15 @@ class Workload:
         # pool slots: a seeded permutation so the page table is exercised
         nslots = U * nb
         perm = rng.permutation(nslots).astype(np.int32)
+        if pool_slots is not None and pool_slots < nslots:
+            perm = perm % np.int32(pool_slots)
+            nslots = int(pool_slots)
         self.page_table = perm.reshape(U, nb)
         inv = np.empty(nslots, dtype=np.int32)
-        inv[perm] = np.arange(nslots, dtype=np.int32)
-        self.slot_owner = inv  # slot -> u * nblk + j
+        inv[perm] = np.arange(U * nb, dtype=np.int32)
+        self.slot_owner = inv  # slot -> u * nblk + j (one owner per slot)
         self.n_slots = nslots
+        self.aliased = nslots < U * nb
 
     # -- bitmaps -----------------------------------------------------------
     def resident_bits(self, resident: np.ndarray | None = None) -> np.ndarray:
