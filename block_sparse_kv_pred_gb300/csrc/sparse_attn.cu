@@ -26,7 +26,7 @@ constexpr int kProducerWarp = kConsumerWarps;      // streams pages with TMA
 constexpr int kEpilogueWarp = kConsumerWarps + 1;  // combines, writes, fixes up split units
 constexpr int kThreads = (kConsumerWarps + 2) * 32;
 constexpr int kMaxUnits = 4096;
-constexpr int kSlots = 1;  // combine slots between the consumer warps and the epilogue warp
+constexpr int kMaxSlots = 2;  // combine slots between the consumer warps and the epilogue warp
 constexpr int kMaxGrid = 1024;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
@@ -52,6 +52,7 @@ struct AttnArgs {
   int Hq, Hkv, G, nblk_cap, k, units;
   int64_t n_slots;
   float scale_log2;  // scale * log2(e)
+  int nslots;  // combine slots that fit in shared memory (1 or 2)
   float* O_part;
   float* lse_part;
   int32_t* counters;   // [units]
@@ -183,12 +184,23 @@ __device__ __forceinline__ void attend_page(uint32_t kbase, uint32_t vbase, int 
 }
 
 // One segment's per-warp softmax states, handed from the consumer warps to the
-// epilogue warp through shared memory.
-struct CombineSlot {
-  float m[kConsumerWarps][kMaxG];
-  float l[kConsumerWarps][kMaxG];
-  float o[kConsumerWarps][kMaxG][kD];
+// epilogue warp through shared memory.  A slot holds m[4][8], l[4][8] and
+// O^T partials o[4][G][128] (fp32); its size depends on G, so two slots fit for the
+// usual GQA groups.
+__host__ __device__ constexpr int slot_floats(int G) { return 64 + kConsumerWarps * G * kD; }
+struct SlotView {
+  float* base;
+  int G;
+  __device__ float& m(int w, int h) const { return base[w * kMaxG + h]; }
+  __device__ float& l(int w, int h) const { return base[32 + w * kMaxG + h]; }
+  __device__ float* o(int w, int h) const { return base + 64 + (w * G + h) * kD; }
 };
+
+__device__ __forceinline__ int ld_acquire(const int* p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
 
 // Walks the unit segments of one CTA's flattened block range [pos, end).
 struct SegIter {
@@ -239,16 +251,17 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const __grid_c
                                                                   const AttnArgs a) {
   using C = Cfg<P>;
   extern __shared__ uint8_t smem_raw[];
-  __shared__ uint64_t full_bar[C::kStages], empty_bar[C::kStages], cfull[kSlots], cempty[kSlots];
+  __shared__ uint64_t full_bar[C::kStages], empty_bar[C::kStages], cfull[kMaxSlots], cempty[kMaxSlots];
   __shared__ int wtot[kThreads / 32];
   __shared__ int meta[C::kStages];  // valid tokens of the block in each stage (0: skipped)
-  __shared__ float ew[kMaxG][kConsumerWarps], ehm[kMaxG], ehl[kMaxG];  // epilogue weights
+  __shared__ float ew[kMaxG][kConsumerWarps], ehm[kMaxG], ehl[kMaxG], eown[kMaxG];  // epilogue weights
 
   // dynamic shared memory: [ring (1024-aligned)][combine slots][unit prefix]
   const uint32_t raw = smem_u32(smem_raw);
   uint8_t* ring = smem_raw + (((raw + 1023u) & ~1023u) - raw);
-  CombineSlot* cb = reinterpret_cast<CombineSlot*>(ring + C::kRingBytes);
-  int* prefix = reinterpret_cast<int*>(cb + kSlots);  // [units + 1]
+  float* cbf = reinterpret_cast<float*>(ring + C::kRingBytes);
+  const int slot_f = slot_floats(a.G);
+  int* prefix = reinterpret_cast<int*>(cbf + a.nslots * slot_f);  // [units + 1]
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   if (tid == 0) {
@@ -256,7 +269,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const __grid_c
       mbar_init(&full_bar[i], 1);
       mbar_init(&empty_bar[i], 1);
     }
-    for (int i = 0; i < kSlots; ++i) {
+    for (int i = 0; i < a.nslots; ++i) {
       mbar_init(&cfull[i], kConsumerWarps);
       mbar_init(&cempty[i], 1);
     }
@@ -392,91 +405,155 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const __grid_c
     int u;
     int64_t lo, hi;
     for (int sg = 0; it.next(u, lo, hi); ++sg) {
-      const int slot = sg % kSlots;
-      if (!mbar_wait(&cfull[slot], (uint32_t)(sg / kSlots) & 1u) && lane == 0) report(a.status, SCOUT_DEV_TIMEOUT);
-      const CombineSlot& cs = cb[slot];
+      const int slot = sg % a.nslots;
+      if (!mbar_wait(&cfull[slot], (uint32_t)(sg / a.nslots) & 1u) && lane == 0) report(a.status, SCOUT_DEV_TIMEOUT);
+      const SlotView cs{cbf + slot * slot_f, a.G};
       const bool whole = lo == prefix[u] && hi == prefix[u + 1];
       const int which = prefix[u] <= start ? 0 : 1;
-      // per-head weights of the four warps' states (normalised), and the head's LSE
+      // per-head weights of the four warps' states (normalised) and this piece's LSE
       if (lane < a.G) {
         float M = -INFINITY;
 #pragma unroll
-        for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, cs.m[w][lane]);
+        for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, cs.m(w, lane));
         float f[kConsumerWarps], L = 0.f;
 #pragma unroll
         for (int w = 0; w < kConsumerWarps; ++w) {
-          f[w] = M == -INFINITY ? 0.f : exp2f(cs.m[w][lane] - M);
-          L += cs.l[w][lane] * f[w];
+          f[w] = M == -INFINITY ? 0.f : exp2f(cs.m(w, lane) - M);
+          L += cs.l(w, lane) * f[w];
         }
 #pragma unroll
         for (int w = 0; w < kConsumerWarps; ++w) ew[lane][w] = L > 0.f ? f[w] / L : 0.f;
-        const float lse = L > 0.f ? (M + log2f(L)) * kLn2 : -INFINITY;
-        if (whole) a.lse_part[(int64_t)u * a.G + lane] = lse;
-        else a.slot_lse[((int64_t)c * 2 + which) * kMaxG + lane] = lse;
+        eown[lane] = L > 0.f ? (M + log2f(L)) * kLn2 : -INFINITY;
       }
       __syncwarp();
-      float* dst = whole ? a.O_part + (int64_t)u * a.G * kD : a.slot_O + ((int64_t)c * 2 + which) * kMaxG * kD;
-      for (int i4 = lane; i4 < a.G * (kD / 4); i4 += 32) {
-        const int h = i4 / (kD / 4), d = (i4 % (kD / 4)) * 4;
+      // this piece's normalised output, 4 dims per lane
+      auto own4 = [&](int h, int d) {
         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
         for (int w = 0; w < kConsumerWarps; ++w) {
-          const float4 o = *reinterpret_cast<const float4*>(&cs.o[w][h][d]);
+          const float4 o = *reinterpret_cast<const float4*>(cs.o(w, h) + d);
           const float f = ew[h][w];
           acc.x += f * o.x;
           acc.y += f * o.y;
           acc.z += f * o.z;
           acc.w += f * o.w;
         }
-        reinterpret_cast<float4*>(dst + h * kD + d)[0] = acc;
+        return acc;
+      };
+      if (whole) {
+        if (lane < a.G) a.lse_part[(int64_t)u * a.G + lane] = eown[lane];
+        for (int i4 = lane; i4 < a.G * (kD / 4); i4 += 32) {
+          const int h = i4 / (kD / 4), d = (i4 % (kD / 4)) * 4;
+          reinterpret_cast<float4*>(a.O_part + ((int64_t)u * a.G + h) * kD + d)[0] = own4(h, d);
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&cempty[slot]);  // the combine slot may be refilled
+        continue;
+      }
+      // a unit cut by a range boundary: pieces c0..c1, one per CTA range it touches
+      const int c0 = cta_of(prefix[u], N, Gp), c1 = cta_of(prefix[u + 1] - 1, N, Gp);
+      auto piece_slot = [&](int cc) {
+        return (int64_t)cc * 2 + (prefix[u] <= range_start(cc, N, Gp) ? 0 : 1);
+      };
+      int seen = 0;
+      if (lane == 0) seen = ld_acquire(&a.counters[u]);
+      seen = __shfl_sync(0xffffffffu, seen, 0);
+      if (seen == c1 - c0) {
+        // every other piece has published: finish the unit from this piece's state
+        // and the others' partials (nothing of this piece goes through memory)
+        if (lane < a.G) {
+          float M = eown[lane];
+          for (int cc = c0; cc <= c1; ++cc)
+            if (cc != c) M = fmaxf(M, __ldcg(a.slot_lse + piece_slot(cc) * kMaxG + lane));
+          float L = 0.f;
+          if (M != -INFINITY) {
+            L = eown[lane] == -INFINITY ? 0.f : expf(eown[lane] - M);
+            for (int cc = c0; cc <= c1; ++cc)
+              if (cc != c) L += expf(__ldcg(a.slot_lse + piece_slot(cc) * kMaxG + lane) - M);
+          }
+          ehm[lane] = M;
+          ehl[lane] = L;
+          a.lse_part[(int64_t)u * a.G + lane] = L > 0.f ? M + logf(L) : -INFINITY;
+        }
+        __syncwarp();
+        for (int i4 = lane; i4 < a.G * (kD / 4); i4 += 32) {
+          const int h = i4 / (kD / 4), d = (i4 % (kD / 4)) * 4;
+          const float M = ehm[h], L = ehl[h];
+          float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+          if (L > 0.f) {
+            if (eown[h] != -INFINITY) {
+              const float f = expf(eown[h] - M) / L;
+              const float4 o = own4(h, d);
+              acc.x = f * o.x;
+              acc.y = f * o.y;
+              acc.z = f * o.z;
+              acc.w = f * o.w;
+            }
+            for (int cc = c0; cc <= c1; ++cc) {
+              if (cc == c) continue;
+              const int64_t sl = piece_slot(cc);
+              const float f = expf(__ldcg(a.slot_lse + sl * kMaxG + h) - M) / L;
+              const float4 o = __ldcg(reinterpret_cast<const float4*>(a.slot_O + (sl * kMaxG + h) * kD + d));
+              acc.x += f * o.x;
+              acc.y += f * o.y;
+              acc.z += f * o.z;
+              acc.w += f * o.w;
+            }
+          }
+          reinterpret_cast<float4*>(a.O_part + ((int64_t)u * a.G + h) * kD + d)[0] = acc;
+        }
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(&cempty[slot]);
+          a.counters[u] = 0;  // ready for the next call
+        }
+        continue;
+      }
+      // publish this piece, then count it; the piece that completes the count finishes the unit
+      const int64_t msl = (int64_t)c * 2 + which;
+      if (lane < a.G) a.slot_lse[msl * kMaxG + lane] = eown[lane];
+      for (int i4 = lane; i4 < a.G * (kD / 4); i4 += 32) {
+        const int h = i4 / (kD / 4), d = (i4 % (kD / 4)) * 4;
+        reinterpret_cast<float4*>(a.slot_O + (msl * kMaxG + h) * kD + d)[0] = own4(h, d);
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&cempty[slot]);  // the combine slot may be refilled
-      if (!whole) {
+      __threadfence();
+      __syncwarp();
+      int last = 0;
+      if (lane == 0) last = atomicAdd(&a.counters[u], 1) == c1 - c0;
+      last = __shfl_sync(0xffffffffu, last, 0);
+      if (last) {
         __threadfence();
-        __syncwarp();
-        const int c0 = cta_of(prefix[u], N, Gp), c1 = cta_of(prefix[u + 1] - 1, N, Gp);
-        int last = 0;
-        if (lane == 0) last = atomicAdd(&a.counters[u], 1) == c1 - c0;
-        last = __shfl_sync(0xffffffffu, last, 0);
-        if (last) {
-          __threadfence();
-          // per head: max and sum of the pieces' LSE weights
-          if (lane < a.G) {
-            float M = -INFINITY;
-            for (int cc = c0; cc <= c1; ++cc) {
-              const int64_t sl = (int64_t)cc * 2 + (prefix[u] <= range_start(cc, N, Gp) ? 0 : 1);
-              M = fmaxf(M, __ldcg(a.slot_lse + sl * kMaxG + lane));
-            }
-            float L = 0.f;
-            if (M != -INFINITY)
-              for (int cc = c0; cc <= c1; ++cc) {
-                const int64_t sl = (int64_t)cc * 2 + (prefix[u] <= range_start(cc, N, Gp) ? 0 : 1);
-                L += expf(__ldcg(a.slot_lse + sl * kMaxG + lane) - M);
-              }
-            ehm[lane] = M;
-            ehl[lane] = L;
-            a.lse_part[(int64_t)u * a.G + lane] = L > 0.f ? M + logf(L) : -INFINITY;
-          }
-          __syncwarp();
-          for (int i4 = lane; i4 < a.G * (kD / 4); i4 += 32) {
-            const int h = i4 / (kD / 4), d = (i4 % (kD / 4)) * 4;
-            const float M = ehm[h], L = ehl[h];
-            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-            if (L > 0.f)
-              for (int cc = c0; cc <= c1; ++cc) {
-                const int64_t sl = (int64_t)cc * 2 + (prefix[u] <= range_start(cc, N, Gp) ? 0 : 1);
-                const float f = expf(__ldcg(a.slot_lse + sl * kMaxG + h) - M) / L;
-                const float4 o = __ldcg(reinterpret_cast<const float4*>(a.slot_O + (sl * kMaxG + h) * kD + d));
-                acc.x += f * o.x;
-                acc.y += f * o.y;
-                acc.z += f * o.z;
-                acc.w += f * o.w;
-              }
-            reinterpret_cast<float4*>(a.O_part + ((int64_t)u * a.G + h) * kD + d)[0] = acc;
-          }
-          if (lane == 0) a.counters[u] = 0;  // ready for the next call
+        // per head: max and sum of the pieces' LSE weights
+        if (lane < a.G) {
+          float M = -INFINITY;
+          for (int cc = c0; cc <= c1; ++cc) M = fmaxf(M, __ldcg(a.slot_lse + piece_slot(cc) * kMaxG + lane));
+          float L = 0.f;
+          if (M != -INFINITY)
+            for (int cc = c0; cc <= c1; ++cc) L += expf(__ldcg(a.slot_lse + piece_slot(cc) * kMaxG + lane) - M);
+          ehm[lane] = M;
+          ehl[lane] = L;
+          a.lse_part[(int64_t)u * a.G + lane] = L > 0.f ? M + logf(L) : -INFINITY;
         }
+        __syncwarp();
+        for (int i4 = lane; i4 < a.G * (kD / 4); i4 += 32) {
+          const int h = i4 / (kD / 4), d = (i4 % (kD / 4)) * 4;
+          const float M = ehm[h], L = ehl[h];
+          float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+          if (L > 0.f)
+            for (int cc = c0; cc <= c1; ++cc) {
+              const int64_t sl = piece_slot(cc);
+              const float f = expf(__ldcg(a.slot_lse + sl * kMaxG + h) - M) / L;
+              const float4 o = __ldcg(reinterpret_cast<const float4*>(a.slot_O + (sl * kMaxG + h) * kD + d));
+              acc.x += f * o.x;
+              acc.y += f * o.y;
+              acc.z += f * o.z;
+              acc.w += f * o.w;
+            }
+          reinterpret_cast<float4*>(a.O_part + ((int64_t)u * a.G + h) * kD + d)[0] = acc;
+        }
+        if (lane == 0) a.counters[u] = 0;  // ready for the next call
       }
     }
     return;
@@ -528,29 +605,29 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const __grid_c
       l0 += __shfl_xor_sync(0xffffffffu, l0, o);
       l1 += __shfl_xor_sync(0xffffffffu, l1, o);
     }
-    const int slot = sg % kSlots;
-    if (!mbar_wait(&cempty[slot], ((uint32_t)(sg / kSlots) & 1u) ^ 1u) && lane == 0) report(a.status, SCOUT_DEV_TIMEOUT);
-    CombineSlot& cs = cb[slot];
+    const int slot = sg % a.nslots;
+    if (!mbar_wait(&cempty[slot], ((uint32_t)(sg / a.nslots) & 1u) ^ 1u) && lane == 0) report(a.status, SCOUT_DEV_TIMEOUT);
+    const SlotView cs{cbf + slot * slot_f, a.G};
     if (g == 0) {
       if (2 * t < a.G) {
-        cs.m[warp][2 * t] = st.m[0];
-        cs.l[warp][2 * t] = l0;
+        cs.m(warp, 2 * t) = st.m[0];
+        cs.l(warp, 2 * t) = l0;
       }
       if (2 * t + 1 < a.G) {
-        cs.m[warp][2 * t + 1] = st.m[1];
-        cs.l[warp][2 * t + 1] = l1;
+        cs.m(warp, 2 * t + 1) = st.m[1];
+        cs.l(warp, 2 * t + 1) = l1;
       }
     }
 #pragma unroll
     for (int md = 0; md < 8; ++md) {
       const int d0 = md * 16 + g;
       if (2 * t < a.G) {
-        cs.o[warp][2 * t][d0] = st.o[md][0];
-        cs.o[warp][2 * t][d0 + 8] = st.o[md][2];
+        cs.o(warp, 2 * t)[d0] = st.o[md][0];
+        cs.o(warp, 2 * t)[d0 + 8] = st.o[md][2];
       }
       if (2 * t + 1 < a.G) {
-        cs.o[warp][2 * t + 1][d0] = st.o[md][1];
-        cs.o[warp][2 * t + 1][d0 + 8] = st.o[md][3];
+        cs.o(warp, 2 * t + 1)[d0] = st.o[md][1];
+        cs.o(warp, 2 * t + 1)[d0 + 8] = st.o[md][3];
       }
     }
     __syncwarp();
@@ -569,9 +646,10 @@ constexpr size_t kSlotLseBytes = (size_t)kMaxGrid * 2 * kMaxG * sizeof(float);
 constexpr size_t kSlotOBytes = (size_t)kMaxGrid * 2 * kMaxG * kD * sizeof(float);
 
 template <int P>
-size_t dyn_smem(int units) {
-  return 1024 + Cfg<P>::kRingBytes + kSlots * sizeof(CombineSlot) + (size_t)(units + 1) * 4;
+size_t dyn_smem(int units, int G, int nslots) {
+  return 1024 + Cfg<P>::kRingBytes + (size_t)nslots * slot_floats(G) * sizeof(float) + (size_t)(units + 1) * 4;
 }
+constexpr size_t kSmemLimit = 232448 - 1024;  // per-block shared memory minus room for static use
 
 // The pool as a 2-D bf16 tensor [n_slots * P rows][128 columns]; boxes of 64 columns
 // x box_rows tokens (one sub-page) with the 128-byte swizzle.
@@ -585,11 +663,12 @@ bool make_page_map(CUtensorMap* map, const void* pool, int64_t n_slots, int P, i
 }
 
 template <int P>
-int launch_attn(const void* K_pool, const void* V_pool, const AttnArgs& a, cudaStream_t stream) {
+int launch_attn(const void* K_pool, const void* V_pool, AttnArgs a, cudaStream_t stream) {
+  a.nslots = dyn_smem<P>(a.units, a.G, 2) <= kSmemLimit ? 2 : 1;
   CUtensorMap tmK, tmV;
   if (!make_page_map(&tmK, K_pool, a.n_slots, P, Cfg<P>::PS) || !make_page_map(&tmV, V_pool, a.n_slots, P, Cfg<P>::PS))
     return SCOUT_ERR_UNSUPPORTED;
-  const size_t smem = dyn_smem<P>(a.units);
+  const size_t smem = dyn_smem<P>(a.units, a.G, a.nslots);
   if (cudaFuncSetAttribute(sparse_attn_kernel<P>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
           cudaSuccess ||
       cudaFuncSetAttribute(sparse_attn_kernel<P>, cudaFuncAttributePreferredSharedMemoryCarveout, 100) != cudaSuccess)
