@@ -1,15 +1,17 @@
 #!/usr/bin/env python
 """Decode-step benchmark of libscout on the Qwen3-14B-shaped layer.
 
-One step = the whole GPU hot path of one layer's decode step:
-  build_digest (append: the tail block of every (sequence, KV head)),
-  predict_q (Q_pred = X W_Q^T, 40 x 5120 x 5120),
-  score_topk (digest scores with Q_pred, top-64 of 1024 blocks, residency split),
-  sparse_attn (true query over the resident selected blocks),
-  merge (with the CPU partial).
+One step = the whole GPU hot path of one layer's decode step, issued as two
+streams on disjoint SMs (layer-ahead prediction, ScoutAttention Algorithm 1):
+  selection stream: predict_q (Q_pred = X W_Q^T, 40 x 5120 x 5120), then
+    score_topk (digest scores with Q_pred, top-64 of 1024 blocks, residency split);
+  attention stream: build_digest (append: the tail block of every (sequence, KV
+    head)), then sparse_attn_merge (true query over the resident blocks the
+    previous step selected, merged with the CPU partial).
 Metric: decode-attention query-heads per second (B * Hq per step, summed over ranks).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--config qwen3_14b] [--impl scout|reference]
+                  [--serial] [--split SEL,ATTN]
 
 --impl reference times the fp64 oracle (the plain CPU implementation) on this
 machine's host cores on a bounded sample of the same workload.
@@ -42,6 +44,8 @@ def parse_args():
     ap.add_argument("--impl", default="scout", choices=["scout", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing leg")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="target oracle time for cpu_baseline")
+    ap.add_argument("--serial", action="store_true", help="one stream, full grids (no overlap)")
+    ap.add_argument("--split", default=None, help="CTAs of the selection,attention kernels (default 110,42)")
     a = ap.parse_args()
     a.warmup = max(a.warmup, 3)
     return a
@@ -115,7 +119,7 @@ class ClockSampler:
 # ---------------------------------------------------------------------------
 # libscout arm
 # ---------------------------------------------------------------------------
-from block_sparse_kv_pred_gb300.step import KERNELS, algorithmic_bytes, setup_step  # noqa: E402
+from block_sparse_kv_pred_gb300.step import KERNELS, SPLIT, algorithmic_bytes, setup_step  # noqa: E402
 
 
 def run_scout(args, rank, world, local):
@@ -127,76 +131,90 @@ def run_scout(args, rank, world, local):
     device = torch.device("cuda", local)
     torch.cuda.set_device(device)
     shape = W.CONFIGS[args.config]()
-    wl, t, calls = setup_step(shape, device)
+    split = tuple(int(x) for x in args.split.split(",")) if args.split else SPLIT
+    wl, t, step = setup_step(shape, device, serial=args.serial, split=split)
     s = shape
 
     def barrier():
         if world > 1:
             dist.barrier()
 
+    cur = torch.cuda.current_stream()
+    ev0 = torch.cuda.Event()
+    ev0.record(cur)
+    step.begin(ev0)
     for i in range(args.warmup):
-        for c in calls:
-            c()
+        step.issue()
+    step.end(None)
     torch.cuda.synchronize()
     if int(t["status"].item()) != 0:
         raise RuntimeError(f"device status {int(t['status'].item())} after warm-up")
 
     sampler = ClockSampler(local)
     sampler.start()
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(calls) + 1)] for _ in range(args.steps)]
+    T = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
+    ev = [{name: (T(), T()) for name in KERNELS} for _ in range(args.steps)]
+    e_start, e_end = T(), T()
     barrier()
     torch.cuda.synchronize()
     wall0 = time.perf_counter()
+    e_start.record(cur)
+    step.begin(e_start)
     for i in range(args.steps):
-        e = ev[i]
-        e[0].record()
-        for j, c in enumerate(calls):
-            c()
-            e[j + 1].record()
+        step.issue(timing=ev[i])
+    step.end(e_end)
     torch.cuda.synchronize()
     barrier()
     wall = time.perf_counter() - wall0
     clocks = sampler.stop()
+    if int(t["status"].item()) != 0:
+        raise RuntimeError(f"device status {int(t['status'].item())} in the timed steps")
 
-    step_ms = [e[0].elapsed_time(e[-1]) for e in ev]
-    kern_ms = {name: statistics.mean(e[j].elapsed_time(e[j + 1]) for e in ev) for j, name in enumerate(KERNELS)}
-    ms = statistics.mean(step_ms)
+    ms = e_start.elapsed_time(e_end) / args.steps
+    kern_ms = {name: statistics.mean(e[name][0].elapsed_time(e[name][1]) for e in ev) for name in KERNELS}
     if world > 1:
         m = torch.tensor([ms], device=device)
         dist.all_reduce(m, op=dist.ReduceOp.MAX)
         ms = float(m.item())
     value = world * s.B * s.Hq / (ms / 1e3)
 
-    e2e = run_e2e(args, t, calls, s, world, device)
+    e2e = run_e2e(args, t, step, s, world, device)
     return s, wl, t, dict(ms=ms, value=value, kern_ms=kern_ms, clocks=clocks, wall=wall, e2e=e2e,
-                          launches=len(calls) * args.steps)
+                          launches=step.launches_per_step * args.steps, split=None if args.serial else split)
 
 
-def run_e2e(args, t, calls, s, world, device):
-    """Same metric with the step's inputs copied from pinned host memory and its results read back."""
+def run_e2e(args, t, step, s, world, device):
+    """Same metric through the public calls with the step's inputs copied from pinned host memory
+    and its results (output, LSE, the CPU work list) read back, one step at a time."""
     import torch
     import torch.distributed as dist
 
     h_in = {n: torch.empty_like(t[n], device="cpu").pin_memory() for n in ("X", "q", "O_cpu", "lse_cpu")}
-    h_out = {n: torch.empty_like(t[n], device="cpu").pin_memory() for n in ("O", "lse", "cpu", "cpu_count")}
     for n in h_in:
         h_in[n].copy_(t[n])
+    outs = ("O", "lse", "cpu", "cpu_count")
+    h_out = {n: torch.empty_like(t[n if n in t else n + "0"], device="cpu").pin_memory() for n in outs}
     h2d = sum(v.numel() * v.element_size() for v in h_in.values())
     d2h = sum(v.numel() * v.element_size() for v in h_out.values())
     steps = max(3, args.steps // 4)
+    cur = torch.cuda.current_stream()
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
     for i in range(steps):
-        ev[i][0].record()
+        ev[i][0].record(cur)
         for n, h in h_in.items():
             t[n].copy_(h, non_blocking=True)
-        for c in calls:
-            c()
+        inputs_in = torch.cuda.Event()
+        inputs_in.record(cur)
+        par = step.i % 2
+        step.begin(inputs_in)
+        step.issue()
+        step.end(None)
         for n, h in h_out.items():
-            h.copy_(t[n], non_blocking=True)
-        ev[i][1].record()
+            h.copy_(t[n] if n in t else t[f"{n}{par}"], non_blocking=True)
+        ev[i][1].record(cur)
     torch.cuda.synchronize()
     ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
     if world > 1:
@@ -291,7 +309,7 @@ def run_reference(args, rank, world):
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "query-heads/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": el / args.steps * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": DATA,
-            "config": config_of(shape, world),
+            "config": config_of(shape, world, SPLIT),
             "cpu_baseline": {"value": value, "unit": "query-heads/s", "cores": 1, "kind": "oracle",
                              "sample": f"each step is one of {len(smp.units)} sampled (sequence, KV head) units "
                                        f"of {shape.name}; single thread"},
@@ -305,12 +323,14 @@ METRIC = "sparse-decode query-heads/s and achieved HBM GB/s vs ~8 TB/s (1xGB300)
 DATA = "synthetic: seeded Qwen3-14B-shaped K/V/q/X/W_Q (stand-in for LongBench prompts and trained weights)"
 
 
-def config_of(s, world):
+def config_of(s, world, split=None):
     return {"workload": s.name, "batch": s.B, "q_heads": s.Hq, "kv_heads": s.Hkv, "head_dim": s.D,
             "context": s.T, "page": s.P, "budget_tokens": s.k * s.P, "resident_frac": s.resident_frac,
             "digest": s.kind, "gemm_mnk": [s.B, s.Hq * s.D, s.hidden],
             "l2": "not flushed: one step reads inputs larger than L2 (see step_input_bytes), in an order "
                   "that evicts each input before its next use",
+            "streams": f"selection on {split[0]} CTAs || attention on {split[1]} CTAs" if split
+            else "one stream",
             "parallelism": f"independent replicas x{world} (one batch of sequences per GPU)"}
 
 
@@ -363,29 +383,27 @@ def main():
         ms = r["kern_ms"][name]
         gbs = nbytes[name] / (ms / 1e3) / 1e9
         kernels[name] = {"ms": ms, "bytes": nbytes[name], "GB_s": gbs, "frac_of_hbm_peak": gbs / peak}
-    dom = "score_topk"
+    dom = max(KERNELS, key=lambda k: r["kern_ms"][k])  # the longest launch of the step
     ach = kernels[dom]["GB_s"]
+    src = f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured" else "fallback 6.8 TB/s"
     roof = {"kernel": dom, "bound": "hbm", "achieved": ach, "peak": peak, "unit": "GB/s", "frac": ach / peak,
-            "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
-            else "fallback 6.8 TB/s", "traffic": traffic_of(dom),
-            "algorithmic_bytes_per_launch": nbytes[dom]}
-    t_attn = r["kern_ms"]["score_topk"] + r["kern_ms"]["sparse_attn"] + r["kern_ms"]["merge"]
-    bytes_attn = nbytes["score_topk"] + nbytes["sparse_attn"] + nbytes["merge"]
+            "peak_source": src, "traffic": traffic_of(dom), "algorithmic_bytes_per_launch": nbytes[dom],
+            "note": "launch duration measured while the other stream's kernels share the GPU"
+            if r["split"] else "serial step"}
+    step_bytes = sum(nbytes[k] for k in KERNELS)
+    step_gbs = step_bytes / (r["ms"] / 1e3) / 1e9
     line = {
         "metric": METRIC, "value": r["value"], "unit": "query-heads/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": r["ms"], "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "bf16", "data": DATA, "config": config_of(s, world),
+        "vs_baseline": None, "dtype": "bf16", "data": DATA, "config": config_of(s, world, r["split"]),
         "roofline": roof,
+        "step_roofline": {"bound": "hbm", "achieved": step_gbs, "peak": peak, "unit": "GB/s",
+                          "frac": step_gbs / peak, "algorithmic_bytes_per_step": step_bytes,
+                          "note": "all four kernels' algorithmic bytes / device time of a step"},
         "e2e": {k: v for k, v in r["e2e"].items() if k in ("value", "unit", "h2d_bytes_per_step",
                                                           "d2h_bytes_per_step", "ms_per_step")},
         "gpu_launches": r["launches"], "clocks": r["clocks"], "kernels": kernels,
-        "attention_path": {"value": s.B * s.Hq / (t_attn / 1e3), "unit": "query-heads/s",
-                           "ms": t_attn, "GB_s": bytes_attn / (t_attn / 1e3) / 1e9,
-                           "frac_of_hbm_peak": bytes_attn / (t_attn / 1e3) / 1e9 / peak,
-                           "note": "score_topk + sparse_attn + merge only"},
-        "kv_tokens_per_s": nbytes["_res_blocks"] * s.P / (r["kern_ms"]["sparse_attn"] / 1e3),
-        "step_GB_s": sum(nbytes[k] for k in KERNELS) / (r["ms"] / 1e3) / 1e9,
-        "step_input_bytes": sum(nbytes[k] for k in KERNELS),
+        "kv_tokens_per_s": nbytes["_res_blocks"] * s.P / (r["kern_ms"]["sparse_attn_merge"] / 1e3),
         "wall_s_timed": r["wall"],
     }
     if world == 1 and not args.no_cpu_baseline:

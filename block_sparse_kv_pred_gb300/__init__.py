@@ -43,21 +43,36 @@ class RecallOp(ctypes.Structure):
 _SIGS = {
     "scout_status_string": ([_i], ctypes.c_char_p),
     "scout_version": ([], _i),
-    "scout_predict_q": ([_p, _p, _p, _i, _i, _i, _p, _p], _i),
+    "scout_predict_q": ([_p, _p, _p, _i, _i, _i, _p, _p, _p], _i),
     "scout_build_digest": ([_i, _p, _i64, _p, _p, _i, _i, _i, _i, _i, _p, _i, _p, _p, _p], _i),
     "scout_score_topk_workspace_bytes": ([_i, _i, _i], _sz),
     "scout_score_topk": ([_i, _p, _p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _i, _p, _p, _p, _p, _p, _p, _p, _p,
-                          _p, _p, _sz, _p], _i),
+                          _p, _p, _sz, _p, _p], _i),
     "scout_score_topk_noalloc_max_bytes": ([], _sz),
     "scout_score_topk_noalloc": ([_i, _p, _p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _i, _p, _p, _p, _p, _p, _p, _p,
                                   _p, _p, _p], _i),
     "scout_sparse_attn_workspace_bytes": ([_i, _i, _i, _i, _i], _sz),
     "scout_sparse_attn": ([_p, _p, _p, _i64, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _i, _f, _p, _p, _p, _sz, _p,
-                           _p], _i),
+                           _p, _p], _i),
+    "scout_sparse_attn_merge": ([_p, _p, _p, _i64, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _i, _f, _p, _p, _p, _p,
+                                 _p, _sz, _p, _p, _p], _i),
     "scout_merge": ([_p, _p, _p, _p, _i, _i, _p, _p, _p], _i),
     "scout_recall_async": ([_p, _i, _p, _p, _p, _p, _i64, _i, _i, _i, _i, _i, _p, _p, _p], _i),
     "scout_commit_residency": ([_p, _i, _p, _p, _i64, _i, _i, _i, _p, _p], _i),
 }
+
+
+class Launch(ctypes.Structure):
+    """scout_launch: launch options of the persistent kernels (max_ctas 0 = one CTA per SM)."""
+    _fields_ = [("max_ctas", ctypes.c_int)]
+
+
+def _launch(max_ctas):
+    if max_ctas is None:
+        return None
+    if max_ctas < 0:
+        raise ScoutError("max_ctas must be >= 0")
+    return ctypes.pointer(Launch(int(max_ctas)))
 
 
 def lib_path() -> str:
@@ -105,7 +120,7 @@ def _opt(t, dtype, name):
 
 
 # ---------------------------------------------------------------------------
-def predict_q(X: torch.Tensor, W: torch.Tensor, Q: torch.Tensor | None = None, status=None,
+def predict_q(X: torch.Tensor, W: torch.Tensor, Q: torch.Tensor | None = None, status=None, max_ctas=None,
               stream=None) -> torch.Tensor:
     """Q_pred = X W^T (bf16 in, fp32 accumulate, bf16 out)."""
     M, K = X.shape
@@ -114,7 +129,7 @@ def predict_q(X: torch.Tensor, W: torch.Tensor, Q: torch.Tensor | None = None, s
         Q = torch.empty((M, N), dtype=torch.bfloat16, device=X.device)
     _check(lib().scout_predict_q(_dev(X, torch.bfloat16, "X"), _dev(W, torch.bfloat16, "W"),
                                  _dev(Q, torch.bfloat16, "Q"), M, N, K, _opt(status, torch.int32, "status"),
-                                 _stream(stream)), "scout_predict_q")
+                                 _launch(max_ctas), _stream(stream)), "scout_predict_q")
     return Q
 
 
@@ -139,7 +154,7 @@ def score_topk_workspace(B, Hkv, nblk_cap, device="cuda") -> torch.Tensor:
 
 
 def score_topk(kind, q, digest, seq_len, resident_bits, B, Hq, Hkv, P, nblk_cap, k, workspace, out=None,
-               prev_cpu=None, scores=None, stream=None) -> dict:
+               prev_cpu=None, scores=None, max_ctas=None, stream=None) -> dict:
     """Score digests, select top-k per unit, split by residency.
 
     ``out`` (optional) is a dict of preallocated outputs with the keys returned.
@@ -164,7 +179,8 @@ def score_topk(kind, q, digest, seq_len, resident_bits, B, Hq, Hkv, P, nblk_cap,
         _dev(out["res"], torch.int32, "res"), _dev(out["res_count"], torch.int32, "res_count"),
         _dev(out["cpu"], torch.int32, "cpu"), _dev(out["cpu_count"], torch.int32, "cpu_count"),
         _dev(out["delta"], torch.int32, "delta"), _dev(out["delta_count"], torch.int32, "delta_count"),
-        _dev(workspace, torch.uint8, "workspace"), workspace.numel(), _stream(stream)), "scout_score_topk")
+        _dev(workspace, torch.uint8, "workspace"), workspace.numel(), _launch(max_ctas), _stream(stream)),
+        "scout_score_topk")
     if scores is not None:
         out["scores"] = scores
     del U
@@ -177,7 +193,7 @@ def sparse_attn_workspace(B, Hq, Hkv, P, D=128, device="cuda") -> torch.Tensor:
 
 
 def sparse_attn(q, K_pool, V_pool, page_table, seq_len, res_list, res_count, B, Hq, Hkv, P, k, scale, workspace,
-                O=None, lse=None, status=None, stream=None):
+                O=None, lse=None, status=None, max_ctas=None, stream=None):
     """GPU partial attention over the resident selected blocks -> (O fp32 [B][Hq][D], lse fp32 [B][Hq])."""
     D = q.shape[-1]
     if O is None:
@@ -190,8 +206,28 @@ def sparse_attn(q, K_pool, V_pool, page_table, seq_len, res_list, res_count, B, 
         _dev(res_list, torch.int32, "res_list"), _dev(res_count, torch.int32, "res_count"), B, Hq, Hkv, D, P,
         page_table.shape[-1], k, float(scale), _dev(O, torch.float32, "O"), _dev(lse, torch.float32, "lse"),
         _dev(workspace, torch.uint8, "workspace"), workspace.numel(), _opt(status, torch.int32, "status"),
-        _stream(stream)), "scout_sparse_attn")
+        _launch(max_ctas), _stream(stream)), "scout_sparse_attn")
     return O, lse
+
+
+def sparse_attn_merge(q, K_pool, V_pool, page_table, seq_len, res_list, res_count, B, Hq, Hkv, P, k, scale,
+                      workspace, O_cpu, lse_cpu, O_out=None, lse_out=None, status=None, max_ctas=None,
+                      stream=None):
+    """GPU partial attention merged with the CPU partial -> (O bf16 [B][Hq][D], lse fp32 [B][Hq])."""
+    D = q.shape[-1]
+    if O_out is None:
+        O_out = torch.empty((B, Hq, D), dtype=torch.bfloat16, device=q.device)
+    if lse_out is None:
+        lse_out = torch.empty((B, Hq), dtype=torch.float32, device=q.device)
+    _check(lib().scout_sparse_attn_merge(
+        _dev(q, torch.bfloat16, "q"), _dev(K_pool, torch.bfloat16, "K_pool"), _dev(V_pool, torch.bfloat16, "V_pool"),
+        K_pool.shape[0], _dev(page_table, torch.int32, "page_table"), _dev(seq_len, torch.int32, "seq_len"),
+        _dev(res_list, torch.int32, "res_list"), _dev(res_count, torch.int32, "res_count"), B, Hq, Hkv, D, P,
+        page_table.shape[-1], k, float(scale), _dev(O_cpu, torch.float32, "O_cpu"),
+        _dev(lse_cpu, torch.float32, "lse_cpu"), _dev(O_out, torch.bfloat16, "O_out"),
+        _dev(lse_out, torch.float32, "lse_out"), _dev(workspace, torch.uint8, "workspace"), workspace.numel(),
+        _opt(status, torch.int32, "status"), _launch(max_ctas), _stream(stream)), "scout_sparse_attn_merge")
+    return O_out, lse_out
 
 
 def merge(O_a, lse_a, O_b, lse_b, O_out=None, lse_out=None, stream=None):

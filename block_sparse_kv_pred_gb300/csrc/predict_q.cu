@@ -223,9 +223,10 @@ bool make_map(CUtensorMap* map, const void* ptr, int rows, int cols, int box_row
 }  // namespace scout
 
 extern "C" int scout_predict_q(const void* X, const void* W, void* Q, int M, int N, int K, int32_t* dev_status,
-                               cudaStream_t stream) {
+                               const scout_launch* launch, cudaStream_t stream) {
   using namespace scout;
   if (X == nullptr || W == nullptr || Q == nullptr || M <= 0 || N <= 0 || K <= 0) return SCOUT_ERR_INVALID_ARG;
+  if (launch != nullptr && launch->max_ctas < 0) return SCOUT_ERR_INVALID_ARG;
   if (M > kMaxN || N % kBM != 0 || K % kBK != 0 || !aligned16(X) || !aligned16(W) || !aligned16(Q))
     return SCOUT_ERR_UNSUPPORTED;
   GemmArgs a;
@@ -241,7 +242,8 @@ extern "C" int scout_predict_q(const void* X, const void* W, void* Q, int M, int
   a.stages = min(kStages, (200 * 1024) / stage_bytes);
   a.status = dev_status;
   const int tiles = N / kBM;
-  const int S = max(1, min(min(8, a.kblocks), sm_count() / tiles));
+  const int cap = launch != nullptr && launch->max_ctas > 0 ? launch->max_ctas : sm_count();
+  const int S = max(1, min(min(8, a.kblocks), cap / tiles));  // split-K so tiles x S fits the CTA budget
   const size_t smem = 1024 + (size_t)max(a.stages * stage_bytes, a.n_pad * kBM * 4);
   CUtensorMap tmW, tmX;
   if (!make_map(&tmW, W, N, K, kBM) || !make_map(&tmX, X, M, K, a.n_pad)) return SCOUT_ERR_UNSUPPORTED;

@@ -595,13 +595,15 @@ extern "C" int scout_score_topk(int kind, const void* q, const void* digest, con
                                 const int32_t* prev_cpu_count, int B, int Hq, int Hkv, int D, int P, int nblk_cap,
                                 int k, float* scores, int32_t* topk_idx, int32_t* topk_count, int32_t* res_list,
                                 int32_t* res_count, int32_t* cpu_list, int32_t* cpu_count, int32_t* delta_list,
-                                int32_t* delta_count, void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+                                int32_t* delta_count, void* workspace, size_t workspace_bytes,
+                                const scout_launch* launch, cudaStream_t stream) {
   using namespace scout;
   if (q == nullptr || digest == nullptr || seq_len == nullptr || resident_bits == nullptr || topk_idx == nullptr ||
       topk_count == nullptr || res_list == nullptr || res_count == nullptr || cpu_list == nullptr ||
       cpu_count == nullptr || delta_list == nullptr || delta_count == nullptr)
     return SCOUT_ERR_INVALID_ARG;
   if ((prev_cpu_list == nullptr) != (prev_cpu_count == nullptr)) return SCOUT_ERR_INVALID_ARG;
+  if (launch != nullptr && launch->max_ctas < 0) return SCOUT_ERR_INVALID_ARG;
   if (kind != SCOUT_DIGEST_MINMAX && kind != SCOUT_DIGEST_MEAN) return SCOUT_ERR_INVALID_ARG;
   if (B <= 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || nblk_cap <= 0 || k <= 0) return SCOUT_ERR_INVALID_ARG;
   const int G = Hq / Hkv;
@@ -661,7 +663,8 @@ extern "C" int scout_score_topk(int kind, const void* q, const void* digest, con
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess ||
       cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, 100) != cudaSuccess)
     return SCOUT_ERR_CUDA;
-  const int grid = (int)(a.n_items < (int64_t)sm_count() ? a.n_items : (int64_t)sm_count());  // <= one CTA per item
+  const int cap = launch != nullptr && launch->max_ctas > 0 ? launch->max_ctas : sm_count();
+  const int grid = (int)(a.n_items < (int64_t)cap ? a.n_items : (int64_t)cap);  // <= one CTA per item
   kern<<<grid, kThreadsAll, smem, stream>>>(tmD, a);
   return launch_status();
 }
@@ -725,5 +728,5 @@ extern "C" int scout_score_topk_noalloc(int kind, const void* q, const void* dig
   if (cudaMemsetAsync(scratch, 0, counters_bytes((int64_t)B * Hkv), stream) != cudaSuccess) return SCOUT_ERR_CUDA;
   return scout_score_topk(kind, q, digest, seq_len, resident_bits, prev_cpu_list, prev_cpu_count, B, Hq, Hkv, D, P,
                           nblk_cap, k, scores, topk_idx, topk_count, res_list, res_count, cpu_list, cpu_count,
-                          delta_list, delta_count, scratch, kNoAllocScratchBytes, stream);
+                          delta_list, delta_count, scratch, kNoAllocScratchBytes, nullptr, stream);
 }

@@ -55,6 +55,11 @@ struct AttnArgs {
   int nslots;  // combine slots that fit in shared memory (1 or 2)
   float* O_part;
   float* lse_part;
+  // merge mode (O_out != nullptr): the CPU partial is merged in and bf16 O written
+  const float* O_cpu;
+  const float* lse_cpu;
+  __nv_bfloat16* O_out;
+  float* lse_out;
   int32_t* counters;   // [units]
   float* slot_lse;     // [kMaxGrid][2][kMaxG]
   float* slot_O;       // [kMaxGrid][2][kMaxG][kD]
@@ -255,6 +260,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const __grid_c
   __shared__ int wtot[kThreads / 32];
   __shared__ int meta[C::kStages];  // valid tokens of the block in each stage (0: skipped)
   __shared__ float ew[kMaxG][kConsumerWarps], ehm[kMaxG], ehl[kMaxG], eown[kMaxG];  // epilogue weights
+  __shared__ float efin[kMaxG], fwg[kMaxG], fwc[kMaxG];  // final LSE, merge weights
 
   // dynamic shared memory: [ring (1024-aligned)][combine slots][unit prefix]
   const uint32_t raw = smem_u32(smem_raw);
@@ -393,11 +399,55 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const __grid_c
 
   if (warp == kEpilogueWarp) {
     // ---------------- epilogue warp ------------------------------------------
+    const bool merge = a.O_out != nullptr;
+    // final per-head LSE of unit uu is in efin[]: write it, or merge it with the CPU partial
+    auto set_final = [&](int uu) {
+      if (lane < a.G) {
+        const int64_t r = (int64_t)uu * a.G + lane;
+        const float lg = efin[lane];
+        if (merge) {
+          const float lc = a.lse_cpu[r], m = fmaxf(lg, lc);
+          float wg = 0.f, wc = 0.f, lse = -INFINITY;
+          if (m != -INFINITY) {
+            wg = expf(lg - m);
+            wc = expf(lc - m);
+            const float sum = wg + wc;
+            lse = m + logf(sum);
+            wg /= sum;
+            wc /= sum;
+          }
+          fwg[lane] = wg;
+          fwc[lane] = wc;
+          if (a.lse_out != nullptr) a.lse_out[r] = lse;
+        } else {
+          a.lse_part[r] = lg;
+        }
+      }
+      __syncwarp();
+    };
+    // four dims of head h of unit uu: the GPU partial, or its merge with the CPU partial
+    auto store4 = [&](int uu, int h, int d, float4 o) {
+      const int64_t off = ((int64_t)uu * a.G + h) * kD + d;
+      if (merge) {
+        const float4 cp = *reinterpret_cast<const float4*>(a.O_cpu + off);
+        const float wg = fwg[h], wc = fwc[h];
+        uint2 pk;
+        pk.x = pack_bf16(wg * o.x + wc * cp.x, wg * o.y + wc * cp.y);
+        pk.y = pack_bf16(wg * o.z + wc * cp.z, wg * o.w + wc * cp.w);
+        *reinterpret_cast<uint2*>(a.O_out + off) = pk;
+      } else {
+        *reinterpret_cast<float4*>(a.O_part + off) = o;
+      }
+    };
     // units with no resident selected block: O = 0, lse = -inf
     for (int u = c; u < a.units; u += gridDim.x) {
       if (prefix[u + 1] != prefix[u]) continue;
-      for (int idx = lane; idx < a.G * kD; idx += 32) a.O_part[(int64_t)u * a.G * kD + idx] = 0.f;
-      if (lane < a.G) a.lse_part[(int64_t)u * a.G + lane] = -INFINITY;
+      if (lane < a.G) efin[lane] = -INFINITY;
+      __syncwarp();
+      set_final(u);
+      for (int i4 = lane; i4 < a.G * (kD / 4); i4 += 32)
+        store4(u, i4 / (kD / 4), (i4 % (kD / 4)) * 4, make_float4(0.f, 0.f, 0.f, 0.f));
+      __syncwarp();
     }
     if (c >= Gp) return;
     const int64_t start = range_start(c, N, Gp), end = range_start(c + 1, N, Gp);
@@ -441,10 +491,12 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const __grid_c
         return acc;
       };
       if (whole) {
-        if (lane < a.G) a.lse_part[(int64_t)u * a.G + lane] = eown[lane];
+        if (lane < a.G) efin[lane] = eown[lane];
+        __syncwarp();
+        set_final(u);
         for (int i4 = lane; i4 < a.G * (kD / 4); i4 += 32) {
           const int h = i4 / (kD / 4), d = (i4 % (kD / 4)) * 4;
-          reinterpret_cast<float4*>(a.O_part + ((int64_t)u * a.G + h) * kD + d)[0] = own4(h, d);
+          store4(u, h, d, own4(h, d));
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&cempty[slot]);  // the combine slot may be refilled
@@ -473,9 +525,10 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const __grid_c
           }
           ehm[lane] = M;
           ehl[lane] = L;
-          a.lse_part[(int64_t)u * a.G + lane] = L > 0.f ? M + logf(L) : -INFINITY;
+          efin[lane] = L > 0.f ? M + logf(L) : -INFINITY;
         }
         __syncwarp();
+        set_final(u);
         for (int i4 = lane; i4 < a.G * (kD / 4); i4 += 32) {
           const int h = i4 / (kD / 4), d = (i4 % (kD / 4)) * 4;
           const float M = ehm[h], L = ehl[h];
@@ -500,7 +553,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const __grid_c
               acc.w += f * o.w;
             }
           }
-          reinterpret_cast<float4*>(a.O_part + ((int64_t)u * a.G + h) * kD + d)[0] = acc;
+          store4(u, h, d, acc);
         }
         __syncwarp();
         if (lane == 0) {
@@ -534,9 +587,10 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const __grid_c
             for (int cc = c0; cc <= c1; ++cc) L += expf(__ldcg(a.slot_lse + piece_slot(cc) * kMaxG + lane) - M);
           ehm[lane] = M;
           ehl[lane] = L;
-          a.lse_part[(int64_t)u * a.G + lane] = L > 0.f ? M + logf(L) : -INFINITY;
+          efin[lane] = L > 0.f ? M + logf(L) : -INFINITY;
         }
         __syncwarp();
+        set_final(u);
         for (int i4 = lane; i4 < a.G * (kD / 4); i4 += 32) {
           const int h = i4 / (kD / 4), d = (i4 % (kD / 4)) * 4;
           const float M = ehm[h], L = ehl[h];
@@ -551,8 +605,9 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const __grid_c
               acc.z += f * o.z;
               acc.w += f * o.w;
             }
-          reinterpret_cast<float4*>(a.O_part + ((int64_t)u * a.G + h) * kD + d)[0] = acc;
+          store4(u, h, d, acc);
         }
+        __syncwarp();
         if (lane == 0) a.counters[u] = 0;  // ready for the next call
       }
     }
@@ -663,7 +718,7 @@ bool make_page_map(CUtensorMap* map, const void* pool, int64_t n_slots, int P, i
 }
 
 template <int P>
-int launch_attn(const void* K_pool, const void* V_pool, AttnArgs a, cudaStream_t stream) {
+int launch_attn(const void* K_pool, const void* V_pool, AttnArgs a, int max_ctas, cudaStream_t stream) {
   a.nslots = dyn_smem<P>(a.units, a.G, 2) <= kSmemLimit ? 2 : 1;
   CUtensorMap tmK, tmV;
   if (!make_page_map(&tmK, K_pool, a.n_slots, P, Cfg<P>::PS) || !make_page_map(&tmV, V_pool, a.n_slots, P, Cfg<P>::PS))
@@ -677,39 +732,35 @@ int launch_attn(const void* K_pool, const void* V_pool, AttnArgs a, cudaStream_t
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, sparse_attn_kernel<P>, kThreads, smem) != cudaSuccess ||
       occ < 1)
     return SCOUT_ERR_CUDA;
-  const int grid = min(kMaxGrid, sm_count() * occ);
+  const int grid = min(kMaxGrid, max_ctas > 0 ? max_ctas : sm_count() * occ);
   sparse_attn_kernel<P><<<grid, kThreads, smem, stream>>>(tmK, tmV, a);
   return launch_status();
 }
 
-}  // namespace
-}  // namespace scout
-
-extern "C" size_t scout_sparse_attn_workspace_bytes(int B, int Hq, int Hkv, int D, int P) {
-  (void)Hq;
-  (void)D;
-  (void)P;
-  if (B <= 0 || Hkv <= 0) return 0;
-  return scout::counters_bytes((int64_t)B * Hkv) + scout::kSlotLseBytes + scout::kSlotOBytes;
-}
-
-extern "C" int scout_sparse_attn(const void* q, const void* K_pool, const void* V_pool, int64_t n_slots,
-                                 const int32_t* page_table, const int32_t* seq_len, const int32_t* res_list,
-                                 const int32_t* res_count, int B, int Hq, int Hkv, int D, int P, int nblk_cap, int k,
-                                 float scale, float* O_part, float* lse_part, void* workspace, size_t workspace_bytes,
-                                 int32_t* dev_status, cudaStream_t stream) {
-  using namespace scout;
+// Shared by both entry points: O_part/lse_part for the partial, or (O_cpu, lse_cpu,
+// O_out, lse_out) for the merged output.
+int attn_entry(const void* q, const void* K_pool, const void* V_pool, int64_t n_slots, const int32_t* page_table,
+               const int32_t* seq_len, const int32_t* res_list, const int32_t* res_count, int B, int Hq, int Hkv,
+               int D, int P, int nblk_cap, int k, float scale, float* O_part, float* lse_part, const float* O_cpu,
+               const float* lse_cpu, __nv_bfloat16* O_out, float* lse_out, void* workspace,
+               size_t workspace_bytes, int32_t* dev_status, const scout_launch* launch, cudaStream_t stream) {
+  const bool merge = O_out != nullptr;
   if (q == nullptr || K_pool == nullptr || V_pool == nullptr || page_table == nullptr || seq_len == nullptr ||
-      res_list == nullptr || res_count == nullptr || O_part == nullptr || lse_part == nullptr)
+      res_list == nullptr || res_count == nullptr)
+    return SCOUT_ERR_INVALID_ARG;
+  if (merge ? (O_cpu == nullptr || lse_cpu == nullptr) : (O_part == nullptr || lse_part == nullptr))
     return SCOUT_ERR_INVALID_ARG;
   if (B <= 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || n_slots <= 0 || nblk_cap <= 0 || k <= 0 ||
       !(scale > 0.f))
     return SCOUT_ERR_INVALID_ARG;
+  if (launch != nullptr && launch->max_ctas < 0) return SCOUT_ERR_INVALID_ARG;
   const int64_t units = (int64_t)B * Hkv;
   const int G = Hq / Hkv;
   if (D != kD || !valid_P(P) || G > kMaxG || units > kMaxUnits || !aligned16(K_pool) || !aligned16(V_pool) ||
       (reinterpret_cast<uintptr_t>(q) & 3u) || n_slots * P > (int64_t)0x7fffffff)
     return SCOUT_ERR_UNSUPPORTED;
+  if (merge && (!aligned16(O_cpu) || (reinterpret_cast<uintptr_t>(O_out) & 7u))) return SCOUT_ERR_UNSUPPORTED;
+  if (!merge && !aligned16(O_part)) return SCOUT_ERR_UNSUPPORTED;
   if (workspace == nullptr || workspace_bytes < scout_sparse_attn_workspace_bytes(B, Hq, Hkv, D, P))
     return SCOUT_ERR_WORKSPACE;
   AttnArgs a;
@@ -728,14 +779,54 @@ extern "C" int scout_sparse_attn(const void* q, const void* K_pool, const void* 
   a.scale_log2 = scale * kLog2e;
   a.O_part = O_part;
   a.lse_part = lse_part;
+  a.O_cpu = O_cpu;
+  a.lse_cpu = lse_cpu;
+  a.O_out = O_out;
+  a.lse_out = lse_out;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   a.counters = reinterpret_cast<int32_t*>(ws);
   a.slot_lse = reinterpret_cast<float*>(ws + counters_bytes(units));
   a.slot_O = reinterpret_cast<float*>(ws + counters_bytes(units) + kSlotLseBytes);
   a.status = dev_status;
+  const int cap = launch != nullptr ? launch->max_ctas : 0;
   switch (P) {
-    case 16: return launch_attn<16>(K_pool, V_pool, a, stream);
-    case 32: return launch_attn<32>(K_pool, V_pool, a, stream);
-    default: return launch_attn<64>(K_pool, V_pool, a, stream);
+    case 16: return launch_attn<16>(K_pool, V_pool, a, cap, stream);
+    case 32: return launch_attn<32>(K_pool, V_pool, a, cap, stream);
+    default: return launch_attn<64>(K_pool, V_pool, a, cap, stream);
   }
+}
+
+}  // namespace
+}  // namespace scout
+
+extern "C" size_t scout_sparse_attn_workspace_bytes(int B, int Hq, int Hkv, int D, int P) {
+  (void)Hq;
+  (void)D;
+  (void)P;
+  if (B <= 0 || Hkv <= 0) return 0;
+  return scout::counters_bytes((int64_t)B * Hkv) + scout::kSlotLseBytes + scout::kSlotOBytes;
+}
+
+extern "C" int scout_sparse_attn(const void* q, const void* K_pool, const void* V_pool, int64_t n_slots,
+                                 const int32_t* page_table, const int32_t* seq_len, const int32_t* res_list,
+                                 const int32_t* res_count, int B, int Hq, int Hkv, int D, int P, int nblk_cap, int k,
+                                 float scale, float* O_part, float* lse_part, void* workspace, size_t workspace_bytes,
+                                 int32_t* dev_status, const scout_launch* launch, cudaStream_t stream) {
+  if (O_part == nullptr || lse_part == nullptr) return SCOUT_ERR_INVALID_ARG;
+  return scout::attn_entry(q, K_pool, V_pool, n_slots, page_table, seq_len, res_list, res_count, B, Hq, Hkv, D, P,
+                           nblk_cap, k, scale, O_part, lse_part, nullptr, nullptr, nullptr, nullptr, workspace,
+                           workspace_bytes, dev_status, launch, stream);
+}
+
+extern "C" int scout_sparse_attn_merge(const void* q, const void* K_pool, const void* V_pool, int64_t n_slots,
+                                       const int32_t* page_table, const int32_t* seq_len, const int32_t* res_list,
+                                       const int32_t* res_count, int B, int Hq, int Hkv, int D, int P, int nblk_cap,
+                                       int k, float scale, const float* O_cpu, const float* lse_cpu, void* O_out,
+                                       float* lse_out, void* workspace, size_t workspace_bytes, int32_t* dev_status,
+                                       const scout_launch* launch, cudaStream_t stream) {
+  if (O_out == nullptr) return SCOUT_ERR_INVALID_ARG;
+  return scout::attn_entry(q, K_pool, V_pool, n_slots, page_table, seq_len, res_list, res_count, B, Hq, Hkv, D, P,
+                           nblk_cap, k, scale, nullptr, nullptr, O_cpu, lse_cpu,
+                           static_cast<__nv_bfloat16*>(O_out), lse_out, workspace, workspace_bytes, dev_status,
+                           launch, stream);
 }

@@ -22,12 +22,16 @@ def main():
     ap.add_argument("--config", default="qwen3_14b")
     ap.add_argument("--pool-slots", type=int, default=65536)
     ap.add_argument("--steps", type=int, default=3)
+    ap.add_argument("--serial", action="store_true", help="one stream, full grids")
     a = ap.parse_args()
     shape = W.CONFIGS[a.config]()
-    wl, t, calls = setup_step(shape, torch.device("cuda", 0), pool_slots=a.pool_slots)
+    wl, t, step = setup_step(shape, torch.device("cuda", 0), pool_slots=a.pool_slots, serial=a.serial)
+    ev = torch.cuda.Event()
+    ev.record()
+    step.begin(ev)
     for _ in range(a.steps):
-        for c in calls:
-            c()
+        step.issue()
+    step.end(None)
     torch.cuda.synchronize()
     status = int(t["status"].item())
     print(f"profile_step {shape.name}: {a.steps} steps, pool slots {wl.n_slots}, status {status}")

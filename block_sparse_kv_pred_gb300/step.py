@@ -1,18 +1,99 @@
 """One decode step of one layer through the libscout C ABI.
 
-``setup_step`` materialises a seeded workload on the device, builds the prefill
-digests and prepares the five calls of a step (digest append, Q_pred, score and
-select, sparse attention, merge) with their arguments converted once, so that a
-step costs five foreign calls of host work.  ``algorithmic_bytes`` gives the
-bytes each kernel must move per launch, the numerator of the roofline.
+ScoutAttention (arXiv HTML), Algorithm 1 (layer-ahead prediction): while layer i
+attends with the block set chosen one layer earlier, the next layer's query is
+predicted and its top-k chosen.  The two halves touch disjoint data, so a step
+is issued as two CUDA streams on disjoint SMs (``scout_launch.max_ctas``):
+
+* selection stream: Q_pred = X W_Q^T (``scout_predict_q``), then scoring and
+  top-k over the next layer's digests (``scout_score_topk``) into list set
+  ``i % 2``;
+* attention stream: digest append for the token just written
+  (``scout_build_digest`` on this layer's tail blocks), then attention over
+  the resident blocks of list set ``(i + 1) % 2`` merged with the CPU partial
+  (``scout_sparse_attn_merge``).
+
+Step i's attention reads the lists step i-1 selected; step i's selection
+overwrites the set step i-1's attention read, so each stream waits for the
+other's previous step (two events per stream, used alternately).  The single
+layer of the synthetic workload stands for both layers: ``digest_next`` (scored)
+and ``digest_cur`` (appended to) are separate buffers, as the two layers' are.
+
+``serial=True`` issues the same four calls on one stream with full grids.
+``algorithmic_bytes`` gives the bytes each kernel must move per launch, the
+numerator of the roofline.
 """
 from __future__ import annotations
 
-KERNELS = ("build_digest", "predict_q", "score_topk", "sparse_attn", "merge")
+KERNELS = ("build_digest", "predict_q", "score_topk", "sparse_attn_merge")
+# stream of each kernel: 0 = selection (next layer), 1 = attention (this layer)
+STREAM_OF = {"build_digest": 1, "predict_q": 0, "score_topk": 0, "sparse_attn_merge": 1}
+SPLIT = (110, 42)  # CTAs of the selection and attention kernels when overlapped (152 SMs)
 
 
-def setup_step(shape, device, pool_slots=None):
-    """Device inputs, prefill digests and the five prepared C-ABI calls of one step."""
+class Step:
+    """The prepared calls, streams and events of a step; ``issue(i)`` launches step i."""
+
+    def __init__(self, t, calls, streams, serial):
+        import torch
+
+        self.t = t
+        self.calls = calls  # name -> Prepared
+        self.streams = streams
+        self.serial = serial
+        self.sel_done = [torch.cuda.Event(), torch.cuda.Event()]
+        self.attn_done = [torch.cuda.Event(), torch.cuda.Event()]
+        self.i = 0
+
+    @property
+    def launches_per_step(self) -> int:
+        return len(KERNELS)
+
+    def begin(self, event):
+        """Make both streams wait for ``event`` (recorded on the current stream)."""
+        for s in self.streams:
+            s.wait_event(event)
+
+    def end(self, event):
+        """Join both streams into the current stream and record ``event`` there."""
+        import torch
+
+        cur = torch.cuda.current_stream()
+        for s in self.streams:
+            ev = torch.cuda.Event()
+            ev.record(s)
+            cur.wait_event(ev)
+        if event is not None:
+            event.record(cur)
+
+    def issue(self, timing=None):
+        """Launch the next step.  ``timing``: optional name -> (start, end) timing events."""
+        i, par = self.i, self.i % 2
+        sA, sB = self.streams[0], self.streams[-1]
+        c = self.calls[par]
+
+        def run(name, stream):
+            if timing is not None:
+                timing[name][0].record(stream)
+            c[name]()
+            if timing is not None:
+                timing[name][1].record(stream)
+
+        run("predict_q", sA)
+        if not self.serial:
+            sA.wait_event(self.attn_done[1 - par])  # step i-1's attention has read list set i % 2
+        run("score_topk", sA)
+        self.sel_done[par].record(sA)
+        run("build_digest", sB)
+        if not self.serial:
+            sB.wait_event(self.sel_done[1 - par])  # step i-1's selection wrote list set (i+1) % 2
+        run("sparse_attn_merge", sB)
+        self.attn_done[par].record(sB)
+        self.i += 1
+
+
+def setup_step(shape, device, pool_slots=None, serial=False, split=SPLIT):
+    """Device inputs, prefill digests, both list sets and the prepared calls of a step."""
     import torch
 
     import block_sparse_kv_pred_gb300 as bs
@@ -24,55 +105,75 @@ def setup_step(shape, device, pool_slots=None):
     d = WD.materialize(wl, device=device)
     U, nb, D = s.units, s.nblk, s.D
     t = {k: v for k, v in d.items()}
-    t["digest"] = torch.empty((s.B, s.Hkv, nb, 2, D), dtype=torch.bfloat16, device=device)
-    bs.build_digest("minmax", d["K_pool"], d["page_table"], d["seq_len"], s.B, s.Hkv, s.P, t["digest"])
+    t["digest_next"] = torch.empty((s.B, s.Hkv, nb, 2, D), dtype=torch.bfloat16, device=device)
+    bs.build_digest("minmax", d["K_pool"], d["page_table"], d["seq_len"], s.B, s.Hkv, s.P, t["digest_next"])
+    t["digest_cur"] = t["digest_next"].clone()
     tail = [[u, int(wl.nvalid[u // s.Hkv]) - 1] for u in range(U)]
     t["tail"] = torch.tensor(tail, dtype=torch.int32, device=device)
     t["Qp"] = torch.empty((s.B, s.Hq * D), dtype=torch.bfloat16, device=device)
     t["ws_t"] = bs.score_topk_workspace(s.B, s.Hkv, nb, device=device)
-    for name in ("topk", "res", "cpu", "delta"):
-        t[name] = torch.full((s.B, s.Hkv, s.k), -1, dtype=torch.int32, device=device)
-        t[name + "_count"] = torch.zeros((s.B, s.Hkv), dtype=torch.int32, device=device)
+    for par in (0, 1):
+        for name in ("topk", "res", "cpu", "delta"):
+            t[f"{name}{par}"] = torch.full((s.B, s.Hkv, s.k), -1, dtype=torch.int32, device=device)
+            t[f"{name}_count{par}"] = torch.zeros((s.B, s.Hkv), dtype=torch.int32, device=device)
     t["ws_a"] = bs.sparse_attn_workspace(s.B, s.Hq, s.Hkv, s.P, device=device)
-    t["O_gpu"] = torch.empty((s.B, s.Hq, D), dtype=torch.float32, device=device)
-    t["lse_gpu"] = torch.empty((s.B, s.Hq), dtype=torch.float32, device=device)
     t["O"] = torch.empty((s.B, s.Hq, D), dtype=torch.bfloat16, device=device)
     t["lse"] = torch.empty((s.B, s.Hq), dtype=torch.float32, device=device)
     t["status"] = torch.zeros(1, dtype=torch.int32, device=device)
-    st = torch.cuda.current_stream(device).cuda_stream
+
+    if serial:
+        streams = [torch.cuda.current_stream(device)]
+        cap_sel = cap_attn = None
+    else:
+        streams = [torch.cuda.Stream(device), torch.cuda.Stream(device)]
+        cap_sel, cap_attn = split
+    t["_launch_sel"] = bs._launch(cap_sel)
+    t["_launch_attn"] = bs._launch(cap_attn)
+    sA, sB = streams[0].cuda_stream, streams[-1].cuda_stream
     p = lambda name: t[name].data_ptr()  # noqa: E731
-    calls = [
-        bs.Prepared("scout_build_digest", bs.MINMAX, p("K_pool"), wl.n_slots, p("page_table"), p("seq_len"), s.B,
-                    s.Hkv, D, s.P, nb, p("tail"), U, p("digest"), p("status"), st),
-        bs.Prepared("scout_predict_q", p("X"), p("W"), p("Qp"), s.B, s.Hq * D, s.hidden, p("status"), st),
-        # the previous step's CPU list is this step's prev list (in place), so delta = newly offloaded blocks
-        bs.Prepared("scout_score_topk", bs.MINMAX, p("Qp"), p("digest"), p("seq_len"), p("resident_bits"), p("cpu"),
-                    p("cpu_count"), s.B, s.Hq, s.Hkv, D, s.P, nb, s.k, None, p("topk"), p("topk_count"), p("res"),
-                    p("res_count"), p("cpu"), p("cpu_count"), p("delta"), p("delta_count"), p("ws_t"),
-                    t["ws_t"].numel(), st),
-        bs.Prepared("scout_sparse_attn", p("q"), p("K_pool"), p("V_pool"), wl.n_slots, p("page_table"),
-                    p("seq_len"), p("res"), p("res_count"), s.B, s.Hq, s.Hkv, D, s.P, nb, s.k, s.scale, p("O_gpu"),
-                    p("lse_gpu"), p("ws_a"), t["ws_a"].numel(), p("status"), st),
-        bs.Prepared("scout_merge", p("O_gpu"), p("lse_gpu"), p("O_cpu"), p("lse_cpu"), s.B * s.Hq, D, p("O"),
-                    p("lse"), st),
-    ]
-    return wl, t, calls
+    append = bs.Prepared("scout_build_digest", bs.MINMAX, p("K_pool"), wl.n_slots, p("page_table"), p("seq_len"),
+                         s.B, s.Hkv, D, s.P, nb, p("tail"), U, p("digest_cur"), p("status"), sB)
+    gemm = bs.Prepared("scout_predict_q", p("X"), p("W"), p("Qp"), s.B, s.Hq * D, s.hidden, p("status"),
+                       t["_launch_sel"], sA)
+    calls = []
+    for par in (0, 1):
+        new, old = str(par), str(1 - par)
+        calls.append({
+            "build_digest": append,
+            "predict_q": gemm,
+            # the previous step's CPU list is the prev list, so delta = newly offloaded blocks
+            "score_topk": bs.Prepared(
+                "scout_score_topk", bs.MINMAX, p("Qp"), p("digest_next"), p("seq_len"), p("resident_bits"),
+                p("cpu" + old), p("cpu_count" + old), s.B, s.Hq, s.Hkv, D, s.P, nb, s.k, None, p("topk" + new),
+                p("topk_count" + new), p("res" + new), p("res_count" + new), p("cpu" + new), p("cpu_count" + new),
+                p("delta" + new), p("delta_count" + new), p("ws_t"), t["ws_t"].numel(), t["_launch_sel"], sA),
+            "sparse_attn_merge": bs.Prepared(
+                "scout_sparse_attn_merge", p("q"), p("K_pool"), p("V_pool"), wl.n_slots, p("page_table"),
+                p("seq_len"), p("res" + old), p("res_count" + old), s.B, s.Hq, s.Hkv, D, s.P, nb, s.k, s.scale,
+                p("O_cpu"), p("lse_cpu"), p("O"), p("lse"), p("ws_a"), t["ws_a"].numel(), p("status"),
+                t["_launch_attn"], sB),
+        })
+    # list set 1 holds a selection before step 0 (the one the prefill step would have made)
+    calls[1]["predict_q"]()
+    calls[1]["score_topk"]()
+    torch.cuda.synchronize(device)
+    return wl, t, Step(t, calls, streams, serial)
 
 
 def algorithmic_bytes(s, wl, t):
     """Bytes each kernel must move per launch (inputs read once, outputs written once)."""
     U, D, P, k = s.units, s.D, s.P, s.k
     nvalid = int(sum(int(wl.nvalid[u // s.Hkv]) for u in range(U)))
-    res_total = int(t["res_count"].sum().item())
-    cpu_total = int(t["cpu_count"].sum().item())
+    res_total = int(t["res_count1"].sum().item())
+    cpu_total = int(t["cpu_count1"].sum().item())
     q_bytes = s.B * s.Hq * D * 2
-    part = s.B * s.Hq * (D * 4 + 4)
+    cpu_part = s.B * s.Hq * (D * 4 + 4)
+    out = s.B * s.Hq * (D * 2 + 4)
     return {
         "build_digest": U * (P * D * 2 + 2 * D * 2 + 8) + s.B * 4,
         "predict_q": s.Hq * D * s.hidden * 2 + s.B * s.hidden * 2 + s.B * s.Hq * D * 2,
         "score_topk": nvalid * 2 * D * 2 + q_bytes + U * s.words * 4 + s.B * 4 + cpu_total * 4 + U * 4
         + 4 * (U * k * 4 + U * 4),
-        "sparse_attn": res_total * (2 * P * D * 2 + 8) + q_bytes + part + U * 4 + s.B * 4,
-        "merge": 2 * part + s.B * s.Hq * (D * 2 + 4),
+        "sparse_attn_merge": res_total * (2 * P * D * 2 + 8) + q_bytes + cpu_part + out + U * 4 + s.B * 4,
         "_res_blocks": res_total,
     }

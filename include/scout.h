@@ -56,6 +56,17 @@ typedef enum scout_digest_kind {
   SCOUT_DIGEST_MEAN = 1    /* MoBA: channel-wise mean of K over a block */
 } scout_digest_kind;
 
+/* Launch options (pass NULL for the defaults).  max_ctas bounds the CTAs a
+ * persistent kernel launches (at most one per SM each): two kernels of
+ * independent work, e.g. the next layer's selection and this layer's attention
+ * (Algorithm 1), can then run at the same time on disjoint SMs from two streams.
+ * 0 means one CTA per SM; a negative value is SCOUT_ERR_INVALID_ARG.  For
+ * scout_predict_q it bounds the split-K factor S so that (N / 128) * S <= max_ctas;
+ * the grid keeps at least one CTA per 128-row tile of W. */
+typedef struct scout_launch {
+  int max_ctas;
+} scout_launch;
+
 /* Human-readable name of a status code (static string, never NULL). */
 const char* scout_status_string(int status);
 
@@ -77,7 +88,7 @@ int scout_version(void);
  * pipeline wait expires.
  * ------------------------------------------------------------------------ */
 int scout_predict_q(const void* X, const void* W, void* Q, int M, int N, int K, int32_t* dev_status,
-                    cudaStream_t stream);
+                    const scout_launch* launch, cudaStream_t stream);
 
 /* ------------------------------------------------------------------------ *
  * Block digests.
@@ -139,7 +150,8 @@ int scout_score_topk(int kind, const void* q, const void* digest, const int32_t*
                      const int32_t* prev_cpu_count, int B, int Hq, int Hkv, int D, int P, int nblk_cap,
                      int k, float* scores, int32_t* topk_idx, int32_t* topk_count, int32_t* res_list,
                      int32_t* res_count, int32_t* cpu_list, int32_t* cpu_count, int32_t* delta_list,
-                     int32_t* delta_count, void* workspace, size_t workspace_bytes, cudaStream_t stream);
+                     int32_t* delta_count, void* workspace, size_t workspace_bytes,
+                     const scout_launch* launch, cudaStream_t stream);
 
 /* ------------------------------------------------------------------------ *
  * scout_score_topk without a caller workspace (no counterpart in the paper).
@@ -187,7 +199,24 @@ int scout_sparse_attn(const void* q, const void* K_pool, const void* V_pool, int
                       const int32_t* page_table, const int32_t* seq_len, const int32_t* res_list,
                       const int32_t* res_count, int B, int Hq, int Hkv, int D, int P, int nblk_cap, int k,
                       float scale, float* O_part, float* lse_part, void* workspace, size_t workspace_bytes,
-                      int32_t* dev_status, cudaStream_t stream);
+                      int32_t* dev_status, const scout_launch* launch, cudaStream_t stream);
+
+/* ------------------------------------------------------------------------ *
+ * GPU partial attention fused with the merge of the CPU partial.
+ * ScoutAttention (arXiv HTML), section 3.2 and Algorithm 1 (A_gpu, then
+ * MERGE(A_gpu, A_cpu)): scout_sparse_attn followed by scout_merge in one launch;
+ * the GPU partial never goes through memory.
+ * Arguments as scout_sparse_attn, then O_cpu fp32 [B][Hq][D] and lse_cpu fp32
+ * [B][Hq] (the CPU partial, lse = -inf when empty), O_out bf16 [B][Hq][D] and
+ * lse_out fp32 [B][Hq] (may be NULL).  O_cpu must be 16-byte and O_out 8-byte
+ * aligned.  The merge is the formula of scout_merge, evaluated in fp32.
+ * ------------------------------------------------------------------------ */
+int scout_sparse_attn_merge(const void* q, const void* K_pool, const void* V_pool, int64_t n_slots,
+                            const int32_t* page_table, const int32_t* seq_len, const int32_t* res_list,
+                            const int32_t* res_count, int B, int Hq, int Hkv, int D, int P, int nblk_cap, int k,
+                            float scale, const float* O_cpu, const float* lse_cpu, void* O_out, float* lse_out,
+                            void* workspace, size_t workspace_bytes, int32_t* dev_status,
+                            const scout_launch* launch, cudaStream_t stream);
 
 /* ------------------------------------------------------------------------ *
  * Merge of the GPU and CPU partial results.

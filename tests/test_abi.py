@@ -50,22 +50,28 @@ def test_host_validation_rejects_without_launch(L):
     fake = ctypes.c_void_p(4096)
     assert L.scout_merge(None, None, None, None, 4, 128, None, None, None) == 1
     assert L.scout_merge(fake, fake, fake, fake, 4, 64, fake, fake, None) == 2  # D != 128
-    assert L.scout_predict_q(fake, fake, fake, 8, 100, 64, None, None) == 2  # N % 128
-    assert L.scout_predict_q(fake, fake, fake, 0, 128, 64, None, None) == 1
-    assert L.scout_predict_q(fake, fake, fake, 257, 128, 64, None, None) == 2  # M > 256
+    assert L.scout_predict_q(fake, fake, fake, 8, 100, 64, None, None, None) == 2  # N % 128
+    assert L.scout_predict_q(fake, fake, fake, 0, 128, 64, None, None, None) == 1
+    assert L.scout_predict_q(fake, fake, fake, 257, 128, 64, None, None, None) == 2  # M > 256
     assert L.scout_build_digest(0, fake, 10, fake, fake, 1, 1, 128, 48, 4, None, 0, fake, None, None) == 2  # P
     assert L.scout_build_digest(7, fake, 10, fake, fake, 1, 1, 128, 32, 4, None, 0, fake, None, None) == 1  # kind
-    args = [0, fake, fake, fake, fake, None, None, 1, 18, 2, 128, 32, 64, 8, None] + [fake] * 8 + [fake, 1 << 20, None]
+    args = [0, fake, fake, fake, fake, None, None, 1, 18, 2, 128, 32, 64, 8, None] + [fake] * 8 + [fake, 1 << 20, None, None]
     assert L.scout_score_topk(*args) == 2  # G = 9 > 8
     args[7:10] = [1, 8, 2]
-    args[-2] = 16
+    args[-3] = 16
     assert L.scout_score_topk(*args) == 3  # workspace too small
     args[5] = fake  # prev list without prev count
     assert L.scout_score_topk(*args) == 1
     assert L.scout_sparse_attn(fake, fake, fake, 100, fake, fake, fake, fake, 1, 8, 2, 128, 32, 8, 4, 0.0, fake,
-                               fake, fake, 1 << 24, None, None) == 1  # scale <= 0
+                               fake, fake, 1 << 24, None, None, None) == 1  # scale <= 0
     assert L.scout_sparse_attn(fake, ctypes.c_void_p(4097), fake, 100, fake, fake, fake, fake, 1, 8, 2, 128, 32, 8,
-                               4, 0.1, fake, fake, fake, 1 << 24, None, None) == 2  # misaligned pool
+                               4, 0.1, fake, fake, fake, 1 << 24, None, None, None) == 2  # misaligned pool
+    neg = ctypes.pointer(bs.Launch(-1))
+    assert L.scout_predict_q(fake, fake, fake, 8, 128, 64, None, neg, None) == 1  # max_ctas < 0
+    assert L.scout_sparse_attn_merge(fake, fake, fake, 100, fake, fake, fake, fake, 1, 8, 2, 128, 32, 8, 4, 0.1,
+                                     None, fake, fake, fake, fake, 1 << 24, None, None, None) == 1  # no O_cpu
+    assert L.scout_sparse_attn_merge(fake, fake, fake, 100, fake, fake, fake, fake, 1, 8, 2, 128, 32, 8, 4, 0.1,
+                                     fake, fake, fake, fake, fake, 1 << 24, None, neg, None) == 1  # max_ctas < 0
     ops = (bs.RecallOp * 1)(bs.RecallOp(0, 5, 3, -1))
     assert L.scout_recall_async(ops, 1, fake, fake, fake, fake, 2, 1, 1, 128, 32, 8, None, None, None) == 1  # slot 3 >= 2
 
