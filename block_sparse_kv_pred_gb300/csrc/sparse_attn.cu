@@ -9,22 +9,27 @@
 // finished by the last of them to arrive (self-resetting counter), which merges
 // the per-CTA partials by their LSE.
 //
-// Inside a CTA: warp 4 lane 0 streams K and V pages into a ring of shared-memory
-// stages with TMA (cp.async.bulk.tensor, 128-byte swizzle) and mbarriers; the
-// four consumer warps take blocks round-robin, run S = Q K^T and O += P V on the
-// tensor cores (mma.sync m16n8k16, bf16 in, fp32 accumulate; P is split into a
-// bf16 high and low part so the probabilities keep ~16 significant bits) and
-// keep an online softmax per warp, combined through shared memory at the end of
-// each unit segment.
+// Inside a CTA: the four consumer warps take the range's sub-pages round-robin.
+// Each warp owns kStages / 4 stages of a shared-memory ring and keeps them
+// filled itself: when it has finished a sub-page it reloads that stage with its
+// sub-page kStages / 4 further on (one 3-D TMA box per K and per V sub-page,
+// 128-byte swizzle, completion on an mbarrier), so a stage is never idle while
+// another warp is behind.  The lanes resolve the warp's next 32 sub-pages (list
+// entry, page-table slot, valid tokens) one batch ahead, so the dependent
+// global loads stay off the critical path.  Per sub-page a warp runs S = Q K^T
+// and O += P V on the tensor cores (mma.sync m16n8k16, bf16 in, fp32 accumulate;
+// P is split into a bf16 high and low part so the probabilities keep ~16
+// significant bits) and keeps an online softmax, combined through shared memory
+// at the end of each unit segment by the epilogue warp.
 #include "common.cuh"
 
 namespace scout {
 namespace {
 
 constexpr int kConsumerWarps = 4;
-constexpr int kProducerWarp = kConsumerWarps;      // streams pages with TMA
-constexpr int kEpilogueWarp = kConsumerWarps + 1;  // combines, writes, fixes up split units
-constexpr int kThreads = (kConsumerWarps + 2) * 32;
+constexpr int kEpilogueWarp = kConsumerWarps;  // combines, writes, fixes up split units
+constexpr int kThreads = (kConsumerWarps + 1) * 32;
+constexpr int kPhaseB = 8;  // page of a batch at which the next batch's page-table loads are issued
 constexpr int kMaxUnits = 4096;
 constexpr int kMaxSlots = 2;  // combine slots between the consumer warps and the epilogue warp
 constexpr int kMaxGrid = 1024;
@@ -32,15 +37,17 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
 // A stage holds K and V of one sub-page of PS tokens (a 64-token block streams as two
-// 32-token sub-pages); every consumer warp owns kStages / 4 stages (3 in flight).
+// 32-token sub-pages); every consumer warp owns kPerWarp stages.
 template <int P>
 struct Cfg {
   static constexpr int PS = P < 32 ? P : 32;         // tokens per stage
   static constexpr int kSub = P / PS;                // stages per block
   static constexpr int kStages = P == 16 ? 24 : 12;  // a multiple of the consumer warps
+  static constexpr int kPerWarp = kStages / kConsumerWarps;
   static constexpr int kHalfBytes = PS * 128;        // one 64-column half of a sub-page
   static constexpr int kStageBytes = 4 * kHalfBytes; // K (2 halves) + V (2 halves)
   static constexpr int kRingBytes = kStages * kStageBytes;
+  static_assert(kStages % kConsumerWarps == 0 && kPhaseB < 32 - kPerWarp, "stage ownership");
 };
 
 struct AttnArgs {
@@ -71,18 +78,6 @@ __device__ __forceinline__ int cta_of(int64_t x, int64_t N, int Gp) {
   return (int)(((x + 1) * Gp + N - 1) / N) - 1;
 }
 __device__ __forceinline__ int64_t range_start(int c, int64_t N, int Gp) { return (int64_t)c * N / Gp; }
-
-// Slot of block j of unit u, or -1 when it is out of range (skipped, reported).
-__device__ __forceinline__ int64_t block_slot(const AttnArgs& a, int u, int j, int P, int* ntok) {
-  const int b = u / a.Hkv;
-  if (j < 0 || j >= a.nblk_cap) return -1;
-  const int nv = min(P, a.seq_len[b] - j * P);
-  if (nv <= 0) return -1;
-  const int32_t s = a.page_table[(int64_t)u * a.nblk_cap + j];
-  if (s < 0 || s >= a.n_slots) return -1;
-  *ntok = nv;
-  return s;
-}
 
 // Row address (shared::cta) of token r, 16-byte chunk C (dims 8C..8C+7) in a
 // page stored as two 64-column halves with the 128-byte TMA swizzle.
@@ -256,9 +251,8 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const __grid_c
                                                                   const AttnArgs a) {
   using C = Cfg<P>;
   extern __shared__ uint8_t smem_raw[];
-  __shared__ uint64_t full_bar[C::kStages], empty_bar[C::kStages], cfull[kMaxSlots], cempty[kMaxSlots];
+  __shared__ uint64_t full_bar[C::kStages], cfull[kMaxSlots], cempty[kMaxSlots];
   __shared__ int wtot[kThreads / 32];
-  __shared__ int meta[C::kStages];  // valid tokens of the block in each stage (0: skipped)
   __shared__ float ew[kMaxG][kConsumerWarps], ehm[kMaxG], ehl[kMaxG], eown[kMaxG];  // epilogue weights
   __shared__ float efin[kMaxG], fwg[kMaxG], fwc[kMaxG];  // final LSE, merge weights
 
@@ -271,17 +265,14 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const __grid_c
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   if (tid == 0) {
-    for (int i = 0; i < C::kStages; ++i) {
-      mbar_init(&full_bar[i], 1);
-      mbar_init(&empty_bar[i], 1);
-    }
+    for (int i = 0; i < C::kStages; ++i) mbar_init(&full_bar[i], 1);
     for (int i = 0; i < a.nslots; ++i) {
       mbar_init(&cfull[i], kConsumerWarps);
       mbar_init(&cempty[i], 1);
     }
     fence_mbar_init();
   }
-  if (warp == kProducerWarp && lane == 0) {
+  if (tid == 32) {
     prefetch_tmap(&tmK);
     prefetch_tmap(&tmV);
   }
@@ -312,90 +303,6 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const __grid_c
   const int64_t N = prefix[a.units];
   const int Gp = (int)min((int64_t)gridDim.x, N);
   const int c = blockIdx.x;
-
-  if (warp == kProducerWarp) {
-    // ---------------- producer warp -------------------------------------------
-    // The 32 lanes resolve the next 32 blocks of the range at once (unit, list
-    // entry, page-table slot, valid tokens); lane 0 then streams them in order.
-    if (c >= Gp) return;
-    const int64_t start = range_start(c, N, Gp), end = range_start(c + 1, N, Gp);
-    int ucur = 0;
-    {
-      int lo = 0, hi = a.units - 1;  // last unit with prefix[u] <= start: the unit holding start
-      while (lo < hi) {
-        const int mid = (lo + hi + 1) >> 1;
-        if (prefix[mid] <= start) lo = mid; else hi = mid - 1;
-      }
-      ucur = lo;
-    }
-    uint32_t i = 0;
-    bool ok = true;
-    for (int64_t pos = start; pos < end && ok; pos += 32) {
-      const int64_t x = pos + lane;
-      int64_t slot = -1;
-      int ntok = 0;
-      if (x < end) {
-        int lo = ucur, hi = a.units - 1;
-        while (lo < hi) {
-          const int mid = (lo + hi + 1) >> 1;
-          if (prefix[mid] <= x) lo = mid; else hi = mid - 1;
-        }
-        const int j = a.res_list[(int64_t)lo * a.k + (x - prefix[lo])];
-        slot = block_slot(a, lo, j, P, &ntok);
-        if (slot < 0) ntok = 0;
-      }
-      {
-        // the unit of the last position of this batch is where the next batch starts
-        int lo = ucur, hi = a.units - 1;
-        const int64_t xl = min(pos + 31, end - 1);
-        while (lo < hi) {
-          const int mid = (lo + hi + 1) >> 1;
-          if (prefix[mid] <= xl) lo = mid; else hi = mid - 1;
-        }
-        ucur = lo;
-      }
-      const int nb = (int)min((int64_t)32, end - pos);
-      for (int t = 0; t < nb; ++t) {
-        const int64_t slot_t = __shfl_sync(0xffffffffu, slot, t);
-        const int ntok_t = __shfl_sync(0xffffffffu, ntok, t);
-        if (lane == 0 && ok) {
-          if (ntok_t == 0) report(a.status, SCOUT_DEV_BAD_INDEX);
-          for (int h = 0; h < C::kSub && ok; ++h) {
-            const int stage = (int)(i % C::kStages);
-            if (!mbar_wait(&empty_bar[stage], ((i / C::kStages) & 1u) ^ 1u)) {
-              report(a.status, SCOUT_DEV_TIMEOUT);
-              ok = false;
-              break;
-            }
-            const int nt = min(max(ntok_t - h * C::PS, 0), C::PS);
-            meta[stage] = nt;  // published to the consumer by the arrive below
-            if (nt == 0) {
-              mbar_arrive(&full_bar[stage]);
-            } else {
-              uint8_t* st = ring + stage * C::kStageBytes;
-              mbar_arrive_tx(&full_bar[stage], C::kStageBytes);
-              const int y = (int)(slot_t * P) + h * C::PS;
-              tma_load_2d(st, &tmK, 0, y, &full_bar[stage]);
-              tma_load_2d(st + C::kHalfBytes, &tmK, 64, y, &full_bar[stage]);
-              tma_load_2d(st + 2 * C::kHalfBytes, &tmV, 0, y, &full_bar[stage]);
-              tma_load_2d(st + 3 * C::kHalfBytes, &tmV, 64, y, &full_bar[stage]);
-            }
-            ++i;
-          }
-        }
-        __syncwarp();
-      }
-      ok = __shfl_sync(0xffffffffu, ok, 0);
-    }
-    // drain: wait until every copy issued into a stage has landed
-    if (lane == 0) {
-      for (uint32_t r = 0; r < C::kStages && r < i; ++r) {
-        const uint32_t last = i - 1 - r;
-        if (!mbar_wait(&full_bar[last % C::kStages], (last / C::kStages) & 1u)) report(a.status, SCOUT_DEV_TIMEOUT);
-      }
-    }
-    return;
-  }
 
   if (warp == kEpilogueWarp) {
     // ---------------- epilogue warp ------------------------------------------
@@ -618,14 +525,71 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const __grid_c
   if (c >= Gp) return;
   const int g = lane >> 2, t = lane & 3;
   const int64_t start = range_start(c, N, Gp), end = range_start(c + 1, N, Gp);
-  SegIter it{prefix, start, end, unit_of(prefix, a.units, start)};
+  // this warp's pages: sub-page i = warp + 4 k of the range, k = 0 .. n_mine-1, in stage i % kStages
+  const int64_t n_sub = (end - start) * C::kSub;
+  const int64_t n_mine = n_sub > warp ? (n_sub - 1 - warp) / kConsumerWarps + 1 : 0;
   const uint32_t ring_s = smem_u32(ring);
+  // Page kk of this warp, first half of its resolution: its unit, list entry and sequence length.
+  auto resolve_a = [&](int64_t kk, int& ru, int& rj, int& rlen) {
+    ru = -1;
+    rj = -1;
+    rlen = 0;
+    if (kk < n_mine) {
+      const int64_t x = start + (warp + (int64_t)kConsumerWarps * kk) / C::kSub;
+      ru = unit_of(prefix, a.units, x);
+      rj = a.res_list[(int64_t)ru * a.k + (x - prefix[ru])];
+      rlen = a.seq_len[ru / a.Hkv];
+    }
+  };
+  // Second half: the pool row of the sub-page and its valid tokens (0 = nothing to load).  An
+  // entry outside the sequence or the pool is skipped and reported.
+  auto resolve_b = [&](int64_t kk, int ru, int rj, int rlen, int& row, int& nt) {
+    row = 0;
+    nt = 0;
+    if (ru < 0) return;
+    const int h = (int)((warp + (int64_t)kConsumerWarps * kk) % C::kSub);
+    int nv = 0;
+    int32_t sl = -1;
+    if (rj >= 0 && rj < a.nblk_cap) {
+      nv = min(P, rlen - rj * P);
+      sl = a.page_table[(int64_t)ru * a.nblk_cap + rj];
+    }
+    if (nv <= 0 || sl < 0 || sl >= a.n_slots) {
+      if (h == 0) report(a.status, SCOUT_DEV_BAD_INDEX);
+      return;
+    }
+    nt = min(max(nv - h * C::PS, 0), C::PS);
+    row = sl * P + h * C::PS;
+  };
+  // Load page kk (lane 0): both 64-column halves of K and of V, one box each.
+  auto issue = [&](int64_t kk, int row, int nt) {
+    const int stage = (int)((warp + (int64_t)kConsumerWarps * kk) % C::kStages);
+    if (nt > 0) {
+      uint8_t* sp = ring + stage * C::kStageBytes;
+      mbar_arrive_tx(&full_bar[stage], C::kStageBytes);
+      tma_load_3d(sp, &tmK, 0, row, 0, &full_bar[stage]);
+      tma_load_3d(sp + 2 * C::kHalfBytes, &tmV, 0, row, 0, &full_bar[stage]);
+    } else {
+      mbar_arrive(&full_bar[stage]);
+    }
+  };
+  // batch b = pages 32 b .. 32 b + 31 of this warp, page 32 b + m resolved by lane m
+  int cur_row, cur_nt, nxt_row = 0, nxt_nt = 0, pu, pj, plen;
+  resolve_a(lane, pu, pj, plen);
+  resolve_b(lane, pu, pj, plen, cur_row, cur_nt);
+  for (int r = 0; r < C::kPerWarp && r < n_mine; ++r) {
+    const int row = __shfl_sync(0xffffffffu, cur_row, r), nt = __shfl_sync(0xffffffffu, cur_nt, r);
+    if (lane == 0) issue(r, row, nt);
+  }
+
+  SegIter it{prefix, start, end, unit_of(prefix, a.units, start)};
   int u;
   int64_t lo, hi;
   bool have = it.next(u, lo, hi);
   uint32_t qa[8][2], qn[8][2];
   if (have) load_q(a, u, lane, qa);
-  uint32_t i = 0;
+  int64_t i = 0;
+  bool ok = true;  // false after a bounded wait ran out
   for (int sg = 0; have; ++sg) {
     // prefetch the next segment's query while this one streams
     SegIter peek = it;
@@ -640,18 +604,34 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const __grid_c
     for (int d = 0; d < 8; ++d) st.o[d][0] = st.o[d][1] = st.o[d][2] = st.o[d][3] = 0.f;
     for (int64_t p = lo * C::kSub; p < hi * C::kSub; ++p, ++i) {  // sub-pages of the segment's blocks
       if ((int)(i % kConsumerWarps) != warp) continue;
+      const int64_t k = i / kConsumerWarps;
+      const int m = (int)(k & 31);
+      if (m == 0) resolve_a(k + 32 + lane, pu, pj, plen);  // next batch: list entries
+      if (m == kPhaseB) resolve_b(k - kPhaseB + 32 + lane, pu, pj, plen, nxt_row, nxt_nt);  // and slots
       const int stage = (int)(i % C::kStages);
-      if (!mbar_wait(&full_bar[stage], (i / C::kStages) & 1u)) {
+      const int ntok = __shfl_sync(0xffffffffu, cur_nt, m);
+      if (!ok) {
+      } else if (!mbar_wait(&full_bar[stage], (uint32_t)(k / C::kPerWarp) & 1u)) {
         if (lane == 0) report(a.status, SCOUT_DEV_TIMEOUT);
-      } else {
-        const int ntok = meta[stage];
-        if (ntok > 0) {
-          const uint32_t kb = ring_s + stage * C::kStageBytes;
-          attend_page<P>(kb, kb + 2 * C::kHalfBytes, ntok, qa, a.scale_log2, st, lane);
-        }
+        ok = false;  // a copy may still be in flight here: issue nothing more
+      } else if (ntok > 0) {
+        const uint32_t kb = ring_s + stage * C::kStageBytes;
+        attend_page<P>(kb, kb + 2 * C::kHalfBytes, ntok, qa, a.scale_log2, st, lane);
       }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&empty_bar[stage]);
+      // reload the stage with this warp's page k + kPerWarp once every lane is done reading it
+      const int64_t kr = k + C::kPerWarp;
+      if (kr < n_mine && ok) {
+        const int mr = m + C::kPerWarp;
+        const int row = __shfl_sync(0xffffffffu, mr < 32 ? cur_row : nxt_row, mr & 31);
+        const int nt = __shfl_sync(0xffffffffu, mr < 32 ? cur_nt : nxt_nt, mr & 31);
+        fence_proxy_async();
+        __syncwarp();
+        if (lane == 0) issue(kr, row, nt);
+      }
+      if (m == 31) {
+        cur_row = nxt_row;
+        cur_nt = nxt_nt;
+      }
     }
     // hand this warp's state for the segment to the epilogue warp
     float l0 = st.l[0], l1 = st.l[1];
@@ -706,14 +686,15 @@ size_t dyn_smem(int units, int G, int nslots) {
 }
 constexpr size_t kSmemLimit = 232448 - 1024;  // per-block shared memory minus room for static use
 
-// The pool as a 2-D bf16 tensor [n_slots * P rows][128 columns]; boxes of 64 columns
-// x box_rows tokens (one sub-page) with the 128-byte swizzle.
+// The pool [n_slots * P rows][128 columns] bf16 seen as a 3-D tensor [2 halves][rows][64
+// columns] (half stride 128 bytes, row stride 256 bytes): one box {64, box_rows, 2} is a whole
+// sub-page, landing in shared memory as two [box_rows][64] halves with the 128-byte swizzle.
 bool make_page_map(CUtensorMap* map, const void* pool, int64_t n_slots, int P, int box_rows) {
-  const cuuint64_t dims[2] = {(cuuint64_t)kD, (cuuint64_t)(n_slots * P)};
-  const cuuint64_t strides[1] = {(cuuint64_t)kD * 2};
-  const cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
-  const cuuint32_t estr[2] = {1, 1};
-  return encode_tiled(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(pool), dims, strides, box, estr,
+  const cuuint64_t dims[3] = {64, (cuuint64_t)(n_slots * P), 2};
+  const cuuint64_t strides[2] = {(cuuint64_t)kD * 2, 128};
+  const cuuint32_t box[3] = {64, (cuuint32_t)box_rows, 2};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return encode_tiled(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(pool), dims, strides, box, estr,
                       CU_TENSOR_MAP_SWIZZLE_128B) == CUDA_SUCCESS;
 }
 
