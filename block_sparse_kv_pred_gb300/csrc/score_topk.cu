@@ -11,8 +11,9 @@
 //    with bf16 operands and fp32 accumulation computes it (products are exact).  The
 //    score pooled over the unit's G query heads (maximum) becomes an orderable key in
 //    shared memory;
-//  * warps 8..11 select each unit as soon as its chunks are scored: radix select of the
-//    k-th key, then one ordered compaction into top-k, resident, CPU and delta lists.
+//  * warps 8..11 select the units as their chunks are scored, one warp per unit and up
+//    to four units at a time: radix select of the k-th key, then one ordered compaction
+//    into top-k, resident, CPU and delta lists.
 // CTA c owns the contiguous item range [c I / Gp, (c+1) I / Gp), so almost every unit
 // is scored and selected inside one CTA; a unit cut by a range boundary goes through
 // global memory and is selected by whichever of its CTAs adds its last chunks to a
@@ -26,12 +27,12 @@ namespace {
 
 constexpr int kScoreWarps = 8;
 constexpr int kSelWarps = 4;
-constexpr int kSelThreads = kSelWarps * 32;
 constexpr int kProducer = kScoreWarps + kSelWarps;  // warp index of the TMA producer
 constexpr int kThreadsAll = (kProducer + 1) * 32;
 constexpr int kChunk = kScoreWarps * 16;  // digest rows (blocks) per work item
 constexpr int kBoxBytes = kChunk * 128;   // one 128-row x 128-byte TMA box
 constexpr int kMaxStagesT = 3;
+constexpr int kMaxKeyBufs = 8;  // key buffers: one being scored, the others being selected
 
 __device__ __forceinline__ uint32_t trunc_bf16(float x) { return __float_as_uint(x) & 0xFFFF0000u; }
 
@@ -156,6 +157,8 @@ struct TopkArgs {
   const int32_t* prev_list;
   const int32_t* prev_count;
   int Hq, Hkv, G, P, nblk_cap, k, words, nchunk, stages;
+  int nkbuf;  // key buffers in shared memory (2 .. kMaxKeyBufs)
+  int nsel;   // selector warps in use (1 .. min(kSelWarps, nkbuf - 1))
   int user_scores;  // 1: the caller asked for every pooled score in `scores`
   int64_t n_items;
   float* scores;  // user buffer or workspace
@@ -170,254 +173,284 @@ __device__ __forceinline__ int unit_nvalid(const TopkArgs& a, int b) {
   return min(a.nblk_cap, (max(a.seq_len[b], 0) + a.P - 1) / a.P);
 }
 
-// The selector warps synchronise among themselves on named barrier 2.
-__device__ __forceinline__ void sbar() { asm volatile("bar.sync 2, %0;" ::"n"(kSelThreads) : "memory"); }
-
-// Exclusive prefix over the selector threads of four counters per thread; returns the totals.
-__device__ __forceinline__ int4 sel_excl_scan4(int4 v, int4* wsum, int4& total) {
-  const int lane = threadIdx.x & 31, w = (threadIdx.x >> 5) - kScoreWarps;
-  int4 inc = v;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int x = __shfl_up_sync(0xffffffffu, inc.x, o), y = __shfl_up_sync(0xffffffffu, inc.y, o);
-    const int z = __shfl_up_sync(0xffffffffu, inc.z, o), ww = __shfl_up_sync(0xffffffffu, inc.w, o);
-    if (lane >= o) {
-      inc.x += x;
-      inc.y += y;
-      inc.z += z;
-      inc.w += ww;
-    }
-  }
-  if (lane == 31) wsum[w] = inc;
-  sbar();
-  int4 base = make_int4(0, 0, 0, 0), tot = make_int4(0, 0, 0, 0);
-#pragma unroll
-  for (int i = 0; i < kSelWarps; ++i) {
-    const int4 s = wsum[i];
-    if (i < w) {
-      base.x += s.x;
-      base.y += s.y;
-      base.z += s.z;
-      base.w += s.w;
-    }
-    tot.x += s.x;
-    tot.y += s.y;
-    tot.z += s.z;
-    tot.w += s.w;
-  }
-  sbar();
-  total = tot;
-  return make_int4(base.x + inc.x - v.x, base.y + inc.y - v.y, base.z + inc.z - v.z, base.w + inc.w - v.w);
+// A selector warp's shared memory: the unit's residency bits, the bits of its previous
+// CPU list, the bits of the chosen candidates, a 256-bin digit histogram and the blocks
+// of up to 32 candidates.
+struct SelWarp {
+  uint32_t* rbits;  // [words]
+  uint32_t* pbits;  // [words]
+  uint32_t* cbits;  // [words]
+  int* hist;        // [256]
+  int* cidx;        // [32]
+};
+// 32-bit words of one selector warp's shared memory
+__host__ __device__ constexpr int selwarp_words(int words) { return 3 * align4(words) + 256 + 32; }
+__device__ __forceinline__ SelWarp selwarp_at(uint32_t* area, int words) {
+  const int w4 = align4(words);
+  return SelWarp{area, area + w4, area + 2 * w4, reinterpret_cast<int*>(area + 3 * w4),
+                 reinterpret_cast<int*>(area + 3 * w4 + 256)};
 }
 
-constexpr int kDigitBits = 12;  // radix digit width of the selection
-constexpr int kBins = 1 << kDigitBits;
-
-struct SelShared {
-  uint32_t* rbits;  // [words] residency of the unit
-  uint32_t* pbits;  // [words] previous CPU list of the unit
-  int* hist;        // [kBins]
-  int4 wsum[kSelWarps];
-  uint32_t kmin[kSelWarps], kmax[kSelWarps];
-  int digit, remaining, count, nvalid;
-};
-
-// Loads the unit's residency bits and previous CPU list into shared memory; issued
-// before the unit's keys are ready so the global-memory latency overlaps the scoring.
-__device__ void prefetch_unit(const TopkArgs& a, int u, SelShared& ss) {
-  const int st = threadIdx.x - kScoreWarps * 32;
-  if (st == 0) ss.nvalid = unit_nvalid(a, u / a.Hkv);
-  for (int i = st; i < a.words; i += kSelThreads) {
-    ss.rbits[i] = a.resident_bits[(int64_t)u * a.words + i];
-    ss.pbits[i] = 0u;
+// Loads the unit's residency bits and previous CPU list into the warp's shared memory.
+__device__ void prefetch_unit(const TopkArgs& a, int u, const SelWarp& sw, int lane) {
+  for (int i = lane; i < a.words; i += 32) {
+    sw.rbits[i] = a.resident_bits[(int64_t)u * a.words + i];
+    sw.pbits[i] = 0u;
   }
-  sbar();
+  __syncwarp();
   if (a.prev_list != nullptr) {
     const int pc = min(max(a.prev_count[u], 0), a.k);
-    for (int i = st; i < pc; i += kSelThreads) {
+    for (int i = lane; i < pc; i += 32) {
       const int j = a.prev_list[(int64_t)u * a.k + i];
-      if (j >= 0 && j < a.nblk_cap) atomicOr(&ss.pbits[j >> 5], 1u << (j & 31));
+      if (j >= 0 && j < a.nblk_cap) atomicOr(&sw.pbits[j >> 5], 1u << (j & 31));
     }
   }
-  sbar();
+  __syncwarp();
 }
 
-// Top-k of one unit's keys (in shared memory), split by residency, delta against the
-// previous CPU list, ordered compaction.  Run by the 128 selector threads after
-// prefetch_unit(u).
-__device__ void select_unit(const TopkArgs& a, int u, const uint32_t* keys, SelShared& ss) {
-  const int st = threadIdx.x - kScoreWarps * 32;  // 0 .. 127
-  const int lane = threadIdx.x & 31, w = st >> 5;
-  const int nvalid = ss.nvalid;
+// Keys g0 + 32 r + lane (r = 0..31) of a group of 1024, minus base, into registers
+// (0 past nvalid).
+__device__ __forceinline__ void load_group(const uint32_t* keys, int nvalid, int g0, int lane, uint32_t (&kv)[32],
+                                           uint32_t base = 0u) {
+#pragma unroll
+  for (int r = 0; r < 32; ++r) {
+    const int j = g0 + 32 * r + lane;
+    kv[r] = j < nvalid ? keys[j] - base : 0u;
+  }
+}
+
+// 32 x 32 bit transpose across a warp: bit j of lane i's word becomes bit i of lane j's
+// word (block swaps of 16, 8, 4, 2 and 1).
+__device__ __forceinline__ uint32_t transpose32(uint32_t x, int lane) {
+#pragma unroll
+  for (int s = 16; s > 0; s >>= 1) {
+    const uint32_t m = s == 16 ? 0x0000FFFFu : s == 8 ? 0x00FF00FFu : s == 4 ? 0x0F0F0F0Fu : s == 2 ? 0x33333333u
+                                                                                                     : 0x55555555u;
+    const uint32_t y = __shfl_xor_sync(0xffffffffu, x, s);
+    x = (lane & s) ? ((x & ~m) | ((y & ~m) >> s)) : ((x & m) | ((y & m) << s));
+  }
+  return x;
+}
+
+// Writes the blocks whose bits are set in the round masks m (lane r holds round r of the
+// group of 1024 starting at block g0) to list[run ..] in ascending order; returns their count.
+// Every lane writes consecutive entries, so the stores are coalesced.
+__device__ __forceinline__ int write_group(int32_t* list, int run, uint32_t m, int g0, int lane) {
+  const int c = __popc(m);
+  int incl = c;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  const int excl = incl - c, total = __shfl_sync(0xffffffffu, incl, 31);
+  for (int p0 = 0; p0 < total; p0 += 32) {  // warp-uniform trips: every lane shuffles
+    const int p = p0 + lane;
+    // the round holding entry p: the last lane whose exclusive count is <= p
+    int lo = 0;
+#pragma unroll
+    for (int step = 16; step > 0; step >>= 1) {
+      const int e = __shfl_sync(0xffffffffu, excl, min(lo + step, 31));
+      if (lo + step <= 31 && e <= p) lo += step;
+    }
+    const uint32_t mr = __shfl_sync(0xffffffffu, m, lo);
+    const int off = p - __shfl_sync(0xffffffffu, excl, lo);
+    if (p < total) list[run + p] = g0 + 32 * lo + (int)__fns(mr, 0, off + 1);
+  }
+  return total;
+}
+
+// Top-k of one unit's keys (shared memory), split by residency, delta against the previous
+// CPU list, written in ascending block order.  One warp, no block-level barrier.
+//
+// The keys are taken 1024 at a time into registers (lane l holds keys 32 r + l), so every
+// step is a run of independent instructions.  The k-th largest key is bracketed by a radix
+// select on key - min: the leading bits zero in all of them are skipped, then 8-bit digits
+// of the keys sharing the current prefix are counted into a 256-bin histogram (shared-memory
+// reductions) until the keys sharing the prefix (the candidates) are the ones still needed
+// or at most 32.  Keys above the prefix are selected.  Of the candidates the `remaining`
+// largest are taken, the lower block index first among equal keys: with at most 32 of them
+// one per lane ranks itself against the others; more can only be left when every candidate
+// key is equal, and then the lowest-index ones are taken.  The chosen candidates go into a
+// bitmap.  Per-round bit masks move between "lane = block" and "lane = round" by a 32 x 32
+// bit transpose, so no step needs a shuffle per round, and the lists are written with
+// coalesced stores.
+__device__ void select_unit(const TopkArgs& a, int u, const uint32_t* keys, int nvalid, const SelWarp& sw,
+                            int lane) {
   const int keff = min(a.k, nvalid);
-  uint32_t prefix = 0u, mask = 0u;
+  const int ngroups = (nvalid + 1023) / 1024;
+  uint32_t kv[32];
+  if (ngroups == 1) load_group(keys, nvalid, 0, lane, kv);  // stays in registers throughout
+  uint32_t prefix = 0u, mask = 0u, base = 0u;  // selection works on key - base
   int remaining = keff, count = nvalid;
   if (keff < nvalid) {
-    // the leading bits every key shares need no radix pass
     uint32_t lo = 0xffffffffu, hi = 0u;
-    for (int j = st; j < nvalid; j += kSelThreads) {
-      lo = min(lo, keys[j]);
-      hi = max(hi, keys[j]);
-    }
+    for (int g = 0; g < ngroups; ++g) {
+      if (ngroups > 1) load_group(keys, nvalid, g * 1024, lane, kv);
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      lo = min(lo, __shfl_xor_sync(0xffffffffu, lo, o));
-      hi = max(hi, __shfl_xor_sync(0xffffffffu, hi, o));
+      for (int r = 0; r < 32; ++r)
+        if (g * 1024 + 32 * r + lane < nvalid) {
+          lo = min(lo, kv[r]);
+          hi = max(hi, kv[r]);
+        }
     }
-    if (lane == 0) {
-      ss.kmin[w] = lo;
-      ss.kmax[w] = hi;
-    }
-    sbar();
+    lo = __reduce_min_sync(0xffffffffu, lo);
+    hi = __reduce_max_sync(0xffffffffu, hi);
+    // relative keys keep the order; their digits start at the top bit of the key range, so
+    // the first digit already spreads the keys over the bins
+    base = lo;
+    if (ngroups == 1) {
 #pragma unroll
-    for (int i = 0; i < kSelWarps; ++i) {
-      lo = min(lo, ss.kmin[i]);
-      hi = max(hi, ss.kmax[i]);
+      for (int r = 0; r < 32; ++r) kv[r] -= base;
     }
-    int fixed = (lo == hi) ? 32 : __clz(lo ^ hi);  // leading bits common to all keys
+    int fixed = lo == hi ? 32 : __clz(hi - lo);  // leading bits zero in every relative key
     mask = fixed == 0 ? 0u : (fixed == 32 ? 0xffffffffu : ~(0xffffffffu >> fixed));
-    prefix = lo & mask;
-    // radix select on 12-bit digits below the common bits; it stops once the keys
-    // sharing the current prefix are exactly the ones still needed
-    while (fixed < 32 && remaining != count) {
-      const int width = min(kDigitBits, 32 - fixed), shift = 32 - fixed - width;
+    int4* h4 = reinterpret_cast<int4*>(sw.hist);
+    while (fixed < 32 && remaining != count && count > 32) {
+      const int width = min(8, 32 - fixed), shift = 32 - fixed - width;
       const uint32_t dmask = (1u << width) - 1u;
-      for (int i = st; i < kBins / 4; i += kSelThreads) reinterpret_cast<int4*>(ss.hist)[i] = make_int4(0, 0, 0, 0);
-      sbar();
-      for (int j = st; j < nvalid; j += kSelThreads) {
-        const uint32_t key = keys[j];
-        if ((key & mask) == prefix) atomicAdd(&ss.hist[(key >> shift) & dmask], 1);
+      h4[lane] = make_int4(0, 0, 0, 0);
+      h4[lane + 32] = make_int4(0, 0, 0, 0);
+      __syncwarp();
+      for (int g = 0; g < ngroups; ++g) {
+        if (ngroups > 1) load_group(keys, nvalid, g * 1024, lane, kv, base);
+#pragma unroll
+        for (int r = 0; r < 32; ++r)
+          if (g * 1024 + 32 * r + lane < nvalid && (kv[r] & mask) == prefix)
+            atomicAdd(&sw.hist[(kv[r] >> shift) & dmask], 1);
       }
-      sbar();
-      // thread st owns the 32 bins [kBins - 32 (st + 1), kBins - 32 st): high bins first
-      constexpr int kPer = kBins / kSelThreads;
-      const int top = kBins - kPer * st - 1;
-      int sum = 0;
-#pragma unroll 8
-      for (int e = 0; e < kPer; ++e) sum += ss.hist[top - ((e + lane) & (kPer - 1))];  // rotated: no bank conflicts
-      int4 tot4;
-      const int before = sel_excl_scan4(make_int4(sum, 0, 0, 0), ss.wsum, tot4).x;
-      if (before < remaining && remaining <= before + sum) {
-        int acc = before;
-        for (int e = 0; e < kPer; ++e) {
-          const int c = ss.hist[top - e];
-          if (acc < remaining && remaining <= acc + c) {
-            ss.digit = top - e;
-            ss.remaining = remaining - acc;
-            ss.count = c;
-            break;
+      __syncwarp();
+      // lane L holds bins 8L .. 8L+7; counts above each lane from the highest bin down
+      const int4 x0 = h4[2 * lane], x1 = h4[2 * lane + 1];
+      const int c8[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+      const int own = x0.x + x0.y + x0.z + x0.w + x1.x + x1.y + x1.z + x1.w;
+      int suf = own;  // bins >= 8L
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_down_sync(0xffffffffu, suf, o);
+        if (lane + o < 32) suf += y;
+      }
+      const int above = suf - own;  // bins > 8L + 7
+      const int L = __ffs(__ballot_sync(0xffffffffu, above < remaining && remaining <= suf)) - 1;
+      int digit = 0, rem = 0, cnt = 0;
+      if (lane == L) {
+        int acc = above;
+#pragma unroll
+        for (int e = 7; e >= 0; --e) {
+          if (acc < remaining && remaining <= acc + c8[e] && cnt == 0) {
+            digit = 8 * L + e;
+            rem = remaining - acc;
+            cnt = c8[e];
           }
-          acc += c;
+          acc += c8[e];
         }
       }
-      sbar();
-      prefix |= (uint32_t)ss.digit << shift;
+      __syncwarp();  // every lane has read the histogram before it is reused
+      prefix |= (uint32_t)__shfl_sync(0xffffffffu, digit, L) << shift;
       mask |= dmask << shift;
-      remaining = ss.remaining;
-      count = ss.count;
+      remaining = __shfl_sync(0xffffffffu, rem, L);
+      count = __shfl_sync(0xffffffffu, cnt, L);
       fixed += width;
     }
   }
-  // selected: masked key above the prefix, or equal to it and (all equal ones needed,
-  // or among the lowest-index `remaining` of them).  Thread st owns the contiguous
-  // blocks [st per, st per + per) in groups of 8 (one residency byte, two 16-byte key
-  // loads); per-thread counts are scanned once, so the lists come out in ascending
-  // block order.
-  const bool all_eq = remaining == count;
-  const int per = ((nvalid + kSelThreads - 1) / kSelThreads + 7) / 8 * 8;
-  const int jlo = min(nvalid, st * per), jhi = min(nvalid, jlo + per);
-  int4 tot;
-  int eq_base = 0;
+  const bool all_eq = remaining == count;  // every candidate is taken
   if (!all_eq) {
-    int n_eq = 0;
-    for (int j = jlo; j < jhi; ++j) n_eq += (keys[j] & mask) == prefix;
-    eq_base = sel_excl_scan4(make_int4(n_eq, 0, 0, 0), ss.wsum, tot).x;
-  }
-  // pass 1: counts
-  int4 cnt = make_int4(0, 0, 0, 0);
-  int eqr = eq_base;
-  for (int g0 = jlo; g0 < jhi; g0 += 8) {
-    uint32_t kv[8];
-    if (g0 + 8 <= jhi) {
-      const uint4 x = *reinterpret_cast<const uint4*>(keys + g0), y = *reinterpret_cast<const uint4*>(keys + g0 + 4);
-      kv[0] = x.x; kv[1] = x.y; kv[2] = x.z; kv[3] = x.w; kv[4] = y.x; kv[5] = y.y; kv[6] = y.z; kv[7] = y.w;
+    for (int i = lane; i < a.words; i += 32) sw.cbits[i] = 0u;
+    __syncwarp();
+    const uint32_t lt = (1u << lane) - 1u;
+    if (count <= 32) {
+      // gather the candidates in block order (lane r takes round r of each group of 1024 after a
+      // bit transpose), then one per lane ranks itself against the others
+      int n = 0;
+      for (int g = 0; g < ngroups; ++g) {
+        if (ngroups > 1) load_group(keys, nvalid, g * 1024, lane, kv, base);
+        uint32_t e = 0u;  // bit r: this lane's key of round r is a candidate
+#pragma unroll
+        for (int r = 0; r < 32; ++r)
+          if (g * 1024 + 32 * r + lane < nvalid && (kv[r] & mask) == prefix) e |= 1u << r;
+        uint32_t em = transpose32(e, lane);  // candidates of round `lane`
+        const int c = __popc(em);
+        int incl = c;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int y = __shfl_up_sync(0xffffffffu, incl, o);
+          if (lane >= o) incl += y;
+        }
+        for (int pos = n + incl - c; em != 0u; ++pos, em &= em - 1u) sw.cidx[pos] = g * 1024 + 32 * lane + __ffs(em) - 1;
+        n += __shfl_sync(0xffffffffu, incl, 31);
+      }
+      __syncwarp();
+      const int ji = lane < count ? sw.cidx[lane] : 0;
+      const uint32_t ki = lane < count ? keys[ji] - base : 0u;
+      int rank = 0;
+#pragma unroll
+      for (int m = 0; m < 32; ++m) {
+        const uint32_t km = __shfl_sync(0xffffffffu, ki, m);
+        const int jm = __shfl_sync(0xffffffffu, ji, m);
+        rank += (m < count && (km > ki || (km == ki && jm < ji))) ? 1 : 0;
+      }
+      if (lane < count && rank < remaining) atomicOr(&sw.cbits[ji >> 5], 1u << (ji & 31));
     } else {
+      // more than 32 candidates are left only when all of them are equal: the lowest-index ones
+      int seen = 0;
+      for (int g = 0; g < ngroups; ++g) {
+        if (ngroups > 1) load_group(keys, nvalid, g * 1024, lane, kv, base);
 #pragma unroll
-      for (int e = 0; e < 8; ++e) kv[e] = g0 + e < jhi ? keys[g0 + e] : 0u;
-    }
-    const uint32_t rb = ss.rbits[g0 >> 5] >> (g0 & 31), pb = ss.pbits[g0 >> 5] >> (g0 & 31);
-#pragma unroll
-    for (int e = 0; e < 8; ++e) {
-      const uint32_t mk = kv[e] & mask;
-      const bool in = g0 + e < jhi, eq = in && mk == prefix;
-      const bool sel = in && (mk > prefix || (eq && (all_eq || eqr < remaining)));
-      eqr += eq;
-      if (sel) {
-        cnt.x += 1;
-        if ((rb >> e) & 1u) cnt.y += 1;
-        else {
-          cnt.z += 1;
-          cnt.w += ((pb >> e) & 1u) ? 0 : 1;
+        for (int r = 0; r < 32; ++r) {
+          const int j = g * 1024 + 32 * r + lane;
+          const bool eq = j < nvalid && (kv[r] & mask) == prefix;
+          const uint32_t eqb = __ballot_sync(0xffffffffu, eq);
+          const uint32_t sb = __ballot_sync(0xffffffffu, eq && seen + __popc(eqb & lt) < remaining);
+          if (lane == 0) sw.cbits[g * 32 + r] = sb;
+          seen += __popc(eqb);
         }
       }
     }
+    __syncwarp();
   }
-  int4 pos = sel_excl_scan4(cnt, ss.wsum, tot);
-  // pass 2: writes
+  // compaction: per lane one bit per round, transposed so that lane r holds round r's
+  // selected blocks; each list is then written with coalesced stores
   const int64_t lb = (int64_t)u * a.k;
-  eqr = eq_base;
-  for (int g0 = jlo; g0 < jhi; g0 += 8) {
-    uint32_t kv[8];
-    if (g0 + 8 <= jhi) {
-      const uint4 x = *reinterpret_cast<const uint4*>(keys + g0), y = *reinterpret_cast<const uint4*>(keys + g0 + 4);
-      kv[0] = x.x; kv[1] = x.y; kv[2] = x.z; kv[3] = x.w; kv[4] = y.x; kv[5] = y.y; kv[6] = y.z; kv[7] = y.w;
-    } else {
+  int nt = 0, nr = 0, nc = 0, nd = 0;
+  for (int g = 0; g < ngroups; ++g) {
+    if (ngroups > 1) load_group(keys, nvalid, g * 1024, lane, kv, base);
+    const int w = g * 32 + lane;  // word of round `lane` in the per-block bitmaps
+    const uint32_t rw = w < a.words ? sw.rbits[w] : 0u, pw = w < a.words ? sw.pbits[w] : 0u;
+    // bit r of tb: the candidate at (round r, this lane) is taken
+    const uint32_t tb = all_eq ? 0xffffffffu : transpose32(w < a.words ? sw.cbits[w] : 0u, lane);
+    uint32_t sel = 0u;  // bit r: this lane's block of round r is selected
 #pragma unroll
-      for (int e = 0; e < 8; ++e) kv[e] = g0 + e < jhi ? keys[g0 + e] : 0u;
+    for (int r = 0; r < 32; ++r) {
+      const uint32_t mk = kv[r] & mask;
+      if (g * 1024 + 32 * r + lane < nvalid && (mk > prefix || (mk == prefix && ((tb >> r) & 1u)))) sel |= 1u << r;
     }
-    const uint32_t rb = ss.rbits[g0 >> 5] >> (g0 & 31), pb = ss.pbits[g0 >> 5] >> (g0 & 31);
-#pragma unroll
-    for (int e = 0; e < 8; ++e) {
-      const uint32_t mk = kv[e] & mask;
-      const bool in = g0 + e < jhi, eq = in && mk == prefix;
-      const bool sel = in && (mk > prefix || (eq && (all_eq || eqr < remaining)));
-      eqr += eq;
-      if (sel) {
-        const int j = g0 + e;
-        a.topk_idx[lb + pos.x++] = j;
-        if ((rb >> e) & 1u) {
-          a.res_list[lb + pos.y++] = j;
-        } else {
-          a.cpu_list[lb + pos.z++] = j;
-          if (!((pb >> e) & 1u)) a.delta_list[lb + pos.w++] = j;
-        }
-      }
-    }
+    const uint32_t ms = transpose32(sel, lane);  // selected blocks of round `lane`
+    const uint32_t mres = ms & rw, mcpu = ms & ~rw, mdel = ms & ~rw & ~pw;
+    nt += write_group(a.topk_idx + lb, nt, ms, g * 1024, lane);
+    nr += write_group(a.res_list + lb, nr, mres, g * 1024, lane);
+    nc += write_group(a.cpu_list + lb, nc, mcpu, g * 1024, lane);
+    nd += write_group(a.delta_list + lb, nd, mdel, g * 1024, lane);
   }
-  for (int i = st; i < a.k; i += kSelThreads) {
-    if (i >= tot.x) a.topk_idx[lb + i] = -1;
-    if (i >= tot.y) a.res_list[lb + i] = -1;
-    if (i >= tot.z) a.cpu_list[lb + i] = -1;
-    if (i >= tot.w) a.delta_list[lb + i] = -1;
+  for (int i = lane; i < a.k; i += 32) {
+    if (i >= nt) a.topk_idx[lb + i] = -1;
+    if (i >= nr) a.res_list[lb + i] = -1;
+    if (i >= nc) a.cpu_list[lb + i] = -1;
+    if (i >= nd) a.delta_list[lb + i] = -1;
   }
-  if (st == 0) {
-    a.topk_count[u] = tot.x;
-    a.res_count[u] = tot.y;
-    a.cpu_count[u] = tot.z;
-    a.delta_count[u] = tot.w;
+  if (lane == 0) {
+    a.topk_count[u] = nt;
+    a.res_count[u] = nr;
+    a.cpu_count[u] = nc;
+    a.delta_count[u] = nd;
   }
-  sbar();  // keys and scratch are reused by the next selection
 }
 
 template <int KIND>
 __global__ void __launch_bounds__(kThreadsAll, 1) score_topk_kernel(const __grid_constant__ CUtensorMap tmD,
                                                                     const TopkArgs a) {
   extern __shared__ uint8_t smem_raw[];
-  __shared__ uint64_t full_bar[kMaxStagesT], empty_bar[kMaxStagesT], kfull[2], kempty[2];
-  __shared__ SelShared ss;
-  __shared__ int s_flag;
-  // dynamic shared memory: [ring (1024-aligned)][2 key buffers][residency bits][previous-list bits]
-  // [radix histogram]
+  __shared__ uint64_t full_bar[kMaxStagesT], empty_bar[kMaxStagesT], kfull[kMaxKeyBufs], kempty[kMaxKeyBufs];
+  // dynamic shared memory: [ring (1024-aligned)][nkbuf key buffers][nsel selector-warp areas]
   const uint32_t raw = smem_u32(smem_raw);
   uint8_t* ring = smem_raw + (((raw + 1023u) & ~1023u) - raw);
   uint32_t* keybuf = reinterpret_cast<uint32_t*>(ring + a.stages * kStageBytesT);
@@ -428,15 +461,11 @@ __global__ void __launch_bounds__(kThreadsAll, 1) score_topk_kernel(const __grid
       mbar_init(&full_bar[i], 1);
       mbar_init(&empty_bar[i], kScoreWarps);
     }
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < a.nkbuf; ++i) {
       mbar_init(&kfull[i], kScoreWarps);
       mbar_init(&kempty[i], 1);
     }
     fence_mbar_init();
-    // every region starts 16-byte aligned (the histogram is zeroed with int4 stores)
-    ss.rbits = keybuf + 2 * align4(a.nblk_cap);
-    ss.pbits = ss.rbits + align4(a.words);
-    ss.hist = reinterpret_cast<int*>(ss.pbits + align4(a.words));
   }
   __syncthreads();
   const int64_t Gp = gridDim.x;  // the host launches at most one CTA per item
@@ -485,36 +514,42 @@ __global__ void __launch_bounds__(kThreadsAll, 1) score_topk_kernel(const __grid
 
   if (warp >= kScoreWarps) {
     // ---------------- selector warps 8..11 -----------------------------------
-    const int st = tid - kScoreWarps * 32;
-    for (int u = u_first; u <= u_last; ++u) {
-      const int e = u - u_first, kb = e & 1;
+    // unit e of the range (e = u - u_first) sits in key buffer e % nkbuf and is selected
+    // by selector warp e % nsel, so up to nsel units are selected at once
+    const int sw_i = warp - kScoreWarps;
+    if (sw_i >= a.nsel) return;
+    uint32_t* area = keybuf + a.nkbuf * align4(a.nblk_cap) + sw_i * selwarp_words(a.words);
+    const SelWarp sw = selwarp_at(area, a.words);
+    for (int u = u_first + sw_i; u <= u_last; u += a.nsel) {
+      const int e = u - u_first, kb = e % a.nkbuf;
       uint32_t* keys = keybuf + kb * align4(a.nblk_cap);
-      prefetch_unit(a, u, ss);  // overlaps the scoring of u
-      if (!mbar_wait(&kfull[kb], (uint32_t)(e >> 1) & 1u) && st == 0) report(a.status, SCOUT_DEV_TIMEOUT);
+      prefetch_unit(a, u, sw, lane);  // overlaps the scoring of u
+      const int nvalid = unit_nvalid(a, u / a.Hkv);
+      if (!mbar_wait(&kfull[kb], (uint32_t)(e / a.nkbuf) & 1u) && lane == 0) report(a.status, SCOUT_DEV_TIMEOUT);
       const int64_t first = (int64_t)u * a.nchunk, last = first + a.nchunk - 1;
       bool doit = first >= it0 && last < it1;  // the whole unit was scored here
       if (!doit) {
-        if (st == 0) {
+        int flag = 0;
+        if (lane == 0) {
           const int64_t mine = min(last, it1 - 1) - max(first, it0) + 1;
           __threadfence();  // publish this CTA's scores of u
           const int old = atomicAdd(&a.counters[u], (int)mine);
-          s_flag = old + (int)mine == a.nchunk;
-          if (s_flag) {
+          flag = old + (int)mine == a.nchunk;
+          if (flag) {
             __threadfence();  // see the other CTAs' scores of u
             a.counters[u] = 0;  // ready for the next call
           }
         }
-        sbar();
-        doit = s_flag;
+        doit = __shfl_sync(0xffffffffu, flag, 0) != 0;
         if (doit) {
-          const int nvalid = unit_nvalid(a, u / a.Hkv);
           const float* scu = a.scores + (int64_t)u * a.nblk_cap;
-          for (int j = st; j < nvalid; j += kSelThreads) keys[j] = score_key(__ldcg(scu + j));
-          sbar();
+          for (int j = lane; j < nvalid; j += 32) keys[j] = score_key(__ldcg(scu + j));
+          __syncwarp();
         }
       }
-      if (doit) select_unit(a, u, keys, ss);
-      if (st == 0) mbar_arrive(&kempty[kb]);  // the key buffer may be refilled
+      if (doit) select_unit(a, u, keys, nvalid, sw, lane);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&kempty[kb]);  // the key buffer may be refilled
     }
     return;
   }
@@ -524,20 +559,25 @@ __global__ void __launch_bounds__(kThreadsAll, 1) score_topk_kernel(const __grid
   int ucur = -1, kb = 0;
   bool split = false;
   uint32_t bmm[16][2], bme[8][2];
+  // item it0 + i is chunk ch of unit u, in stage st
+  int u = (int)(it0 / a.nchunk), ch = (int)(it0 - (int64_t)u * a.nchunk), st = 0;
+  int nvalid = unit_nvalid(a, u / a.Hkv);
   for (int64_t i = 0; i < it1 - it0; ++i) {
-    const int64_t item = it0 + i;
-    const int u = (int)(item / a.nchunk), ch = (int)(item - (int64_t)u * a.nchunk);
-    const int nvalid = unit_nvalid(a, u / a.Hkv);
-    const int st = (int)(i % a.stages);
+    if (ch == a.nchunk) {
+      ch = 0;
+      ++u;
+      nvalid = unit_nvalid(a, u / a.Hkv);
+    }
     const bool landed = mbar_wait(&full_bar[st], (uint32_t)((i / a.stages) & 1));
     if (!landed && lane == 0) report(a.status, SCOUT_DEV_TIMEOUT);
     const uint8_t* sp = ring + st * kStageBytesT;
     if (u != ucur) {  // the unit's first item in this range
       ucur = u;
       const int e = u - u_first;
-      kb = e & 1;
+      kb = e % a.nkbuf;
       split = (int64_t)u * a.nchunk < it0 || (int64_t)u * a.nchunk + a.nchunk - 1 >= it1;
-      if (!mbar_wait(&kempty[kb], ((uint32_t)(e >> 1) & 1u) ^ 1u) && lane == 0) report(a.status, SCOUT_DEV_TIMEOUT);
+      if (!mbar_wait(&kempty[kb], ((uint32_t)(e / a.nkbuf) & 1u) ^ 1u) && lane == 0)
+        report(a.status, SCOUT_DEV_TIMEOUT);
       if (ch * kChunk < nvalid && landed) {
         const __nv_bfloat16* qs = reinterpret_cast<const __nv_bfloat16*>(sp + 4 * kBoxBytes);
         if (KIND == SCOUT_DIGEST_MINMAX) {
@@ -576,6 +616,8 @@ __global__ void __launch_bounds__(kThreadsAll, 1) score_topk_kernel(const __grid
       mbar_arrive(&empty_bar[st]);
       if (ch == a.nchunk - 1 || i == it1 - it0 - 1) mbar_arrive(&kfull[kb]);  // this warp's keys of u are in
     }
+    ++ch;
+    if (++st == a.stages) st = 0;
   }
 }
 
@@ -654,11 +696,24 @@ extern "C" int scout_score_topk(int kind, const void* q, const void* digest, con
                      CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
       return SCOUT_ERR_UNSUPPORTED;
   }
-  const size_t keys_bytes = (size_t)(2 * align4(nblk_cap) + 2 * align4(a.words) + kBins) * sizeof(uint32_t);
-  // per-block limit 232448 bytes (227 KiB) covers static (< 512 bytes here) and dynamic shared memory
-  const size_t budget = 232448 - 512 - 1024 - keys_bytes;
-  a.stages = (int)min((size_t)kMaxStagesT, budget / kStageBytesT);
-  const size_t smem = 1024 + (size_t)a.stages * kStageBytesT + keys_bytes;
+  // per-block limit 232448 bytes (227 KiB) covers static (< 512 bytes here) and dynamic shared
+  // memory: the most ring stages, then the most key buffers (at least two) that fit
+  const size_t avail = 232448 - 512 - 1024;
+  const size_t kbuf_bytes = (size_t)align4(nblk_cap) * 4, selw_bytes = (size_t)selwarp_words(a.words) * 4;
+  auto need = [&](int stages, int nkbuf) {
+    return (size_t)stages * kStageBytesT + nkbuf * kbuf_bytes + min(kSelWarps, nkbuf - 1) * selw_bytes;
+  };
+  a.stages = 0;
+  for (int st = kMaxStagesT; st >= 1 && a.stages == 0; --st)
+    for (int nk = kMaxKeyBufs; nk >= 2; --nk)
+      if (need(st, nk) <= avail) {
+        a.stages = st;
+        a.nkbuf = nk;
+        break;
+      }
+  if (a.stages == 0) return SCOUT_ERR_UNSUPPORTED;
+  a.nsel = min(kSelWarps, a.nkbuf - 1);
+  const size_t smem = 1024 + need(a.stages, a.nkbuf);
   auto kern = kind == SCOUT_DIGEST_MINMAX ? score_topk_kernel<SCOUT_DIGEST_MINMAX> : score_topk_kernel<SCOUT_DIGEST_MEAN>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess ||
       cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, 100) != cudaSuccess)
