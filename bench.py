@@ -45,7 +45,7 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing leg")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="target oracle time for cpu_baseline")
     ap.add_argument("--serial", action="store_true", help="one stream, full grids (no overlap)")
-    ap.add_argument("--split", default=None, help="CTAs of the selection,attention kernels (default 100,52)")
+    ap.add_argument("--split", default=None, help="CTAs of the selection,attention kernels (default 80,72)")
     a = ap.parse_args()
     a.warmup = max(a.warmup, 3)
     return a
@@ -338,7 +338,7 @@ def traffic_of(kernel):
     """DRAM bytes per launch from the committed ncu summary, if the kernel source is unchanged since."""
     import hashlib
 
-    path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    path = os.path.join(ROOT, "profiles", "dram_traffic_per_launch_qwen3_14b_b40_t32k.txt")
     if not os.path.exists(path):
         return None
     with open(path) as f:
@@ -383,7 +383,7 @@ def main():
         ms = r["kern_ms"][name]
         gbs = nbytes[name] / (ms / 1e3) / 1e9
         kernels[name] = {"ms": ms, "bytes": nbytes[name], "GB_s": gbs, "frac_of_hbm_peak": gbs / peak}
-    dom = max(KERNELS, key=lambda k: r["kern_ms"][k])  # the longest launch of the step
+    dom = max(KERNELS, key=lambda k: nbytes[k])  # the kernel that moves the most bytes
     ach = kernels[dom]["GB_s"]
     src = f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured" else "fallback 6.8 TB/s"
     roof = {"kernel": dom, "bound": "hbm", "achieved": ach, "peak": peak, "unit": "GB/s", "frac": ach / peak,

@@ -2,7 +2,7 @@
 
     python -m block_sparse_kv_pred_gb300.profile_step --config qwen3_14b --pool-slots 65536 --steps 3
 
-``--pool-slots`` makes blocks share K/V pool slots so the device holds about
+``--pool-slots`` (0: one slot per block) makes blocks share K/V pool slots so the device holds about
 1.3 GB instead of 5.4 GB while every kernel keeps the launch configuration,
 the digest size and the block counts of the full workload.  Outputs are not
 checked (the aliased pool does not hold each block's own keys).
@@ -25,7 +25,7 @@ def main():
     ap.add_argument("--serial", action="store_true", help="one stream, full grids")
     a = ap.parse_args()
     shape = W.CONFIGS[a.config]()
-    wl, t, step = setup_step(shape, torch.device("cuda", 0), pool_slots=a.pool_slots, serial=a.serial)
+    wl, t, step = setup_step(shape, torch.device("cuda", 0), pool_slots=a.pool_slots or None, serial=a.serial)
     ev = torch.cuda.Event()
     ev.record()
     step.begin(ev)
