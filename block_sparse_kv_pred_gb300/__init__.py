@@ -59,6 +59,7 @@ _SIGS = {
     "scout_merge": ([_p, _p, _p, _p, _i, _i, _p, _p, _p], _i),
     "scout_recall_async": ([_p, _i, _p, _p, _p, _p, _i64, _i, _i, _i, _i, _i, _p, _p, _p], _i),
     "scout_commit_residency": ([_p, _i, _p, _p, _i64, _i, _i, _i, _p, _p], _i),
+    "scout_plan_recall": ([_p, _p, _p, _p, _p, _i, _i, _i, _p, _i, _p], _i),
 }
 
 
@@ -266,6 +267,30 @@ def commit_residency(d_ops, page_table, resident_bits, n_slots, B, Hkv, wait_eve
                                         _dev(resident_bits, torch.int32, "resident_bits"), n_slots, B, Hkv,
                                         page_table.shape[-1], None if wait_event is None else wait_event.cuda_event,
                                         _stream(stream)), "scout_commit_residency")
+
+
+def plan_recall(scores, topk_idx, topk_count, resident_bits, page_table, k):
+    """Recall ops (unit, block, slot, evicted block) for one recall step, planned on the host.
+
+    All arguments are host numpy arrays: scores fp32 [units][nblk_cap], topk_idx int32
+    [units][k], topk_count int32 [units], resident_bits uint32 [units][words], page_table
+    int32 [units][nblk_cap].  Returns an int32 array [n][4].
+    """
+    import numpy as np
+
+    sc = np.ascontiguousarray(scores, dtype=np.float32)
+    ti = np.ascontiguousarray(topk_idx, dtype=np.int32)
+    tc = np.ascontiguousarray(topk_count, dtype=np.int32)
+    rb = np.ascontiguousarray(resident_bits, dtype=np.uint32)
+    pt = np.ascontiguousarray(page_table, dtype=np.int32)
+    units, nblk = sc.shape
+    cap = max(1, int(tc.clip(0, k).sum()))
+    ops = (RecallOp * cap)()
+    n = ctypes.c_int(0)
+    ptr = lambda a: a.ctypes.data_as(ctypes.c_void_p)  # noqa: E731
+    _check(lib().scout_plan_recall(ptr(sc), ptr(ti), ptr(tc), ptr(rb), ptr(pt), units, nblk, k, ops, cap,
+                                   ctypes.byref(n)), "scout_plan_recall")
+    return np.array([[o.unit, o.block, o.slot, o.evict_block] for o in ops[: n.value]], dtype=np.int32).reshape(-1, 4)
 
 
 class Prepared:

@@ -7,6 +7,9 @@
 // consecutive blocks landing in consecutive slots).  Page table and residency
 // bits change only in scout_commit_residency, which the caller orders after the
 // copies' event, so a block never looks resident before its bytes have landed.
+#include <algorithm>
+#include <vector>
+
 #include "common.cuh"
 
 namespace scout {
@@ -87,4 +90,53 @@ extern "C" int scout_commit_residency(const scout_recall_op* d_ops, int n_ops, i
   commit_kernel<<<1, 1024, 0, stream>>>(d_ops, n_ops, page_table, resident_bits, n_slots, B * Hkv, nblk_cap,
                                         (nblk_cap + 31) / 32);
   return launch_status();
+}
+
+// Host-side plan of one recall step.  Per unit: the selected blocks that are not
+// resident come in, the most important first (score descending, lower block first);
+// each takes the slot of a resident block that is not selected, the least important
+// first (score ascending, lower block first); the unit's resident set keeps its size.
+extern "C" int scout_plan_recall(const float* scores, const int32_t* topk_idx, const int32_t* topk_count,
+                                 const uint32_t* resident_bits, const int32_t* page_table, int units, int nblk_cap,
+                                 int k, scout_recall_op* ops, int max_ops, int* n_ops) {
+  if (scores == nullptr || topk_idx == nullptr || topk_count == nullptr || resident_bits == nullptr ||
+      page_table == nullptr || n_ops == nullptr || units <= 0 || nblk_cap <= 0 || k <= 0 || max_ops < 0 ||
+      (ops == nullptr && max_ops > 0))
+    return SCOUT_ERR_INVALID_ARG;
+  const int words = (nblk_cap + 31) / 32;
+  std::vector<char> sel(nblk_cap);
+  std::vector<int> in, ev;
+  int n = 0;
+  for (int u = 0; u < units; ++u) {
+    const float* U = scores + (int64_t)u * nblk_cap;
+    const uint32_t* bits = resident_bits + (int64_t)u * words;
+    auto resident = [&](int j) { return ((bits[j >> 5] >> (j & 31)) & 1u) != 0; };
+    std::fill(sel.begin(), sel.end(), 0);
+    const int cnt = std::min(std::max(topk_count[u], 0), k);
+    for (int i = 0; i < cnt; ++i) {
+      const int j = topk_idx[(int64_t)u * k + i];
+      if (j < 0 || j >= nblk_cap) return SCOUT_ERR_INVALID_ARG;
+      sel[j] = 1;
+    }
+    in.clear();
+    ev.clear();
+    for (int j = 0; j < nblk_cap; ++j) {
+      if (sel[j] && !resident(j)) in.push_back(j);
+      if (!sel[j] && resident(j)) ev.push_back(j);
+    }
+    // exact comparisons of the fp32 scores; equal scores fall back to the block index
+    std::stable_sort(in.begin(), in.end(), [&](int x, int y) { return U[x] > U[y]; });
+    std::stable_sort(ev.begin(), ev.end(), [&](int x, int y) { return U[x] < U[y]; });
+    const size_t m = std::min(in.size(), ev.size());
+    const int first = n;
+    for (size_t i = 0; i < m; ++i) {
+      const int32_t slot = page_table[(int64_t)u * nblk_cap + ev[i]];
+      if (slot < 0) return SCOUT_ERR_INVALID_ARG;  // a resident block must own a slot
+      if (n >= max_ops) return SCOUT_ERR_WORKSPACE;
+      ops[n++] = scout_recall_op{u, in[i], slot, ev[i]};
+    }
+    std::sort(ops + first, ops + n, [](const scout_recall_op& x, const scout_recall_op& y) { return x.block < y.block; });
+  }
+  *n_ops = n;
+  return SCOUT_OK;
 }

@@ -267,6 +267,25 @@ int scout_commit_residency(const scout_recall_op* d_ops, int n_ops, int32_t* pag
                            int64_t n_slots, int B, int Hkv, int nblk_cap, cudaEvent_t wait_event,
                            cudaStream_t stream);
 
+/* Plan of one recall step (host code, HOST memory in and out).
+ * ScoutAttention (arXiv HTML), section 3.4 says only that important blocks are
+ * recalled periodically; the policy here is a reading: per unit u, the selected
+ * blocks that are not resident come in, the most important first (score
+ * descending, lower block first), each into the slot of a resident block that is
+ * not selected, the least important first (score ascending, lower block first);
+ * the unit's resident set keeps its size and the recall stops when either side
+ * runs out.
+ * scores fp32 [units][nblk_cap] (the pooled scores scout_score_topk writes, -inf
+ * past the valid blocks), topk_idx int32 [units][k] and topk_count [units],
+ * resident_bits uint32 [units][ceil(nblk_cap / 32)], page_table int32
+ * [units][nblk_cap].  Writes up to max_ops ops (per unit in ascending block
+ * order) and their number to *n_ops.  SCOUT_ERR_WORKSPACE if more are needed;
+ * SCOUT_ERR_INVALID_ARG for a list entry out of range or a resident block
+ * without a slot. */
+int scout_plan_recall(const float* scores, const int32_t* topk_idx, const int32_t* topk_count,
+                      const uint32_t* resident_bits, const int32_t* page_table, int units, int nblk_cap, int k,
+                      scout_recall_op* ops, int max_ops, int* n_ops);
+
 #ifdef __cplusplus
 }
 #endif

@@ -163,6 +163,48 @@ def delta_list(cpu, prev_cpu) -> np.ndarray:
 
 
 # ---------------------------------------------------------------------------
+# asynchronous periodic recall  (section 3.4)
+# ---------------------------------------------------------------------------
+def recall_plan(U, selected, resident_mask, slot_of):
+    """One unit's recall at a recall step (section 3.4: important blocks are copied back
+    into GPU memory).  Reading of the policy, which the pages leave open:
+
+    * the blocks brought in are the selected blocks that are not resident, the most
+      important first (score descending, lower index first);
+    * each takes the pool slot of a resident block that is not selected, the least
+      important first (score ascending, lower index first), so the resident set keeps its
+      size;
+    * the recall stops when either side runs out.
+
+    U: scores per block (all blocks of the unit's table); selected: the top-k blocks;
+    resident_mask: bool per block; slot_of: pool slot per block.  Returns the ops
+    (block, slot, evicted block) in ascending order of the block brought in.
+    """
+    U = np.asarray(U, dtype=np.float64)
+    sel = set(int(j) for j in selected)
+    incoming = sorted((int(j) for j in sel if not resident_mask[j]), key=lambda j: (-U[j], j))
+    evictable = sorted((j for j in range(len(resident_mask)) if resident_mask[j] and j not in sel),
+                       key=lambda j: (U[j], j))
+    n = min(len(incoming), len(evictable))
+    ops = [(incoming[i], int(slot_of[evictable[i]]), evictable[i]) for i in range(n)]
+    return sorted(ops)
+
+
+def apply_recall(slot_of, resident_mask, ops):
+    """Page-table and residency of the unit after its recall ops: evictions first, then
+    the recalled blocks take their slots."""
+    slot_of = np.array(slot_of, copy=True)
+    resident_mask = np.array(resident_mask, dtype=bool, copy=True)
+    for _, _, e in ops:
+        slot_of[e] = -1
+        resident_mask[e] = False
+    for b, slot, _ in ops:
+        slot_of[b] = slot
+        resident_mask[b] = True
+    return slot_of, resident_mask
+
+
+# ---------------------------------------------------------------------------
 # partial attention and merge  (section 3.2; FlashAttention / online softmax)
 # ---------------------------------------------------------------------------
 def block_tokens(blocks, P: int, seq_len: int) -> np.ndarray:

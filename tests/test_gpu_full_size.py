@@ -1,0 +1,142 @@
+"""Full-size workloads on sampled units: the Qwen3-14B-shaped layer in the launch
+configuration bench.py times (two streams, capped grids), the Qwen3-8B-shaped layer,
+and the stress shapes (page 16/32/64, budgets 512/2048/8192, min/max and mean digests,
+128K context, plus the dense edge case), each checked against the fp64 oracle on a
+handful of (sequence, KV head) units the oracle finishes in seconds."""
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+import block_sparse_kv_pred_gb300 as bs
+from block_sparse_kv_pred_gb300 import workload as W
+from block_sparse_kv_pred_gb300.step import SPLIT, setup_step
+from block_sparse_kv_pred_gb300.workload import device as WD
+from _parity import bf16_bits, check_attention, check_selection, ensure_built, to_dev
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    ensure_built()
+
+
+def _sample(U):
+    return sorted({0, 1, U // 3, U // 2, U - 1})
+
+
+def _check_unit(wl, u, q_sel_bits, kind, topk, tc, res, rc, cpu, cc, O_out, L_out, o_cpu, l_cpu):
+    """Selection of unit u against the oracle's, then the output over the GPU's own resident
+    list (merged with the CPU partial) against the oracle's attention over that list."""
+    s = wl.s
+    b, kvh = divmod(u, s.Hkv)
+    L = int(wl.seq_len[b])
+    Kb = wl.unit_kv(u)
+    qs = O.bf16_to_f64(q_sel_bits)
+    if kind == "minmax":
+        mn, mx = O.digest_minmax(Kb, L, s.P)
+        Uref = O.pool_group(O.scores_minmax(qs, mn, mx))
+    else:
+        Uref = O.pool_group(O.scores_mean(qs, O.digest_mean(Kb, L, s.P)))
+    S_gpu = topk[u, :tc[u]]
+    if check_selection(Uref, s.k, S_gpu, what=u):  # same set: the lists are bit-exact
+        r_ref, c_ref = O.split_residency(O.select_topk(Uref, s.k), wl.resident[u].astype(bool))
+        assert list(res[u, :rc[u]]) == list(r_ref) and list(cpu[u, :cc[u]]) == list(c_ref), u
+    else:  # a near-tie: the split of the GPU's own set must still be exact
+        r_ref, c_ref = O.split_residency(S_gpu, wl.resident[u].astype(bool))
+        assert list(res[u, :rc[u]]) == list(r_ref), u
+    assert all(t == -1 for t in topk[u, tc[u]:]) and all(t == -1 for t in res[u, rc[u]:])
+    K, V = O.bf16_to_f64(Kb), O.bf16_to_f64(wl.unit_kv(u, "V"))
+    toks = O.block_tokens(res[u, :rc[u]], s.P, L)
+    for h in range(s.G):
+        hq = kvh * s.G + h
+        og, lg = O.attention_partial(O.bf16_to_f64(wl.q[b, hq]), K[toks], V[toks], s.scale)
+        o, l = O.merge(og, lg, o_cpu[b, hq].astype(np.float64), float(l_cpu[b, hq]))
+        check_attention(O_out[b, hq], L_out[b, hq], o, l, what=(u, h))
+
+
+@pytest.mark.parametrize("cfg,serial", [("qwen3_14b", False), ("qwen3_8b", True)])
+def test_full_size_step_sampled(cfg, serial):
+    """Three steps of the decode step at full size; selection with Q_pred, attention with q."""
+    shape = W.CONFIGS[cfg]()
+    wl, t, step = setup_step(shape, torch.device("cuda", 0), serial=serial, split=SPLIT)
+    ev = torch.cuda.Event()
+    ev.record()
+    step.begin(ev)
+    for _ in range(3):
+        step.issue()
+    step.end(None)
+    torch.cuda.synchronize()
+    assert int(t["status"].item()) == 0
+    s = shape
+    par = 1 - (step.i - 1) % 2  # the list set the last attention read
+    grab = lambda n: t[f"{n}{par}"].cpu().numpy().reshape(s.units, -1)  # noqa: E731
+    topk, res, cpu = grab("topk"), grab("res"), grab("cpu")
+    tc, rc, cc = (t[f"{n}_count{par}"].cpu().numpy().reshape(-1) for n in ("topk", "res", "cpu"))
+    qp = bf16_bits(t["Qp"]).reshape(s.B, s.Hq, s.D)
+    O_out, L_out = t["O"].float().cpu().numpy(), t["lse"].cpu().numpy()
+    o_cpu, l_cpu = wl.cpu_partial()
+    for u in _sample(s.units):
+        b, kvh = divmod(u, s.Hkv)
+        _check_unit(wl, u, qp[b, kvh * s.G:(kvh + 1) * s.G], "minmax", topk, tc, res, rc, cpu, cc, O_out, L_out,
+                    o_cpu, l_cpu)
+
+
+STRESS = [(16, 2048, "minmax"), (32, 2048, "minmax"), (64, 2048, "minmax"), (32, 512, "minmax"),
+          (32, 8192, "minmax"), (16, 8192, "mean"), (32, 2048, "mean"), (64, 512, "mean")]
+
+
+@pytest.mark.parametrize("P,budget,kind", STRESS)
+def test_stress_shapes_sampled(P, budget, kind):
+    """B=4 at 128K context: k up to 512 blocks, nblk up to 8192, both digest kinds."""
+    s = W.stress(P, budget, kind)
+    wl = W.Workload(s)
+    d = WD.materialize(wl, with_gemm=False)
+    nb = s.nblk
+    if kind == "minmax":
+        dg = torch.empty((s.B, s.Hkv, nb, 2, s.D), dtype=torch.bfloat16, device="cuda")
+    else:
+        dg = torch.empty((s.B, s.Hkv, nb, s.D), dtype=torch.float32, device="cuda")
+    bs.build_digest(kind, d["K_pool"], d["page_table"], d["seq_len"], s.B, s.Hkv, P, dg)
+    ws = bs.score_topk_workspace(s.B, s.Hkv, nb)
+    out = bs.score_topk(kind, d["q"], dg, d["seq_len"], d["resident_bits"], s.B, s.Hq, s.Hkv, P, nb, s.k, ws)
+    wa = bs.sparse_attn_workspace(s.B, s.Hq, s.Hkv, P)
+    O_out, L_out = bs.sparse_attn_merge(d["q"], d["K_pool"], d["V_pool"], d["page_table"], d["seq_len"], out["res"],
+                                        out["res_count"], s.B, s.Hq, s.Hkv, P, s.k, s.scale, wa, d["O_cpu"],
+                                        d["lse_cpu"])
+    torch.cuda.synchronize()
+    grab = lambda n: out[n].cpu().numpy().reshape(s.units, -1)  # noqa: E731
+    cnt = lambda n: out[n].cpu().numpy().reshape(-1)  # noqa: E731
+    o_cpu, l_cpu = wl.cpu_partial()
+    for u in (0, s.units - 1):
+        b, kvh = divmod(u, s.Hkv)
+        _check_unit(wl, u, wl.q[b, kvh * s.G:(kvh + 1) * s.G], kind, grab("topk"), cnt("topk_count"), grab("res"),
+                    cnt("res_count"), grab("cpu"), cnt("cpu_count"), O_out.float().cpu().numpy(),
+                    L_out.cpu().numpy(), o_cpu, l_cpu)
+
+
+def test_dense_edge_case_at_128k():
+    """top-k = every block and everything resident: the output is full softmax attention."""
+    s = W.Shape("dense_128k", B=2, Hq=40, Hkv=8, T=131072 - 7, P=32, k=4096, resident_frac=1.0)
+    wl = W.Workload(s)
+    d = WD.materialize(wl, with_gemm=False)
+    dg = torch.empty((s.B, s.Hkv, s.nblk, 2, s.D), dtype=torch.bfloat16, device="cuda")
+    bs.build_digest("minmax", d["K_pool"], d["page_table"], d["seq_len"], s.B, s.Hkv, s.P, dg)
+    ws = bs.score_topk_workspace(s.B, s.Hkv, s.nblk)
+    out = bs.score_topk("minmax", d["q"], dg, d["seq_len"], d["resident_bits"], s.B, s.Hq, s.Hkv, s.P, s.nblk, s.k,
+                        ws)
+    wa = bs.sparse_attn_workspace(s.B, s.Hq, s.Hkv, s.P)
+    Og, Lg = bs.sparse_attn(d["q"], d["K_pool"], d["V_pool"], d["page_table"], d["seq_len"], out["res"],
+                            out["res_count"], s.B, s.Hq, s.Hkv, s.P, s.k, s.scale, wa)
+    torch.cuda.synchronize()
+    assert torch.all(out["res_count"] == s.nblk) and torch.all(out["cpu_count"] == 0)
+    Og, Lg = Og.cpu().numpy(), Lg.cpu().numpy()
+    for u in (3, s.units - 1):
+        b, kvh = divmod(u, s.Hkv)
+        L = int(wl.seq_len[b])
+        K, V = O.bf16_to_f64(wl.unit_kv(u))[:L], O.bf16_to_f64(wl.unit_kv(u, "V"))[:L]
+        for h in (0, s.G - 1):
+            hq = kvh * s.G + h
+            o, l = O.attention_partial(O.bf16_to_f64(wl.q[b, hq]), K, V, s.scale)
+            check_attention(Og[b, hq], Lg[b, hq], o, l, what=(u, h))

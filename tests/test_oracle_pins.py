@@ -378,3 +378,48 @@ def test_layout_constant_matches_the_pages():
     assert per_token * s.P == g["page_bytes"] and s.P == g["page_tokens"]
     ev = read_golden("evaluation_setup.txt")
     assert s.k * s.P == ev["budget_tokens"] and s.P == ev["block_size"]
+
+
+# ---------------------------------------------------------------------------
+# recall (section 3.4): properties any correct plan has, and a hand example
+# ---------------------------------------------------------------------------
+def test_recall_plan_hand_example_with_ties():
+    # blocks 0..7; resident {0, 1, 2, 5}; selected {1, 3, 4, 6}
+    U = [0.5, 9.0, 0.5, 7.0, 8.0, 0.1, 7.0, 3.0]
+    res = np.array([1, 1, 1, 0, 0, 1, 0, 0], dtype=bool)
+    slot = np.array([10, 11, 12, -1, -1, 15, -1, -1])
+    ops = O.recall_plan(U, [1, 3, 4, 6], res, slot)
+    # incoming by importance: 4 (8.0), 3 (7.0, lower index), 6 (7.0); evict by least importance:
+    # 5 (0.1), 0 (0.5, lower index), 2 (0.5)
+    assert ops == [(3, 10, 0), (4, 15, 5), (6, 12, 2)]
+    slot2, res2 = O.apply_recall(slot, res, ops)
+    assert list(np.flatnonzero(res2)) == [1, 3, 4, 6]
+    assert sorted(slot2[res2]) == [10, 11, 12, 15]
+
+
+@pytest.mark.parametrize("seed", range(20))
+def test_recall_plan_properties_random(seed):
+    rng = np.random.default_rng(seed)
+    n = int(rng.integers(1, 40))
+    U = np.round(rng.standard_normal(n), 1)  # coarse values: many ties
+    res = rng.random(n) < rng.random()
+    slot = np.where(res, rng.permutation(1000)[:n], -1)
+    sel = O.select_topk(U, int(rng.integers(1, n + 1)))
+    ops = O.recall_plan(U, sel, res, slot)
+    incoming = [j for j in sel if not res[j]]
+    evictable = [j for j in range(n) if res[j] and j not in set(sel)]
+    assert len(ops) == min(len(incoming), len(evictable))
+    brought = [b for b, _, _ in ops]
+    evicted = [e for _, _, e in ops]
+    assert brought == sorted(brought) and set(brought) <= set(incoming) and set(evicted) <= set(evictable)
+    key_in = lambda j: (-U[j], j)  # noqa: E731  (importance order of the pages' reading)
+    key_ev = lambda j: (U[j], j)  # noqa: E731
+    for j in set(incoming) - set(brought):  # every block left out is less important than every one brought
+        assert all(key_in(b) < key_in(j) for b in brought)
+    for j in set(evictable) - set(evicted):  # every kept block is more important than every evicted one
+        assert all(key_ev(e) < key_ev(j) for e in evicted)
+    slot2, res2 = O.apply_recall(slot, res, ops)
+    assert res2.sum() == res.sum()  # the pool keeps its size
+    assert sorted(slot2[res2]) == sorted(slot[res])  # the same slots, reassigned
+    if len(evictable) >= len(incoming):
+        assert all(res2[j] for j in sel)
