@@ -116,6 +116,18 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
+def max_over_ranks(x: float, device) -> float:
+    """The largest of every rank's x (x itself on one rank)."""
+    import torch
+    import torch.distributed as dist
+
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return x
+    m = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(m, op=dist.ReduceOp.MAX)
+    return float(m.item())
+
+
 # ---------------------------------------------------------------------------
 # libscout arm
 # ---------------------------------------------------------------------------
@@ -172,10 +184,7 @@ def run_scout(args, rank, world, local):
 
     ms = e_start.elapsed_time(e_end) / args.steps
     kern_ms = {name: statistics.mean(e[name][0].elapsed_time(e[name][1]) for e in ev) for name in KERNELS}
-    if world > 1:
-        m = torch.tensor([ms], device=device)
-        dist.all_reduce(m, op=dist.ReduceOp.MAX)
-        ms = float(m.item())
+    ms = max_over_ranks(ms, device)
     value = world * s.B * s.Hq / (ms / 1e3)
 
     e2e = run_e2e(args, t, step, s, world, device)
@@ -216,11 +225,7 @@ def run_e2e(args, t, step, s, world, device):
             h.copy_(t[n] if n in t else t[f"{n}{par}"], non_blocking=True)
         ev[i][1].record(cur)
     torch.cuda.synchronize()
-    ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
-    if world > 1:
-        m = torch.tensor([ms], device=device)
-        dist.all_reduce(m, op=dist.ReduceOp.MAX)
-        ms = float(m.item())
+    ms = max_over_ranks(statistics.mean(a.elapsed_time(b) for a, b in ev), device)
     return {"value": world * s.B * s.Hq / (ms / 1e3), "unit": "query-heads/s", "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "ms_per_step": ms, "steps": steps}
 

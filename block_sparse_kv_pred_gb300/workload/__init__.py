@@ -295,6 +295,37 @@ class Workload:
         r0, r1 = rows.start, rows.stop
         return normal_bf16(s.seed, STREAM_W, (r1 - r0, s.hidden), sigma=s.w_sigma, offset=r0 * s.hidden)
 
+    # -- multi-step query walk ----------------------------------------------
+    def walk(self, steps: int, cosine: float = 0.93, noise: float = 0.3):
+        """True and predicted queries of decode steps 0 .. steps-1, bf16 bits [steps][B][Hq][D].
+
+        q_0 is ``self.q``; q_t = sqrt(D) * normalize(q^_{t-1} + noise * n_t / sqrt(D)) with n_t
+        ~ N(0, I) and q^ the unit vector (a step cosine near 0.96), rounded to bf16 each step.  Q_pred_t has the norm
+        of q_t and cosine ``cosine`` to it: ||q_t|| (c q^_t + sqrt(1 - c^2) w_t) with w_t a
+        seeded unit vector orthogonal to q_t.  (Table 1 of the pages gives cosines 0.93-0.97
+        between predicted and true queries; the sweep uses the smallest.)
+        """
+        s = self.s
+        n = s.B * s.Hq * s.D
+        sqd = np.sqrt(np.float64(s.D))
+        q = bf16_to_f32(self.q).astype(np.float64).reshape(s.B, s.Hq, s.D)
+        qs, ps = [], []
+        for t in range(steps):
+            if t > 0:
+                z = irwin_hall(s.seed, STREAM_WALK, np.arange(t * n, (t + 1) * n, dtype=np.uint64))
+                q = q / np.linalg.norm(q, axis=-1, keepdims=True) + noise * z.astype(np.float64).reshape(q.shape) / sqd
+                q = sqd * q / np.linalg.norm(q, axis=-1, keepdims=True)
+                q = bf16_to_f32(f32_to_bf16(q.astype(np.float32))).astype(np.float64)
+            qh = q / np.linalg.norm(q, axis=-1, keepdims=True)
+            w = irwin_hall(s.seed, STREAM_QPRED, np.arange(t * n, (t + 1) * n, dtype=np.uint64))
+            w = w.astype(np.float64).reshape(q.shape)
+            w = w - (w * qh).sum(-1, keepdims=True) * qh
+            w = w / np.linalg.norm(w, axis=-1, keepdims=True)
+            pred = np.linalg.norm(q, axis=-1, keepdims=True) * (cosine * qh + np.sqrt(1.0 - cosine ** 2) * w)
+            qs.append(f32_to_bf16(q.astype(np.float32)))
+            ps.append(f32_to_bf16(pred.astype(np.float32)))
+        return np.stack(qs), np.stack(ps)
+
     # -- CPU-side partial (stands in for the CPU worker's output) -----------
     def cpu_partial(self):
         """(O_cpu fp32 [B][Hq][D], LSE_cpu fp32 [B][Hq]) drawn from the generator."""

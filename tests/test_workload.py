@@ -45,3 +45,19 @@ def test_workload_structure():
     non_heavy = ~np.repeat(wl.heavy[1].astype(bool), s.P)
     sd = Kf[non_heavy].std(axis=0)
     assert np.all(sd[wl.outliers] > 6.0) and np.median(sd) < 1.2
+
+
+def test_query_walk_cosines_and_norms():
+    """The walk keeps ||q|| = sqrt(D), steps at cosine ~0.96, and Q_pred sits at cosine 0.93
+    (the smallest value of the pages' Table 1) from the true query."""
+    wl = W.Workload(W.tiny())
+    q, p = wl.walk(6)
+    f = lambda a: W.bf16_to_f32(a).astype(np.float64)  # noqa: E731
+    cos = lambda a, b: (a * b).sum(-1) / np.linalg.norm(a, axis=-1) / np.linalg.norm(b, axis=-1)  # noqa: E731
+    assert np.array_equal(q[0], wl.q)
+    for t in range(1, 6):
+        assert abs(cos(f(q[t]), f(q[t - 1])).mean() - 1 / np.sqrt(1.09)) < 0.02
+        assert np.allclose(cos(f(q[t]), f(p[t])), 0.93, atol=3e-3)
+        assert np.allclose(np.linalg.norm(f(q[t]), axis=-1), np.sqrt(128), rtol=5e-3)
+    q2, p2 = wl.walk(6)
+    assert np.array_equal(q, q2) and np.array_equal(p, p2)
