@@ -1,13 +1,14 @@
 #!/usr/bin/env python
 """Decode-step benchmark of libscout on the Qwen3-14B-shaped layer.
 
-One step = the whole GPU hot path of one layer's decode step, issued as two
-streams on disjoint SMs (layer-ahead prediction, ScoutAttention Algorithm 1):
+One step = the whole GPU hot path of one layer's decode step, issued as three
+streams (layer-ahead prediction, ScoutAttention Algorithm 1), the persistent
+kernels on disjoint SMs:
   selection stream: predict_q (Q_pred = X W_Q^T, 40 x 5120 x 5120), then
     score_topk (digest scores with Q_pred, top-64 of 1024 blocks, residency split);
-  attention stream: build_digest (append: the tail block of every (sequence, KV
-    head)), then sparse_attn_merge (true query over the resident blocks the
-    previous step selected, merged with the CPU partial).
+  attention stream: sparse_attn_merge (true query over the resident blocks the
+    previous step selected, merged with the CPU partial);
+  append stream: build_digest (append: the tail block of every (sequence, KV head)).
 Metric: decode-attention query-heads per second (B * Hq per step, summed over ranks).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--config qwen3_14b] [--impl scout|reference]
@@ -334,7 +335,7 @@ def config_of(s, world, split=None):
             "digest": s.kind, "gemm_mnk": [s.B, s.Hq * s.D, s.hidden],
             "l2": "not flushed: one step reads inputs larger than L2 (see step_input_bytes), in an order "
                   "that evicts each input before its next use",
-            "streams": f"selection on {split[0]} CTAs || attention on {split[1]} CTAs" if split
+            "streams": f"selection on {split[0]} CTAs || attention on {split[1]} CTAs || digest append" if split
             else "one stream",
             "parallelism": f"independent replicas x{world} (one batch of sequences per GPU)"}
 

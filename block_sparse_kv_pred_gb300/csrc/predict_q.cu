@@ -18,7 +18,7 @@ namespace {
 
 constexpr int kBM = 128;      // W rows per CTA (MMA M)
 constexpr int kBK = 64;       // k columns per stage (one 128-byte swizzle atom of bf16)
-constexpr int kStages = 6;
+constexpr int kStages = 16;  // upper bound; the ring takes what shared memory holds
 constexpr int kThreadsQ = 128;
 constexpr int kMaxN = 256;    // padded batch (MMA N) limit
 constexpr int kWTileBytes = kBM * kBK * 2;  // 16 KiB
@@ -239,7 +239,7 @@ extern "C" int scout_predict_q(const void* X, const void* W, void* Q, int M, int
   a.kblocks = K / kBK;
   a.x_tile_bytes = (a.n_pad * 128 + 1023) / 1024 * 1024;
   const int stage_bytes = kWTileBytes + a.x_tile_bytes;
-  a.stages = min(kStages, (200 * 1024) / stage_bytes);
+  a.stages = min(kStages, (224 * 1024) / stage_bytes);  // ~220 KB in flight per SM
   a.status = dev_status;
   const int tiles = N / kBM;
   const int cap = launch != nullptr && launch->max_ctas > 0 ? launch->max_ctas : sm_count();

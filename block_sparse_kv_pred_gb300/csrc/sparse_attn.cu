@@ -26,7 +26,18 @@
 namespace scout {
 namespace {
 
-constexpr int kConsumerWarps = 4;
+// Consumer warps and tokens per stage: four warps (one per scheduler) with 32-token
+// stages, three per warp in a 192 KB ring.  (Measured on GB300: eight warps with 16-token
+// stages are ~15% slower on the Qwen3-14B-shaped residency; the per-page overhead doubles
+// and the combine state no longer leaves room for two slots.)
+#ifndef SCOUT_ATTN_CONSUMERS
+#define SCOUT_ATTN_CONSUMERS 4
+#endif
+#ifndef SCOUT_ATTN_SUBPAGE
+#define SCOUT_ATTN_SUBPAGE 32
+#endif
+constexpr int kConsumerWarps = SCOUT_ATTN_CONSUMERS;
+constexpr int kSubTokens = SCOUT_ATTN_SUBPAGE;
 constexpr int kEpilogueWarp = kConsumerWarps;  // combines, writes, fixes up split units
 constexpr int kThreads = (kConsumerWarps + 1) * 32;
 constexpr int kPhaseB = 8;  // page of a batch at which the next batch's page-table loads are issued
@@ -36,13 +47,22 @@ constexpr int kMaxGrid = 1024;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
-// A stage holds K and V of one sub-page of PS tokens (a 64-token block streams as two
-// 32-token sub-pages); every consumer warp owns kPerWarp stages.
+// A stage holds K and V of one sub-page of PS tokens (a block streams as P / PS
+// sub-pages); the ring has S stages and every consumer warp owns kPerWarp of them.
+constexpr int kRingTarget = 192 * 1024;
 template <int P>
+constexpr int big_ring() {  // stages of the 192 KB ring
+  return kRingTarget / (4 * (P < kSubTokens ? P : kSubTokens) * 128) / kConsumerWarps * kConsumerWarps;
+}
+template <int P>
+constexpr int small_ring() {  // two thirds of it, for groups and batches whose combine state is large
+  return big_ring<P>() * 2 / 3 / kConsumerWarps * kConsumerWarps;
+}
+template <int P, int S>
 struct Cfg {
-  static constexpr int PS = P < 32 ? P : 32;         // tokens per stage
-  static constexpr int kSub = P / PS;                // stages per block
-  static constexpr int kStages = P == 16 ? 24 : 12;  // a multiple of the consumer warps
+  static constexpr int PS = P < kSubTokens ? P : kSubTokens;  // tokens per stage
+  static constexpr int kSub = P / PS;                          // stages per block
+  static constexpr int kStages = S;
   static constexpr int kPerWarp = kStages / kConsumerWarps;
   static constexpr int kHalfBytes = PS * 128;        // one 64-column half of a sub-page
   static constexpr int kStageBytes = 4 * kHalfBytes; // K (2 halves) + V (2 halves)
@@ -79,11 +99,11 @@ __device__ __forceinline__ int cta_of(int64_t x, int64_t N, int Gp) {
 }
 __device__ __forceinline__ int64_t range_start(int c, int64_t N, int Gp) { return (int64_t)c * N / Gp; }
 
-// Row address (shared::cta) of token r, 16-byte chunk C (dims 8C..8C+7) in a
-// page stored as two 64-column halves with the 128-byte TMA swizzle.
-template <int P>
+// Row address (shared::cta) of token r, 16-byte chunk C (dims 8C..8C+7) in a sub-page
+// of PS tokens stored as two 64-column halves with the 128-byte TMA swizzle.
+template <int PS>
 __device__ __forceinline__ uint32_t page_addr(uint32_t base, int r, int C) {
-  return base + (uint32_t)((C >> 3) * Cfg<P>::kHalfBytes + r * 128 + ((((C & 7) ^ (r & 7))) << 4));
+  return base + (uint32_t)((C >> 3) * PS * 128 + r * 128 + ((((C & 7) ^ (r & 7))) << 4));
 }
 
 struct WarpState {
@@ -102,10 +122,10 @@ __device__ __forceinline__ uint32_t movmatrix_t(uint32_t x) {
 //   S^T = K Q^T (tokens x heads), online softmax per head (column),
 //   O^T += V^T P^T (dims x heads); P^T reaches the B-operand layout by movmatrix.
 // qb holds Q^T fragments: qb[s] = heads g, dims 16s + 2t (+8).
-template <int P>
+template <int PS>
 __device__ __forceinline__ void attend_page(uint32_t kbase, uint32_t vbase, int ntok, const uint32_t (&qb)[8][2],
                                             float scale_log2, WarpState& st, int lane) {
-  constexpr int MT = Cfg<P>::PS / 16;  // 16-token tiles per stage
+  constexpr int MT = PS / 16;  // 16-token tiles per stage
   const int g = lane >> 2;
   float s[MT][4];
 #pragma unroll
@@ -116,8 +136,8 @@ __device__ __forceinline__ void attend_page(uint32_t kbase, uint32_t vbase, int 
 #pragma unroll
     for (int ks = 0; ks < 8; ks += 2) {
       uint32_t a0, a1, a2, a3, c0, c1, c2, c3;
-      ldsm_x4(page_addr<P>(kbase, r, 2 * ks + (lane >> 4)), a0, a1, a2, a3);
-      ldsm_x4(page_addr<P>(kbase, r, 2 * ks + 2 + (lane >> 4)), c0, c1, c2, c3);
+      ldsm_x4(page_addr<PS>(kbase, r, 2 * ks + (lane >> 4)), a0, a1, a2, a3);
+      ldsm_x4(page_addr<PS>(kbase, r, 2 * ks + 2 + (lane >> 4)), c0, c1, c2, c3);
       mma_bf16(s[mt], a0, a1, a2, a3, qb[ks][0], qb[ks][1]);
       mma_bf16(s2, c0, c1, c2, c3, qb[ks + 1][0], qb[ks + 1][1]);
     }
@@ -176,7 +196,7 @@ __device__ __forceinline__ void attend_page(uint32_t kbase, uint32_t vbase, int 
 #pragma unroll
     for (int md = 0; md < 8; ++md) {
       uint32_t a0, a1, a2, a3;
-      ldsm_x4_t(page_addr<P>(vbase, r, 2 * md + ((lane >> 3) & 1)), a0, a1, a2, a3);
+      ldsm_x4_t(page_addr<PS>(vbase, r, 2 * md + ((lane >> 3) & 1)), a0, a1, a2, a3);
       mma_bf16(st.o[md], a0, a1, a2, a3, bh0, bh1);
       mma_bf16(st.o[md], a0, a1, a2, a3, bl0, bl1);
     }
@@ -184,16 +204,15 @@ __device__ __forceinline__ void attend_page(uint32_t kbase, uint32_t vbase, int 
 }
 
 // One segment's per-warp softmax states, handed from the consumer warps to the
-// epilogue warp through shared memory.  A slot holds m[4][8], l[4][8] and
-// O^T partials o[4][G][128] (fp32); its size depends on G, so two slots fit for the
-// usual GQA groups.
-__host__ __device__ constexpr int slot_floats(int G) { return 64 + kConsumerWarps * G * kD; }
+// epilogue warp through shared memory.  A slot holds m[warps][8], l[warps][8] and
+// O^T partials o[warps][G][128] (fp32); its size depends on G.
+__host__ __device__ constexpr int slot_floats(int G) { return 2 * kConsumerWarps * kMaxG + kConsumerWarps * G * kD; }
 struct SlotView {
   float* base;
   int G;
   __device__ float& m(int w, int h) const { return base[w * kMaxG + h]; }
-  __device__ float& l(int w, int h) const { return base[32 + w * kMaxG + h]; }
-  __device__ float* o(int w, int h) const { return base + 64 + (w * G + h) * kD; }
+  __device__ float& l(int w, int h) const { return base[(kConsumerWarps + w) * kMaxG + h]; }
+  __device__ float* o(int w, int h) const { return base + 2 * kConsumerWarps * kMaxG + (w * G + h) * kD; }
 };
 
 __device__ __forceinline__ int ld_acquire(const int* p) {
@@ -245,11 +264,11 @@ __device__ __forceinline__ void load_q(const AttnArgs& a, int u, int lane, uint3
   }
 }
 
-template <int P>
+template <int P, int S>
 __global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const __grid_constant__ CUtensorMap tmK,
                                                                   const __grid_constant__ CUtensorMap tmV,
                                                                   const AttnArgs a) {
-  using C = Cfg<P>;
+  using C = Cfg<P, S>;
   extern __shared__ uint8_t smem_raw[];
   __shared__ uint64_t full_bar[C::kStages], cfull[kMaxSlots], cempty[kMaxSlots];
   __shared__ int wtot[kThreads / 32];
@@ -616,7 +635,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const __grid_c
         ok = false;  // a copy may still be in flight here: issue nothing more
       } else if (ntok > 0) {
         const uint32_t kb = ring_s + stage * C::kStageBytes;
-        attend_page<P>(kb, kb + 2 * C::kHalfBytes, ntok, qa, a.scale_log2, st, lane);
+        attend_page<C::PS>(kb, kb + 2 * C::kHalfBytes, ntok, qa, a.scale_log2, st, lane);
       }
       // reload the stage with this warp's page k + kPerWarp once every lane is done reading it
       const int64_t kr = k + C::kPerWarp;
@@ -680,9 +699,9 @@ inline size_t counters_bytes(int64_t units) { return (size_t)((units * 4 + 255) 
 constexpr size_t kSlotLseBytes = (size_t)kMaxGrid * 2 * kMaxG * sizeof(float);
 constexpr size_t kSlotOBytes = (size_t)kMaxGrid * 2 * kMaxG * kD * sizeof(float);
 
-template <int P>
+template <int P, int S>
 size_t dyn_smem(int units, int G, int nslots) {
-  return 1024 + Cfg<P>::kRingBytes + (size_t)nslots * slot_floats(G) * sizeof(float) + (size_t)(units + 1) * 4;
+  return 1024 + Cfg<P, S>::kRingBytes + (size_t)nslots * slot_floats(G) * sizeof(float) + (size_t)(units + 1) * 4;
 }
 constexpr size_t kSmemLimit = 232448 - 1024;  // per-block shared memory minus room for static use
 
@@ -698,24 +717,42 @@ bool make_page_map(CUtensorMap* map, const void* pool, int64_t n_slots, int P, i
                       CU_TENSOR_MAP_SWIZZLE_128B) == CUDA_SUCCESS;
 }
 
-template <int P>
-int launch_attn(const void* K_pool, const void* V_pool, AttnArgs a, int max_ctas, cudaStream_t stream) {
-  a.nslots = dyn_smem<P>(a.units, a.G, 2) <= kSmemLimit ? 2 : 1;
-  CUtensorMap tmK, tmV;
-  if (!make_page_map(&tmK, K_pool, a.n_slots, P, Cfg<P>::PS) || !make_page_map(&tmV, V_pool, a.n_slots, P, Cfg<P>::PS))
-    return SCOUT_ERR_UNSUPPORTED;
-  const size_t smem = dyn_smem<P>(a.units, a.G, a.nslots);
-  if (cudaFuncSetAttribute(sparse_attn_kernel<P>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+template <int P, int S>
+int launch_ring(const CUtensorMap& tmK, const CUtensorMap& tmV, AttnArgs a, int max_ctas, cudaStream_t stream) {
+  const size_t smem = dyn_smem<P, S>(a.units, a.G, a.nslots);
+  if (cudaFuncSetAttribute(sparse_attn_kernel<P, S>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
           cudaSuccess ||
-      cudaFuncSetAttribute(sparse_attn_kernel<P>, cudaFuncAttributePreferredSharedMemoryCarveout, 100) != cudaSuccess)
+      cudaFuncSetAttribute(sparse_attn_kernel<P, S>, cudaFuncAttributePreferredSharedMemoryCarveout, 100) !=
+          cudaSuccess)
     return SCOUT_ERR_CUDA;
   int occ = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, sparse_attn_kernel<P>, kThreads, smem) != cudaSuccess ||
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, sparse_attn_kernel<P, S>, kThreads, smem) != cudaSuccess ||
       occ < 1)
     return SCOUT_ERR_CUDA;
   const int grid = min(kMaxGrid, max_ctas > 0 ? max_ctas : sm_count() * occ);
-  sparse_attn_kernel<P><<<grid, kThreads, smem, stream>>>(tmK, tmV, a);
+  sparse_attn_kernel<P, S><<<grid, kThreads, smem, stream>>>(tmK, tmV, a);
   return launch_status();
+}
+
+// The biggest ring, then the most combine slots, that fit in shared memory.
+template <int P>
+int launch_attn(const void* K_pool, const void* V_pool, AttnArgs a, int max_ctas, cudaStream_t stream) {
+  constexpr int SB = big_ring<P>(), SS = small_ring<P>();
+  constexpr int PS = Cfg<P, SB>::PS;
+  CUtensorMap tmK, tmV;
+  if (!make_page_map(&tmK, K_pool, a.n_slots, P, PS) || !make_page_map(&tmV, V_pool, a.n_slots, P, PS))
+    return SCOUT_ERR_UNSUPPORTED;
+  for (int ns = kMaxSlots; ns >= 1; --ns)
+    if (dyn_smem<P, SB>(a.units, a.G, ns) <= kSmemLimit) {
+      a.nslots = ns;
+      return launch_ring<P, SB>(tmK, tmV, a, max_ctas, stream);
+    }
+  for (int ns = kMaxSlots; ns >= 1; --ns)
+    if (dyn_smem<P, SS>(a.units, a.G, ns) <= kSmemLimit) {
+      a.nslots = ns;
+      return launch_ring<P, SS>(tmK, tmV, a, max_ctas, stream);
+    }
+  return SCOUT_ERR_UNSUPPORTED;
 }
 
 // Shared by both entry points: O_part/lse_part for the partial, or (O_cpu, lse_cpu,

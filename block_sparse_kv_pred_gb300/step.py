@@ -8,10 +8,12 @@ is issued as two CUDA streams on disjoint SMs (``scout_launch.max_ctas``):
 * selection stream: Q_pred = X W_Q^T (``scout_predict_q``), then scoring and
   top-k over the next layer's digests (``scout_score_topk``) into list set
   ``i % 2``;
-* attention stream: digest append for the token just written
-  (``scout_build_digest`` on this layer's tail blocks), then attention over
-  the resident blocks of list set ``(i + 1) % 2`` merged with the CPU partial
-  (``scout_sparse_attn_merge``).
+* attention stream: attention over the resident blocks of list set
+  ``(i + 1) % 2`` merged with the CPU partial (``scout_sparse_attn_merge``);
+* append stream: the digest append for the token just written
+  (``scout_build_digest`` on this layer's tail blocks).  Nothing in the step
+  reads it (the next step's selection of this layer does), so its few small
+  CTAs run beside the persistent kernels and its latency is hidden.
 
 Step i's attention reads the lists step i-1 selected; step i's selection
 overwrites the set step i-1's attention read, so each stream waits for the
@@ -27,7 +29,7 @@ from __future__ import annotations
 
 KERNELS = ("build_digest", "predict_q", "score_topk", "sparse_attn_merge")
 # stream of each kernel: 0 = selection (next layer), 1 = attention (this layer)
-STREAM_OF = {"build_digest": 1, "predict_q": 0, "score_topk": 0, "sparse_attn_merge": 1}
+STREAM_OF = {"build_digest": 2, "predict_q": 0, "score_topk": 0, "sparse_attn_merge": 1}
 SPLIT = (80, 72)  # CTAs of the selection and attention kernels when overlapped (152 SMs)
 
 
@@ -68,8 +70,8 @@ class Step:
 
     def issue(self, timing=None):
         """Launch the next step.  ``timing``: optional name -> (start, end) timing events."""
-        i, par = self.i, self.i % 2
-        sA, sB = self.streams[0], self.streams[-1]
+        par = self.i % 2
+        sA, sB, sC = (self.streams * 3)[:3] if self.serial else self.streams
         c = self.calls[par]
 
         def run(name, stream):
@@ -84,7 +86,7 @@ class Step:
             sA.wait_event(self.attn_done[1 - par])  # step i-1's attention has read list set i % 2
         run("score_topk", sA)
         self.sel_done[par].record(sA)
-        run("build_digest", sB)
+        run("build_digest", sC)
         if not self.serial:
             sB.wait_event(self.sel_done[1 - par])  # step i-1's selection wrote list set (i+1) % 2
         run("sparse_attn_merge", sB)
@@ -125,14 +127,15 @@ def setup_step(shape, device, pool_slots=None, serial=False, split=SPLIT):
         streams = [torch.cuda.current_stream(device)]
         cap_sel = cap_attn = None
     else:
-        streams = [torch.cuda.Stream(device), torch.cuda.Stream(device)]
+        streams = [torch.cuda.Stream(device) for _ in range(3)]
         cap_sel, cap_attn = split
     t["_launch_sel"] = bs._launch(cap_sel)
     t["_launch_attn"] = bs._launch(cap_attn)
-    sA, sB = streams[0].cuda_stream, streams[-1].cuda_stream
+    sA, sB, sC = ((streams * 3)[:3] if serial else streams)
+    sA, sB, sC = sA.cuda_stream, sB.cuda_stream, sC.cuda_stream
     p = lambda name: t[name].data_ptr()  # noqa: E731
     append = bs.Prepared("scout_build_digest", bs.MINMAX, p("K_pool"), wl.n_slots, p("page_table"), p("seq_len"),
-                         s.B, s.Hkv, D, s.P, nb, p("tail"), U, p("digest_cur"), p("status"), sB)
+                         s.B, s.Hkv, D, s.P, nb, p("tail"), U, p("digest_cur"), p("status"), sC)
     gemm = bs.Prepared("scout_predict_q", p("X"), p("W"), p("Qp"), s.B, s.Hq * D, s.hidden, p("status"),
                        t["_launch_sel"], sA)
     calls = []
