@@ -64,16 +64,17 @@ _SIGS = {
 
 
 class Launch(ctypes.Structure):
-    """scout_launch: launch options of the persistent kernels (max_ctas 0 = one CTA per SM)."""
-    _fields_ = [("max_ctas", ctypes.c_int)]
+    """scout_launch: launch options of the persistent kernels (max_ctas 0 = one CTA per SM;
+    pdl 1 = programmatic dependent launch of scout_score_topk after the kernel writing q)."""
+    _fields_ = [("max_ctas", ctypes.c_int), ("pdl", ctypes.c_int)]
 
 
-def _launch(max_ctas):
-    if max_ctas is None:
+def _launch(max_ctas, pdl=False):
+    if max_ctas is None and not pdl:
         return None
-    if max_ctas < 0:
+    if max_ctas is not None and max_ctas < 0:
         raise ScoutError("max_ctas must be >= 0")
-    return ctypes.pointer(Launch(int(max_ctas)))
+    return ctypes.pointer(Launch(int(max_ctas or 0), int(bool(pdl))))
 
 
 def lib_path() -> str:

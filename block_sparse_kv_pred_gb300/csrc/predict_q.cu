@@ -115,6 +115,9 @@ __global__ void __launch_bounds__(kThreadsQ, 1) predict_q_kernel(const __grid_co
   const uint32_t S = gridDim.y, rank = cluster_rank();
   const int kb0 = (int)(rank * a.kblocks / S), kb1 = (int)((rank + 1) * a.kblocks / S);
   const int nkb = kb1 - kb0;
+  // a kernel launched after this one as a programmatic dependent (scout_score_topk) may start
+  // as soon as SMs free up; it waits for this grid to finish before it reads Q
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
   if (tid == 0) {
     for (int i = 0; i < a.stages; ++i) {

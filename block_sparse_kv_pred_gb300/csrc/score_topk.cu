@@ -477,6 +477,7 @@ __global__ void __launch_bounds__(kThreadsAll, 1) score_topk_kernel(const __grid
     if (lane != 0) return;
     prefetch_tmap(&tmD);
     int64_t issued = 0;
+    bool q_ready = false;
     for (int64_t i = 0; i < it1 - it0; ++i) {
       const int64_t item = it0 + i;
       const int u = (int)(item / a.nchunk), ch = (int)(item - (int64_t)u * a.nchunk);
@@ -494,6 +495,12 @@ __global__ void __launch_bounds__(kThreadsAll, 1) score_topk_kernel(const __grid
 #pragma unroll
         for (int bx = 0; bx < 4; ++bx) tma_load_2d(sp + bx * kBoxBytes, &tmD, bx * 64, y, &full_bar[st]);
         const __nv_bfloat16* qg = a.q + ((int64_t)b * a.Hq + (int64_t)kvh * a.G) * kD;
+        if (with_q && !q_ready) {
+          // launched as a programmatic dependent: q is written by the previous kernel on the
+          // stream, so wait for it here (digest loads above need not); a no-op otherwise
+          asm volatile("griddepcontrol.wait;" ::: "memory");
+          q_ready = true;
+        }
         for (int h = 0; h < (with_q ? a.G : 0); ++h)
           asm volatile(
               "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
@@ -720,7 +727,17 @@ extern "C" int scout_score_topk(int kind, const void* q, const void* digest, con
     return SCOUT_ERR_CUDA;
   const int cap = launch != nullptr && launch->max_ctas > 0 ? launch->max_ctas : sm_count();
   const int grid = (int)(a.n_items < (int64_t)cap ? a.n_items : (int64_t)cap);  // <= one CTA per item
-  kern<<<grid, kThreadsAll, smem, stream>>>(tmD, a);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid);
+  cfg.blockDim = dim3(kThreadsAll);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = launch != nullptr && launch->pdl ? 1 : 0;
+  if (cudaLaunchKernelEx(&cfg, kern, tmD, a) != cudaSuccess) return SCOUT_ERR_CUDA;
   return launch_status();
 }
 

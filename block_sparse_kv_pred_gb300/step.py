@@ -15,9 +15,12 @@ is issued as two CUDA streams on disjoint SMs (``scout_launch.max_ctas``):
   reads it (the next step's selection of this layer does), so its few small
   CTAs run beside the persistent kernels and its latency is hidden.
 
-Step i's attention reads the lists step i-1 selected; step i's selection
-overwrites the set step i-1's attention read, so each stream waits for the
-other's previous step (two events per stream, used alternately).  The single
+Step i's attention reads the lists step i-1 selected, and its query comes from
+the input X of the layer, which the previous layer's attention produced; step
+i's selection starts from that same X and overwrites the set step i-1's
+attention read.  So the selection stream waits for the previous attention, and
+the attention stream for the previous selection (two events per stream, used
+alternately).  The single
 layer of the synthetic workload stands for both layers: ``digest_next`` (scored)
 and ``digest_cur`` (appended to) are separate buffers, as the two layers' are.
 
@@ -81,9 +84,11 @@ class Step:
             if timing is not None:
                 timing[name][1].record(stream)
 
-        run("predict_q", sA)
         if not self.serial:
-            sA.wait_event(self.attn_done[1 - par])  # step i-1's attention has read list set i % 2
+            # the layer's input X is the previous layer's attention output (through the merge
+            # and the MLP), and step i-1's attention has read list set i % 2
+            sA.wait_event(self.attn_done[1 - par])
+        run("predict_q", sA)
         run("score_topk", sA)
         self.sel_done[par].record(sA)
         run("build_digest", sC)
@@ -130,6 +135,8 @@ def setup_step(shape, device, pool_slots=None, serial=False, split=SPLIT):
         streams = [torch.cuda.Stream(device) for _ in range(3)]
         cap_sel, cap_attn = split
     t["_launch_sel"] = bs._launch(cap_sel)
+    # the selection starts streaming digests while the GEMM that writes Q_pred finishes
+    t["_launch_score"] = bs._launch(cap_sel, pdl=True)
     t["_launch_attn"] = bs._launch(cap_attn)
     sA, sB, sC = ((streams * 3)[:3] if serial else streams)
     sA, sB, sC = sA.cuda_stream, sB.cuda_stream, sC.cuda_stream
@@ -149,7 +156,7 @@ def setup_step(shape, device, pool_slots=None, serial=False, split=SPLIT):
                 "scout_score_topk", bs.MINMAX, p("Qp"), p("digest_next"), p("seq_len"), p("resident_bits"),
                 p("cpu" + old), p("cpu_count" + old), s.B, s.Hq, s.Hkv, D, s.P, nb, s.k, None, p("topk" + new),
                 p("topk_count" + new), p("res" + new), p("res_count" + new), p("cpu" + new), p("cpu_count" + new),
-                p("delta" + new), p("delta_count" + new), p("ws_t"), t["ws_t"].numel(), t["_launch_sel"], sA),
+                p("delta" + new), p("delta_count" + new), p("ws_t"), t["ws_t"].numel(), t["_launch_score"], sA),
             "sparse_attn_merge": bs.Prepared(
                 "scout_sparse_attn_merge", p("q"), p("K_pool"), p("V_pool"), wl.n_slots, p("page_table"),
                 p("seq_len"), p("res" + old), p("res_count" + old), s.B, s.Hq, s.Hkv, D, s.P, nb, s.k, s.scale,

@@ -65,6 +65,11 @@ typedef enum scout_digest_kind {
  * the grid keeps at least one CTA per 128-row tile of W. */
 typedef struct scout_launch {
   int max_ctas;
+  int pdl; /* scout_score_topk only: 1 = programmatic dependent launch.  The kernel may
+              start while the previous kernel on the stream (normally the scout_predict_q
+              that writes q) is still running: it streams digests at once and waits for
+              that kernel only before reading q.  Everything else it reads must be
+              complete before that previous kernel started. */
 } scout_launch;
 
 /* Human-readable name of a status code (static string, never NULL). */
