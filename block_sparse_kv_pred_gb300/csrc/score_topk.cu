@@ -175,16 +175,17 @@ __device__ __forceinline__ int unit_nvalid(const TopkArgs& a, int b) {
 
 // A selector warp's shared memory: the unit's residency bits, the bits of its previous
 // CPU list, the bits of the chosen candidates, a 256-bin digit histogram and the blocks
-// of up to 32 candidates.
+// of up to kMaxCand candidates.
 struct SelWarp {
   uint32_t* rbits;  // [words]
   uint32_t* pbits;  // [words]
   uint32_t* cbits;  // [words]
   int* hist;        // [256]
-  int* cidx;        // [32]
+  int* cidx;        // [kMaxCand]
 };
 // 32-bit words of one selector warp's shared memory
-__host__ __device__ constexpr int selwarp_words(int words) { return 3 * align4(words) + 256 + 32; }
+constexpr int kMaxCand = 64;  // candidates ranked exactly in the warp (two per lane)
+__host__ __device__ constexpr int selwarp_words(int words) { return 3 * align4(words) + 256 + kMaxCand; }
 __device__ __forceinline__ SelWarp selwarp_at(uint32_t* area, int words) {
   const int w4 = align4(words);
   return SelWarp{area, area + w4, area + 2 * w4, reinterpret_cast<int*>(area + 3 * w4),
@@ -232,32 +233,21 @@ __device__ __forceinline__ uint32_t transpose32(uint32_t x, int lane) {
   return x;
 }
 
-// Writes the blocks whose bits are set in the round masks m (lane r holds round r of the
-// group of 1024 starting at block g0) to list[run ..] in ascending order; returns their count.
-// Every lane writes consecutive entries, so the stores are coalesced.
-__device__ __forceinline__ int write_group(int32_t* list, int run, uint32_t m, int g0, int lane) {
-  const int c = __popc(m);
-  int incl = c;
+// Exclusive prefix sums over the lanes of two counts (each < 2^15 in total) with one scan:
+// the counts travel as the two 16-bit halves of one word.  Also returns the totals.
+__device__ __forceinline__ void scan_pair(int x, int y, int lane, int& ex, int& ey, int& tx, int& ty) {
+  const int v = x | (y << 16);
+  int incl = v;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
-    const int y = __shfl_up_sync(0xffffffffu, incl, o);
-    if (lane >= o) incl += y;
+    const int z = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += z;
   }
-  const int excl = incl - c, total = __shfl_sync(0xffffffffu, incl, 31);
-  for (int p0 = 0; p0 < total; p0 += 32) {  // warp-uniform trips: every lane shuffles
-    const int p = p0 + lane;
-    // the round holding entry p: the last lane whose exclusive count is <= p
-    int lo = 0;
-#pragma unroll
-    for (int step = 16; step > 0; step >>= 1) {
-      const int e = __shfl_sync(0xffffffffu, excl, min(lo + step, 31));
-      if (lo + step <= 31 && e <= p) lo += step;
-    }
-    const uint32_t mr = __shfl_sync(0xffffffffu, m, lo);
-    const int off = p - __shfl_sync(0xffffffffu, excl, lo);
-    if (p < total) list[run + p] = g0 + 32 * lo + (int)__fns(mr, 0, off + 1);
-  }
-  return total;
+  const int tot = __shfl_sync(0xffffffffu, incl, 31), e = incl - v;
+  ex = e & 0xffff;
+  ey = e >> 16;
+  tx = tot & 0xffff;
+  ty = tot >> 16;
 }
 
 // Top-k of one unit's keys (shared memory), split by residency, delta against the previous
@@ -268,13 +258,13 @@ __device__ __forceinline__ int write_group(int32_t* list, int run, uint32_t m, i
 // select on key - min: the leading bits zero in all of them are skipped, then 8-bit digits
 // of the keys sharing the current prefix are counted into a 256-bin histogram (shared-memory
 // reductions) until the keys sharing the prefix (the candidates) are the ones still needed
-// or at most 32.  Keys above the prefix are selected.  Of the candidates the `remaining`
-// largest are taken, the lower block index first among equal keys: with at most 32 of them
-// one per lane ranks itself against the others; more can only be left when every candidate
+// or at most 64.  Keys above the prefix are selected.  Of the candidates the `remaining`
+// largest are taken, the lower block index first among equal keys: with at most 64 of them
+// each lane ranks two against all the others; more can only be left when every candidate
 // key is equal, and then the lowest-index ones are taken.  The chosen candidates go into a
 // bitmap.  Per-round bit masks move between "lane = block" and "lane = round" by a 32 x 32
-// bit transpose, so no step needs a shuffle per round, and the lists are written with
-// coalesced stores.
+// bit transpose, so no step needs a shuffle per round; lane r then writes round r's blocks
+// at the list positions two packed prefix scans give it.
 __device__ void select_unit(const TopkArgs& a, int u, const uint32_t* keys, int nvalid, const SelWarp& sw,
                             int lane) {
   const int keff = min(a.k, nvalid);
@@ -306,7 +296,7 @@ __device__ void select_unit(const TopkArgs& a, int u, const uint32_t* keys, int 
     int fixed = lo == hi ? 32 : __clz(hi - lo);  // leading bits zero in every relative key
     mask = fixed == 0 ? 0u : (fixed == 32 ? 0xffffffffu : ~(0xffffffffu >> fixed));
     int4* h4 = reinterpret_cast<int4*>(sw.hist);
-    while (fixed < 32 && remaining != count && count > 32) {
+    while (fixed < 32 && remaining != count && count > kMaxCand) {
       const int width = min(8, 32 - fixed), shift = 32 - fixed - width;
       const uint32_t dmask = (1u << width) - 1u;
       h4[lane] = make_int4(0, 0, 0, 0);
@@ -358,7 +348,7 @@ __device__ void select_unit(const TopkArgs& a, int u, const uint32_t* keys, int 
     for (int i = lane; i < a.words; i += 32) sw.cbits[i] = 0u;
     __syncwarp();
     const uint32_t lt = (1u << lane) - 1u;
-    if (count <= 32) {
+    if (count <= kMaxCand) {
       // gather the candidates in block order (lane r takes round r of each group of 1024 after a
       // bit transpose), then one per lane ranks itself against the others
       int n = 0;
@@ -380,18 +370,25 @@ __device__ void select_unit(const TopkArgs& a, int u, const uint32_t* keys, int 
         n += __shfl_sync(0xffffffffu, incl, 31);
       }
       __syncwarp();
-      const int ji = lane < count ? sw.cidx[lane] : 0;
-      const uint32_t ki = lane < count ? keys[ji] - base : 0u;
-      int rank = 0;
+      // lane l ranks candidates l and l + 32 against all of them
+      const int j0 = lane < count ? sw.cidx[lane] : 0, j1 = lane + 32 < count ? sw.cidx[lane + 32] : 0;
+      const uint32_t k0 = lane < count ? keys[j0] - base : 0u, k1 = lane + 32 < count ? keys[j1] - base : 0u;
+      int r0 = 0, r1 = 0;
+      for (int h = 0; h < (count + 31) / 32; ++h) {
 #pragma unroll
-      for (int m = 0; m < 32; ++m) {
-        const uint32_t km = __shfl_sync(0xffffffffu, ki, m);
-        const int jm = __shfl_sync(0xffffffffu, ji, m);
-        rank += (m < count && (km > ki || (km == ki && jm < ji))) ? 1 : 0;
+        for (int m = 0; m < 32; ++m) {
+          const uint32_t km = __shfl_sync(0xffffffffu, h ? k1 : k0, m);
+          const int jm = __shfl_sync(0xffffffffu, h ? j1 : j0, m);
+          if (32 * h + m < count) {
+            r0 += (km > k0 || (km == k0 && jm < j0)) ? 1 : 0;
+            r1 += (km > k1 || (km == k1 && jm < j1)) ? 1 : 0;
+          }
+        }
       }
-      if (lane < count && rank < remaining) atomicOr(&sw.cbits[ji >> 5], 1u << (ji & 31));
+      if (lane < count && r0 < remaining) atomicOr(&sw.cbits[j0 >> 5], 1u << (j0 & 31));
+      if (lane + 32 < count && r1 < remaining) atomicOr(&sw.cbits[j1 >> 5], 1u << (j1 & 31));
     } else {
-      // more than 32 candidates are left only when all of them are equal: the lowest-index ones
+      // more than kMaxCand candidates are left only when all of them are equal: the lowest-index ones
       int seen = 0;
       for (int g = 0; g < ngroups; ++g) {
         if (ngroups > 1) load_group(keys, nvalid, g * 1024, lane, kv, base);
@@ -426,10 +423,19 @@ __device__ void select_unit(const TopkArgs& a, int u, const uint32_t* keys, int 
     }
     const uint32_t ms = transpose32(sel, lane);  // selected blocks of round `lane`
     const uint32_t mres = ms & rw, mcpu = ms & ~rw, mdel = ms & ~rw & ~pw;
-    nt += write_group(a.topk_idx + lb, nt, ms, g * 1024, lane);
-    nr += write_group(a.res_list + lb, nr, mres, g * 1024, lane);
-    nc += write_group(a.cpu_list + lb, nc, mcpu, g * 1024, lane);
-    nd += write_group(a.delta_list + lb, nd, mdel, g * 1024, lane);
+    // lane r writes its round's blocks; two packed scans give every lane's list positions
+    int et, er, ec, ed, tt, tr, tc, td;
+    scan_pair(__popc(ms), __popc(mres), lane, et, er, tt, tr);
+    scan_pair(__popc(mcpu), __popc(mdel), lane, ec, ed, tc, td);
+    const int j0 = g * 1024 + 32 * lane;
+    for (uint32_t m = ms, q = nt + et; m != 0u; m &= m - 1u, ++q) a.topk_idx[lb + q] = j0 + __ffs(m) - 1;
+    for (uint32_t m = mres, q = nr + er; m != 0u; m &= m - 1u, ++q) a.res_list[lb + q] = j0 + __ffs(m) - 1;
+    for (uint32_t m = mcpu, q = nc + ec; m != 0u; m &= m - 1u, ++q) a.cpu_list[lb + q] = j0 + __ffs(m) - 1;
+    for (uint32_t m = mdel, q = nd + ed; m != 0u; m &= m - 1u, ++q) a.delta_list[lb + q] = j0 + __ffs(m) - 1;
+    nt += tt;
+    nr += tr;
+    nc += tc;
+    nd += td;
   }
   for (int i = lane; i < a.k; i += 32) {
     if (i >= nt) a.topk_idx[lb + i] = -1;
