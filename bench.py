@@ -46,7 +46,7 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing leg")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="target oracle time for cpu_baseline")
     ap.add_argument("--serial", action="store_true", help="one stream, full grids (no overlap)")
-    ap.add_argument("--split", default=None, help="CTAs of the selection,attention kernels (default 80,72)")
+    ap.add_argument("--split", default=None, help="CTAs of the selection,attention kernels (default 90,62)")
     a = ap.parse_args()
     a.warmup = max(a.warmup, 3)
     return a

@@ -484,9 +484,18 @@ __global__ void __launch_bounds__(kThreadsAll, 1) score_topk_kernel(const __grid
     prefetch_tmap(&tmD);
     int64_t issued = 0;
     bool q_ready = false;
-    for (int64_t i = 0; i < it1 - it0; ++i) {
-      const int64_t item = it0 + i;
-      const int u = (int)(item / a.nchunk), ch = (int)(item - (int64_t)u * a.nchunk);
+    // item it0 + i is chunk ch of unit u; the valid-block count of the next unit is loaded a
+    // unit ahead, so no item waits on a global load before its copies are issued
+    int u = (int)(it0 / a.nchunk), ch = (int)(it0 - (int64_t)u * a.nchunk);
+    int nv = unit_nvalid(a, u / a.Hkv);
+    int nv_next = u < u_last ? unit_nvalid(a, (u + 1) / a.Hkv) : 0;
+    for (int64_t i = 0; i < it1 - it0; ++i, ++ch) {
+      if (ch == a.nchunk) {
+        ch = 0;
+        ++u;
+        nv = nv_next;
+        nv_next = u < u_last ? unit_nvalid(a, (u + 1) / a.Hkv) : 0;
+      }
       const int b = u / a.Hkv, kvh = u - b * a.Hkv;
       const int st = (int)(i % a.stages);
       if (!mbar_wait(&empty_bar[st], (uint32_t)((i / a.stages) & 1) ^ 1u)) {
@@ -494,7 +503,7 @@ __global__ void __launch_bounds__(kThreadsAll, 1) score_topk_kernel(const __grid
         break;
       }
       uint8_t* sp = ring + st * kStageBytesT;
-      if (ch * kChunk < unit_nvalid(a, b)) {
+      if (ch * kChunk < nv) {
         const bool with_q = i == 0 || ch == 0;  // the scoring warps read q on a unit's first item
         mbar_arrive_tx(&full_bar[st], 4 * kBoxBytes + (with_q ? a.G * kD * 2 : 0));
         const int y = u * a.nblk_cap + ch * kChunk;
