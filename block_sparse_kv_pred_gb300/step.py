@@ -33,7 +33,7 @@ from __future__ import annotations
 KERNELS = ("build_digest", "predict_q", "score_topk", "sparse_attn_merge")
 # stream of each kernel: 0 = selection (next layer), 1 = attention (this layer)
 STREAM_OF = {"build_digest": 2, "predict_q": 0, "score_topk": 0, "sparse_attn_merge": 1}
-SPLIT = (90, 62)  # CTAs of the selection and attention kernels when overlapped (152 SMs)
+SPLIT = (80, 72)  # CTAs of the selection and attention kernels when overlapped (152 SMs)
 
 
 class Step:
