@@ -106,6 +106,19 @@ __device__ __forceinline__ uint32_t page_addr(uint32_t base, int r, int C) {
   return base + (uint32_t)((C >> 3) * PS * 128 + r * 128 + ((((C & 7) ^ (r & 7))) << 4));
 }
 
+// Zero the V rows of tokens ntok .. PS-1 of a stage (the part of a sequence's last page
+// past its end), so that their zero probabilities never meet non-finite stale values.
+template <int PS>
+__device__ __forceinline__ void clear_tail_rows(uint8_t* vstage, int ntok, int lane) {
+  // two 64-column halves of PS rows x 128 bytes; 8 lanes per 128-byte row
+  for (int idx = ntok * 8 + lane; idx < PS * 8; idx += 32) {
+    const int r = idx >> 3, c = idx & 7;
+    *reinterpret_cast<uint4*>(vstage + r * 128 + c * 16) = make_uint4(0, 0, 0, 0);
+    *reinterpret_cast<uint4*>(vstage + PS * 128 + r * 128 + c * 16) = make_uint4(0, 0, 0, 0);
+  }
+  __syncwarp();
+}
+
 struct WarpState {
   float m[2];  // running max of scaled scores (log2 units) of heads 2t, 2t+1
   float l[2];  // running sum of exp2(s - m) over this lane's tokens, heads 2t, 2t+1
@@ -118,43 +131,50 @@ __device__ __forceinline__ uint32_t movmatrix_t(uint32_t x) {
   return y;
 }
 
-// One page, computed transposed so that tokens and head dims fill the MMA's M:
+// NP pages of one warp at once, computed transposed so that tokens and head dims fill the
+// MMA's M:
 //   S^T = K Q^T (tokens x heads), online softmax per head (column),
 //   O^T += V^T P^T (dims x heads); P^T reaches the B-operand layout by movmatrix.
-// qb holds Q^T fragments: qb[s] = heads g, dims 16s + 2t (+8).
-template <int PS>
-__device__ __forceinline__ void attend_page(uint32_t kbase, uint32_t vbase, int ntok, const uint32_t (&qb)[8][2],
-                                            float scale_log2, WarpState& st, int lane) {
+// Taking two pages together gives the MMA chains of both to the scheduler at once and
+// pays the running-max rescale once.  qb holds Q^T fragments: qb[s] = heads g, dims
+// 16s + 2t (+8).
+template <int PS, int NP>
+__device__ __forceinline__ void attend_pages(const uint32_t (&kbase)[NP], const uint32_t (&vbase)[NP],
+                                             const int (&ntok)[NP], const uint32_t (&qb)[8][2], float scale_log2,
+                                             WarpState& st, int lane) {
   constexpr int MT = PS / 16;  // 16-token tiles per stage
+  constexpr int T = NP * MT;   // tiles in all
   const int g = lane >> 2;
-  float s[MT][4];
+  float s[T][4];
 #pragma unroll
-  for (int mt = 0; mt < MT; ++mt) {
+  for (int tt = 0; tt < T; ++tt) {
+    const int pg = tt / MT, mt = tt % MT;
     float s2[4] = {0.f, 0.f, 0.f, 0.f};  // second accumulator: halves the dependent MMA chain
-    s[mt][0] = s[mt][1] = s[mt][2] = s[mt][3] = 0.f;
+    s[tt][0] = s[tt][1] = s[tt][2] = s[tt][3] = 0.f;
     const int r = mt * 16 + ((lane >> 3) & 1) * 8 + (lane & 7);
 #pragma unroll
     for (int ks = 0; ks < 8; ks += 2) {
       uint32_t a0, a1, a2, a3, c0, c1, c2, c3;
-      ldsm_x4(page_addr<PS>(kbase, r, 2 * ks + (lane >> 4)), a0, a1, a2, a3);
-      ldsm_x4(page_addr<PS>(kbase, r, 2 * ks + 2 + (lane >> 4)), c0, c1, c2, c3);
-      mma_bf16(s[mt], a0, a1, a2, a3, qb[ks][0], qb[ks][1]);
+      ldsm_x4(page_addr<PS>(kbase[pg], r, 2 * ks + (lane >> 4)), a0, a1, a2, a3);
+      ldsm_x4(page_addr<PS>(kbase[pg], r, 2 * ks + 2 + (lane >> 4)), c0, c1, c2, c3);
+      mma_bf16(s[tt], a0, a1, a2, a3, qb[ks][0], qb[ks][1]);
       mma_bf16(s2, c0, c1, c2, c3, qb[ks + 1][0], qb[ks + 1][1]);
     }
 #pragma unroll
-    for (int e = 0; e < 4; ++e) s[mt][e] += s2[e];
+    for (int e = 0; e < 4; ++e) s[tt][e] += s2[e];
   }
-  // per-head (column) max over this page's tokens
+  // per-head (column) max over the pages' tokens
   float bm0 = -INFINITY, bm1 = -INFINITY;
 #pragma unroll
-  for (int mt = 0; mt < MT; ++mt) {
+  for (int tt = 0; tt < T; ++tt) {
+    const int pg = tt / MT, mt = tt % MT;
     const int t0 = mt * 16 + g, t1 = t0 + 8;
-    s[mt][0] = t0 < ntok ? s[mt][0] * scale_log2 : -INFINITY;
-    s[mt][1] = t0 < ntok ? s[mt][1] * scale_log2 : -INFINITY;
-    s[mt][2] = t1 < ntok ? s[mt][2] * scale_log2 : -INFINITY;
-    s[mt][3] = t1 < ntok ? s[mt][3] * scale_log2 : -INFINITY;
-    bm0 = fmaxf(bm0, fmaxf(s[mt][0], s[mt][2]));
-    bm1 = fmaxf(bm1, fmaxf(s[mt][1], s[mt][3]));
+    s[tt][0] = t0 < ntok[pg] ? s[tt][0] * scale_log2 : -INFINITY;
+    s[tt][1] = t0 < ntok[pg] ? s[tt][1] * scale_log2 : -INFINITY;
+    s[tt][2] = t1 < ntok[pg] ? s[tt][2] * scale_log2 : -INFINITY;
+    s[tt][3] = t1 < ntok[pg] ? s[tt][3] * scale_log2 : -INFINITY;
+    bm0 = fmaxf(bm0, fmaxf(s[tt][0], s[tt][2]));
+    bm1 = fmaxf(bm1, fmaxf(s[tt][1], s[tt][3]));
   }
 #pragma unroll
   for (int o = 4; o < 32; o <<= 1) {
@@ -162,18 +182,18 @@ __device__ __forceinline__ void attend_page(uint32_t kbase, uint32_t vbase, int 
     bm1 = fmaxf(bm1, __shfl_xor_sync(0xffffffffu, bm1, o));
   }
   const float n0 = fmaxf(st.m[0], bm0), n1 = fmaxf(st.m[1], bm1);
-  const float al0 = exp2f(st.m[0] - n0), al1 = exp2f(st.m[1] - n1);  // 0 on the first page
+  const float al0 = exp2f(st.m[0] - n0), al1 = exp2f(st.m[1] - n1);  // 0 on the first pages
   st.m[0] = n0;
   st.m[1] = n1;
   float ps0 = 0.f, ps1 = 0.f;
 #pragma unroll
-  for (int mt = 0; mt < MT; ++mt) {
-    s[mt][0] = exp2f(s[mt][0] - n0);
-    s[mt][1] = exp2f(s[mt][1] - n1);
-    s[mt][2] = exp2f(s[mt][2] - n0);
-    s[mt][3] = exp2f(s[mt][3] - n1);
-    ps0 += s[mt][0] + s[mt][2];
-    ps1 += s[mt][1] + s[mt][3];
+  for (int tt = 0; tt < T; ++tt) {
+    s[tt][0] = exp2f(s[tt][0] - n0);
+    s[tt][1] = exp2f(s[tt][1] - n1);
+    s[tt][2] = exp2f(s[tt][2] - n0);
+    s[tt][3] = exp2f(s[tt][3] - n1);
+    ps0 += s[tt][0] + s[tt][2];
+    ps1 += s[tt][1] + s[tt][3];
   }
   st.l[0] = st.l[0] * al0 + ps0;
   st.l[1] = st.l[1] * al1 + ps1;
@@ -185,18 +205,19 @@ __device__ __forceinline__ void attend_page(uint32_t kbase, uint32_t vbase, int 
     st.o[md][3] *= al1;
   }
 #pragma unroll
-  for (int kk = 0; kk < MT; ++kk) {
+  for (int tt = 0; tt < T; ++tt) {
+    const int pg = tt / MT, mt = tt % MT;
     // P^T as B operand (k = tokens, n = heads), split into bf16 high and low parts
-    const uint32_t ht = pack_bf16(s[kk][0], s[kk][1]), hb = pack_bf16(s[kk][2], s[kk][3]);
-    const uint32_t lt = pack_bf16(s[kk][0] - bf16_lo(ht), s[kk][1] - bf16_hi(ht));
-    const uint32_t lb = pack_bf16(s[kk][2] - bf16_lo(hb), s[kk][3] - bf16_hi(hb));
+    const uint32_t ht = pack_bf16(s[tt][0], s[tt][1]), hb = pack_bf16(s[tt][2], s[tt][3]);
+    const uint32_t lt = pack_bf16(s[tt][0] - bf16_lo(ht), s[tt][1] - bf16_hi(ht));
+    const uint32_t lb = pack_bf16(s[tt][2] - bf16_lo(hb), s[tt][3] - bf16_hi(hb));
     const uint32_t bh0 = movmatrix_t(ht), bh1 = movmatrix_t(hb);
     const uint32_t bl0 = movmatrix_t(lt), bl1 = movmatrix_t(lb);
-    const int r = kk * 16 + (lane >> 4) * 8 + (lane & 7);
+    const int r = mt * 16 + (lane >> 4) * 8 + (lane & 7);
 #pragma unroll
     for (int md = 0; md < 8; ++md) {
       uint32_t a0, a1, a2, a3;
-      ldsm_x4_t(page_addr<PS>(vbase, r, 2 * md + ((lane >> 3) & 1)), a0, a1, a2, a3);
+      ldsm_x4_t(page_addr<PS>(vbase[pg], r, 2 * md + ((lane >> 3) & 1)), a0, a1, a2, a3);
       mma_bf16(st.o[md], a0, a1, a2, a3, bh0, bh1);
       mma_bf16(st.o[md], a0, a1, a2, a3, bl0, bl1);
     }
@@ -592,10 +613,37 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const __grid_c
       mbar_arrive(&full_bar[stage]);
     }
   };
-  // batch b = pages 32 b .. 32 b + 31 of this warp, page 32 b + m resolved by lane m
-  int cur_row, cur_nt, nxt_row = 0, nxt_nt = 0, pu, pj, plen;
+  // batch b = pages 32 b .. 32 b + 31 of this warp, page 32 b + m resolved by lane m; cur_*
+  // hold batch cur_b, nxt_* batch cur_b + 1 once it is resolved
+  int cur_row, cur_nt, nxt_row = 0, nxt_nt = 0, pu, pj, plen, cur_b = 0;
   resolve_a(lane, pu, pj, plen);
   resolve_b(lane, pu, pj, plen, cur_row, cur_nt);
+  auto nt_of = [&](int64_t kk) {
+    return __shfl_sync(0xffffffffu, (kk >> 5) == cur_b ? cur_nt : nxt_nt, (int)(kk & 31));
+  };
+  auto row_of = [&](int64_t kk) {
+    return __shfl_sync(0xffffffffu, (kk >> 5) == cur_b ? cur_row : nxt_row, (int)(kk & 31));
+  };
+  // page kk is next in this warp's order: move to its batch when it opens one, and start
+  // resolving the batch after it (list entries now, page-table slots kPhaseB pages later)
+  auto advance = [&](int64_t kk) {
+    const int m = (int)(kk & 31);
+    if (m == 0 && kk > 0) {
+      cur_row = nxt_row;
+      cur_nt = nxt_nt;
+      ++cur_b;
+    }
+    if (m == 0) resolve_a(kk + 32 + lane, pu, pj, plen);
+    if (m == kPhaseB) resolve_b(kk - kPhaseB + 32 + lane, pu, pj, plen, nxt_row, nxt_nt);
+  };
+  // after page kk: its stage takes this warp's page kk + kPerWarp
+  auto refill = [&](int64_t kk) {
+    const int64_t kr = kk + C::kPerWarp;
+    if (kr < n_mine) {
+      const int row = row_of(kr), nt = nt_of(kr);
+      if (lane == 0) issue(kr, row, nt);
+    }
+  };
   for (int r = 0; r < C::kPerWarp && r < n_mine; ++r) {
     const int row = __shfl_sync(0xffffffffu, cur_row, r), nt = __shfl_sync(0xffffffffu, cur_nt, r);
     if (lane == 0) issue(r, row, nt);
@@ -621,37 +669,57 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const __grid_c
     st.l[0] = st.l[1] = 0.f;
 #pragma unroll
     for (int d = 0; d < 8; ++d) st.o[d][0] = st.o[d][1] = st.o[d][2] = st.o[d][3] = 0.f;
-    for (int64_t p = lo * C::kSub; p < hi * C::kSub; ++p, ++i) {  // sub-pages of the segment's blocks
-      if ((int)(i % kConsumerWarps) != warp) continue;
-      const int64_t k = i / kConsumerWarps;
-      const int m = (int)(k & 31);
-      if (m == 0) resolve_a(k + 32 + lane, pu, pj, plen);  // next batch: list entries
-      if (m == kPhaseB) resolve_b(k - kPhaseB + 32 + lane, pu, pj, plen, nxt_row, nxt_nt);  // and slots
-      const int stage = (int)(i % C::kStages);
-      const int ntok = __shfl_sync(0xffffffffu, cur_nt, m);
-      if (!ok) {
-      } else if (!mbar_wait(&full_bar[stage], (uint32_t)(k / C::kPerWarp) & 1u)) {
-        if (lane == 0) report(a.status, SCOUT_DEV_TIMEOUT);
-        ok = false;  // a copy may still be in flight here: issue nothing more
-      } else if (ntok > 0) {
-        const uint32_t kb = ring_s + stage * C::kStageBytes;
-        attend_page<C::PS>(kb, kb + 2 * C::kHalfBytes, ntok, qa, a.scale_log2, st, lane);
+    // this warp's sub-pages of the segment (global sub-page numbers ii = warp (mod 4)), two at a time
+    const int64_t seg_lo = i, seg_hi = i + (hi - lo) * C::kSub;
+    for (int64_t ii = seg_lo + (warp - seg_lo % kConsumerWarps + kConsumerWarps) % kConsumerWarps; ii < seg_hi;
+         ii += 2 * kConsumerWarps) {
+      const bool two = ii + kConsumerWarps < seg_hi;
+      const int64_t k = ii / kConsumerWarps;
+      advance(k);
+      const int nt0 = nt_of(k);
+      int nt1 = 0;
+      if (two) {
+        advance(k + 1);
+        nt1 = nt_of(k + 1);
       }
-      // reload the stage with this warp's page k + kPerWarp once every lane is done reading it
-      const int64_t kr = k + C::kPerWarp;
-      if (kr < n_mine && ok) {
-        const int mr = m + C::kPerWarp;
-        const int row = __shfl_sync(0xffffffffu, mr < 32 ? cur_row : nxt_row, mr & 31);
-        const int nt = __shfl_sync(0xffffffffu, mr < 32 ? cur_nt : nxt_nt, mr & 31);
+      const int st0 = (int)(ii % C::kStages), st1 = (int)((ii + kConsumerWarps) % C::kStages);
+      bool got = ok && mbar_wait(&full_bar[st0], (uint32_t)(k / C::kPerWarp) & 1u);
+      if (got && two) got = mbar_wait(&full_bar[st1], (uint32_t)((k + 1) / C::kPerWarp) & 1u);
+      if (ok && !got) {
+        if (lane == 0) report(a.status, SCOUT_DEV_TIMEOUT);
+        ok = false;  // a copy may still be in flight: issue nothing more
+      }
+      if (got) {
+        const uint32_t kb0 = ring_s + st0 * C::kStageBytes, kb1 = ring_s + st1 * C::kStageBytes;
+        if (nt0 > 0 && nt0 < C::PS) clear_tail_rows<C::PS>(ring + st0 * C::kStageBytes + 2 * C::kHalfBytes, nt0, lane);
+        if (two && nt1 > 0 && nt1 < C::PS)
+          clear_tail_rows<C::PS>(ring + st1 * C::kStageBytes + 2 * C::kHalfBytes, nt1, lane);
+        if (two && nt0 > 0 && nt1 > 0) {
+          const uint32_t kbs[2] = {kb0, kb1}, vbs[2] = {kb0 + 2 * C::kHalfBytes, kb1 + 2 * C::kHalfBytes};
+          const int nts[2] = {nt0, nt1};
+          attend_pages<C::PS, 2>(kbs, vbs, nts, qa, a.scale_log2, st, lane);
+        } else {
+          if (nt0 > 0) {
+            const uint32_t kbs[1] = {kb0}, vbs[1] = {kb0 + 2 * C::kHalfBytes};
+            const int nts[1] = {nt0};
+            attend_pages<C::PS, 1>(kbs, vbs, nts, qa, a.scale_log2, st, lane);
+          }
+          if (two && nt1 > 0) {
+            const uint32_t kbs[1] = {kb1}, vbs[1] = {kb1 + 2 * C::kHalfBytes};
+            const int nts[1] = {nt1};
+            attend_pages<C::PS, 1>(kbs, vbs, nts, qa, a.scale_log2, st, lane);
+          }
+        }
+      }
+      // reload the stages with this warp's pages kPerWarp further on once every lane is done
+      if (ok) {
         fence_proxy_async();
         __syncwarp();
-        if (lane == 0) issue(kr, row, nt);
-      }
-      if (m == 31) {
-        cur_row = nxt_row;
-        cur_nt = nxt_nt;
+        refill(k);
+        if (two) refill(k + 1);
       }
     }
+    i = seg_hi;
     // hand this warp's state for the segment to the epilogue warp
     float l0 = st.l[0], l1 = st.l[1];
 #pragma unroll

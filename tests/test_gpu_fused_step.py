@@ -153,3 +153,39 @@ def test_two_stream_step_matches_oracle(serial):
             hq = kvh * s.G + h
             o, l = O.merge(r["O"][h], r["L"][h], o_cpu[b, hq].astype(np.float64), float(l_cpu[b, hq]))
             check_attention(Of[b, hq], Lf[b, hq], o, l, what=(serial, u, h))
+
+
+def test_stale_nan_rows_past_the_sequence_end_do_not_leak():
+    """Rows of a sequence's last page past its end may hold anything (a reused page, fresh
+    memory): fill them with NaN and infinities; the output must still equal the oracle's."""
+    wl, d = get("ragged_g5_p32")
+    s = wl.s
+    Kp, Vp = d["K_pool"].clone(), d["V_pool"].clone()
+    table = d["page_table"].cpu().numpy().reshape(s.units, -1)
+    lists = np.full((s.units, s.k), -1, np.int32)
+    counts = np.zeros(s.units, np.int32)
+    for u in range(s.units):
+        L = int(wl.seq_len[u // s.Hkv])
+        j, v = (L - 1) // s.P, L % s.P
+        if v:
+            slot = int(table[u, j])
+            Kp.view(torch.int16)[slot, v:] = 0x7FC0  # NaN
+            Vp.view(torch.int16)[slot, v:] = 0x7F80  # +inf
+        nv = -(-L // s.P)
+        sel = sorted(set([nv - 1] + list(range(min(s.k - 1, nv - 1)))))
+        lists[u, :len(sel)] = sel
+        counts[u] = len(sel)
+    ws = bs.sparse_attn_workspace(s.B, s.Hq, s.Hkv, s.P)
+    Og, Lg = bs.sparse_attn(d["q"], Kp, Vp, d["page_table"], d["seq_len"], to_dev(lists.reshape(s.B, s.Hkv, s.k)),
+                            to_dev(counts.reshape(s.B, s.Hkv)), s.B, s.Hq, s.Hkv, s.P, s.k, s.scale, ws)
+    torch.cuda.synchronize()
+    Og, Lg = Og.cpu().numpy(), Lg.cpu().numpy()
+    assert np.all(np.isfinite(Og)) and np.all(np.isfinite(Lg))
+    for u in range(s.units):
+        b, kvh = divmod(u, s.Hkv)
+        K, V = O.bf16_to_f64(wl.unit_kv(u)), O.bf16_to_f64(wl.unit_kv(u, "V"))
+        toks = O.block_tokens(lists[u, :counts[u]], s.P, int(wl.seq_len[b]))
+        for h in range(s.G):
+            hq = kvh * s.G + h
+            o, l = O.attention_partial(O.bf16_to_f64(wl.q[b, hq]), K[toks], V[toks], s.scale)
+            check_attention(Og[b, hq], Lg[b, hq], o, l, what=(u, h))
