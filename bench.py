@@ -117,6 +117,9 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
+GRAPH_STEPS = 20  # steps per captured CUDA graph (even: the list sets alternate)
+
+
 def max_over_ranks(x: float, device) -> float:
     """The largest of every rank's x (x itself on one rank)."""
     import torch
@@ -163,18 +166,28 @@ def run_scout(args, rank, world, local):
     if int(t["status"].item()) != 0:
         raise RuntimeError(f"device status {int(t['status'].item())} after warm-up")
 
+    # the timed steps replay CUDA graphs of GRAPH_STEPS steps (plus one graph of the remainder),
+    # captured from the same calls; every replay waits for the previous one to finish
+    T = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
+    gstep = step.fresh()
+    n_full, rest = divmod(args.steps, GRAPH_STEPS)
+    g_full = gstep.capture(GRAPH_STEPS, device) if n_full else None
+    g_rest = gstep.capture(rest, device) if rest else None
+    for _ in range(max(1, args.warmup // GRAPH_STEPS)):
+        (g_full or g_rest).replay()
+    torch.cuda.synchronize()
     sampler = ClockSampler(local)
     sampler.start()
-    T = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
     e_start, e_end = T(), T()
     barrier()
     torch.cuda.synchronize()
     wall0 = time.perf_counter()
     e_start.record(cur)
-    step.begin(e_start)
-    for i in range(args.steps):
-        step.issue()
-    step.end(e_end)
+    for _ in range(n_full):
+        g_full.replay()
+    if g_rest is not None:
+        g_rest.replay()
+    e_end.record(cur)
     torch.cuda.synchronize()
     barrier()
     wall = time.perf_counter() - wall0
@@ -183,8 +196,9 @@ def run_scout(args, rank, world, local):
         raise RuntimeError(f"device status {int(t['status'].item())} in the timed steps")
     ms = e_start.elapsed_time(e_end) / args.steps
 
-    # per-kernel durations from a second pass with events around every launch (the events sit
-    # between the selection stream's two kernels, so this pass is not the timed one)
+    # per-kernel durations from a second pass, issued on the streams with events around every
+    # launch (not the timed pass: the events sit between the selection stream's two kernels)
+    step = step.fresh()
     n_prof = max(50, args.steps // 4)
     ev = [{name: (T(), T()) for name in KERNELS} for _ in range(n_prof)]
     e0, e1 = T(), T()

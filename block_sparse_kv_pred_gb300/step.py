@@ -54,6 +54,29 @@ class Step:
     def launches_per_step(self) -> int:
         return len(KERNELS)
 
+    def fresh(self):
+        """The same calls and streams with their own events (for a separate issue sequence,
+        e.g. one captured in a CUDA graph, whose events may not be waited on outside it)."""
+        twin = Step(self.t, self.calls, self.streams, self.serial)
+        twin.i = self.i
+        return twin
+
+    def capture(self, n_steps, device):
+        """A CUDA graph of n_steps steps (its first step ordered by the graph launch itself)."""
+        import torch
+
+        g = torch.cuda.CUDAGraph()
+        side = torch.cuda.Stream(device)
+        with torch.cuda.graph(g, stream=side):
+            cur = torch.cuda.current_stream()
+            ev = torch.cuda.Event()
+            ev.record(cur)
+            self.begin(ev)
+            for j in range(n_steps):
+                self.issue(after_begin=(j == 0))
+            self.end(None)
+        return g
+
     def begin(self, event):
         """Make both streams wait for ``event`` (recorded on the current stream)."""
         for s in self.streams:
@@ -71,9 +94,13 @@ class Step:
         if event is not None:
             event.record(cur)
 
-    def issue(self, timing=None):
-        """Launch the next step.  ``timing``: optional name -> (start, end) timing events."""
+    def issue(self, timing=None, after_begin=False):
+        """Launch the next step.  ``timing``: optional name -> (start, end) timing events.
+        ``after_begin``: the step directly follows ``begin`` (e.g. the first step of a CUDA
+        graph), whose event already orders it after everything before, so it waits for no
+        earlier step's events (a graph capture may not wait on events recorded outside it)."""
         par = self.i % 2
+        cross = not self.serial and not after_begin
         sA, sB, sC = (self.streams * 3)[:3] if self.serial else self.streams
         c = self.calls[par]
 
@@ -84,7 +111,7 @@ class Step:
             if timing is not None:
                 timing[name][1].record(stream)
 
-        if not self.serial:
+        if cross:
             # the layer's input X is the previous layer's attention output (through the merge
             # and the MLP), and step i-1's attention has read list set i % 2
             sA.wait_event(self.attn_done[1 - par])
@@ -92,7 +119,7 @@ class Step:
         run("score_topk", sA)
         self.sel_done[par].record(sA)
         run("build_digest", sC)
-        if not self.serial:
+        if cross:
             sB.wait_event(self.sel_done[1 - par])  # step i-1's selection wrote list set (i+1) % 2
         run("sparse_attn_merge", sB)
         self.attn_done[par].record(sB)
@@ -129,7 +156,7 @@ def setup_step(shape, device, pool_slots=None, serial=False, split=SPLIT):
     t["status"] = torch.zeros(1, dtype=torch.int32, device=device)
 
     if serial:
-        streams = [torch.cuda.current_stream(device)]
+        streams = [torch.cuda.Stream(device)]  # not the legacy default stream: it can be captured
         cap_sel = cap_attn = None
     else:
         streams = [torch.cuda.Stream(device) for _ in range(3)]
