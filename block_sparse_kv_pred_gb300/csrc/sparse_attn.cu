@@ -40,7 +40,8 @@ constexpr int kConsumerWarps = SCOUT_ATTN_CONSUMERS;
 constexpr int kSubTokens = SCOUT_ATTN_SUBPAGE;
 constexpr int kEpilogueWarp = kConsumerWarps;  // combines, writes, fixes up split units
 constexpr int kThreads = (kConsumerWarps + 1) * 32;
-constexpr int kPhaseB = 8;  // page of a batch at which the next batch's page-table loads are issued
+constexpr int kPhaseB = 8;   // page of a batch at which the next batch's page-table loads are issued
+constexpr int kPhaseC = 16;  // and at which their values are used
 constexpr int kMaxUnits = 4096;
 constexpr int kMaxSlots = 2;  // combine slots between the consumer warps and the epilogue warp
 constexpr int kMaxGrid = 1024;
@@ -67,7 +68,8 @@ struct Cfg {
   static constexpr int kHalfBytes = PS * 128;        // one 64-column half of a sub-page
   static constexpr int kStageBytes = 4 * kHalfBytes; // K (2 halves) + V (2 halves)
   static constexpr int kRingBytes = kStages * kStageBytes;
-  static_assert(kStages % kConsumerWarps == 0 && kPhaseB < 32 - kPerWarp, "stage ownership");
+  static_assert(kStages % kConsumerWarps == 0 && kPhaseB < kPhaseC && kPhaseC < 32 - kPerWarp - 1,
+                "stage ownership and resolution phases");
 };
 
 struct AttnArgs {
@@ -583,17 +585,20 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const __grid_c
   };
   // Second half: the pool row of the sub-page and its valid tokens (0 = nothing to load).  An
   // entry outside the sequence or the pool is skipped and reported.
-  auto resolve_b = [&](int64_t kk, int ru, int rj, int rlen, int& row, int& nt) {
+  // Second: the page-table slot of the list entry (issued here, first used kPhaseC - kPhaseB
+  // pages later, so the load's latency stays off the warp's path).
+  auto resolve_b = [&](int ru, int rj, int& rsl) {
+    rsl = -1;
+    if (ru >= 0 && rj >= 0 && rj < a.nblk_cap) rsl = a.page_table[(int64_t)ru * a.nblk_cap + rj];
+  };
+  // Third: the pool row of the sub-page and its valid tokens (0 = nothing to load).  An entry
+  // outside the sequence or the pool is skipped and reported.
+  auto resolve_c = [&](int64_t kk, int ru, int rj, int rlen, int sl, int& row, int& nt) {
     row = 0;
     nt = 0;
     if (ru < 0) return;
     const int h = (int)((warp + (int64_t)kConsumerWarps * kk) % C::kSub);
-    int nv = 0;
-    int32_t sl = -1;
-    if (rj >= 0 && rj < a.nblk_cap) {
-      nv = min(P, rlen - rj * P);
-      sl = a.page_table[(int64_t)ru * a.nblk_cap + rj];
-    }
+    const int nv = rj >= 0 && rj < a.nblk_cap ? min(P, rlen - rj * P) : 0;
     if (nv <= 0 || sl < 0 || sl >= a.n_slots) {
       if (h == 0) report(a.status, SCOUT_DEV_BAD_INDEX);
       return;
@@ -615,14 +620,12 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const __grid_c
   };
   // batch b = pages 32 b .. 32 b + 31 of this warp, page 32 b + m resolved by lane m; cur_*
   // hold batch cur_b, nxt_* batch cur_b + 1 once it is resolved
-  int cur_row, cur_nt, nxt_row = 0, nxt_nt = 0, pu, pj, plen, cur_b = 0;
+  int cur_row, cur_nt, nxt_row = 0, nxt_nt = 0, pu, pj, plen, psl, cur_b = 0;
   resolve_a(lane, pu, pj, plen);
-  resolve_b(lane, pu, pj, plen, cur_row, cur_nt);
+  resolve_b(pu, pj, psl);
+  resolve_c(lane, pu, pj, plen, psl, cur_row, cur_nt);
   auto nt_of = [&](int64_t kk) {
     return __shfl_sync(0xffffffffu, (kk >> 5) == cur_b ? cur_nt : nxt_nt, (int)(kk & 31));
-  };
-  auto row_of = [&](int64_t kk) {
-    return __shfl_sync(0xffffffffu, (kk >> 5) == cur_b ? cur_row : nxt_row, (int)(kk & 31));
   };
   // page kk is next in this warp's order: move to its batch when it opens one, and start
   // resolving the batch after it (list entries now, page-table slots kPhaseB pages later)
@@ -634,15 +637,18 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const __grid_c
       ++cur_b;
     }
     if (m == 0) resolve_a(kk + 32 + lane, pu, pj, plen);
-    if (m == kPhaseB) resolve_b(kk - kPhaseB + 32 + lane, pu, pj, plen, nxt_row, nxt_nt);
+    if (m == kPhaseB) resolve_b(pu, pj, psl);
+    if (m == kPhaseC) resolve_c(kk - kPhaseC + 32 + lane, pu, pj, plen, psl, nxt_row, nxt_nt);
   };
-  // after page kk: its stage takes this warp's page kk + kPerWarp
-  auto refill = [&](int64_t kk) {
-    const int64_t kr = kk + C::kPerWarp;
-    if (kr < n_mine) {
-      const int row = row_of(kr), nt = nt_of(kr);
-      if (lane == 0) issue(kr, row, nt);
-    }
+  // after pages kk .. kk + n - 1 (n = 1 or 2): their stages take this warp's pages kPerWarp
+  // further on; lane j issues the copies of page kk + j, so the two go out together
+  auto refill = [&](int64_t kk, int n) {
+    const int64_t kr = kk + C::kPerWarp + (lane < n ? lane : 0);
+    const int src = (int)(kr & 31);
+    const int rc = __shfl_sync(0xffffffffu, cur_row, src), rn = __shfl_sync(0xffffffffu, nxt_row, src);
+    const int tc = __shfl_sync(0xffffffffu, cur_nt, src), tn = __shfl_sync(0xffffffffu, nxt_nt, src);
+    const bool in_cur = (kr >> 5) == cur_b;
+    if (lane < n && kr < n_mine) issue(kr, in_cur ? rc : rn, in_cur ? tc : tn);
   };
   for (int r = 0; r < C::kPerWarp && r < n_mine; ++r) {
     const int row = __shfl_sync(0xffffffffu, cur_row, r), nt = __shfl_sync(0xffffffffu, cur_nt, r);
@@ -715,8 +721,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const __grid_c
       if (ok) {
         fence_proxy_async();
         __syncwarp();
-        refill(k);
-        if (two) refill(k + 1);
+        refill(k, two ? 2 : 1);
       }
     }
     i = seg_hi;
