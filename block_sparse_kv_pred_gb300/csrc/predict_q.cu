@@ -8,9 +8,12 @@
 // W and X tiles (64 k-columns, 128-byte swizzle) stream in by TMA through a ring of
 // shared-memory stages guarded by mbarriers; one thread issues tcgen05.mma into a
 // TMEM accumulator and frees each stage with tcgen05.commit.  The K dimension is
-// split over the CTAs of a thread-block cluster so that about one CTA runs per SM;
-// the partial accumulators are summed through distributed shared memory by the
-// cluster's first CTA, which writes bf16 Q.  No global scratch is used.
+// split over the CTAs of a thread-block cluster so that about one CTA runs per SM.
+// The batch columns of the accumulator are dealt out over the cluster's CTAs: each
+// CTA stores the columns another CTA owns straight into that CTA's shared memory
+// (distributed shared memory), then sums the partials of its own columns and writes
+// them as bf16 Q.  No global scratch is used.
+
 #include "common.cuh"
 
 namespace scout {
@@ -74,10 +77,8 @@ __device__ __forceinline__ uint32_t map_peer(uint32_t addr, uint32_t rank) {
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
   return r;
 }
-__device__ __forceinline__ float ld_peer(uint32_t addr) {
-  float v;
-  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
-  return v;
+__device__ __forceinline__ void st_peer(uint32_t addr, float v) {
+  asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
 }
 
 // Shared-memory matrix descriptor: K-major operand, 128-byte swizzle, rows of 128 bytes,
@@ -101,6 +102,14 @@ struct GemmArgs {
   int32_t* status;
 };
 
+// Stage i of CTA (tile, split range starting at k-block kb0): the W tile and the X tile.
+__device__ __forceinline__ void load_stage(uint8_t* sW, const CUtensorMap* tmW, const CUtensorMap* tmX,
+                                           const GemmArgs& a, int tile, int kb, uint64_t* bar, int stage_bytes) {
+  mbar_arrive_tx(bar, (uint32_t)stage_bytes);
+  tma_load_2d(sW, tmW, kb * kBK, tile * kBM, bar);
+  tma_load_2d(sW + kWTileBytes, tmX, kb * kBK, 0, bar);
+}
+
 __global__ void __launch_bounds__(kThreadsQ, 1) predict_q_kernel(const __grid_constant__ CUtensorMap tmW,
                                                                  const __grid_constant__ CUtensorMap tmX,
                                                                  const GemmArgs a) {
@@ -119,6 +128,8 @@ __global__ void __launch_bounds__(kThreadsQ, 1) predict_q_kernel(const __grid_co
   // as soon as SMs free up; it waits for this grid to finish before it reads Q
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
+  // the first pass over the ring needs no free slot: issue it before the TMEM allocation
+  const int first = min(a.stages, nkb);
   if (tid == 0) {
     for (int i = 0; i < a.stages; ++i) {
       mbar_init(&full_bar[i], 1);
@@ -126,6 +137,10 @@ __global__ void __launch_bounds__(kThreadsQ, 1) predict_q_kernel(const __grid_co
     }
     mbar_init(&done_bar, 1);
     fence_mbar_init();
+    prefetch_tmap(&tmW);
+    prefetch_tmap(&tmX);
+    for (int i = 0; i < first; ++i)
+      load_stage(base + i * stage_bytes, &tmW, &tmX, a, tile, kb0 + i, &full_bar[i], stage_bytes);
   }
   if (warp == 2) tmem_alloc(&tmem_slot, (uint32_t)a.tmem_cols);
   tc_fence_before();
@@ -134,21 +149,15 @@ __global__ void __launch_bounds__(kThreadsQ, 1) predict_q_kernel(const __grid_co
   const uint32_t tmem = tmem_slot;
 
   if (warp == 0 && lane == 0) {
-    // TMA producer
-    prefetch_tmap(&tmW);
-    prefetch_tmap(&tmX);
-    int issued = 0;
-    for (int i = 0; i < nkb; ++i) {
+    // TMA producer: the rest of the k range, each stage once the MMAs have freed it
+    int issued = first;
+    for (int i = first; i < nkb; ++i) {
       const int st = i % a.stages;
       if (!mbar_wait(&empty_bar[st], ((i / a.stages) & 1) ^ 1)) {
         report(a.status, SCOUT_DEV_TIMEOUT);
         break;
       }
-      uint8_t* sW = base + st * stage_bytes;
-      mbar_arrive_tx(&full_bar[st], (uint32_t)stage_bytes);
-      const int kx = (kb0 + i) * kBK;
-      tma_load_2d(sW, &tmW, kx, tile * kBM, &full_bar[st]);
-      tma_load_2d(sW + kWTileBytes, &tmX, kx, 0, &full_bar[st]);
+      load_stage(base + st * stage_bytes, &tmW, &tmX, a, tile, kb0 + i, &full_bar[st], stage_bytes);
       issued = i + 1;
     }
     // every issued copy lands before the CTA can retire
@@ -177,37 +186,44 @@ __global__ void __launch_bounds__(kThreadsQ, 1) predict_q_kernel(const __grid_co
   __syncwarp();
 
   // ---- epilogue: thread (warp w, lane l) owns W row tile*128 + 32w + l (TMEM lane) ----
+  // Column group g (8 batch columns) belongs to CTA g % S of the cluster.  recv holds, for
+  // every source CTA s and every group this CTA owns, s's partial: [S][owned][8][128] fp32.
   if (!mbar_wait(&done_bar, 0)) report(a.status, SCOUT_DEV_TIMEOUT);
   tc_fence_after();
   const int r_local = warp * 32 + lane;
   const int row = tile * kBM + r_local;
   const uint32_t trow = tmem + ((uint32_t)(warp * 32) << 16);
-  float* part = reinterpret_cast<float*>(base);  // [n_pad][128]: the stage ring is idle now
+  const int ngroups = a.n_pad / 8;
+  const int owned = (ngroups + (int)S - 1) / (int)S;
+  float* recv = reinterpret_cast<float*>(base);  // the stage ring is idle now
   float v[8];
-  if (S > 1 && rank != 0) {
-    for (int c = 0; c < a.n_pad; c += 8) {
-      tmem_ld8(trow + (uint32_t)c, v);
+  if (S > 1) {
+    cluster_sync();  // every CTA of the cluster is done with its ring: it may be written
+    for (int g = 0; g < ngroups; ++g) {
+      const uint32_t owner = (uint32_t)g % S;
+      if (owner == rank) continue;
+      tmem_ld8(trow + (uint32_t)(g * 8), v);
+      const int slot = ((int)rank * owned + g / (int)S) * 8;
+      const uint32_t dst = map_peer(smem_u32(recv + slot * kBM + r_local), owner);
 #pragma unroll
-      for (int e = 0; e < 8; ++e) part[(c + e) * kBM + r_local] = v[e];
+      for (int e = 0; e < 8; ++e) st_peer(dst + (uint32_t)(e * kBM * 4), v[e]);
+    }
+    cluster_sync();  // the partials have landed (release/acquire across the cluster)
+  }
+  for (int g = (int)rank; g < ngroups; g += (int)S) {
+    tmem_ld8(trow + (uint32_t)(g * 8), v);
+    for (uint32_t s = 0; s < S; ++s) {
+      if (s == rank) continue;
+      const float* src = recv + ((int)s * owned + g / (int)S) * 8 * kBM + r_local;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) v[e] += src[e * kBM];
+    }
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      const int m = g * 8 + e;
+      if (m < a.M && row < a.N) a.Q[(int64_t)m * a.N + row] = __float2bfloat16_rn(v[e]);
     }
   }
-  if (S > 1) cluster_sync();
-  if (rank == 0) {
-    for (int c = 0; c < a.n_pad; c += 8) {
-      tmem_ld8(trow + (uint32_t)c, v);
-      for (uint32_t r = 1; r < S; ++r) {
-        const uint32_t pa = map_peer(smem_u32(part + c * kBM + r_local), r);
-#pragma unroll
-        for (int e = 0; e < 8; ++e) v[e] += ld_peer(pa + (uint32_t)(e * kBM * 4));
-      }
-#pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        const int m = c + e;
-        if (m < a.M && row < a.N) a.Q[(int64_t)m * a.N + row] = __float2bfloat16_rn(v[e]);
-      }
-    }
-  }
-  if (S > 1) cluster_sync();  // peers keep their shared memory until the first CTA has read it
   tc_fence_before();
   __syncthreads();
   if (warp == 2) tmem_dealloc(tmem, (uint32_t)a.tmem_cols);
@@ -247,7 +263,8 @@ extern "C" int scout_predict_q(const void* X, const void* W, void* Q, int M, int
   const int tiles = N / kBM;
   const int cap = launch != nullptr && launch->max_ctas > 0 ? launch->max_ctas : sm_count();
   const int S = max(1, min(min(8, a.kblocks), cap / tiles));  // split-K so tiles x S fits the CTA budget
-  const size_t smem = 1024 + (size_t)max(a.stages * stage_bytes, a.n_pad * kBM * 4);
+  const int owned = (a.n_pad / 8 + S - 1) / S;                  // column groups per CTA in the reduction
+  const size_t smem = 1024 + (size_t)max(a.stages * stage_bytes, S * owned * 8 * kBM * 4);
   CUtensorMap tmW, tmX;
   if (!make_map(&tmW, W, N, K, kBM) || !make_map(&tmX, X, M, K, a.n_pad)) return SCOUT_ERR_UNSUPPORTED;
   if (cudaFuncSetAttribute(predict_q_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)

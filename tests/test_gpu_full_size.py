@@ -56,17 +56,23 @@ def _check_unit(wl, u, q_sel_bits, kind, topk, tc, res, rc, cpu, cc, O_out, L_ou
         check_attention(O_out[b, hq], L_out[b, hq], o, l, what=(u, h))
 
 
-@pytest.mark.parametrize("cfg,serial", [("qwen3_14b", False), ("qwen3_8b", True)])
-def test_full_size_step_sampled(cfg, serial):
-    """Three steps of the decode step at full size; selection with Q_pred, attention with q."""
+@pytest.mark.parametrize("cfg,mode", [("qwen3_14b", "streams"), ("qwen3_14b", "graph"), ("qwen3_8b", "serial")])
+def test_full_size_step_sampled(cfg, mode):
+    """Three steps of the decode step at full size (or, as bench.py times it, a captured CUDA
+    graph of two steps replayed twice); selection with Q_pred, attention with q."""
     shape = W.CONFIGS[cfg]()
-    wl, t, step = setup_step(shape, torch.device("cuda", 0), serial=serial, split=SPLIT)
-    ev = torch.cuda.Event()
-    ev.record()
-    step.begin(ev)
-    for _ in range(3):
-        step.issue()
-    step.end(None)
+    wl, t, step = setup_step(shape, torch.device("cuda", 0), serial=(mode == "serial"), split=SPLIT)
+    if mode == "graph":
+        g = step.capture(2, torch.device("cuda", 0))
+        for _ in range(2):
+            g.replay()
+    else:
+        ev = torch.cuda.Event()
+        ev.record()
+        step.begin(ev)
+        for _ in range(3):
+            step.issue()
+        step.end(None)
     torch.cuda.synchronize()
     assert int(t["status"].item()) == 0
     s = shape

@@ -185,7 +185,7 @@ def test_score_topk_parity(name):
     assert exact >= s.units - 1
 
 
-def _integer_case(kind, seed=0):
+def _integer_case(kind, seed=0, k_range=(-3, 4), q_range=(-2, 3)):
     """Small-integer K and q: every fp32 score is exact, so GPU and fp64 scores agree bit for bit and
     the many ties exercise the lowest-index rule."""
     rng = np.random.default_rng(seed)
@@ -193,9 +193,9 @@ def _integer_case(kind, seed=0):
     G, D = Hq // Hkv, 128
     nb = -(-T // P)
     seq = np.array([T, 130 * 32 + 1], dtype=np.int32)
-    Ku = W.f32_to_bf16(rng.integers(-3, 4, size=(B * Hkv, nb * P, D)).astype(np.float32))
+    Ku = W.f32_to_bf16(rng.integers(*k_range, size=(B * Hkv, nb * P, D)).astype(np.float32))
     Vu = W.f32_to_bf16(rng.standard_normal((B * Hkv, nb * P, D)).astype(np.float32))
-    q = W.f32_to_bf16(rng.integers(-2, 3, size=(B, Hq, D)).astype(np.float32))
+    q = W.f32_to_bf16(rng.integers(*q_range, size=(B, Hq, D)).astype(np.float32))
     Kp, Vp, table = pools_from_units(Ku, Vu, P, rng)
     resident = rng.random((B * Hkv, nb)) < 0.3
     dev = dict(K_pool=to_dev(Kp), V_pool=to_dev(Vp), page_table=to_dev(table.reshape(B, Hkv, nb)),
@@ -204,9 +204,7 @@ def _integer_case(kind, seed=0):
                 dev=dev)
 
 
-@pytest.mark.parametrize("kind", ["minmax", "mean"])
-def test_score_topk_bit_exact_on_exact_scores(kind):
-    c = _integer_case(kind)
+def _check_integer_case(c, kind, max_ctas=None, min_ties=0):
     B, Hkv, nb, k, P = c["B"], c["Hkv"], c["nb"], c["k"], c["P"]
     d = c["dev"]
     dg = (torch.empty((B, Hkv, nb, 2, 128), dtype=torch.bfloat16, device="cuda") if kind == "minmax"
@@ -215,7 +213,7 @@ def test_score_topk_bit_exact_on_exact_scores(kind):
     ws = bs.score_topk_workspace(B, Hkv, nb)
     scores = torch.empty((B, Hkv, nb), dtype=torch.float32, device="cuda")
     out = bs.score_topk(kind, d["q"], dg, d["seq_len"], d["resident_bits"], B, c["Hq"], Hkv, P, nb, k, ws,
-                        scores=scores)
+                        scores=scores, max_ctas=max_ctas)
     torch.cuda.synchronize()
     res = {kk: v.cpu().numpy().reshape(B * Hkv, -1) for kk, v in out.items()}
     ties = 0
@@ -229,8 +227,26 @@ def test_score_topk_bit_exact_on_exact_scores(kind):
         ties += len(r["scores"]) - len(np.unique(r["scores"]))
         for key in ("topk", "res", "cpu", "delta"):
             n = res[key + "_count"][u][0]
-            assert n == len(r[key]) and list(res[key][u][:n]) == list(r[key]), (key, u)
-    assert ties > 100
+            assert n == len(r[key]) and list(res[key][u][:n]) == list(r[key]), (key, u, max_ctas)
+            assert np.all(res[key][u][n:] == -1)
+    assert ties > min_ties
+
+
+@pytest.mark.parametrize("max_ctas", [None, 1, 2, 3])
+@pytest.mark.parametrize("kind", ["minmax", "mean"])
+def test_score_topk_bit_exact_on_exact_scores(kind, max_ctas):
+    """Uncapped, every unit is scored by several CTAs and selected by the last one to finish; with
+    a CTA cap a CTA scores whole units and selects them itself: both give the oracle's lists."""
+    _check_integer_case(_integer_case(kind), kind, max_ctas, min_ties=100)
+
+
+@pytest.mark.parametrize("max_ctas", [None, 1, 2])
+@pytest.mark.parametrize("k_range", [(0, 1), (0, 2)])
+def test_score_topk_ties_beyond_the_candidate_limit(k_range, max_ctas):
+    """K = 0 everywhere (every score equal) or K in {0, 1} (almost every block maximal): far more
+    than 64 candidates share the k-th key, and the lowest-index ones are taken."""
+    c = _integer_case("minmax", seed=3, k_range=k_range, q_range=(1, 2))
+    _check_integer_case(c, "minmax", max_ctas, min_ties=200)
 
 
 def _attn_lists(s, rng, force_split=False):
@@ -358,6 +374,20 @@ def test_predict_q_parity(M, N, K):
     got = O.bf16_to_f64(bf16_bits(Q))
     assert np.linalg.norm(got - ref) <= 1e-2 * np.linalg.norm(ref)
     # stronger than the acceptance bound: each entry within bf16 rounding of the fp32 sum
+    assert np.all(np.abs(got - ref) <= 2.0 ** -8 * np.abs(ref) + 1e-3 * np.abs(ref).max())
+
+
+@pytest.mark.parametrize("max_ctas", [10, 20, 30, 110])
+def test_predict_q_split_k_reduction(max_ctas):
+    """M = 130 pads to 144 batch columns (18 groups of 8); 10 W tiles under caps of 10, 20, 30 and
+    110 CTAs give split-K clusters of 1, 2, 3 and 8 CTAs, over which the groups are dealt: every
+    group is reduced by its owner CTA, whatever the cluster size."""
+    X = W.normal_bf16(3, W.STREAM_X, (130, 2048))
+    Wq = W.normal_bf16(3, W.STREAM_W, (1280, 2048), sigma=0.02)
+    Q = bs.predict_q(to_dev(X), to_dev(Wq), max_ctas=max_ctas)
+    torch.cuda.synchronize()
+    ref = O.predict_q(X, Wq)
+    got = O.bf16_to_f64(bf16_bits(Q))
     assert np.all(np.abs(got - ref) <= 2.0 ** -8 * np.abs(ref) + 1e-3 * np.abs(ref).max())
 
 
