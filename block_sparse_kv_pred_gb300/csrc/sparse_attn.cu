@@ -7,7 +7,10 @@
 // N) takes the contiguous range [c N / Gp, (c+1) N / Gp).  A unit that falls
 // inside one range is finished by that CTA; a unit split over several CTAs is
 // finished by the last of them to arrive (self-resetting counter), which merges
-// the per-CTA partials by their LSE.
+// the per-CTA partials by their LSE.  Only a range's first and last segment can be
+// cut, and the range is walked last segment first: both of a CTA's cut pieces are
+// then produced early, and a dedicated split warp publishes them and does the
+// cross-CTA merge (dependent global round trips) while the whole units stream.
 //
 // Inside a CTA: the four consumer warps take the range's sub-pages round-robin.
 // Each warp owns kStages / 4 stages of a shared-memory ring and keeps them
@@ -38,8 +41,10 @@ namespace {
 #endif
 constexpr int kConsumerWarps = SCOUT_ATTN_CONSUMERS;
 constexpr int kSubTokens = SCOUT_ATTN_SUBPAGE;
-constexpr int kEpilogueWarp = kConsumerWarps;  // combines, writes, fixes up split units
-constexpr int kThreads = (kConsumerWarps + 1) * 32;
+constexpr int kEpilogueWarp = kConsumerWarps;     // combines the warps' states, writes whole units
+constexpr int kSplitWarp = kConsumerWarps + 1;     // merges the units cut by range boundaries
+constexpr int kThreads = (kConsumerWarps + 2) * 32;
+constexpr int kMaxSplit = 2;  // pieces of cut units per CTA range: its first and its last segment
 constexpr int kPhaseB = 8;   // page of a batch at which the next batch's page-table loads are issued
 constexpr int kPhaseC = 16;  // and at which their values are used
 constexpr int kMaxUnits = 4096;
@@ -244,12 +249,26 @@ __device__ __forceinline__ int ld_acquire(const int* p) {
   return v;
 }
 
-// Walks the unit segments of one CTA's flattened block range [pos, end).
+// Walks the unit segments of one CTA's flattened block range in processing order: the
+// range's last segment first (when the range holds more than one), then the others from the
+// start.  The last and the first segment are the ones a range boundary can cut, so both of
+// a CTA's pieces of units shared with its neighbours come early, and the cross-CTA merge of
+// those units (dependent global round trips) overlaps the streaming of the whole units.
 struct SegIter {
   const int* prefix;
-  int64_t pos, end;
+  int64_t pos, end;  // the in-order walk over [start, end of the walk)
   int u;
+  bool rot;          // the rotated-in last segment is still to come
+  int rot_u;
+  int64_t rot_lo, rot_hi;
   __device__ __forceinline__ bool next(int& uu, int64_t& lo, int64_t& hi) {
+    if (rot) {
+      rot = false;
+      uu = rot_u;
+      lo = rot_lo;
+      hi = rot_hi;
+      return true;
+    }
     while (pos < end) {
       const int64_t h = min(end, (int64_t)prefix[u + 1]);
       if (h > pos) {
@@ -275,6 +294,27 @@ __device__ __forceinline__ int unit_of(const int* prefix, int units, int64_t x, 
   return lo;
 }
 
+// The processing order of a CTA's range [start, end): its last unit segment [last_lo, end)
+// first, then [start, last_lo).  at(p) is the block at position p of that order.
+struct RangeOrder {
+  int64_t start, end, last_lo;
+  __device__ __forceinline__ int64_t at(int64_t p) const {
+    const int64_t nl = end - last_lo;
+    return p < nl ? last_lo + p : start + (p - nl);
+  }
+};
+__device__ __forceinline__ RangeOrder range_order(const int* prefix, int units, int64_t start, int64_t end) {
+  int64_t last_lo = start;
+  if (end > start) last_lo = max(start, (int64_t)prefix[unit_of(prefix, units, end - 1)]);
+  return RangeOrder{start, end, last_lo};
+}
+__device__ __forceinline__ SegIter seg_iter(const int* prefix, int units, const RangeOrder& ro) {
+  const bool rot = ro.last_lo > ro.start;  // more than one segment: the last one goes first
+  const int u_last = ro.end > ro.start ? unit_of(prefix, units, ro.end - 1) : 0;
+  return SegIter{prefix, ro.start, rot ? ro.last_lo : ro.end, unit_of(prefix, units, ro.start), rot, u_last,
+                 ro.last_lo, ro.end};
+}
+
 // Q^T fragments (B operand) of unit u: head g, dims 16 ks + 2t (+8); zero for g >= G.
 __device__ __forceinline__ void load_q(const AttnArgs& a, int u, int lane, uint32_t (&qf)[8][2]) {
   const int g = lane >> 2, t = lane & 3;
@@ -287,23 +327,86 @@ __device__ __forceinline__ void load_q(const AttnArgs& a, int u, int lane, uint3
   }
 }
 
+// A piece of a cut unit handed from the epilogue warp to the split warp in shared memory:
+// per-head LSE (natural log) then the normalised output, [G][128] fp32.
+__host__ __device__ constexpr int stage_floats(int G) { return kMaxG + G * kD; }
+
+// The CPU partial of a unit (merge only): lane l holds dims 4l .. 4l+3 of every head and the
+// LSE of head l.  Loaded ahead of its use so that the latency overlaps other work.
+struct CpuPart {
+  float4 o[kMaxG];
+  float lse;
+};
+__device__ __forceinline__ void load_cpu(const AttnArgs& a, int uu, int lane, CpuPart& cp) {
+  if (a.O_out == nullptr) return;
+#pragma unroll
+  for (int h = 0; h < kMaxG; ++h)
+    if (h < a.G) cp.o[h] = __ldcs(reinterpret_cast<const float4*>(a.O_cpu + ((int64_t)uu * a.G + h) * kD + 4 * lane));
+  cp.lse = lane < a.G ? __ldcs(a.lse_cpu + (int64_t)uu * a.G + lane) : -INFINITY;
+}
+// The final per-head GPU LSE of unit uu is in fin[]: write it (partial), or its merge with the
+// CPU partial, leaving the merge weights in wg[] / wc[] (one warp; per-warp shared scratch).
+__device__ __forceinline__ void unit_final(const AttnArgs& a, int uu, int lane, const float* fin, float* wgs,
+                                           float* wcs, const CpuPart& cp) {
+  if (lane < a.G) {
+    const int64_t r = (int64_t)uu * a.G + lane;
+    const float lg = fin[lane];
+    if (a.O_out != nullptr) {
+      const float lc = cp.lse, m = fmaxf(lg, lc);
+      float wg = 0.f, wc = 0.f, lse = -INFINITY;
+      if (m != -INFINITY) {
+        wg = expf(lg - m);
+        wc = expf(lc - m);
+        const float sum = wg + wc;
+        lse = m + logf(sum);
+        wg /= sum;
+        wc /= sum;
+      }
+      wgs[lane] = wg;
+      wcs[lane] = wc;
+      if (a.lse_out != nullptr) a.lse_out[r] = lse;
+    } else {
+      a.lse_part[r] = lg;
+    }
+  }
+  __syncwarp();
+}
+// Dims 4 lane .. 4 lane + 3 of head h of unit uu: the GPU partial o, or its merge with the CPU
+// partial by the weights unit_final left.
+__device__ __forceinline__ void store4(const AttnArgs& a, int uu, int h, int lane, float4 o, const float* wgs,
+                                       const float* wcs, const CpuPart& cpu) {
+  const int64_t off = ((int64_t)uu * a.G + h) * kD + 4 * lane;
+  if (a.O_out != nullptr) {
+    const float4 cp = cpu.o[h];
+    const float wg = wgs[h], wc = wcs[h];
+    uint2 pk;
+    pk.x = pack_bf16(wg * o.x + wc * cp.x, wg * o.y + wc * cp.y);
+    pk.y = pack_bf16(wg * o.z + wc * cp.z, wg * o.w + wc * cp.w);
+    *reinterpret_cast<uint2*>(a.O_out + off) = pk;
+  } else {
+    *reinterpret_cast<float4*>(a.O_part + off) = o;
+  }
+}
+
 template <int P, int S>
 __global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const __grid_constant__ CUtensorMap tmK,
                                                                   const __grid_constant__ CUtensorMap tmV,
                                                                   const AttnArgs a) {
   using C = Cfg<P, S>;
   extern __shared__ uint8_t smem_raw[];
-  __shared__ uint64_t full_bar[C::kStages], cfull[kMaxSlots], cempty[kMaxSlots];
+  __shared__ uint64_t full_bar[C::kStages], cfull[kMaxSlots], cempty[kMaxSlots], sbar[kMaxSplit];
   __shared__ int wtot[kThreads / 32];
-  __shared__ float ew[kMaxG][kConsumerWarps], ehm[kMaxG], ehl[kMaxG], eown[kMaxG];  // epilogue weights
-  __shared__ float efin[kMaxG], fwg[kMaxG], fwc[kMaxG];  // final LSE, merge weights
+  __shared__ float ew[kMaxG][kConsumerWarps], eown[kMaxG];  // epilogue weights
+  __shared__ float efin[kMaxG], fwg[kMaxG], fwc[kMaxG];     // epilogue final LSE, merge weights
+  __shared__ float sfin[kMaxG], swg[kMaxG], swc[kMaxG];    // split warp final LSE, merge weights
 
-  // dynamic shared memory: [ring (1024-aligned)][combine slots][unit prefix]
+  // dynamic shared memory: [ring (1024-aligned)][combine slots][split pieces][unit prefix]
   const uint32_t raw = smem_u32(smem_raw);
   uint8_t* ring = smem_raw + (((raw + 1023u) & ~1023u) - raw);
   float* cbf = reinterpret_cast<float*>(ring + C::kRingBytes);
   const int slot_f = slot_floats(a.G);
-  int* prefix = reinterpret_cast<int*>(cbf + a.nslots * slot_f);  // [units + 1]
+  float* staging = cbf + a.nslots * slot_f;  // [kMaxSplit][stage_floats(G)]
+  int* prefix = reinterpret_cast<int*>(staging + kMaxSplit * stage_floats(a.G));  // [units + 1]
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   if (tid == 0) {
@@ -312,6 +415,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const __grid_c
       mbar_init(&cfull[i], kConsumerWarps);
       mbar_init(&cempty[i], 1);
     }
+    for (int i = 0; i < kMaxSplit; ++i) mbar_init(&sbar[i], 1);
     fence_mbar_init();
   }
   if (tid == 32) {
@@ -323,7 +427,10 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const __grid_c
     const int per = (a.units + kThreads - 1) / kThreads;
     const int lo = min(a.units, tid * per), hi = min(a.units, lo + per);
     int sum = 0;
-    for (int u = lo; u < hi; ++u) sum += min(max(a.res_count[u], 0), a.k);
+    for (int u = lo; u < hi; ++u) {  // the counts are read once, kept in place of the prefix
+      prefix[u] = min(max(a.res_count[u], 0), a.k);
+      sum += prefix[u];
+    }
     int inc = sum;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -336,8 +443,9 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const __grid_c
     for (int w = 0; w < warp; ++w) base += wtot[w];
     int run = base + inc - sum;
     for (int u = lo; u < hi; ++u) {
+      const int n = prefix[u];
       prefix[u] = run;
-      run += min(max(a.res_count[u], 0), a.k);
+      run += n;
     }
     if (tid == kThreads - 1) prefix[a.units] = run;
     __syncthreads();
@@ -348,67 +456,30 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const __grid_c
 
   if (warp == kEpilogueWarp) {
     // ---------------- epilogue warp ------------------------------------------
-    const bool merge = a.O_out != nullptr;
-    // final per-head LSE of unit uu is in efin[]: write it, or merge it with the CPU partial
-    auto set_final = [&](int uu) {
-      if (lane < a.G) {
-        const int64_t r = (int64_t)uu * a.G + lane;
-        const float lg = efin[lane];
-        if (merge) {
-          const float lc = a.lse_cpu[r], m = fmaxf(lg, lc);
-          float wg = 0.f, wc = 0.f, lse = -INFINITY;
-          if (m != -INFINITY) {
-            wg = expf(lg - m);
-            wc = expf(lc - m);
-            const float sum = wg + wc;
-            lse = m + logf(sum);
-            wg /= sum;
-            wc /= sum;
-          }
-          fwg[lane] = wg;
-          fwc[lane] = wc;
-          if (a.lse_out != nullptr) a.lse_out[r] = lse;
-        } else {
-          a.lse_part[r] = lg;
-        }
-      }
-      __syncwarp();
-    };
-    // four dims of head h of unit uu: the GPU partial, or its merge with the CPU partial
-    auto store4 = [&](int uu, int h, int d, float4 o) {
-      const int64_t off = ((int64_t)uu * a.G + h) * kD + d;
-      if (merge) {
-        const float4 cp = *reinterpret_cast<const float4*>(a.O_cpu + off);
-        const float wg = fwg[h], wc = fwc[h];
-        uint2 pk;
-        pk.x = pack_bf16(wg * o.x + wc * cp.x, wg * o.y + wc * cp.y);
-        pk.y = pack_bf16(wg * o.z + wc * cp.z, wg * o.w + wc * cp.w);
-        *reinterpret_cast<uint2*>(a.O_out + off) = pk;
-      } else {
-        *reinterpret_cast<float4*>(a.O_part + off) = o;
-      }
-    };
+    CpuPart cpu;
     // units with no resident selected block: O = 0, lse = -inf
     for (int u = c; u < a.units; u += gridDim.x) {
       if (prefix[u + 1] != prefix[u]) continue;
+      load_cpu(a, u, lane, cpu);
       if (lane < a.G) efin[lane] = -INFINITY;
       __syncwarp();
-      set_final(u);
-      for (int i4 = lane; i4 < a.G * (kD / 4); i4 += 32)
-        store4(u, i4 / (kD / 4), (i4 % (kD / 4)) * 4, make_float4(0.f, 0.f, 0.f, 0.f));
+      unit_final(a, u, lane, efin, fwg, fwc, cpu);
+#pragma unroll
+      for (int h = 0; h < kMaxG; ++h)
+        if (h < a.G) store4(a, u, h, lane, make_float4(0.f, 0.f, 0.f, 0.f), fwg, fwc, cpu);
       __syncwarp();
     }
     if (c >= Gp) return;
     const int64_t start = range_start(c, N, Gp), end = range_start(c + 1, N, Gp);
-    SegIter it{prefix, start, end, unit_of(prefix, a.units, start)};
-    int u;
+    SegIter it = seg_iter(prefix, a.units, range_order(prefix, a.units, start, end));
+    int u, nsplit = 0;
     int64_t lo, hi;
     for (int sg = 0; it.next(u, lo, hi); ++sg) {
       const int slot = sg % a.nslots;
+      const bool whole = lo == prefix[u] && hi == prefix[u + 1];
+      if (whole) load_cpu(a, u, lane, cpu);  // in flight while the unit's pages still stream
       if (!mbar_wait(&cfull[slot], (uint32_t)(sg / a.nslots) & 1u) && lane == 0) report(a.status, SCOUT_DEV_TIMEOUT);
       const SlotView cs{cbf + slot * slot_f, a.G};
-      const bool whole = lo == prefix[u] && hi == prefix[u + 1];
-      const int which = prefix[u] <= start ? 0 : 1;
       // per-head weights of the four warps' states (normalised) and this piece's LSE
       if (lane < a.G) {
         float M = -INFINITY;
@@ -426,11 +497,11 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const __grid_c
       }
       __syncwarp();
       // this piece's normalised output, 4 dims per lane
-      auto own4 = [&](int h, int d) {
+      auto own4 = [&](int h) {
         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
         for (int w = 0; w < kConsumerWarps; ++w) {
-          const float4 o = *reinterpret_cast<const float4*>(cs.o(w, h) + d);
+          const float4 o = *reinterpret_cast<const float4*>(cs.o(w, h) + 4 * lane);
           const float f = ew[h][w];
           acc.x += f * o.x;
           acc.y += f * o.y;
@@ -442,123 +513,117 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const __grid_c
       if (whole) {
         if (lane < a.G) efin[lane] = eown[lane];
         __syncwarp();
-        set_final(u);
-        for (int i4 = lane; i4 < a.G * (kD / 4); i4 += 32) {
-          const int h = i4 / (kD / 4), d = (i4 % (kD / 4)) * 4;
-          store4(u, h, d, own4(h, d));
-        }
+        unit_final(a, u, lane, efin, fwg, fwc, cpu);
+#pragma unroll
+        for (int h = 0; h < kMaxG; ++h)
+          if (h < a.G) store4(a, u, h, lane, own4(h), fwg, fwc, cpu);
+      } else {
+        // a unit cut by a range boundary: the piece goes to the split warp through shared
+        // memory, so that no global round trip holds the combine slot or this warp
+        float* stg = staging + min(nsplit, kMaxSplit - 1) * stage_floats(a.G);
+        if (lane < a.G) stg[lane] = eown[lane];
+#pragma unroll
+        for (int h = 0; h < kMaxG; ++h)
+          if (h < a.G) *reinterpret_cast<float4*>(stg + kMaxG + h * kD + 4 * lane) = own4(h);
         __syncwarp();
-        if (lane == 0) mbar_arrive(&cempty[slot]);  // the combine slot may be refilled
-        continue;
+        if (lane == 0 && nsplit < kMaxSplit) mbar_arrive(&sbar[nsplit]);
+        ++nsplit;
       }
-      // a unit cut by a range boundary: pieces c0..c1, one per CTA range it touches
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&cempty[slot]);  // the combine slot may be refilled
+    }
+    return;
+  }
+
+  if (warp == kSplitWarp) {
+    // ---------------- split warp -----------------------------------------------
+    // A unit cut by range boundaries has one piece per CTA range it touches (c0 .. c1).  Each
+    // piece is published to the workspace and counted; the piece that completes the count
+    // (last to arrive) merges all of them by their LSE.  Nothing waits on another CTA.
+    if (c >= Gp) return;
+    const int64_t start = range_start(c, N, Gp), end = range_start(c + 1, N, Gp);
+    SegIter it = seg_iter(prefix, a.units, range_order(prefix, a.units, start, end));
+    int u, k = 0;
+    int64_t lo, hi;
+    CpuPart cpu;
+    while (it.next(u, lo, hi)) {
+      if (lo == prefix[u] && hi == prefix[u + 1]) continue;  // whole: the epilogue warp's
+      if (k >= kMaxSplit) break;  // a range has at most two cut segments
+      load_cpu(a, u, lane, cpu);  // used only if this piece completes the unit
+      if (!mbar_wait(&sbar[k], 0u) && lane == 0) report(a.status, SCOUT_DEV_TIMEOUT);
+      const float* stg = staging + k * stage_floats(a.G);
+      ++k;
       const int c0 = cta_of(prefix[u], N, Gp), c1 = cta_of(prefix[u + 1] - 1, N, Gp);
       auto piece_slot = [&](int cc) {
         return (int64_t)cc * 2 + (prefix[u] <= range_start(cc, N, Gp) ? 0 : 1);
       };
-      int seen = 0;
-      if (lane == 0) seen = ld_acquire(&a.counters[u]);
-      seen = __shfl_sync(0xffffffffu, seen, 0);
-      if (seen == c1 - c0) {
-        // every other piece has published: finish the unit from this piece's state
-        // and the others' partials (nothing of this piece goes through memory)
-        if (lane < a.G) {
-          float M = eown[lane];
-          for (int cc = c0; cc <= c1; ++cc)
-            if (cc != c) M = fmaxf(M, __ldcg(a.slot_lse + piece_slot(cc) * kMaxG + lane));
-          float L = 0.f;
-          if (M != -INFINITY) {
-            L = eown[lane] == -INFINITY ? 0.f : expf(eown[lane] - M);
-            for (int cc = c0; cc <= c1; ++cc)
-              if (cc != c) L += expf(__ldcg(a.slot_lse + piece_slot(cc) * kMaxG + lane) - M);
-          }
-          ehm[lane] = M;
-          ehl[lane] = L;
-          efin[lane] = L > 0.f ? M + logf(L) : -INFINITY;
-        }
-        __syncwarp();
-        set_final(u);
-        for (int i4 = lane; i4 < a.G * (kD / 4); i4 += 32) {
-          const int h = i4 / (kD / 4), d = (i4 % (kD / 4)) * 4;
-          const float M = ehm[h], L = ehl[h];
-          float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-          if (L > 0.f) {
-            if (eown[h] != -INFINITY) {
-              const float f = expf(eown[h] - M) / L;
-              const float4 o = own4(h, d);
-              acc.x = f * o.x;
-              acc.y = f * o.y;
-              acc.z = f * o.z;
-              acc.w = f * o.w;
-            }
-            for (int cc = c0; cc <= c1; ++cc) {
-              if (cc == c) continue;
-              const int64_t sl = piece_slot(cc);
-              const float f = expf(__ldcg(a.slot_lse + sl * kMaxG + h) - M) / L;
-              const float4 o = __ldcg(reinterpret_cast<const float4*>(a.slot_O + (sl * kMaxG + h) * kD + d));
-              acc.x += f * o.x;
-              acc.y += f * o.y;
-              acc.z += f * o.z;
-              acc.w += f * o.w;
-            }
-          }
-          store4(u, h, d, acc);
-        }
-        __syncwarp();
-        if (lane == 0) {
-          mbar_arrive(&cempty[slot]);
-          a.counters[u] = 0;  // ready for the next call
-        }
-        continue;
-      }
-      // publish this piece, then count it; the piece that completes the count finishes the unit
-      const int64_t msl = (int64_t)c * 2 + which;
-      if (lane < a.G) a.slot_lse[msl * kMaxG + lane] = eown[lane];
-      for (int i4 = lane; i4 < a.G * (kD / 4); i4 += 32) {
-        const int h = i4 / (kD / 4), d = (i4 % (kD / 4)) * 4;
-        reinterpret_cast<float4*>(a.slot_O + (msl * kMaxG + h) * kD + d)[0] = own4(h, d);
-      }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&cempty[slot]);  // the combine slot may be refilled
+      const int64_t msl = piece_slot(c);
+      if (lane < a.G) a.slot_lse[msl * kMaxG + lane] = stg[lane];
+#pragma unroll
+      for (int h = 0; h < kMaxG; ++h)
+        if (h < a.G)
+          *reinterpret_cast<float4*>(a.slot_O + (msl * kMaxG + h) * kD + 4 * lane) =
+              *reinterpret_cast<const float4*>(stg + kMaxG + h * kD + 4 * lane);
       __threadfence();
       __syncwarp();
       int last = 0;
       if (lane == 0) last = atomicAdd(&a.counters[u], 1) == c1 - c0;
       last = __shfl_sync(0xffffffffu, last, 0);
-      if (last) {
-        __threadfence();
-        // per head: max and sum of the pieces' LSE weights
-        if (lane < a.G) {
-          float M = -INFINITY;
-          for (int cc = c0; cc <= c1; ++cc) M = fmaxf(M, __ldcg(a.slot_lse + piece_slot(cc) * kMaxG + lane));
-          float L = 0.f;
-          if (M != -INFINITY)
-            for (int cc = c0; cc <= c1; ++cc) L += expf(__ldcg(a.slot_lse + piece_slot(cc) * kMaxG + lane) - M);
-          ehm[lane] = M;
-          ehl[lane] = L;
-          efin[lane] = L > 0.f ? M + logf(L) : -INFINITY;
-        }
-        __syncwarp();
-        set_final(u);
-        for (int i4 = lane; i4 < a.G * (kD / 4); i4 += 32) {
-          const int h = i4 / (kD / 4), d = (i4 % (kD / 4)) * 4;
-          const float M = ehm[h], L = ehl[h];
-          float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-          if (L > 0.f)
-            for (int cc = c0; cc <= c1; ++cc) {
-              const int64_t sl = piece_slot(cc);
-              const float f = expf(__ldcg(a.slot_lse + sl * kMaxG + h) - M) / L;
-              const float4 o = __ldcg(reinterpret_cast<const float4*>(a.slot_O + (sl * kMaxG + h) * kD + d));
-              acc.x += f * o.x;
-              acc.y += f * o.y;
-              acc.z += f * o.z;
-              acc.w += f * o.w;
-            }
-          store4(u, h, d, acc);
-        }
-        __syncwarp();
-        if (lane == 0) a.counters[u] = 0;  // ready for the next call
+      if (!last) continue;
+      __threadfence();
+      // merge the pieces by their LSE in one pass (running max per head): every load of a
+      // piece is issued at once, this CTA's own piece comes from shared memory
+      float mx[kMaxG], sm[kMaxG];
+      float4 acc[kMaxG];
+#pragma unroll
+      for (int h = 0; h < kMaxG; ++h) {
+        mx[h] = -INFINITY;
+        sm[h] = 0.f;
+        acc[h] = make_float4(0.f, 0.f, 0.f, 0.f);
       }
+      for (int cc = c0; cc <= c1; ++cc) {
+        float pl[kMaxG];
+        float4 po[kMaxG];
+        const int64_t sl = piece_slot(cc);
+#pragma unroll
+        for (int h = 0; h < kMaxG; ++h) {
+          if (h >= a.G) continue;
+          if (cc == c) {
+            pl[h] = stg[h];
+            po[h] = *reinterpret_cast<const float4*>(stg + kMaxG + h * kD + 4 * lane);
+          } else {
+            pl[h] = __ldcg(a.slot_lse + sl * kMaxG + h);
+            po[h] = __ldcg(reinterpret_cast<const float4*>(a.slot_O + (sl * kMaxG + h) * kD + 4 * lane));
+          }
+        }
+#pragma unroll
+        for (int h = 0; h < kMaxG; ++h) {
+          if (h >= a.G || pl[h] == -INFINITY) continue;  // a piece without tokens weighs nothing
+          const float nm = fmaxf(mx[h], pl[h]);
+          const float keep = mx[h] == -INFINITY ? 0.f : expf(mx[h] - nm), w = expf(pl[h] - nm);
+          acc[h].x = acc[h].x * keep + w * po[h].x;
+          acc[h].y = acc[h].y * keep + w * po[h].y;
+          acc[h].z = acc[h].z * keep + w * po[h].z;
+          acc[h].w = acc[h].w * keep + w * po[h].w;
+          sm[h] = sm[h] * keep + w;
+          mx[h] = nm;
+        }
+      }
+      float fin = -INFINITY;
+#pragma unroll
+      for (int h = 0; h < kMaxG; ++h)
+        if (h == lane && sm[h] > 0.f) fin = mx[h] + logf(sm[h]);
+      if (lane < a.G) sfin[lane] = fin;
+      __syncwarp();
+      unit_final(a, u, lane, sfin, swg, swc, cpu);
+#pragma unroll
+      for (int h = 0; h < kMaxG; ++h) {
+        if (h >= a.G) continue;
+        const float r = sm[h] > 0.f ? 1.f / sm[h] : 0.f;
+        store4(a, u, h, lane, make_float4(acc[h].x * r, acc[h].y * r, acc[h].z * r, acc[h].w * r), swg, swc, cpu);
+      }
+      __syncwarp();
+      if (lane == 0) a.counters[u] = 0;  // ready for the next call
     }
     return;
   }
@@ -567,6 +632,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const __grid_c
   if (c >= Gp) return;
   const int g = lane >> 2, t = lane & 3;
   const int64_t start = range_start(c, N, Gp), end = range_start(c + 1, N, Gp);
+  const RangeOrder order = range_order(prefix, a.units, start, end);
   // this warp's pages: sub-page i = warp + 4 k of the range, k = 0 .. n_mine-1, in stage i % kStages
   const int64_t n_sub = (end - start) * C::kSub;
   const int64_t n_mine = n_sub > warp ? (n_sub - 1 - warp) / kConsumerWarps + 1 : 0;
@@ -577,7 +643,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const __grid_c
     rj = -1;
     rlen = 0;
     if (kk < n_mine) {
-      const int64_t x = start + (warp + (int64_t)kConsumerWarps * kk) / C::kSub;
+      const int64_t x = order.at((warp + (int64_t)kConsumerWarps * kk) / C::kSub);
       ru = unit_of(prefix, a.units, x);
       rj = a.res_list[(int64_t)ru * a.k + (x - prefix[ru])];
       rlen = a.seq_len[ru / a.Hkv];
@@ -655,7 +721,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const __grid_c
     if (lane == 0) issue(r, row, nt);
   }
 
-  SegIter it{prefix, start, end, unit_of(prefix, a.units, start)};
+  SegIter it = seg_iter(prefix, a.units, order);
   int u;
   int64_t lo, hi;
   bool have = it.next(u, lo, hi);
@@ -774,7 +840,8 @@ constexpr size_t kSlotOBytes = (size_t)kMaxGrid * 2 * kMaxG * kD * sizeof(float)
 
 template <int P, int S>
 size_t dyn_smem(int units, int G, int nslots) {
-  return 1024 + Cfg<P, S>::kRingBytes + (size_t)nslots * slot_floats(G) * sizeof(float) + (size_t)(units + 1) * 4;
+  return 1024 + Cfg<P, S>::kRingBytes + (size_t)nslots * slot_floats(G) * sizeof(float) +
+         (size_t)kMaxSplit * stage_floats(G) * sizeof(float) + (size_t)(units + 1) * 4;
 }
 constexpr size_t kSmemLimit = 232448 - 1024;  // per-block shared memory minus room for static use
 
