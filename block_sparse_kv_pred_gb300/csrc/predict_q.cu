@@ -6,7 +6,9 @@
 // computed swapped: D[n][m] = sum_k W[n][k] X[m][k].  A CTA owns 128 rows of W (the
 // MMA's M = 128 TMEM lanes); the batch, padded to a multiple of 16, is the MMA's N.
 // W and X tiles (64 k-columns, 128-byte swizzle) stream in by TMA through a ring of
-// shared-memory stages guarded by mbarriers; one thread issues tcgen05.mma into a
+// shared-memory stages guarded by mbarriers, up to four k-blocks per stage (measured on
+// GB300: one k-block per stage streams ~25% slower, the barrier round trip of a stage
+// being paid per 22 KB instead of per 88 KB); one thread issues tcgen05.mma into a
 // TMEM accumulator and frees each stage with tcgen05.commit.  The K dimension is
 // split over the CTAs of a thread-block cluster so that about one CTA runs per SM.
 // The batch columns of the accumulator are dealt out over the cluster's CTAs: each
@@ -20,7 +22,8 @@ namespace scout {
 namespace {
 
 constexpr int kBM = 128;      // W rows per CTA (MMA M)
-constexpr int kBK = 64;       // k columns per stage (one 128-byte swizzle atom of bf16)
+constexpr int kBK = 64;       // k columns per k-block (one 128-byte swizzle atom of bf16)
+constexpr int kMaxKps = 4;    // k-blocks per ring stage, at most
 constexpr int kStages = 16;  // upper bound; the ring takes what shared memory holds
 constexpr int kThreadsQ = 128;
 constexpr int kMaxN = 256;    // padded batch (MMA N) limit
@@ -99,15 +102,18 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int n) {
 struct GemmArgs {
   __nv_bfloat16* Q;
   int M, N, n_pad, tmem_cols, kblocks, stages, x_tile_bytes;
+  int kps;  // k-blocks per ring stage
   int32_t* status;
 };
 
-// Stage i of CTA (tile, split range starting at k-block kb0): the W tile and the X tile.
-__device__ __forceinline__ void load_stage(uint8_t* sW, const CUtensorMap* tmW, const CUtensorMap* tmX,
-                                           const GemmArgs& a, int tile, int kb, uint64_t* bar, int stage_bytes) {
-  mbar_arrive_tx(bar, (uint32_t)stage_bytes);
-  tma_load_2d(sW, tmW, kb * kBK, tile * kBM, bar);
-  tma_load_2d(sW + kWTileBytes, tmX, kb * kBK, 0, bar);
+// A ring stage holds nk <= kps consecutive k-blocks: their W tiles first, then their X tiles.
+__device__ __forceinline__ void load_stage(uint8_t* st, const CUtensorMap* tmW, const CUtensorMap* tmX,
+                                           const GemmArgs& a, int tile, int kb, int nk, uint64_t* bar) {
+  mbar_arrive_tx(bar, (uint32_t)(nk * (kWTileBytes + a.x_tile_bytes)));
+  for (int j = 0; j < nk; ++j) {
+    tma_load_2d(st + j * kWTileBytes, tmW, (kb + j) * kBK, tile * kBM, bar);
+    tma_load_2d(st + a.kps * kWTileBytes + j * a.x_tile_bytes, tmX, (kb + j) * kBK, 0, bar);
+  }
 }
 
 __global__ void __launch_bounds__(kThreadsQ, 1) predict_q_kernel(const __grid_constant__ CUtensorMap tmW,
@@ -118,18 +124,19 @@ __global__ void __launch_bounds__(kThreadsQ, 1) predict_q_kernel(const __grid_co
   __shared__ uint32_t tmem_slot;
   const uint32_t raw = smem_u32(smem_raw);
   uint8_t* base = smem_raw + (((raw + 1023u) & ~1023u) - raw);
-  const int stage_bytes = kWTileBytes + a.x_tile_bytes;
+  const int stage_bytes = a.kps * (kWTileBytes + a.x_tile_bytes);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int tile = blockIdx.x;
   const uint32_t S = gridDim.y, rank = cluster_rank();
   const int kb0 = (int)(rank * a.kblocks / S), kb1 = (int)((rank + 1) * a.kblocks / S);
-  const int nkb = kb1 - kb0;
+  const int nst = (kb1 - kb0 + a.kps - 1) / a.kps;  // ring stages of this CTA's k range
+  auto nk_of = [&](int i) { return min(a.kps, kb1 - kb0 - i * a.kps); };
   // a kernel launched after this one as a programmatic dependent (scout_score_topk) may start
   // as soon as SMs free up; it waits for this grid to finish before it reads Q
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
   // the first pass over the ring needs no free slot: issue it before the TMEM allocation
-  const int first = min(a.stages, nkb);
+  const int first = min(a.stages, nst);
   if (tid == 0) {
     for (int i = 0; i < a.stages; ++i) {
       mbar_init(&full_bar[i], 1);
@@ -140,7 +147,7 @@ __global__ void __launch_bounds__(kThreadsQ, 1) predict_q_kernel(const __grid_co
     prefetch_tmap(&tmW);
     prefetch_tmap(&tmX);
     for (int i = 0; i < first; ++i)
-      load_stage(base + i * stage_bytes, &tmW, &tmX, a, tile, kb0 + i, &full_bar[i], stage_bytes);
+      load_stage(base + i * stage_bytes, &tmW, &tmX, a, tile, kb0 + i * a.kps, nk_of(i), &full_bar[i]);
   }
   if (warp == 2) tmem_alloc(&tmem_slot, (uint32_t)a.tmem_cols);
   tc_fence_before();
@@ -151,13 +158,13 @@ __global__ void __launch_bounds__(kThreadsQ, 1) predict_q_kernel(const __grid_co
   if (warp == 0 && lane == 0) {
     // TMA producer: the rest of the k range, each stage once the MMAs have freed it
     int issued = first;
-    for (int i = first; i < nkb; ++i) {
+    for (int i = first; i < nst; ++i) {
       const int st = i % a.stages;
       if (!mbar_wait(&empty_bar[st], ((i / a.stages) & 1) ^ 1)) {
         report(a.status, SCOUT_DEV_TIMEOUT);
         break;
       }
-      load_stage(base + st * stage_bytes, &tmW, &tmX, a, tile, kb0 + i, &full_bar[st], stage_bytes);
+      load_stage(base + st * stage_bytes, &tmW, &tmX, a, tile, kb0 + i * a.kps, nk_of(i), &full_bar[st]);
       issued = i + 1;
     }
     // every issued copy lands before the CTA can retire
@@ -168,17 +175,22 @@ __global__ void __launch_bounds__(kThreadsQ, 1) predict_q_kernel(const __grid_co
   } else if (warp == 1 && lane == 0) {
     // MMA issuer
     const uint32_t idesc = idesc_bf16(a.n_pad);
-    for (int i = 0; i < nkb; ++i) {
+    for (int i = 0; i < nst; ++i) {
       const int st = i % a.stages;
       if (!mbar_wait(&full_bar[st], (i / a.stages) & 1)) {
         report(a.status, SCOUT_DEV_TIMEOUT);
         break;
       }
       tc_fence_after();
-      const uint32_t sW = smem_u32(base + st * stage_bytes), sX = sW + kWTileBytes;
+      const uint32_t s0 = smem_u32(base + st * stage_bytes);
+      const int nk = nk_of(i);
+      for (int j = 0; j < nk; ++j) {
+        const uint32_t sW = s0 + j * kWTileBytes, sX = s0 + a.kps * kWTileBytes + j * a.x_tile_bytes;
 #pragma unroll
-      for (int kk = 0; kk < kBK / 16; ++kk)
-        umma_bf16(tmem, sw128_desc(sW + kk * 32), sw128_desc(sX + kk * 32), idesc, (i > 0 || kk > 0) ? 1u : 0u);
+        for (int kk = 0; kk < kBK / 16; ++kk)
+          umma_bf16(tmem, sw128_desc(sW + kk * 32), sw128_desc(sX + kk * 32), idesc,
+                    (i > 0 || j > 0 || kk > 0) ? 1u : 0u);
+      }
       umma_commit(&empty_bar[st]);
     }
     umma_commit(&done_bar);
@@ -257,8 +269,12 @@ extern "C" int scout_predict_q(const void* X, const void* W, void* Q, int M, int
   while (a.tmem_cols < a.n_pad) a.tmem_cols <<= 1;
   a.kblocks = K / kBK;
   a.x_tile_bytes = (a.n_pad * 128 + 1023) / 1024 * 1024;
-  const int stage_bytes = kWTileBytes + a.x_tile_bytes;
-  a.stages = min(kStages, (224 * 1024) / stage_bytes);  // ~220 KB in flight per SM
+  // ~220 KB in flight per SM, in stages of up to kMaxKps k-blocks (the fewer the stages, the
+  // fewer barrier round trips per byte) but at least two, so that copies and MMAs overlap
+  constexpr int kRingBytes = 224 * 1024;
+  a.kps = max(1, min(kMaxKps, kRingBytes / 2 / (kWTileBytes + a.x_tile_bytes)));
+  const int stage_bytes = a.kps * (kWTileBytes + a.x_tile_bytes);
+  a.stages = min(kStages, kRingBytes / stage_bytes);
   a.status = dev_status;
   const int tiles = N / kBM;
   const int cap = launch != nullptr && launch->max_ctas > 0 ? launch->max_ctas : sm_count();
