@@ -14,10 +14,10 @@
 //  * warps 8..11 select the units as their chunks are scored, one warp per unit and up
 //    to four units at a time: radix select of the k-th key, then one ordered compaction
 //    into top-k, resident, CPU and delta lists.
-// CTA c owns the contiguous item range [c I / Gp, (c+1) I / Gp), so almost every unit
-// is scored and selected inside one CTA; a unit cut by a range boundary goes through
-// global memory and is selected by whichever of its CTAs adds its last chunks to a
-// per-unit counter.
+// Whole units are dealt out to the CTAs one at a time from a ticket counter in the
+// workspace: a unit is always scored and selected inside one CTA, and a CTA that starts
+// late (its SM was still busy with another kernel when the grid launched) or draws short
+// units takes more of them, so a grid of one CTA per SM fills SMs as they free up.
 #include <mutex>
 
 #include "common.cuh"
@@ -160,9 +160,9 @@ struct TopkArgs {
   int nkbuf;  // key buffers in shared memory (2 .. kMaxKeyBufs)
   int nsel;   // selector warps in use (1 .. min(kSelWarps, nkbuf - 1))
   int user_scores;  // 1: the caller asked for every pooled score in `scores`
-  int64_t n_items;
-  float* scores;  // user buffer or workspace
-  int32_t* counters;
+  int units;
+  float* scores;  // the caller's buffer, written only when user_scores
+  int32_t* counters;  // [0]: the unit ticket counter (zero between calls)
   int32_t* status;
   int32_t *topk_idx, *topk_count, *res_list, *res_count, *cpu_list, *cpu_count, *delta_list, *delta_count;
 };
@@ -455,7 +455,9 @@ template <int KIND>
 __global__ void __launch_bounds__(kThreadsAll, 1) score_topk_kernel(const __grid_constant__ CUtensorMap tmD,
                                                                     const TopkArgs a) {
   extern __shared__ uint8_t smem_raw[];
-  __shared__ uint64_t full_bar[kMaxStagesT], empty_bar[kMaxStagesT], kfull[kMaxKeyBufs], kempty[kMaxKeyBufs];
+  __shared__ uint64_t full_bar[kMaxStagesT], empty_bar[kMaxStagesT], kfull[kMaxKeyBufs], kempty[kMaxKeyBufs],
+      kunit_bar[kMaxKeyBufs];
+  __shared__ int stage_unit[kMaxStagesT], kunit[kMaxKeyBufs];  // unit of a stage / of a key buffer, -1 = end
   // dynamic shared memory: [ring (1024-aligned)][nkbuf key buffers][nsel selector-warp areas]
   const uint32_t raw = smem_u32(smem_raw);
   uint8_t* ring = smem_raw + (((raw + 1023u) & ~1023u) - raw);
@@ -470,65 +472,82 @@ __global__ void __launch_bounds__(kThreadsAll, 1) score_topk_kernel(const __grid
     for (int i = 0; i < a.nkbuf; ++i) {
       mbar_init(&kfull[i], kScoreWarps);
       mbar_init(&kempty[i], 1);
+      mbar_init(&kunit_bar[i], 1);
     }
     fence_mbar_init();
   }
   __syncthreads();
-  const int64_t Gp = gridDim.x;  // the host launches at most one CTA per item
-  const int64_t it0 = blockIdx.x * a.n_items / Gp, it1 = (blockIdx.x + 1) * a.n_items / Gp;
-  const int u_first = (int)(it0 / a.nchunk), u_last = (int)((it1 - 1) / a.nchunk);
 
   if (warp == kProducer) {
     // ---------------- producer warp ------------------------------------------
+    // Units are dealt out one at a time from a ticket counter, so a CTA that starts late
+    // (its SM was busy) or scores a short unit simply takes more of them.  Every CTA draws
+    // exactly one ticket past the last unit; the draw of the launch's very last ticket
+    // resets the counter for the next call.
     if (lane != 0) return;
     prefetch_tmap(&tmD);
-    int64_t issued = 0;
-    bool q_ready = false;
-    // item it0 + i is chunk ch of unit u; the valid-block count of the next unit is loaded a
-    // unit ahead, so no item waits on a global load before its copies are issued
-    int u = (int)(it0 / a.nchunk), ch = (int)(it0 - (int64_t)u * a.nchunk);
-    int nv = unit_nvalid(a, u / a.Hkv);
-    int nv_next = u < u_last ? unit_nvalid(a, (u + 1) / a.Hkv) : 0;
-    for (int64_t i = 0; i < it1 - it0; ++i, ++ch) {
-      if (ch == a.nchunk) {
-        ch = 0;
-        ++u;
-        nv = nv_next;
-        nv_next = u < u_last ? unit_nvalid(a, (u + 1) / a.Hkv) : 0;
-      }
+    const int last_ticket = a.units + (int)gridDim.x - 1;
+    auto take = [&]() {
+      const int t = atomicAdd(a.counters, 1);
+      if (t == last_ticket) *a.counters = 0;
+      return t < a.units ? t : -1;
+    };
+    int64_t i = 0;  // stages issued
+    bool q_ready = false, ok = true;
+    // the next unit's ticket and length are fetched a unit ahead, so no stage waits on them
+    int u = take();
+    int nv = u >= 0 ? unit_nvalid(a, u / a.Hkv) : 0;
+    while (u >= 0 && ok) {
+      const int u_next = take();
+      const int nv_next = u_next >= 0 ? unit_nvalid(a, u_next / a.Hkv) : 0;
       const int b = u / a.Hkv, kvh = u - b * a.Hkv;
-      const int st = (int)(i % a.stages);
-      if (!mbar_wait(&empty_bar[st], (uint32_t)((i / a.stages) & 1) ^ 1u)) {
-        report(a.status, SCOUT_DEV_TIMEOUT);
-        break;
-      }
-      uint8_t* sp = ring + st * kStageBytesT;
-      if (ch * kChunk < nv) {
-        const bool with_q = i == 0 || ch == 0;  // the scoring warps read q on a unit's first item
-        mbar_arrive_tx(&full_bar[st], 4 * kBoxBytes + (with_q ? a.G * kD * 2 : 0));
-        const int y = u * a.nblk_cap + ch * kChunk;
-#pragma unroll
-        for (int bx = 0; bx < 4; ++bx) tma_load_2d(sp + bx * kBoxBytes, &tmD, bx * 64, y, &full_bar[st]);
-        const __nv_bfloat16* qg = a.q + ((int64_t)b * a.Hq + (int64_t)kvh * a.G) * kD;
-        if (with_q && !q_ready) {
-          // launched as a programmatic dependent: q is written by the previous kernel on the
-          // stream, so wait for it here (digest loads above need not); a no-op otherwise
-          asm volatile("griddepcontrol.wait;" ::: "memory");
-          q_ready = true;
+      for (int ch = 0; ch < a.nchunk; ++ch, ++i) {
+        const int st = (int)(i % a.stages);
+        if (!mbar_wait(&empty_bar[st], (uint32_t)((i / a.stages) & 1) ^ 1u)) {
+          report(a.status, SCOUT_DEV_TIMEOUT);
+          ok = false;
+          break;
         }
-        for (int h = 0; h < (with_q ? a.G : 0); ++h)
-          asm volatile(
-              "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-                  smem_u32(sp + 4 * kBoxBytes + h * kQStride * 2)),
-              "l"(qg + h * kD), "r"(kD * 2), "r"(smem_u32(&full_bar[st]))
-              : "memory");
-      } else {
-        mbar_arrive(&full_bar[st]);
+        stage_unit[st] = u;  // published by the arrive below
+        uint8_t* sp = ring + st * kStageBytesT;
+        if (ch * kChunk < nv) {
+          const bool with_q = ch == 0;  // the scoring warps read q on a unit's first chunk
+          mbar_arrive_tx(&full_bar[st], 4 * kBoxBytes + (with_q ? a.G * kD * 2 : 0));
+          const int y = u * a.nblk_cap + ch * kChunk;
+#pragma unroll
+          for (int bx = 0; bx < 4; ++bx) tma_load_2d(sp + bx * kBoxBytes, &tmD, bx * 64, y, &full_bar[st]);
+          const __nv_bfloat16* qg = a.q + ((int64_t)b * a.Hq + (int64_t)kvh * a.G) * kD;
+          if (with_q && !q_ready) {
+            // launched as a programmatic dependent: q is written by the previous kernel on the
+            // stream, so wait for it here (digest loads above need not); a no-op otherwise
+            asm volatile("griddepcontrol.wait;" ::: "memory");
+            q_ready = true;
+          }
+          for (int h = 0; h < (with_q ? a.G : 0); ++h)
+            asm volatile(
+                "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                    smem_u32(sp + 4 * kBoxBytes + h * kQStride * 2)),
+                "l"(qg + h * kD), "r"(kD * 2), "r"(smem_u32(&full_bar[st]))
+                : "memory");
+        } else {
+          mbar_arrive(&full_bar[st]);
+        }
       }
-      issued = i + 1;
+      u = u_next;
+      nv = nv_next;
     }
-    for (int64_t r = 0; r < a.stages && r < issued; ++r) {  // every copy lands before the CTA retires
-      const int64_t last = issued - 1 - r;
+    if (ok) {  // a stage tagged -1 ends the scoring warps' loop
+      const int st = (int)(i % a.stages);
+      if (mbar_wait(&empty_bar[st], (uint32_t)((i / a.stages) & 1) ^ 1u)) {
+        stage_unit[st] = -1;
+        mbar_arrive(&full_bar[st]);
+        ++i;
+      } else {
+        report(a.status, SCOUT_DEV_TIMEOUT);
+      }
+    }
+    for (int64_t r = 0; r < a.stages && r < i; ++r) {  // every copy lands before the CTA retires
+      const int64_t last = i - 1 - r;
       if (!mbar_wait(&full_bar[last % a.stages], (uint32_t)((last / a.stages) & 1))) report(a.status, SCOUT_DEV_TIMEOUT);
     }
     return;
@@ -536,40 +555,26 @@ __global__ void __launch_bounds__(kThreadsAll, 1) score_topk_kernel(const __grid
 
   if (warp >= kScoreWarps) {
     // ---------------- selector warps 8..11 -----------------------------------
-    // unit e of the range (e = u - u_first) sits in key buffer e % nkbuf and is selected
-    // by selector warp e % nsel, so up to nsel units are selected at once
+    // the e-th unit of this CTA sits in key buffer e % nkbuf and is selected by selector
+    // warp e % nsel, so up to nsel units are selected at once; its id arrives when its
+    // scoring starts, so the residency bits load while it is scored
     const int sw_i = warp - kScoreWarps;
     if (sw_i >= a.nsel) return;
     uint32_t* area = keybuf + a.nkbuf * align4(a.nblk_cap) + sw_i * selwarp_words(a.words);
     const SelWarp sw = selwarp_at(area, a.words);
-    for (int u = u_first + sw_i; u <= u_last; u += a.nsel) {
-      const int e = u - u_first, kb = e % a.nkbuf;
+    for (int e = sw_i;; e += a.nsel) {
+      const int kb = e % a.nkbuf;
+      if (!mbar_wait(&kunit_bar[kb], (uint32_t)(e / a.nkbuf) & 1u)) {
+        if (lane == 0) report(a.status, SCOUT_DEV_TIMEOUT);
+        return;
+      }
+      const int u = kunit[kb];
+      if (u < 0) return;
       uint32_t* keys = keybuf + kb * align4(a.nblk_cap);
       prefetch_unit(a, u, sw, lane);  // overlaps the scoring of u
       const int nvalid = unit_nvalid(a, u / a.Hkv);
       if (!mbar_wait(&kfull[kb], (uint32_t)(e / a.nkbuf) & 1u) && lane == 0) report(a.status, SCOUT_DEV_TIMEOUT);
-      const int64_t first = (int64_t)u * a.nchunk, last = first + a.nchunk - 1;
-      bool doit = first >= it0 && last < it1;  // the whole unit was scored here
-      if (!doit) {
-        int flag = 0;
-        if (lane == 0) {
-          const int64_t mine = min(last, it1 - 1) - max(first, it0) + 1;
-          __threadfence();  // publish this CTA's scores of u
-          const int old = atomicAdd(&a.counters[u], (int)mine);
-          flag = old + (int)mine == a.nchunk;
-          if (flag) {
-            __threadfence();  // see the other CTAs' scores of u
-            a.counters[u] = 0;  // ready for the next call
-          }
-        }
-        doit = __shfl_sync(0xffffffffu, flag, 0) != 0;
-        if (doit) {
-          const float* scu = a.scores + (int64_t)u * a.nblk_cap;
-          for (int j = lane; j < nvalid; j += 32) keys[j] = score_key(__ldcg(scu + j));
-          __syncwarp();
-        }
-      }
-      if (doit) select_unit(a, u, keys, nvalid, sw, lane);
+      select_unit(a, u, keys, nvalid, sw, lane);
       __syncwarp();
       if (lane == 0) mbar_arrive(&kempty[kb]);  // the key buffer may be refilled
     }
@@ -578,29 +583,28 @@ __global__ void __launch_bounds__(kThreadsAll, 1) score_topk_kernel(const __grid
 
   // ---------------- scoring warps 0..7 -----------------------------------------
   const int g = lane >> 2, t = lane & 3;
-  int ucur = -1, kb = 0;
-  bool split = false;
+  int ucur = -1, kb = 0, e = -1, ch = 0, nvalid = 0;
   uint32_t bmm[16][2], bme[8][2];
-  // item it0 + i is chunk ch of unit u, in stage st
-  int u = (int)(it0 / a.nchunk), ch = (int)(it0 - (int64_t)u * a.nchunk), st = 0;
-  int nvalid = unit_nvalid(a, u / a.Hkv);
-  for (int64_t i = 0; i < it1 - it0; ++i) {
-    if (ch == a.nchunk) {
-      ch = 0;
-      ++u;
-      nvalid = unit_nvalid(a, u / a.Hkv);
-    }
+  for (int64_t i = 0;; ++i) {
+    const int st = (int)(i % a.stages);
     const bool landed = mbar_wait(&full_bar[st], (uint32_t)((i / a.stages) & 1));
     if (!landed && lane == 0) report(a.status, SCOUT_DEV_TIMEOUT);
+    const int u = landed ? stage_unit[st] : -1;
+    if (u < 0) break;
     const uint8_t* sp = ring + st * kStageBytesT;
-    if (u != ucur) {  // the unit's first item in this range
+    if (u != ucur) {  // the unit's first chunk: take its key buffer and read its query group
       ucur = u;
-      const int e = u - u_first;
+      ch = 0;
+      ++e;
       kb = e % a.nkbuf;
-      split = (int64_t)u * a.nchunk < it0 || (int64_t)u * a.nchunk + a.nchunk - 1 >= it1;
+      nvalid = unit_nvalid(a, u / a.Hkv);
       if (!mbar_wait(&kempty[kb], ((uint32_t)(e / a.nkbuf) & 1u) ^ 1u) && lane == 0)
         report(a.status, SCOUT_DEV_TIMEOUT);
-      if (ch * kChunk < nvalid && landed) {
+      if (warp == 0 && lane == 0) {
+        kunit[kb] = u;
+        mbar_arrive(&kunit_bar[kb]);
+      }
+      if (nvalid > 0) {
         const __nv_bfloat16* qs = reinterpret_cast<const __nv_bfloat16*>(sp + 4 * kBoxBytes);
         if (KIND == SCOUT_DIGEST_MINMAX) {
           minmax_b_frag(qs, a.G, lane, bmm);
@@ -612,7 +616,7 @@ __global__ void __launch_bounds__(kThreadsAll, 1) score_topk_kernel(const __grid
     const int j0 = ch * kChunk + warp * 16;
     if (j0 < a.nblk_cap) {
       float c[4] = {0.f, 0.f, 0.f, 0.f};
-      if (j0 < nvalid && landed) score_tile<KIND>(smem_u32(sp), warp * 16, lane, bmm, bme, c);
+      if (j0 < nvalid) score_tile<KIND>(smem_u32(sp), warp * 16, lane, bmm, bme, c);
       // pool over the heads of the group (columns 2t, 2t+1 < G), then across t
       const float ninf = -INFINITY;
       float m0 = fmaxf(2 * t < a.G ? c[0] : ninf, 2 * t + 1 < a.G ? c[1] : ninf);
@@ -626,7 +630,7 @@ __global__ void __launch_bounds__(kThreadsAll, 1) score_topk_kernel(const __grid
         uint32_t* keys = keybuf + kb * align4(a.nblk_cap);
         if (r0 < nvalid) keys[r0] = score_key(m0);
         if (r1 < nvalid) keys[r1] = score_key(m1);
-        if (a.user_scores || split) {
+        if (a.user_scores) {
           float* scu = a.scores + (int64_t)u * a.nblk_cap;
           if (r0 < a.nblk_cap) scu[r0] = r0 < nvalid ? m0 : ninf;
           if (r1 < a.nblk_cap) scu[r1] = r1 < nvalid ? m1 : ninf;
@@ -636,10 +640,19 @@ __global__ void __launch_bounds__(kThreadsAll, 1) score_topk_kernel(const __grid
     __syncwarp();
     if (lane == 0) {
       mbar_arrive(&empty_bar[st]);
-      if (ch == a.nchunk - 1 || i == it1 - it0 - 1) mbar_arrive(&kfull[kb]);  // this warp's keys of u are in
+      if (ch == a.nchunk - 1) mbar_arrive(&kfull[kb]);  // this warp's keys of u are in
     }
     ++ch;
-    if (++st == a.stages) st = 0;
+  }
+  // no more units: an id of -1 in the next key buffer of every selector warp ends its loop
+  for (int j = 0; j < a.nsel; ++j) {
+    const int e2 = e + 1 + j, kb2 = e2 % a.nkbuf;
+    if (!mbar_wait(&kempty[kb2], ((uint32_t)(e2 / a.nkbuf) & 1u) ^ 1u) && lane == 0)
+      report(a.status, SCOUT_DEV_TIMEOUT);
+    if (warp == 0 && lane == 0) {
+      kunit[kb2] = -1;
+      mbar_arrive(&kunit_bar[kb2]);
+    }
   }
 }
 
@@ -692,7 +705,7 @@ extern "C" int scout_score_topk(int kind, const void* q, const void* digest, con
   a.k = k;
   a.words = (nblk_cap + 31) / 32;
   a.nchunk = (nblk_cap + kChunk - 1) / kChunk;
-  a.n_items = units * a.nchunk;
+  a.units = (int)units;
   a.counters = static_cast<int32_t*>(workspace);
   a.status = nullptr;
   a.user_scores = scores != nullptr;
@@ -741,7 +754,7 @@ extern "C" int scout_score_topk(int kind, const void* q, const void* digest, con
       cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, 100) != cudaSuccess)
     return SCOUT_ERR_CUDA;
   const int cap = launch != nullptr && launch->max_ctas > 0 ? launch->max_ctas : sm_count();
-  const int grid = (int)(a.n_items < (int64_t)cap ? a.n_items : (int64_t)cap);  // <= one CTA per item
+  const int grid = (int)(units < (int64_t)cap ? units : (int64_t)cap);  // <= one CTA per unit
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)grid);
   cfg.blockDim = dim3(kThreadsAll);

@@ -235,8 +235,8 @@ def _check_integer_case(c, kind, max_ctas=None, min_ties=0):
 @pytest.mark.parametrize("max_ctas", [None, 1, 2, 3])
 @pytest.mark.parametrize("kind", ["minmax", "mean"])
 def test_score_topk_bit_exact_on_exact_scores(kind, max_ctas):
-    """Uncapped, every unit is scored by several CTAs and selected by the last one to finish; with
-    a CTA cap a CTA scores whole units and selects them itself: both give the oracle's lists."""
+    """Whole units are dealt to the CTAs from a ticket counter: one CTA per unit (uncapped) and
+    grids of 1 to 3 CTAs that each take many units give the oracle's lists."""
     _check_integer_case(_integer_case(kind), kind, max_ctas, min_ties=100)
 
 
