@@ -824,7 +824,8 @@ extern "C" int scout_score_topk_noalloc(int kind, const void* q, const void* dig
   void* scratch = nullptr;
   const int rc = scratch_address(&scratch);
   if (rc != SCOUT_OK) return rc;
-  // the array keeps whatever the previous call left: zero the per-unit counters
+  // the array keeps whatever the previous call left (a timed-out call may leave the unit
+  // ticket counter non-zero): zero the counters
   if (cudaMemsetAsync(scratch, 0, counters_bytes((int64_t)B * Hkv), stream) != cudaSuccess) return SCOUT_ERR_CUDA;
   return scout_score_topk(kind, q, digest, seq_len, resident_bits, prev_cpu_list, prev_cpu_count, B, Hq, Hkv, D, P,
                           nblk_cap, k, scores, topk_idx, topk_count, res_list, res_count, cpu_list, cpu_count,
