@@ -364,6 +364,17 @@ def config_of(s, world, split=None):
             "parallelism": f"independent replicas x{world} (one batch of sequences per GPU)"}
 
 
+def attention_path(s, nbytes, kern_ms, peak):
+    """The selection and attention kernels on their own: B * Hq over the sum of their durations
+    (the merge runs inside the attention kernel), with the bytes they move over that time."""
+    ms = kern_ms["score_topk"] + kern_ms["sparse_attn_merge"]
+    nb = nbytes["score_topk"] + nbytes["sparse_attn_merge"]
+    gbs = nb / (ms / 1e3) / 1e9
+    return {"value": s.B * s.Hq / (ms / 1e3), "unit": "query-heads/s", "ms": ms, "bytes": nb, "GB_s": gbs,
+            "frac_of_hbm_peak": gbs / peak,
+            "note": "score_topk + sparse_attn_merge concurrent durations summed (they overlap inside the step)"}
+
+
 def traffic_of(kernel):
     """DRAM bytes per launch from the committed ncu summary, if the kernel source is unchanged since."""
     import hashlib
@@ -434,6 +445,7 @@ def main():
                                                           "d2h_bytes_per_step", "ms_per_step")},
         "gpu_launches": r["launches"], "clocks": r["clocks"], "kernels": kernels,
         "kv_tokens_per_s": nbytes["_res_blocks"] * s.P / (r["kern_ms"]["sparse_attn_merge"] / 1e3),
+        "attention_path": attention_path(s, nbytes, r["kern_ms"], peak),
         "wall_s_timed": r["wall"],
     }
     if world == 1 and not args.no_cpu_baseline:
