@@ -1,18 +1,20 @@
 #!/usr/bin/env python
 """Decode-step benchmark of libscout on the Qwen3-14B-shaped layer.
 
-One step = the whole GPU hot path of one layer's decode step, issued as three
-streams (layer-ahead prediction, ScoutAttention Algorithm 1), the persistent
-kernels on disjoint SMs:
-  selection stream: predict_q (Q_pred = X W_Q^T, 40 x 5120 x 5120), then
-    score_topk (digest scores with Q_pred, top-64 of 1024 blocks, residency split);
+One step = the whole GPU hot path of one layer's decode step (ScoutAttention
+Algorithm 1, layer-ahead prediction), issued on four streams with the persistent
+kernels capped to share the SMs:
+  GEMM stream: predict_q (next layer's Q_pred = X W_Q^T, 40 x 5120 x 5120), after the
+    previous step's attention (its output is this step's layer input);
+  selection stream: score_topk (digest scores with Q_pred, top-64 of 1024 blocks,
+    residency split), after this step's GEMM;
   attention stream: sparse_attn_merge (true query over the resident blocks the
     previous step selected, merged with the CPU partial);
   append stream: build_digest (append: the tail block of every (sequence, KV head)).
 Metric: decode-attention query-heads per second (B * Hq per step, summed over ranks).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--config qwen3_14b] [--impl scout|reference]
-                  [--serial] [--split SEL,ATTN]
+                  [--serial] [--split GEMM,SEL,ATTN]
 
 --impl reference times the fp64 oracle (the plain CPU implementation) on this
 machine's host cores on a bounded sample of the same workload.
@@ -46,7 +48,9 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing leg")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="target oracle time for cpu_baseline")
     ap.add_argument("--serial", action="store_true", help="one stream, full grids (no overlap)")
-    ap.add_argument("--split", default=None, help="CTAs of the selection,attention kernels (default 80,72)")
+    ap.add_argument("--split", default=None,
+                    help="CTAs of the GEMM,selection,attention kernels (default 80,0,72, 0 = one per SM; two "
+                         "values: GEMM and selection share the first)")
     a = ap.parse_args()
     a.warmup = max(a.warmup, 3)
     return a
@@ -353,14 +357,22 @@ METRIC = "sparse-decode query-heads/s and achieved HBM GB/s vs ~8 TB/s (1xGB300)
 DATA = "synthetic: seeded Qwen3-14B-shaped K/V/q/X/W_Q (stand-in for LongBench prompts and trained weights)"
 
 
+def streams_of(split):
+    if not split:
+        return "one stream"
+    g, sel, att = split if len(split) == 3 else (split[0], split[0], split[1])
+    n = lambda c: f"{c} CTAs" if c else "one CTA per SM"  # noqa: E731
+    return (f"GEMM ({n(g)}) after the previous attention || selection ({n(sel)}) after the GEMM || "
+            f"attention ({n(att)}) after the previous selection || digest append")
+
+
 def config_of(s, world, split=None):
     return {"workload": s.name, "batch": s.B, "q_heads": s.Hq, "kv_heads": s.Hkv, "head_dim": s.D,
             "context": s.T, "page": s.P, "budget_tokens": s.k * s.P, "resident_frac": s.resident_frac,
             "digest": s.kind, "gemm_mnk": [s.B, s.Hq * s.D, s.hidden],
             "l2": "not flushed: one step reads inputs larger than L2 (see step_input_bytes), in an order "
                   "that evicts each input before its next use",
-            "streams": f"selection on {split[0]} CTAs || attention on {split[1]} CTAs || digest append" if split
-            else "one stream",
+            "streams": streams_of(split),
             "parallelism": f"independent replicas x{world} (one batch of sequences per GPU)"}
 
 

@@ -2,27 +2,30 @@
 
 ScoutAttention (arXiv HTML), Algorithm 1 (layer-ahead prediction): while layer i
 attends with the block set chosen one layer earlier, the next layer's query is
-predicted and its top-k chosen.  The two halves touch disjoint data, so a step
-is issued as two CUDA streams on disjoint SMs (``scout_launch.max_ctas``):
+predicted and its top-k chosen.  Step i here is layer i's attention together with
+layer i+1's selection, issued on four CUDA streams, the persistent kernels capped to
+share the SMs (``scout_launch.max_ctas``):
 
-* selection stream: Q_pred = X W_Q^T (``scout_predict_q``), then scoring and
-  top-k over the next layer's digests (``scout_score_topk``) into list set
-  ``i % 2``;
-* attention stream: attention over the resident blocks of list set
-  ``(i + 1) % 2`` merged with the CPU partial (``scout_sparse_attn_merge``);
-* append stream: the digest append for the token just written
-  (``scout_build_digest`` on this layer's tail blocks).  Nothing in the step
-  reads it (the next step's selection of this layer does), so its few small
-  CTAs run beside the persistent kernels and its latency is hidden.
+* GEMM stream: Q_pred = X W_Q^T (``scout_predict_q``) into Q_pred buffer ``i % 2``;
+* selection stream: scoring and top-k over the next layer's digests
+  (``scout_score_topk``) with that Q_pred, into list set ``i % 2``;
+* attention stream: attention over the resident blocks of list set ``(i + 1) % 2``
+  merged with the CPU partial (``scout_sparse_attn_merge``);
+* append stream: the digest append for the token just written (``scout_build_digest``
+  on this layer's tail blocks).  Nothing in the step reads it (the next step's selection
+  of this layer does), so its few small CTAs run beside the persistent kernels.
 
-Step i's attention reads the lists step i-1 selected, and its query comes from
-the input X of the layer, which the previous layer's attention produced; step
-i's selection starts from that same X and overwrites the set step i-1's
-attention read.  So the selection stream waits for the previous attention, and
-the attention stream for the previous selection (two events per stream, used
-alternately).  The single
-layer of the synthetic workload stands for both layers: ``digest_next`` (scored)
-and ``digest_cur`` (appended to) are separate buffers, as the two layers' are.
+The layer input X of step i is the output of step i-1's attention (through the merge and
+the MLP), so step i's GEMM waits for step i-1's attention and nothing else; its
+selection waits for its GEMM (and, being on one stream, for step i-1's selection); step
+i's attention waits for step i-1's selection, whose lists it reads.  The GEMM of a step
+therefore runs beside the previous step's selection, on the SMs the attention has just
+left, and the period is bounded by (attention + GEMM + selection) / 2 rather than by
+GEMM + selection.  Q_pred alternates between two buffers, as the lists do: a GEMM
+overwrites the buffer the selection two steps earlier read, and that selection finished
+before the attention the GEMM waits for began.  The single layer of the synthetic
+workload stands for both layers: ``digest_next`` (scored) and ``digest_cur`` (appended
+to) are separate buffers, as the two layers' are.
 
 ``serial=True`` issues the same four calls on one stream with full grids.
 ``algorithmic_bytes`` gives the bytes each kernel must move per launch, the
@@ -31,9 +34,13 @@ numerator of the roofline.
 from __future__ import annotations
 
 KERNELS = ("build_digest", "predict_q", "score_topk", "sparse_attn_merge")
-# stream of each kernel: 0 = selection (next layer), 1 = attention (this layer)
-STREAM_OF = {"build_digest": 2, "predict_q": 0, "score_topk": 0, "sparse_attn_merge": 1}
-SPLIT = (80, 72)  # CTAs of the selection and attention kernels when overlapped (152 SMs)
+# stream of each kernel: 0 = selection, 1 = attention, 2 = digest append, 3 = GEMM
+STREAM_OF = {"build_digest": 2, "predict_q": 3, "score_topk": 0, "sparse_attn_merge": 1}
+# CTAs of the GEMM, selection and attention kernels when overlapped (0: one per SM).  The
+# selection deals whole units to its CTAs as they start, so it takes every SM the others
+# leave; measured on GB300 (graph replay): 80/0/72 60.6 us per step, 80/72/72 62.9 us,
+# 80/0/56 62.7 us, 80/0/88 61.2 us, 120/0/72 61.4 us.
+SPLIT = (80, 0, 72)
 
 
 class Step:
@@ -46,6 +53,7 @@ class Step:
         self.calls = calls  # name -> Prepared
         self.streams = streams
         self.serial = serial
+        self.gemm_done = [torch.cuda.Event(), torch.cuda.Event()]
         self.sel_done = [torch.cuda.Event(), torch.cuda.Event()]
         self.attn_done = [torch.cuda.Event(), torch.cuda.Event()]
         self.i = 0
@@ -78,12 +86,12 @@ class Step:
         return g
 
     def begin(self, event):
-        """Make both streams wait for ``event`` (recorded on the current stream)."""
+        """Make every stream wait for ``event`` (recorded on the current stream)."""
         for s in self.streams:
             s.wait_event(event)
 
     def end(self, event):
-        """Join both streams into the current stream and record ``event`` there."""
+        """Join every stream into the current stream and record ``event`` there."""
         import torch
 
         cur = torch.cuda.current_stream()
@@ -101,7 +109,7 @@ class Step:
         earlier step's events (a graph capture may not wait on events recorded outside it)."""
         par = self.i % 2
         cross = not self.serial and not after_begin
-        sA, sB, sC = (self.streams * 3)[:3] if self.serial else self.streams
+        sA, sB, sC, sD = (self.streams * 4)[:4] if self.serial else self.streams
         c = self.calls[par]
 
         def run(name, stream):
@@ -112,11 +120,12 @@ class Step:
                 timing[name][1].record(stream)
 
         if cross:
-            # the layer's input X is the previous layer's attention output (through the merge
-            # and the MLP), and step i-1's attention has read list set i % 2
-            sA.wait_event(self.attn_done[1 - par])
-        run("predict_q", sA)
-        run("score_topk", sA)
+            sD.wait_event(self.attn_done[1 - par])  # X of this layer: the previous attention's output
+        run("predict_q", sD)  # Q_pred buffer i % 2
+        if not self.serial:
+            self.gemm_done[par].record(sD)
+            sA.wait_event(self.gemm_done[par])
+        run("score_topk", sA)  # list set i % 2
         self.sel_done[par].record(sA)
         run("build_digest", sC)
         if cross:
@@ -144,7 +153,8 @@ def setup_step(shape, device, pool_slots=None, serial=False, split=SPLIT):
     t["digest_cur"] = t["digest_next"].clone()
     tail = [[u, int(wl.nvalid[u // s.Hkv]) - 1] for u in range(U)]
     t["tail"] = torch.tensor(tail, dtype=torch.int32, device=device)
-    t["Qp"] = torch.empty((s.B, s.Hq * D), dtype=torch.bfloat16, device=device)
+    for par in (0, 1):
+        t[f"Qp{par}"] = torch.empty((s.B, s.Hq * D), dtype=torch.bfloat16, device=device)
     t["ws_t"] = bs.score_topk_workspace(s.B, s.Hkv, nb, device=device)
     for par in (0, 1):
         for name in ("topk", "res", "cpu", "delta"):
@@ -157,30 +167,28 @@ def setup_step(shape, device, pool_slots=None, serial=False, split=SPLIT):
 
     if serial:
         streams = [torch.cuda.Stream(device)]  # not the legacy default stream: it can be captured
-        cap_sel = cap_attn = None
+        cap_gemm = cap_sel = cap_attn = None
     else:
-        streams = [torch.cuda.Stream(device) for _ in range(3)]
-        cap_sel, cap_attn = split
-    t["_launch_sel"] = bs._launch(cap_sel)
-    # the selection starts streaming digests while the GEMM that writes Q_pred finishes
-    t["_launch_score"] = bs._launch(cap_sel, pdl=True)
+        streams = [torch.cuda.Stream(device) for _ in range(4)]
+        cap_gemm, cap_sel, cap_attn = split if len(split) == 3 else (split[0], split[0], split[1])
+    t["_launch_gemm"] = bs._launch(cap_gemm)
+    t["_launch_score"] = bs._launch(cap_sel)
     t["_launch_attn"] = bs._launch(cap_attn)
-    sA, sB, sC = ((streams * 3)[:3] if serial else streams)
-    sA, sB, sC = sA.cuda_stream, sB.cuda_stream, sC.cuda_stream
+    sA, sB, sC, sD = ((streams * 4)[:4] if serial else streams)
+    sA, sB, sC, sD = sA.cuda_stream, sB.cuda_stream, sC.cuda_stream, sD.cuda_stream
     p = lambda name: t[name].data_ptr()  # noqa: E731
     append = bs.Prepared("scout_build_digest", bs.MINMAX, p("K_pool"), wl.n_slots, p("page_table"), p("seq_len"),
                          s.B, s.Hkv, D, s.P, nb, p("tail"), U, p("digest_cur"), p("status"), sC)
-    gemm = bs.Prepared("scout_predict_q", p("X"), p("W"), p("Qp"), s.B, s.Hq * D, s.hidden, p("status"),
-                       t["_launch_sel"], sA)
     calls = []
     for par in (0, 1):
         new, old = str(par), str(1 - par)
         calls.append({
             "build_digest": append,
-            "predict_q": gemm,
+            "predict_q": bs.Prepared("scout_predict_q", p("X"), p("W"), p("Qp" + new), s.B, s.Hq * D, s.hidden,
+                                     p("status"), t["_launch_gemm"], sD),
             # the previous step's CPU list is the prev list, so delta = newly offloaded blocks
             "score_topk": bs.Prepared(
-                "scout_score_topk", bs.MINMAX, p("Qp"), p("digest_next"), p("seq_len"), p("resident_bits"),
+                "scout_score_topk", bs.MINMAX, p("Qp" + new), p("digest_next"), p("seq_len"), p("resident_bits"),
                 p("cpu" + old), p("cpu_count" + old), s.B, s.Hq, s.Hkv, D, s.P, nb, s.k, None, p("topk" + new),
                 p("topk_count" + new), p("res" + new), p("res_count" + new), p("cpu" + new), p("cpu_count" + new),
                 p("delta" + new), p("delta_count" + new), p("ws_t"), t["ws_t"].numel(), t["_launch_score"], sA),
@@ -192,6 +200,7 @@ def setup_step(shape, device, pool_slots=None, serial=False, split=SPLIT):
         })
     # list set 1 holds a selection before step 0 (the one the prefill step would have made)
     calls[1]["predict_q"]()
+    torch.cuda.synchronize(device)  # the two calls sit on different streams
     calls[1]["score_topk"]()
     torch.cuda.synchronize(device)
     return wl, t, Step(t, calls, streams, serial)

@@ -80,7 +80,8 @@ def test_full_size_step_sampled(cfg, mode):
     grab = lambda n: t[f"{n}{par}"].cpu().numpy().reshape(s.units, -1)  # noqa: E731
     topk, res, cpu = grab("topk"), grab("res"), grab("cpu")
     tc, rc, cc = (t[f"{n}_count{par}"].cpu().numpy().reshape(-1) for n in ("topk", "res", "cpu"))
-    qp = bf16_bits(t["Qp"]).reshape(s.B, s.Hq, s.D)
+    qp = bf16_bits(t["Qp0"]).reshape(s.B, s.Hq, s.D)
+    assert np.array_equal(qp.reshape(-1), bf16_bits(t["Qp1"]).reshape(-1))  # same X and W_Q every step
     O_out, L_out = t["O"].float().cpu().numpy(), t["lse"].cpu().numpy()
     o_cpu, l_cpu = wl.cpu_partial()
     for u in _sample(s.units):

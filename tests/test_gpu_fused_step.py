@@ -132,7 +132,8 @@ def test_two_stream_step_matches_oracle(serial):
     torch.cuda.synchronize()
     assert int(t["status"].item()) == 0
     last = (step.i - 1) % 2  # set written by the last step; the last attention read the other set
-    qp_bits = bf16_bits(t["Qp"])
+    qp_bits = bf16_bits(t["Qp0"])
+    assert np.array_equal(qp_bits, bf16_bits(t["Qp1"]))  # same X and W_Q every step
     lists = {par: (t[f"topk{par}"].cpu().numpy().reshape(s.units, -1),
                    t[f"res{par}"].cpu().numpy().reshape(s.units, -1),
                    t[f"res_count{par}"].cpu().numpy().reshape(-1)) for par in (0, 1)}
