@@ -1,5 +1,5 @@
 """Full-size workloads on sampled units: the Qwen3-14B-shaped layer in the launch
-configuration bench.py times (two streams, capped grids), the Qwen3-8B-shaped layer,
+configuration bench.py times (four streams, capped grids), the Qwen3-8B-shaped layer,
 and the stress shapes (page 16/32/64, budgets 512/2048/8192, min/max and mean digests,
 128K context, plus the dense edge case), each checked against the fp64 oracle on a
 handful of (sequence, KV head) units the oracle finishes in seconds."""

@@ -1,5 +1,5 @@
 """GPU parity of the fused attention + merge entry point, of the launch options
-(CTA caps) of the persistent kernels, and of the two-stream decode step, against
+(CTA caps) of the persistent kernels, and of the multi-stream decode step, against
 the fp64 oracle."""
 import numpy as np
 import pytest
@@ -117,7 +117,7 @@ def test_predict_q_with_cta_cap(max_ctas):
 
 @pytest.mark.parametrize("serial", [False, True])
 def test_two_stream_step_matches_oracle(serial):
-    """Three steps of the two-stream step: the lists step i selects with Q_pred are the
+    """Three steps of the multi-stream step: the lists step i selects with Q_pred are the
     oracle's, and step i+1's output is attention over those resident blocks merged with
     the CPU partial."""
     s = W.Shape("step_g4", B=2, Hq=8, Hkv=2, T=4100, P=32, k=16, resident_frac=0.5, hidden=1024,
