@@ -1,0 +1,197 @@
+"""Multi-step decode of one layer through the libscout C ABI: the residency sweep.
+
+ScoutAttention (arXiv HTML), section 3.4 and Algorithm 1: a decode step appends one
+token per sequence, selects the next blocks with the predicted query against the
+previous step's CPU work list (so only the delta is new CPU work), and attends the
+resident part of the selection on the GPU; every ``recall_every`` steps the selected
+blocks that are not resident are brought in, taking the slots of unselected resident
+blocks (lowest score first).
+
+Readings taken where the pages leave it open (the same as the oracle's):
+  * the GPU holds k blocks per (sequence, KV head) plus the block being written; the
+    initial resident set is the top-k of the first decode step's true query (the
+    blocks found important right after prefill) and each unit's tail block;
+  * the true query walks by ``Workload.walk`` (step cosine ~0.96) and the predicted
+    query sits at cosine 0.93 to it; selection uses the predicted query, GPU attention
+    the true one;
+  * a token that starts a new block gets a fresh page (copied from the host copy of
+    the layer's KV, which stands for the page the model writes), and the block being
+    written is never evicted by a recall.
+
+Per step the sweep reports the CPU work-list size, its delta against the previous step,
+the CPU ratio (CPU blocks over the budget) and, on recall steps, the bytes moved and
+the host-to-device rate.  ``python -m block_sparse_kv_pred_gb300.sweep`` runs the
+64-step sweep at batch 16 and 64K context and prints one line per step.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+
+import numpy as np
+import torch
+
+import block_sparse_kv_pred_gb300 as bs
+from block_sparse_kv_pred_gb300 import workload as W
+from block_sparse_kv_pred_gb300.workload import device as WD
+
+
+def c4_shape(steps: int = 64) -> W.Shape:
+    """Batch 16, 40/8 heads, 64K context (+ room for the appended tokens), 32-token pages,
+    budget 2048 tokens (k = 64 blocks per KV head)."""
+    T0 = 65536
+    return W.Shape("sweep_b16_t64k", B=16, Hq=40, Hkv=8, T=T0 + steps, P=32, k=64, resident_frac=0.0,
+                   seq_lens=(T0,) * 16, hidden=0)
+
+
+def _bits(mask: np.ndarray) -> np.ndarray:
+    """bool [units][nblk] -> uint32 [units][words]."""
+    U, nb = mask.shape
+    words = -(-nb // 32)
+    padded = np.zeros((U, words * 32), dtype=np.uint64)
+    padded[:, :nb] = mask
+    w = padded.reshape(U, words, 32) << np.arange(32, dtype=np.uint64)
+    return w.sum(axis=-1).astype(np.uint32)
+
+
+class DecodeSweep:
+    """The layer's state on the GPU and the host, and one method per decode step."""
+
+    def __init__(self, shape: W.Shape, steps: int, recall_every: int = 16, device="cuda"):
+        self.s = s = shape
+        self.steps, self.recall_every = steps, recall_every
+        dev = self.dev = torch.device(device)
+        self.wl = wl = W.Workload(s)
+        self.qs, self.ps = wl.walk(steps)
+        U, nb, P, D = s.units, s.nblk, s.P, s.D
+        full = WD.materialize(wl, device=dev, with_gemm=False)
+        # every block in logical order [U][nblk][P][D]; its host copy (pinned) is the CPU-resident
+        # KV that recalls read
+        order = full["page_table"].reshape(-1).long()
+        logical = {}
+        for n in ("K", "V"):
+            logical[n] = full[n + "_pool"][order]
+            host = torch.empty((U, nb, P, D), dtype=torch.bfloat16, pin_memory=True)
+            host.copy_(logical[n].reshape(U, nb, P, D))
+            setattr(self, "h" + n, host)
+        # prefill: digests over every valid block (the whole context was on the GPU)
+        self.seq = wl.seq_len.astype(np.int32).copy()
+        self.d_seq = WD.to_dev(self.seq, dev)
+        self.digest = torch.empty((s.B, s.Hkv, nb, 2, D), dtype=torch.bfloat16, device=dev)
+        bs.build_digest("minmax", full["K_pool"], full["page_table"], self.d_seq, s.B, s.Hkv, P, self.digest)
+        # initial residency: the top-k of the first step's true query, plus the tail block
+        self.ws = bs.score_topk_workspace(s.B, s.Hkv, nb, device=dev)
+        none = torch.zeros((s.B, s.Hkv, s.words), dtype=torch.int32, device=dev)
+        first = bs.score_topk("minmax", WD.to_dev(self.qs[0], dev), self.digest, self.d_seq, none, s.B, s.Hq, s.Hkv,
+                              P, nb, s.k, self.ws)
+        topk = first["topk"].cpu().numpy().reshape(U, -1)
+        tc = first["topk_count"].cpu().numpy().reshape(-1)
+        res = np.zeros((U, nb), dtype=bool)
+        for u in range(U):
+            res[u, topk[u, :tc[u]]] = True
+            res[u, (int(self.seq[u // s.Hkv]) - 1) // P] = True
+        # the pool: k + 1 resident blocks per unit and room for the blocks the decode starts
+        spare_per_unit = -(-steps // P) + 1
+        self.n_slots = int(res.sum()) + spare_per_unit * U
+        table = np.full((U, nb), -1, dtype=np.int32)
+        table[res] = np.arange(int(res.sum()), dtype=np.int32)
+        self.spare = list(range(int(res.sum()), self.n_slots))
+        src = torch.from_numpy(np.flatnonzero(res.reshape(-1)).astype(np.int64)).to(dev)
+        self.K_pool = torch.zeros((self.n_slots, P, D), dtype=torch.bfloat16, device=dev)
+        self.V_pool = torch.zeros((self.n_slots, P, D), dtype=torch.bfloat16, device=dev)
+        self.K_pool[: src.numel()] = logical["K"][src]
+        self.V_pool[: src.numel()] = logical["V"][src]
+        del full, order, src, logical
+        torch.cuda.empty_cache()
+        self.res, self.table = res, table
+        self.d_table = WD.to_dev(table.reshape(s.B, s.Hkv, nb), dev)
+        self.d_bits = WD.to_dev(_bits(res).reshape(s.B, s.Hkv, -1).view(np.int32), dev)
+        self.wa = bs.sparse_attn_workspace(s.B, s.Hq, s.Hkv, P, device=dev)
+        self.scores = torch.empty((s.B, s.Hkv, nb), dtype=torch.float32, device=dev)
+        self.side = torch.cuda.Stream(dev)
+        self.prev = None
+        self.t = 0
+
+    def _move_in(self, ops) -> tuple[int, float]:
+        """Copy the ops' blocks from the host into their slots on the side stream, then commit
+        the page table and residency bits after the copy.  Returns (bytes, seconds)."""
+        s = self.s
+        t0, done = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t0.record(self.side)
+        bs.recall_async([tuple(int(x) for x in r) for r in ops], self.hK, self.hV, self.K_pool, self.V_pool, s.B,
+                        s.Hkv, s.P, s.nblk, self.side)
+        done.record(self.side)
+        bs.commit_residency(WD.to_dev(np.asarray(ops, dtype=np.int32).reshape(-1, 4), self.dev), self.d_table,
+                            self.d_bits, self.n_slots, s.B, s.Hkv, wait_event=done)
+        done.synchronize()
+        return len(ops) * 2 * s.P * s.D * 2, t0.elapsed_time(done) / 1e3
+
+    def step(self) -> dict:
+        """One decode step.  Returns host copies of its outputs and the state it ran on."""
+        s, t = self.s, self.t
+        U, P = s.units, s.P
+        # one token per sequence; a block that starts gets a fresh page
+        self.seq += 1
+        fresh = []
+        for u in range(U):
+            j = (int(self.seq[u // s.Hkv]) - 1) // P
+            if not self.res[u, j]:
+                slot = self.spare.pop()
+                fresh.append((u, j, slot, -1))
+                self.res[u, j], self.table[u, j] = True, slot
+        if fresh:
+            self._move_in(fresh)
+        self.d_seq = WD.to_dev(self.seq, self.dev)
+        tail = WD.to_dev(np.array([[u, (int(self.seq[u // s.Hkv]) - 1) // P] for u in range(U)], np.int32), self.dev)
+        bs.build_digest("minmax", self.K_pool, self.d_table, self.d_seq, s.B, s.Hkv, P, self.digest, block_list=tail)
+        resident_before = self.res.copy()
+        out = bs.score_topk("minmax", WD.to_dev(self.ps[t], self.dev), self.digest, self.d_seq, self.d_bits, s.B,
+                            s.Hq, s.Hkv, P, s.nblk, s.k, self.ws, prev_cpu=self.prev, scores=self.scores)
+        O, lse = bs.sparse_attn(WD.to_dev(self.qs[t], self.dev), self.K_pool, self.V_pool, self.d_table, self.d_seq,
+                                out["res"], out["res_count"], s.B, s.Hq, s.Hkv, P, s.k, s.scale, self.wa)
+        torch.cuda.synchronize(self.dev)
+        rec = {"t": t, "seq": self.seq.copy(), "resident": resident_before, "O": O.cpu().numpy(),
+               "lse": lse.cpu().numpy(), "prev_cpu": None}
+        if self.prev is not None:
+            rec["prev_cpu"] = (self.prev[0].cpu().numpy().reshape(U, -1), self.prev[1].cpu().numpy().reshape(-1))
+        for n in ("topk", "res", "cpu", "delta"):
+            rec[n] = out[n].cpu().numpy().reshape(U, -1)
+            rec[n + "_count"] = out[n + "_count"].cpu().numpy().reshape(-1)
+        self.prev = (out["cpu"].clone(), out["cpu_count"].clone())
+        n_cpu, n_delta = int(rec["cpu_count"].sum()), int(rec["delta_count"].sum())
+        stats = {"step": t, "cpu_blocks": n_cpu, "delta_blocks": n_delta, "cpu_ratio": n_cpu / (s.k * U),
+                 "recall_blocks": 0, "recall_bytes": 0, "recall_h2d_gbs": None}
+        if t % self.recall_every == self.recall_every - 1:
+            # the block being written stays on the GPU: the planner sees it as the most important
+            # resident block, so it is evicted last, and never (at least k + 1 blocks are resident,
+            # at most k come in)
+            sc = self.scores.cpu().numpy().reshape(U, s.nblk).copy()
+            for u in range(U):
+                sc[u, (int(self.seq[u // s.Hkv]) - 1) // P] = np.inf
+            rec.update(scores=sc, res_before=self.res.copy(), table_before=self.table.copy())
+            ops = bs.plan_recall(sc, rec["topk"], rec["topk_count"], _bits(self.res), self.table, s.k)
+            if len(ops):
+                nbytes, secs = self._move_in(ops)
+                for u, j, slot, ev in ops:
+                    if ev >= 0:
+                        self.res[u, ev], self.table[u, ev] = False, -1
+                    self.res[u, j], self.table[u, j] = True, slot
+                stats.update(recall_blocks=len(ops), recall_bytes=nbytes, recall_h2d_gbs=nbytes / secs / 1e9)
+            rec["ops"] = ops
+        rec["stats"] = stats
+        self.t += 1
+        return rec
+
+
+def main():
+    ap = argparse.ArgumentParser(description="Residency sweep: one layer, many decode steps, per-step report")
+    ap.add_argument("--steps", type=int, default=64)
+    ap.add_argument("--recall-every", type=int, default=16)
+    a = ap.parse_args()
+    sw = DecodeSweep(c4_shape(a.steps), a.steps, a.recall_every)
+    for _ in range(a.steps):
+        print(json.dumps(sw.step()["stats"]), flush=True)
+
+
+if __name__ == "__main__":
+    main()
