@@ -222,41 +222,73 @@ def run_scout(args, rank, world, local):
 
 
 def run_e2e(args, t, step, s, world, device):
-    """Same metric through the public calls with the step's inputs copied from pinned host memory
-    and its results (output, LSE, the CPU work list) read back, one step at a time."""
+    """Same metric through the public calls with every step's inputs copied from pinned host
+    memory and its results (output, LSE, the CPU work list) read back.  The inputs (X, q and the
+    CPU partial) alternate between two device buffers, as Q_pred and the lists do: step i's
+    copies run on a copy stream once the step two back has read that buffer, and step i's
+    kernels wait for them; the results are read back on the stream of the kernel that wrote
+    them.  So the copies overlap the kernels as the steps do.  Like the timed loop, the steps
+    replay CUDA graphs captured from those calls."""
     import torch
     import torch.distributed as dist
 
-    h_in = {n: torch.empty_like(t[n], device="cpu").pin_memory() for n in ("X", "q", "O_cpu", "lse_cpu")}
+    names = ("X", "q", "O_cpu", "lse_cpu")
+    h_in = {n: torch.empty_like(t[n], device="cpu").pin_memory() for n in names}
     for n in h_in:
         h_in[n].copy_(t[n])
     outs = ("O", "lse", "cpu", "cpu_count")
     h_out = {n: torch.empty_like(t[n if n in t else n + "0"], device="cpu").pin_memory() for n in outs}
     h2d = sum(v.numel() * v.element_size() for v in h_in.values())
     d2h = sum(v.numel() * v.element_size() for v in h_out.values())
-    steps = max(3, args.steps // 4)
+    gstep = step.fresh()
+    sA, sB, sC, sD = (gstep.streams * 4)[:4] if gstep.serial else gstep.streams
+    sE = sA if gstep.serial else torch.cuda.Stream(device)  # host-to-device copies
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=torch.cuda.Stream(device)):
+        cur = torch.cuda.current_stream()
+        start = torch.cuda.Event()
+        start.record(cur)
+        gstep.begin(start)
+        sE.wait_event(start)
+        for j in range(GRAPH_STEPS):
+            par = gstep.i % 2
+            if j >= 2 and not gstep.serial:  # buffer par was last read two steps back
+                sE.wait_event(gstep.gemm_done[par])
+                sE.wait_event(gstep.attn_done[par])
+            with torch.cuda.stream(sE):
+                for n in names:
+                    t[f"{n}{par}"].copy_(h_in[n], non_blocking=True)
+            landed = torch.cuda.Event()
+            landed.record(sE)
+            sD.wait_event(landed)
+            sB.wait_event(landed)
+            gstep.issue(after_begin=(j == 0))
+            with torch.cuda.stream(sB):
+                h_out["O"].copy_(t["O"], non_blocking=True)
+                h_out["lse"].copy_(t["lse"], non_blocking=True)
+            with torch.cuda.stream(sA):
+                h_out["cpu"].copy_(t[f"cpu{par}"], non_blocking=True)
+                h_out["cpu_count"].copy_(t[f"cpu_count{par}"], non_blocking=True)
+        gstep.end(None)
+        done = torch.cuda.Event()
+        done.record(sE)
+        cur.wait_event(done)
+    for _ in range(3):
+        g.replay()
+    reps = max(3, args.steps // (4 * GRAPH_STEPS))
     cur = torch.cuda.current_stream()
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
-    for i in range(steps):
-        ev[i][0].record(cur)
-        for n, h in h_in.items():
-            t[n].copy_(h, non_blocking=True)
-        inputs_in = torch.cuda.Event()
-        inputs_in.record(cur)
-        par = step.i % 2
-        step.begin(inputs_in)
-        step.issue()
-        step.end(None)
-        for n, h in h_out.items():
-            h.copy_(t[n] if n in t else t[f"{n}{par}"], non_blocking=True)
-        ev[i][1].record(cur)
+    a.record(cur)
+    for _ in range(reps):
+        g.replay()
+    b.record(cur)
     torch.cuda.synchronize()
-    ms = max_over_ranks(statistics.mean(a.elapsed_time(b) for a, b in ev), device)
+    ms = max_over_ranks(a.elapsed_time(b) / (reps * GRAPH_STEPS), device)
     return {"value": world * s.B * s.Hq / (ms / 1e3), "unit": "query-heads/s", "h2d_bytes_per_step": h2d,
-            "d2h_bytes_per_step": d2h, "ms_per_step": ms, "steps": steps}
+            "d2h_bytes_per_step": d2h, "ms_per_step": ms, "steps": reps * GRAPH_STEPS}
 
 
 # ---------------------------------------------------------------------------

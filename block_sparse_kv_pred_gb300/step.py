@@ -155,6 +155,10 @@ def setup_step(shape, device, pool_slots=None, serial=False, split=SPLIT):
     t["tail"] = torch.tensor(tail, dtype=torch.int32, device=device)
     for par in (0, 1):
         t[f"Qp{par}"] = torch.empty((s.B, s.Hq * D), dtype=torch.bfloat16, device=device)
+        # the step's inputs (layer input X, query, CPU partial) alternate between two buffers too,
+        # so that a copy of step i+1's inputs may land while step i still reads its own
+        for n in ("X", "q", "O_cpu", "lse_cpu"):
+            t[f"{n}{par}"] = t[n] if par == 0 else t[n].clone()
     t["ws_t"] = bs.score_topk_workspace(s.B, s.Hkv, nb, device=device)
     for par in (0, 1):
         for name in ("topk", "res", "cpu", "delta"):
@@ -184,8 +188,8 @@ def setup_step(shape, device, pool_slots=None, serial=False, split=SPLIT):
         new, old = str(par), str(1 - par)
         calls.append({
             "build_digest": append,
-            "predict_q": bs.Prepared("scout_predict_q", p("X"), p("W"), p("Qp" + new), s.B, s.Hq * D, s.hidden,
-                                     p("status"), t["_launch_gemm"], sD),
+            "predict_q": bs.Prepared("scout_predict_q", p("X" + new), p("W"), p("Qp" + new), s.B, s.Hq * D,
+                                     s.hidden, p("status"), t["_launch_gemm"], sD),
             # the previous step's CPU list is the prev list, so delta = newly offloaded blocks
             "score_topk": bs.Prepared(
                 "scout_score_topk", bs.MINMAX, p("Qp" + new), p("digest_next"), p("seq_len"), p("resident_bits"),
@@ -193,9 +197,9 @@ def setup_step(shape, device, pool_slots=None, serial=False, split=SPLIT):
                 p("topk_count" + new), p("res" + new), p("res_count" + new), p("cpu" + new), p("cpu_count" + new),
                 p("delta" + new), p("delta_count" + new), p("ws_t"), t["ws_t"].numel(), t["_launch_score"], sA),
             "sparse_attn_merge": bs.Prepared(
-                "scout_sparse_attn_merge", p("q"), p("K_pool"), p("V_pool"), wl.n_slots, p("page_table"),
+                "scout_sparse_attn_merge", p("q" + new), p("K_pool"), p("V_pool"), wl.n_slots, p("page_table"),
                 p("seq_len"), p("res" + old), p("res_count" + old), s.B, s.Hq, s.Hkv, D, s.P, nb, s.k, s.scale,
-                p("O_cpu"), p("lse_cpu"), p("O"), p("lse"), p("ws_a"), t["ws_a"].numel(), p("status"),
+                p("O_cpu" + new), p("lse_cpu" + new), p("O"), p("lse"), p("ws_a"), t["ws_a"].numel(), p("status"),
                 t["_launch_attn"], sB),
         })
     # list set 1 holds a selection before step 0 (the one the prefill step would have made)
