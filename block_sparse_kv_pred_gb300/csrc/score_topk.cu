@@ -458,6 +458,7 @@ __global__ void __launch_bounds__(kThreadsAll, 1) score_topk_kernel(const __grid
   __shared__ uint64_t full_bar[kMaxStagesT], empty_bar[kMaxStagesT], kfull[kMaxKeyBufs], kempty[kMaxKeyBufs],
       kunit_bar[kMaxKeyBufs];
   __shared__ int stage_unit[kMaxStagesT], kunit[kMaxKeyBufs];  // unit of a stage / of a key buffer, -1 = end
+  __shared__ int stage_nv[kMaxStagesT], knv[kMaxKeyBufs];       // and its valid-block count
   // dynamic shared memory: [ring (1024-aligned)][nkbuf key buffers][nsel selector-warp areas]
   const uint32_t raw = smem_u32(smem_raw);
   uint8_t* ring = smem_raw + (((raw + 1023u) & ~1023u) - raw);
@@ -508,7 +509,8 @@ __global__ void __launch_bounds__(kThreadsAll, 1) score_topk_kernel(const __grid
           ok = false;
           break;
         }
-        stage_unit[st] = u;  // published by the arrive below
+        stage_unit[st] = u;  // published by the arrive below, with the unit's valid-block count
+        stage_nv[st] = nv;
         uint8_t* sp = ring + st * kStageBytesT;
         if (ch * kChunk < nv) {
           const bool with_q = ch == 0;  // the scoring warps read q on a unit's first chunk
@@ -568,11 +570,10 @@ __global__ void __launch_bounds__(kThreadsAll, 1) score_topk_kernel(const __grid
         if (lane == 0) report(a.status, SCOUT_DEV_TIMEOUT);
         return;
       }
-      const int u = kunit[kb];
+      const int u = kunit[kb], nvalid = knv[kb];
       if (u < 0) return;
       uint32_t* keys = keybuf + kb * align4(a.nblk_cap);
       prefetch_unit(a, u, sw, lane);  // overlaps the scoring of u
-      const int nvalid = unit_nvalid(a, u / a.Hkv);
       if (!mbar_wait(&kfull[kb], (uint32_t)(e / a.nkbuf) & 1u) && lane == 0) report(a.status, SCOUT_DEV_TIMEOUT);
       select_unit(a, u, keys, nvalid, sw, lane);
       __syncwarp();
@@ -597,11 +598,12 @@ __global__ void __launch_bounds__(kThreadsAll, 1) score_topk_kernel(const __grid
       ch = 0;
       ++e;
       kb = e % a.nkbuf;
-      nvalid = unit_nvalid(a, u / a.Hkv);
+      nvalid = stage_nv[st];
       if (!mbar_wait(&kempty[kb], ((uint32_t)(e / a.nkbuf) & 1u) ^ 1u) && lane == 0)
         report(a.status, SCOUT_DEV_TIMEOUT);
       if (warp == 0 && lane == 0) {
         kunit[kb] = u;
+        knv[kb] = nvalid;
         mbar_arrive(&kunit_bar[kb]);
       }
       if (nvalid > 0) {
