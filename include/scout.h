@@ -57,12 +57,13 @@ typedef enum scout_digest_kind {
 } scout_digest_kind;
 
 /* Launch options (pass NULL for the defaults).  max_ctas bounds the CTAs a
- * persistent kernel launches (at most one per SM each): two kernels of
- * independent work, e.g. the next layer's selection and this layer's attention
- * (Algorithm 1), can then run at the same time on disjoint SMs from two streams.
- * 0 means one CTA per SM; a negative value is SCOUT_ERR_INVALID_ARG.  For
- * scout_predict_q it bounds the split-K factor S so that (N / 128) * S <= max_ctas;
- * the grid keeps at least one CTA per 128-row tile of W. */
+ * persistent kernel launches (at most one per SM each): kernels of independent
+ * work, e.g. the next layer's selection and this layer's attention (Algorithm 1),
+ * can then share the SMs from separate streams.  0 means one CTA per SM; a
+ * negative value is SCOUT_ERR_INVALID_ARG.  scout_score_topk deals whole units to
+ * its CTAs as they start, so with 0 it also takes the SMs other kernels free up
+ * while it runs.  For scout_predict_q it bounds the split-K factor S so that
+ * (N / 128) * S <= max_ctas; the grid keeps at least one CTA per 128-row tile of W. */
 typedef struct scout_launch {
   int max_ctas;
   int pdl; /* scout_score_topk only: 1 = programmatic dependent launch.  The kernel may
