@@ -666,7 +666,7 @@ inline size_t counters_bytes(int64_t units) { return (size_t)((units * 4 + 255) 
 extern "C" size_t scout_score_topk_workspace_bytes(int B, int Hkv, int nblk_cap) {
   if (B <= 0 || Hkv <= 0 || nblk_cap <= 0) return 0;
   const int64_t units = (int64_t)B * Hkv;
-  return scout::counters_bytes(units) + (size_t)units * nblk_cap * sizeof(float);
+  return scout::counters_bytes(units);  // the unit ticket counter (room for one word per unit)
 }
 
 extern "C" int scout_score_topk(int kind, const void* q, const void* digest, const int32_t* seq_len,
@@ -711,8 +711,7 @@ extern "C" int scout_score_topk(int kind, const void* q, const void* digest, con
   a.counters = static_cast<int32_t*>(workspace);
   a.status = nullptr;
   a.user_scores = scores != nullptr;
-  a.scores = scores != nullptr ? scores
-                               : reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + counters_bytes(units));
+  a.scores = scores;
   a.topk_idx = topk_idx;
   a.topk_count = topk_count;
   a.res_list = res_list;
@@ -784,7 +783,7 @@ extern "C" int scout_score_topk(int kind, const void* q, const void* digest, con
 namespace scout {
 namespace {
 
-constexpr size_t kNoAllocScratchBytes = 4u << 20;  // 4 MiB: counters + fp32 scores
+constexpr size_t kNoAllocScratchBytes = 4u << 20;  // 4 MiB: the unit ticket counter(s)
 constexpr int kNoAllocMaxDevices = 64;
 
 static __device__ __align__(256) uint8_t g_topk_scratch[kNoAllocScratchBytes];

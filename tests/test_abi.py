@@ -40,7 +40,7 @@ def test_status_strings_and_version(L):
 
 
 def test_workspace_sizes(L):
-    assert L.scout_score_topk_workspace_bytes(40, 8, 1024) == 1280 + 40 * 8 * 1024 * 4
+    assert L.scout_score_topk_workspace_bytes(40, 8, 1024) == 1280
     assert L.scout_score_topk_workspace_bytes(0, 8, 1024) == 0
     assert L.scout_sparse_attn_workspace_bytes(40, 40, 8, 128, 32) > 1024 * 2 * 8 * 128 * 4
 

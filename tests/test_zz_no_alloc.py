@@ -80,7 +80,7 @@ def test_noalloc_rejects_problems_beyond_its_fixed_scratch():
     L = bs.lib()
     cap = L.scout_score_topk_noalloc_max_bytes()
     assert cap == 4 << 20
-    # 64 x 8 units x 8192 blocks need 16 MiB of scratch: rejected before any launch
+    # 262,144 x 8 units need 8 MiB of counters: rejected before any launch
     fake = ctypes.c_void_p(256)
-    args = [0, fake, fake, fake, fake, None, None, 64, 320, 8, 128, 16, 8192, 32] + [None] + [fake] * 8 + [None]
+    args = [0, fake, fake, fake, fake, None, None, 262144, 40, 8, 128, 16, 64, 32] + [None] + [fake] * 8 + [None]
     assert L.scout_score_topk_noalloc(*args) == 3
