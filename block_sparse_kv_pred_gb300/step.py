@@ -44,7 +44,7 @@ SPLIT = (80, 0, 72)
 
 
 class Step:
-    """The prepared calls, streams and events of a step; ``issue(i)`` launches step i."""
+    """The prepared calls, streams and events of a step; ``issue()`` launches the next step."""
 
     def __init__(self, t, calls, streams, serial):
         import torch
