@@ -14,7 +14,8 @@ import torch
 
 __all__ = [
     "ScoutError", "lib", "MINMAX", "MEAN", "predict_q", "build_digest", "score_topk", "score_topk_workspace",
-    "sparse_attn", "sparse_attn_workspace", "merge", "recall_async", "commit_residency", "RecallOp",
+    "sparse_attn", "sparse_attn_merge", "sparse_attn_workspace", "merge", "recall_async", "commit_residency",
+    "plan_recall", "RecallOp", "Launch", "Prepared",
 ]
 
 MINMAX = 0
