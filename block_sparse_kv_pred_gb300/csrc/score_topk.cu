@@ -33,6 +33,7 @@ constexpr int kChunk = kScoreWarps * 16;  // digest rows (blocks) per work item
 constexpr int kBoxBytes = kChunk * 128;   // one 128-row x 128-byte TMA box
 constexpr int kMaxStagesT = 3;
 constexpr int kMaxKeyBufs = 8;  // key buffers: one being scored, the others being selected
+constexpr int kSeqCache = 256;  // sequence lengths kept in shared memory (larger batches read the rest)
 
 __device__ __forceinline__ uint32_t trunc_bf16(float x) { return __float_as_uint(x) & 0xFFFF0000u; }
 
@@ -169,9 +170,6 @@ struct TopkArgs {
 
 __host__ __device__ constexpr int align4(int n) { return (n + 3) / 4 * 4; }  // words to a 16-byte multiple
 
-__device__ __forceinline__ int unit_nvalid(const TopkArgs& a, int b) {
-  return min(a.nblk_cap, (max(a.seq_len[b], 0) + a.P - 1) / a.P);
-}
 
 // A selector warp's shared memory: the unit's residency bits, the bits of its previous
 // CPU list, the bits of the chosen candidates, a 256-bin digit histogram and the blocks
@@ -459,6 +457,7 @@ __global__ void __launch_bounds__(kThreadsAll, 1) score_topk_kernel(const __grid
       kunit_bar[kMaxKeyBufs];
   __shared__ int stage_unit[kMaxStagesT], kunit[kMaxKeyBufs];  // unit of a stage / of a key buffer, -1 = end
   __shared__ int stage_nv[kMaxStagesT], knv[kMaxKeyBufs];       // and its valid-block count
+  __shared__ int s_seq[kSeqCache];
   // dynamic shared memory: [ring (1024-aligned)][nkbuf key buffers][nsel selector-warp areas]
   const uint32_t raw = smem_u32(smem_raw);
   uint8_t* ring = smem_raw + (((raw + 1023u) & ~1023u) - raw);
@@ -477,6 +476,8 @@ __global__ void __launch_bounds__(kThreadsAll, 1) score_topk_kernel(const __grid
     }
     fence_mbar_init();
   }
+  const int B = a.units / a.Hkv;
+  for (int b = tid; b < min(B, kSeqCache); b += blockDim.x) s_seq[b] = a.seq_len[b];
   __syncthreads();
 
   if (warp == kProducer) {
@@ -488,19 +489,22 @@ __global__ void __launch_bounds__(kThreadsAll, 1) score_topk_kernel(const __grid
     if (lane != 0) return;
     prefetch_tmap(&tmD);
     const int last_ticket = a.units + (int)gridDim.x - 1;
-    auto take = [&]() {
-      const int t = atomicAdd(a.counters, 1);
+    auto resolve = [&](int t) {
       if (t == last_ticket) *a.counters = 0;
       return t < a.units ? t : -1;
     };
+    auto nvalid_of = [&](int b) {
+      const int L = b < kSeqCache ? s_seq[b] : a.seq_len[b];
+      return min(a.nblk_cap, (max(L, 0) + a.P - 1) / a.P);
+    };
     int64_t i = 0;  // stages issued
     bool q_ready = false, ok = true;
-    // the next unit's ticket and length are fetched a unit ahead, so no stage waits on them
-    int u = take();
-    int nv = u >= 0 ? unit_nvalid(a, u / a.Hkv) : 0;
+    int u = resolve(atomicAdd(a.counters, 1));
     while (u >= 0 && ok) {
-      const int u_next = take();
-      const int nv_next = u_next >= 0 ? unit_nvalid(a, u_next / a.Hkv) : 0;
+      // the next ticket is drawn now and read only once this unit's stages are issued, so the
+      // atomic's round trip never holds the ring up
+      const int t_next = atomicAdd(a.counters, 1);
+      const int nv = nvalid_of(u / a.Hkv);
       const int b = u / a.Hkv, kvh = u - b * a.Hkv;
       for (int ch = 0; ch < a.nchunk; ++ch, ++i) {
         const int st = (int)(i % a.stages);
@@ -535,8 +539,7 @@ __global__ void __launch_bounds__(kThreadsAll, 1) score_topk_kernel(const __grid
           mbar_arrive(&full_bar[st]);
         }
       }
-      u = u_next;
-      nv = nv_next;
+      u = resolve(t_next);
     }
     if (ok) {  // a stage tagged -1 ends the scoring warps' loop
       const int st = (int)(i % a.stages);
@@ -732,9 +735,9 @@ extern "C" int scout_score_topk(int kind, const void* q, const void* digest, con
                      CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
       return SCOUT_ERR_UNSUPPORTED;
   }
-  // per-block limit 232448 bytes (227 KiB) covers static (< 512 bytes here) and dynamic shared
+  // per-block limit 232448 bytes (227 KiB) covers static (< 2 KiB here) and dynamic shared
   // memory: the most ring stages, then the most key buffers (at least two) that fit
-  const size_t avail = 232448 - 512 - 1024;
+  const size_t avail = 232448 - 2048 - 1024;
   const size_t kbuf_bytes = (size_t)align4(nblk_cap) * 4, selw_bytes = (size_t)selwarp_words(a.words) * 4;
   auto need = [&](int stages, int nkbuf) {
     return (size_t)stages * kStageBytesT + nkbuf * kbuf_bytes + min(kSelWarps, nkbuf - 1) * selw_bytes;
