@@ -223,12 +223,13 @@ def run_scout(args, rank, world, local):
 
 def run_e2e(args, t, step, s, world, device):
     """Same metric through the public calls with every step's inputs copied from pinned host
-    memory and its results (output, LSE, the CPU work list) read back.  The inputs (X, q and the
-    CPU partial) alternate between two device buffers, as Q_pred and the lists do: step i's
-    copies run on a copy stream once the step two back has read that buffer, and step i's
-    kernels wait for them; the results are read back on the stream of the kernel that wrote
-    them.  So the copies overlap the kernels as the steps do.  Like the timed loop, the steps
-    replay CUDA graphs captured from those calls."""
+    memory and its results (output, LSE, the CPU work list) read back.  Inputs and outputs
+    alternate between two device buffers, as Q_pred and the lists do: step i's inputs are
+    copied on one copy stream once the step two back has read that buffer, and step i's
+    kernels wait for them; its results are read back on another once its kernels are done, and
+    the kernels two steps later, which write those buffers again, wait for that.  So the copies
+    overlap the kernels as the steps do.  Like the timed loop, the steps replay CUDA graphs
+    captured from those calls."""
     import torch
     import torch.distributed as dist
 
@@ -237,12 +238,14 @@ def run_e2e(args, t, step, s, world, device):
     for n in h_in:
         h_in[n].copy_(t[n])
     outs = ("O", "lse", "cpu", "cpu_count")
-    h_out = {n: torch.empty_like(t[n if n in t else n + "0"], device="cpu").pin_memory() for n in outs}
+    h_out = {n: torch.empty_like(t[n + "0"], device="cpu").pin_memory() for n in outs}
     h2d = sum(v.numel() * v.element_size() for v in h_in.values())
     d2h = sum(v.numel() * v.element_size() for v in h_out.values())
     gstep = step.fresh()
     sA, sB, sC, sD = (gstep.streams * 4)[:4] if gstep.serial else gstep.streams
     sE = sA if gstep.serial else torch.cuda.Stream(device)  # host-to-device copies
+    sF = sA if gstep.serial else torch.cuda.Stream(device)  # device-to-host copies
+    read = [torch.cuda.Event(), torch.cuda.Event()]  # step i's results are read back (per parity)
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g, stream=torch.cuda.Stream(device)):
         cur = torch.cuda.current_stream()
@@ -250,11 +253,16 @@ def run_e2e(args, t, step, s, world, device):
         start.record(cur)
         gstep.begin(start)
         sE.wait_event(start)
+        sF.wait_event(start)
         for j in range(GRAPH_STEPS):
             par = gstep.i % 2
-            if j >= 2 and not gstep.serial:  # buffer par was last read two steps back
+            if j >= 2 and not gstep.serial:
+                # buffers par were last read two steps back: the inputs by that step's GEMM and
+                # attention, the outputs by that step's read-back
                 sE.wait_event(gstep.gemm_done[par])
                 sE.wait_event(gstep.attn_done[par])
+                sA.wait_event(read[par])
+                sB.wait_event(read[par])
             with torch.cuda.stream(sE):
                 for n in names:
                     t[f"{n}{par}"].copy_(h_in[n], non_blocking=True)
@@ -263,16 +271,18 @@ def run_e2e(args, t, step, s, world, device):
             sD.wait_event(landed)
             sB.wait_event(landed)
             gstep.issue(after_begin=(j == 0))
-            with torch.cuda.stream(sB):
-                h_out["O"].copy_(t["O"], non_blocking=True)
-                h_out["lse"].copy_(t["lse"], non_blocking=True)
-            with torch.cuda.stream(sA):
-                h_out["cpu"].copy_(t[f"cpu{par}"], non_blocking=True)
-                h_out["cpu_count"].copy_(t[f"cpu_count{par}"], non_blocking=True)
+            if not gstep.serial:
+                sF.wait_event(gstep.sel_done[par])
+                sF.wait_event(gstep.attn_done[par])
+            with torch.cuda.stream(sF):
+                for n in outs:
+                    h_out[n].copy_(t[f"{n}{par}"], non_blocking=True)
+            read[par].record(sF)
         gstep.end(None)
-        done = torch.cuda.Event()
-        done.record(sE)
-        cur.wait_event(done)
+        for side in (sE, sF):
+            done = torch.cuda.Event()
+            done.record(side)
+            cur.wait_event(done)
     for _ in range(3):
         g.replay()
     reps = max(3, args.steps // (4 * GRAPH_STEPS))

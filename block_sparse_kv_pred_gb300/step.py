@@ -165,8 +165,9 @@ def setup_step(shape, device, pool_slots=None, serial=False, split=SPLIT):
             t[f"{name}{par}"] = torch.full((s.B, s.Hkv, s.k), -1, dtype=torch.int32, device=device)
             t[f"{name}_count{par}"] = torch.zeros((s.B, s.Hkv), dtype=torch.int32, device=device)
     t["ws_a"] = bs.sparse_attn_workspace(s.B, s.Hq, s.Hkv, s.P, device=device)
-    t["O"] = torch.empty((s.B, s.Hq, D), dtype=torch.bfloat16, device=device)
-    t["lse"] = torch.empty((s.B, s.Hq), dtype=torch.float32, device=device)
+    for par in (0, 1):  # the outputs alternate too, so a step's may be read back while the next is written
+        t[f"O{par}"] = torch.empty((s.B, s.Hq, D), dtype=torch.bfloat16, device=device)
+        t[f"lse{par}"] = torch.empty((s.B, s.Hq), dtype=torch.float32, device=device)
     t["status"] = torch.zeros(1, dtype=torch.int32, device=device)
 
     if serial:
@@ -199,8 +200,8 @@ def setup_step(shape, device, pool_slots=None, serial=False, split=SPLIT):
             "sparse_attn_merge": bs.Prepared(
                 "scout_sparse_attn_merge", p("q" + new), p("K_pool"), p("V_pool"), wl.n_slots, p("page_table"),
                 p("seq_len"), p("res" + old), p("res_count" + old), s.B, s.Hq, s.Hkv, D, s.P, nb, s.k, s.scale,
-                p("O_cpu" + new), p("lse_cpu" + new), p("O"), p("lse"), p("ws_a"), t["ws_a"].numel(), p("status"),
-                t["_launch_attn"], sB),
+                p("O_cpu" + new), p("lse_cpu" + new), p("O" + new), p("lse" + new), p("ws_a"), t["ws_a"].numel(),
+                p("status"), t["_launch_attn"], sB),
         })
     # list set 1 holds a selection before step 0 (the one the prefill step would have made)
     calls[1]["predict_q"]()

@@ -137,7 +137,7 @@ def test_two_stream_step_matches_oracle(serial):
     lists = {par: (t[f"topk{par}"].cpu().numpy().reshape(s.units, -1),
                    t[f"res{par}"].cpu().numpy().reshape(s.units, -1),
                    t[f"res_count{par}"].cpu().numpy().reshape(-1)) for par in (0, 1)}
-    Of, Lf = t["O"].float().cpu().numpy(), t["lse"].cpu().numpy()
+    Of, Lf = t[f"O{last}"].float().cpu().numpy(), t[f"lse{last}"].cpu().numpy()
     o_cpu, l_cpu = wl.cpu_partial()
     for u in range(s.units):
         b, kvh = divmod(u, s.Hkv)
