@@ -51,6 +51,9 @@ def parse_args():
     ap.add_argument("--split", default=None,
                     help="CTAs of the GEMM,selection,attention kernels (default 80,0,72, 0 = one per SM; two "
                          "values: GEMM and selection share the first)")
+    ap.add_argument("--early", default=None,
+                    help="kernels that start early after the kernel they wait for, comma-separated among "
+                         "predict_q,score_topk,sparse_attn_merge ('none' for none; default: the step's)")
     a = ap.parse_args()
     a.warmup = max(a.warmup, 3)
     return a
@@ -139,7 +142,7 @@ def max_over_ranks(x: float, device) -> float:
 # ---------------------------------------------------------------------------
 # libscout arm
 # ---------------------------------------------------------------------------
-from block_sparse_kv_pred_gb300.step import KERNELS, SPLIT, algorithmic_bytes, setup_step  # noqa: E402
+from block_sparse_kv_pred_gb300.step import EARLY, KERNELS, SPLIT, algorithmic_bytes, setup_step  # noqa: E402
 
 
 def run_scout(args, rank, world, local):
@@ -152,7 +155,8 @@ def run_scout(args, rank, world, local):
     torch.cuda.set_device(device)
     shape = W.CONFIGS[args.config]()
     split = tuple(int(x) for x in args.split.split(",")) if args.split else SPLIT
-    wl, t, step = setup_step(shape, device, serial=args.serial, split=split)
+    early = EARLY if args.early is None else tuple(x for x in args.early.split(",") if x and x != "none")
+    wl, t, step = setup_step(shape, device, serial=args.serial, split=split, early=early)
     s = shape
 
     def barrier():
@@ -218,7 +222,8 @@ def run_scout(args, rank, world, local):
 
     e2e = run_e2e(args, t, step, s, world, device)
     return s, wl, t, dict(ms=ms, value=value, kern_ms=kern_ms, clocks=clocks, wall=wall, e2e=e2e,
-                          launches=step.launches_per_step * args.steps, split=None if args.serial else split)
+                          launches=step.launches_per_step * args.steps, split=None if args.serial else split,
+                          early=() if args.serial else early)
 
 
 def run_e2e(args, t, step, s, world, device):
@@ -385,7 +390,7 @@ def run_reference(args, rank, world):
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "query-heads/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": el / args.steps * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": DATA,
-            "config": config_of(shape, world, SPLIT),
+            "config": config_of(shape, world, SPLIT, EARLY),
             "cpu_baseline": {"value": value, "unit": "query-heads/s", "cores": 1, "kind": "oracle",
                              "sample": f"each step is one of {len(smp.units)} sampled (sequence, KV head) units "
                                        f"of {shape.name}; single thread"},
@@ -408,13 +413,14 @@ def streams_of(split):
             f"attention ({n(att)}) after the previous selection || digest append")
 
 
-def config_of(s, world, split=None):
+def config_of(s, world, split=None, early=()):
     return {"workload": s.name, "batch": s.B, "q_heads": s.Hq, "kv_heads": s.Hkv, "head_dim": s.D,
             "context": s.T, "page": s.P, "budget_tokens": s.k * s.P, "resident_frac": s.resident_frac,
             "digest": s.kind, "gemm_mnk": [s.B, s.Hq * s.D, s.hidden],
             "l2": "not flushed: one step reads inputs larger than L2 (see step_input_bytes), in an order "
                   "that evicts each input before its next use",
             "streams": streams_of(split),
+            "early_start": list(early),
             "parallelism": f"independent replicas x{world} (one batch of sequences per GPU)"}
 
 
@@ -490,7 +496,7 @@ def main():
     line = {
         "metric": METRIC, "value": r["value"], "unit": "query-heads/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": r["ms"], "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "bf16", "data": DATA, "config": config_of(s, world, r["split"]),
+        "vs_baseline": None, "dtype": "bf16", "data": DATA, "config": config_of(s, world, r["split"], r["early"]),
         "roofline": roof,
         "step_roofline": {"bound": "hbm", "achieved": step_gbs, "peak": peak, "unit": "GB/s",
                           "frac": step_gbs / peak, "algorithmic_bytes_per_step": step_bytes,

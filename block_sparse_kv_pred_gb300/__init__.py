@@ -65,17 +65,25 @@ _SIGS = {
 
 
 class Launch(ctypes.Structure):
-    """scout_launch: launch options of the persistent kernels (max_ctas 0 = one CTA per SM;
-    pdl 1 = programmatic dependent launch of scout_score_topk after the kernel writing q)."""
-    _fields_ = [("max_ctas", ctypes.c_int), ("pdl", ctypes.c_int)]
+    """scout_launch: launch options of the persistent kernels.  max_ctas 0 = one CTA per SM;
+    pdl 1 = start early after the previous kernel on the stream; early_event = a
+    cudaEvent_t (timing disabled) this launch records programmatically, so that one of the
+    three persistent kernels on a stream waiting for it may start early."""
+    _fields_ = [("max_ctas", ctypes.c_int), ("pdl", ctypes.c_int), ("early_event", ctypes.c_void_p)]
 
 
-def _launch(max_ctas, pdl=False):
-    if max_ctas is None and not pdl:
+def _launch(max_ctas, pdl=False, early_event=None):
+    """Launch options, or None for the defaults.  ``early_event``: a torch.cuda.Event created
+    without timing and already recorded once (so that it exists), or a raw handle."""
+    if max_ctas is None and not pdl and early_event is None:
         return None
     if max_ctas is not None and max_ctas < 0:
         raise ScoutError("max_ctas must be >= 0")
-    return ctypes.pointer(Launch(int(max_ctas or 0), int(bool(pdl))))
+    if early_event is not None and not isinstance(early_event, int):
+        if not early_event.cuda_event:
+            raise ScoutError("early_event has not been created yet: record it once first")
+        early_event = early_event.cuda_event
+    return ctypes.pointer(Launch(int(max_ctas or 0), int(bool(pdl)), early_event))
 
 
 def lib_path() -> str:

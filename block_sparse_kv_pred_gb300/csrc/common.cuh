@@ -22,6 +22,30 @@ constexpr uint32_t kWaitLimit = 1u << 24;
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 inline bool valid_P(int P) { return P == 16 || P == 32 || P == 64; }
 inline int launch_status() { return cudaGetLastError() == cudaSuccess ? SCOUT_OK : SCOUT_ERR_CUDA; }
+// Appends the early-start attributes of `launch` (may be NULL) at attr[n]; returns the new count.
+// pdl: this launch may start before the previous kernel on the stream ends; early_event: this
+// launch records the event programmatically, so a dependent on another stream may start early.
+inline unsigned early_start_attrs(const scout_launch* launch, cudaLaunchAttribute* attr, unsigned n) {
+  if (launch == nullptr) return n;
+  if (launch->pdl) {
+    attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[n].val.programmaticStreamSerializationAllowed = 1;
+    ++n;
+  }
+  if (launch->early_event != nullptr) {
+    attr[n].id = cudaLaunchAttributeProgrammaticEvent;
+    attr[n].val.programmaticEvent.event = launch->early_event;
+    attr[n].val.programmaticEvent.flags = 0;
+    attr[n].val.programmaticEvent.triggerAtBlockStart = 0;
+    ++n;
+  }
+  return n;
+}
+// Device side of an early start: wait for the grids this one depends on programmatically (a
+// no-op when it was launched without such a dependency), and let this grid's own programmatic
+// dependents start (counted per CTA; a CTA that exits counts as well).
+__device__ __forceinline__ void wait_prerequisites() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void release_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 int sm_count();  // SMs of the current device
 // cuTensorMapEncodeTiled resolved through the runtime (no libcuda link needed)
 CUresult encode_tiled(CUtensorMap* map, CUtensorMapDataType dt, uint32_t rank, void* addr, const cuuint64_t* dims,

@@ -107,13 +107,16 @@ struct GemmArgs {
 };
 
 // A ring stage holds nk <= kps consecutive k-blocks: their W tiles first, then their X tiles.
-__device__ __forceinline__ void load_stage(uint8_t* st, const CUtensorMap* tmW, const CUtensorMap* tmX,
-                                           const GemmArgs& a, int tile, int kb, int nk, uint64_t* bar) {
+// One arrival expects both; the W and the X copies may be issued apart.
+__device__ __forceinline__ void load_w(uint8_t* st, const CUtensorMap* tmW, const GemmArgs& a, int tile, int kb,
+                                       int nk, uint64_t* bar) {
   mbar_arrive_tx(bar, (uint32_t)(nk * (kWTileBytes + a.x_tile_bytes)));
-  for (int j = 0; j < nk; ++j) {
-    tma_load_2d(st + j * kWTileBytes, tmW, (kb + j) * kBK, tile * kBM, bar);
+  for (int j = 0; j < nk; ++j) tma_load_2d(st + j * kWTileBytes, tmW, (kb + j) * kBK, tile * kBM, bar);
+}
+__device__ __forceinline__ void load_x(uint8_t* st, const CUtensorMap* tmX, const GemmArgs& a, int kb, int nk,
+                                       uint64_t* bar) {
+  for (int j = 0; j < nk; ++j)
     tma_load_2d(st + a.kps * kWTileBytes + j * a.x_tile_bytes, tmX, (kb + j) * kBK, 0, bar);
-  }
 }
 
 __global__ void __launch_bounds__(kThreadsQ, 1) predict_q_kernel(const __grid_constant__ CUtensorMap tmW,
@@ -131,11 +134,13 @@ __global__ void __launch_bounds__(kThreadsQ, 1) predict_q_kernel(const __grid_co
   const int kb0 = (int)(rank * a.kblocks / S), kb1 = (int)((rank + 1) * a.kblocks / S);
   const int nst = (kb1 - kb0 + a.kps - 1) / a.kps;  // ring stages of this CTA's k range
   auto nk_of = [&](int i) { return min(a.kps, kb1 - kb0 - i * a.kps); };
-  // a kernel launched after this one as a programmatic dependent (scout_score_topk) may start
-  // as soon as SMs free up; it waits for this grid to finish before it reads Q
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  // a kernel that starts early after this one (scout_score_topk) may take SMs as they free up;
+  // it waits for this grid to finish before it reads Q
+  release_dependents();
 
-  // the first pass over the ring needs no free slot: issue it before the TMEM allocation
+  // the first pass over the ring needs no free slot: issue it before the TMEM allocation.  W
+  // does not depend on an earlier kernel; X may be written by the one this launch follows, so
+  // an early start waits for it between the two
   const int first = min(a.stages, nst);
   if (tid == 0) {
     for (int i = 0; i < a.stages; ++i) {
@@ -147,7 +152,9 @@ __global__ void __launch_bounds__(kThreadsQ, 1) predict_q_kernel(const __grid_co
     prefetch_tmap(&tmW);
     prefetch_tmap(&tmX);
     for (int i = 0; i < first; ++i)
-      load_stage(base + i * stage_bytes, &tmW, &tmX, a, tile, kb0 + i * a.kps, nk_of(i), &full_bar[i]);
+      load_w(base + i * stage_bytes, &tmW, a, tile, kb0 + i * a.kps, nk_of(i), &full_bar[i]);
+    wait_prerequisites();
+    for (int i = 0; i < first; ++i) load_x(base + i * stage_bytes, &tmX, a, kb0 + i * a.kps, nk_of(i), &full_bar[i]);
   }
   if (warp == 2) tmem_alloc(&tmem_slot, (uint32_t)a.tmem_cols);
   tc_fence_before();
@@ -164,7 +171,8 @@ __global__ void __launch_bounds__(kThreadsQ, 1) predict_q_kernel(const __grid_co
         report(a.status, SCOUT_DEV_TIMEOUT);
         break;
       }
-      load_stage(base + st * stage_bytes, &tmW, &tmX, a, tile, kb0 + i * a.kps, nk_of(i), &full_bar[st]);
+      load_w(base + st * stage_bytes, &tmW, a, tile, kb0 + i * a.kps, nk_of(i), &full_bar[st]);
+      load_x(base + st * stage_bytes, &tmX, a, kb0 + i * a.kps, nk_of(i), &full_bar[st]);
       issued = i + 1;
     }
     // every issued copy lands before the CTA can retire
@@ -290,13 +298,13 @@ extern "C" int scout_predict_q(const void* X, const void* W, void* Q, int M, int
   cfg.blockDim = dim3(kThreadsQ, 1, 1);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[3];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = 1;
   attr[0].val.clusterDim.y = (unsigned)S;
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = early_start_attrs(launch, attr, 1);
   if (cudaLaunchKernelEx(&cfg, predict_q_kernel, tmW, tmX, a) != cudaSuccess) return SCOUT_ERR_CUDA;
   return launch_status();
 }

@@ -524,9 +524,9 @@ __global__ void __launch_bounds__(kThreadsAll, 1) score_topk_kernel(const __grid
           for (int bx = 0; bx < 4; ++bx) tma_load_2d(sp + bx * kBoxBytes, &tmD, bx * 64, y, &full_bar[st]);
           const __nv_bfloat16* qg = a.q + ((int64_t)b * a.Hq + (int64_t)kvh * a.G) * kD;
           if (with_q && !q_ready) {
-            // launched as a programmatic dependent: q is written by the previous kernel on the
-            // stream, so wait for it here (digest loads above need not); a no-op otherwise
-            asm volatile("griddepcontrol.wait;" ::: "memory");
+            // started early: q is written by the kernel this launch depends on, so wait for it
+            // here (the digest loads above need not); a no-op otherwise
+            wait_prerequisites();
             q_ready = true;
           }
           for (int h = 0; h < (with_q ? a.G : 0); ++h)
@@ -541,6 +541,9 @@ __global__ void __launch_bounds__(kThreadsAll, 1) score_topk_kernel(const __grid
       }
       u = resolve(t_next);
     }
+    // every unit is handed out: a kernel that starts early after this one may take the SMs
+    // this grid's CTAs leave while they finish their last units
+    release_dependents();
     if (ok) {  // a stage tagged -1 ends the scoring warps' loop
       const int st = (int)(i % a.stages);
       if (mbar_wait(&empty_bar[st], (uint32_t)((i / a.stages) & 1) ^ 1u)) {
@@ -764,11 +767,9 @@ extern "C" int scout_score_topk(int kind, const void* q, const void* digest, con
   cfg.blockDim = dim3(kThreadsAll);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchAttribute attr[2];
   cfg.attrs = attr;
-  cfg.numAttrs = launch != nullptr && launch->pdl ? 1 : 0;
+  cfg.numAttrs = early_start_attrs(launch, attr, 0);
   if (cudaLaunchKernelEx(&cfg, kern, tmD, a) != cudaSuccess) return SCOUT_ERR_CUDA;
   return launch_status();
 }

@@ -422,6 +422,9 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const __grid_c
     prefetch_tmap(&tmK);
     prefetch_tmap(&tmV);
   }
+  // started early: the lists (and possibly anything else read below) are written by the kernel
+  // this launch depends on; a no-op otherwise
+  wait_prerequisites();
   // exclusive prefix of the clamped resident counts over all units
   {
     const int per = (a.units + kThreads - 1) / kThreads;
@@ -832,6 +835,9 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const __grid_c
       qa[ks][1] = qn[ks][1];
     }
   }
+  // this CTA's pages are done: a kernel that starts early after this one may take the SMs the
+  // grid leaves while the epilogue and split warps finish
+  release_dependents();
 }
 
 inline size_t counters_bytes(int64_t units) { return (size_t)((units * 4 + 255) / 256 * 256); }
@@ -858,7 +864,9 @@ bool make_page_map(CUtensorMap* map, const void* pool, int64_t n_slots, int P, i
 }
 
 template <int P, int S>
-int launch_ring(const CUtensorMap& tmK, const CUtensorMap& tmV, AttnArgs a, int max_ctas, cudaStream_t stream) {
+int launch_ring(const CUtensorMap& tmK, const CUtensorMap& tmV, AttnArgs a, const scout_launch* launch,
+                cudaStream_t stream) {
+  const int max_ctas = launch != nullptr ? launch->max_ctas : 0;
   const size_t smem = dyn_smem<P, S>(a.units, a.G, a.nslots);
   if (cudaFuncSetAttribute(sparse_attn_kernel<P, S>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
           cudaSuccess ||
@@ -870,13 +878,21 @@ int launch_ring(const CUtensorMap& tmK, const CUtensorMap& tmV, AttnArgs a, int 
       occ < 1)
     return SCOUT_ERR_CUDA;
   const int grid = min(kMaxGrid, max_ctas > 0 ? max_ctas : sm_count() * occ);
-  sparse_attn_kernel<P, S><<<grid, kThreads, smem, stream>>>(tmK, tmV, a);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[2];
+  cfg.attrs = attr;
+  cfg.numAttrs = early_start_attrs(launch, attr, 0);
+  if (cudaLaunchKernelEx(&cfg, sparse_attn_kernel<P, S>, tmK, tmV, a) != cudaSuccess) return SCOUT_ERR_CUDA;
   return launch_status();
 }
 
 // The biggest ring, then the most combine slots, that fit in shared memory.
 template <int P>
-int launch_attn(const void* K_pool, const void* V_pool, AttnArgs a, int max_ctas, cudaStream_t stream) {
+int launch_attn(const void* K_pool, const void* V_pool, AttnArgs a, const scout_launch* launch, cudaStream_t stream) {
   constexpr int SB = big_ring<P>(), SS = small_ring<P>();
   constexpr int PS = Cfg<P, SB>::PS;
   CUtensorMap tmK, tmV;
@@ -885,12 +901,12 @@ int launch_attn(const void* K_pool, const void* V_pool, AttnArgs a, int max_ctas
   for (int ns = kMaxSlots; ns >= 1; --ns)
     if (dyn_smem<P, SB>(a.units, a.G, ns) <= kSmemLimit) {
       a.nslots = ns;
-      return launch_ring<P, SB>(tmK, tmV, a, max_ctas, stream);
+      return launch_ring<P, SB>(tmK, tmV, a, launch, stream);
     }
   for (int ns = kMaxSlots; ns >= 1; --ns)
     if (dyn_smem<P, SS>(a.units, a.G, ns) <= kSmemLimit) {
       a.nslots = ns;
-      return launch_ring<P, SS>(tmK, tmV, a, max_ctas, stream);
+      return launch_ring<P, SS>(tmK, tmV, a, launch, stream);
     }
   return SCOUT_ERR_UNSUPPORTED;
 }
@@ -946,11 +962,10 @@ int attn_entry(const void* q, const void* K_pool, const void* V_pool, int64_t n_
   a.slot_lse = reinterpret_cast<float*>(ws + counters_bytes(units));
   a.slot_O = reinterpret_cast<float*>(ws + counters_bytes(units) + kSlotLseBytes);
   a.status = dev_status;
-  const int cap = launch != nullptr ? launch->max_ctas : 0;
   switch (P) {
-    case 16: return launch_attn<16>(K_pool, V_pool, a, cap, stream);
-    case 32: return launch_attn<32>(K_pool, V_pool, a, cap, stream);
-    default: return launch_attn<64>(K_pool, V_pool, a, cap, stream);
+    case 16: return launch_attn<16>(K_pool, V_pool, a, launch, stream);
+    case 32: return launch_attn<32>(K_pool, V_pool, a, launch, stream);
+    default: return launch_attn<64>(K_pool, V_pool, a, launch, stream);
   }
 }
 

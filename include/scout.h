@@ -63,14 +63,34 @@ typedef enum scout_digest_kind {
  * negative value is SCOUT_ERR_INVALID_ARG.  scout_score_topk deals whole units to
  * its CTAs as they start, so with 0 it also takes the SMs other kernels free up
  * while it runs.  For scout_predict_q it bounds the split-K factor S so that
- * (N / 128) * S <= max_ctas; the grid keeps at least one CTA per 128-row tile of W. */
+ * (N / 128) * S <= max_ctas; the grid keeps at least one CTA per 128-row tile of W.
+ *
+ * Early starts (programmatic dependent launch), for scout_predict_q,
+ * scout_score_topk and scout_sparse_attn(_merge).  Each of these kernels may start
+ * before the kernel it depends on has finished, do the part of its work that does
+ * not read that kernel's output, and wait for that kernel (its completion and the
+ * visibility of its writes) just before the first read that may:
+ *   scout_predict_q    streams W, then waits before it reads X;
+ *   scout_score_topk   streams digests, then waits before it reads q;
+ *   scout_sparse_attn  sets up its barriers, then waits before its first global read.
+ * Each writes its outputs only after that wait.  Everything else it reads must be
+ * complete before the kernel it depends on started.  Two ways to start early:
+ *   pdl = 1          the dependency is the previous kernel on the same stream;
+ *   early_event      set on the launch of the kernel depended on (the primary): the
+ *                    event (created with cudaEventDisableTiming) is recorded
+ *                    programmatically and fires before the primary completes, once
+ *                    every CTA of it has passed its trigger: scout_predict_q at its
+ *                    start, scout_score_topk once its last unit has been handed out,
+ *                    scout_sparse_attn once its attention warps are done.  One of the
+ *                    three kernels launched on a stream that waits for the event then
+ *                    starts early as above.  Anything else that waits for the event
+ *                    (a copy, a host wait, another library's kernel) is NOT ordered
+ *                    after the primary's writes: record a plain event after the call
+ *                    for those.  NULL: no programmatic event. */
 typedef struct scout_launch {
   int max_ctas;
-  int pdl; /* scout_score_topk only: 1 = programmatic dependent launch.  The kernel may
-              start while the previous kernel on the stream (normally the scout_predict_q
-              that writes q) is still running: it streams digests at once and waits for
-              that kernel only before reading q.  Everything else it reads must be
-              complete before that previous kernel started. */
+  int pdl;
+  cudaEvent_t early_event;
 } scout_launch;
 
 /* Human-readable name of a status code (static string, never NULL). */

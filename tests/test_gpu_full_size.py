@@ -10,7 +10,7 @@ import torch
 import oracle as O
 import block_sparse_kv_pred_gb300 as bs
 from block_sparse_kv_pred_gb300 import workload as W
-from block_sparse_kv_pred_gb300.step import SPLIT, setup_step
+from block_sparse_kv_pred_gb300.step import EARLY_OF, SPLIT, setup_step
 from block_sparse_kv_pred_gb300.workload import device as WD
 from _parity import bf16_bits, check_attention, check_selection, ensure_built, to_dev
 
@@ -56,12 +56,15 @@ def _check_unit(wl, u, q_sel_bits, kind, topk, tc, res, rc, cpu, cc, O_out, L_ou
         check_attention(O_out[b, hq], L_out[b, hq], o, l, what=(u, h))
 
 
-@pytest.mark.parametrize("cfg,mode", [("qwen3_14b", "streams"), ("qwen3_14b", "graph"), ("qwen3_8b", "serial")])
-def test_full_size_step_sampled(cfg, mode):
+@pytest.mark.parametrize("cfg,mode,early", [("qwen3_14b", "streams", ()), ("qwen3_14b", "graph", ()),
+                                            ("qwen3_14b", "streams", tuple(EARLY_OF)),
+                                            ("qwen3_14b", "graph", tuple(EARLY_OF)), ("qwen3_8b", "serial", ())])
+def test_full_size_step_sampled(cfg, mode, early):
     """Three steps of the decode step at full size (or, as bench.py times it, a captured CUDA
-    graph of two steps replayed twice); selection with Q_pred, attention with q."""
+    graph of two steps replayed twice), with and without early starts; selection with Q_pred,
+    attention with q."""
     shape = W.CONFIGS[cfg]()
-    wl, t, step = setup_step(shape, torch.device("cuda", 0), serial=(mode == "serial"), split=SPLIT)
+    wl, t, step = setup_step(shape, torch.device("cuda", 0), serial=(mode == "serial"), split=SPLIT, early=early)
     if mode == "graph":
         g = step.capture(2, torch.device("cuda", 0))
         for _ in range(2):
@@ -89,6 +92,42 @@ def test_full_size_step_sampled(cfg, mode):
         b, kvh = divmod(u, s.Hkv)
         _check_unit(wl, u, qp[b, kvh * s.G:(kvh + 1) * s.G], "minmax", topk, tc, res, rc, cpu, cc, O_out, L_out,
                     o_cpu, l_cpu)
+
+
+def _run_steps(early, graph, n=3):
+    """n steps of the Qwen3-14B-shaped layer; every output buffer of both parities, on the host."""
+    dev = torch.device("cuda", 0)
+    wl, t, step = setup_step(W.CONFIGS["qwen3_14b"](), dev, split=SPLIT, early=early)
+    if graph:
+        step.capture(n, dev).replay()
+    else:
+        ev = torch.cuda.Event()
+        ev.record()
+        step.begin(ev)
+        for _ in range(n):
+            step.issue()
+        step.end(None)
+    torch.cuda.synchronize()
+    assert int(t["status"].item()) == 0
+    names = ["Qp", "O", "lse"] + [f"{n}{c}" for n in ("topk", "res", "cpu", "delta") for c in ("", "_count")]
+    out = {f"{n}{par}": t[f"{n}{par}"].view(torch.int16 if t[f"{n}{par}"].dtype == torch.bfloat16 else
+                                            (torch.int32 if t[f"{n}{par}"].dtype == torch.float32 else
+                                             t[f"{n}{par}"].dtype)).cpu().numpy()
+           for n in names for par in (0, 1)}
+    del wl, t, step
+    torch.cuda.empty_cache()
+    return out
+
+
+def test_early_start_changes_no_bit():
+    """The step with every kernel starting early after the one it waits for (programmatic
+    dependent launch, graph-captured as bench.py times it) leaves every output buffer bit for bit
+    as the step without early starts does: each kernel waits before it reads what the other wrote,
+    and writes only after that wait."""
+    plain = _run_steps((), graph=False)
+    early = _run_steps(tuple(EARLY_OF), graph=True)
+    for k in plain:
+        assert np.array_equal(plain[k], early[k]), k
 
 
 STRESS = [(16, 2048, "minmax"), (32, 2048, "minmax"), (64, 2048, "minmax"), (32, 512, "minmax"),
