@@ -243,12 +243,6 @@ struct SlotView {
   __device__ float* o(int w, int h) const { return base + 2 * kConsumerWarps * kMaxG + (w * G + h) * kD; }
 };
 
-__device__ __forceinline__ int ld_acquire(const int* p) {
-  int v;
-  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-  return v;
-}
-
 // Walks the unit segments of one CTA's flattened block range in processing order: the
 // range's last segment first (when the range holds more than one), then the others from the
 // start.  The last and the first segment are the ones a range boundary can cut, so both of
