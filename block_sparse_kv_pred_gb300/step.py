@@ -159,9 +159,17 @@ class Step:
         self.i += 1
 
 
-def setup_step(shape, device, pool_slots=None, serial=False, split=SPLIT, early=EARLY):
+def setup_step(shape, device, pool_slots=None, serial=False, split=SPLIT, early=EARLY, pdl=False):
     """Device inputs, prefill digests, both list sets and the prepared calls of a step.
-    ``early``: the kernels (of ``EARLY_OF``) that start early after the kernel they wait for."""
+    ``early``: the kernels (of ``EARLY_OF``) that start early after the kernel they wait for.
+    ``pdl`` (serial only): the three persistent kernels start early after the kernel before
+    them on the one stream (the selection after the GEMM, the attention after the digest
+    append, which itself waits for the selection, the GEMM after the attention)."""
+    if pdl and not serial:
+        raise ValueError("pdl applies to the serial step: on four streams the kernel before a selection on its "
+                         "stream is the previous selection, whose CPU list it reads before it waits")
+    if any(k not in EARLY_OF for k in early):
+        raise ValueError(f"early starters must be among {sorted(EARLY_OF)}")
     import torch
 
     import block_sparse_kv_pred_gb300 as bs
@@ -202,14 +210,12 @@ def setup_step(shape, device, pool_slots=None, serial=False, split=SPLIT, early=
         streams = [torch.cuda.Stream(device) for _ in range(4)]
         cap_gemm, cap_sel, cap_attn = split if len(split) == 3 else (split[0], split[0], split[1])
     early = () if serial else tuple(early)
-    if any(k not in EARLY_OF for k in early):
-        raise ValueError(f"early starters must be among {sorted(EARLY_OF)}")
     # launch options per kernel and parity; a Step writes the programmatic event of each kernel
     # that an early starter waits for into its options before the launch
     t["_early_kernels"] = early
     for par in (0, 1):
         for key, cap in (("gemm", cap_gemm), ("score", cap_sel), ("attn", cap_attn)):
-            t[f"_launch_{key}{par}"] = bs._launch(cap if cap is not None or not early else 0)
+            t[f"_launch_{key}{par}"] = bs._launch(cap if cap is not None or not early else 0, pdl=pdl)
     sA, sB, sC, sD = ((streams * 4)[:4] if serial else streams)
     sA, sB, sC, sD = sA.cuda_stream, sB.cuda_stream, sC.cuda_stream, sD.cuda_stream
     p = lambda name: t[name].data_ptr()  # noqa: E731

@@ -83,3 +83,26 @@ def test_generator_library_exports():
         B.build()
     L = WD.gen_lib()
     assert hasattr(L, "scoutgen_fill_normal_bf16") and hasattr(L, "scoutgen_fill_pool_bf16")
+
+
+def test_launch_options_layout_and_step_checks():
+    """scout_launch as the binding lays it out (two ints, then the event handle), an event that
+    does not exist yet refused, and the step's early-start options checked before any device work."""
+    assert ctypes.sizeof(bs.Launch) == 16 and bs.Launch.early_event.offset == 8
+    lp = bs._launch(0, early_event=0x1234)
+    assert (lp.contents.max_ctas, lp.contents.pdl, lp.contents.early_event) == (0, 0, 0x1234)
+    assert bs._launch(None, pdl=True).contents.pdl == 1
+    assert bs._launch(None) is None
+
+    class Uncreated:  # a torch.cuda.Event before its first record
+        cuda_event = 0
+
+    with pytest.raises(bs.ScoutError):
+        bs._launch(0, early_event=Uncreated())
+    from block_sparse_kv_pred_gb300 import workload as W
+    from block_sparse_kv_pred_gb300.step import setup_step
+
+    with pytest.raises(ValueError, match="serial"):
+        setup_step(W.tiny(), "cpu", pdl=True)
+    with pytest.raises(ValueError, match="early starters"):
+        setup_step(W.tiny(), "cpu", early=("build_digest",))

@@ -94,10 +94,10 @@ def test_full_size_step_sampled(cfg, mode, early):
                     o_cpu, l_cpu)
 
 
-def _run_steps(early, graph, n=3):
+def _run_steps(early, graph, n=3, serial=False, pdl=False):
     """n steps of the Qwen3-14B-shaped layer; every output buffer of both parities, on the host."""
     dev = torch.device("cuda", 0)
-    wl, t, step = setup_step(W.CONFIGS["qwen3_14b"](), dev, split=SPLIT, early=early)
+    wl, t, step = setup_step(W.CONFIGS["qwen3_14b"](), dev, serial=serial, split=SPLIT, early=early, pdl=pdl)
     if graph:
         step.capture(n, dev).replay()
     else:
@@ -126,6 +126,17 @@ def test_early_start_changes_no_bit():
     and writes only after that wait."""
     plain = _run_steps((), graph=False)
     early = _run_steps(tuple(EARLY_OF), graph=True)
+    for k in plain:
+        assert np.array_equal(plain[k], early[k]), k
+
+
+@pytest.mark.parametrize("graph", [False, True])
+def test_same_stream_early_start_changes_no_bit(graph):
+    """The serial step with its three persistent kernels started early after the kernel before
+    them on the one stream (scout_launch.pdl) leaves every output buffer as the plain serial step
+    does, issued on the stream and captured in a CUDA graph."""
+    plain = _run_steps((), graph=False, serial=True)
+    early = _run_steps((), graph=graph, serial=True, pdl=True)
     for k in plain:
         assert np.array_equal(plain[k], early[k]), k
 
