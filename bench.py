@@ -227,25 +227,22 @@ def run_scout(args, rank, world, local):
 
 
 def run_e2e(args, t, step, s, world, device):
-    """Same metric through the public calls with every step's inputs copied from pinned host
-    memory and its results (output, LSE, the CPU work list) read back.  Inputs and outputs
-    alternate between two device buffers, as Q_pred and the lists do: step i's inputs are
-    copied on one copy stream once the step two back has read that buffer, and step i's
-    kernels wait for them; its results are read back on another once its kernels are done, and
-    the kernels two steps later, which write those buffers again, wait for that.  So the copies
-    overlap the kernels as the steps do.  Like the timed loop, the steps replay CUDA graphs
-    captured from those calls."""
+    """Same metric through the public calls with every step's inputs (X, q, the CPU partial)
+    copied from pinned host memory and its results (output, LSE, the CPU work list) read back,
+    one copy each way (each set is one buffer).  Inputs and outputs alternate between two
+    device buffers, as Q_pred and the lists do: step i's inputs are copied on one copy stream
+    once the step two back has read that buffer, and step i's kernels wait for them; its
+    results are read back on another once its kernels are done, and the kernels two steps
+    later, which write those buffers again, wait for that.  So the copies overlap the kernels
+    as the steps do.  Like the timed loop, the steps replay CUDA graphs captured from those
+    calls."""
     import torch
     import torch.distributed as dist
 
-    names = ("X", "q", "O_cpu", "lse_cpu")
-    h_in = {n: torch.empty_like(t[n], device="cpu").pin_memory() for n in names}
-    for n in h_in:
-        h_in[n].copy_(t[n])
-    outs = ("O", "lse", "cpu", "cpu_count")
-    h_out = {n: torch.empty_like(t[n + "0"], device="cpu").pin_memory() for n in outs}
-    h2d = sum(v.numel() * v.element_size() for v in h_in.values())
-    d2h = sum(v.numel() * v.element_size() for v in h_out.values())
+    h_in = torch.empty_like(t["in0"], device="cpu").pin_memory()
+    h_in.copy_(t["in0"])
+    h_out = torch.empty_like(t["out0"], device="cpu").pin_memory()
+    h2d, d2h = h_in.numel(), h_out.numel()
     gstep = step.fresh()
     sA, sB, sC, sD = (gstep.streams * 4)[:4] if gstep.serial else gstep.streams
     sE = sA if gstep.serial else torch.cuda.Stream(device)  # host-to-device copies
@@ -269,8 +266,7 @@ def run_e2e(args, t, step, s, world, device):
                 sA.wait_event(read[par])
                 sB.wait_event(read[par])
             with torch.cuda.stream(sE):
-                for n in names:
-                    t[f"{n}{par}"].copy_(h_in[n], non_blocking=True)
+                t[f"in{par}"].copy_(h_in, non_blocking=True)
             landed = torch.cuda.Event()
             landed.record(sE)
             sD.wait_event(landed)
@@ -280,8 +276,7 @@ def run_e2e(args, t, step, s, world, device):
                 sF.wait_event(gstep.sel_done[par])
                 sF.wait_event(gstep.attn_done[par])
             with torch.cuda.stream(sF):
-                for n in outs:
-                    h_out[n].copy_(t[f"{n}{par}"], non_blocking=True)
+                h_out.copy_(t[f"out{par}"], non_blocking=True)
             read[par].record(sF)
         gstep.end(None)
         for side in (sE, sF):

@@ -33,6 +33,8 @@ numerator of the roofline.
 """
 from __future__ import annotations
 
+import math
+
 KERNELS = ("build_digest", "predict_q", "score_topk", "sparse_attn_merge")
 # stream of each kernel: 0 = selection, 1 = attention, 2 = digest append, 3 = GEMM
 STREAM_OF = {"build_digest": 2, "predict_q": 3, "score_topk": 0, "sparse_attn_merge": 1}
@@ -159,6 +161,20 @@ class Step:
         self.i += 1
 
 
+def packed(specs, device):
+    """One byte buffer holding tensors of the given (name, shape, dtype), each at a 256-byte
+    aligned offset, and the tensors as views of it (one copy moves them all)."""
+    import torch
+
+    layout, off = [], 0
+    for name, shape, dtype in specs:
+        n = int(math.prod(shape)) * torch.empty((), dtype=dtype).element_size()
+        layout.append((name, tuple(shape), dtype, off, n))
+        off += (n + 255) // 256 * 256
+    buf = torch.empty(off, dtype=torch.uint8, device=device)
+    return buf, {name: buf[o:o + n].view(dtype).view(shape) for name, shape, dtype, o, n in layout}
+
+
 def setup_step(shape, device, pool_slots=None, serial=False, split=SPLIT, early=EARLY, pdl=False):
     """Device inputs, prefill digests, both list sets and the prepared calls of a step.
     ``early``: the kernels (of ``EARLY_OF``) that start early after the kernel they wait for.
@@ -186,21 +202,30 @@ def setup_step(shape, device, pool_slots=None, serial=False, split=SPLIT, early=
     t["digest_cur"] = t["digest_next"].clone()
     tail = [[u, int(wl.nvalid[u // s.Hkv]) - 1] for u in range(U)]
     t["tail"] = torch.tensor(tail, dtype=torch.int32, device=device)
+    i32, f32, bf16 = torch.int32, torch.float32, torch.bfloat16
     for par in (0, 1):
-        t[f"Qp{par}"] = torch.empty((s.B, s.Hq * D), dtype=torch.bfloat16, device=device)
+        t[f"Qp{par}"] = torch.empty((s.B, s.Hq * D), dtype=bf16, device=device)
         # the step's inputs (layer input X, query, CPU partial) alternate between two buffers too,
-        # so that a copy of step i+1's inputs may land while step i still reads its own
-        for n in ("X", "q", "O_cpu", "lse_cpu"):
-            t[f"{n}{par}"] = t[n] if par == 0 else t[n].clone()
-    t["ws_t"] = bs.score_topk_workspace(s.B, s.Hkv, nb, device=device)
-    for par in (0, 1):
+        # so that a copy of step i+1's inputs may land while step i still reads its own; each set
+        # is one buffer, so that one copy brings it in
+        t[f"in{par}"], views = packed([(n, t[n].shape, t[n].dtype) for n in ("X", "q", "O_cpu", "lse_cpu")], device)
+        for n, v in views.items():
+            t[f"{n}{par}"] = v
+            v.copy_(t[n])
+        # the outputs alternate too, so a step's may be read back while the next is written; the
+        # ones read back every step (O, LSE, the CPU work list) are one buffer
+        t[f"out{par}"], views = packed([("O", (s.B, s.Hq, D), bf16), ("lse", (s.B, s.Hq), f32),
+                                        ("cpu", (s.B, s.Hkv, s.k), i32), ("cpu_count", (s.B, s.Hkv), i32)], device)
+        for n, v in views.items():
+            t[f"{n}{par}"] = v
+        for name in ("topk", "res", "delta"):
+            t[f"{name}{par}"] = torch.empty((s.B, s.Hkv, s.k), dtype=i32, device=device)
+            t[f"{name}_count{par}"] = torch.empty((s.B, s.Hkv), dtype=i32, device=device)
         for name in ("topk", "res", "cpu", "delta"):
-            t[f"{name}{par}"] = torch.full((s.B, s.Hkv, s.k), -1, dtype=torch.int32, device=device)
-            t[f"{name}_count{par}"] = torch.zeros((s.B, s.Hkv), dtype=torch.int32, device=device)
+            t[f"{name}{par}"].fill_(-1)
+            t[f"{name}_count{par}"].zero_()
+    t["ws_t"] = bs.score_topk_workspace(s.B, s.Hkv, nb, device=device)
     t["ws_a"] = bs.sparse_attn_workspace(s.B, s.Hq, s.Hkv, s.P, device=device)
-    for par in (0, 1):  # the outputs alternate too, so a step's may be read back while the next is written
-        t[f"O{par}"] = torch.empty((s.B, s.Hq, D), dtype=torch.bfloat16, device=device)
-        t[f"lse{par}"] = torch.empty((s.B, s.Hq), dtype=torch.float32, device=device)
     t["status"] = torch.zeros(1, dtype=torch.int32, device=device)
 
     if serial:
