@@ -15,7 +15,7 @@ import torch
 __all__ = [
     "ScoutError", "lib", "MINMAX", "MEAN", "predict_q", "build_digest", "score_topk", "score_topk_workspace",
     "sparse_attn", "sparse_attn_merge", "sparse_attn_workspace", "merge", "recall_async", "commit_residency",
-    "plan_recall", "RecallOp", "Launch", "Prepared",
+    "plan_recall", "cpu_attend", "RecallOp", "Launch", "Prepared",
 ]
 
 MINMAX = 0
@@ -61,6 +61,7 @@ _SIGS = {
     "scout_recall_async": ([_p, _i, _p, _p, _p, _p, _i64, _i, _i, _i, _i, _i, _p, _p, _p], _i),
     "scout_commit_residency": ([_p, _i, _p, _p, _i64, _i, _i, _i, _p, _p], _i),
     "scout_plan_recall": ([_p, _p, _p, _p, _p, _i, _i, _i, _p, _i, _p], _i),
+    "scout_cpu_attend": ([_p, _p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _i, _f, _p, _p, _i], _i),
 }
 
 
@@ -301,6 +302,42 @@ def plan_recall(scores, topk_idx, topk_count, resident_bits, page_table, k):
     _check(lib().scout_plan_recall(ptr(sc), ptr(ti), ptr(tc), ptr(rb), ptr(pt), units, nblk, k, ops, cap,
                                    ctypes.byref(n)), "scout_plan_recall")
     return np.array([[o.unit, o.block, o.slot, o.evict_block] for o in ops[: n.value]], dtype=np.int32).reshape(-1, 4)
+
+
+def _host(t, dtype, name: str) -> int:
+    if not isinstance(t, torch.Tensor) or t.is_cuda:
+        raise ScoutError(f"{name} must be a host tensor")
+    if t.dtype != dtype:
+        raise ScoutError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ScoutError(f"{name} must be contiguous")
+    return t.data_ptr()
+
+
+def cpu_attend(q, K, V, seq_len, cpu_list, cpu_count, B, Hq, Hkv, P, k, scale, O_cpu=None, lse_cpu=None,
+               n_threads=0):
+    """CPU-side attention over the CPU work list, on the host cores (synchronous).
+
+    Host tensors: q bf16 [B][Hq][D]; K, V bf16 [B][Hkv][nblk_cap][P][D] (every block of the
+    layer in logical order); seq_len int32 [B]; cpu_list int32 [B][Hkv][k] and cpu_count
+    int32 [B][Hkv] as scout_score_topk writes them.  Returns (O_cpu fp32 [B][Hq][D],
+    lse_cpu fp32 [B][Hq]), the partial that scout_merge / scout_sparse_attn_merge take.
+    The foreign call releases the GIL, so other Python threads run meanwhile."""
+    D = q.shape[-1]
+    per_block = B * Hkv * P * D
+    if K.numel() != V.numel() or K.numel() % per_block:
+        raise ScoutError("K and V must hold [B][Hkv][nblk_cap][P][D] elements")
+    nblk_cap = K.numel() // per_block
+    if O_cpu is None:
+        O_cpu = torch.empty((B, Hq, D), dtype=torch.float32)
+    if lse_cpu is None:
+        lse_cpu = torch.empty((B, Hq), dtype=torch.float32)
+    _check(lib().scout_cpu_attend(_host(q, torch.bfloat16, "q"), _host(K, torch.bfloat16, "K"),
+                                  _host(V, torch.bfloat16, "V"), _host(seq_len, torch.int32, "seq_len"),
+                                  _host(cpu_list, torch.int32, "cpu_list"), _host(cpu_count, torch.int32, "cpu_count"),
+                                  B, Hq, Hkv, D, P, nblk_cap, k, float(scale), _host(O_cpu, torch.float32, "O_cpu"),
+                                  _host(lse_cpu, torch.float32, "lse_cpu"), int(n_threads)), "scout_cpu_attend")
+    return O_cpu, lse_cpu
 
 
 class Prepared:

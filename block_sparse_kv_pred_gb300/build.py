@@ -18,12 +18,12 @@ ROOT = os.path.dirname(PKG)
 BUILD = os.path.join(PKG, "_build")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 CFLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",
-          "-I" + os.path.join(ROOT, "include")]
+          "-Xcompiler", "-pthread", "-I" + os.path.join(ROOT, "include")]
 
 LIBS = {
     "libscout.so": [os.path.join(PKG, "csrc", f) for f in
                     ("api.cu", "digest.cu", "score_topk.cu", "sparse_attn.cu", "merge.cu", "predict_q.cu",
-                     "recall.cu")],
+                     "recall.cu", "cpu_attend.cpp")],
     "libscoutgen.so": [os.path.join(PKG, "workload", "gen.cu")],
 }
 
@@ -36,7 +36,7 @@ def nvcc() -> str:
 
 
 def _compile(src: str, extra: list[str]) -> str:
-    obj = os.path.join(BUILD, os.path.basename(src).replace(".cu", ".o"))
+    obj = os.path.join(BUILD, os.path.splitext(os.path.basename(src))[0] + ".o")
     cmd = [nvcc(), *ARCH, *CFLAGS, *extra, "-c", src, "-o", obj]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
@@ -58,7 +58,7 @@ def build(verbose: bool = False, extra: list[str] | None = None) -> dict[str, st
     for name, lib_srcs in LIBS.items():
         target = lib_path(name)
         tmp = target + ".tmp"
-        cmd = [nvcc(), *ARCH, "-shared", "-o", tmp, *[objs[s] for s in lib_srcs], "-lcudart"]
+        cmd = [nvcc(), *ARCH, "-shared", "-o", tmp, *[objs[s] for s in lib_srcs], "-lcudart", "-Xcompiler", "-pthread"]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError(f"link failed for {name}:\n{r.stdout}\n{r.stderr}")

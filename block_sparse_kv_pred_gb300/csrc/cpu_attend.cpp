@@ -1,0 +1,158 @@
+// scout_cpu_attend: attention over the offloaded blocks on the host cores.
+// ScoutAttention (arXiv HTML), section 3.2 and Algorithm 1 (CPUAttn of B_cpu, spawned one
+// layer ahead): the selected blocks that are not resident on the GPU are attended on the CPU,
+// next to the host copy of the KV cache, with the predicted query; the GPU merges the result.
+//
+// The threads take whole units (sequence, KV head) from an atomic counter.  For a unit, the G
+// query rows are held in fp32.  Each listed block's K rows are widened from bf16 once and
+// dotted with all G rows, with 16 independent partial sums per product, so the loop vectorises
+// without reassociating.  A block-wise online softmax then rescales the running sums to the
+// block's maximum, and the block's V rows are accumulated with its probabilities.  Portable
+// C++ only: no intrinsics, the compiler's vectoriser does the rest on x86-64 and AArch64.
+#include <algorithm>
+#include <atomic>
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <thread>
+#include <vector>
+
+#include "scout.h"
+
+namespace {
+
+constexpr int kDim = 128;      // head dimension
+constexpr int kMaxGroup = 8;   // query heads per KV head
+constexpr int kMaxPage = 64;   // tokens per block
+constexpr int kLanes = 16;     // partial sums per dot product
+
+inline float widen(uint16_t v) {  // bf16 -> fp32 (exact)
+  const uint32_t u = static_cast<uint32_t>(v) << 16;
+  float f;
+  std::memcpy(&f, &u, sizeof f);
+  return f;
+}
+
+struct Job {
+  const uint16_t* q;
+  const uint16_t* K;
+  const uint16_t* V;
+  const int32_t* seq_len;
+  const int32_t* list;
+  const int32_t* count;
+  int Hq, Hkv, G, P, nblk_cap, k;
+  float scale;
+  float* O;
+  float* lse;
+};
+
+void attend_unit(const Job& a, int u) {
+  const int b = u / a.Hkv, kvh = u - b * a.Hkv, G = a.G, P = a.P;
+  alignas(64) float q[kMaxGroup][kDim];
+  alignas(64) float acc[kMaxGroup][kDim];
+  alignas(64) float s[kMaxGroup][kMaxPage];
+  alignas(64) float row[kDim];
+  float m[kMaxGroup], l[kMaxGroup];
+  const uint16_t* qg = a.q + (static_cast<int64_t>(b) * a.Hq + static_cast<int64_t>(kvh) * G) * kDim;
+  for (int h = 0; h < G; ++h) {
+    for (int d = 0; d < kDim; ++d) {
+      q[h][d] = widen(qg[h * kDim + d]);
+      acc[h][d] = 0.f;
+    }
+    m[h] = -INFINITY;
+    l[h] = 0.f;
+  }
+  const int L = a.seq_len[b];
+  const int n = a.count[u];
+  const int32_t* blocks = a.list + static_cast<int64_t>(u) * a.k;
+  for (int i = 0; i < n; ++i) {
+    const int j = blocks[i];
+    const int valid = std::min(P, L - j * P);
+    if (valid <= 0) continue;  // no token of this block is in the sequence yet
+    const int64_t base = (static_cast<int64_t>(u) * a.nblk_cap + j) * P * kDim;
+    const uint16_t* Kb = a.K + base;
+    const uint16_t* Vb = a.V + base;
+    // scores s = scale * q_h . k_t
+    for (int t = 0; t < valid; ++t) {
+      for (int d = 0; d < kDim; ++d) row[d] = widen(Kb[t * kDim + d]);
+      for (int h = 0; h < G; ++h) {
+        float part[kLanes] = {};
+        for (int d = 0; d < kDim; d += kLanes)
+          for (int e = 0; e < kLanes; ++e) part[e] += q[h][d + e] * row[d + e];
+        for (int w = kLanes / 2; w > 0; w /= 2)
+          for (int e = 0; e < w; ++e) part[e] += part[e + w];
+        s[h][t] = a.scale * part[0];
+      }
+    }
+    // online softmax: the running sums move to the new maximum, s becomes the probabilities
+    for (int h = 0; h < G; ++h) {
+      float mb = m[h];
+      for (int t = 0; t < valid; ++t) mb = std::max(mb, s[h][t]);
+      const float corr = m[h] == -INFINITY ? 0.f : std::exp(m[h] - mb);
+      float sum = 0.f;
+      for (int t = 0; t < valid; ++t) {
+        s[h][t] = std::exp(s[h][t] - mb);
+        sum += s[h][t];
+      }
+      l[h] = l[h] * corr + sum;
+      if (corr != 1.f)
+        for (int d = 0; d < kDim; ++d) acc[h][d] *= corr;
+      m[h] = mb;
+    }
+    // acc_h += p_h(t) v_t
+    for (int t = 0; t < valid; ++t) {
+      for (int d = 0; d < kDim; ++d) row[d] = widen(Vb[t * kDim + d]);
+      for (int h = 0; h < G; ++h) {
+        const float p = s[h][t];
+        for (int d = 0; d < kDim; ++d) acc[h][d] += p * row[d];
+      }
+    }
+  }
+  for (int h = 0; h < G; ++h) {
+    const int64_t r = static_cast<int64_t>(b) * a.Hq + static_cast<int64_t>(kvh) * G + h;
+    const float inv = l[h] > 0.f ? 1.f / l[h] : 0.f;
+    for (int d = 0; d < kDim; ++d) a.O[r * kDim + d] = acc[h][d] * inv;
+    a.lse[r] = l[h] > 0.f ? m[h] + std::log(l[h]) : -INFINITY;
+  }
+}
+
+}  // namespace
+
+extern "C" int scout_cpu_attend(const void* q, const void* K, const void* V, const int32_t* seq_len,
+                                const int32_t* cpu_list, const int32_t* cpu_count, int B, int Hq, int Hkv, int D,
+                                int P, int nblk_cap, int k, float scale, float* O_cpu, float* lse_cpu,
+                                int n_threads) {
+  if (q == nullptr || K == nullptr || V == nullptr || seq_len == nullptr || cpu_list == nullptr ||
+      cpu_count == nullptr || O_cpu == nullptr || lse_cpu == nullptr || B <= 0 || Hq <= 0 || Hkv <= 0 ||
+      nblk_cap <= 0 || k <= 0 || Hq % Hkv != 0 || Hq / Hkv > kMaxGroup || !(scale > 0.f) || !std::isfinite(scale))
+    return SCOUT_ERR_INVALID_ARG;
+  if (D != kDim || (P != 16 && P != 32 && P != 64)) return SCOUT_ERR_UNSUPPORTED;
+  const int units = B * Hkv;
+  for (int u = 0; u < units; ++u) {  // every list is checked before anything is written
+    const int n = cpu_count[u];
+    if (n < 0 || n > k) return SCOUT_ERR_INVALID_ARG;
+    for (int i = 0; i < n; ++i) {
+      const int j = cpu_list[static_cast<int64_t>(u) * k + i];
+      if (j < 0 || j >= nblk_cap) return SCOUT_ERR_INVALID_ARG;
+    }
+  }
+  const Job a{static_cast<const uint16_t*>(q), static_cast<const uint16_t*>(K), static_cast<const uint16_t*>(V),
+              seq_len, cpu_list, cpu_count, Hq, Hkv, Hq / Hkv, P, nblk_cap, k, scale, O_cpu, lse_cpu};
+  int nt = n_threads > 0 ? n_threads : static_cast<int>(std::max(1u, std::thread::hardware_concurrency()));
+  nt = std::min(nt, units);
+  std::atomic<int> next{0};
+  auto work = [&a, &next, units]() {
+    for (int u = next.fetch_add(1); u < units; u = next.fetch_add(1)) attend_unit(a, u);
+  };
+  std::vector<std::thread> pool;
+  for (int i = 1; i < nt; ++i) {
+    try {
+      pool.emplace_back(work);
+    } catch (...) {  // no thread to be had: the ones running (at least this one) do the rest
+      break;
+    }
+  }
+  work();
+  for (auto& th : pool) th.join();
+  return SCOUT_OK;
+}

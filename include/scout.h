@@ -312,6 +312,37 @@ int scout_plan_recall(const float* scores, const int32_t* topk_idx, const int32_
                       const uint32_t* resident_bits, const int32_t* page_table, int units, int nblk_cap, int k,
                       scout_recall_op* ops, int max_ops, int* n_ops);
 
+/* ------------------------------------------------------------------------ *
+ * CPU-side attention over the offloaded blocks (host code; no GPU involved).
+ * ScoutAttention (arXiv HTML), section 3.2 and Algorithm 1 (CPUAttn of B_cpu,
+ * spawned one layer ahead): the selected blocks that are not resident on the GPU
+ * are attended on the CPU, next to the host copy of the KV cache, with the
+ * predicted query; the GPU merges the result with its own partial
+ * (scout_merge, scout_sparse_attn_merge).
+ *
+ * q         bf16 [B][Hq][D] host: the query of the CPU side (Q_pred, one layer ahead)
+ * K, V      bf16 [B][Hkv][nblk_cap][P][D] host: every block of the layer in logical
+ *           order (block j of unit u = b * Hkv + kvh at K + ((u * nblk_cap + j) * P) * D)
+ * seq_len   int32 [B] host; tokens t >= seq_len[b] are masked
+ * cpu_list  int32 [B][Hkv][k] host, cpu_count int32 [B][Hkv] host: the CPU work list
+ *           as scout_score_topk writes it (the first cpu_count[u] entries are used)
+ * O_cpu     fp32 [B][Hq][D] host out: per query head the normalised output over the
+ *           tokens of the unit's listed blocks (query head h reads KV head h / (Hq / Hkv))
+ * lse_cpu   fp32 [B][Hq] host out: natural-log LSE of scale * q.k over those tokens;
+ *           a unit with no token gives O = 0, LSE = -inf
+ * n_threads worker threads, the calling thread included (0: one per hardware thread);
+ *           never more than one per unit.  Units are dealt to the threads one at a time.
+ * Synchronous: returns when every unit is done.  fp32 arithmetic, online softmax block
+ * by block; each block's K and V are read once for all Hq / Hkv query heads of its KV
+ * head.  No allocation visible to the caller; the threads live for the call.
+ * Errors (nothing written): SCOUT_ERR_INVALID_ARG for a NULL pointer, a non-positive
+ * size, Hq not a multiple of Hkv (or more than 8 query heads per KV head), scale <= 0,
+ * a count outside [0, k] or a listed block outside [0, nblk_cap);
+ * SCOUT_ERR_UNSUPPORTED for D != 128 or P not in {16, 32, 64}. */
+int scout_cpu_attend(const void* q, const void* K, const void* V, const int32_t* seq_len, const int32_t* cpu_list,
+                     const int32_t* cpu_count, int B, int Hq, int Hkv, int D, int P, int nblk_cap, int k,
+                     float scale, float* O_cpu, float* lse_cpu, int n_threads);
+
 #ifdef __cplusplus
 }
 #endif
