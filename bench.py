@@ -46,6 +46,7 @@ def parse_args():
     ap.add_argument("--config", default="qwen3_14b")
     ap.add_argument("--impl", default="scout", choices=["scout", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing leg")
+    ap.add_argument("--no-cpu-side", action="store_true", help="skip timing scout_cpu_attend on the host cores")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="target oracle time for cpu_baseline")
     ap.add_argument("--serial", action="store_true", help="one stream, full grids (no overlap)")
     ap.add_argument("--split", default=None,
@@ -301,6 +302,50 @@ def run_e2e(args, t, step, s, world, device):
             "d2h_bytes_per_step": d2h, "ms_per_step": ms, "steps": reps * GRAPH_STEPS}
 
 
+def cpu_side(s, t, seconds=0.5, max_seqs=8):
+    """The CPU side of the collaborative attention (scout_cpu_attend) on this host's cores:
+    attention over the CPU work list of the last timed step with its Q_pred, for the first
+    ``max_seqs`` sequences (their K/V gathered from the pool into logical block order on the
+    host).  Reported beside the GPU numbers, never part of them; a failure is reported, not
+    raised, so that it cannot cost the GPU measurement."""
+    import numpy as np
+
+    import block_sparse_kv_pred_gb300 as bs
+
+    try:
+        Bs = min(s.B, max_seqs)
+        slots = t["page_table"][:Bs].reshape(-1).long()
+        if int(slots.min()) < 0:
+            return {"unavailable": "a block of the sample has no pool slot"}
+        kv = {n: t[n + "_pool"].index_select(0, slots).view(Bs, s.Hkv, s.nblk, s.P, s.D).cpu() for n in "KV"}
+        q = t["Qp1"][:Bs].reshape(Bs, s.Hq, s.D).cpu()
+        lst, cnt, seq = (t[n][:Bs].cpu().contiguous() for n in ("cpu1", "cpu_count1", "seq_len"))
+        listed = np.arange(s.k)[None, None, :] < cnt.numpy()[:, :, None]
+        toks = np.clip(seq.numpy().astype(np.int64)[:, None, None] - lst.numpy().astype(np.int64) * s.P, 0, s.P)
+        nbytes = int((toks * listed).sum()) * s.D * 2 * 2  # K and V of the listed blocks' tokens
+        threads = os.cpu_count() or 1
+
+        def call():
+            bs.cpu_attend(q, kv["K"], kv["V"], seq, lst, cnt, Bs, s.Hq, s.Hkv, s.P, s.k, s.scale, n_threads=threads)
+
+        call()
+        n, t0 = 0, time.perf_counter()
+        while True:
+            call()
+            n += 1
+            el = time.perf_counter() - t0
+            if el >= seconds or n >= 50:
+                break
+        per = el / n
+        return {"value": nbytes / per / 1e9, "unit": "GB/s", "kind": "scout_cpu_attend", "threads": threads,
+                "ms_per_call": per * 1e3, "query_heads_per_s": Bs * s.Hq / per, "kv_bytes_per_call": nbytes,
+                "full_batch_ms_estimate": per * 1e3 * s.B / Bs,
+                "sample": f"{Bs} of {s.B} sequences of {s.name}: the CPU work list of the last timed step with "
+                          f"its Q_pred, {n} calls"}
+    except Exception as e:  # noqa: BLE001
+        return {"unavailable": f"{type(e).__name__}: {e}"[:300]}
+
+
 # ---------------------------------------------------------------------------
 # oracle timing (cpu_baseline leg and --impl reference)
 # ---------------------------------------------------------------------------
@@ -503,6 +548,8 @@ def main():
         "attention_path": attention_path(s, nbytes, r["kern_ms"], peak),
         "wall_s_timed": r["wall"],
     }
+    if world == 1 and not args.no_cpu_side:
+        line["cpu_side"] = cpu_side(s, t)
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(s, args.cpu_seconds)
     print(json.dumps(line), flush=True)

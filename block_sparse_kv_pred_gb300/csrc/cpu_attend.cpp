@@ -7,8 +7,10 @@
 // query rows are held in fp32.  Each listed block's K rows are widened from bf16 once and
 // dotted with all G rows, with 16 independent partial sums per product, so the loop vectorises
 // without reassociating.  A block-wise online softmax then rescales the running sums to the
-// block's maximum, and the block's V rows are accumulated with its probabilities.  Portable
-// C++ only: no intrinsics, the compiler's vectoriser does the rest on x86-64 and AArch64.
+// block's maximum, and the block's V rows are accumulated with its probabilities, four rows per
+// pass over the running sums (measured 10-30% faster than one; two K rows per pass over the
+// query rows was four times slower, the loop no longer vectorising).  Portable C++ only: no
+// intrinsics, the compiler's vectoriser does the rest on x86-64 and AArch64.
 #include <algorithm>
 #include <atomic>
 #include <cmath>
@@ -25,6 +27,12 @@ constexpr int kDim = 128;      // head dimension
 constexpr int kMaxGroup = 8;   // query heads per KV head
 constexpr int kMaxPage = 64;   // tokens per block
 constexpr int kLanes = 16;     // partial sums per dot product
+
+inline float fold(float (&p)[kLanes]) {  // sum of the partial sums, pairwise
+  for (int w = kLanes / 2; w > 0; w /= 2)
+    for (int e = 0; e < w; ++e) p[e] += p[e + w];
+  return p[0];
+}
 
 inline float widen(uint16_t v) {  // bf16 -> fp32 (exact)
   const uint32_t u = static_cast<uint32_t>(v) << 16;
@@ -52,6 +60,8 @@ void attend_unit(const Job& a, int u) {
   alignas(64) float acc[kMaxGroup][kDim];
   alignas(64) float s[kMaxGroup][kMaxPage];
   alignas(64) float row[kDim];
+  alignas(64) float row2[kDim];
+  alignas(64) float vr[4][kDim];
   float m[kMaxGroup], l[kMaxGroup];
   const uint16_t* qg = a.q + (static_cast<int64_t>(b) * a.Hq + static_cast<int64_t>(kvh) * G) * kDim;
   for (int h = 0; h < G; ++h) {
@@ -73,38 +83,50 @@ void attend_unit(const Job& a, int u) {
     const uint16_t* Kb = a.K + base;
     const uint16_t* Vb = a.V + base;
     // scores s = scale * q_h . k_t
-    for (int t = 0; t < valid; ++t) {
+    int t = 0;
+    for (; t < valid; ++t) {
       for (int d = 0; d < kDim; ++d) row[d] = widen(Kb[t * kDim + d]);
       for (int h = 0; h < G; ++h) {
-        float part[kLanes] = {};
+        float p0[kLanes] = {};
         for (int d = 0; d < kDim; d += kLanes)
-          for (int e = 0; e < kLanes; ++e) part[e] += q[h][d + e] * row[d + e];
-        for (int w = kLanes / 2; w > 0; w /= 2)
-          for (int e = 0; e < w; ++e) part[e] += part[e + w];
-        s[h][t] = a.scale * part[0];
+          for (int e = 0; e < kLanes; ++e) p0[e] += q[h][d + e] * row[d + e];
+        s[h][t] = a.scale * fold(p0);
       }
     }
     // online softmax: the running sums move to the new maximum, s becomes the probabilities
     for (int h = 0; h < G; ++h) {
       float mb = m[h];
-      for (int t = 0; t < valid; ++t) mb = std::max(mb, s[h][t]);
+      for (int x = 0; x < valid; ++x) mb = std::max(mb, s[h][x]);
       const float corr = m[h] == -INFINITY ? 0.f : std::exp(m[h] - mb);
       float sum = 0.f;
-      for (int t = 0; t < valid; ++t) {
-        s[h][t] = std::exp(s[h][t] - mb);
-        sum += s[h][t];
+      for (int x = 0; x < valid; ++x) {
+        s[h][x] = std::exp(s[h][x] - mb);
+        sum += s[h][x];
       }
       l[h] = l[h] * corr + sum;
       if (corr != 1.f)
         for (int d = 0; d < kDim; ++d) acc[h][d] *= corr;
       m[h] = mb;
     }
-    // acc_h += p_h(t) v_t
-    for (int t = 0; t < valid; ++t) {
+    // acc_h += p_h(t) v_t, four tokens per pass over acc_h
+    for (t = 0; t + 4 <= valid; t += 4) {
+      for (int d = 0; d < kDim; ++d) {
+        vr[0][d] = widen(Vb[t * kDim + d]);
+        vr[1][d] = widen(Vb[(t + 1) * kDim + d]);
+        vr[2][d] = widen(Vb[(t + 2) * kDim + d]);
+        vr[3][d] = widen(Vb[(t + 3) * kDim + d]);
+      }
+      for (int h = 0; h < G; ++h) {
+        const float w0 = s[h][t], w1 = s[h][t + 1], w2 = s[h][t + 2], w3 = s[h][t + 3];
+        for (int d = 0; d < kDim; ++d)
+          acc[h][d] += (w0 * vr[0][d] + w1 * vr[1][d]) + (w2 * vr[2][d] + w3 * vr[3][d]);
+      }
+    }
+    for (; t < valid; ++t) {
       for (int d = 0; d < kDim; ++d) row[d] = widen(Vb[t * kDim + d]);
       for (int h = 0; h < G; ++h) {
-        const float p = s[h][t];
-        for (int d = 0; d < kDim; ++d) acc[h][d] += p * row[d];
+        const float w0 = s[h][t];
+        for (int d = 0; d < kDim; ++d) acc[h][d] += w0 * row[d];
       }
     }
   }
