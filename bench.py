@@ -323,7 +323,8 @@ def cpu_side(s, t, seconds=0.5, max_seqs=8):
         listed = np.arange(s.k)[None, None, :] < cnt.numpy()[:, :, None]
         toks = np.clip(seq.numpy().astype(np.int64)[:, None, None] - lst.numpy().astype(np.int64) * s.P, 0, s.P)
         nbytes = int((toks * listed).sum()) * s.D * 2 * 2  # K and V of the listed blocks' tokens
-        threads = os.cpu_count() or 1
+        # the cores this process may run on (the machine may have more)
+        threads = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else (os.cpu_count() or 1)
 
         def call():
             bs.cpu_attend(q, kv["K"], kv["V"], seq, lst, cnt, Bs, s.Hq, s.Hkv, s.P, s.k, s.scale, n_threads=threads)
