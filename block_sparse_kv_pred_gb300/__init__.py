@@ -15,7 +15,7 @@ import torch
 __all__ = [
     "ScoutError", "lib", "MINMAX", "MEAN", "predict_q", "build_digest", "score_topk", "score_topk_workspace",
     "sparse_attn", "sparse_attn_merge", "sparse_attn_workspace", "merge", "recall_async", "commit_residency",
-    "plan_recall", "cpu_attend", "RecallOp", "Launch", "Prepared",
+    "plan_recall", "recall_intervals", "cpu_attend", "RecallOp", "Launch", "Prepared",
 ]
 
 MINMAX = 0
@@ -62,6 +62,7 @@ _SIGS = {
     "scout_commit_residency": ([_p, _i, _p, _p, _i64, _i, _i, _i, _p, _p], _i),
     "scout_plan_recall": ([_p, _p, _p, _p, _p, _i, _i, _i, _p, _i, _p], _i),
     "scout_cpu_attend": ([_p, _p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _i, _f, _p, _p, _i], _i),
+    "scout_recall_intervals": ([_p, _i, _i, _f, _p], _i),
 }
 
 
@@ -302,6 +303,23 @@ def plan_recall(scores, topk_idx, topk_count, resident_bits, page_table, k):
     _check(lib().scout_plan_recall(ptr(sc), ptr(ti), ptr(tc), ptr(rb), ptr(pt), units, nblk, k, ops, cap,
                                    ctypes.byref(n)), "scout_plan_recall")
     return np.array([[o.unit, o.block, o.slot, o.evict_block] for o in ops[: n.value]], dtype=np.int32).reshape(-1, 4)
+
+
+def recall_intervals(ratio, beta=0.12):
+    """Per-layer recall intervals (section 3.4) from CPU-compute-ratio traces.
+
+    ``ratio``: host array [layers][steps], layer l's ratio at the (s+1)-th decoding step after
+    a refresh, from a profiling run without recalls.  Returns int32 [layers]: the largest number
+    of leading steps whose ratio is below ``beta``, at least 1 and at most ``steps``."""
+    import numpy as np
+
+    r = np.ascontiguousarray(ratio, dtype=np.float32)
+    if r.ndim != 2:
+        raise ScoutError("ratio must be [layers][steps]")
+    out = np.zeros(r.shape[0], dtype=np.int32)
+    _check(lib().scout_recall_intervals(r.ctypes.data_as(ctypes.c_void_p), r.shape[0], r.shape[1], float(beta),
+                                        out.ctypes.data_as(ctypes.c_void_p)), "scout_recall_intervals")
+    return out
 
 
 def _host(t, dtype, name: str) -> int:

@@ -8,6 +8,7 @@
 // bits change only in scout_commit_residency, which the caller orders after the
 // copies' event, so a block never looks resident before its bytes have landed.
 #include <algorithm>
+#include <cmath>
 #include <vector>
 
 #include "common.cuh"
@@ -138,5 +139,19 @@ extern "C" int scout_plan_recall(const float* scores, const int32_t* topk_idx, c
     std::sort(ops + first, ops + n, [](const scout_recall_op& x, const scout_recall_op& y) { return x.block < y.block; });
   }
   *n_ops = n;
+  return SCOUT_OK;
+}
+
+// Per-layer recall intervals (section 3.4): for each layer, the number of leading profiled
+// steps whose CPU compute ratio stays below beta, at least 1 and at most the profile's length.
+extern "C" int scout_recall_intervals(const float* ratio, int layers, int steps, float beta, int32_t* interval) {
+  if (ratio == nullptr || interval == nullptr || layers <= 0 || steps <= 0 || !(beta > 0.f) || !std::isfinite(beta))
+    return SCOUT_ERR_INVALID_ARG;
+  for (int l = 0; l < layers; ++l) {
+    const float* r = ratio + (int64_t)l * steps;
+    int n = 0;
+    while (n < steps && r[n] < beta) ++n;  // a NaN is not below beta
+    interval[l] = n > 0 ? n : 1;
+  }
   return SCOUT_OK;
 }

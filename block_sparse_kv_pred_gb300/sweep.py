@@ -21,7 +21,9 @@ Readings taken where the pages leave it open (the same as the oracle's):
 Per step the sweep reports the CPU work-list size, its delta against the previous step,
 the CPU ratio (CPU blocks over the budget) and, on recall steps, the bytes moved and
 the host-to-device rate.  ``python -m block_sparse_kv_pred_gb300.sweep`` runs the
-64-step sweep at batch 16 and 64K context and prints one line per step.
+64-step sweep at batch 16 and 64K context and prints one line per step;
+``--profile-layers L`` instead decodes L seeded layers without recalls and prints each
+layer's recall interval (section 3.4, threshold ``--beta``).
 """
 from __future__ import annotations
 
@@ -58,6 +60,7 @@ class DecodeSweep:
     """The layer's state on the GPU and the host, and one method per decode step."""
 
     def __init__(self, shape: W.Shape, steps: int, recall_every: int = 16, device="cuda"):
+        """``recall_every`` 0: no recall (the profile from which recall intervals are read)."""
         self.s = s = shape
         self.steps, self.recall_every = steps, recall_every
         dev = self.dev = torch.device(device)
@@ -161,7 +164,7 @@ class DecodeSweep:
         n_cpu, n_delta = int(rec["cpu_count"].sum()), int(rec["delta_count"].sum())
         stats = {"step": t, "cpu_blocks": n_cpu, "delta_blocks": n_delta, "cpu_ratio": n_cpu / (s.k * U),
                  "recall_blocks": 0, "recall_bytes": 0, "recall_h2d_gbs": None}
-        if t % self.recall_every == self.recall_every - 1:
+        if self.recall_every > 0 and t % self.recall_every == self.recall_every - 1:
             # the block being written stays on the GPU: the planner sees it as the most important
             # resident block, so it is evicted last, and never (at least k + 1 blocks are resident,
             # at most k come in)
@@ -183,11 +186,39 @@ class DecodeSweep:
         return rec
 
 
+def profile_recall_intervals(layers: int, steps: int, beta: float = 0.12, shape: W.Shape | None = None):
+    """Offline profile of section 3.4: each layer (its own seeded workload) decodes ``steps``
+    steps without recalls; its CPU compute ratio trace gives its recall interval, the largest
+    number of steps that keeps the ratio below ``beta``.  Returns (traces [layers][steps],
+    intervals [layers])."""
+    import dataclasses
+
+    base = shape or c4_shape(steps)
+    traces = np.zeros((layers, steps), dtype=np.float32)
+    for layer in range(layers):
+        sw = DecodeSweep(dataclasses.replace(base, seed=base.seed + layer), steps, recall_every=0)
+        for t in range(steps):
+            traces[layer, t] = sw.step()["stats"]["cpu_ratio"]
+        del sw
+        torch.cuda.empty_cache()
+    return traces, bs.recall_intervals(traces, beta)
+
+
 def main():
     ap = argparse.ArgumentParser(description="Residency sweep: one layer, many decode steps, per-step report")
     ap.add_argument("--steps", type=int, default=64)
-    ap.add_argument("--recall-every", type=int, default=16)
+    ap.add_argument("--recall-every", type=int, default=16, help="0: no recall")
+    ap.add_argument("--profile-layers", type=int, default=0,
+                    help="instead: profile this many layers without recalls and print their recall intervals")
+    ap.add_argument("--beta", type=float, default=0.12, help="CPU compute ratio threshold of the profile")
     a = ap.parse_args()
+    if a.profile_layers > 0:
+        traces, iv = profile_recall_intervals(a.profile_layers, a.steps, a.beta)
+        for layer in range(a.profile_layers):
+            print(json.dumps({"layer": layer, "interval": int(iv[layer]),
+                              "ratio": [round(float(x), 4) for x in traces[layer]]}), flush=True)
+        print(json.dumps({"beta": a.beta, "mean_interval": float(iv.mean())}), flush=True)
+        return
     sw = DecodeSweep(c4_shape(a.steps), a.steps, a.recall_every)
     for _ in range(a.steps):
         print(json.dumps(sw.step()["stats"]), flush=True)

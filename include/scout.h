@@ -313,6 +313,24 @@ int scout_plan_recall(const float* scores, const int32_t* topk_idx, const int32_
                       scout_recall_op* ops, int max_ops, int* n_ops);
 
 /* ------------------------------------------------------------------------ *
+ * Per-layer recall intervals from an offline profile (host code).
+ * ScoutAttention (arXiv HTML), section 3.4: the recall interval of each layer is
+ * the largest number of decoding steps that keeps the measured CPU compute ratio
+ * (tokens computed on the CPU over the sparse budget) below a threshold beta
+ * (12% by default in the pages), read from a profiling run without recalls.
+ *
+ * ratio     fp32 [layers][steps] host: layer l's CPU compute ratio at the (s+1)-th
+ *           decoding step after its resident set was refreshed (prefill or recall)
+ * interval  int32 [layers] host out: the largest n in [1, steps] with
+ *           ratio[l][s] < beta for every s < n; 1 when even the first step is not
+ *           below beta (recall every step); steps when no profiled step reaches beta
+ *           (the profile's horizon bounds the interval).  A NaN ratio counts as not
+ *           below beta.
+ * Errors (nothing written): SCOUT_ERR_INVALID_ARG for a NULL pointer, layers or
+ * steps <= 0, or beta not a positive finite number. */
+int scout_recall_intervals(const float* ratio, int layers, int steps, float beta, int32_t* interval);
+
+/* ------------------------------------------------------------------------ *
  * CPU-side attention over the offloaded blocks (host code; no GPU involved).
  * ScoutAttention (arXiv HTML), section 3.2 and Algorithm 1 (CPUAttn of B_cpu,
  * spawned one layer ahead): the selected blocks that are not resident on the GPU

@@ -204,6 +204,22 @@ def apply_recall(slot_of, resident_mask, ops):
     return slot_of, resident_mask
 
 
+def recall_intervals(traces, beta=0.12):
+    """Per-layer recall intervals from an offline profile (section 3.4: for each layer, the
+    largest number of steps that keeps the measured CPU compute ratio below the threshold beta,
+    12% by default).  traces[l][s] is layer l's ratio at the (s+1)-th step after a refresh.
+    Readings: every step of the interval must be below beta (strictly); an interval is at least
+    one step (recall every step) and at most the profiled length."""
+    out = []
+    for trace in traces:
+        best = 0
+        for n in range(1, len(trace) + 1):  # every candidate length, checked in full
+            if all(float(r) < beta for r in trace[:n]):
+                best = n
+        out.append(max(best, 1))
+    return out
+
+
 # ---------------------------------------------------------------------------
 # partial attention and merge  (section 3.2; FlashAttention / online softmax)
 # ---------------------------------------------------------------------------
