@@ -24,7 +24,10 @@ CPU Pre-computation for LLM Inference", arXiv 2603.27138):
   Q_pred^{i+1} = W_Q^{i+1} X^i; B_pred = TopK(Q_pred K_digest^T);
   B_cpu = B_pred minus B_gpu; A = MERGE(A_gpu, A_cpu).
 * arXiv HTML, section 3.4 (asynchronous periodic recall): important blocks are
-  periodically copied back into GPU memory.
+  periodically copied back into GPU memory; each layer's recall interval is the
+  largest number of decoding steps that keeps its CPU compute ratio (CPU tokens
+  over the sparse budget) below a threshold beta, 12% by default, read from an
+  offline profile.
 
 Readings where the pages are silent (listed again in the design notes):
 * GQA: query head h reads KV head h // G; one selection per (sequence, KV head),
