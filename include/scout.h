@@ -11,6 +11,10 @@
  *   the work is enqueued.  Arguments are checked on the host before any launch;
  *   a rejected call launches nothing.  A launch failure reported by the CUDA
  *   runtime returns SCOUT_ERR_CUDA.
+ * - The host-side entry points (scout_plan_recall, scout_recall_intervals,
+ *   scout_cpu_attend) are the exception: host pointers only, synchronous, no GPU
+ *   involved.  scout_cpu_attend also runs on worker threads it starts and joins
+ *   within the call.
  * - bf16 tensors are IEEE bfloat16 (2 bytes); fp32 are IEEE binary32.
  * - Shapes: B sequences, Hq query heads, Hkv KV heads (G = Hq / Hkv query heads
  *   per KV head, 1 <= G <= 8), D = 128 head dims, P tokens per KV block
