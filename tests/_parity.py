@@ -18,7 +18,6 @@ import torch
 import oracle as O
 import block_sparse_kv_pred_gb300 as bs
 from block_sparse_kv_pred_gb300 import build as B
-from block_sparse_kv_pred_gb300 import workload as W
 
 ATOL, RTOL = 2e-3, 1e-2
 SCORE_REL = 1e-4

@@ -12,7 +12,7 @@ import block_sparse_kv_pred_gb300 as bs
 from block_sparse_kv_pred_gb300 import workload as W
 from block_sparse_kv_pred_gb300.step import EARLY_OF, SPLIT, setup_step
 from block_sparse_kv_pred_gb300.workload import device as WD
-from _parity import bf16_bits, check_attention, check_selection, ensure_built, to_dev
+from _parity import bf16_bits, check_attention, check_selection, ensure_built
 
 pytestmark = pytest.mark.gpu
 
