@@ -60,7 +60,6 @@ void attend_unit(const Job& a, int u) {
   alignas(64) float acc[kMaxGroup][kDim];
   alignas(64) float s[kMaxGroup][kMaxPage];
   alignas(64) float row[kDim];
-  alignas(64) float row2[kDim];
   alignas(64) float vr[4][kDim];
   float m[kMaxGroup], l[kMaxGroup];
   const uint16_t* qg = a.q + (static_cast<int64_t>(b) * a.Hq + static_cast<int64_t>(kvh) * G) * kDim;
