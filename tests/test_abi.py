@@ -106,3 +106,30 @@ def test_launch_options_layout_and_step_checks():
         setup_step(W.tiny(), "cpu", pdl=True)
     with pytest.raises(ValueError, match="early starters"):
         setup_step(W.tiny(), "cpu", early=("build_digest",))
+
+
+def test_packed_step_buffers_are_aligned_and_disjoint():
+    """The step's per-parity input and output sets are views of one byte buffer each (one copy
+    moves a set): every view starts on a 256-byte boundary (TMA needs 16), has its shape and
+    dtype, and no two views overlap."""
+    import torch
+
+    from block_sparse_kv_pred_gb300.step import packed
+
+    specs = [("X", (40, 5120), torch.bfloat16), ("lse", (40, 40), torch.float32), ("cnt", (3, 5), torch.int32),
+             ("q", (40, 40, 128), torch.bfloat16)]
+    buf, views = packed(specs, "cpu")
+    base = buf.data_ptr()
+    spans = []
+    for name, shape, dtype in specs:
+        v = views[name]
+        assert v.shape == shape and v.dtype == dtype and v.is_contiguous()
+        off = v.data_ptr() - base
+        assert off % 256 == 0
+        spans.append((off, off + v.numel() * v.element_size()))
+    spans.sort()
+    assert all(a[1] <= b[0] for a, b in zip(spans, spans[1:])) and spans[-1][1] <= buf.numel()
+    for i, (name, _, _) in enumerate(specs):
+        views[name].fill_(i + 1)
+    for i, (name, _, _) in enumerate(specs):
+        assert torch.all(views[name] == i + 1)
