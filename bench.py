@@ -223,7 +223,7 @@ def run_scout(args, rank, world, local):
     e2e = run_e2e(args, t, step, s, world, device)
     return s, wl, t, dict(ms=ms, value=value, kern_ms=kern_ms, clocks=clocks, wall=wall, e2e=e2e,
                           launches=step.launches_per_step * args.steps, split=None if args.serial else split,
-                          early=() if args.serial else early)
+                          early=() if args.serial else early, step=step)
 
 
 def run_e2e(args, t, step, s, world, device):
@@ -344,6 +344,112 @@ def cpu_side(s, t, seconds=0.5, max_seqs=8):
                           f"its Q_pred, {n} calls"}
     except Exception as e:  # noqa: BLE001
         return {"unavailable": f"{type(e).__name__}: {e}"[:300]}
+
+
+def layer_ahead(s, t, step, gpu_ms, steps=24, warm=4, limit_s=60.0):
+    """Algorithm 1's pipeline with the CPU side computed for real: after step i's selection its
+    CPU work list and Q_pred go down to the host, where scout_cpu_attend computes the next
+    layer's CPU partial on the host cores (one worker thread driving the library's threads)
+    while the GPU goes on; the partial goes up before step i+1's attention, which waits for it.
+    The single synthetic layer stands for every layer, as in the step.  Host wall time per step
+    against the GPU-only step (graph replay) gives the fraction of the time the GPU would idle.
+    Every wait is bounded and a failure is reported, not raised, so that it cannot cost the
+    GPU measurement."""
+    import concurrent.futures as cf
+
+    import torch
+
+    import block_sparse_kv_pred_gb300 as bs
+
+    if step.serial:
+        return {"unavailable": "serial step"}
+    pool = cf.ThreadPoolExecutor(1)
+    dev = t["Qp0"].device
+    try:
+        t_end = time.perf_counter() + limit_s
+        slots = t["page_table"].reshape(-1).long()
+        if int(slots.min()) < 0:
+            return {"unavailable": "a block has no pool slot"}
+        # the layer's K/V in logical block order on the host: the copy the CPU side attends
+        hkv = {n: t[n + "_pool"].index_select(0, slots).view(s.B, s.Hkv, s.nblk, s.P, s.D).cpu() for n in "KV"}
+        seq = t["seq_len"].cpu().contiguous()
+        threads = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else (os.cpu_count() or 1)
+        st = step.fresh()
+        sB = st.streams[1]
+        sH = torch.cuda.Stream(dev)  # the pipeline's host<->device copies, in issue order
+
+        def pin(x):
+            return torch.empty_like(x, device="cpu").pin_memory()
+
+        h_q = [pin(t[f"Qp{p}"]) for p in (0, 1)]
+        h_list = [pin(t[f"cpu{p}"]) for p in (0, 1)]
+        h_cnt = [pin(t[f"cpu_count{p}"]) for p in (0, 1)]
+        h_O = [pin(t["O_cpu0"]) for _ in (0, 1)]
+        h_L = [pin(t["lse_cpu0"]) for _ in (0, 1)]
+        down = [torch.cuda.Event(), torch.cuda.Event()]
+        up = [torch.cuda.Event(), torch.cuda.Event()]
+        cpu_s = []
+
+        def cpu_layer(par):
+            # the next layer's CPU partial from the step of parity par (its list and Q_pred)
+            while not down[par].query():
+                if time.perf_counter() > t_end:
+                    raise TimeoutError("the work list did not reach the host")
+                time.sleep(2e-5)
+            c0 = time.perf_counter()
+            bs.cpu_attend(h_q[par].view(s.B, s.Hq, s.D), hkv["K"], hkv["V"], seq, h_list[par], h_cnt[par], s.B,
+                          s.Hq, s.Hkv, s.P, s.k, s.scale, O_cpu=h_O[1 - par], lse_cpu=h_L[1 - par], n_threads=threads)
+            cpu_s.append(time.perf_counter() - c0)
+            return 1 - par
+
+        ev0 = torch.cuda.Event()
+        ev0.record(torch.cuda.current_stream(dev))
+        st.begin(ev0)
+        sH.wait_event(ev0)
+        pending, t0 = None, None
+        for i in range(warm + steps):
+            if i == warm:
+                t0 = time.perf_counter()
+            par = st.i % 2
+            if pending is not None:
+                if pending.result(timeout=max(0.0, t_end - time.perf_counter())) != par:
+                    raise RuntimeError("pipeline parity")
+                if i >= 2:
+                    sH.wait_event(st.attn_done[par])  # the attention two steps back read this buffer
+                with torch.cuda.stream(sH):
+                    t[f"O_cpu{par}"].copy_(h_O[par], non_blocking=True)
+                    t[f"lse_cpu{par}"].copy_(h_L[par], non_blocking=True)
+                up[par].record(sH)
+                sB.wait_event(up[par])
+            st.issue(after_begin=(i == 0))
+            sH.wait_event(st.sel_done[par])  # the selection (after its GEMM) wrote list set par
+            with torch.cuda.stream(sH):
+                h_q[par].copy_(t[f"Qp{par}"], non_blocking=True)
+                h_list[par].copy_(t[f"cpu{par}"], non_blocking=True)
+                h_cnt[par].copy_(t[f"cpu_count{par}"], non_blocking=True)
+            down[par].record(sH)
+            pending = pool.submit(cpu_layer, par)
+        pending.result(timeout=max(0.0, t_end - time.perf_counter()))
+        st.end(None)
+        torch.cuda.synchronize(dev)
+        ms = (time.perf_counter() - t0) / steps * 1e3
+        cpu_ms = statistics.mean(cpu_s[warm:]) * 1e3 if len(cpu_s) > warm else None
+        if int(t["status"].item()) != 0:
+            return {"unavailable": f"device status {int(t['status'].item())}"}
+        return {"ms_per_step": ms, "value": s.B * s.Hq / (ms / 1e3), "unit": "query-heads/s",
+                "cpu_ms_per_layer": cpu_ms, "gpu_step_ms": gpu_ms, "gpu_idle_frac": max(0.0, 1.0 - gpu_ms / ms),
+                "threads": threads, "steps": steps,
+                "note": "the step issued on its streams (not graph-replayed), the CPU partial of every step "
+                        "computed by scout_cpu_attend from the previous step's work list; gpu_idle_frac compares "
+                        "the graph-replayed GPU-only step with this wall time"}
+    except Exception as e:  # noqa: BLE001
+        return {"unavailable": f"{type(e).__name__}: {e}"[:300]}
+    finally:
+        pool.shutdown(wait=False)
+        try:
+            torch.cuda.synchronize(dev)
+        except Exception:  # noqa: BLE001  (already reported above)
+            pass
 
 
 # ---------------------------------------------------------------------------
@@ -550,6 +656,7 @@ def main():
     }
     if world == 1 and not args.no_cpu_side:
         line["cpu_side"] = cpu_side(s, t)
+        line["layer_ahead"] = layer_ahead(s, t, r["step"], r["ms"])
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(s, args.cpu_seconds)
     print(json.dumps(line), flush=True)
