@@ -67,3 +67,33 @@ def test_bad_arguments_are_rejected():
     assert L.scout_recall_intervals(p(r), 2, 3, f(float("nan")), p(out)) == 1
     assert np.all(out == -7)
     assert L.scout_recall_intervals(p(r), 2, 3, f(0.12), p(out)) == 0 and list(out) == [3, 3]
+
+
+def test_profile_assembles_one_seeded_trace_per_layer(monkeypatch):
+    """sweep.profile_recall_intervals without a GPU: a scripted stand-in for the decode sweep
+    checks that every layer gets its own seed, decodes without recalls, and that the traces are
+    assembled in step order and turned into intervals by the rule."""
+    torch = pytest.importorskip("torch")
+    import block_sparse_kv_pred_gb300.sweep as S
+    from block_sparse_kv_pred_gb300 import workload as W
+
+    seen = []
+
+    class Scripted:
+        def __init__(self, shape, steps, recall_every=16, device="cuda"):
+            assert recall_every == 0
+            seen.append(shape.seed)
+            self.slope, self.t = 0.01 * (shape.seed + 1), 0
+
+        def step(self):
+            self.t += 1
+            return {"stats": {"cpu_ratio": self.slope * self.t}}
+
+    monkeypatch.setattr(S, "DecodeSweep", Scripted)
+    monkeypatch.setattr(torch.cuda, "empty_cache", lambda: None)
+    base = W.Shape("p", B=1, Hq=8, Hkv=2, T=256, P=32, k=4, resident_frac=0.0, seed=3)
+    traces, iv = S.profile_recall_intervals(3, 10, 0.12, shape=base)
+    assert seen == [3, 4, 5]
+    want = np.array([[0.01 * (sd + 1) * (t + 1) for t in range(10)] for sd in (3, 4, 5)], dtype=np.float32)
+    assert np.allclose(traces, want)
+    assert list(iv) == O.recall_intervals(traces.tolist(), np.float32(0.12))
