@@ -9,7 +9,7 @@ import pytest
 import torch
 
 import oracle as O
-from block_sparse_kv_pred_gb300.sweep import DecodeSweep, c4_shape, profile_recall_intervals
+from block_sparse_kv_pred_gb300.sweep import DecodeSweep, c4_shape
 from _parity import check_attention, check_selection, ensure_built
 
 pytestmark = pytest.mark.gpu
@@ -71,12 +71,3 @@ def test_c4_sweep_full_shape():
     # right after a recall the whole selection is resident, so the CPU list only holds what
     # the next selection adds
     assert stats[RECALL_EVERY]["cpu_blocks"] < stats[RECALL_EVERY - 1]["cpu_blocks"]
-
-
-def test_recall_interval_profile():
-    """Section 3.4's offline profile at the sweep shape: two seeded layers decode without
-    recalls; each trace holds a CPU compute ratio per step, and each interval is the oracle's
-    rule applied to that trace."""
-    traces, iv = profile_recall_intervals(2, 4, 0.12)
-    assert traces.shape == (2, 4) and np.all((traces >= 0) & (traces <= 1))
-    assert list(iv) == O.recall_intervals(traces.tolist(), np.float32(0.12))
