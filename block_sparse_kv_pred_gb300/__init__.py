@@ -15,7 +15,7 @@ import torch
 __all__ = [
     "ScoutError", "lib", "MINMAX", "MEAN", "predict_q", "build_digest", "score_topk", "score_topk_workspace",
     "sparse_attn", "sparse_attn_merge", "sparse_attn_workspace", "merge", "recall_async", "commit_residency",
-    "plan_recall", "recall_intervals", "cpu_attend", "RecallOp", "Launch", "Prepared",
+    "plan_recall", "plan_recall_pages", "recall_intervals", "cpu_attend", "RecallOp", "Launch", "Prepared",
 ]
 
 MINMAX = 0
@@ -63,6 +63,7 @@ _SIGS = {
     "scout_plan_recall": ([_p, _p, _p, _p, _p, _i, _i, _i, _p, _i, _p], _i),
     "scout_cpu_attend": ([_p, _p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _i, _f, _p, _p, _i], _i),
     "scout_recall_intervals": ([_p, _i, _i, _f, _p], _i),
+    "scout_plan_recall_pages": ([_p, _p, _p, _p, _p, _i, _i, _i, _i, _p, _i, _p], _i),
 }
 
 
@@ -302,6 +303,29 @@ def plan_recall(scores, topk_idx, topk_count, resident_bits, page_table, k):
     ptr = lambda a: a.ctypes.data_as(ctypes.c_void_p)  # noqa: E731
     _check(lib().scout_plan_recall(ptr(sc), ptr(ti), ptr(tc), ptr(rb), ptr(pt), units, nblk, k, ops, cap,
                                    ctypes.byref(n)), "scout_plan_recall")
+    return np.array([[o.unit, o.block, o.slot, o.evict_block] for o in ops[: n.value]], dtype=np.int32).reshape(-1, 4)
+
+
+def plan_recall_pages(scores, topk_idx, topk_count, resident_bits, page_table, B, Hkv, k):
+    """Recall ops with residency per page (one block of a sequence for all its KV heads).
+
+    Host arrays as for plan_recall (units = B * Hkv; the residency bits of a sequence's heads
+    must be identical).  Returns int32 [n][4] (unit, block in, slot, block out): one op per KV
+    head and page pair, grouped by unit, ascending block in."""
+    import numpy as np
+
+    sc = np.ascontiguousarray(scores, dtype=np.float32)
+    ti = np.ascontiguousarray(topk_idx, dtype=np.int32)
+    tc = np.ascontiguousarray(topk_count, dtype=np.int32)
+    rb = np.ascontiguousarray(resident_bits, dtype=np.uint32)
+    pt = np.ascontiguousarray(page_table, dtype=np.int32)
+    nblk = sc.shape[-1]
+    cap = max(1, int(tc.clip(0, k).sum()) * Hkv)
+    ops = (RecallOp * cap)()
+    n = ctypes.c_int(0)
+    ptr = lambda a: a.ctypes.data_as(ctypes.c_void_p)  # noqa: E731
+    _check(lib().scout_plan_recall_pages(ptr(sc), ptr(ti), ptr(tc), ptr(rb), ptr(pt), B, Hkv, nblk, k, ops, cap,
+                                         ctypes.byref(n)), "scout_plan_recall_pages")
     return np.array([[o.unit, o.block, o.slot, o.evict_block] for o in ops[: n.value]], dtype=np.int32).reshape(-1, 4)
 
 

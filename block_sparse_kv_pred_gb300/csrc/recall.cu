@@ -9,6 +9,7 @@
 // copies' event, so a block never looks resident before its bytes have landed.
 #include <algorithm>
 #include <cmath>
+#include <utility>
 #include <vector>
 
 #include "common.cuh"
@@ -137,6 +138,69 @@ extern "C" int scout_plan_recall(const float* scores, const int32_t* topk_idx, c
       ops[n++] = scout_recall_op{u, in[i], slot, ev[i]};
     }
     std::sort(ops + first, ops + n, [](const scout_recall_op& x, const scout_recall_op& y) { return x.block < y.block; });
+  }
+  *n_ops = n;
+  return SCOUT_OK;
+}
+
+// Recall plan with residency per page (one block of a sequence for all its KV heads): the
+// pages some head selects that are not resident come in, the most important first (the largest
+// of the heads' scores); each takes the slots of a resident page no head selects, the least
+// important first; one op per KV head and pair.
+extern "C" int scout_plan_recall_pages(const float* scores, const int32_t* topk_idx, const int32_t* topk_count,
+                                       const uint32_t* resident_bits, const int32_t* page_table, int B, int Hkv,
+                                       int nblk_cap, int k, scout_recall_op* ops, int max_ops, int* n_ops) {
+  if (scores == nullptr || topk_idx == nullptr || topk_count == nullptr || resident_bits == nullptr ||
+      page_table == nullptr || n_ops == nullptr || B <= 0 || Hkv <= 0 || nblk_cap <= 0 || k <= 0 || max_ops < 0 ||
+      (ops == nullptr && max_ops > 0))
+    return SCOUT_ERR_INVALID_ARG;
+  const int words = (nblk_cap + 31) / 32;
+  std::vector<char> sel(nblk_cap);
+  std::vector<float> imp(nblk_cap);
+  std::vector<int> in, ev;
+  std::vector<std::pair<int, int>> pairs;
+  int n = 0;
+  for (int b = 0; b < B; ++b) {
+    const int u0 = b * Hkv;
+    const uint32_t* bits = resident_bits + (int64_t)u0 * words;
+    for (int h = 1; h < Hkv; ++h)  // one residency per page: every head's bits are the same
+      if (!std::equal(bits, bits + words, resident_bits + (int64_t)(u0 + h) * words)) return SCOUT_ERR_INVALID_ARG;
+    auto resident = [&](int j) { return ((bits[j >> 5] >> (j & 31)) & 1u) != 0; };
+    std::fill(sel.begin(), sel.end(), 0);
+    for (int j = 0; j < nblk_cap; ++j) {
+      float m = scores[(int64_t)u0 * nblk_cap + j];
+      for (int h = 1; h < Hkv; ++h) m = std::max(m, scores[(int64_t)(u0 + h) * nblk_cap + j]);
+      imp[j] = m;
+    }
+    for (int h = 0; h < Hkv; ++h) {
+      const int u = u0 + h;
+      const int cnt = std::min(std::max(topk_count[u], 0), k);
+      for (int i = 0; i < cnt; ++i) {
+        const int j = topk_idx[(int64_t)u * k + i];
+        if (j < 0 || j >= nblk_cap) return SCOUT_ERR_INVALID_ARG;
+        sel[j] = 1;
+      }
+    }
+    in.clear();
+    ev.clear();
+    for (int j = 0; j < nblk_cap; ++j) {
+      if (sel[j] && !resident(j)) in.push_back(j);
+      if (!sel[j] && resident(j)) ev.push_back(j);
+    }
+    std::stable_sort(in.begin(), in.end(), [&](int x, int y) { return imp[x] > imp[y]; });
+    std::stable_sort(ev.begin(), ev.end(), [&](int x, int y) { return imp[x] < imp[y]; });
+    pairs.clear();
+    for (size_t i = 0; i < std::min(in.size(), ev.size()); ++i) pairs.emplace_back(in[i], ev[i]);
+    std::sort(pairs.begin(), pairs.end());  // ascending incoming block
+    for (int h = 0; h < Hkv; ++h) {
+      const int u = u0 + h;
+      for (const auto& pr : pairs) {
+        const int32_t slot = page_table[(int64_t)u * nblk_cap + pr.second];
+        if (slot < 0) return SCOUT_ERR_INVALID_ARG;  // a resident page owns a slot in every head
+        if (n >= max_ops) return SCOUT_ERR_WORKSPACE;
+        ops[n++] = scout_recall_op{u, pr.first, slot, pr.second};
+      }
+    }
   }
   *n_ops = n;
   return SCOUT_OK;

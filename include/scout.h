@@ -11,9 +11,9 @@
  *   the work is enqueued.  Arguments are checked on the host before any launch;
  *   a rejected call launches nothing.  A launch failure reported by the CUDA
  *   runtime returns SCOUT_ERR_CUDA.
- * - The host-side entry points (scout_plan_recall, scout_recall_intervals,
- *   scout_cpu_attend) are the exception: host pointers only, synchronous, no GPU
- *   involved.  scout_cpu_attend also runs on worker threads it starts and joins
+ * - The host-side entry points (scout_plan_recall, scout_plan_recall_pages,
+ *   scout_recall_intervals, scout_cpu_attend) are the exception: host pointers
+ *   only, synchronous, no GPU involved.  scout_cpu_attend also runs on worker threads it starts and joins
  *   within the call.
  * - bf16 tensors are IEEE bfloat16 (2 bytes); fp32 are IEEE binary32.
  * - Shapes: B sequences, Hq query heads, Hkv KV heads (G = Hq / Hkv query heads
@@ -315,6 +315,27 @@ int scout_commit_residency(const scout_recall_op* d_ops, int n_ops, int32_t* pag
 int scout_plan_recall(const float* scores, const int32_t* topk_idx, const int32_t* topk_count,
                       const uint32_t* resident_bits, const int32_t* page_table, int units, int nblk_cap, int k,
                       scout_recall_op* ops, int max_ops, int* n_ops);
+
+/* ------------------------------------------------------------------------ *
+ * Recall plan with residency per page (host code): a page is one block of one
+ * sequence for all its KV heads (32 tokens x 8 heads x K and V = 128 KB in the
+ * Qwen3 layout), the transfer unit whose PCIe rate the pages compare with
+ * per-token transfers (arXiv HTML, the background on recall-based offloading,
+ * Figure 3).  Selection stays per (sequence,
+ * KV head) and the residency bits of a sequence's heads are identical.
+ * Reading (section 3.4 leaves it open): per sequence, the pages some head selects
+ * that are not resident come in, the most important first (importance = the
+ * largest of its heads' scores; ties to the lower block); each takes the slots of
+ * a resident page that no head selects, the least important first; the plan
+ * stops when either side runs out.  Each pair becomes one op per KV head, (unit,
+ * incoming block, that unit's slot of the evicted block, evicted block), grouped
+ * by unit and, within a unit, in ascending incoming block order.
+ * Arguments as for scout_plan_recall with units = B * Hkv.  Errors: as for
+ * scout_plan_recall, plus SCOUT_ERR_INVALID_ARG when the residency bits of one
+ * sequence's heads differ or an evicted page lacks a slot in some head. */
+int scout_plan_recall_pages(const float* scores, const int32_t* topk_idx, const int32_t* topk_count,
+                            const uint32_t* resident_bits, const int32_t* page_table, int B, int Hkv, int nblk_cap,
+                            int k, scout_recall_op* ops, int max_ops, int* n_ops);
 
 /* ------------------------------------------------------------------------ *
  * Per-layer recall intervals from an offline profile (host code).

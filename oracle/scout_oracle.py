@@ -207,6 +207,27 @@ def apply_recall(slot_of, resident_mask, ops):
     return slot_of, resident_mask
 
 
+def recall_plan_pages(U_heads, selected_heads, resident_mask, slot_of_heads):
+    """One sequence's recall with residency per page, a page being one block for all KV heads
+    (the 128 KB transfer unit of the pages' PCIe comparison; section 3.4 for the recall).
+    Reading, which the pages leave open: the pages some head selects that are not resident come
+    in, the most important first, importance being the largest of the heads' scores (ties to the
+    lower block); each replaces a resident page that no head selects, the least important first;
+    the plan stops when either side runs out.  U_heads [Hkv][nblk] pooled scores,
+    selected_heads: each head's selected blocks, resident_mask [nblk] (the sequence's pages),
+    slot_of_heads [Hkv][nblk].  Returns, per head, [(block in, its slot, block out)] in
+    ascending block-in order."""
+    Hkv, nblk = len(U_heads), len(resident_mask)
+    importance = [max(float(U_heads[h][j]) for h in range(Hkv)) for j in range(nblk)]
+    chosen = set()
+    for blocks in selected_heads:
+        chosen.update(int(j) for j in blocks)
+    need = sorted((j for j in chosen if not resident_mask[j]), key=lambda j: (-importance[j], j))
+    free = sorted((j for j in range(nblk) if resident_mask[j] and j not in chosen), key=lambda j: (importance[j], j))
+    pairs = sorted(zip(need, free))
+    return [[(j_in, int(slot_of_heads[h][j_out]), j_out) for j_in, j_out in pairs] for h in range(Hkv)]
+
+
 def recall_intervals(traces, beta=0.12):
     """Per-layer recall intervals from an offline profile (section 3.4: for each layer, the
     largest number of steps that keeps the measured CPU compute ratio below the threshold beta,
