@@ -38,6 +38,11 @@ Readings where the pages are silent (listed again in the design notes):
 * LSE is the natural log of sum exp(scale * q.k); partial outputs are normalised;
   an empty set gives O = 0, LSE = -inf.
 * Tokens t >= seq_len are never attended and never enter a digest.
+* Recall interval: every profiled step of the interval is strictly below beta;
+  the interval is at least one step and at most the profiled length.
+* Residency per page (one block of a sequence for all KV heads): a page is needed
+  when any head selects it and ranked by the largest of its heads' scores (parity
+  unpinned: the pages do not say how per-head selections map to shared pages).
 """
 from __future__ import annotations
 
