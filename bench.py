@@ -142,7 +142,7 @@ def max_over_ranks(x: float, device) -> float:
 # ---------------------------------------------------------------------------
 # libscout arm
 # ---------------------------------------------------------------------------
-from block_sparse_kv_pred_gb300.step import EARLY, KERNELS, SPLIT, algorithmic_bytes, setup_step  # noqa: E402
+from block_sparse_kv_pred_gb300.step import EARLY, KERNELS, SPLIT, STREAM_OF, algorithmic_bytes, setup_step  # noqa: E402
 
 
 def run_scout(args, rank, world, local):
@@ -224,6 +224,68 @@ def run_scout(args, rank, world, local):
     return s, wl, t, dict(ms=ms, value=value, kern_ms=kern_ms, clocks=clocks, wall=wall, e2e=e2e,
                           launches=step.launches_per_step * args.steps, split=None if args.serial else split,
                           early=() if args.serial else early, step=step)
+
+
+def isolated(t, step, nbytes, peak, reps=20):
+    """Each kernel on its own: full grids (one CTA per SM), the L2 flushed before every launch by
+    reading a 256 MB buffer (a read leaves no dirty lines whose write-back would fall inside the
+    next launch).  Device time only: a CUDA graph of ``reps`` (flush, launch) pairs is timed
+    against a graph of the flushes alone, so no host enqueue gap is counted.  The selection and
+    the attention together are the pair the roofline target names; their serialised durations
+    sum to the pair's time."""
+    import torch
+
+    dev = t["Qp0"].device
+    flush = torch.ones(64 << 20, dtype=torch.float32, device=dev)
+    saved = {}
+    for key in ("gemm", "score", "attn"):
+        for par in (0, 1):
+            lp = t.get(f"_launch_{key}{par}")
+            if lp:
+                saved[(key, par)] = lp.contents.max_ctas
+                lp.contents.max_ctas = 0
+
+    def graph_ms(stream, call):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for _ in range(reps):
+                flush.sum()
+                if call is not None:
+                    call()
+        best = None
+        for _ in range(4):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            g.replay()
+            b.record(stream)
+            b.synchronize()
+            ms = a.elapsed_time(b)
+            best = ms if best is None else min(best, ms)
+        return best
+
+    try:
+        out = {}
+        calls = step.calls[0]
+        for name in KERNELS:
+            stream = step.streams[0 if step.serial else STREAM_OF[name]]
+            torch.cuda.synchronize()
+            m = (graph_ms(stream, calls[name]) - graph_ms(stream, None)) / reps
+            gbs = nbytes[name] / (m / 1e3) / 1e9
+            out[name] = {"us": m * 1e3, "GB_s": gbs, "frac_of_hbm_peak": gbs / peak}
+        pair_us = out["score_topk"]["us"] + out["sparse_attn_merge"]["us"]
+        pair_b = nbytes["score_topk"] + nbytes["sparse_attn_merge"]
+        out["score_topk+sparse_attn_merge"] = {"us": pair_us, "bytes": pair_b,
+                                               "GB_s": pair_b / (pair_us / 1e6) / 1e9,
+                                               "frac_of_hbm_peak": pair_b / (pair_us / 1e6) / 1e9 / peak}
+        out["note"] = (f"one kernel at a time, one CTA per SM, L2 flushed before each launch; graph of {reps} "
+                       f"(flush, launch) pairs minus a graph of the flushes, best of 4")
+        torch.cuda.synchronize()
+        if int(t["status"].item()) != 0:
+            return {"unavailable": f"device status {int(t['status'].item())}"}
+        return out
+    finally:
+        for (key, par), v in saved.items():
+            t[f"_launch_{key}{par}"].contents.max_ctas = v
 
 
 def run_e2e(args, t, step, s, world, device):
@@ -313,10 +375,12 @@ def cpu_side(s, t, seconds=0.5, max_seqs=8):
 
     try:
         Bs = min(s.B, max_seqs)
-        slots = t["page_table"][:Bs].reshape(-1).long()
+        # the whole cache (the step's compact pool holds only the GPU's share of it)
+        slots = t.get("page_table_all", t["page_table"])[:Bs].reshape(-1).long()
         if int(slots.min()) < 0:
             return {"unavailable": "a block of the sample has no pool slot"}
-        kv = {n: t[n + "_pool"].index_select(0, slots).view(Bs, s.Hkv, s.nblk, s.P, s.D).cpu() for n in "KV"}
+        kv = {n: t.get(n + "_all", t[n + "_pool"]).index_select(0, slots).view(Bs, s.Hkv, s.nblk, s.P, s.D).cpu()
+              for n in "KV"}
         q = t["Qp1"][:Bs].reshape(Bs, s.Hq, s.D).cpu()
         lst, cnt, seq = (t[n][:Bs].cpu().contiguous() for n in ("cpu1", "cpu_count1", "seq_len"))
         listed = np.arange(s.k)[None, None, :] < cnt.numpy()[:, :, None]
@@ -367,11 +431,12 @@ def layer_ahead(s, t, step, gpu_ms, steps=24, warm=4, limit_s=60.0):
     dev = t["Qp0"].device
     try:
         t_end = time.perf_counter() + limit_s
-        slots = t["page_table"].reshape(-1).long()
+        slots = t.get("page_table_all", t["page_table"]).reshape(-1).long()
         if int(slots.min()) < 0:
             return {"unavailable": "a block has no pool slot"}
         # the layer's K/V in logical block order on the host: the copy the CPU side attends
-        hkv = {n: t[n + "_pool"].index_select(0, slots).view(s.B, s.Hkv, s.nblk, s.P, s.D).cpu() for n in "KV"}
+        hkv = {n: t.get(n + "_all", t[n + "_pool"]).index_select(0, slots).view(s.B, s.Hkv, s.nblk, s.P, s.D).cpu()
+               for n in "KV"}
         seq = t["seq_len"].cpu().contiguous()
         threads = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else (os.cpu_count() or 1)
         st = step.fresh()
@@ -559,8 +624,12 @@ def streams_of(split):
             f"attention ({n(att)}) after the previous selection || digest append")
 
 
-def config_of(s, world, split=None, early=()):
-    return {"workload": s.name, "batch": s.B, "q_heads": s.Hq, "kv_heads": s.Hkv, "head_dim": s.D,
+def config_of(s, world, split=None, early=(), n_slots=None):
+    pool = None
+    if n_slots is not None:
+        pool = (f"{n_slots} slots of {s.P}-token K and V pages ({2 * n_slots * s.P * s.D * 2 / 1e9:.2f} GB): the "
+                f"resident blocks and each unit's tail block, in a seeded slot order")
+    return {"workload": s.name, "kv_pool": pool, "batch": s.B, "q_heads": s.Hq, "kv_heads": s.Hkv, "head_dim": s.D,
             "context": s.T, "page": s.P, "budget_tokens": s.k * s.P, "resident_frac": s.resident_frac,
             "digest": s.kind, "gemm_mnk": [s.B, s.Hq * s.D, s.hidden],
             "l2": "not flushed: one step reads inputs larger than L2 (see step_input_bytes), in an order "
@@ -642,7 +711,7 @@ def main():
     line = {
         "metric": METRIC, "value": r["value"], "unit": "query-heads/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": r["ms"], "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "bf16", "data": DATA, "config": config_of(s, world, r["split"], r["early"]),
+        "vs_baseline": None, "dtype": "bf16", "data": DATA, "config": config_of(s, world, r["split"], r["early"], t["n_slots"]),
         "roofline": roof,
         "step_roofline": {"bound": "hbm", "achieved": step_gbs, "peak": peak, "unit": "GB/s",
                           "frac": step_gbs / peak, "algorithmic_bytes_per_step": step_bytes,
@@ -652,6 +721,7 @@ def main():
         "gpu_launches": r["launches"], "clocks": r["clocks"], "kernels": kernels,
         "kv_tokens_per_s": nbytes["_res_blocks"] * s.P / (r["kern_ms"]["sparse_attn_merge"] / 1e3),
         "attention_path": attention_path(s, nbytes, r["kern_ms"], peak),
+        "kernels_isolated": isolated(t, r["step"], nbytes, peak),
         "wall_s_timed": r["wall"],
     }
     if world == 1 and not args.no_cpu_side:

@@ -16,6 +16,7 @@ __all__ = [
     "ScoutError", "lib", "MINMAX", "MEAN", "predict_q", "build_digest", "score_topk", "score_topk_workspace",
     "sparse_attn", "sparse_attn_merge", "sparse_attn_workspace", "merge", "recall_async", "commit_residency",
     "plan_recall", "plan_recall_pages", "recall_intervals", "cpu_attend", "RecallOp", "Launch", "Prepared",
+    "INJECT_NONE", "INJECT_ABANDON", "INJECT_COPY_FAIL", "recall_gather_async", "CpuPool",
 ]
 
 MINMAX = 0
@@ -48,21 +49,27 @@ _SIGS = {
     "scout_build_digest": ([_i, _p, _i64, _p, _p, _i, _i, _i, _i, _i, _p, _i, _p, _p, _p], _i),
     "scout_score_topk_workspace_bytes": ([_i, _i, _i], _sz),
     "scout_score_topk": ([_i, _p, _p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _i, _p, _p, _p, _p, _p, _p, _p, _p,
-                          _p, _p, _sz, _p, _p], _i),
+                          _p, _p, _sz, _p, _p, _p], _i),
     "scout_score_topk_noalloc_max_bytes": ([], _sz),
     "scout_score_topk_noalloc": ([_i, _p, _p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _i, _p, _p, _p, _p, _p, _p, _p,
-                                  _p, _p, _p], _i),
+                                  _p, _p, _p, _p], _i),
     "scout_sparse_attn_workspace_bytes": ([_i, _i, _i, _i, _i], _sz),
     "scout_sparse_attn": ([_p, _p, _p, _i64, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _i, _f, _p, _p, _p, _sz, _p,
                            _p, _p], _i),
     "scout_sparse_attn_merge": ([_p, _p, _p, _i64, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _i, _f, _p, _p, _p, _p,
                                  _p, _sz, _p, _p, _p], _i),
     "scout_merge": ([_p, _p, _p, _p, _i, _i, _p, _p, _p], _i),
-    "scout_recall_async": ([_p, _i, _p, _p, _p, _p, _i64, _i, _i, _i, _i, _i, _p, _p, _p], _i),
+    "scout_recall_async": ([_p, _i, _p, _p, _p, _p, _i64, _i, _i, _i, _i, _i, _p, _p, _p, _p], _i),
+    "scout_recall_gather_async": ([_p, _i, _p, _p, _p, _p, _i64, _i, _i, _i, _i, _i, _p, _p, _p, _p, _p], _i),
     "scout_commit_residency": ([_p, _i, _p, _p, _i64, _i, _i, _i, _p, _p], _i),
     "scout_plan_recall": ([_p, _p, _p, _p, _p, _i, _i, _i, _p, _i, _p], _i),
     "scout_cpu_attend": ([_p, _p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _i, _f, _p, _p, _i], _i),
     "scout_recall_intervals": ([_p, _i, _i, _f, _p], _i),
+    "scout_cpu_pool_create": ([_i], _p),
+    "scout_cpu_pool_threads": ([_p], _i),
+    "scout_cpu_pool_destroy": ([_p], None),
+    "scout_cpu_attend_async": ([_p, _p, _p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _i, _f, _p, _p], _i),
+    "scout_cpu_pool_wait": ([_p, _i64], _i),
     "scout_plan_recall_pages": ([_p, _p, _p, _p, _p, _i, _i, _i, _i, _p, _i, _p], _i),
 }
 
@@ -71,14 +78,21 @@ class Launch(ctypes.Structure):
     """scout_launch: launch options of the persistent kernels.  max_ctas 0 = one CTA per SM;
     pdl 1 = start early after the previous kernel on the stream; early_event = a
     cudaEvent_t (timing disabled) this launch records programmatically, so that one of the
-    three persistent kernels on a stream waiting for it may start early."""
-    _fields_ = [("max_ctas", ctypes.c_int), ("pdl", ctypes.c_int), ("early_event", ctypes.c_void_p)]
+    three persistent kernels on a stream waiting for it may start early; inject = a
+    SCOUT_INJECT_* fault for tests (0 in normal use)."""
+    _fields_ = [("max_ctas", ctypes.c_int), ("pdl", ctypes.c_int), ("early_event", ctypes.c_void_p),
+                ("inject", ctypes.c_int)]
 
 
-def _launch(max_ctas, pdl=False, early_event=None):
+INJECT_NONE = 0
+INJECT_ABANDON = 1
+INJECT_COPY_FAIL = 2
+
+
+def _launch(max_ctas, pdl=False, early_event=None, inject=INJECT_NONE):
     """Launch options, or None for the defaults.  ``early_event``: a torch.cuda.Event created
     without timing and already recorded once (so that it exists), or a raw handle."""
-    if max_ctas is None and not pdl and early_event is None:
+    if max_ctas is None and not pdl and early_event is None and not inject:
         return None
     if max_ctas is not None and max_ctas < 0:
         raise ScoutError("max_ctas must be >= 0")
@@ -86,7 +100,7 @@ def _launch(max_ctas, pdl=False, early_event=None):
         if not early_event.cuda_event:
             raise ScoutError("early_event has not been created yet: record it once first")
         early_event = early_event.cuda_event
-    return ctypes.pointer(Launch(int(max_ctas or 0), int(bool(pdl)), early_event))
+    return ctypes.pointer(Launch(int(max_ctas or 0), int(bool(pdl)), early_event, int(inject)))
 
 
 def lib_path() -> str:
@@ -168,11 +182,13 @@ def score_topk_workspace(B, Hkv, nblk_cap, device="cuda") -> torch.Tensor:
 
 
 def score_topk(kind, q, digest, seq_len, resident_bits, B, Hq, Hkv, P, nblk_cap, k, workspace, out=None,
-               prev_cpu=None, scores=None, max_ctas=None, stream=None) -> dict:
+               prev_cpu=None, scores=None, status=None, max_ctas=None, inject=INJECT_NONE, stream=None) -> dict:
     """Score digests, select top-k per unit, split by residency.
 
     ``out`` (optional) is a dict of preallocated outputs with the keys returned.
     ``prev_cpu`` is an optional (list, count) pair from the previous step.
+    ``status`` (optional int32 device tensor) receives SCOUT_DEV_TIMEOUT (2) if a bounded wait
+    expired.  ``inject`` is a test hook (INJECT_ABANDON).
     """
     kind = _KIND[kind]
     dev = q.device
@@ -193,8 +209,8 @@ def score_topk(kind, q, digest, seq_len, resident_bits, B, Hq, Hkv, P, nblk_cap,
         _dev(out["res"], torch.int32, "res"), _dev(out["res_count"], torch.int32, "res_count"),
         _dev(out["cpu"], torch.int32, "cpu"), _dev(out["cpu_count"], torch.int32, "cpu_count"),
         _dev(out["delta"], torch.int32, "delta"), _dev(out["delta_count"], torch.int32, "delta_count"),
-        _dev(workspace, torch.uint8, "workspace"), workspace.numel(), _launch(max_ctas), _stream(stream)),
-        "scout_score_topk")
+        _dev(workspace, torch.uint8, "workspace"), workspace.numel(), _opt(status, torch.int32, "status"),
+        _launch(max_ctas, inject=inject), _stream(stream)), "scout_score_topk")
     if scores is not None:
         out["scores"] = scores
     del U
@@ -260,17 +276,34 @@ def merge(O_a, lse_a, O_b, lse_b, O_out=None, lse_out=None, stream=None):
 
 
 def recall_async(ops, host_K, host_V, K_pool, V_pool, B, Hkv, P, nblk_cap, side_stream, wait_event=None,
-                 done_event=None):
-    """Queue host->pool copies of recalled blocks on side_stream. ``ops``: list of (unit, block, slot, evict)."""
+                 done_event=None, inject=INJECT_NONE):
+    """Queue host->pool copies of recalled blocks on side_stream (one cudaMemcpyAsync per run of
+    consecutive blocks and slots). ``ops``: list of (unit, block, slot, evict)."""
     arr = (RecallOp * max(1, len(ops)))(*[RecallOp(*o) for o in ops])
     for t, n in ((host_K, "host_K"), (host_V, "host_V")):
         if t.is_cuda or not t.is_contiguous() or t.dtype != torch.bfloat16:
             raise ScoutError(f"{n} must be a contiguous bf16 host tensor")
     _check(lib().scout_recall_async(arr, len(ops), host_K.data_ptr(), host_V.data_ptr(),
                                     _dev(K_pool, torch.bfloat16, "K_pool"), _dev(V_pool, torch.bfloat16, "V_pool"),
-                                    K_pool.shape[0], B, Hkv, K_pool.shape[-1], P, nblk_cap,
+                                    K_pool.shape[0], B, Hkv, K_pool.shape[-1], P, nblk_cap, _launch(None, inject=inject),
                                     None if wait_event is None else wait_event.cuda_event, side_stream.cuda_stream,
                                     None if done_event is None else done_event.cuda_event), "scout_recall_async")
+
+
+def recall_gather_async(d_ops, host_K, host_V, K_pool, V_pool, B, Hkv, P, nblk_cap, side_stream, wait_event=None,
+                        done_event=None, status=None, inject=INJECT_NONE):
+    """Move the recalled blocks with one gather kernel on side_stream that reads them straight from
+    pinned, mapped host memory.  ``d_ops``: device int32 [n][4] (unit, block, slot, evict)."""
+    for t, n in ((host_K, "host_K"), (host_V, "host_V")):
+        if t.is_cuda or not t.is_contiguous() or t.dtype != torch.bfloat16 or not t.is_pinned():
+            raise ScoutError(f"{n} must be a contiguous, pinned bf16 host tensor")
+    n = 0 if d_ops is None else d_ops.shape[0]
+    _check(lib().scout_recall_gather_async(
+        _opt(d_ops, torch.int32, "ops"), n, host_K.data_ptr(), host_V.data_ptr(), _dev(K_pool, torch.bfloat16, "K_pool"),
+        _dev(V_pool, torch.bfloat16, "V_pool"), K_pool.shape[0], B, Hkv, K_pool.shape[-1], P, nblk_cap,
+        _opt(status, torch.int32, "status"), _launch(None, inject=inject),
+        None if wait_event is None else wait_event.cuda_event, side_stream.cuda_stream,
+        None if done_event is None else done_event.cuda_event), "scout_recall_gather_async")
 
 
 def commit_residency(d_ops, page_table, resident_bits, n_slots, B, Hkv, wait_event=None, stream=None):
@@ -280,6 +313,21 @@ def commit_residency(d_ops, page_table, resident_bits, n_slots, B, Hkv, wait_eve
                                         _dev(resident_bits, torch.int32, "resident_bits"), n_slots, B, Hkv,
                                         page_table.shape[-1], None if wait_event is None else wait_event.cuda_event,
                                         _stream(stream)), "scout_commit_residency")
+
+
+def _check_plan_shapes(sc, ti, tc, rb, pt, units, nblk, k):
+    """The host planners read these arrays by (units, nblk_cap, k): refuse any other shape."""
+    words = -(-nblk // 32)
+    if sc.size != units * nblk or sc.shape[0] != units:
+        raise ScoutError(f"scores must be [{units}][{nblk}], got {sc.shape}")
+    if ti.size != units * k or ti.shape[-1] != k:
+        raise ScoutError(f"topk_idx must be [{units}][{k}], got {ti.shape}")
+    if tc.size != units:
+        raise ScoutError(f"topk_count must hold {units} counts, got {tc.shape}")
+    if rb.size != units * words or rb.shape[-1] != words:
+        raise ScoutError(f"resident_bits must be [{units}][{words}], got {rb.shape}")
+    if pt.size != units * nblk or pt.shape[-1] != nblk:
+        raise ScoutError(f"page_table must be [{units}][{nblk}], got {pt.shape}")
 
 
 def plan_recall(scores, topk_idx, topk_count, resident_bits, page_table, k):
@@ -297,6 +345,7 @@ def plan_recall(scores, topk_idx, topk_count, resident_bits, page_table, k):
     rb = np.ascontiguousarray(resident_bits, dtype=np.uint32)
     pt = np.ascontiguousarray(page_table, dtype=np.int32)
     units, nblk = sc.shape
+    _check_plan_shapes(sc, ti, tc, rb, pt, units, nblk, k)
     cap = max(1, int(tc.clip(0, k).sum()))
     ops = (RecallOp * cap)()
     n = ctypes.c_int(0)
@@ -320,6 +369,7 @@ def plan_recall_pages(scores, topk_idx, topk_count, resident_bits, page_table, B
     rb = np.ascontiguousarray(resident_bits, dtype=np.uint32)
     pt = np.ascontiguousarray(page_table, dtype=np.int32)
     nblk = sc.shape[-1]
+    _check_plan_shapes(sc.reshape(-1, nblk), ti, tc, rb, pt, B * Hkv, nblk, k)
     cap = max(1, int(tc.clip(0, k).sum()) * Hkv)
     ops = (RecallOp * cap)()
     n = ctypes.c_int(0)
@@ -380,6 +430,62 @@ def cpu_attend(q, K, V, seq_len, cpu_list, cpu_count, B, Hq, Hkv, P, k, scale, O
                                   B, Hq, Hkv, D, P, nblk_cap, k, float(scale), _host(O_cpu, torch.float32, "O_cpu"),
                                   _host(lse_cpu, torch.float32, "lse_cpu"), int(n_threads)), "scout_cpu_attend")
     return O_cpu, lse_cpu
+
+
+class CpuPool:
+    """A caller-owned pool of CPU worker threads (scout_cpu_pool): ``submit`` starts the CPU-side
+    attention of one layer and returns at once; ``wait(timeout_s)`` returns True when it is done
+    and False when it is still running after the timeout (a late CPU partial).  ``close`` (or
+    leaving a ``with`` block) waits for a running job and joins the workers."""
+
+    def __init__(self, n_threads: int = 0):
+        self._p = lib().scout_cpu_pool_create(int(n_threads))
+        if not self._p:
+            raise ScoutError("scout_cpu_pool_create: no worker thread could be started")
+        self.threads = lib().scout_cpu_pool_threads(self._p)
+        self._keep = ()
+
+    def submit(self, q, K, V, seq_len, cpu_list, cpu_count, B, Hq, Hkv, P, k, scale, O_cpu, lse_cpu):
+        """Host tensors as for ``cpu_attend``; O_cpu / lse_cpu are written when the job is done."""
+        if not self._p:
+            raise ScoutError("the pool is closed")
+        D = q.shape[-1]
+        per_block = B * Hkv * P * D
+        if K.numel() != V.numel() or K.numel() % per_block:
+            raise ScoutError("K and V must hold [B][Hkv][nblk_cap][P][D] elements")
+        nblk_cap = K.numel() // per_block
+        args = (_host(q, torch.bfloat16, "q"), _host(K, torch.bfloat16, "K"), _host(V, torch.bfloat16, "V"),
+                _host(seq_len, torch.int32, "seq_len"), _host(cpu_list, torch.int32, "cpu_list"),
+                _host(cpu_count, torch.int32, "cpu_count"))
+        outs = (_host(O_cpu, torch.float32, "O_cpu"), _host(lse_cpu, torch.float32, "lse_cpu"))
+        _check(lib().scout_cpu_attend_async(self._p, *args, B, Hq, Hkv, D, P, nblk_cap, k, float(scale), *outs),
+               "scout_cpu_attend_async")
+        self._keep = (q, K, V, seq_len, cpu_list, cpu_count, O_cpu, lse_cpu)  # alive until the job is done
+
+    def wait(self, timeout_s: float) -> bool:
+        rc = lib().scout_cpu_pool_wait(self._p, max(0, int(timeout_s * 1e6)))
+        if rc == 5:
+            return False
+        _check(rc, "scout_cpu_pool_wait")
+        return True
+
+    def close(self):
+        if self._p:
+            lib().scout_cpu_pool_destroy(self._p)
+            self._p = None
+            self._keep = ()
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        self.close()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:  # noqa: BLE001  (interpreter shutdown)
+            pass
 
 
 class Prepared:

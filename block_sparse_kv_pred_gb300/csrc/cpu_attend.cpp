@@ -13,9 +13,12 @@
 // intrinsics, the compiler's vectoriser does the rest on x86-64 and AArch64.
 #include <algorithm>
 #include <atomic>
+#include <chrono>
 #include <cmath>
+#include <condition_variable>
 #include <cstdint>
 #include <cstring>
+#include <mutex>
 #include <thread>
 #include <vector>
 
@@ -137,12 +140,10 @@ void attend_unit(const Job& a, int u) {
   }
 }
 
-}  // namespace
-
-extern "C" int scout_cpu_attend(const void* q, const void* K, const void* V, const int32_t* seq_len,
-                                const int32_t* cpu_list, const int32_t* cpu_count, int B, int Hq, int Hkv, int D,
-                                int P, int nblk_cap, int k, float scale, float* O_cpu, float* lse_cpu,
-                                int n_threads) {
+// Every argument check of scout_cpu_attend; fills the job when they pass.
+int make_job(const void* q, const void* K, const void* V, const int32_t* seq_len, const int32_t* cpu_list,
+             const int32_t* cpu_count, int B, int Hq, int Hkv, int D, int P, int nblk_cap, int k, float scale,
+             float* O_cpu, float* lse_cpu, Job* job) {
   if (q == nullptr || K == nullptr || V == nullptr || seq_len == nullptr || cpu_list == nullptr ||
       cpu_count == nullptr || O_cpu == nullptr || lse_cpu == nullptr || B <= 0 || Hq <= 0 || Hkv <= 0 ||
       nblk_cap <= 0 || k <= 0 || Hq % Hkv != 0 || Hq / Hkv > kMaxGroup || !(scale > 0.f) || !std::isfinite(scale))
@@ -157,8 +158,22 @@ extern "C" int scout_cpu_attend(const void* q, const void* K, const void* V, con
       if (j < 0 || j >= nblk_cap) return SCOUT_ERR_INVALID_ARG;
     }
   }
-  const Job a{static_cast<const uint16_t*>(q), static_cast<const uint16_t*>(K), static_cast<const uint16_t*>(V),
-              seq_len, cpu_list, cpu_count, Hq, Hkv, Hq / Hkv, P, nblk_cap, k, scale, O_cpu, lse_cpu};
+  *job = Job{static_cast<const uint16_t*>(q), static_cast<const uint16_t*>(K), static_cast<const uint16_t*>(V),
+             seq_len, cpu_list, cpu_count, Hq, Hkv, Hq / Hkv, P, nblk_cap, k, scale, O_cpu, lse_cpu};
+  return SCOUT_OK;
+}
+
+}  // namespace
+
+extern "C" int scout_cpu_attend(const void* q, const void* K, const void* V, const int32_t* seq_len,
+                                const int32_t* cpu_list, const int32_t* cpu_count, int B, int Hq, int Hkv, int D,
+                                int P, int nblk_cap, int k, float scale, float* O_cpu, float* lse_cpu,
+                                int n_threads) {
+  Job a;
+  const int rc = make_job(q, K, V, seq_len, cpu_list, cpu_count, B, Hq, Hkv, D, P, nblk_cap, k, scale, O_cpu,
+                          lse_cpu, &a);
+  if (rc != SCOUT_OK) return rc;
+  const int units = B * Hkv;
   int nt = n_threads > 0 ? n_threads : static_cast<int>(std::max(1u, std::thread::hardware_concurrency()));
   nt = std::min(nt, units);
   std::atomic<int> next{0};
@@ -176,4 +191,102 @@ extern "C" int scout_cpu_attend(const void* q, const void* K, const void* V, con
   work();
   for (auto& th : pool) th.join();
   return SCOUT_OK;
+}
+
+// ---------------------------------------------------------------------------
+// A caller-owned pool of worker threads for the CPU side, so that a pipeline calling it every
+// layer does not start and join threads each time, and can wait for a layer's partial with a
+// bound (a late CPU partial is reported, not waited for without end).  One job at a time.
+// ---------------------------------------------------------------------------
+struct scout_cpu_pool {
+  std::vector<std::thread> threads;
+  std::mutex mu;
+  std::condition_variable cv_work, cv_done;
+  Job job{};
+  int units = 0;
+  std::atomic<int> next{0};
+  unsigned generation = 0;  // bumped by every submission
+  int active = 0;           // workers still on the current job
+  bool running = false, stop = false;
+
+  void worker() {
+    unsigned seen = 0;
+    for (;;) {
+      Job j;
+      int n;
+      {
+        std::unique_lock<std::mutex> lk(mu);
+        cv_work.wait(lk, [&] { return stop || generation != seen; });
+        if (stop) return;
+        seen = generation;
+        j = job;
+        n = units;
+      }
+      for (int u = next.fetch_add(1); u < n; u = next.fetch_add(1)) attend_unit(j, u);
+      std::lock_guard<std::mutex> lk(mu);
+      if (--active == 0) {
+        running = false;
+        cv_done.notify_all();
+      }
+    }
+  }
+};
+
+extern "C" scout_cpu_pool* scout_cpu_pool_create(int n_threads) {
+  const int nt = n_threads > 0 ? n_threads : static_cast<int>(std::max(1u, std::thread::hardware_concurrency()));
+  scout_cpu_pool* p = nullptr;
+  try {
+    p = new scout_cpu_pool;
+    for (int i = 0; i < nt; ++i) p->threads.emplace_back([p] { p->worker(); });
+  } catch (...) {
+    if (p != nullptr) scout_cpu_pool_destroy(p);
+    return nullptr;
+  }
+  return p;
+}
+
+extern "C" int scout_cpu_pool_threads(const scout_cpu_pool* pool) {
+  return pool == nullptr ? 0 : static_cast<int>(pool->threads.size());
+}
+
+extern "C" void scout_cpu_pool_destroy(scout_cpu_pool* pool) {
+  if (pool == nullptr) return;
+  {
+    std::unique_lock<std::mutex> lk(pool->mu);
+    pool->cv_done.wait(lk, [&] { return !pool->running; });  // a job in flight finishes first
+    pool->stop = true;
+  }
+  pool->cv_work.notify_all();
+  for (auto& th : pool->threads) th.join();
+  delete pool;
+}
+
+extern "C" int scout_cpu_attend_async(scout_cpu_pool* pool, const void* q, const void* K, const void* V,
+                                      const int32_t* seq_len, const int32_t* cpu_list, const int32_t* cpu_count,
+                                      int B, int Hq, int Hkv, int D, int P, int nblk_cap, int k, float scale,
+                                      float* O_cpu, float* lse_cpu) {
+  if (pool == nullptr || pool->threads.empty()) return SCOUT_ERR_INVALID_ARG;
+  Job a;
+  const int rc = make_job(q, K, V, seq_len, cpu_list, cpu_count, B, Hq, Hkv, D, P, nblk_cap, k, scale, O_cpu,
+                          lse_cpu, &a);
+  if (rc != SCOUT_OK) return rc;
+  {
+    std::lock_guard<std::mutex> lk(pool->mu);
+    if (pool->running) return SCOUT_ERR_INVALID_ARG;  // one job at a time: wait for the last one first
+    pool->job = a;
+    pool->units = B * Hkv;
+    pool->next.store(0);
+    pool->active = static_cast<int>(pool->threads.size());
+    pool->running = true;
+    ++pool->generation;
+  }
+  pool->cv_work.notify_all();
+  return SCOUT_OK;
+}
+
+extern "C" int scout_cpu_pool_wait(scout_cpu_pool* pool, int64_t timeout_us) {
+  if (pool == nullptr || timeout_us < 0) return SCOUT_ERR_INVALID_ARG;
+  std::unique_lock<std::mutex> lk(pool->mu);
+  const bool done = pool->cv_done.wait_for(lk, std::chrono::microseconds(timeout_us), [&] { return !pool->running; });
+  return done ? SCOUT_OK : SCOUT_ERR_TIMEOUT;
 }

@@ -165,6 +165,8 @@ struct TopkArgs {
   float* scores;  // the caller's buffer, written only when user_scores
   int32_t* counters;  // [0]: the unit ticket counter (zero between calls)
   int32_t* status;
+  uint32_t score_wait;  // poll limit of the scoring warps' waits for a stage to land
+  int inject;           // SCOUT_INJECT_* (tests)
   int32_t *topk_idx, *topk_count, *res_list, *res_count, *cpu_list, *cpu_count, *delta_list, *delta_count;
 };
 
@@ -484,8 +486,10 @@ __global__ void __launch_bounds__(kThreadsAll, 1) score_topk_kernel(const __grid
     // ---------------- producer warp ------------------------------------------
     // Units are dealt out one at a time from a ticket counter, so a CTA that starts late
     // (its SM was busy) or scores a short unit simply takes more of them.  Every CTA draws
-    // exactly one ticket past the last unit; the draw of the launch's very last ticket
-    // resets the counter for the next call.
+    // exactly one ticket past the last unit, and the draw of the launch's very last ticket
+    // resets the counter for the next call.  A CTA whose wait has expired stops issuing
+    // work but keeps drawing tickets until it draws one past the last unit, so that the
+    // counter is reset all the same and the next call on the workspace starts from zero.
     if (lane != 0) return;
     prefetch_tmap(&tmD);
     const int last_ticket = a.units + (int)gridDim.x - 1;
@@ -500,13 +504,13 @@ __global__ void __launch_bounds__(kThreadsAll, 1) score_topk_kernel(const __grid
     int64_t i = 0;  // stages issued
     bool q_ready = false, ok = true;
     int u = resolve(atomicAdd(a.counters, 1));
-    while (u >= 0 && ok) {
+    while (u >= 0) {
       // the next ticket is drawn now and read only once this unit's stages are issued, so the
       // atomic's round trip never holds the ring up
       const int t_next = atomicAdd(a.counters, 1);
       const int nv = nvalid_of(u / a.Hkv);
       const int b = u / a.Hkv, kvh = u - b * a.Hkv;
-      for (int ch = 0; ch < a.nchunk; ++ch, ++i) {
+      for (int ch = 0; ok && ch < a.nchunk; ++ch, ++i) {
         const int st = (int)(i % a.stages);
         if (!mbar_wait(&empty_bar[st], (uint32_t)((i / a.stages) & 1) ^ 1u)) {
           report(a.status, SCOUT_DEV_TIMEOUT);
@@ -538,6 +542,10 @@ __global__ void __launch_bounds__(kThreadsAll, 1) score_topk_kernel(const __grid
         } else {
           mbar_arrive(&full_bar[st]);
         }
+      }
+      if (ok && a.inject == SCOUT_INJECT_ABANDON) {  // as if the next wait had expired
+        report(a.status, SCOUT_DEV_TIMEOUT);
+        ok = false;
       }
       u = resolve(t_next);
     }
@@ -594,7 +602,7 @@ __global__ void __launch_bounds__(kThreadsAll, 1) score_topk_kernel(const __grid
   uint32_t bmm[16][2], bme[8][2];
   for (int64_t i = 0;; ++i) {
     const int st = (int)(i % a.stages);
-    const bool landed = mbar_wait(&full_bar[st], (uint32_t)((i / a.stages) & 1));
+    const bool landed = mbar_wait_n(&full_bar[st], (uint32_t)((i / a.stages) & 1), a.score_wait);
     if (!landed && lane == 0) report(a.status, SCOUT_DEV_TIMEOUT);
     const int u = landed ? stage_unit[st] : -1;
     if (u < 0) break;
@@ -675,20 +683,24 @@ extern "C" size_t scout_score_topk_workspace_bytes(int B, int Hkv, int nblk_cap)
   return scout::counters_bytes(units);  // the unit ticket counter (room for one word per unit)
 }
 
-extern "C" int scout_score_topk(int kind, const void* q, const void* digest, const int32_t* seq_len,
-                                const uint32_t* resident_bits, const int32_t* prev_cpu_list,
-                                const int32_t* prev_cpu_count, int B, int Hq, int Hkv, int D, int P, int nblk_cap,
-                                int k, float* scores, int32_t* topk_idx, int32_t* topk_count, int32_t* res_list,
-                                int32_t* res_count, int32_t* cpu_list, int32_t* cpu_count, int32_t* delta_list,
-                                int32_t* delta_count, void* workspace, size_t workspace_bytes,
-                                const scout_launch* launch, cudaStream_t stream) {
-  using namespace scout;
+namespace scout {
+namespace {
+
+// Every host-side check of scout_score_topk except the workspace's: SCOUT_OK or the error.
+int check_topk_args(int kind, const void* q, const void* digest, const int32_t* seq_len,
+                    const uint32_t* resident_bits, const int32_t* prev_cpu_list, const int32_t* prev_cpu_count,
+                    int B, int Hq, int Hkv, int D, int P, int nblk_cap, int k, const int32_t* topk_idx,
+                    const int32_t* topk_count, const int32_t* res_list, const int32_t* res_count,
+                    const int32_t* cpu_list, const int32_t* cpu_count, const int32_t* delta_list,
+                    const int32_t* delta_count, const scout_launch* launch) {
   if (q == nullptr || digest == nullptr || seq_len == nullptr || resident_bits == nullptr || topk_idx == nullptr ||
       topk_count == nullptr || res_list == nullptr || res_count == nullptr || cpu_list == nullptr ||
       cpu_count == nullptr || delta_list == nullptr || delta_count == nullptr)
     return SCOUT_ERR_INVALID_ARG;
   if ((prev_cpu_list == nullptr) != (prev_cpu_count == nullptr)) return SCOUT_ERR_INVALID_ARG;
-  if (launch != nullptr && launch->max_ctas < 0) return SCOUT_ERR_INVALID_ARG;
+  if (launch != nullptr && (launch->max_ctas < 0 || launch->inject < SCOUT_INJECT_NONE ||
+                            launch->inject > SCOUT_INJECT_ABANDON))
+    return SCOUT_ERR_INVALID_ARG;
   if (kind != SCOUT_DIGEST_MINMAX && kind != SCOUT_DIGEST_MEAN) return SCOUT_ERR_INVALID_ARG;
   if (B <= 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || nblk_cap <= 0 || k <= 0) return SCOUT_ERR_INVALID_ARG;
   const int G = Hq / Hkv;
@@ -696,8 +708,35 @@ extern "C" int scout_score_topk(int kind, const void* q, const void* digest, con
   if (D != kD || !valid_P(P) || G > kMaxG || nblk_cap > kMaxNblk || units * nblk_cap > 0x7fffffffLL ||
       !aligned16(digest) || !aligned16(q))
     return SCOUT_ERR_UNSUPPORTED;
+  return SCOUT_OK;
+}
+
+// Poll limit of the scoring warps' stage waits under SCOUT_INJECT_ABANDON: long enough for
+// any copy that was issued to land, short enough that the test's expired wait ends quickly.
+constexpr uint32_t kInjectWaitLimit = 1u << 15;
+
+}  // namespace
+}  // namespace scout
+
+namespace scout {
+namespace {
+// scout_score_topk; with zero_counter set, the workspace's counter bytes are zeroed on the
+// stream after every host-side check has passed, just before the launch.
+int score_topk_entry(int kind, const void* q, const void* digest, const int32_t* seq_len,
+                     const uint32_t* resident_bits, const int32_t* prev_cpu_list, const int32_t* prev_cpu_count, int B,
+                     int Hq, int Hkv, int D, int P, int nblk_cap, int k, float* scores, int32_t* topk_idx,
+                     int32_t* topk_count, int32_t* res_list, int32_t* res_count, int32_t* cpu_list,
+                     int32_t* cpu_count, int32_t* delta_list, int32_t* delta_count, void* workspace,
+                     size_t workspace_bytes, int32_t* dev_status, const scout_launch* launch, cudaStream_t stream,
+                     bool zero_counter) {
+  const int rc = check_topk_args(kind, q, digest, seq_len, resident_bits, prev_cpu_list, prev_cpu_count, B, Hq, Hkv,
+                                 D, P, nblk_cap, k, topk_idx, topk_count, res_list, res_count, cpu_list, cpu_count,
+                                 delta_list, delta_count, launch);
+  if (rc != SCOUT_OK) return rc;
   if (workspace == nullptr || workspace_bytes < scout_score_topk_workspace_bytes(B, Hkv, nblk_cap))
     return SCOUT_ERR_WORKSPACE;
+  const int G = Hq / Hkv;
+  const int64_t units = (int64_t)B * Hkv;
   TopkArgs a;
   a.q = static_cast<const __nv_bfloat16*>(q);
   a.digest = static_cast<const uint8_t*>(digest);
@@ -715,7 +754,9 @@ extern "C" int scout_score_topk(int kind, const void* q, const void* digest, con
   a.nchunk = (nblk_cap + kChunk - 1) / kChunk;
   a.units = (int)units;
   a.counters = static_cast<int32_t*>(workspace);
-  a.status = nullptr;
+  a.status = dev_status;
+  a.inject = launch != nullptr ? launch->inject : SCOUT_INJECT_NONE;
+  a.score_wait = a.inject == SCOUT_INJECT_ABANDON ? kInjectWaitLimit : kWaitLimit;
   a.user_scores = scores != nullptr;
   a.scores = scores;
   a.topk_idx = topk_idx;
@@ -770,8 +811,25 @@ extern "C" int scout_score_topk(int kind, const void* q, const void* digest, con
   cudaLaunchAttribute attr[2];
   cfg.attrs = attr;
   cfg.numAttrs = early_start_attrs(launch, attr, 0);
+  if (zero_counter && cudaMemsetAsync(workspace, 0, counters_bytes(units), stream) != cudaSuccess)
+    return SCOUT_ERR_CUDA;
   if (cudaLaunchKernelEx(&cfg, kern, tmD, a) != cudaSuccess) return SCOUT_ERR_CUDA;
   return launch_status();
+}
+}  // namespace
+}  // namespace scout
+
+extern "C" int scout_score_topk(int kind, const void* q, const void* digest, const int32_t* seq_len,
+                                const uint32_t* resident_bits, const int32_t* prev_cpu_list,
+                                const int32_t* prev_cpu_count, int B, int Hq, int Hkv, int D, int P, int nblk_cap,
+                                int k, float* scores, int32_t* topk_idx, int32_t* topk_count, int32_t* res_list,
+                                int32_t* res_count, int32_t* cpu_list, int32_t* cpu_count, int32_t* delta_list,
+                                int32_t* delta_count, void* workspace, size_t workspace_bytes, int32_t* dev_status,
+                                const scout_launch* launch, cudaStream_t stream) {
+  return scout::score_topk_entry(kind, q, digest, seq_len, resident_bits, prev_cpu_list, prev_cpu_count, B, Hq, Hkv,
+                                 D, P, nblk_cap, k, scores, topk_idx, topk_count, res_list, res_count, cpu_list,
+                                 cpu_count, delta_list, delta_count, workspace, workspace_bytes, dev_status, launch,
+                                 stream, false);
 }
 
 // ---------------------------------------------------------------------------
@@ -787,7 +845,7 @@ extern "C" int scout_score_topk(int kind, const void* q, const void* digest, con
 namespace scout {
 namespace {
 
-constexpr size_t kNoAllocScratchBytes = 4u << 20;  // 4 MiB: the unit ticket counter(s)
+constexpr size_t kNoAllocScratchBytes = 4u << 20;  // 4 MiB, sized as a workspace of B * Hkv <= 1,048,576 units
 constexpr int kNoAllocMaxDevices = 64;
 
 static __device__ __align__(256) uint8_t g_topk_scratch[kNoAllocScratchBytes];
@@ -795,17 +853,24 @@ static __device__ __align__(256) uint8_t g_topk_scratch[kNoAllocScratchBytes];
 std::mutex g_scratch_mu;
 void* g_scratch_addr[kNoAllocMaxDevices] = {};
 
-// Device address of g_topk_scratch on the current device, looked up once per
-// device (the host-side symbol is only a stand-in and must never reach a kernel).
-int scratch_address(void** out) {
+// Device address of g_topk_scratch on the current device (the host-side symbol is only a
+// stand-in and must never reach a kernel).  Looked up afresh whenever `stream` is not being
+// captured, so that a cudaDeviceReset (after which the module, and the array, are loaded
+// anew) cannot leave a stale address behind; during a capture the address found by the last
+// call outside one is used, since the lookup may load the module.
+int scratch_address(cudaStream_t stream, void** out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return SCOUT_ERR_CUDA;
   if (dev < 0 || dev >= kNoAllocMaxDevices) return SCOUT_ERR_UNSUPPORTED;
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(stream, &cap) != cudaSuccess) return SCOUT_ERR_CUDA;
   std::lock_guard<std::mutex> lock(g_scratch_mu);
-  if (g_scratch_addr[dev] == nullptr) {
+  if (cap == cudaStreamCaptureStatusNone) {
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_topk_scratch) != cudaSuccess || p == nullptr) return SCOUT_ERR_CUDA;
     g_scratch_addr[dev] = p;
+  } else if (g_scratch_addr[dev] == nullptr) {
+    return SCOUT_ERR_CUDA;  // never called on this device outside a capture
   }
   *out = g_scratch_addr[dev];
   return SCOUT_OK;
@@ -821,18 +886,21 @@ extern "C" int scout_score_topk_noalloc(int kind, const void* q, const void* dig
                                         const int32_t* prev_cpu_count, int B, int Hq, int Hkv, int D, int P,
                                         int nblk_cap, int k, float* scores, int32_t* topk_idx, int32_t* topk_count,
                                         int32_t* res_list, int32_t* res_count, int32_t* cpu_list, int32_t* cpu_count,
-                                        int32_t* delta_list, int32_t* delta_count, cudaStream_t stream) {
+                                        int32_t* delta_list, int32_t* delta_count, int32_t* dev_status,
+                                        cudaStream_t stream) {
   using namespace scout;
-  const size_t need = scout_score_topk_workspace_bytes(B, Hkv, nblk_cap);
-  if (need == 0) return SCOUT_ERR_INVALID_ARG;
-  if (need > kNoAllocScratchBytes) return SCOUT_ERR_WORKSPACE;  // beyond the fixed scratch
-  void* scratch = nullptr;
-  const int rc = scratch_address(&scratch);
+  // every argument is checked before the shared array is touched
+  const int rc = check_topk_args(kind, q, digest, seq_len, resident_bits, prev_cpu_list, prev_cpu_count, B, Hq, Hkv,
+                                 D, P, nblk_cap, k, topk_idx, topk_count, res_list, res_count, cpu_list, cpu_count,
+                                 delta_list, delta_count, nullptr);
   if (rc != SCOUT_OK) return rc;
-  // the array keeps whatever the previous call left (a timed-out call may leave the unit
-  // ticket counter non-zero): zero the counters
-  if (cudaMemsetAsync(scratch, 0, counters_bytes((int64_t)B * Hkv), stream) != cudaSuccess) return SCOUT_ERR_CUDA;
-  return scout_score_topk(kind, q, digest, seq_len, resident_bits, prev_cpu_list, prev_cpu_count, B, Hq, Hkv, D, P,
+  if (scout_score_topk_workspace_bytes(B, Hkv, nblk_cap) > kNoAllocScratchBytes) return SCOUT_ERR_WORKSPACE;
+  void* scratch = nullptr;
+  const int ra = scratch_address(stream, &scratch);
+  if (ra != SCOUT_OK) return ra;
+  // the array keeps whatever the previous call left: its counter is zeroed on the stream once
+  // the remaining checks have passed, just before the launch
+  return score_topk_entry(kind, q, digest, seq_len, resident_bits, prev_cpu_list, prev_cpu_count, B, Hq, Hkv, D, P,
                           nblk_cap, k, scores, topk_idx, topk_count, res_list, res_count, cpu_list, cpu_count,
-                          delta_list, delta_count, scratch, kNoAllocScratchBytes, nullptr, stream);
+                          delta_list, delta_count, scratch, kNoAllocScratchBytes, dev_status, nullptr, stream, true);
 }

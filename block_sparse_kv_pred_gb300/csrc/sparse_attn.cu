@@ -39,8 +39,12 @@ namespace {
 #ifndef SCOUT_ATTN_SUBPAGE
 #define SCOUT_ATTN_SUBPAGE 32
 #endif
+#ifndef SCOUT_ATTN_PAIR
+#define SCOUT_ATTN_PAIR 2
+#endif
 constexpr int kConsumerWarps = SCOUT_ATTN_CONSUMERS;
 constexpr int kSubTokens = SCOUT_ATTN_SUBPAGE;
+constexpr int kPair = SCOUT_ATTN_PAIR;  // pages a consumer warp attends in one pass (1 or 2)
 constexpr int kEpilogueWarp = kConsumerWarps;     // combines the warps' states, writes whole units
 constexpr int kSplitWarp = kConsumerWarps + 1;     // merges the units cut by range boundaries
 constexpr int kThreads = (kConsumerWarps + 2) * 32;
@@ -144,15 +148,17 @@ __device__ __forceinline__ uint32_t movmatrix_t(uint32_t x) {
 //   O^T += V^T P^T (dims x heads); P^T reaches the B-operand layout by movmatrix.
 // Taking two pages together gives the MMA chains of both to the scheduler at once and
 // pays the running-max rescale once.  qb holds Q^T fragments: qb[s] = heads g, dims
-// 16s + 2t (+8).
+// 16s + 2t (+8).  The work is cut in two, so that the K halves of the stages can be refilled
+// as soon as the scores are computed, while the softmax and P V still run:
+//   attend_scores   s = scale * log2(e) * K q (masked past ntok), reading only K;
+//   attend_values   the online-softmax update and O^T += V^T P^T, reading only V.
 template <int PS, int NP>
-__device__ __forceinline__ void attend_pages(const uint32_t (&kbase)[NP], const uint32_t (&vbase)[NP],
-                                             const int (&ntok)[NP], const uint32_t (&qb)[8][2], float scale_log2,
-                                             WarpState& st, int lane) {
+__device__ __forceinline__ void attend_scores(const uint32_t (&kbase)[NP], const int (&ntok)[NP],
+                                              const uint32_t (&qb)[8][2], float scale_log2,
+                                              float (&s)[NP * (PS / 16)][4], int lane) {
   constexpr int MT = PS / 16;  // 16-token tiles per stage
   constexpr int T = NP * MT;   // tiles in all
   const int g = lane >> 2;
-  float s[T][4];
 #pragma unroll
   for (int tt = 0; tt < T; ++tt) {
     const int pg = tt / MT, mt = tt % MT;
@@ -170,8 +176,6 @@ __device__ __forceinline__ void attend_pages(const uint32_t (&kbase)[NP], const 
 #pragma unroll
     for (int e = 0; e < 4; ++e) s[tt][e] += s2[e];
   }
-  // per-head (column) max over the pages' tokens
-  float bm0 = -INFINITY, bm1 = -INFINITY;
 #pragma unroll
   for (int tt = 0; tt < T; ++tt) {
     const int pg = tt / MT, mt = tt % MT;
@@ -180,6 +184,18 @@ __device__ __forceinline__ void attend_pages(const uint32_t (&kbase)[NP], const 
     s[tt][1] = t0 < ntok[pg] ? s[tt][1] * scale_log2 : -INFINITY;
     s[tt][2] = t1 < ntok[pg] ? s[tt][2] * scale_log2 : -INFINITY;
     s[tt][3] = t1 < ntok[pg] ? s[tt][3] * scale_log2 : -INFINITY;
+  }
+}
+
+template <int PS, int NP>
+__device__ __forceinline__ void attend_values(const uint32_t (&vbase)[NP], float (&s)[NP * (PS / 16)][4],
+                                              WarpState& st, int lane) {
+  constexpr int MT = PS / 16;
+  constexpr int T = NP * MT;
+  // per-head (column) max over the pages' tokens
+  float bm0 = -INFINITY, bm1 = -INFINITY;
+#pragma unroll
+  for (int tt = 0; tt < T; ++tt) {
     bm0 = fmaxf(bm0, fmaxf(s[tt][0], s[tt][2]));
     bm1 = fmaxf(bm1, fmaxf(s[tt][1], s[tt][3]));
   }
@@ -388,7 +404,8 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const __grid_c
                                                                   const AttnArgs a) {
   using C = Cfg<P, S>;
   extern __shared__ uint8_t smem_raw[];
-  __shared__ uint64_t full_bar[C::kStages], cfull[kMaxSlots], cempty[kMaxSlots], sbar[kMaxSplit];
+  // kfull / vfull: the K / V half of a stage has landed (one phase per fill of the stage)
+  __shared__ uint64_t kfull[C::kStages], vfull[C::kStages], cfull[kMaxSlots], cempty[kMaxSlots], sbar[kMaxSplit];
   __shared__ int wtot[kThreads / 32];
   __shared__ float ew[kMaxG][kConsumerWarps], eown[kMaxG];  // epilogue weights
   __shared__ float efin[kMaxG], fwg[kMaxG], fwc[kMaxG];     // epilogue final LSE, merge weights
@@ -404,7 +421,10 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const __grid_c
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   if (tid == 0) {
-    for (int i = 0; i < C::kStages; ++i) mbar_init(&full_bar[i], 1);
+    for (int i = 0; i < C::kStages; ++i) {
+      mbar_init(&kfull[i], 1);
+      mbar_init(&vfull[i], 1);
+    }
     for (int i = 0; i < a.nslots; ++i) {
       mbar_init(&cfull[i], kConsumerWarps);
       mbar_init(&cempty[i], 1);
@@ -669,16 +689,17 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const __grid_c
     nt = min(max(nv - h * C::PS, 0), C::PS);
     row = sl * P + h * C::PS;
   };
-  // Load page kk (lane 0): both 64-column halves of K and of V, one box each.
-  auto issue = [&](int64_t kk, int row, int nt) {
+  // Load the K (which = 0) or V (which = 1) half of page kk (one lane): both 64-column halves
+  // in one box.
+  auto issue = [&](int64_t kk, int row, int nt, int which) {
     const int stage = (int)((warp + (int64_t)kConsumerWarps * kk) % C::kStages);
+    uint64_t* bar = which ? &vfull[stage] : &kfull[stage];
     if (nt > 0) {
-      uint8_t* sp = ring + stage * C::kStageBytes;
-      mbar_arrive_tx(&full_bar[stage], C::kStageBytes);
-      tma_load_3d(sp, &tmK, 0, row, 0, &full_bar[stage]);
-      tma_load_3d(sp + 2 * C::kHalfBytes, &tmV, 0, row, 0, &full_bar[stage]);
+      uint8_t* sp = ring + stage * C::kStageBytes + which * 2 * C::kHalfBytes;
+      mbar_arrive_tx(bar, 2 * C::kHalfBytes);
+      tma_load_3d(sp, which ? &tmV : &tmK, 0, row, 0, bar);
     } else {
-      mbar_arrive(&full_bar[stage]);
+      mbar_arrive(bar);
     }
   };
   // batch b = pages 32 b .. 32 b + 31 of this warp, page 32 b + m resolved by lane m; cur_*
@@ -704,18 +725,28 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const __grid_c
     if (m == kPhaseC) resolve_c(kk - kPhaseC + 32 + lane, pu, pj, plen, psl, nxt_row, nxt_nt);
   };
   // after pages kk .. kk + n - 1 (n = 1 or 2): their stages take this warp's pages kPerWarp
-  // further on; lane j issues the copies of page kk + j, so the two go out together
-  auto refill = [&](int64_t kk, int n) {
+  // further on, the K halves once the scores are computed, the V halves after P V; lane j
+  // issues the copy of page kk + j, so the two go out together.  where() gives a lane the
+  // pool row and valid tokens of its page (read before the halves are issued).
+  auto where = [&](int64_t kk, int n, int& row, int& nt) {
     const int64_t kr = kk + C::kPerWarp + (lane < n ? lane : 0);
     const int src = (int)(kr & 31);
     const int rc = __shfl_sync(0xffffffffu, cur_row, src), rn = __shfl_sync(0xffffffffu, nxt_row, src);
     const int tc = __shfl_sync(0xffffffffu, cur_nt, src), tn = __shfl_sync(0xffffffffu, nxt_nt, src);
     const bool in_cur = (kr >> 5) == cur_b;
-    if (lane < n && kr < n_mine) issue(kr, in_cur ? rc : rn, in_cur ? tc : tn);
+    row = in_cur ? rc : rn;
+    nt = in_cur ? tc : tn;
+  };
+  auto refill = [&](int64_t kk, int n, int row, int nt, int which) {
+    const int64_t kr = kk + C::kPerWarp + (lane < n ? lane : 0);
+    if (lane < n && kr < n_mine) issue(kr, row, nt, which);
   };
   for (int r = 0; r < C::kPerWarp && r < n_mine; ++r) {
     const int row = __shfl_sync(0xffffffffu, cur_row, r), nt = __shfl_sync(0xffffffffu, cur_nt, r);
-    if (lane == 0) issue(r, row, nt);
+    if (lane == 0) {
+      issue(r, row, nt, 0);
+      issue(r, row, nt, 1);
+    }
   }
 
   SegIter it = seg_iter(prefix, a.units, order);
@@ -741,8 +772,8 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const __grid_c
     // this warp's sub-pages of the segment (global sub-page numbers ii = warp (mod 4)), two at a time
     const int64_t seg_lo = i, seg_hi = i + (hi - lo) * C::kSub;
     for (int64_t ii = seg_lo + (warp - seg_lo % kConsumerWarps + kConsumerWarps) % kConsumerWarps; ii < seg_hi;
-         ii += 2 * kConsumerWarps) {
-      const bool two = ii + kConsumerWarps < seg_hi;
+         ii += kPair * kConsumerWarps) {
+      const bool two = kPair == 2 && ii + kConsumerWarps < seg_hi;
       const int64_t k = ii / kConsumerWarps;
       advance(k);
       const int nt0 = nt_of(k);
@@ -752,39 +783,62 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const __grid_c
         nt1 = nt_of(k + 1);
       }
       const int st0 = (int)(ii % C::kStages), st1 = (int)((ii + kConsumerWarps) % C::kStages);
-      bool got = ok && mbar_wait(&full_bar[st0], (uint32_t)(k / C::kPerWarp) & 1u);
-      if (got && two) got = mbar_wait(&full_bar[st1], (uint32_t)((k + 1) / C::kPerWarp) & 1u);
+      const uint32_t ph0 = (uint32_t)(k / C::kPerWarp) & 1u, ph1 = (uint32_t)((k + 1) / C::kPerWarp) & 1u;
+      int nrow, nnt;  // the page (of the next ones) whose halves this lane refills
+      where(k, two ? 2 : 1, nrow, nnt);
+      bool got = ok && mbar_wait(&kfull[st0], ph0);
+      if (got && two) got = mbar_wait(&kfull[st1], ph1);
       if (ok && !got) {
         if (lane == 0) report(a.status, SCOUT_DEV_TIMEOUT);
         ok = false;  // a copy may still be in flight: issue nothing more
       }
+      const uint32_t kb0 = ring_s + st0 * C::kStageBytes, kb1 = ring_s + st1 * C::kStageBytes;
+      constexpr int MT = C::PS / 16;
+      float sc[2 * MT][4];  // the scores of one or two pages
+      const bool pair = two && nt0 > 0 && nt1 > 0;  // both pages in one pass
       if (got) {
-        const uint32_t kb0 = ring_s + st0 * C::kStageBytes, kb1 = ring_s + st1 * C::kStageBytes;
-        if (nt0 > 0 && nt0 < C::PS) clear_tail_rows<C::PS>(ring + st0 * C::kStageBytes + 2 * C::kHalfBytes, nt0, lane);
-        if (two && nt1 > 0 && nt1 < C::PS)
-          clear_tail_rows<C::PS>(ring + st1 * C::kStageBytes + 2 * C::kHalfBytes, nt1, lane);
-        if (two && nt0 > 0 && nt1 > 0) {
-          const uint32_t kbs[2] = {kb0, kb1}, vbs[2] = {kb0 + 2 * C::kHalfBytes, kb1 + 2 * C::kHalfBytes};
+        if (pair) {
+          const uint32_t kbs[2] = {kb0, kb1};
           const int nts[2] = {nt0, nt1};
-          attend_pages<C::PS, 2>(kbs, vbs, nts, qa, a.scale_log2, st, lane);
+          attend_scores<C::PS, 2>(kbs, nts, qa, a.scale_log2, sc, lane);
         } else {
-          if (nt0 > 0) {
-            const uint32_t kbs[1] = {kb0}, vbs[1] = {kb0 + 2 * C::kHalfBytes};
-            const int nts[1] = {nt0};
-            attend_pages<C::PS, 1>(kbs, vbs, nts, qa, a.scale_log2, st, lane);
-          }
-          if (two && nt1 > 0) {
-            const uint32_t kbs[1] = {kb1}, vbs[1] = {kb1 + 2 * C::kHalfBytes};
-            const int nts[1] = {nt1};
-            attend_pages<C::PS, 1>(kbs, vbs, nts, qa, a.scale_log2, st, lane);
-          }
+          const int ntx = nt0 > 0 ? nt0 : nt1;  // the one page with tokens (if any)
+          const uint32_t kbs[1] = {nt0 > 0 ? kb0 : kb1};
+          const int nts[1] = {ntx};
+          if (ntx > 0) attend_scores<C::PS, 1>(kbs, nts, qa, a.scale_log2, reinterpret_cast<float(&)[MT][4]>(sc), lane);
         }
       }
-      // reload the stages with this warp's pages kPerWarp further on once every lane is done
+      // the K halves may be reloaded once every lane has read them
       if (ok) {
         fence_proxy_async();
         __syncwarp();
-        refill(k, two ? 2 : 1);
+        refill(k, two ? 2 : 1, nrow, nnt, 0);
+      }
+      if (got) {
+        got = mbar_wait(&vfull[st0], ph0);
+        if (got && two) got = mbar_wait(&vfull[st1], ph1);
+        if (ok && !got) {
+          if (lane == 0) report(a.status, SCOUT_DEV_TIMEOUT);
+          ok = false;
+        }
+      }
+      if (got) {
+        if (nt0 > 0 && nt0 < C::PS) clear_tail_rows<C::PS>(ring + st0 * C::kStageBytes + 2 * C::kHalfBytes, nt0, lane);
+        if (two && nt1 > 0 && nt1 < C::PS)
+          clear_tail_rows<C::PS>(ring + st1 * C::kStageBytes + 2 * C::kHalfBytes, nt1, lane);
+        if (pair) {
+          const uint32_t vbs[2] = {kb0 + 2 * C::kHalfBytes, kb1 + 2 * C::kHalfBytes};
+          attend_values<C::PS, 2>(vbs, sc, st, lane);
+        } else if (nt0 > 0 || (two && nt1 > 0)) {
+          const uint32_t vbs[1] = {(nt0 > 0 ? kb0 : kb1) + 2 * C::kHalfBytes};
+          attend_values<C::PS, 1>(vbs, reinterpret_cast<float(&)[MT][4]>(sc), st, lane);
+        }
+      }
+      // and the V halves once P V is done
+      if (ok) {
+        fence_proxy_async();
+        __syncwarp();
+        refill(k, two ? 2 : 1, nrow, nnt, 1);
       }
     }
     i = seg_hi;

@@ -59,8 +59,14 @@ def _bits(mask: np.ndarray) -> np.ndarray:
 class DecodeSweep:
     """The layer's state on the GPU and the host, and one method per decode step."""
 
-    def __init__(self, shape: W.Shape, steps: int, recall_every: int = 16, device="cuda"):
-        """``recall_every`` 0: no recall (the profile from which recall intervals are read)."""
+    def __init__(self, shape: W.Shape, steps: int, recall_every: int = 16, device="cuda", host=None,
+                 gather=True):
+        """``recall_every`` 0: no recall (the profile from which recall intervals are read).
+        ``host``: optional pair of pinned bf16 host tensors of at least [units][nblk][P][D]
+        elements each, reused for the host copy of the layer's K/V (a multi-layer sweep keeps
+        one pair).  ``gather``: recalls move their pages with the gather kernel reading mapped
+        host memory (scout_recall_gather_async); False: one cudaMemcpyAsync per run of pages."""
+        self.gather = gather
         self.s = s = shape
         self.steps, self.recall_every = steps, recall_every
         dev = self.dev = torch.device(device)
@@ -72,11 +78,14 @@ class DecodeSweep:
         # KV that recalls read
         order = full["page_table"].reshape(-1).long()
         logical = {}
-        for n in ("K", "V"):
+        for i, n in enumerate(("K", "V")):
             logical[n] = full[n + "_pool"][order]
-            host = torch.empty((U, nb, P, D), dtype=torch.bfloat16, pin_memory=True)
-            host.copy_(logical[n].reshape(U, nb, P, D))
-            setattr(self, "h" + n, host)
+            if host is None:
+                hbuf = torch.empty((U, nb, P, D), dtype=torch.bfloat16, pin_memory=True)
+            else:
+                hbuf = host[i].view(-1)[: U * nb * P * D].view(U, nb, P, D)
+            hbuf.copy_(logical[n].reshape(U, nb, P, D))
+            setattr(self, "h" + n, hbuf)
         # prefill: digests over every valid block (the whole context was on the GPU)
         self.seq = wl.seq_len.astype(np.int32).copy()
         self.d_seq = WD.to_dev(self.seq, dev)
@@ -112,6 +121,7 @@ class DecodeSweep:
         self.wa = bs.sparse_attn_workspace(s.B, s.Hq, s.Hkv, P, device=dev)
         self.scores = torch.empty((s.B, s.Hkv, nb), dtype=torch.float32, device=dev)
         self.side = torch.cuda.Stream(dev)
+        self.status = torch.zeros(1, dtype=torch.int32, device=dev)
         self.prev = None
         self.t = 0
 
@@ -119,13 +129,18 @@ class DecodeSweep:
         """Copy the ops' blocks from the host into their slots on the side stream, then commit
         the page table and residency bits after the copy.  Returns (bytes, seconds)."""
         s = self.s
+        d_ops = WD.to_dev(np.asarray(ops, dtype=np.int32).reshape(-1, 4), self.dev)
+        self.side.wait_stream(torch.cuda.current_stream(self.dev))  # d_ops is on the device
         t0, done = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         t0.record(self.side)
-        bs.recall_async([tuple(int(x) for x in r) for r in ops], self.hK, self.hV, self.K_pool, self.V_pool, s.B,
-                        s.Hkv, s.P, s.nblk, self.side)
+        if self.gather:
+            bs.recall_gather_async(d_ops, self.hK, self.hV, self.K_pool, self.V_pool, s.B, s.Hkv, s.P, s.nblk, self.side,
+                                   status=self.status)
+        else:
+            bs.recall_async([tuple(int(x) for x in r) for r in ops], self.hK, self.hV, self.K_pool, self.V_pool, s.B,
+                            s.Hkv, s.P, s.nblk, self.side)
         done.record(self.side)
-        bs.commit_residency(WD.to_dev(np.asarray(ops, dtype=np.int32).reshape(-1, 4), self.dev), self.d_table,
-                            self.d_bits, self.n_slots, s.B, s.Hkv, wait_event=done)
+        bs.commit_residency(d_ops, self.d_table, self.d_bits, self.n_slots, s.B, s.Hkv, wait_event=done)
         done.synchronize()
         return len(ops) * 2 * s.P * s.D * 2, t0.elapsed_time(done) / 1e3
 
@@ -149,10 +164,14 @@ class DecodeSweep:
         bs.build_digest("minmax", self.K_pool, self.d_table, self.d_seq, s.B, s.Hkv, P, self.digest, block_list=tail)
         resident_before = self.res.copy()
         out = bs.score_topk("minmax", WD.to_dev(self.ps[t], self.dev), self.digest, self.d_seq, self.d_bits, s.B,
-                            s.Hq, s.Hkv, P, s.nblk, s.k, self.ws, prev_cpu=self.prev, scores=self.scores)
+                            s.Hq, s.Hkv, P, s.nblk, s.k, self.ws, prev_cpu=self.prev, scores=self.scores,
+                            status=self.status)
         O, lse = bs.sparse_attn(WD.to_dev(self.qs[t], self.dev), self.K_pool, self.V_pool, self.d_table, self.d_seq,
-                                out["res"], out["res_count"], s.B, s.Hq, s.Hkv, P, s.k, s.scale, self.wa)
+                                out["res"], out["res_count"], s.B, s.Hq, s.Hkv, P, s.k, s.scale, self.wa,
+                                status=self.status)
         torch.cuda.synchronize(self.dev)
+        if int(self.status.item()) != 0:
+            raise RuntimeError(f"device status {int(self.status.item())} at step {t}")
         rec = {"t": t, "seq": self.seq.copy(), "resident": resident_before, "O": O.cpu().numpy(),
                "lse": lse.cpu().numpy(), "prev_cpu": None}
         if self.prev is not None:
@@ -204,6 +223,83 @@ def profile_recall_intervals(layers: int, steps: int, beta: float = 0.12, shape:
     return traces, bs.recall_intervals(traces, beta)
 
 
+def run_layers(layers: int, steps: int, recall_every=16, beta: float = 0.12, shape: W.Shape | None = None,
+               gather: bool = True):
+    """The decode sweep over ``layers`` layers, one after another (each its own seeded workload,
+    freed before the next, the pinned host copy of its K/V reused): yields (layer, sweep, record)
+    for every decode step.  ``recall_every``: a step count, or a sequence of per-layer intervals
+    (e.g. the recall intervals profiled by :func:`profile_recall_intervals`, section 3.4)."""
+    import dataclasses
+
+    base = shape or c4_shape(steps)
+    U, nb, P, D = base.units, base.nblk, base.P, base.D
+    host = [torch.empty(U * nb * P * D, dtype=torch.bfloat16, pin_memory=True) for _ in range(2)]
+    every = [int(recall_every)] * layers if np.isscalar(recall_every) else [int(x) for x in recall_every]
+    if len(every) != layers:
+        raise ValueError("one recall interval per layer")
+    for layer in range(layers):
+        sw = DecodeSweep(dataclasses.replace(base, seed=base.seed + layer), steps, recall_every=every[layer],
+                         host=host, gather=gather)
+        for _ in range(steps):
+            yield layer, sw, sw.step()
+        del sw
+        torch.cuda.empty_cache()
+
+
+def probe_recall_bandwidth(total_mib: int = 256, device="cuda", seed: int = 0) -> list[dict]:
+    """Host-to-device rate of recall transfers by granularity (the pages compare ~800 MB/s for
+    4 KB per-token transfers with ~15 GB/s for 128 KB pages over PCIe 4.0; section 2.3, Figure 3).
+    Pages of P tokens (P x 128 bf16 = P * 256 bytes for K, the same for V) move from pinned host
+    memory into randomly chosen pool slots; 4 KB = P 16 and 8 KB = P 32 scattered, 128 KB = runs of
+    16 consecutive 8 KB pages into consecutive slots.  Both movers: one cudaMemcpyAsync per run of
+    pages (scout_recall_async) and the gather kernel (scout_recall_gather_async)."""
+    dev = torch.device(device)
+    rng = np.random.default_rng(seed)
+    out = []
+    side = torch.cuda.Stream(dev)
+    for gran, P, run in ((4096, 16, 1), (8192, 32, 1), (131072, 32, 16)):
+        page = P * 128 * 2
+        n_ops = (total_mib << 20) // (2 * page)  # K and V
+        nb = n_ops  # one unit holding every block: block i of the host copy
+        hK = torch.empty((nb, P, 128), dtype=torch.bfloat16, pin_memory=True)
+        hV = torch.empty_like(hK, pin_memory=True)
+        hK.view(torch.int16).copy_(torch.from_numpy(rng.integers(-2 ** 15, 2 ** 15, size=hK.shape, dtype=np.int16)))
+        hV.copy_(hK)
+        runs = n_ops // run
+        slot0 = rng.permutation(runs) * run  # each run lands on `run` consecutive slots, runs scattered
+        ops = np.array([(0, r * run + i, slot0[r] + i, -1) for r in range(runs) for i in range(run)], np.int32)
+        Kp = torch.empty((n_ops, P, 128), dtype=torch.bfloat16, device=dev)
+        Vp = torch.empty_like(Kp)
+        d_ops = WD.to_dev(ops, dev)
+        h_ops = (bs.RecallOp * n_ops)(*[bs.RecallOp(*(int(x) for x in o)) for o in ops])  # built before timing
+        row = {"granularity_bytes": gran, "transfers": int(2 * runs), "bytes": int(2 * n_ops * page)}
+        for name in ("copies", "gather"):
+            best = None
+            for _ in range(3):
+                torch.cuda.synchronize(dev)
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record(side)
+                if name == "copies":
+                    rc = bs.lib().scout_recall_async(h_ops, n_ops, hK.data_ptr(), hV.data_ptr(), Kp.data_ptr(),
+                                                     Vp.data_ptr(), n_ops, 1, 1, 128, P, nb, None, None,
+                                                     side.cuda_stream, None)
+                    if rc:
+                        raise bs.ScoutError(f"scout_recall_async: {rc}")
+                else:
+                    bs.recall_gather_async(d_ops, hK, hV, Kp, Vp, 1, 1, P, nb, side)
+                b.record(side)
+                b.synchronize()
+                ms = a.elapsed_time(b)
+                best = ms if best is None else min(best, ms)
+            row[name + "_GB_s"] = row["bytes"] / (best / 1e3) / 1e9
+        # both movers put every page where the ops say
+        assert torch.equal(Kp.view(torch.int16)[torch.from_numpy(ops[:, 2]).long().to(dev)].cpu(),
+                           hK.view(torch.int16)[torch.from_numpy(ops[:, 1]).long()])
+        out.append(row)
+        del hK, hV, Kp, Vp
+    return out
+
+
 def main():
     ap = argparse.ArgumentParser(description="Residency sweep: one layer, many decode steps, per-step report")
     ap.add_argument("--steps", type=int, default=64)
@@ -211,7 +307,29 @@ def main():
     ap.add_argument("--profile-layers", type=int, default=0,
                     help="instead: profile this many layers without recalls and print their recall intervals")
     ap.add_argument("--beta", type=float, default=0.12, help="CPU compute ratio threshold of the profile")
+    ap.add_argument("--layers", type=int, default=0,
+                    help="instead: the sweep over this many seeded layers, one JSON row per (layer, step); with "
+                         "--recall-every 0 ... no recall, with --profiled the per-layer intervals of a profile")
+    ap.add_argument("--profiled", action="store_true",
+                    help="with --layers: recall at each layer's interval profiled without recalls first (--beta)")
+    ap.add_argument("--copies", action="store_true", help="recall with cudaMemcpyAsync calls, not the gather kernel")
+    ap.add_argument("--probe-recall", action="store_true",
+                    help="instead: host-to-device recall rate at 4 KB, 8 KB and 128 KB granularity")
     a = ap.parse_args()
+    if a.probe_recall:
+        for row in probe_recall_bandwidth():
+            print(json.dumps(row), flush=True)
+        return
+    if a.layers > 0:
+        every = a.recall_every
+        if a.profiled:
+            traces, iv = profile_recall_intervals(a.layers, a.steps, a.beta)
+            print(json.dumps({"profile_beta": a.beta, "intervals": [int(x) for x in iv],
+                              "mean_interval": float(iv.mean())}), flush=True)
+            every = iv
+        for layer, sw, rec in run_layers(a.layers, a.steps, every, gather=not a.copies):
+            print(json.dumps({"layer": layer, **rec["stats"]}), flush=True)
+        return
     if a.profile_layers > 0:
         traces, iv = profile_recall_intervals(a.profile_layers, a.steps, a.beta)
         for layer in range(a.profile_layers):

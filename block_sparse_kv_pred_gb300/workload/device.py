@@ -82,3 +82,35 @@ def materialize(wl: Workload, device="cuda", with_gemm: bool = True) -> dict:
     out["O_cpu"] = to_dev(o, dev)
     out["lse_cpu"] = to_dev(lse, dev)
     return out
+
+
+def materialize_pool(wl: Workload, keep: np.ndarray, device="cuda", seed_offset: int = 7919):
+    """A K/V pool holding only the blocks marked in ``keep`` (bool [units][nblk]), each in a slot of
+    a seeded permutation, as a GPU holding part of the cache keeps them.  Returns (K_pool, V_pool,
+    page_table int32 [B][Hkv][nblk] with -1 for blocks without a slot, n_slots); the pages equal
+    ``Workload.unit_kv`` bit for bit."""
+    s = wl.s
+    dev = torch.device(device)
+    idx = np.flatnonzero(np.asarray(keep, dtype=bool).reshape(-1)).astype(np.int32)  # u * nblk + j
+    n = int(idx.size)
+    if n == 0:
+        raise ValueError("the pool would hold no block")
+    perm = np.random.Generator(np.random.PCG64(s.seed + seed_offset)).permutation(n).astype(np.int32)
+    owner = np.empty(n, dtype=np.int32)
+    owner[perm] = idx  # slot perm[i] holds block idx[i]
+    table = np.full(s.units * s.nblk, -1, dtype=np.int32)
+    table[idx] = perm
+    d_owner = to_dev(owner, dev)
+    chan = to_dev(wl.chan_scale, dev)
+    heavy = to_dev(wl.heavy, dev)
+    hdir = to_dev(wl.hdir, dev)
+    pools = []
+    for sid, hv in ((STREAM_K, True), (STREAM_V, False)):
+        pool = torch.empty((n, s.P, s.D), dtype=torch.bfloat16, device=dev)
+        rc = gen_lib().scoutgen_fill_pool_bf16(pool.data_ptr(), n, s.P, s.D, d_owner.data_ptr(), s.nblk, s.seed, sid,
+                                               chan.data_ptr(), heavy.data_ptr() if hv else None,
+                                               hdir.data_ptr() if hv else None, _stream())
+        if rc:
+            raise RuntimeError(f"scoutgen_fill_pool_bf16 failed ({rc})")
+        pools.append(pool)
+    return pools[0], pools[1], to_dev(table.reshape(s.B, s.Hkv, s.nblk), dev), n

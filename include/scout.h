@@ -12,9 +12,11 @@
  *   a rejected call launches nothing.  A launch failure reported by the CUDA
  *   runtime returns SCOUT_ERR_CUDA.
  * - The host-side entry points (scout_plan_recall, scout_plan_recall_pages,
- *   scout_recall_intervals, scout_cpu_attend) are the exception: host pointers
- *   only, synchronous, no GPU involved.  scout_cpu_attend also runs on worker threads it starts and joins
- *   within the call.
+ *   scout_recall_intervals, scout_cpu_attend, scout_cpu_pool_*,
+ *   scout_cpu_attend_async) are the exception: host pointers only, no GPU
+ *   involved, synchronous except scout_cpu_attend_async.  scout_cpu_attend runs on
+ *   worker threads it starts and joins within the call; the pool calls run on the
+ *   caller's pool.
  * - bf16 tensors are IEEE bfloat16 (2 bytes); fp32 are IEEE binary32.
  * - Shapes: B sequences, Hq query heads, Hkv KV heads (G = Hq / Hkv query heads
  *   per KV head, 1 <= G <= 8), D = 128 head dims, P tokens per KV block
@@ -26,7 +28,9 @@
  *   *dev_status.  Bounded waits that expire set SCOUT_DEV_TIMEOUT.
  * - No C++ exception crosses this interface and the library keeps no mutable
  *   global state: calls on different streams with different buffers are
- *   independent.
+ *   independent.  The one exception is scout_score_topk_noalloc, whose scratch
+ *   is a device array inside the library shared by all its calls: overlapping
+ *   calls of it must be serialised (see its comment).
  */
 #ifndef SCOUT_H_
 #define SCOUT_H_
@@ -95,7 +99,24 @@ typedef struct scout_launch {
   int max_ctas;
   int pdl;
   cudaEvent_t early_event;
+  int inject; /* fault injection for tests; 0 (SCOUT_INJECT_NONE) in normal use */
 } scout_launch;
+
+/* Values of scout_launch.inject.  They make a failure happen without faulting or hanging
+ * the GPU, so that tests can check how it is reported and that it does no lasting harm.
+ *   SCOUT_INJECT_ABANDON  scout_score_topk only: every CTA behaves as if a bounded wait of
+ *     its copy-issuing warp had expired after its first unit: it reports SCOUT_DEV_TIMEOUT,
+ *     hands out no further work, lets every copy it started land, and leaves the scoring
+ *     warps to wait for a stage that never comes, under a short poll limit (a real bounded
+ *     wait that expires).  The units it skipped keep stale lists.  The call still leaves
+ *     its workspace counter at zero, so the next call on the same workspace is correct.
+ *   SCOUT_INJECT_COPY_FAIL  scout_recall_async and scout_recall_gather_async only: the
+ *     call returns SCOUT_ERR_CUDA as if the CUDA runtime had refused a copy or the launch
+ *     (scout_recall_async: its second run of copies, after the first was enqueued;
+ *     scout_recall_gather_async: the gather launch, so nothing is enqueued). */
+#define SCOUT_INJECT_NONE 0
+#define SCOUT_INJECT_ABANDON 1
+#define SCOUT_INJECT_COPY_FAIL 2
 
 /* Human-readable name of a status code (static string, never NULL). */
 const char* scout_status_string(int status);
@@ -169,9 +190,14 @@ int scout_build_digest(int kind, const void* K_pool, int64_t n_slots, const int3
  *   topk_idx/topk_count  B_pred;  res_list/res_count  B_pred with bit set;
  *   cpu_list/cpu_count   B_pred with bit clear;  delta_list/delta_count
  *   cpu list minus the previous cpu list.
- * workspace    scout_score_topk_workspace_bytes() bytes; its first
- *              4 * B * Hkv bytes must be zero before the first use and are
- *              left zero by every call.
+ * workspace    scout_score_topk_workspace_bytes() bytes (4 * B * Hkv rounded
+ *              up to 256; the kernel uses its first word, a unit ticket
+ *              counter); it must be zero before the first use and every call,
+ *              including one whose bounded waits expired, leaves it zero.
+ * dev_status   int32 (may be NULL): SCOUT_DEV_TIMEOUT is OR-ed in when a bounded
+ *              wait expired; the lists of the units left unfinished are then
+ *              stale.  The call still returns SCOUT_OK (the failure is found on
+ *              the device, after the launch).
  * Requires k >= 1, nblk_cap <= 8192, G <= 8.
  * ------------------------------------------------------------------------ */
 size_t scout_score_topk_workspace_bytes(int B, int Hkv, int nblk_cap);
@@ -180,7 +206,7 @@ int scout_score_topk(int kind, const void* q, const void* digest, const int32_t*
                      const int32_t* prev_cpu_count, int B, int Hq, int Hkv, int D, int P, int nblk_cap,
                      int k, float* scores, int32_t* topk_idx, int32_t* topk_count, int32_t* res_list,
                      int32_t* res_count, int32_t* cpu_list, int32_t* cpu_count, int32_t* delta_list,
-                     int32_t* delta_count, void* workspace, size_t workspace_bytes,
+                     int32_t* delta_count, void* workspace, size_t workspace_bytes, int32_t* dev_status,
                      const scout_launch* launch, cudaStream_t stream);
 
 /* ------------------------------------------------------------------------ *
@@ -190,16 +216,21 @@ int scout_score_topk(int kind, const void* q, const void* digest, const int32_t*
  * engine that reserves all GPU memory in one pool at start-up and forbids later
  * cudaMalloc calls, or a host that loads this library as a plugin without giving
  * it an allocator.  Same arguments and results as scout_score_topk, minus the
- * workspace.  The scratch is one fixed device array of
+ * workspace and the launch options.  The scratch is one fixed device array of
  * scout_score_topk_noalloc_max_bytes() bytes (4 MiB) inside the library, held by
- * every GPU that loads it until the process exits; a call whose
- * scout_score_topk_workspace_bytes(B, Hkv, nblk_cap) exceeds that returns
- * SCOUT_ERR_WORKSPACE and launches nothing.  It never calls cudaMalloc or
- * cudaFree.  The first call on a device looks up the array's device address
- * (once per device, with that device current); make that first call before any
- * stream capture.  Each call zeroes the array's counters on `stream` before its
- * kernel.  All calls share the one array, so calls whose kernels overlap on the
- * GPU (different streams, or different host threads) race: serialise them.
+ * every GPU that loads it until the process exits.  The kernel uses one counter
+ * word of it, but the array is sized like the caller workspace, so it accepts
+ * B * Hkv <= 1,048,576 units; a call whose scout_score_topk_workspace_bytes(B, Hkv,
+ * nblk_cap) exceeds the array returns SCOUT_ERR_WORKSPACE.  Every argument is
+ * checked before anything is enqueued: a rejected call leaves the array alone.
+ * It never calls cudaMalloc or cudaFree.  The array's device address is looked up
+ * (cudaGetSymbolAddress, with the caller's device current) on every call made
+ * outside a stream capture, so it stays right after cudaDeviceReset; a call
+ * inside a capture uses the address the last call outside one found on that
+ * device, so make one call on each device before capturing.  Each call zeroes
+ * the array's counter on `stream` before its kernel.  All calls share the one
+ * array, so calls whose kernels overlap on the GPU (different streams, or
+ * different host threads) race: serialise them.
  * ------------------------------------------------------------------------ */
 size_t scout_score_topk_noalloc_max_bytes(void);
 int scout_score_topk_noalloc(int kind, const void* q, const void* digest, const int32_t* seq_len,
@@ -207,7 +238,7 @@ int scout_score_topk_noalloc(int kind, const void* q, const void* digest, const 
                              const int32_t* prev_cpu_count, int B, int Hq, int Hkv, int D, int P, int nblk_cap,
                              int k, float* scores, int32_t* topk_idx, int32_t* topk_count, int32_t* res_list,
                              int32_t* res_count, int32_t* cpu_list, int32_t* cpu_count, int32_t* delta_list,
-                             int32_t* delta_count, cudaStream_t stream);
+                             int32_t* delta_count, int32_t* dev_status, cudaStream_t stream);
 
 /* ------------------------------------------------------------------------ *
  * GPU partial attention over the resident selected blocks.
@@ -275,10 +306,25 @@ int scout_merge(const float* O_a, const float* lse_a, const float* O_b, const fl
  *
  * scout_recall_async: on side_stream, waits for wait_event (may be NULL), copies
  * K and V of every op (adjacent ops with consecutive blocks and slots become one
- * copy), then records done_event (may be NULL).
+ * cudaMemcpyAsync), then records done_event (may be NULL).  host_K / host_V may be
+ * any pinned host memory.  If a copy is refused (SCOUT_ERR_CUDA), the copies before
+ * it stay enqueued and done_event is not recorded: the slots the ops name then hold
+ * undefined bytes while the tables still give them to the evicted blocks, so the
+ * caller must commit the evictions alone (the same ops with block = -1) before the
+ * pool is read again.
+ * scout_recall_gather_async: the same move as ONE kernel on side_stream, which reads
+ * the pages straight from host memory (a warp per K or V page, 16-byte loads) and
+ * writes them into their slots; scattered pages cost no copy call each.  d_ops is a
+ * DEVICE array of the ops; host_K / host_V must be pinned host memory mapped into the
+ * device's address space (cudaHostAlloc / cudaMallocHost, or cudaHostRegister-ed, on
+ * a system with unified addressing; 16-byte aligned), else SCOUT_ERR_UNSUPPORTED.  An
+ * op outside the tables or the pool is skipped and SCOUT_DEV_BAD_INDEX set in
+ * dev_status (may be NULL).  A refused launch enqueues nothing and records no
+ * done_event, so the pool and the tables are as before.
  * scout_commit_residency: on stream, waits for wait_event (normally the recall's
  * done_event), then for every op clears evict_block's page-table entry (-1) and
- * residency bit, and afterwards sets block's entry to slot and its bit.
+ * residency bit, and afterwards sets block's entry to slot and its bit (an op with
+ * block = -1 only evicts).
  * d_ops is a DEVICE copy of the same ops.  Until the commit runs, the tables
  * still describe the old residency, so a failed or unfinished copy never makes a
  * block look resident.
@@ -292,7 +338,12 @@ typedef struct scout_recall_op {
 
 int scout_recall_async(const scout_recall_op* ops, int n_ops, const void* host_K, const void* host_V,
                        void* K_pool, void* V_pool, int64_t n_slots, int B, int Hkv, int D, int P,
-                       int nblk_cap, cudaEvent_t wait_event, cudaStream_t side_stream, cudaEvent_t done_event);
+                       int nblk_cap, const scout_launch* launch, cudaEvent_t wait_event, cudaStream_t side_stream,
+                       cudaEvent_t done_event);
+int scout_recall_gather_async(const scout_recall_op* d_ops, int n_ops, const void* host_K, const void* host_V,
+                              void* K_pool, void* V_pool, int64_t n_slots, int B, int Hkv, int D, int P,
+                              int nblk_cap, int32_t* dev_status, const scout_launch* launch, cudaEvent_t wait_event,
+                              cudaStream_t side_stream, cudaEvent_t done_event);
 int scout_commit_residency(const scout_recall_op* d_ops, int n_ops, int32_t* page_table, uint32_t* resident_bits,
                            int64_t n_slots, int B, int Hkv, int nblk_cap, cudaEvent_t wait_event,
                            cudaStream_t stream);
@@ -385,6 +436,36 @@ int scout_recall_intervals(const float* ratio, int layers, int steps, float beta
 int scout_cpu_attend(const void* q, const void* K, const void* V, const int32_t* seq_len, const int32_t* cpu_list,
                      const int32_t* cpu_count, int B, int Hq, int Hkv, int D, int P, int nblk_cap, int k,
                      float scale, float* O_cpu, float* lse_cpu, int n_threads);
+
+/* ------------------------------------------------------------------------ *
+ * The CPU side on a caller-owned pool of worker threads (host code).
+ * ScoutAttention (arXiv HTML), section 3.3 and Algorithm 1: the CPU attention of
+ * layer i+1 is spawned one layer ahead and runs while the GPU computes layer i; its
+ * partial must be back before layer i+1 merges it.  A pipeline calling this every
+ * layer keeps one pool (no thread start per call) and waits for each layer's
+ * partial with a bound, so a late CPU side is reported instead of stalling it.
+ *
+ * scout_cpu_pool_create(n_threads): n_threads workers (0: one per hardware thread);
+ *   NULL if no thread could be started.  scout_cpu_pool_threads: their number.
+ * scout_cpu_attend_async(pool, ...): the arguments and checks of scout_cpu_attend
+ *   (same errors, nothing written on error); starts the job on the pool's workers and
+ *   returns at once.  One job at a time: SCOUT_ERR_INVALID_ARG while the previous
+ *   one runs.  The buffers must stay valid until the job is done.  Results are bit
+ *   for bit those of scout_cpu_attend (a unit is one worker's, whatever the count).
+ * scout_cpu_pool_wait(pool, timeout_us): SCOUT_OK once the job is done (or when no
+ *   job was started), SCOUT_ERR_TIMEOUT if it is still running after timeout_us
+ *   microseconds (it keeps running: wait again, or destroy the pool, which waits).
+ * scout_cpu_pool_destroy(pool): waits for a running job, joins the workers, frees
+ *   the pool (NULL is a no-op).  No thread of the pool outlives it.
+ * ------------------------------------------------------------------------ */
+typedef struct scout_cpu_pool scout_cpu_pool;
+scout_cpu_pool* scout_cpu_pool_create(int n_threads);
+int scout_cpu_pool_threads(const scout_cpu_pool* pool);
+void scout_cpu_pool_destroy(scout_cpu_pool* pool);
+int scout_cpu_attend_async(scout_cpu_pool* pool, const void* q, const void* K, const void* V, const int32_t* seq_len,
+                           const int32_t* cpu_list, const int32_t* cpu_count, int B, int Hq, int Hkv, int D, int P,
+                           int nblk_cap, int k, float scale, float* O_cpu, float* lse_cpu);
+int scout_cpu_pool_wait(scout_cpu_pool* pool, int64_t timeout_us);
 
 #ifdef __cplusplus
 }

@@ -55,10 +55,11 @@ def test_host_validation_rejects_without_launch(L):
     assert L.scout_predict_q(fake, fake, fake, 257, 128, 64, None, None, None) == 2  # M > 256
     assert L.scout_build_digest(0, fake, 10, fake, fake, 1, 1, 128, 48, 4, None, 0, fake, None, None) == 2  # P
     assert L.scout_build_digest(7, fake, 10, fake, fake, 1, 1, 128, 32, 4, None, 0, fake, None, None) == 1  # kind
-    args = [0, fake, fake, fake, fake, None, None, 1, 18, 2, 128, 32, 64, 8, None] + [fake] * 8 + [fake, 1 << 20, None, None]
+    args = [0, fake, fake, fake, fake, None, None, 1, 18, 2, 128, 32, 64, 8, None] + [fake] * 8 + [fake, 1 << 20, None,
+                                                                                                   None, None]
     assert L.scout_score_topk(*args) == 2  # G = 9 > 8
     args[7:10] = [1, 8, 2]
-    args[-3] = 16
+    args[-4] = 16
     assert L.scout_score_topk(*args) == 3  # workspace too small
     args[5] = fake  # prev list without prev count
     assert L.scout_score_topk(*args) == 1
@@ -73,7 +74,13 @@ def test_host_validation_rejects_without_launch(L):
     assert L.scout_sparse_attn_merge(fake, fake, fake, 100, fake, fake, fake, fake, 1, 8, 2, 128, 32, 8, 4, 0.1,
                                      fake, fake, fake, fake, fake, 1 << 24, None, neg, None) == 1  # max_ctas < 0
     ops = (bs.RecallOp * 1)(bs.RecallOp(0, 5, 3, -1))
-    assert L.scout_recall_async(ops, 1, fake, fake, fake, fake, 2, 1, 1, 128, 32, 8, None, None, None) == 1  # slot 3 >= 2
+    assert L.scout_recall_async(ops, 1, fake, fake, fake, fake, 2, 1, 1, 128, 32, 8, None, None, None,
+                                None) == 1  # slot 3 >= 2
+    assert L.scout_recall_gather_async(fake, 1, fake, fake, fake, fake, 2, 1, 1, 128, 48, 8, None, None, None, None,
+                                       None) == 2  # P = 48
+    bad = ctypes.pointer(bs.Launch(0, 0, None, bs.INJECT_ABANDON))  # not an injection the recall knows
+    assert L.scout_recall_gather_async(fake, 1, fake, fake, fake, fake, 2, 1, 1, 128, 32, 8, None, bad, None, None,
+                                       None) == 1
 
 
 def test_generator_library_exports():
@@ -88,7 +95,7 @@ def test_generator_library_exports():
 def test_launch_options_layout_and_step_checks():
     """scout_launch as the binding lays it out (two ints, then the event handle), an event that
     does not exist yet refused, and the step's early-start options checked before any device work."""
-    assert ctypes.sizeof(bs.Launch) == 16 and bs.Launch.early_event.offset == 8
+    assert ctypes.sizeof(bs.Launch) == 24 and bs.Launch.early_event.offset == 8 and bs.Launch.inject.offset == 16
     lp = bs._launch(0, early_event=0x1234)
     assert (lp.contents.max_ctas, lp.contents.pdl, lp.contents.early_event) == (0, 0, 0x1234)
     assert bs._launch(None, pdl=True).contents.pdl == 1

@@ -192,3 +192,56 @@ def test_bad_arguments_are_rejected_before_anything_is_written():
     lst[0, 0, 0] = 0
     assert call() == 0
     assert np.all(np.isfinite(Lc))
+
+
+def _random_job(B=4, Hq=40, Hkv=8, nb=96, P=32, k=64, seed=3):
+    """Host inputs of a larger job (no oracle: the pool is compared with the synchronous call)."""
+    rng = np.random.default_rng(seed)
+    bf = lambda a: _bf16((a.astype(np.float32).view(np.uint32) >> 16).astype(np.uint16))  # noqa: E731
+    q = bf(rng.standard_normal((B, Hq, 128)))
+    K = bf(rng.standard_normal((B, Hkv, nb, P, 128)))
+    V = bf(rng.standard_normal((B, Hkv, nb, P, 128)))
+    seq = torch.full((B,), nb * P - 5, dtype=torch.int32)
+    lists = np.sort(np.stack([rng.choice(nb, size=k, replace=False) for _ in range(B * Hkv)]), axis=-1)
+    cnt = torch.from_numpy(rng.integers(k // 2, k + 1, size=(B, Hkv)).astype(np.int32))
+    return q, K, V, seq, torch.from_numpy(lists.astype(np.int32).reshape(B, Hkv, k)), cnt, (B, Hq, Hkv, P, k)
+
+
+@pytest.mark.parametrize("name", sorted(SHAPES))
+def test_pool_gives_the_synchronous_results_bit_for_bit(name):
+    """scout_cpu_attend_async on a caller-owned pool computes exactly what scout_cpu_attend does."""
+    s = SHAPES[name]
+    wl, Kb, Vb, cpu, cnt, _ = _setup(s)
+    O_ref, L_ref = _run(s, wl, Kb, Vb, cpu, cnt)
+    with bs.CpuPool(3) as pool:
+        assert pool.threads == 3
+        for _ in range(2):  # the pool takes job after job
+            O_p = torch.full_like(O_ref, 7.0)
+            L_p = torch.full_like(L_ref, 7.0)
+            pool.submit(_bf16(wl.q), _bf16(Kb), _bf16(Vb), torch.from_numpy(wl.seq_len.astype(np.int32)),
+                        torch.from_numpy(cpu.reshape(s.B, s.Hkv, s.k)), torch.from_numpy(cnt.reshape(s.B, s.Hkv)),
+                        s.B, s.Hq, s.Hkv, s.P, s.k, s.scale, O_p, L_p)
+            assert pool.wait(60.0)
+            assert torch.equal(O_p, O_ref) and torch.equal(L_p, L_ref)
+
+
+def test_late_cpu_partial_is_a_timeout_not_a_stall():
+    """A CPU partial that is not ready within the caller's bound comes back as SCOUT_ERR_TIMEOUT
+    (the pipeline's signal that the CPU side is late); the job goes on, a second submission is
+    refused meanwhile, and a later wait finds the results exact."""
+    q, K, V, seq, lists, cnt, (B, Hq, Hkv, P, k) = _random_job()
+    O_ref, L_ref = bs.cpu_attend(q, K, V, seq, lists, cnt, B, Hq, Hkv, P, k, 0.088, n_threads=2)
+    pool = bs.CpuPool(1)  # one worker: the job takes tens of milliseconds
+    O_p, L_p = torch.zeros_like(O_ref), torch.zeros_like(L_ref)
+    pool.submit(q, K, V, seq, lists, cnt, B, Hq, Hkv, P, k, 0.088, O_p, L_p)
+    L = bs.lib()
+    assert L.scout_cpu_pool_wait(pool._p, 0) == 5  # SCOUT_ERR_TIMEOUT
+    with pytest.raises(bs.ScoutError, match="INVALID_ARG"):
+        pool.submit(q, K, V, seq, lists, cnt, B, Hq, Hkv, P, k, 0.088, O_p, L_p)
+    assert pool.wait(120.0)
+    assert torch.equal(O_p, O_ref) and torch.equal(L_p, L_ref)
+    assert L.scout_cpu_pool_wait(pool._p, -1) == 1  # a negative bound is refused
+    # closing the pool while a job runs waits for it
+    pool.submit(q, K, V, seq, lists, cnt, B, Hq, Hkv, P, k, 0.088, O_p, L_p)
+    pool.close()
+    assert torch.equal(O_p, O_ref)

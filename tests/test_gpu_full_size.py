@@ -141,13 +141,14 @@ def test_same_stream_early_start_changes_no_bit(graph):
         assert np.array_equal(plain[k], early[k]), k
 
 
-STRESS = [(16, 2048, "minmax"), (32, 2048, "minmax"), (64, 2048, "minmax"), (32, 512, "minmax"),
-          (32, 8192, "minmax"), (16, 8192, "mean"), (32, 2048, "mean"), (64, 512, "mean")]
+# every point of the stress sweep: page 16/32/64 x budget 512/2048/8192 tokens x min/max and mean
+STRESS = [(P, budget, kind) for P in (16, 32, 64) for budget in (512, 2048, 8192) for kind in ("minmax", "mean")]
 
 
 @pytest.mark.parametrize("P,budget,kind", STRESS)
 def test_stress_shapes_sampled(P, budget, kind):
-    """B=4 at 128K context: k up to 512 blocks, nblk up to 8192, both digest kinds."""
+    """B=4 at 128K context: k from 8 to 512 blocks, nblk from 2048 to 8192, both digest kinds;
+    three units checked against the oracle, and the list algebra of every unit."""
     s = W.stress(P, budget, kind)
     wl = W.Workload(s)
     d = WD.materialize(wl, with_gemm=False)
@@ -167,11 +168,28 @@ def test_stress_shapes_sampled(P, budget, kind):
     grab = lambda n: out[n].cpu().numpy().reshape(s.units, -1)  # noqa: E731
     cnt = lambda n: out[n].cpu().numpy().reshape(-1)  # noqa: E731
     o_cpu, l_cpu = wl.cpu_partial()
-    for u in (0, s.units - 1):
+    _check_list_algebra(s, wl, grab, cnt)
+    for u in (0, s.units // 2 + 1, s.units - 1):
         b, kvh = divmod(u, s.Hkv)
         _check_unit(wl, u, wl.q[b, kvh * s.G:(kvh + 1) * s.G], kind, grab("topk"), cnt("topk_count"), grab("res"),
                     cnt("res_count"), grab("cpu"), cnt("cpu_count"), O_out.float().cpu().numpy(),
                     L_out.cpu().numpy(), o_cpu, l_cpu)
+
+
+def _check_list_algebra(s, wl, grab, cnt):
+    """Every unit, without the oracle: k_eff entries in ascending order, res and cpu partition the
+    selection by the residency bits, the delta (no previous list) is the cpu list, -1 past the counts."""
+    topk, tc, res, rc, cpu, cc, dl, dc = (grab("topk"), cnt("topk_count"), grab("res"), cnt("res_count"), grab("cpu"),
+                                          cnt("cpu_count"), grab("delta"), cnt("delta_count"))
+    for u in range(s.units):
+        nv = int(wl.nvalid[u // s.Hkv])
+        S = topk[u, :tc[u]]
+        assert tc[u] == min(s.k, nv) and np.all(np.diff(S) > 0) and np.all(topk[u, tc[u]:] == -1), u
+        r, c = res[u, :rc[u]], cpu[u, :cc[u]]
+        assert rc[u] + cc[u] == tc[u] and np.array_equal(np.union1d(r, c), S), u
+        assert np.all(wl.resident[u, r] == 1) and np.all(wl.resident[u, c] == 0), u
+        assert dc[u] == cc[u] and np.array_equal(dl[u, :dc[u]], c), u
+        assert np.all(res[u, rc[u]:] == -1) and np.all(cpu[u, cc[u]:] == -1) and np.all(dl[u, dc[u]:] == -1), u
 
 
 def test_dense_edge_case_at_128k():

@@ -176,12 +176,16 @@ def test_score_topk_parity(name):
                 n = res[key + "_count"][u][0]
                 assert n == len(r[key]) and list(res[key][u][:n]) == list(r[key]), (key, u)
                 assert np.all(res[key][u][n:] == -1)
-        else:  # near-tie: the GPU lists must still split its own selection
+        else:  # near-tie: the GPU lists must still split its own selection, and the delta follow
             Rm = wl.resident[u].astype(bool)
             rr = list(res["res"][u][: res["res_count"][u][0]])
             cc = list(res["cpu"][u][: res["cpu_count"][u][0]])
             assert sorted(rr + cc) == list(S) and rr == sorted(rr) and cc == sorted(cc)
             assert all(Rm[j] for j in rr) and not any(Rm[j] for j in cc)
+            dd = list(res["delta"][u][: res["delta_count"][u][0]])
+            assert dd == [int(j) for j in O.delta_list(cc, pl[u, :pc[u]])], u
+            for key in ("res", "cpu", "delta"):
+                assert np.all(res[key][u][res[key + "_count"][u][0]:] == -1), (key, u)
     assert exact >= s.units - 1
 
 

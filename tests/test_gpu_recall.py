@@ -23,7 +23,8 @@ def _host_bf16(a):
     return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).pin_memory()
 
 
-def test_recall_then_attention_over_the_new_residency():
+def _setup():
+    """A small pool holding the resident blocks, the selection over the full cache, and the plan."""
     s = W.Shape("recall_g4", B=2, Hq=8, Hkv=2, T=3000, P=32, k=12, resident_frac=0.3, seq_lens=(3000, 2050))
     wl = W.Workload(s)
     d = WD.materialize(wl, with_gemm=False)
@@ -64,14 +65,36 @@ def test_recall_then_attention_over_the_new_residency():
     want = [(u, b, sl, e) for u in range(U)
             for b, sl, e in O.recall_plan(sc[u].astype(np.float64), topk[u, :cnt[u]], res[u], table[u])]
     assert [tuple(int(x) for x in r) for r in ops] == want and len(ops) > 0
+    return dict(s=s, wl=wl, d=d, hostK=hostK, hostV=hostV, res=res, table=table, n_slots=n_slots, K_pool=K_pool,
+                V_pool=V_pool, d_table=d_table, d_bits=d_bits, topk=topk, cnt=cnt, ops=ops, want=want)
 
+
+def _snapshot(st):
+    return [t.clone() for t in (st["K_pool"], st["V_pool"], st["d_table"], st["d_bits"])]
+
+
+@pytest.mark.parametrize("mode", ["copies", "gather"])
+def test_recall_then_attention_over_the_new_residency(mode):
+    st = _setup()
+    s, wl, d, hostK, hostV, res, table, n_slots = (st[k] for k in ("s", "wl", "d", "hostK", "hostV", "res", "table",
+                                                                    "n_slots"))
+    K_pool, V_pool, d_table, d_bits, topk, cnt, ops, want = (st[k] for k in ("K_pool", "V_pool", "d_table", "d_bits",
+                                                                             "topk", "cnt", "ops", "want"))
+    U, nb, P = s.units, s.nblk, s.P
     side = torch.cuda.Stream()
     done = torch.cuda.Event()
     hK, hV = _host_bf16(hostK), _host_bf16(hostV)
-    bs.recall_async([tuple(int(x) for x in r) for r in ops], hK, hV, K_pool, V_pool, s.B, s.Hkv, P, nb, side,
-                    done_event=done)
-    bs.commit_residency(to_dev(ops), d_table, d_bits, n_slots, s.B, s.Hkv, wait_event=done)
+    d_ops = to_dev(ops)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    if mode == "copies":
+        bs.recall_async([tuple(int(x) for x in r) for r in ops], hK, hV, K_pool, V_pool, s.B, s.Hkv, P, nb, side,
+                        done_event=done)
+    else:
+        bs.recall_gather_async(d_ops, hK, hV, K_pool, V_pool, s.B, s.Hkv, P, nb, side, done_event=done,
+                               status=status)
+    bs.commit_residency(d_ops, d_table, d_bits, n_slots, s.B, s.Hkv, wait_event=done)
     torch.cuda.synchronize()
+    assert int(status.item()) == 0
 
     # the tables are the oracle's, and every recalled slot holds its block's keys and values
     table2, res2 = table.copy(), res.copy()
@@ -120,3 +143,70 @@ def test_rejected_recall_leaves_pool_and_tables_unchanged():
         bs.recall_async([(0, 1, 0, -1), (0, 2, 5, -1)], hostK, hostV, Kp, Vp, B_, Hkv, P, nb, side)
     torch.cuda.synchronize()
     assert int(Kp.abs().sum().item()) == 0 and int(Vp.abs().sum().item()) == 0
+
+
+def test_recall_copy_refused_midway_leaves_tables_and_evictions_recover():
+    """A copy the runtime refuses midway (an error code injected in place of cudaMemcpyAsync's):
+    the call reports SCOUT_ERR_CUDA, the tables still describe the old residency (nothing is
+    committed), and committing the evictions alone, as the header asks, leaves no block whose
+    slot may have been overwritten looking resident."""
+    st = _setup()
+    s, ops = st["s"], st["ops"]
+    runs = 1 + sum(1 for a, b in zip(ops, ops[1:]) if not (a[0] == b[0] and b[1] == a[1] + 1 and b[2] == a[2] + 1))
+    assert runs >= 2  # the injected refusal hits the second run
+    before = _snapshot(st)
+    side = torch.cuda.Stream()
+    hK, hV = _host_bf16(st["hostK"]), _host_bf16(st["hostV"])
+    with pytest.raises(bs.ScoutError, match="SCOUT_ERR_CUDA"):
+        bs.recall_async([tuple(int(x) for x in r) for r in ops], hK, hV, st["K_pool"], st["V_pool"], s.B, s.Hkv, s.P,
+                        s.nblk, side, inject=bs.INJECT_COPY_FAIL)
+    torch.cuda.synchronize()
+    assert torch.equal(st["d_table"], before[2]) and torch.equal(st["d_bits"], before[3])
+    evict_only = np.array([(u, -1, sl, e) for u, _, sl, e in ops], np.int32)
+    bs.commit_residency(to_dev(evict_only), st["d_table"], st["d_bits"], st["n_slots"], s.B, s.Hkv)
+    torch.cuda.synchronize()
+    U, nb = s.units, s.nblk
+    table = st["table"].copy()
+    res = st["res"].copy()
+    for u, _, _, e in ops:
+        table[u, e], res[u, e] = -1, False
+    assert np.array_equal(st["d_table"].cpu().numpy().reshape(U, nb), table)
+    assert np.array_equal(st["d_bits"].cpu().numpy().view(np.uint32).reshape(U, -1), bits_from_mask(res).reshape(U, -1))
+
+
+def test_recall_gather_refused_enqueues_nothing():
+    """The gather recall is one launch: refused (injected), it leaves the pool and the tables bit for
+    bit as they were; the same recall then succeeds."""
+    st = _setup()
+    s, ops = st["s"], st["ops"]
+    before = _snapshot(st)
+    side = torch.cuda.Stream()
+    hK, hV = _host_bf16(st["hostK"]), _host_bf16(st["hostV"])
+    d_ops = to_dev(ops)
+    with pytest.raises(bs.ScoutError, match="SCOUT_ERR_CUDA"):
+        bs.recall_gather_async(d_ops, hK, hV, st["K_pool"], st["V_pool"], s.B, s.Hkv, s.P, s.nblk, side,
+                               inject=bs.INJECT_COPY_FAIL)
+    torch.cuda.synchronize()
+    for a, b in zip(_snapshot(st), before):
+        assert torch.equal(a, b)
+    done = torch.cuda.Event()
+    bs.recall_gather_async(d_ops, hK, hV, st["K_pool"], st["V_pool"], s.B, s.Hkv, s.P, s.nblk, side, done_event=done)
+    bs.commit_residency(d_ops, st["d_table"], st["d_bits"], st["n_slots"], s.B, s.Hkv, wait_event=done)
+    torch.cuda.synchronize()
+    Kg = st["K_pool"].cpu().view(torch.int16).numpy().view(np.uint16)
+    for u, b, sl, _ in st["want"]:
+        assert np.array_equal(Kg[sl], st["hostK"][u, b])
+
+
+def test_recall_gather_needs_mapped_host_memory():
+    """Pageable host memory is not pinned and mapped: the gather recall refuses it before any launch,
+    whether or not the device could reach it through the host's page tables."""
+    B_, Hkv, P, D, nb = 1, 1, 32, 128, 4
+    Kp = torch.zeros((2, P, D), dtype=torch.bfloat16, device="cuda")
+    hostK = torch.ones((B_, Hkv, nb, P, D), dtype=torch.bfloat16)  # not pinned
+    L = bs.lib()
+    rc = L.scout_recall_gather_async(to_dev(np.array([[0, 1, 0, -1]], np.int32)).data_ptr(), 1, hostK.data_ptr(),
+                                     hostK.data_ptr(), Kp.data_ptr(), Kp.data_ptr(), 2, B_, Hkv, D, P, nb, None, None,
+                                     None, torch.cuda.current_stream().cuda_stream, None)
+    torch.cuda.synchronize()
+    assert rc == 2 and int(Kp.abs().sum().item()) == 0

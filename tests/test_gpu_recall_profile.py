@@ -1,7 +1,7 @@
 """Section 3.4's offline recall-interval profile at the sweep shape (batch 16, 40/8 heads, 64K
 context, k = 64 blocks held per KV head): seeded layers decode without recalls through the
 library, and each layer's interval is the oracle's rule applied to its CPU compute ratio trace.
-(Named to run after the parity suites.)"""
+"""
 import numpy as np
 import pytest
 

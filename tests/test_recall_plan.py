@@ -61,3 +61,17 @@ def test_plan_recall_rejects_bad_input():
     if any(len(O.recall_plan(scores[u].astype(np.float64), topk[u, : cnt[u]], res[u], table[u])) for u in range(2)):
         with pytest.raises(bs.ScoutError):
             bs.plan_recall(scores, topk, cnt, bits, lost, k)
+
+
+def test_planner_shapes_are_checked_before_the_foreign_call():
+    """Arrays whose shapes do not match (units, nblk_cap, k) are refused by the binding before the
+    C planner could read past them."""
+    scores, topk, cnt, bits, table, _, k = _case(5)
+    for bad in (dict(topk=topk[:-1]), dict(topk=topk[:, :-1]), dict(cnt=cnt[:-1]), dict(bits=bits[:, :1]),
+                dict(table=table[:, :-3]), dict(table=table[:-1])):
+        a = dict(scores=scores, topk=topk, cnt=cnt, bits=bits, table=table)
+        a.update(bad)
+        with pytest.raises(bs.ScoutError):
+            bs.plan_recall(a["scores"], a["topk"], a["cnt"], a["bits"], a["table"], k)
+    with pytest.raises(bs.ScoutError):
+        bs.plan_recall_pages(scores, topk, cnt[:-1], bits, table, 3, 2, k)

@@ -30,6 +30,7 @@ def _outputs(s):
         o[name] = torch.full((s.B, s.Hkv, s.k), -7, dtype=torch.int32, device="cuda")
         o[name + "_count"] = torch.full((s.B, s.Hkv), -7, dtype=torch.int32, device="cuda")
     o["scores"] = torch.zeros((s.B, s.Hkv, s.nblk), dtype=torch.float32, device="cuda")
+    o["status"] = torch.zeros(1, dtype=torch.int32, device="cuda")
     return o
 
 
@@ -39,7 +40,7 @@ def _noalloc(s, d, dg, o, prev):
     rc = bs.lib().scout_score_topk_noalloc(
         kind, p(d["q"]), p(dg), p(d["seq_len"]), p(d["resident_bits"]), p(prev[0]), p(prev[1]), s.B, s.Hq, s.Hkv,
         s.D, s.P, s.nblk, s.k, p(o["scores"]), p(o["topk"]), p(o["topk_count"]), p(o["res"]), p(o["res_count"]),
-        p(o["cpu"]), p(o["cpu_count"]), p(o["delta"]), p(o["delta_count"]),
+        p(o["cpu"]), p(o["cpu_count"]), p(o["delta"]), p(o["delta_count"]), p(o["status"]),
         ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
     assert rc == 0, bs.lib().scout_status_string(rc)
 
@@ -67,6 +68,7 @@ def test_noalloc_matches_workspace_entry_point_on_consecutive_calls(s):
         got = _outputs(s)
         _noalloc(s, d, dg, got, (prev_l, prev_c))
         torch.cuda.synchronize()
+        assert int(got["status"].item()) == 0, call
         for key in ("topk", "res", "cpu", "delta", "topk_count", "res_count", "cpu_count", "delta_count"):
             assert torch.equal(got[key], ref[key]), (call, key)
         big = ref["scores"][torch.isfinite(ref["scores"])].abs().max()
@@ -82,5 +84,11 @@ def test_noalloc_rejects_problems_beyond_its_fixed_scratch():
     assert cap == 4 << 20
     # 262,144 x 8 units need 8 MiB of counters: rejected before any launch
     fake = ctypes.c_void_p(256)
-    args = [0, fake, fake, fake, fake, None, None, 262144, 40, 8, 128, 16, 64, 32] + [None] + [fake] * 8 + [None]
+    args = [0, fake, fake, fake, fake, None, None, 262144, 40, 8, 128, 16, 64, 32] + [None] + [fake] * 8 + [None, None]
     assert L.scout_score_topk_noalloc(*args) == 3
+    # 131,072 x 8 units (1,048,576) is the largest problem the array takes; one more sequence is not
+    args[7] = 131073
+    assert L.scout_score_topk_noalloc(*args) == 3
+    # a bad argument is rejected before the shared array is touched (no stream work at all)
+    args[7], args[0] = 4, 7
+    assert L.scout_score_topk_noalloc(*args) == 1
