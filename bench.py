@@ -255,9 +255,10 @@ def isolated(t, step, nbytes, peak, reps=20):
         best = None
         for _ in range(4):
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            a.record(stream)
-            g.replay()
-            b.record(stream)
+            with torch.cuda.stream(stream):  # a graph replays on the current stream
+                a.record(stream)
+                g.replay()
+                b.record(stream)
             b.synchronize()
             ms = a.elapsed_time(b)
             best = ms if best is None else min(best, ms)

@@ -31,10 +31,11 @@ CPU Pre-computation for LLM Inference", arXiv 2603.27138):
 
 Readings where the pages are silent (listed again in the design notes):
 * GQA: query head h reads KV head h // G; one selection per (sequence, KV head),
-  scored by the maximum over the G query heads of the group.
+  scored by the maximum over the G query heads of the group (the sum is a variant).
 * Top-k order: score descending, ties to the lower block index; k_eff =
   min(k, number of valid blocks); lists are returned in ascending block order.
-* The GPU partial attends S intersect R (the resident part of the top-k set).
+* The GPU partial attends S intersect R (the resident part of the top-k set); attending
+  every resident block is a variant (parity unpinned: a reading).
 * LSE is the natural log of sum exp(scale * q.k); partial outputs are normalised;
   an empty set gives O = 0, LSE = -inf.
 * Tokens t >= seq_len are never attended and never enter a digest.
@@ -141,6 +142,13 @@ def scores_mean(q_group, mean) -> np.ndarray:
 def pool_group(u) -> np.ndarray:
     """One score per block for the KV head: the maximum over its G query heads."""
     return np.asarray(u).max(axis=0)
+
+
+def pool_group_sum(u) -> np.ndarray:
+    """The other pooling of a GQA group (a variant; the pages name none): the sum of the block's
+    scores over the G query heads.  For the mean digest it is the group's summed query dotted
+    with the digest; for the min/max bound it bounds the group's summed logit q_sum . k_t."""
+    return np.asarray(u).sum(axis=0)
 
 
 # ---------------------------------------------------------------------------
@@ -294,12 +302,16 @@ def merge(O1, L1, O2, L2):
 # one (sequence, KV head): the whole step  (Algorithm 1, one layer)
 # ---------------------------------------------------------------------------
 def unit_step(q_sel_bits, q_attn_bits, K_bits, V_bits, seq_len: int, P: int, k: int, kind: str,
-              resident_mask, scale: float, prev_cpu=None):
+              resident_mask, scale: float, prev_cpu=None, pool: str = "max", gpu_blocks: str = "selected"):
     """Selection with q_sel (the predicted query), GPU partial with q_attn.
 
     q_sel_bits, q_attn_bits: [G][D] bf16 bits of the group's query heads.
     Returns a dict with scores (pooled, [nvalid]), per-head scores, topk, res,
-    cpu, delta, and per-head GPU partials over S intersect R (O [G][D], L [G]).
+    cpu, delta, and per-head GPU partials (O [G][D], L [G]) over the blocks the GPU
+    attends: S intersect R (``gpu_blocks="selected"``, the reading of section 3.2), or
+    every valid resident block R (``"resident"``, the other reading of Algorithm 1's
+    GPUATTN(Q, B_gpu), a variant; its merge with the CPU partial over S minus R is then
+    attention over R union S).  ``pool``: "max" (default) or "sum" over the group.
     """
     qs = bf16_to_f64(q_sel_bits)
     qa = bf16_to_f64(q_attn_bits)
@@ -310,16 +322,25 @@ def unit_step(q_sel_bits, q_attn_bits, K_bits, V_bits, seq_len: int, P: int, k: 
         u = scores_mean(qs, digest_mean(K_bits, seq_len, P))
     else:
         raise ValueError(kind)
-    U = pool_group(u) if u.shape[1] else np.zeros(0)
+    if pool not in ("max", "sum"):
+        raise ValueError(pool)
+    U = (pool_group(u) if pool == "max" else pool_group_sum(u)) if u.shape[1] else np.zeros(0)
     S = select_topk(U, k)
     res, cpu = split_residency(S, resident_mask)
     delta = delta_list(cpu, prev_cpu if prev_cpu is not None else [])
     K = bf16_to_f64(K_bits)
     V = bf16_to_f64(V_bits)
-    toks = block_tokens(res, P, seq_len)
+    if gpu_blocks == "selected":
+        gpu = res
+    elif gpu_blocks == "resident":
+        nvalid = -(-seq_len // P)
+        gpu = np.flatnonzero(np.asarray(resident_mask, dtype=bool)[:nvalid])
+    else:
+        raise ValueError(gpu_blocks)
+    toks = block_tokens(gpu, P, seq_len)
     G = qa.shape[0]
     O = np.zeros((G, qa.shape[1]))
     L = np.full(G, NEG_INF)
     for h in range(G):
         O[h], L[h] = attention_partial(qa[h], K[toks], V[toks], scale)
-    return dict(scores=U, head_scores=u, topk=S, res=res, cpu=cpu, delta=delta, O=O, L=L)
+    return dict(scores=U, head_scores=u, topk=S, res=res, cpu=cpu, delta=delta, gpu=gpu, O=O, L=L)

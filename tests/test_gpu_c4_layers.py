@@ -76,16 +76,19 @@ def test_forty_layers_sixty_four_steps():
         if t == 0:  # the sampled unit's K/V (host copy = the pool's pages) and its digests
             hK = sw.hK[u].view(torch.int16).numpy().view(np.uint16).reshape(nb * P, D)
             hV = sw.hV[u].view(torch.int16).numpy().view(np.uint16).reshape(nb * P, D)
-            mn, mx = O.digest_minmax(hK, L, P)
+            mn, mx = np.zeros((nb, D)), np.zeros((nb, D))  # rows past the valid blocks are never read
+            v = -(-L // P)
+            mn[:v], mx[:v] = O.digest_minmax(hK, L, P)
             state = dict(K=O.bf16_to_f64(hK), V=O.bf16_to_f64(hV), Kbits=hK, mn=mn, mx=mx)
-        else:  # the appended token changes the tail block's digest only
+        else:  # the appended token changes the tail block's digest only (it may start a new block)
             j = (L - 1) // P
             tmn, tmx = O.digest_minmax(state["Kbits"][j * P:(j + 1) * P], L - j * P, P)
             state["mn"][j], state["mx"][j] = tmn[0], tmx[0]
         per_layer.setdefault(layer, []).append(rec["stats"])
         if t in CHECKED:
-            Uref = O.pool_group(O.scores_minmax(O.bf16_to_f64(sw.ps[t][b, kvh * G:(kvh + 1) * G]), state["mn"],
-                                                state["mx"]))
+            v = -(-L // P)
+            Uref = O.pool_group(O.scores_minmax(O.bf16_to_f64(sw.ps[t][b, kvh * G:(kvh + 1) * G]), state["mn"][:v],
+                                                state["mx"][:v]))
             S = rec["topk"][u, :rec["topk_count"][u]]
             check_selection(Uref, s.k, S, what=(layer, t, u))
             r_ref, _ = O.split_residency(S, rec["resident"][u])

@@ -205,6 +205,31 @@ def test_pool_group_takes_max_over_heads():
     assert np.array_equal(O.pool_group(u), np.array([3.0, 5.0, -1.0]))
 
 
+def test_sum_pooling_is_the_summed_query_against_the_digest():
+    """Sum pooling (a variant): for the mean digest, linearity makes it the group's summed query
+    dotted with each block's mean key; for one-token blocks the min/max bound is tight, so it is
+    the summed query's logit exactly; with one head it equals max pooling."""
+    rng = np.random.default_rng(21)
+    G, D, P, T = 3, 8, 4, 22
+    K = W.f32_to_bf16(rng.integers(-4, 5, size=(T, D)).astype(np.float32))
+    q = W.f32_to_bf16(rng.integers(-3, 4, size=(G, D)).astype(np.float32))
+    Kf, qf = O.bf16_to_f64(K), O.bf16_to_f64(q)
+    mean = O.digest_mean(K, T, P)
+    U = O.pool_group_sum(O.scores_mean(qf, mean))
+    for j in range(len(U)):
+        rows = Kf[j * P:min(T, (j + 1) * P)]
+        assert U[j] == pytest.approx(float(qf.sum(axis=0) @ rows.mean(axis=0)), abs=1e-12)
+    mn, mx = O.digest_minmax(K, T, 1)  # one token per block
+    assert np.array_equal(O.pool_group_sum(O.scores_minmax(qf, mn, mx)), Kf @ qf.sum(axis=0))
+    one = O.scores_minmax(qf[:1], mn, mx)
+    assert np.array_equal(O.pool_group_sum(one), O.pool_group(one))
+    # and the bound: the summed logit of every token of a block is at most the block's sum-pooled score
+    mn, mx = O.digest_minmax(K, T, P)
+    Us = O.pool_group_sum(O.scores_minmax(qf, mn, mx))
+    for t in range(T):
+        assert float(Kf[t] @ qf.sum(axis=0)) <= Us[t // P] + 1e-12
+
+
 # ---------------------------------------------------------------------------
 # top-k (Algorithm 1: B_pred = TopK(...)), ties to the lower block index
 # ---------------------------------------------------------------------------
@@ -365,6 +390,41 @@ def test_gpu_plus_cpu_partials_merge_to_attention_over_topk():
         logits = 0.25 * (Kf[ts] @ qf[h])
         assert np.allclose(o, scipy.special.softmax(logits) @ Vf[ts], atol=1e-12)
         assert l == pytest.approx(float(scipy.special.logsumexp(logits)), abs=1e-12)
+
+
+def test_all_resident_variant_merges_to_attention_over_resident_and_selected():
+    """The variant where the GPU attends every resident block: its partial merged with the CPU
+    partial over S minus R is softmax attention over R union S (computed here directly); with
+    R inside S it is the main reading's result; sum pooling picks the blocks of the summed query."""
+    rng = np.random.default_rng(15)
+    G, D, P, T, k = 2, 16, 4, 62, 5
+    K = W.f32_to_bf16(rng.standard_normal((T, D)).astype(np.float32))
+    V = W.f32_to_bf16(rng.standard_normal((T, D)).astype(np.float32))
+    q = W.f32_to_bf16(rng.standard_normal((G, D)).astype(np.float32))
+    Kf, Vf, qf = O.bf16_to_f64(K), O.bf16_to_f64(V), O.bf16_to_f64(q)
+    nb = -(-T // P)
+    R = rng.random(nb) < 0.4
+    for pool in ("max", "sum"):
+        r = O.unit_step(q, q, K, V, T, P, k, "minmax", R, 0.25, pool=pool, gpu_blocks="resident")
+        assert list(r["gpu"]) == list(np.flatnonzero(R))
+        union = sorted(set(np.flatnonzero(R)) | set(int(j) for j in r["topk"]))
+        tu, tc = O.block_tokens(union, P, T), O.block_tokens(r["cpu"], P, T)
+        for h in range(G):
+            o, l = O.merge(r["O"][h], r["L"][h], *O.attention_partial(qf[h], Kf[tc], Vf[tc], 0.25))
+            logits = 0.25 * (Kf[tu] @ qf[h])
+            assert np.allclose(o, scipy.special.softmax(logits) @ Vf[tu], atol=1e-12)
+            assert l == pytest.approx(float(scipy.special.logsumexp(logits)), abs=1e-12)
+        mn, mx = O.digest_minmax(K, T, P)
+        sc = O.scores_minmax(qf, mn, mx)
+        want = sc.max(axis=0) if pool == "max" else sc.sum(axis=0)
+        assert list(r["topk"]) == sorted(np.argsort(-want, kind="stable")[:k])
+    # R inside S: both readings attend the same blocks
+    r0 = O.unit_step(q, q, K, V, T, P, k, "minmax", np.zeros(nb, bool), 0.25)
+    Rin = np.zeros(nb, bool)
+    Rin[r0["topk"][:2]] = True
+    a = O.unit_step(q, q, K, V, T, P, k, "minmax", Rin, 0.25)
+    b = O.unit_step(q, q, K, V, T, P, k, "minmax", Rin, 0.25, gpu_blocks="resident")
+    assert np.array_equal(a["O"], b["O"]) and np.array_equal(a["L"], b["L"])
 
 
 # ---------------------------------------------------------------------------
