@@ -16,11 +16,13 @@ __all__ = [
     "ScoutError", "lib", "MINMAX", "MEAN", "predict_q", "build_digest", "score_topk", "score_topk_workspace",
     "sparse_attn", "sparse_attn_merge", "sparse_attn_workspace", "merge", "recall_async", "commit_residency",
     "plan_recall", "plan_recall_pages", "recall_intervals", "cpu_attend", "RecallOp", "Launch", "Prepared",
-    "INJECT_NONE", "INJECT_ABANDON", "INJECT_COPY_FAIL", "recall_gather_async", "CpuPool",
+    "INJECT_NONE", "INJECT_ABANDON", "INJECT_COPY_FAIL", "recall_gather_async", "CpuPool", "resident_list",
+    "POOL_SUM",
 ]
 
 MINMAX = 0
 MEAN = 1
+POOL_SUM = 0x10  # OR-ed into the kind: the group's scores summed instead of their maximum
 _KIND = {"minmax": MINMAX, "mean": MEAN, MINMAX: MINMAX, MEAN: MEAN}
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -65,6 +67,7 @@ _SIGS = {
     "scout_plan_recall": ([_p, _p, _p, _p, _p, _i, _i, _i, _p, _i, _p], _i),
     "scout_cpu_attend": ([_p, _p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _i, _f, _p, _p, _i], _i),
     "scout_recall_intervals": ([_p, _i, _i, _f, _p], _i),
+    "scout_resident_list": ([_p, _p, _i, _i, _i, _i, _i, _p, _p, _p, _p], _i),
     "scout_cpu_pool_create": ([_i], _p),
     "scout_cpu_pool_threads": ([_p], _i),
     "scout_cpu_pool_destroy": ([_p], None),
@@ -182,15 +185,19 @@ def score_topk_workspace(B, Hkv, nblk_cap, device="cuda") -> torch.Tensor:
 
 
 def score_topk(kind, q, digest, seq_len, resident_bits, B, Hq, Hkv, P, nblk_cap, k, workspace, out=None,
-               prev_cpu=None, scores=None, status=None, max_ctas=None, inject=INJECT_NONE, stream=None) -> dict:
+               prev_cpu=None, scores=None, status=None, max_ctas=None, inject=INJECT_NONE, pool="max",
+               stream=None) -> dict:
     """Score digests, select top-k per unit, split by residency.
 
     ``out`` (optional) is a dict of preallocated outputs with the keys returned.
     ``prev_cpu`` is an optional (list, count) pair from the previous step.
     ``status`` (optional int32 device tensor) receives SCOUT_DEV_TIMEOUT (2) if a bounded wait
-    expired.  ``inject`` is a test hook (INJECT_ABANDON).
+    expired.  ``inject`` is a test hook (INJECT_ABANDON).  ``pool``: "max" (the group's scores
+    pooled by their maximum) or "sum".
     """
     kind = _KIND[kind]
+    if pool not in ("max", "sum"):
+        raise ScoutError(f"pool must be 'max' or 'sum', got {pool!r}")
     dev = q.device
     U = B * Hkv
     if out is None:
@@ -201,7 +208,7 @@ def score_topk(kind, q, digest, seq_len, resident_bits, B, Hq, Hkv, P, nblk_cap,
     pl, pc = (None, None) if prev_cpu is None else prev_cpu
     ddt = torch.bfloat16 if kind == MINMAX else torch.float32
     _check(lib().scout_score_topk(
-        kind, _dev(q, torch.bfloat16, "q"), _dev(digest, ddt, "digest"), _dev(seq_len, torch.int32, "seq_len"),
+        kind | (POOL_SUM if pool == "sum" else 0), _dev(q, torch.bfloat16, "q"), _dev(digest, ddt, "digest"), _dev(seq_len, torch.int32, "seq_len"),
         _dev(resident_bits, torch.int32, "resident_bits"), _opt(pl, torch.int32, "prev_cpu_list"),
         _opt(pc, torch.int32, "prev_cpu_count"), B, Hq, Hkv, q.shape[-1], P, nblk_cap, k,
         _opt(scores, torch.float32, "scores"),
@@ -215,6 +222,19 @@ def score_topk(kind, q, digest, seq_len, resident_bits, B, Hq, Hkv, P, nblk_cap,
         out["scores"] = scores
     del U
     return out
+
+
+def resident_list(resident_bits, seq_len, B, Hkv, P, nblk_cap, cap, out=None, status=None, stream=None):
+    """Every valid resident block of each unit, ascending -> (list int32 [B][Hkv][cap], count
+    int32 [B][Hkv]); the GPU's blocks under the "all resident blocks" reading."""
+    dev = resident_bits.device
+    lst, cnt = out if out is not None else (torch.empty((B, Hkv, cap), dtype=torch.int32, device=dev),
+                                            torch.empty((B, Hkv), dtype=torch.int32, device=dev))
+    _check(lib().scout_resident_list(_dev(resident_bits, torch.int32, "resident_bits"),
+                                     _dev(seq_len, torch.int32, "seq_len"), B, Hkv, P, nblk_cap, cap,
+                                     _dev(lst, torch.int32, "list"), _dev(cnt, torch.int32, "count"),
+                                     _opt(status, torch.int32, "status"), _stream(stream)), "scout_resident_list")
+    return lst, cnt
 
 
 def sparse_attn_workspace(B, Hq, Hkv, P, D=128, device="cuda") -> torch.Tensor:

@@ -23,7 +23,7 @@ CFLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler",
 LIBS = {
     "libscout.so": [os.path.join(PKG, "csrc", f) for f in
                     ("api.cu", "digest.cu", "score_topk.cu", "sparse_attn.cu", "merge.cu", "predict_q.cu",
-                     "recall.cu", "cpu_attend.cpp")],
+                     "recall.cu", "lists.cu", "cpu_attend.cpp")],
     "libscoutgen.so": [os.path.join(PKG, "workload", "gen.cu")],
 }
 

@@ -451,7 +451,9 @@ __device__ void select_unit(const TopkArgs& a, int u, const uint32_t* keys, int 
   }
 }
 
-template <int KIND>
+// KIND: the digest (min/max bound or mean); SUM: the block score of a unit is the sum of its
+// query heads' scores instead of their maximum.
+template <int KIND, bool SUM>
 __global__ void __launch_bounds__(kThreadsAll, 1) score_topk_kernel(const __grid_constant__ CUtensorMap tmD,
                                                                     const TopkArgs a) {
   extern __shared__ uint8_t smem_raw[];
@@ -633,14 +635,25 @@ __global__ void __launch_bounds__(kThreadsAll, 1) score_topk_kernel(const __grid
     if (j0 < a.nblk_cap) {
       float c[4] = {0.f, 0.f, 0.f, 0.f};
       if (j0 < nvalid) score_tile<KIND>(smem_u32(sp), warp * 16, lane, bmm, bme, c);
-      // pool over the heads of the group (columns 2t, 2t+1 < G), then across t
+      // pool over the heads of the group (columns 2t, 2t+1 < G), then across t; for the sum the
+      // order is ((h0 + h1) + (h2 + h3)) + ((h4 + h5) + (h6 + h7)), the same on every lane
       const float ninf = -INFINITY;
-      float m0 = fmaxf(2 * t < a.G ? c[0] : ninf, 2 * t + 1 < a.G ? c[1] : ninf);
-      float m1 = fmaxf(2 * t < a.G ? c[2] : ninf, 2 * t + 1 < a.G ? c[3] : ninf);
-      m0 = fmaxf(m0, __shfl_xor_sync(0xffffffffu, m0, 1));
-      m0 = fmaxf(m0, __shfl_xor_sync(0xffffffffu, m0, 2));
-      m1 = fmaxf(m1, __shfl_xor_sync(0xffffffffu, m1, 1));
-      m1 = fmaxf(m1, __shfl_xor_sync(0xffffffffu, m1, 2));
+      float m0, m1;
+      if (SUM) {
+        m0 = (2 * t < a.G ? c[0] : 0.f) + (2 * t + 1 < a.G ? c[1] : 0.f);
+        m1 = (2 * t < a.G ? c[2] : 0.f) + (2 * t + 1 < a.G ? c[3] : 0.f);
+        m0 += __shfl_xor_sync(0xffffffffu, m0, 1);
+        m0 += __shfl_xor_sync(0xffffffffu, m0, 2);
+        m1 += __shfl_xor_sync(0xffffffffu, m1, 1);
+        m1 += __shfl_xor_sync(0xffffffffu, m1, 2);
+      } else {
+        m0 = fmaxf(2 * t < a.G ? c[0] : ninf, 2 * t + 1 < a.G ? c[1] : ninf);
+        m1 = fmaxf(2 * t < a.G ? c[2] : ninf, 2 * t + 1 < a.G ? c[3] : ninf);
+        m0 = fmaxf(m0, __shfl_xor_sync(0xffffffffu, m0, 1));
+        m0 = fmaxf(m0, __shfl_xor_sync(0xffffffffu, m0, 2));
+        m1 = fmaxf(m1, __shfl_xor_sync(0xffffffffu, m1, 1));
+        m1 = fmaxf(m1, __shfl_xor_sync(0xffffffffu, m1, 2));
+      }
       if (t == 0) {
         const int r0 = j0 + g, r1 = j0 + g + 8;
         uint32_t* keys = keybuf + kb * align4(a.nblk_cap);
@@ -701,6 +714,7 @@ int check_topk_args(int kind, const void* q, const void* digest, const int32_t* 
   if (launch != nullptr && (launch->max_ctas < 0 || launch->inject < SCOUT_INJECT_NONE ||
                             launch->inject > SCOUT_INJECT_ABANDON))
     return SCOUT_ERR_INVALID_ARG;
+  kind &= ~SCOUT_POOL_SUM;
   if (kind != SCOUT_DIGEST_MINMAX && kind != SCOUT_DIGEST_MEAN) return SCOUT_ERR_INVALID_ARG;
   if (B <= 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || nblk_cap <= 0 || k <= 0) return SCOUT_ERR_INVALID_ARG;
   const int G = Hq / Hkv;
@@ -735,6 +749,8 @@ int score_topk_entry(int kind, const void* q, const void* digest, const int32_t*
   if (rc != SCOUT_OK) return rc;
   if (workspace == nullptr || workspace_bytes < scout_score_topk_workspace_bytes(B, Hkv, nblk_cap))
     return SCOUT_ERR_WORKSPACE;
+  const bool sum_pool = (kind & SCOUT_POOL_SUM) != 0;
+  kind &= ~SCOUT_POOL_SUM;
   const int G = Hq / Hkv;
   const int64_t units = (int64_t)B * Hkv;
   TopkArgs a;
@@ -797,11 +813,20 @@ int score_topk_entry(int kind, const void* q, const void* digest, const int32_t*
   if (a.stages == 0) return SCOUT_ERR_UNSUPPORTED;
   a.nsel = min(kSelWarps, a.nkbuf - 1);
   const size_t smem = 1024 + need(a.stages, a.nkbuf);
-  auto kern = kind == SCOUT_DIGEST_MINMAX ? score_topk_kernel<SCOUT_DIGEST_MINMAX> : score_topk_kernel<SCOUT_DIGEST_MEAN>;
+  auto kern = kind == SCOUT_DIGEST_MINMAX
+                  ? (sum_pool ? score_topk_kernel<SCOUT_DIGEST_MINMAX, true> : score_topk_kernel<SCOUT_DIGEST_MINMAX, false>)
+                  : (sum_pool ? score_topk_kernel<SCOUT_DIGEST_MEAN, true> : score_topk_kernel<SCOUT_DIGEST_MEAN, false>);
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess ||
       cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, 100) != cudaSuccess)
     return SCOUT_ERR_CUDA;
-  const int cap = launch != nullptr && launch->max_ctas > 0 ? launch->max_ctas : sm_count();
+  // Default grid: the fewest CTAs that still take ceil(units / SMs) units each, so that the last
+  // round of units does not leave most SMs idle while a few stream on (320 units on 152 SMs: 107
+  // CTAs of three units rather than 152 CTAs of which 16 take a third).  A cap is taken as given.
+  int cap = launch != nullptr ? launch->max_ctas : 0;
+  if (cap <= 0) {
+    const int64_t sms = sm_count(), rounds = (units + sms - 1) / sms;
+    cap = (int)((units + rounds - 1) / rounds);
+  }
   const int grid = (int)(units < (int64_t)cap ? units : (int64_t)cap);  // <= one CTA per unit
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)grid);

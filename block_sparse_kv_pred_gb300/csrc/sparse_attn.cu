@@ -40,11 +40,16 @@ namespace {
 #define SCOUT_ATTN_SUBPAGE 32
 #endif
 #ifndef SCOUT_ATTN_PAIR
-#define SCOUT_ATTN_PAIR 2
+#define SCOUT_ATTN_PAIR 1
 #endif
+
 constexpr int kConsumerWarps = SCOUT_ATTN_CONSUMERS;
 constexpr int kSubTokens = SCOUT_ATTN_SUBPAGE;
-constexpr int kPair = SCOUT_ATTN_PAIR;  // pages a consumer warp attends in one pass (1 or 2)
+// pages a consumer warp attends in one pass (1 or 2); measured on GB300 in the graph-replayed
+// Qwen3-14B-shaped step: one 59.55 us per step, two 60.35 (with one, a stage holds a page for
+// less time, so more of the ring is loading)
+constexpr int kPair = SCOUT_ATTN_PAIR;
+
 constexpr int kEpilogueWarp = kConsumerWarps;     // combines the warps' states, writes whole units
 constexpr int kSplitWarp = kConsumerWarps + 1;     // merges the units cut by range boundaries
 constexpr int kThreads = (kConsumerWarps + 2) * 32;
@@ -79,6 +84,7 @@ struct Cfg {
   static constexpr int kRingBytes = kStages * kStageBytes;
   static_assert(kStages % kConsumerWarps == 0 && kPhaseB < kPhaseC && kPhaseC < 32 - kPerWarp - 1,
                 "stage ownership and resolution phases");
+
 };
 
 struct AttnArgs {
@@ -398,6 +404,101 @@ __device__ __forceinline__ void store4(const AttnArgs& a, int uu, int h, int lan
   }
 }
 
+// The split warp of a CTA: a unit cut by range boundaries has one piece per CTA range it
+// touches (c0 .. c1).  Each piece (staged in shared memory by the CTA's epilogue, signalled on
+// sbar) is published to the workspace and counted; the piece that completes the count (last
+// to arrive) merges all of them by their LSE.  Nothing waits on another CTA.
+__device__ void run_split_warp(const AttnArgs& a, const int* prefix, int64_t N, int Gp, int c, const float* staging,
+                               uint64_t* sbar, float* sfin, float* swg, float* swc, int lane) {
+  // A unit cut by range boundaries has one piece per CTA range it touches (c0 .. c1).  Each
+  // piece is published to the workspace and counted; the piece that completes the count
+  // (last to arrive) merges all of them by their LSE.  Nothing waits on another CTA.
+  const int64_t start = range_start(c, N, Gp), end = range_start(c + 1, N, Gp);
+  SegIter it = seg_iter(prefix, a.units, range_order(prefix, a.units, start, end));
+  int u, k = 0;
+  int64_t lo, hi;
+  CpuPart cpu;
+  while (it.next(u, lo, hi)) {
+    if (lo == prefix[u] && hi == prefix[u + 1]) continue;  // whole: the epilogue warp's
+    if (k >= kMaxSplit) break;  // a range has at most two cut segments
+    load_cpu(a, u, lane, cpu);  // used only if this piece completes the unit
+    if (!mbar_wait(&sbar[k], 0u) && lane == 0) report(a.status, SCOUT_DEV_TIMEOUT);
+    const float* stg = staging + k * stage_floats(a.G);
+    ++k;
+    const int c0 = cta_of(prefix[u], N, Gp), c1 = cta_of(prefix[u + 1] - 1, N, Gp);
+    auto piece_slot = [&](int cc) {
+      return (int64_t)cc * 2 + (prefix[u] <= range_start(cc, N, Gp) ? 0 : 1);
+    };
+    const int64_t msl = piece_slot(c);
+    if (lane < a.G) a.slot_lse[msl * kMaxG + lane] = stg[lane];
+#pragma unroll
+    for (int h = 0; h < kMaxG; ++h)
+      if (h < a.G)
+        *reinterpret_cast<float4*>(a.slot_O + (msl * kMaxG + h) * kD + 4 * lane) =
+            *reinterpret_cast<const float4*>(stg + kMaxG + h * kD + 4 * lane);
+    __threadfence();
+    __syncwarp();
+    int last = 0;
+    if (lane == 0) last = atomicAdd(&a.counters[u], 1) == c1 - c0;
+    last = __shfl_sync(0xffffffffu, last, 0);
+    if (!last) continue;
+    __threadfence();
+    // merge the pieces by their LSE in one pass (running max per head): every load of a
+    // piece is issued at once, this CTA's own piece comes from shared memory
+    float mx[kMaxG], sm[kMaxG];
+    float4 acc[kMaxG];
+#pragma unroll
+    for (int h = 0; h < kMaxG; ++h) {
+      mx[h] = -INFINITY;
+      sm[h] = 0.f;
+      acc[h] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    for (int cc = c0; cc <= c1; ++cc) {
+      float pl[kMaxG];
+      float4 po[kMaxG];
+      const int64_t sl = piece_slot(cc);
+#pragma unroll
+      for (int h = 0; h < kMaxG; ++h) {
+        if (h >= a.G) continue;
+        if (cc == c) {
+          pl[h] = stg[h];
+          po[h] = *reinterpret_cast<const float4*>(stg + kMaxG + h * kD + 4 * lane);
+        } else {
+          pl[h] = __ldcg(a.slot_lse + sl * kMaxG + h);
+          po[h] = __ldcg(reinterpret_cast<const float4*>(a.slot_O + (sl * kMaxG + h) * kD + 4 * lane));
+        }
+      }
+#pragma unroll
+      for (int h = 0; h < kMaxG; ++h) {
+        if (h >= a.G || pl[h] == -INFINITY) continue;  // a piece without tokens weighs nothing
+        const float nm = fmaxf(mx[h], pl[h]);
+        const float keep = mx[h] == -INFINITY ? 0.f : expf(mx[h] - nm), w = expf(pl[h] - nm);
+        acc[h].x = acc[h].x * keep + w * po[h].x;
+        acc[h].y = acc[h].y * keep + w * po[h].y;
+        acc[h].z = acc[h].z * keep + w * po[h].z;
+        acc[h].w = acc[h].w * keep + w * po[h].w;
+        sm[h] = sm[h] * keep + w;
+        mx[h] = nm;
+      }
+    }
+    float fin = -INFINITY;
+#pragma unroll
+    for (int h = 0; h < kMaxG; ++h)
+      if (h == lane && sm[h] > 0.f) fin = mx[h] + logf(sm[h]);
+    if (lane < a.G) sfin[lane] = fin;
+    __syncwarp();
+    unit_final(a, u, lane, sfin, swg, swc, cpu);
+#pragma unroll
+    for (int h = 0; h < kMaxG; ++h) {
+      if (h >= a.G) continue;
+      const float r = sm[h] > 0.f ? 1.f / sm[h] : 0.f;
+      store4(a, u, h, lane, make_float4(acc[h].x * r, acc[h].y * r, acc[h].z * r, acc[h].w * r), swg, swc, cpu);
+    }
+    __syncwarp();
+    if (lane == 0) a.counters[u] = 0;  // ready for the next call
+  }
+}
+
 template <int P, int S>
 __global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const __grid_constant__ CUtensorMap tmK,
                                                                   const __grid_constant__ CUtensorMap tmV,
@@ -553,95 +654,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const __grid_c
   }
 
   if (warp == kSplitWarp) {
-    // ---------------- split warp -----------------------------------------------
-    // A unit cut by range boundaries has one piece per CTA range it touches (c0 .. c1).  Each
-    // piece is published to the workspace and counted; the piece that completes the count
-    // (last to arrive) merges all of them by their LSE.  Nothing waits on another CTA.
-    if (c >= Gp) return;
-    const int64_t start = range_start(c, N, Gp), end = range_start(c + 1, N, Gp);
-    SegIter it = seg_iter(prefix, a.units, range_order(prefix, a.units, start, end));
-    int u, k = 0;
-    int64_t lo, hi;
-    CpuPart cpu;
-    while (it.next(u, lo, hi)) {
-      if (lo == prefix[u] && hi == prefix[u + 1]) continue;  // whole: the epilogue warp's
-      if (k >= kMaxSplit) break;  // a range has at most two cut segments
-      load_cpu(a, u, lane, cpu);  // used only if this piece completes the unit
-      if (!mbar_wait(&sbar[k], 0u) && lane == 0) report(a.status, SCOUT_DEV_TIMEOUT);
-      const float* stg = staging + k * stage_floats(a.G);
-      ++k;
-      const int c0 = cta_of(prefix[u], N, Gp), c1 = cta_of(prefix[u + 1] - 1, N, Gp);
-      auto piece_slot = [&](int cc) {
-        return (int64_t)cc * 2 + (prefix[u] <= range_start(cc, N, Gp) ? 0 : 1);
-      };
-      const int64_t msl = piece_slot(c);
-      if (lane < a.G) a.slot_lse[msl * kMaxG + lane] = stg[lane];
-#pragma unroll
-      for (int h = 0; h < kMaxG; ++h)
-        if (h < a.G)
-          *reinterpret_cast<float4*>(a.slot_O + (msl * kMaxG + h) * kD + 4 * lane) =
-              *reinterpret_cast<const float4*>(stg + kMaxG + h * kD + 4 * lane);
-      __threadfence();
-      __syncwarp();
-      int last = 0;
-      if (lane == 0) last = atomicAdd(&a.counters[u], 1) == c1 - c0;
-      last = __shfl_sync(0xffffffffu, last, 0);
-      if (!last) continue;
-      __threadfence();
-      // merge the pieces by their LSE in one pass (running max per head): every load of a
-      // piece is issued at once, this CTA's own piece comes from shared memory
-      float mx[kMaxG], sm[kMaxG];
-      float4 acc[kMaxG];
-#pragma unroll
-      for (int h = 0; h < kMaxG; ++h) {
-        mx[h] = -INFINITY;
-        sm[h] = 0.f;
-        acc[h] = make_float4(0.f, 0.f, 0.f, 0.f);
-      }
-      for (int cc = c0; cc <= c1; ++cc) {
-        float pl[kMaxG];
-        float4 po[kMaxG];
-        const int64_t sl = piece_slot(cc);
-#pragma unroll
-        for (int h = 0; h < kMaxG; ++h) {
-          if (h >= a.G) continue;
-          if (cc == c) {
-            pl[h] = stg[h];
-            po[h] = *reinterpret_cast<const float4*>(stg + kMaxG + h * kD + 4 * lane);
-          } else {
-            pl[h] = __ldcg(a.slot_lse + sl * kMaxG + h);
-            po[h] = __ldcg(reinterpret_cast<const float4*>(a.slot_O + (sl * kMaxG + h) * kD + 4 * lane));
-          }
-        }
-#pragma unroll
-        for (int h = 0; h < kMaxG; ++h) {
-          if (h >= a.G || pl[h] == -INFINITY) continue;  // a piece without tokens weighs nothing
-          const float nm = fmaxf(mx[h], pl[h]);
-          const float keep = mx[h] == -INFINITY ? 0.f : expf(mx[h] - nm), w = expf(pl[h] - nm);
-          acc[h].x = acc[h].x * keep + w * po[h].x;
-          acc[h].y = acc[h].y * keep + w * po[h].y;
-          acc[h].z = acc[h].z * keep + w * po[h].z;
-          acc[h].w = acc[h].w * keep + w * po[h].w;
-          sm[h] = sm[h] * keep + w;
-          mx[h] = nm;
-        }
-      }
-      float fin = -INFINITY;
-#pragma unroll
-      for (int h = 0; h < kMaxG; ++h)
-        if (h == lane && sm[h] > 0.f) fin = mx[h] + logf(sm[h]);
-      if (lane < a.G) sfin[lane] = fin;
-      __syncwarp();
-      unit_final(a, u, lane, sfin, swg, swc, cpu);
-#pragma unroll
-      for (int h = 0; h < kMaxG; ++h) {
-        if (h >= a.G) continue;
-        const float r = sm[h] > 0.f ? 1.f / sm[h] : 0.f;
-        store4(a, u, h, lane, make_float4(acc[h].x * r, acc[h].y * r, acc[h].z * r, acc[h].w * r), swg, swc, cpu);
-      }
-      __syncwarp();
-      if (lane == 0) a.counters[u] = 0;  // ready for the next call
-    }
+    if (c < Gp) run_split_warp(a, prefix, N, Gp, c, staging, sbar, sfin, swg, swc, lane);
     return;
   }
 
@@ -741,6 +754,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const __grid_c
     const int64_t kr = kk + C::kPerWarp + (lane < n ? lane : 0);
     if (lane < n && kr < n_mine) issue(kr, row, nt, which);
   };
+
   for (int r = 0; r < C::kPerWarp && r < n_mine; ++r) {
     const int row = __shfl_sync(0xffffffffu, cur_row, r), nt = __shfl_sync(0xffffffffu, cur_nt, r);
     if (lane == 0) {
@@ -898,6 +912,9 @@ size_t dyn_smem(int units, int G, int nslots) {
          (size_t)kMaxSplit * stage_floats(G) * sizeof(float) + (size_t)(units + 1) * 4;
 }
 constexpr size_t kSmemLimit = 232448 - 1024;  // per-block shared memory minus room for static use
+
+
+
 
 // The pool [n_slots * P rows][128 columns] bf16 seen as a 3-D tensor [2 halves][rows][64
 // columns] (half stride 128 bytes, row stride 256 bytes): one box {64, box_rows, 2} is a whole

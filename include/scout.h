@@ -64,13 +64,19 @@ typedef enum scout_digest_kind {
   SCOUT_DIGEST_MEAN = 1    /* MoBA: channel-wise mean of K over a block */
 } scout_digest_kind;
 
+/* OR-ed into scout_score_topk's kind: pool a GQA group's scores by their sum instead of
+ * their maximum (a variant; the pages do not say how a group's heads share a selection). */
+#define SCOUT_POOL_SUM 0x10
+
 /* Launch options (pass NULL for the defaults).  max_ctas bounds the CTAs a
  * persistent kernel launches (at most one per SM each): kernels of independent
  * work, e.g. the next layer's selection and this layer's attention (Algorithm 1),
  * can then share the SMs from separate streams.  0 means one CTA per SM; a
  * negative value is SCOUT_ERR_INVALID_ARG.  scout_score_topk deals whole units to
- * its CTAs as they start, so with 0 it also takes the SMs other kernels free up
- * while it runs.  For scout_predict_q it bounds the split-K factor S so that
+ * its CTAs as they start, so it also takes the SMs other kernels free up while it
+ * runs; its default (0) is the fewest CTAs that take ceil(units / SMs) units each
+ * (a last round of units then keeps as many SMs streaming as the others).  For
+ * scout_predict_q it bounds the split-K factor S so that
  * (N / 128) * S <= max_ctas; the grid keeps at least one CTA per 128-row tile of W.
  *
  * Early starts (programmatic dependent launch), for scout_predict_q,
@@ -173,7 +179,9 @@ int scout_build_digest(int kind, const void* K_pool, int64_t n_slots, const int3
  * Score of block j for query head h:  MINMAX  sum_c max(q_hc min_jc, q_hc max_jc)
  *                                     MEAN    sum_c q_hc mean_jc
  * One selection per unit: the block score is the maximum over the G query
- * heads of the unit.  Valid blocks are j < ceil(seq_len[b] / P).
+ * heads of the unit (with kind | SCOUT_POOL_SUM: their sum, added in the order
+ * ((h0 + h1) + (h2 + h3)) + ((h4 + h5) + (h6 + h7)) in fp32).  Valid blocks are
+ * j < ceil(seq_len[b] / P).
  * Top-k: k_eff = min(k, valid blocks) blocks by (score desc, index asc).
  *
  * q            bf16 [B][Hq][D]   (query head hq belongs to KV head hq / G)
@@ -239,6 +247,23 @@ int scout_score_topk_noalloc(int kind, const void* q, const void* digest, const 
                              int k, float* scores, int32_t* topk_idx, int32_t* topk_count, int32_t* res_list,
                              int32_t* res_count, int32_t* cpu_list, int32_t* cpu_count, int32_t* delta_list,
                              int32_t* delta_count, int32_t* dev_status, cudaStream_t stream);
+
+/* ------------------------------------------------------------------------ *
+ * List of every resident block (a variant of which blocks the GPU attends).
+ * ScoutAttention (arXiv HTML), Algorithm 1 writes the GPU's share as
+ * GPUATTN(Q, B_gpu), which can be read as all the blocks in GPU memory rather than
+ * the selected ones among them (section 3.2).  This builds that list, so that
+ * scout_sparse_attn(_merge) can attend it: per unit, the valid blocks
+ * j < ceil(seq_len[b] / P) whose residency bit is set, ascending.
+ *
+ * resident_bits uint32 [B][Hkv][ceil(nblk_cap/32)], seq_len int32 [B];
+ * list int32 [B][Hkv][cap] (entries past the count set to -1), count int32
+ * [B][Hkv].  A unit with more than cap such blocks gets its first cap of them and
+ * SCOUT_DEV_OVERFLOW in dev_status (may be NULL).  One warp per unit.
+ * ------------------------------------------------------------------------ */
+#define SCOUT_DEV_OVERFLOW 4
+int scout_resident_list(const uint32_t* resident_bits, const int32_t* seq_len, int B, int Hkv, int P, int nblk_cap,
+                        int cap, int32_t* list, int32_t* count, int32_t* dev_status, cudaStream_t stream);
 
 /* ------------------------------------------------------------------------ *
  * GPU partial attention over the resident selected blocks.
