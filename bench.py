@@ -412,106 +412,34 @@ def cpu_side(s, t, seconds=0.5, max_seqs=8):
 
 
 def layer_ahead(s, t, step, gpu_ms, steps=24, warm=4, limit_s=60.0):
-    """Algorithm 1's pipeline with the CPU side computed for real: after step i's selection its
-    CPU work list and Q_pred go down to the host, where scout_cpu_attend computes the next
-    layer's CPU partial on the host cores (one worker thread driving the library's threads)
-    while the GPU goes on; the partial goes up before step i+1's attention, which waits for it.
-    The single synthetic layer stands for every layer, as in the step.  Host wall time per step
-    against the GPU-only step (graph replay) gives the fraction of the time the GPU would idle.
-    Every wait is bounded and a failure is reported, not raised, so that it cannot cost the
-    GPU measurement."""
-    import concurrent.futures as cf
-
+    """Algorithm 1's pipeline with the CPU side computed for real (``pipeline.LayerAhead``):
+    after step i's selection its CPU work list and Q_pred go down to the host, where the
+    worker pool computes the next layer's CPU partial on the host cores while the GPU goes on;
+    the partial goes up before step i+1's attention, which waits for it.  Host wall time per
+    step against the GPU-only step (graph replay) gives the fraction of the time the GPU would
+    idle.  Every wait is bounded and a failure is reported, not raised, so that it cannot cost
+    the GPU measurement."""
     import torch
 
-    import block_sparse_kv_pred_gb300 as bs
+    from block_sparse_kv_pred_gb300.pipeline import LayerAhead
 
     if step.serial:
         return {"unavailable": "serial step"}
-    pool = cf.ThreadPoolExecutor(1)
     dev = t["Qp0"].device
     try:
-        t_end = time.perf_counter() + limit_s
-        slots = t.get("page_table_all", t["page_table"]).reshape(-1).long()
-        if int(slots.min()) < 0:
-            return {"unavailable": "a block has no pool slot"}
-        # the layer's K/V in logical block order on the host: the copy the CPU side attends
-        hkv = {n: t.get(n + "_all", t[n + "_pool"]).index_select(0, slots).view(s.B, s.Hkv, s.nblk, s.P, s.D).cpu()
-               for n in "KV"}
-        seq = t["seq_len"].cpu().contiguous()
-        threads = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else (os.cpu_count() or 1)
-        st = step.fresh()
-        sB = st.streams[1]
-        sH = torch.cuda.Stream(dev)  # the pipeline's host<->device copies, in issue order
-
-        def pin(x):
-            return torch.empty_like(x, device="cpu").pin_memory()
-
-        h_q = [pin(t[f"Qp{p}"]) for p in (0, 1)]
-        h_list = [pin(t[f"cpu{p}"]) for p in (0, 1)]
-        h_cnt = [pin(t[f"cpu_count{p}"]) for p in (0, 1)]
-        h_O = [pin(t["O_cpu0"]) for _ in (0, 1)]
-        h_L = [pin(t["lse_cpu0"]) for _ in (0, 1)]
-        down = [torch.cuda.Event(), torch.cuda.Event()]
-        up = [torch.cuda.Event(), torch.cuda.Event()]
-        cpu_s = []
-
-        def cpu_layer(par):
-            # the next layer's CPU partial from the step of parity par (its list and Q_pred)
-            while not down[par].query():
-                if time.perf_counter() > t_end:
-                    raise TimeoutError("the work list did not reach the host")
-                time.sleep(2e-5)
-            c0 = time.perf_counter()
-            bs.cpu_attend(h_q[par].view(s.B, s.Hq, s.D), hkv["K"], hkv["V"], seq, h_list[par], h_cnt[par], s.B,
-                          s.Hq, s.Hkv, s.P, s.k, s.scale, O_cpu=h_O[1 - par], lse_cpu=h_L[1 - par], n_threads=threads)
-            cpu_s.append(time.perf_counter() - c0)
-            return 1 - par
-
-        ev0 = torch.cuda.Event()
-        ev0.record(torch.cuda.current_stream(dev))
-        st.begin(ev0)
-        sH.wait_event(ev0)
-        pending, t0 = None, None
-        for i in range(warm + steps):
-            if i == warm:
-                t0 = time.perf_counter()
-            par = st.i % 2
-            if pending is not None:
-                if pending.result(timeout=max(0.0, t_end - time.perf_counter())) != par:
-                    raise RuntimeError("pipeline parity")
-                if i >= 2:
-                    sH.wait_event(st.attn_done[par])  # the attention two steps back read this buffer
-                with torch.cuda.stream(sH):
-                    t[f"O_cpu{par}"].copy_(h_O[par], non_blocking=True)
-                    t[f"lse_cpu{par}"].copy_(h_L[par], non_blocking=True)
-                up[par].record(sH)
-                sB.wait_event(up[par])
-            st.issue(after_begin=(i == 0))
-            sH.wait_event(st.sel_done[par])  # the selection (after its GEMM) wrote list set par
-            with torch.cuda.stream(sH):
-                h_q[par].copy_(t[f"Qp{par}"], non_blocking=True)
-                h_list[par].copy_(t[f"cpu{par}"], non_blocking=True)
-                h_cnt[par].copy_(t[f"cpu_count{par}"], non_blocking=True)
-            down[par].record(sH)
-            pending = pool.submit(cpu_layer, par)
-        pending.result(timeout=max(0.0, t_end - time.perf_counter()))
-        st.end(None)
-        torch.cuda.synchronize(dev)
-        ms = (time.perf_counter() - t0) / steps * 1e3
-        cpu_ms = statistics.mean(cpu_s[warm:]) * 1e3 if len(cpu_s) > warm else None
-        if int(t["status"].item()) != 0:
-            return {"unavailable": f"device status {int(t['status'].item())}"}
+        with LayerAhead(s, t, step, timeout_s=limit_s) as la:
+            r = la.run(steps, warm)
+        ms = r["ms_per_step"]
         return {"ms_per_step": ms, "value": s.B * s.Hq / (ms / 1e3), "unit": "query-heads/s",
-                "cpu_ms_per_layer": cpu_ms, "gpu_step_ms": gpu_ms, "gpu_idle_frac": max(0.0, 1.0 - gpu_ms / ms),
-                "threads": threads, "steps": steps,
+                "cpu_ms_per_layer": r["cpu_ms_per_layer"], "host_wait_ms_per_step": r["host_wait_ms"],
+                "gpu_step_ms": gpu_ms, "gpu_idle_frac": max(0.0, 1.0 - gpu_ms / ms), "threads": r["threads"],
+                "steps": steps,
                 "note": "the step issued on its streams (not graph-replayed), the CPU partial of every step "
-                        "computed by scout_cpu_attend from the previous step's work list; gpu_idle_frac compares "
-                        "the graph-replayed GPU-only step with this wall time"}
+                        "computed by the worker pool (scout_cpu_pool) from the previous step's work list; "
+                        "gpu_idle_frac compares the graph-replayed GPU-only step with this wall time"}
     except Exception as e:  # noqa: BLE001
         return {"unavailable": f"{type(e).__name__}: {e}"[:300]}
     finally:
-        pool.shutdown(wait=False)
         try:
             torch.cuda.synchronize(dev)
         except Exception:  # noqa: BLE001  (already reported above)
@@ -524,7 +452,9 @@ def layer_ahead(s, t, step, gpu_ms, steps=24, warm=4, limit_s=60.0):
 class OracleSample:
     """The fp64 oracle's version of one step, on a few (sequence, KV head) units."""
 
-    def __init__(self, shape, n_units=8):
+    STAGES = ("build_digest", "predict_q", "score_topk", "sparse_attn", "merge")
+
+    def __init__(self, shape, n_units=8, seed=1):
         import numpy as np
 
         import oracle as O
@@ -533,7 +463,7 @@ class OracleSample:
         self.O, self.np = O, np
         s = self.s = shape
         wl = self.wl = W.Workload(s)
-        rng = np.random.default_rng(1)
+        rng = np.random.default_rng(seed)
         self.units = sorted(int(u) for u in rng.choice(s.units, size=min(n_units, s.units), replace=False))
         X = wl.gemm_x()
         o_cpu, l_cpu = wl.cpu_partial()
@@ -550,38 +480,78 @@ class OracleSample:
                                   prev=[]))
         self.i = 0
 
-    def step(self):
-        """One unit: tail digest, Q_pred rows, scores, top-k, split, GPU-side attention, merge."""
+    def step(self, timer=None):
+        """One unit: tail digest, Q_pred rows, scores, top-k, split, GPU-side attention, merge.
+        ``timer``: optional dict stage -> seconds, to which each stage's time is added."""
         O, s = self.O, self.s
         d = self.data[self.i % len(self.data)]
         self.i += 1
+        t0 = time.perf_counter()
         j = -(-d["L"] // s.P) - 1
         tmn, tmx = O.digest_minmax(d["K"][j * s.P:], d["L"] - j * s.P, s.P)
         d["mn"][j], d["mx"][j] = tmn[0], tmx[0]
+        t1 = time.perf_counter()
         qp = O.f64_to_bf16(O.predict_q(d["X"], d["Wr"])).reshape(s.G, s.D)
+        t2 = time.perf_counter()
         U = O.pool_group(O.scores_minmax(O.bf16_to_f64(qp), d["mn"], d["mx"]))
         S = O.select_topk(U, s.k)
         res, cpu = O.split_residency(S, self.wl.resident[d["u"]])
         O.delta_list(cpu, d["prev"])
         d["prev"] = cpu
+        t3 = time.perf_counter()
         toks = O.block_tokens(res, s.P, d["L"])
         qa = O.bf16_to_f64(d["q"])
-        for h in range(s.G):
-            o, l = O.attention_partial(qa[h], d["Kf"][toks], d["Vf"][toks], s.scale)
+        parts = [O.attention_partial(qa[h], d["Kf"][toks], d["Vf"][toks], s.scale) for h in range(s.G)]
+        t4 = time.perf_counter()
+        for h, (o, l) in enumerate(parts):
             O.merge(o, l, d["ocpu"][h].astype("float64"), float(d["lcpu"][h]))
+        t5 = time.perf_counter()
+        if timer is not None:
+            for name, dt in zip(self.STAGES, (t1 - t0, t2 - t1, t3 - t2, t4 - t3, t5 - t4)):
+                timer[name] = timer.get(name, 0.0) + dt
         return s.G  # query heads processed
 
 
-def cpu_baseline(shape, seconds):
-    smp = OracleSample(shape)
+def _oracle_worker(job):
+    """One process of the all-cores oracle timing: its own units, its own timing loop."""
+    shape, seed, seconds = job
+    smp = OracleSample(shape, n_units=2, seed=seed)
     smp.step()
     heads, t0 = 0, time.perf_counter()
     while time.perf_counter() - t0 < seconds:
         heads += smp.step()
+    return heads, time.perf_counter() - t0
+
+
+def cpu_baseline(shape, seconds, all_cores=True):
+    """The oracle on the host cores: one thread with each stage timed, then (``all_cores``) one
+    process per core over different sampled units at once (started with spawn: this process
+    has used the GPU).  The value is the single-thread rate; the all-cores rate sits beside it."""
+    smp = OracleSample(shape)
+    smp.step()
+    heads, timer, t0 = 0, {}, time.perf_counter()
+    while time.perf_counter() - t0 < seconds:
+        heads += smp.step(timer)
     el = time.perf_counter() - t0
-    return {"value": heads / el, "unit": "query-heads/s", "cores": 1, "kind": "oracle",
-            "sample": f"{len(smp.units)} of {shape.units} (sequence, KV head) units of {shape.name}, "
-                      f"{smp.i - 1} unit-steps in {el:.1f} s, single thread (BLAS/OpenMP pinned to 1)"}
+    n = smp.i - 1
+    out = {"value": heads / el, "unit": "query-heads/s", "cores": 1, "kind": "oracle",
+           "sample": f"{len(smp.units)} of {shape.units} (sequence, KV head) units of {shape.name}, "
+                     f"{n} unit-steps in {el:.1f} s, single thread (BLAS/OpenMP pinned to 1)",
+           "stages_ms_per_unit_step": {k: v / n * 1e3 for k, v in timer.items()}}
+    if all_cores:
+        import multiprocessing as mp
+
+        cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else (os.cpu_count() or 1)
+        try:
+            with mp.get_context("spawn").Pool(cores) as pool:
+                res = pool.map(_oracle_worker, [(shape, 100 + i, seconds / 2) for i in range(cores)])
+            out["all_cores"] = {"value": sum(h / e for h, e in res), "unit": "query-heads/s", "cores": cores,
+                                "processes": cores,
+                                "sample": f"one process per core, each on 2 sampled units of {shape.name} for "
+                                          f"{seconds / 2:.1f} s (rates summed)"}
+        except Exception as e:  # noqa: BLE001
+            out["all_cores"] = {"unavailable": f"{type(e).__name__}: {e}"[:300]}
+    return out
 
 
 def run_reference(args, rank, world):

@@ -66,6 +66,7 @@ _SIGS = {
     "scout_commit_residency": ([_p, _i, _p, _p, _i64, _i, _i, _i, _p, _p], _i),
     "scout_plan_recall": ([_p, _p, _p, _p, _p, _i, _i, _i, _p, _i, _p], _i),
     "scout_cpu_attend": ([_p, _p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _i, _f, _p, _p, _i], _i),
+    "scout_cpu_attend_scalar": ([_p, _p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _i, _f, _p, _p, _i], _i),
     "scout_recall_intervals": ([_p, _i, _i, _f, _p], _i),
     "scout_resident_list": ([_p, _p, _i, _i, _i, _i, _i, _p, _p, _p, _p], _i),
     "scout_cpu_pool_create": ([_i], _p),
@@ -427,14 +428,15 @@ def _host(t, dtype, name: str) -> int:
 
 
 def cpu_attend(q, K, V, seq_len, cpu_list, cpu_count, B, Hq, Hkv, P, k, scale, O_cpu=None, lse_cpu=None,
-               n_threads=0):
+               n_threads=0, scalar=False):
     """CPU-side attention over the CPU work list, on the host cores (synchronous).
 
     Host tensors: q bf16 [B][Hq][D]; K, V bf16 [B][Hkv][nblk_cap][P][D] (every block of the
     layer in logical order); seq_len int32 [B]; cpu_list int32 [B][Hkv][k] and cpu_count
     int32 [B][Hkv] as scout_score_topk writes them.  Returns (O_cpu fp32 [B][Hq][D],
     lse_cpu fp32 [B][Hq]), the partial that scout_merge / scout_sparse_attn_merge take.
-    The foreign call releases the GIL, so other Python threads run meanwhile."""
+    The foreign call releases the GIL, so other Python threads run meanwhile.  ``scalar``: the
+    plain-loop form (scout_cpu_attend_scalar) instead of the register-tiled one."""
     D = q.shape[-1]
     per_block = B * Hkv * P * D
     if K.numel() != V.numel() or K.numel() % per_block:
@@ -444,11 +446,12 @@ def cpu_attend(q, K, V, seq_len, cpu_list, cpu_count, B, Hq, Hkv, P, k, scale, O
         O_cpu = torch.empty((B, Hq, D), dtype=torch.float32)
     if lse_cpu is None:
         lse_cpu = torch.empty((B, Hq), dtype=torch.float32)
-    _check(lib().scout_cpu_attend(_host(q, torch.bfloat16, "q"), _host(K, torch.bfloat16, "K"),
-                                  _host(V, torch.bfloat16, "V"), _host(seq_len, torch.int32, "seq_len"),
-                                  _host(cpu_list, torch.int32, "cpu_list"), _host(cpu_count, torch.int32, "cpu_count"),
-                                  B, Hq, Hkv, D, P, nblk_cap, k, float(scale), _host(O_cpu, torch.float32, "O_cpu"),
-                                  _host(lse_cpu, torch.float32, "lse_cpu"), int(n_threads)), "scout_cpu_attend")
+    fn = lib().scout_cpu_attend_scalar if scalar else lib().scout_cpu_attend
+    _check(fn(_host(q, torch.bfloat16, "q"), _host(K, torch.bfloat16, "K"), _host(V, torch.bfloat16, "V"),
+              _host(seq_len, torch.int32, "seq_len"), _host(cpu_list, torch.int32, "cpu_list"),
+              _host(cpu_count, torch.int32, "cpu_count"), B, Hq, Hkv, D, P, nblk_cap, k, float(scale),
+              _host(O_cpu, torch.float32, "O_cpu"), _host(lse_cpu, torch.float32, "lse_cpu"), int(n_threads)),
+           "scout_cpu_attend_scalar" if scalar else "scout_cpu_attend")
     return O_cpu, lse_cpu
 
 

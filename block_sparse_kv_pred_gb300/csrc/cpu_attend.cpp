@@ -4,13 +4,21 @@
 // next to the host copy of the KV cache, with the predicted query; the GPU merges the result.
 //
 // The threads take whole units (sequence, KV head) from an atomic counter.  For a unit, the G
-// query rows are held in fp32.  Each listed block's K rows are widened from bf16 once and
-// dotted with all G rows, with 16 independent partial sums per product, so the loop vectorises
-// without reassociating.  A block-wise online softmax then rescales the running sums to the
-// block's maximum, and the block's V rows are accumulated with its probabilities, four rows per
-// pass over the running sums (measured 10-30% faster than one; two K rows per pass over the
-// query rows was four times slower, the loop no longer vectorising).  Portable C++ only: no
-// intrinsics, the compiler's vectoriser does the rest on x86-64 and AArch64.
+// query rows are held in fp32, and a block-wise online softmax rescales the running sums to
+// each block's maximum.  Two implementations of a unit:
+//
+// * the tiled one (the default), written with the compiler's generic 4 x fp32 vectors (GCC
+//   vector extensions: NEON on AArch64, SSE on x86-64; no intrinsics, no target flags):
+//   scores in register tiles of TT tokens x G heads (G q rows against TT widened K rows,
+//   4 dimensions per step, one horizontal sum per score at the end), then the block's V
+//   accumulated in register tiles of 16 (8 for more than six heads) dimensions x G heads
+//   over every token of the block, the running sums loaded, rescaled and stored once per
+//   tile (tiles sized for AArch64's 32 vector registers);
+// * the scalar one (scout_cpu_attend_scalar), plain loops with 16 partial sums per product,
+//   the reference the tiled one is tested against.
+#if !defined(__GNUC__)
+#error "the tiled CPU attention uses GCC/Clang vector extensions"
+#endif
 #include <algorithm>
 #include <atomic>
 #include <chrono>
@@ -57,7 +65,127 @@ struct Job {
   float* lse;
 };
 
-void attend_unit(const Job& a, int u) {
+typedef float f32x4 __attribute__((vector_size(16)));
+typedef uint32_t u32x4 __attribute__((vector_size(16)));
+typedef uint16_t u16x4 __attribute__((vector_size(8)));
+
+inline f32x4 widen4(const uint16_t* p) {  // four bf16 -> four fp32 (exact)
+  u16x4 h;
+  std::memcpy(&h, p, sizeof h);
+  const u32x4 w = __builtin_convertvector(h, u32x4) << 16;
+  f32x4 f;
+  std::memcpy(&f, &w, sizeof f);
+  return f;
+}
+
+inline float hsum(f32x4 v) { return (v[0] + v[1]) + (v[2] + v[3]); }
+
+// One unit with register tiles; G query heads per KV head (a template argument, so that the
+// tiles are fixed-size arrays the compiler keeps in registers).
+template <int G>
+void attend_unit_tiled(const Job& a, int u) {
+  constexpr int TT = G <= 4 ? 4 : (G <= 6 ? 3 : 2);  // tokens per score tile: G x TT accumulators
+  constexpr int DV = G <= 6 ? 4 : 2;                  // 4-wide vectors per V tile: G x DV accumulators
+  const int b = u / a.Hkv, kvh = u - b * a.Hkv, P = a.P;
+  alignas(64) f32x4 q[G][kDim / 4];
+  alignas(64) f32x4 acc[G][kDim / 4];
+  alignas(64) float s[G][kMaxPage + 4];
+  float m[G], l[G], corr[G];
+  const uint16_t* qg = a.q + (static_cast<int64_t>(b) * a.Hq + static_cast<int64_t>(kvh) * G) * kDim;
+  for (int h = 0; h < G; ++h) {
+    for (int c = 0; c < kDim / 4; ++c) {
+      q[h][c] = widen4(qg + h * kDim + 4 * c);
+      acc[h][c] = f32x4{0.f, 0.f, 0.f, 0.f};
+    }
+    m[h] = -INFINITY;
+    l[h] = 0.f;
+  }
+  const int L = a.seq_len[b];
+  const int n = a.count[u];
+  const int32_t* blocks = a.list + static_cast<int64_t>(u) * a.k;
+  for (int i = 0; i < n; ++i) {
+    const int j = blocks[i];
+    const int valid = std::min(P, L - j * P);
+    if (valid <= 0) continue;  // no token of this block is in the sequence yet
+    const int64_t base = (static_cast<int64_t>(u) * a.nblk_cap + j) * P * kDim;
+    const uint16_t* Kb = a.K + base;
+    const uint16_t* Vb = a.V + base;
+    // scores: tiles of TT tokens (rows past the valid ones stay inside the block's P rows; their
+    // scores are computed and never used)
+    for (int t0 = 0; t0 < valid; t0 += TT) {
+      f32x4 c[G][TT];
+      for (int h = 0; h < G; ++h)
+        for (int x = 0; x < TT; ++x) c[h][x] = f32x4{0.f, 0.f, 0.f, 0.f};
+      const int rows = std::min(TT, P - t0);  // TT need not divide P
+      for (int d = 0; d < kDim / 4; ++d) {
+        f32x4 kr[TT];
+        for (int x = 0; x < TT; ++x) kr[x] = x < rows ? widen4(Kb + (t0 + x) * kDim + 4 * d) : f32x4{};
+        for (int h = 0; h < G; ++h)
+          for (int x = 0; x < TT; ++x) c[h][x] += q[h][d] * kr[x];
+      }
+      for (int h = 0; h < G; ++h)
+        for (int x = 0; x < TT; ++x) s[h][t0 + x] = a.scale * hsum(c[h][x]);
+    }
+    // online softmax: s becomes the probabilities, corr the factor of the running sums
+    for (int h = 0; h < G; ++h) {
+      float mb = m[h];
+      for (int x = 0; x < valid; ++x) mb = std::max(mb, s[h][x]);
+      corr[h] = m[h] == -INFINITY ? 0.f : std::exp(m[h] - mb);
+      float sum = 0.f;
+      for (int x = 0; x < valid; ++x) {
+        s[h][x] = std::exp(s[h][x] - mb);
+        sum += s[h][x];
+      }
+      l[h] = l[h] * corr[h] + sum;
+      m[h] = mb;
+    }
+    // acc_h = corr_h acc_h + sum_t p_h(t) v_t, one tile of 4 * DV dimensions at a time
+    for (int c0 = 0; c0 < kDim / 4; c0 += DV) {
+      f32x4 r[G][DV];
+      for (int h = 0; h < G; ++h)
+        for (int e = 0; e < DV; ++e) r[h][e] = acc[h][c0 + e] * corr[h];
+      for (int t = 0; t < valid; ++t) {
+        f32x4 v[DV];
+        for (int e = 0; e < DV; ++e) v[e] = widen4(Vb + t * kDim + 4 * (c0 + e));
+        for (int h = 0; h < G; ++h) {
+          const float w = s[h][t];
+          for (int e = 0; e < DV; ++e) r[h][e] += w * v[e];
+        }
+      }
+      for (int h = 0; h < G; ++h)
+        for (int e = 0; e < DV; ++e) acc[h][c0 + e] = r[h][e];
+    }
+  }
+  for (int h = 0; h < G; ++h) {
+    const int64_t row = static_cast<int64_t>(b) * a.Hq + static_cast<int64_t>(kvh) * G + h;
+    const float inv = l[h] > 0.f ? 1.f / l[h] : 0.f;
+    for (int c = 0; c < kDim / 4; ++c) {
+      const f32x4 o = acc[h][c] * inv;
+      std::memcpy(a.O + row * kDim + 4 * c, &o, sizeof o);
+    }
+    a.lse[row] = l[h] > 0.f ? m[h] + std::log(l[h]) : -INFINITY;
+  }
+}
+
+void attend_unit_scalar(const Job& a, int u);
+
+// The implementation a job runs, by its group size.
+using UnitFn = void (*)(const Job&, int);
+UnitFn unit_fn(int G, bool scalar) {
+  if (scalar) return attend_unit_scalar;
+  switch (G) {
+    case 1: return attend_unit_tiled<1>;
+    case 2: return attend_unit_tiled<2>;
+    case 3: return attend_unit_tiled<3>;
+    case 4: return attend_unit_tiled<4>;
+    case 5: return attend_unit_tiled<5>;
+    case 6: return attend_unit_tiled<6>;
+    case 7: return attend_unit_tiled<7>;
+    default: return attend_unit_tiled<8>;
+  }
+}
+
+void attend_unit_scalar(const Job& a, int u) {
   const int b = u / a.Hkv, kvh = u - b * a.Hkv, G = a.G, P = a.P;
   alignas(64) float q[kMaxGroup][kDim];
   alignas(64) float acc[kMaxGroup][kDim];
@@ -163,12 +291,10 @@ int make_job(const void* q, const void* K, const void* V, const int32_t* seq_len
   return SCOUT_OK;
 }
 
-}  // namespace
-
-extern "C" int scout_cpu_attend(const void* q, const void* K, const void* V, const int32_t* seq_len,
-                                const int32_t* cpu_list, const int32_t* cpu_count, int B, int Hq, int Hkv, int D,
-                                int P, int nblk_cap, int k, float scale, float* O_cpu, float* lse_cpu,
-                                int n_threads) {
+// scout_cpu_attend and scout_cpu_attend_scalar: threads started and joined by the call.
+int attend_sync(const void* q, const void* K, const void* V, const int32_t* seq_len, const int32_t* cpu_list,
+                const int32_t* cpu_count, int B, int Hq, int Hkv, int D, int P, int nblk_cap, int k, float scale,
+                float* O_cpu, float* lse_cpu, int n_threads, bool scalar) {
   Job a;
   const int rc = make_job(q, K, V, seq_len, cpu_list, cpu_count, B, Hq, Hkv, D, P, nblk_cap, k, scale, O_cpu,
                           lse_cpu, &a);
@@ -177,8 +303,9 @@ extern "C" int scout_cpu_attend(const void* q, const void* K, const void* V, con
   int nt = n_threads > 0 ? n_threads : static_cast<int>(std::max(1u, std::thread::hardware_concurrency()));
   nt = std::min(nt, units);
   std::atomic<int> next{0};
-  auto work = [&a, &next, units]() {
-    for (int u = next.fetch_add(1); u < units; u = next.fetch_add(1)) attend_unit(a, u);
+  const UnitFn fn = unit_fn(a.G, scalar);
+  auto work = [&a, &next, units, fn]() {
+    for (int u = next.fetch_add(1); u < units; u = next.fetch_add(1)) fn(a, u);
   };
   std::vector<std::thread> pool;
   for (int i = 1; i < nt; ++i) {
@@ -191,6 +318,24 @@ extern "C" int scout_cpu_attend(const void* q, const void* K, const void* V, con
   work();
   for (auto& th : pool) th.join();
   return SCOUT_OK;
+}
+
+}  // namespace
+
+extern "C" int scout_cpu_attend(const void* q, const void* K, const void* V, const int32_t* seq_len,
+                                const int32_t* cpu_list, const int32_t* cpu_count, int B, int Hq, int Hkv, int D,
+                                int P, int nblk_cap, int k, float scale, float* O_cpu, float* lse_cpu,
+                                int n_threads) {
+  return attend_sync(q, K, V, seq_len, cpu_list, cpu_count, B, Hq, Hkv, D, P, nblk_cap, k, scale, O_cpu, lse_cpu,
+                     n_threads, false);
+}
+
+extern "C" int scout_cpu_attend_scalar(const void* q, const void* K, const void* V, const int32_t* seq_len,
+                                       const int32_t* cpu_list, const int32_t* cpu_count, int B, int Hq, int Hkv,
+                                       int D, int P, int nblk_cap, int k, float scale, float* O_cpu, float* lse_cpu,
+                                       int n_threads) {
+  return attend_sync(q, K, V, seq_len, cpu_list, cpu_count, B, Hq, Hkv, D, P, nblk_cap, k, scale, O_cpu, lse_cpu,
+                     n_threads, true);
 }
 
 // ---------------------------------------------------------------------------
@@ -222,7 +367,8 @@ struct scout_cpu_pool {
         j = job;
         n = units;
       }
-      for (int u = next.fetch_add(1); u < n; u = next.fetch_add(1)) attend_unit(j, u);
+      const UnitFn fn = unit_fn(j.G, false);
+      for (int u = next.fetch_add(1); u < n; u = next.fetch_add(1)) fn(j, u);
       std::lock_guard<std::mutex> lk(mu);
       if (--active == 0) {
         running = false;

@@ -123,11 +123,14 @@ class Step:
         if event is not None:
             event.record(cur)
 
-    def issue(self, timing=None, after_begin=False):
+    def issue(self, timing=None, after_begin=False, before_attention=None):
         """Launch the next step.  ``timing``: optional name -> (start, end) timing events.
         ``after_begin``: the step directly follows ``begin`` (e.g. the first step of a CUDA
         graph), whose event already orders it after everything before, so it waits for no
-        earlier step's events (a graph capture may not wait on events recorded outside it)."""
+        earlier step's events (a graph capture may not wait on events recorded outside it).
+        ``before_attention``: optional callable, given the step's parity and the attention
+        stream, called after the GEMM, selection and digest append are issued and before the
+        attention is (the layer-ahead pipeline brings the CPU partial in there)."""
         par = self.i % 2
         cross = not self.serial and not after_begin
         sA, sB, sC, sD = (self.streams * 4)[:4] if self.serial else self.streams
@@ -156,6 +159,8 @@ class Step:
         if cross:
             # step i-1's selection wrote list set (i+1) % 2
             sB.wait_event((early.get("sparse_attn_merge") or self.sel_done)[1 - par])
+        if before_attention is not None:
+            before_attention(par, sB)
         run("sparse_attn_merge", sB)
         self.attn_done[par].record(sB)
         self.i += 1

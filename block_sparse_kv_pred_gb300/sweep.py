@@ -60,13 +60,18 @@ class DecodeSweep:
     """The layer's state on the GPU and the host, and one method per decode step."""
 
     def __init__(self, shape: W.Shape, steps: int, recall_every: int = 16, device="cuda", host=None,
-                 gather=True):
+                 gather=True, pages=False):
         """``recall_every`` 0: no recall (the profile from which recall intervals are read).
         ``host``: optional pair of pinned bf16 host tensors of at least [units][nblk][P][D]
         elements each, reused for the host copy of the layer's K/V (a multi-layer sweep keeps
         one pair).  ``gather``: recalls move their pages with the gather kernel reading mapped
-        host memory (scout_recall_gather_async); False: one cudaMemcpyAsync per run of pages."""
+        host memory (scout_recall_gather_async); False: one cudaMemcpyAsync per run of pages.
+        ``pages``: residency per page, a page being one block of a sequence for all its KV heads
+        (the 128 KB transfer unit of section 2.3, Figure 3): the initial resident pages are the k
+        most important of each sequence (importance: the largest of its heads' scores, ties to the
+        lower block) and each recall follows scout_plan_recall_pages; otherwise per block."""
         self.gather = gather
+        self.pages = pages
         self.s = s = shape
         self.steps, self.recall_every = steps, recall_every
         dev = self.dev = torch.device(device)
@@ -94,14 +99,24 @@ class DecodeSweep:
         # initial residency: the top-k of the first step's true query, plus the tail block
         self.ws = bs.score_topk_workspace(s.B, s.Hkv, nb, device=dev)
         none = torch.zeros((s.B, s.Hkv, s.words), dtype=torch.int32, device=dev)
+        sc0 = torch.empty((s.B, s.Hkv, nb), dtype=torch.float32, device=dev)
         first = bs.score_topk("minmax", WD.to_dev(self.qs[0], dev), self.digest, self.d_seq, none, s.B, s.Hq, s.Hkv,
-                              P, nb, s.k, self.ws)
+                              P, nb, s.k, self.ws, scores=sc0)
         topk = first["topk"].cpu().numpy().reshape(U, -1)
         tc = first["topk_count"].cpu().numpy().reshape(-1)
         res = np.zeros((U, nb), dtype=bool)
-        for u in range(U):
-            res[u, topk[u, :tc[u]]] = True
-            res[u, (int(self.seq[u // s.Hkv]) - 1) // P] = True
+        if pages:
+            imp = sc0.cpu().numpy().max(axis=1)  # [B][nblk], -inf past the valid blocks
+            for b in range(s.B):
+                nv = -(-int(self.seq[b]) // P)
+                order = sorted(range(nv), key=lambda j: (-float(imp[b, j]), j))[: s.k]
+                res[b * s.Hkv:(b + 1) * s.Hkv, order] = True
+                res[b * s.Hkv:(b + 1) * s.Hkv, nv - 1] = True
+        else:
+            for u in range(U):
+                res[u, topk[u, :tc[u]]] = True
+                res[u, (int(self.seq[u // s.Hkv]) - 1) // P] = True
+        del sc0
         # the pool: k + 1 resident blocks per unit and room for the blocks the decode starts
         spare_per_unit = -(-steps // P) + 1
         self.n_slots = int(res.sum()) + spare_per_unit * U
@@ -191,7 +206,11 @@ class DecodeSweep:
             for u in range(U):
                 sc[u, (int(self.seq[u // s.Hkv]) - 1) // P] = np.inf
             rec.update(scores=sc, res_before=self.res.copy(), table_before=self.table.copy())
-            ops = bs.plan_recall(sc, rec["topk"], rec["topk_count"], _bits(self.res), self.table, s.k)
+            if self.pages:
+                ops = bs.plan_recall_pages(sc, rec["topk"], rec["topk_count"], _bits(self.res), self.table, s.B,
+                                           s.Hkv, s.k)
+            else:
+                ops = bs.plan_recall(sc, rec["topk"], rec["topk_count"], _bits(self.res), self.table, s.k)
             if len(ops):
                 nbytes, secs = self._move_in(ops)
                 for u, j, slot, ev in ops:
@@ -224,7 +243,7 @@ def profile_recall_intervals(layers: int, steps: int, beta: float = 0.12, shape:
 
 
 def run_layers(layers: int, steps: int, recall_every=16, beta: float = 0.12, shape: W.Shape | None = None,
-               gather: bool = True):
+               gather: bool = True, pages: bool = False):
     """The decode sweep over ``layers`` layers, one after another (each its own seeded workload,
     freed before the next, the pinned host copy of its K/V reused): yields (layer, sweep, record)
     for every decode step.  ``recall_every``: a step count, or a sequence of per-layer intervals
@@ -239,7 +258,7 @@ def run_layers(layers: int, steps: int, recall_every=16, beta: float = 0.12, sha
         raise ValueError("one recall interval per layer")
     for layer in range(layers):
         sw = DecodeSweep(dataclasses.replace(base, seed=base.seed + layer), steps, recall_every=every[layer],
-                         host=host, gather=gather)
+                         host=host, gather=gather, pages=pages)
         for _ in range(steps):
             yield layer, sw, sw.step()
         del sw
@@ -313,6 +332,8 @@ def main():
     ap.add_argument("--profiled", action="store_true",
                     help="with --layers: recall at each layer's interval profiled without recalls first (--beta)")
     ap.add_argument("--copies", action="store_true", help="recall with cudaMemcpyAsync calls, not the gather kernel")
+    ap.add_argument("--pages", action="store_true",
+                    help="residency per page (a block of a sequence for all its KV heads), not per block")
     ap.add_argument("--probe-recall", action="store_true",
                     help="instead: host-to-device recall rate at 4 KB, 8 KB and 128 KB granularity")
     a = ap.parse_args()
@@ -327,7 +348,7 @@ def main():
             print(json.dumps({"profile_beta": a.beta, "intervals": [int(x) for x in iv],
                               "mean_interval": float(iv.mean())}), flush=True)
             every = iv
-        for layer, sw, rec in run_layers(a.layers, a.steps, every, gather=not a.copies):
+        for layer, sw, rec in run_layers(a.layers, a.steps, every, gather=not a.copies, pages=a.pages):
             print(json.dumps({"layer": layer, **rec["stats"]}), flush=True)
         return
     if a.profile_layers > 0:
@@ -337,7 +358,7 @@ def main():
                               "ratio": [round(float(x), 4) for x in traces[layer]]}), flush=True)
         print(json.dumps({"beta": a.beta, "mean_interval": float(iv.mean())}), flush=True)
         return
-    sw = DecodeSweep(c4_shape(a.steps), a.steps, a.recall_every)
+    sw = DecodeSweep(c4_shape(a.steps), a.steps, a.recall_every, gather=not a.copies, pages=a.pages)
     for _ in range(a.steps):
         print(json.dumps(sw.step()["stats"]), flush=True)
 

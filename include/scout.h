@@ -12,7 +12,7 @@
  *   a rejected call launches nothing.  A launch failure reported by the CUDA
  *   runtime returns SCOUT_ERR_CUDA.
  * - The host-side entry points (scout_plan_recall, scout_plan_recall_pages,
- *   scout_recall_intervals, scout_cpu_attend, scout_cpu_pool_*,
+ *   scout_recall_intervals, scout_cpu_attend(_scalar), scout_cpu_pool_*,
  *   scout_cpu_attend_async) are the exception: host pointers only, no GPU
  *   involved, synchronous except scout_cpu_attend_async.  scout_cpu_attend runs on
  *   worker threads it starts and joins within the call; the pool calls run on the
@@ -453,7 +453,8 @@ int scout_recall_intervals(const float* ratio, int layers, int steps, float beta
  *           never more than one per unit.  Units are dealt to the threads one at a time.
  * Synchronous: returns when every unit is done.  fp32 arithmetic, online softmax block
  * by block; each block's K and V are read once for all Hq / Hkv query heads of its KV
- * head.  No allocation visible to the caller; the threads live for the call.
+ * head, in register tiles of 4-wide fp32 vectors (the compiler's generic vectors: NEON on
+ * AArch64).  No allocation visible to the caller; the threads live for the call.
  * Errors (nothing written): SCOUT_ERR_INVALID_ARG for a NULL pointer, a non-positive
  * size, Hq not a multiple of Hkv (or more than 8 query heads per KV head), scale <= 0,
  * a count outside [0, k] or a listed block outside [0, nblk_cap);
@@ -461,6 +462,14 @@ int scout_recall_intervals(const float* ratio, int layers, int steps, float beta
 int scout_cpu_attend(const void* q, const void* K, const void* V, const int32_t* seq_len, const int32_t* cpu_list,
                      const int32_t* cpu_count, int B, int Hq, int Hkv, int D, int P, int nblk_cap, int k,
                      float scale, float* O_cpu, float* lse_cpu, int n_threads);
+
+/* scout_cpu_attend_scalar: the same call, arguments, checks and outputs, computed with plain
+ * scalar loops (16 partial sums per dot product, no register tiles): the portable form the
+ * tiled one is checked against.  The two agree to fp32 rounding (they sum in different
+ * orders), not bit for bit. */
+int scout_cpu_attend_scalar(const void* q, const void* K, const void* V, const int32_t* seq_len,
+                            const int32_t* cpu_list, const int32_t* cpu_count, int B, int Hq, int Hkv, int D, int P,
+                            int nblk_cap, int k, float scale, float* O_cpu, float* lse_cpu, int n_threads);
 
 /* ------------------------------------------------------------------------ *
  * The CPU side on a caller-owned pool of worker threads (host code).

@@ -80,6 +80,22 @@ def check_attention(o_gpu, l_gpu, o_ref, l_ref, what=""):
     assert np.all(err <= 0), (what, float(np.max(np.abs(o_gpu - o_ref))))
 
 
+def oracle_qpred(s):
+    """The oracle's Q_pred of a step's synthetic layer, rounded to bf16 bits [B][Hq*D]: from the
+    seeded X and W_Q (the host side of the generator that filled the device buffers)."""
+    from block_sparse_kv_pred_gb300 import workload as W
+
+    X = W.normal_bf16(s.seed, W.STREAM_X, (s.B, s.hidden))
+    Wq = W.normal_bf16(s.seed, W.STREAM_W, (s.Hq * s.D, s.hidden), s.w_sigma)
+    return O.f64_to_bf16(O.predict_q(X, Wq))
+
+
+def check_qpred(got_bits, ref_bits):
+    """The Q_pred bar: |gpu - oracle| <= 2^-8 |oracle| + 1e-3 max |oracle| element-wise."""
+    got, ref = O.bf16_to_f64(got_bits), O.bf16_to_f64(ref_bits)
+    assert np.all(np.abs(got - ref) <= 2.0 ** -8 * np.abs(ref) + 1e-3 * np.abs(ref).max())
+
+
 def check_selection(U_ref, k, S_gpu, what=""):
     """GPU top-k set equals the fp64 one except for blocks within SCORE_REL of the k-th score."""
     S_ref = O.select_topk(U_ref, k)
@@ -104,3 +120,37 @@ def check_topk_property(scores, S, k, nv, what=""):
     rest = np.nonzero(~sel)[0]
     best_out = max(rest, key=lambda j: (scores[j], -j))
     assert (scores[worst_in] > scores[best_out]) or (scores[worst_in] == scores[best_out] and worst_in < best_out), what
+
+
+def _mask(lst, cnt, nb):
+    """bool [U][nb]: the first cnt[u] entries of each list; raises on a duplicate or a bad entry."""
+    U, k = lst.shape
+    live = np.arange(k)[None, :] < cnt[:, None]
+    assert np.all((lst[live] >= 0) & (lst[live] < nb)) and np.all(lst[~live] == -1)
+    m = np.zeros((U, nb + 1), bool)
+    m[np.arange(U)[:, None], np.where(live, lst, nb)] = True
+    m = m[:, :nb]
+    assert np.array_equal(m.sum(1), cnt)  # no entry twice
+    return m
+
+
+def check_list_algebra(s, rec, nb):
+    """The lists of every unit of a sweep record: top-k count, each list ascending and without
+    repeats, res and cpu the split of top-k by residency, delta = cpu minus the previous cpu."""
+    U, k = s.units, s.k
+    nvalid = -(-rec["seq"].astype(np.int64) // s.P)
+    tc = rec["topk_count"]
+    assert np.array_equal(tc, np.minimum(k, np.repeat(nvalid, s.Hkv)))
+    for n in ("topk", "res", "cpu", "delta"):
+        lst, c = rec[n], rec[n + "_count"]
+        live = np.arange(k)[None, :] < c[:, None]
+        d = np.diff(np.where(live, lst, np.iinfo(np.int32).max), axis=1)
+        assert np.all(d[live[:, 1:]] > 0), n  # ascending
+    T = _mask(rec["topk"], tc, nb)
+    Rm = _mask(rec["res"], rec["res_count"], nb)
+    Cm = _mask(rec["cpu"], rec["cpu_count"], nb)
+    Dm = _mask(rec["delta"], rec["delta_count"], nb)
+    assert np.array_equal(Rm | Cm, T) and not np.any(Rm & Cm)
+    assert np.array_equal(Rm, T & rec["resident"]) and np.array_equal(Cm, T & ~rec["resident"])
+    prev = np.zeros_like(Cm) if rec["prev_cpu"] is None else _mask(*rec["prev_cpu"], nb)
+    assert np.array_equal(Dm, Cm & ~prev)

@@ -98,6 +98,30 @@ def test_cpu_partial_matches_oracle(name):
             check_fp32(O_cpu[b, kvh * s.G + h], L_cpu[b, kvh * s.G + h], o, l, what=(name, u, h))
 
 
+@pytest.mark.parametrize("G", range(1, 9))
+def test_tiled_and_scalar_forms_agree_within_the_fp32_bar(G):
+    """The register-tiled form (the default) against the plain scalar loops, for every group
+    size (each is its own tile shape, three tokens per tile with five or six heads, so the tile
+    does not divide the page) and the three page sizes; both against the oracle as well."""
+    P = (16, 32, 64)[G % 3]
+    s = W.Shape(f"g{G}_p{P}", B=2, Hq=2 * G, Hkv=2, T=2500, P=P, k=2048 // P, resident_frac=0.25,
+                seq_lens=(2500, 1111))
+    wl, Kb, Vb, cpu, cnt, _ = _setup(s)
+    args = (_bf16(wl.q), _bf16(Kb), _bf16(Vb), torch.from_numpy(wl.seq_len.astype(np.int32)),
+            torch.from_numpy(cpu.reshape(s.B, s.Hkv, s.k)), torch.from_numpy(cnt.reshape(s.B, s.Hkv)),
+            s.B, s.Hq, s.Hkv, s.P, s.k, s.scale)
+    Ot, Lt = (x.numpy() for x in bs.cpu_attend(*args, n_threads=2))
+    Os, Ls = (x.numpy() for x in bs.cpu_attend(*args, n_threads=2, scalar=True))
+    assert cnt.max() > 0
+    for u in range(s.units):
+        b, kvh = divmod(u, s.Hkv)
+        for h, (o, l) in enumerate(_ref(s, wl, Kb, Vb, u, cpu[u, :cnt[u]])):
+            hq = kvh * s.G + h
+            check_fp32(Ot[b, hq], Lt[b, hq], o, l, what=("tiled", u, h))
+            check_fp32(Os[b, hq], Ls[b, hq], o, l, what=("scalar", u, h))
+            check_fp32(Ot[b, hq], Lt[b, hq], Os[b, hq].astype(np.float64), float(Ls[b, hq]), what=("pair", u, h))
+
+
 def test_split_merged_with_the_resident_partial_is_the_selection():
     """The CPU partial over S minus R, merged by LSE with the partial over S and R, equals
     attention over the whole selected set S (the merge of section 3.2)."""

@@ -15,7 +15,7 @@ import torch
 
 import oracle as O
 from block_sparse_kv_pred_gb300.sweep import c4_shape, run_layers
-from _parity import check_attention, check_selection, ensure_built
+from _parity import check_attention, check_list_algebra, check_selection, ensure_built
 
 pytestmark = pytest.mark.gpu
 
@@ -28,38 +28,6 @@ def _built():
     ensure_built()
 
 
-def _mask(lst, cnt, nb):
-    """bool [U][nb]: the first cnt[u] entries of each list; raises on a duplicate or a bad entry."""
-    U, k = lst.shape
-    live = np.arange(k)[None, :] < cnt[:, None]
-    assert np.all((lst[live] >= 0) & (lst[live] < nb)) and np.all(lst[~live] == -1)
-    m = np.zeros((U, nb + 1), bool)
-    m[np.arange(U)[:, None], np.where(live, lst, nb)] = True
-    m = m[:, :nb]
-    assert np.array_equal(m.sum(1), cnt)  # no entry twice
-    return m
-
-
-def _check_algebra(s, rec, nb):
-    U, k = s.units, s.k
-    nvalid = -(-rec["seq"].astype(np.int64) // s.P)
-    tc = rec["topk_count"]
-    assert np.array_equal(tc, np.minimum(k, np.repeat(nvalid, s.Hkv)))
-    for n in ("topk", "res", "cpu", "delta"):
-        lst, c = rec[n], rec[n + "_count"]
-        live = np.arange(k)[None, :] < c[:, None]
-        d = np.diff(np.where(live, lst, np.iinfo(np.int32).max), axis=1)
-        assert np.all(d[live[:, 1:]] > 0), n  # ascending
-    T = _mask(rec["topk"], tc, nb)
-    Rm = _mask(rec["res"], rec["res_count"], nb)
-    Cm = _mask(rec["cpu"], rec["cpu_count"], nb)
-    Dm = _mask(rec["delta"], rec["delta_count"], nb)
-    assert np.array_equal(Rm | Cm, T) and not np.any(Rm & Cm)
-    assert np.array_equal(Rm, T & rec["resident"]) and np.array_equal(Cm, T & ~rec["resident"])
-    prev = np.zeros_like(Cm) if rec["prev_cpu"] is None else _mask(*rec["prev_cpu"], nb)
-    assert np.array_equal(Dm, Cm & ~prev)
-
-
 def test_forty_layers_sixty_four_steps():
     s0 = c4_shape(STEPS)
     nb, P, D, G = s0.nblk, s0.P, s0.D, s0.G
@@ -69,7 +37,7 @@ def test_forty_layers_sixty_four_steps():
     state = {}
     for layer, sw, rec in run_layers(LAYERS, STEPS, EVERY):
         s, t = sw.s, rec["t"]
-        _check_algebra(s, rec, nb)
+        check_list_algebra(s, rec, nb)
         u = int(units[layer])
         b, kvh = divmod(u, s.Hkv)
         L = int(rec["seq"][b])

@@ -10,7 +10,7 @@ import block_sparse_kv_pred_gb300 as bs
 from block_sparse_kv_pred_gb300 import workload as W
 from block_sparse_kv_pred_gb300.step import setup_step
 from block_sparse_kv_pred_gb300.workload import device as WD
-from _parity import bf16_bits, check_attention, ensure_built, nvalid, to_dev
+from _parity import bf16_bits, check_attention, check_qpred, check_selection, ensure_built, nvalid, oracle_qpred, to_dev
 
 pytestmark = pytest.mark.gpu
 
@@ -132,8 +132,9 @@ def test_two_stream_step_matches_oracle(serial):
     torch.cuda.synchronize()
     assert int(t["status"].item()) == 0
     last = (step.i - 1) % 2  # set written by the last step; the last attention read the other set
-    qp_bits = bf16_bits(t["Qp0"])
-    assert np.array_equal(qp_bits, bf16_bits(t["Qp1"]))  # same X and W_Q every step
+    assert np.array_equal(bf16_bits(t["Qp0"]), bf16_bits(t["Qp1"]))  # same X and W_Q every step
+    qp_bits = oracle_qpred(s)  # the oracle's own Q_pred, which the GPU's must match first
+    check_qpred(bf16_bits(t["Qp0"]), qp_bits)
     lists = {par: (t[f"topk{par}"].cpu().numpy().reshape(s.units, -1),
                    t[f"res{par}"].cpu().numpy().reshape(s.units, -1),
                    t[f"res_count{par}"].cpu().numpy().reshape(-1)) for par in (0, 1)}
@@ -145,10 +146,15 @@ def test_two_stream_step_matches_oracle(serial):
         qg = qp_bits[b, kvh * s.G * s.D:(kvh + 1) * s.G * s.D].reshape(s.G, s.D)
         r = O.unit_step(qg, wl.q[b, kvh * s.G:(kvh + 1) * s.G], wl.unit_kv(u), wl.unit_kv(u, "V"), L, s.P, s.k,
                         "minmax", wl.resident[u].astype(bool), s.scale)
+        exact = True
         for par in (0, 1):  # both sets hold the same selection (same Q_pred and digests)
             topk, res, rc = lists[par]
-            assert list(topk[u][: len(r["topk"])]) == list(r["topk"])
-            assert list(res[u][: rc[u]]) == list(r["res"])
+            exact &= check_selection(r["scores"], s.k, topk[u][: len(r["topk"])], what=(serial, u))
+            if exact:
+                assert list(topk[u][: len(r["topk"])]) == list(r["topk"])
+                assert list(res[u][: rc[u]]) == list(r["res"])
+        if not exact:
+            continue  # a near-tie: the resident part differs from the oracle's, so does the output
         assert lists[1 - last][2][u] == len(r["res"])
         for h in range(s.G):
             hq = kvh * s.G + h

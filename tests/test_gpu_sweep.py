@@ -10,7 +10,7 @@ import oracle as O
 import block_sparse_kv_pred_gb300 as bs
 from block_sparse_kv_pred_gb300 import workload as W
 from block_sparse_kv_pred_gb300.workload import device as WD
-from _parity import bits_from_mask, check_attention, check_selection, ensure_built, to_dev
+from _parity import bits_from_mask, check_attention, check_list_algebra, check_selection, ensure_built, to_dev
 
 pytestmark = pytest.mark.gpu
 
@@ -139,3 +139,55 @@ def test_decode_sweep_with_walk_append_delta_and_recall():
     print("cpu list sizes", cpu_sizes)
     print("delta sizes", delta_sizes)
     assert delta_sizes[0] == cpu_sizes[0] and all(dz <= cz for dz, cz in zip(delta_sizes, cpu_sizes))
+
+
+def test_page_granular_residency_sweep():
+    """The NEXT variant of residency per page (one block of a sequence for all its KV heads, the
+    transfer unit of section 2.3, Figure 3) through the decode sweep: the residency of a
+    sequence's heads stays identical, every step's lists, split and attention match the oracle,
+    and every recall is the oracle's page plan (recall_plan_pages) applied to each head."""
+    from block_sparse_kv_pred_gb300.sweep import DecodeSweep
+
+    steps, every = 20, 6
+    s = W.Shape("sweep_pages", B=2, Hq=8, Hkv=2, T=4096, P=32, k=16, resident_frac=0.0, seq_lens=(4000, 3950),
+                hidden=0)
+    sw = DecodeSweep(s, steps, recall_every=every, pages=True)
+    U, nb, P, D = s.units, s.nblk, s.P, s.D
+    hK = {u: sw.hK[u].view(torch.int16).numpy().view(np.uint16).reshape(nb * P, D) for u in range(U)}
+    hV = {u: sw.hV[u].view(torch.int16).numpy().view(np.uint16).reshape(nb * P, D) for u in range(U)}
+    n_recalls = 0
+    for t in range(steps):
+        rec = sw.step()
+        check_list_algebra(s, rec, nb)
+        res = rec["resident"].reshape(s.B, s.Hkv, nb)
+        assert np.all(res == res[:, :1, :]), t  # one residency per page
+        for u in range(U):
+            b, kvh = divmod(u, s.Hkv)
+            L = int(rec["seq"][b])
+            mn, mx = O.digest_minmax(hK[u], L, P)
+            Uref = O.pool_group(O.scores_minmax(O.bf16_to_f64(sw.ps[t][b, kvh * s.G:(kvh + 1) * s.G]), mn, mx))
+            S = rec["topk"][u, :rec["topk_count"][u]]
+            check_selection(Uref, s.k, S, what=(t, u))
+            r_ref, _ = O.split_residency(S, rec["resident"][u])
+            toks = O.block_tokens(r_ref, P, L)
+            K, V = O.bf16_to_f64(hK[u]), O.bf16_to_f64(hV[u])
+            for h in range(s.G):
+                hq = kvh * s.G + h
+                o, l = O.attention_partial(O.bf16_to_f64(sw.qs[t][b, hq]), K[toks], V[toks], s.scale)
+                check_attention(rec["O"][b, hq], rec["lse"][b, hq], o, l, what=(t, u, h))
+        if "ops" in rec:
+            n_recalls += 1
+            ops = np.asarray(rec["ops"]).reshape(-1, 4)
+            for b in range(s.B):
+                us = range(b * s.Hkv, (b + 1) * s.Hkv)
+                want = O.recall_plan_pages([rec["scores"][u].astype(np.float64) for u in us],
+                                           [rec["topk"][u, :rec["topk_count"][u]] for u in us],
+                                           rec["res_before"][b * s.Hkv], [rec["table_before"][u] for u in us])
+                for h, u in enumerate(us):
+                    got = [(int(j), int(sl), int(e)) for uu, j, sl, e in ops if uu == u]
+                    assert got == want[h], (t, u)
+            # the pool holds each recalled block's own K/V at its new slot
+            Kp = sw.K_pool.view(torch.int16).cpu().numpy().view(np.uint16)
+            for u, j, sl, _ in ops[:: max(1, len(ops) // 8)]:
+                assert np.array_equal(Kp[sl], hK[int(u)][int(j) * P:(int(j) + 1) * P]), (t, u, j)
+    assert n_recalls == steps // every

@@ -61,3 +61,33 @@ def test_query_walk_cosines_and_norms():
         assert np.allclose(np.linalg.norm(f(q[t]), axis=-1), np.sqrt(128), rtol=5e-3)
     q2, p2 = wl.walk(6)
     assert np.array_equal(q, q2) and np.array_equal(p, p2)
+
+
+def _table1():
+    """Model -> cosine between predicted and true query, from the golden file (the pages'
+    section 3.3, Table 1)."""
+    import os
+
+    path = os.path.join(os.path.dirname(__file__), "golden", "table1_query_cosine.txt")
+    rows = [ln.split() for ln in open(path) if ln.strip() and not ln.startswith("#")]
+    return {name: float(v) for name, v in rows}
+
+
+def test_walk_draws_qpred_at_the_table_cosines():
+    """The walk's default predicted-query cosine is the smallest of Table 1's, and for every
+    model's value the predicted queries it draws sit at that cosine to the true ones (up to the
+    bf16 rounding of both)."""
+    import inspect
+
+    table = _table1()
+    assert len(table) == 5 and all(0.9 < v < 1.0 for v in table.values())
+    assert inspect.signature(W.Workload.walk).parameters["cosine"].default == min(table.values())
+    s = W.Shape("walk", B=2, Hq=8, Hkv=2, T=256, P=32, k=4, resident_frac=0.25, seq_lens=(256, 200))
+    wl = W.Workload(s)
+    for name, c in sorted(table.items()):
+        qs, ps = wl.walk(3, cosine=c)
+        q = W.bf16_to_f32(qs).astype(np.float64)
+        p = W.bf16_to_f32(ps).astype(np.float64)
+        cos = (q * p).sum(-1) / np.linalg.norm(q, axis=-1) / np.linalg.norm(p, axis=-1)
+        assert np.all(np.abs(cos - c) < 3e-3), (name, float(np.abs(cos - c).max()))
+        assert abs(cos.mean() - c) < 5e-4, name
