@@ -133,8 +133,9 @@ def test_two_stream_step_matches_oracle(serial):
     assert int(t["status"].item()) == 0
     last = (step.i - 1) % 2  # set written by the last step; the last attention read the other set
     assert np.array_equal(bf16_bits(t["Qp0"]), bf16_bits(t["Qp1"]))  # same X and W_Q every step
-    qp_bits = oracle_qpred(s)  # the oracle's own Q_pred, which the GPU's must match first
-    check_qpred(bf16_bits(t["Qp0"]), qp_bits)
+    qp_ref = oracle_qpred(s)  # the oracle's own Q_pred, which the GPU's must match first
+    check_qpred(bf16_bits(t["Qp0"]), qp_ref)
+    qp_bits = O.f64_to_bf16(qp_ref)  # rounded as the step stores it
     lists = {par: (t[f"topk{par}"].cpu().numpy().reshape(s.units, -1),
                    t[f"res{par}"].cpu().numpy().reshape(s.units, -1),
                    t[f"res_count{par}"].cpu().numpy().reshape(-1)) for par in (0, 1)}
