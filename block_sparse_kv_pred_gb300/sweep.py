@@ -69,7 +69,8 @@ class DecodeSweep:
         ``pages``: residency per page, a page being one block of a sequence for all its KV heads
         (the 128 KB transfer unit of section 2.3, Figure 3): the initial resident pages are the k
         most important of each sequence (importance: the largest of its heads' scores, ties to the
-        lower block) and each recall follows scout_plan_recall_pages; otherwise per block."""
+        lower block) plus the page being written, and each recall follows scout_plan_recall_pages
+        with the page being written counted as selected by every head; otherwise per block."""
         self.gather = gather
         self.pages = pages
         self.s = s = shape
@@ -207,8 +208,18 @@ class DecodeSweep:
                 sc[u, (int(self.seq[u // s.Hkv]) - 1) // P] = np.inf
             rec.update(scores=sc, res_before=self.res.copy(), table_before=self.table.copy())
             if self.pages:
-                ops = bs.plan_recall_pages(sc, rec["topk"], rec["topk_count"], _bits(self.res), self.table, s.B,
-                                           s.Hkv, s.k)
+                # the page being written is never evicted: it joins every head's selection (more
+                # than k + 1 pages may come in with pages, so its infinite score is not enough)
+                tails = np.array([(int(self.seq[u // s.Hkv]) - 1) // P for u in range(U)], np.int32)
+                ti = np.concatenate([rec["topk"], tails[:, None]], axis=1)
+                tc = rec["topk_count"].copy()
+                for u in range(U):
+                    if tails[u] in ti[u, :tc[u]]:
+                        ti[u, tc[u]:] = -1
+                    else:
+                        ti[u, tc[u]], ti[u, tc[u] + 1:] = tails[u], -1
+                        tc[u] += 1
+                ops = bs.plan_recall_pages(sc, ti, tc, _bits(self.res), self.table, s.B, s.Hkv, s.k + 1)
             else:
                 ops = bs.plan_recall(sc, rec["topk"], rec["topk_count"], _bits(self.res), self.table, s.k)
             if len(ops):

@@ -142,10 +142,11 @@ def test_decode_sweep_with_walk_append_delta_and_recall():
 
 
 def test_page_granular_residency_sweep():
-    """The NEXT variant of residency per page (one block of a sequence for all its KV heads, the
+    """The variant of residency per page (one block of a sequence for all its KV heads, the
     transfer unit of section 2.3, Figure 3) through the decode sweep: the residency of a
     sequence's heads stays identical, every step's lists, split and attention match the oracle,
-    and every recall is the oracle's page plan (recall_plan_pages) applied to each head."""
+    every recall is the oracle's page plan (recall_plan_pages, the page being written counted as
+    selected) applied to each head, and the page being written stays resident."""
     from block_sparse_kv_pred_gb300.sweep import DecodeSweep
 
     steps, every = 20, 6
@@ -180,8 +181,9 @@ def test_page_granular_residency_sweep():
             ops = np.asarray(rec["ops"]).reshape(-1, 4)
             for b in range(s.B):
                 us = range(b * s.Hkv, (b + 1) * s.Hkv)
+                tail = (int(rec["seq"][b]) - 1) // P  # the page being written counts as selected
                 want = O.recall_plan_pages([rec["scores"][u].astype(np.float64) for u in us],
-                                           [rec["topk"][u, :rec["topk_count"][u]] for u in us],
+                                           [list(rec["topk"][u, :rec["topk_count"][u]]) + [tail] for u in us],
                                            rec["res_before"][b * s.Hkv], [rec["table_before"][u] for u in us])
                 for h, u in enumerate(us):
                     got = [(int(j), int(sl), int(e)) for uu, j, sl, e in ops if uu == u]
@@ -190,4 +192,6 @@ def test_page_granular_residency_sweep():
             Kp = sw.K_pool.view(torch.int16).cpu().numpy().view(np.uint16)
             for u, j, sl, _ in ops[:: max(1, len(ops) // 8)]:
                 assert np.array_equal(Kp[sl], hK[int(u)][int(j) * P:(int(j) + 1) * P]), (t, u, j)
+        tails = (rec["seq"].astype(np.int64) - 1) // P
+        assert all(sw.res[u, tails[u // s.Hkv]] for u in range(U)), t  # the page being written stays
     assert n_recalls == steps // every
