@@ -9,8 +9,10 @@
 //
 // * the tiled one (the default), written with the compiler's generic 4 x fp32 vectors (GCC
 //   vector extensions: NEON on AArch64, SSE on x86-64; no intrinsics, no target flags):
-//   scores in register tiles of TT tokens x G heads (G q rows against TT widened K rows,
-//   4 dimensions per step, one horizontal sum per score at the end), then the block's V
+//   bf16 widened by interleaving with zero halves (a zip per four values), scores in register
+//   tiles of TT tokens x G heads (G q rows against TT widened K rows, 8 dimensions per step,
+//   one horizontal sum per score at the end), the softmax weights four at a time with an
+//   exponential of its own (Cody-Waite reduction and a Taylor polynomial), then the block's V
 //   accumulated in register tiles of 16 (8 for more than six heads) dimensions x G heads
 //   over every token of the block, the running sums loaded, rescaled and stored once per
 //   tile (tiles sized for AArch64's 32 vector registers);
@@ -66,19 +68,51 @@ struct Job {
 };
 
 typedef float f32x4 __attribute__((vector_size(16)));
-typedef uint32_t u32x4 __attribute__((vector_size(16)));
-typedef uint16_t u16x4 __attribute__((vector_size(8)));
+typedef uint16_t u16x8 __attribute__((vector_size(16)));
 
-inline f32x4 widen4(const uint16_t* p) {  // four bf16 -> four fp32 (exact)
-  u16x4 h;
+// Eight bf16 -> two vectors of four fp32 (exact): a bf16 is the upper half of its fp32, so each
+// value is interleaved with a zero half (a zip with a zero vector; one instruction per half on
+// AArch64).  The element order of the vector types is the memory order on both targets.
+inline void widen8(const uint16_t* p, f32x4& lo, f32x4& hi) {
+  u16x8 h;
   std::memcpy(&h, p, sizeof h);
-  const u32x4 w = __builtin_convertvector(h, u32x4) << 16;
-  f32x4 f;
-  std::memcpy(&f, &w, sizeof f);
-  return f;
+  const u16x8 z = {0, 0, 0, 0, 0, 0, 0, 0};
+  const u16x8 a = __builtin_shuffle(z, h, (u16x8){0, 8, 1, 9, 2, 10, 3, 11});
+  const u16x8 c = __builtin_shuffle(z, h, (u16x8){4, 12, 5, 13, 6, 14, 7, 15});
+  std::memcpy(&lo, &a, sizeof lo);
+  std::memcpy(&hi, &c, sizeof hi);
 }
 
 inline float hsum(f32x4 v) { return (v[0] + v[1]) + (v[2] + v[3]); }
+
+typedef int32_t i32x4 __attribute__((vector_size(16)));
+
+// e^x for four x <= 0 (softmax weights), by Cody and Waite's reduction (W. J. Cody and W. Waite,
+// Software Manual for the Elementary Functions, 1980): x = n ln 2 + r with n the nearest integer
+// to x / ln 2 and ln 2 split into a short high part (exact products n * hi) and a low part, so
+// |r| <= ln(2) / 2; e^r by its Taylor polynomial of degree 7 (truncation below 1e-8 relative on
+// that interval); 2^n placed in the exponent field.  Arguments below -87 are taken as -87
+// (e^-87 ~ 1.6e-38, still a normal float; the weight is negligible next to the row maximum's 1).
+inline f32x4 exp_nonpos(f32x4 x) {
+  const f32x4 lo = {-87.f, -87.f, -87.f, -87.f};
+  x = x < lo ? lo : x;
+  const float inv_ln2 = 1.4426950408889634f, ln2_hi = 0.693145751953125f, ln2_lo = 1.4286068203094172e-6f;
+  // x <= 0: truncation of x / ln2 - 1/2 toward zero is the nearest integer (halves downwards)
+  const i32x4 n = __builtin_convertvector(x * inv_ln2 - 0.5f, i32x4);
+  const f32x4 nf = __builtin_convertvector(n, f32x4);
+  const f32x4 r = (x - nf * ln2_hi) - nf * ln2_lo;
+  f32x4 p = r * (1.f / 5040.f) + 1.f / 720.f;
+  p = p * r + 1.f / 120.f;
+  p = p * r + 1.f / 24.f;
+  p = p * r + 1.f / 6.f;
+  p = p * r + 0.5f;
+  p = p * r + 1.f;
+  p = p * r + 1.f;
+  const i32x4 e = (n + 127) << 23;
+  f32x4 scale;
+  std::memcpy(&scale, &e, sizeof scale);
+  return p * scale;
+}
 
 // One unit with register tiles; G query heads per KV head (a template argument, so that the
 // tiles are fixed-size arrays the compiler keeps in registers).
@@ -93,9 +127,9 @@ void attend_unit_tiled(const Job& a, int u) {
   float m[G], l[G], corr[G];
   const uint16_t* qg = a.q + (static_cast<int64_t>(b) * a.Hq + static_cast<int64_t>(kvh) * G) * kDim;
   for (int h = 0; h < G; ++h) {
-    for (int c = 0; c < kDim / 4; ++c) {
-      q[h][c] = widen4(qg + h * kDim + 4 * c);
-      acc[h][c] = f32x4{0.f, 0.f, 0.f, 0.f};
+    for (int c = 0; c < kDim / 4; c += 2) {
+      widen8(qg + h * kDim + 4 * c, q[h][c], q[h][c + 1]);
+      acc[h][c] = acc[h][c + 1] = f32x4{0.f, 0.f, 0.f, 0.f};
     }
     m[h] = -INFINITY;
     l[h] = 0.f;
@@ -116,27 +150,42 @@ void attend_unit_tiled(const Job& a, int u) {
       f32x4 c[G][TT];
       for (int h = 0; h < G; ++h)
         for (int x = 0; x < TT; ++x) c[h][x] = f32x4{0.f, 0.f, 0.f, 0.f};
-      const int rows = std::min(TT, P - t0);  // TT need not divide P
-      for (int d = 0; d < kDim / 4; ++d) {
-        f32x4 kr[TT];
-        for (int x = 0; x < TT; ++x) kr[x] = x < rows ? widen4(Kb + (t0 + x) * kDim + 4 * d) : f32x4{};
+      // TT need not divide P: the last tile of a block re-reads its last rows (in bounds; the
+      // scores of rows past P are never used)
+      const int r0 = std::min(t0, P - TT);
+      for (int d = 0; d < kDim / 4; d += 2) {
+        f32x4 k0[TT], k1[TT];
+        for (int x = 0; x < TT; ++x) widen8(Kb + (r0 + x) * kDim + 4 * d, k0[x], k1[x]);
         for (int h = 0; h < G; ++h)
-          for (int x = 0; x < TT; ++x) c[h][x] += q[h][d] * kr[x];
+          for (int x = 0; x < TT; ++x) c[h][x] += q[h][d] * k0[x];
+        for (int h = 0; h < G; ++h)
+          for (int x = 0; x < TT; ++x) c[h][x] += q[h][d + 1] * k1[x];
       }
       for (int h = 0; h < G; ++h)
-        for (int x = 0; x < TT; ++x) s[h][t0 + x] = a.scale * hsum(c[h][x]);
+        for (int x = 0; x < TT; ++x) s[h][r0 + x] = a.scale * hsum(c[h][x]);
     }
     // online softmax: s becomes the probabilities, corr the factor of the running sums
     for (int h = 0; h < G; ++h) {
       float mb = m[h];
       for (int x = 0; x < valid; ++x) mb = std::max(mb, s[h][x]);
       corr[h] = m[h] == -INFINITY ? 0.f : std::exp(m[h] - mb);
-      float sum = 0.f;
-      for (int x = 0; x < valid; ++x) {
-        s[h][x] = std::exp(s[h][x] - mb);
-        sum += s[h][x];
+      // four weights at a time; lanes past `valid` (scores never computed) are taken as the
+      // maximum, stored and never read, and left out of the sum
+      f32x4 sum4 = {0.f, 0.f, 0.f, 0.f};
+      const f32x4 mb4 = {mb, mb, mb, mb};
+      for (int x = 0; x < valid; x += 4) {
+        f32x4 v;
+        std::memcpy(&v, &s[h][x], sizeof v);
+        const int left = valid - x;  // lanes of v inside the row
+        if (left < 4)
+          for (int e = left; e < 4; ++e) v[e] = mb;
+        v = exp_nonpos(v - mb4);
+        std::memcpy(&s[h][x], &v, sizeof v);
+        if (left < 4)
+          for (int e = left; e < 4; ++e) v[e] = 0.f;
+        sum4 += v;
       }
-      l[h] = l[h] * corr[h] + sum;
+      l[h] = l[h] * corr[h] + hsum(sum4);
       m[h] = mb;
     }
     // acc_h = corr_h acc_h + sum_t p_h(t) v_t, one tile of 4 * DV dimensions at a time
@@ -146,7 +195,7 @@ void attend_unit_tiled(const Job& a, int u) {
         for (int e = 0; e < DV; ++e) r[h][e] = acc[h][c0 + e] * corr[h];
       for (int t = 0; t < valid; ++t) {
         f32x4 v[DV];
-        for (int e = 0; e < DV; ++e) v[e] = widen4(Vb + t * kDim + 4 * (c0 + e));
+        for (int e = 0; e < DV; e += 2) widen8(Vb + t * kDim + 4 * (c0 + e), v[e], v[e + 1]);
         for (int h = 0; h < G; ++h) {
           const float w = s[h][t];
           for (int e = 0; e < DV; ++e) r[h][e] += w * v[e];
