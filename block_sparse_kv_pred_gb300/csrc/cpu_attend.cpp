@@ -11,11 +11,13 @@
 //   vector extensions: NEON on AArch64, SSE on x86-64; no intrinsics, no target flags):
 //   bf16 widened by interleaving with zero halves (a zip per four values), scores in register
 //   tiles of TT tokens x G heads (G q rows against TT widened K rows, 8 dimensions per step,
-//   one horizontal sum per score at the end), the softmax weights four at a time with an
-//   exponential of its own (Cody-Waite reduction and a Taylor polynomial), then the block's V
-//   accumulated in register tiles of 16 (8 for more than six heads) dimensions x G heads
-//   over every token of the block, the running sums loaded, rescaled and stored once per
-//   tile (tiles sized for AArch64's 32 vector registers);
+//   one horizontal sum per score at the end), then the block's V accumulated in register
+//   tiles of 16 (8 for more than six heads) dimensions x G heads over every token of the
+//   block, the running sums loaded, rescaled and stored once per tile (tiles sized for
+//   AArch64's 32 vector registers).  Measured on the Grace cores against the first version
+//   of this form, which widened bf16 by a vector conversion: 7.2 against 4.0 GB/s on one core
+//   (the conversion compiled to lane-by-lane inserts); an exponential of its own, four
+//   weights at a time, and a software prefetch of the next block did not help;
 // * the scalar one (scout_cpu_attend_scalar), plain loops with 16 partial sums per product,
 //   the reference the tiled one is tested against.
 #if !defined(__GNUC__)
@@ -85,35 +87,6 @@ inline void widen8(const uint16_t* p, f32x4& lo, f32x4& hi) {
 
 inline float hsum(f32x4 v) { return (v[0] + v[1]) + (v[2] + v[3]); }
 
-typedef int32_t i32x4 __attribute__((vector_size(16)));
-
-// e^x for four x <= 0 (softmax weights), by Cody and Waite's reduction (W. J. Cody and W. Waite,
-// Software Manual for the Elementary Functions, 1980): x = n ln 2 + r with n the nearest integer
-// to x / ln 2 and ln 2 split into a short high part (exact products n * hi) and a low part, so
-// |r| <= ln(2) / 2; e^r by its Taylor polynomial of degree 7 (truncation below 1e-8 relative on
-// that interval); 2^n placed in the exponent field.  Arguments below -87 are taken as -87
-// (e^-87 ~ 1.6e-38, still a normal float; the weight is negligible next to the row maximum's 1).
-inline f32x4 exp_nonpos(f32x4 x) {
-  const f32x4 lo = {-87.f, -87.f, -87.f, -87.f};
-  x = x < lo ? lo : x;
-  const float inv_ln2 = 1.4426950408889634f, ln2_hi = 0.693145751953125f, ln2_lo = 1.4286068203094172e-6f;
-  // x <= 0: truncation of x / ln2 - 1/2 toward zero is the nearest integer (halves downwards)
-  const i32x4 n = __builtin_convertvector(x * inv_ln2 - 0.5f, i32x4);
-  const f32x4 nf = __builtin_convertvector(n, f32x4);
-  const f32x4 r = (x - nf * ln2_hi) - nf * ln2_lo;
-  f32x4 p = r * (1.f / 5040.f) + 1.f / 720.f;
-  p = p * r + 1.f / 120.f;
-  p = p * r + 1.f / 24.f;
-  p = p * r + 1.f / 6.f;
-  p = p * r + 0.5f;
-  p = p * r + 1.f;
-  p = p * r + 1.f;
-  const i32x4 e = (n + 127) << 23;
-  f32x4 scale;
-  std::memcpy(&scale, &e, sizeof scale);
-  return p * scale;
-}
-
 // One unit with register tiles; G query heads per KV head (a template argument, so that the
 // tiles are fixed-size arrays the compiler keeps in registers).
 template <int G>
@@ -169,23 +142,12 @@ void attend_unit_tiled(const Job& a, int u) {
       float mb = m[h];
       for (int x = 0; x < valid; ++x) mb = std::max(mb, s[h][x]);
       corr[h] = m[h] == -INFINITY ? 0.f : std::exp(m[h] - mb);
-      // four weights at a time; lanes past `valid` (scores never computed) are taken as the
-      // maximum, stored and never read, and left out of the sum
-      f32x4 sum4 = {0.f, 0.f, 0.f, 0.f};
-      const f32x4 mb4 = {mb, mb, mb, mb};
-      for (int x = 0; x < valid; x += 4) {
-        f32x4 v;
-        std::memcpy(&v, &s[h][x], sizeof v);
-        const int left = valid - x;  // lanes of v inside the row
-        if (left < 4)
-          for (int e = left; e < 4; ++e) v[e] = mb;
-        v = exp_nonpos(v - mb4);
-        std::memcpy(&s[h][x], &v, sizeof v);
-        if (left < 4)
-          for (int e = left; e < 4; ++e) v[e] = 0.f;
-        sum4 += v;
+      float sum = 0.f;
+      for (int x = 0; x < valid; ++x) {
+        s[h][x] = std::exp(s[h][x] - mb);
+        sum += s[h][x];
       }
-      l[h] = l[h] * corr[h] + hsum(sum4);
+      l[h] = l[h] * corr[h] + sum;
       m[h] = mb;
     }
     // acc_h = corr_h acc_h + sum_t p_h(t) v_t, one tile of 4 * DV dimensions at a time
