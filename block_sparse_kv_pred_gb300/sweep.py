@@ -29,6 +29,7 @@ from __future__ import annotations
 
 import argparse
 import json
+import time
 
 import numpy as np
 import torch
@@ -60,7 +61,7 @@ class DecodeSweep:
     """The layer's state on the GPU and the host, and one method per decode step."""
 
     def __init__(self, shape: W.Shape, steps: int, recall_every: int = 16, device="cuda", host=None,
-                 gather=True, pages=False):
+                 gather=True, pages=False, cpu_pool=None):
         """``recall_every`` 0: no recall (the profile from which recall intervals are read).
         ``host``: optional pair of pinned bf16 host tensors of at least [units][nblk][P][D]
         elements each, reused for the host copy of the layer's K/V (a multi-layer sweep keeps
@@ -70,9 +71,13 @@ class DecodeSweep:
         (the 128 KB transfer unit of section 2.3, Figure 3): the initial resident pages are the k
         most important of each sequence (importance: the largest of its heads' scores, ties to the
         lower block) plus the page being written, and each recall follows scout_plan_recall_pages
-        with the page being written counted as selected by every head; otherwise per block."""
+        with the page being written counted as selected by every head; otherwise per block.
+        ``cpu_pool``: a ``CpuPool``; each step then also computes the CPU side (section 3.2: the
+        CPU list attended with Q_pred on the host copy of the K/V) on the pool's threads and
+        reports its time beside the GPU time of the step's kernels."""
         self.gather = gather
         self.pages = pages
+        self.cpu_pool = cpu_pool
         self.s = s = shape
         self.steps, self.recall_every = steps, recall_every
         dev = self.dev = torch.device(device)
@@ -177,14 +182,16 @@ class DecodeSweep:
             self._move_in(fresh)
         self.d_seq = WD.to_dev(self.seq, self.dev)
         tail = WD.to_dev(np.array([[u, (int(self.seq[u // s.Hkv]) - 1) // P] for u in range(U)], np.int32), self.dev)
+        qp, q = WD.to_dev(self.ps[t], self.dev), WD.to_dev(self.qs[t], self.dev)
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+        ev[0].record()  # the step's kernels: digest append, selection, attention
         bs.build_digest("minmax", self.K_pool, self.d_table, self.d_seq, s.B, s.Hkv, P, self.digest, block_list=tail)
         resident_before = self.res.copy()
-        out = bs.score_topk("minmax", WD.to_dev(self.ps[t], self.dev), self.digest, self.d_seq, self.d_bits, s.B,
-                            s.Hq, s.Hkv, P, s.nblk, s.k, self.ws, prev_cpu=self.prev, scores=self.scores,
-                            status=self.status)
-        O, lse = bs.sparse_attn(WD.to_dev(self.qs[t], self.dev), self.K_pool, self.V_pool, self.d_table, self.d_seq,
-                                out["res"], out["res_count"], s.B, s.Hq, s.Hkv, P, s.k, s.scale, self.wa,
-                                status=self.status)
+        out = bs.score_topk("minmax", qp, self.digest, self.d_seq, self.d_bits, s.B, s.Hq, s.Hkv, P, s.nblk, s.k,
+                            self.ws, prev_cpu=self.prev, scores=self.scores, status=self.status)
+        O, lse = bs.sparse_attn(q, self.K_pool, self.V_pool, self.d_table, self.d_seq, out["res"], out["res_count"],
+                                s.B, s.Hq, s.Hkv, P, s.k, s.scale, self.wa, status=self.status)
+        ev[1].record()
         torch.cuda.synchronize(self.dev)
         if int(self.status.item()) != 0:
             raise RuntimeError(f"device status {int(self.status.item())} at step {t}")
@@ -198,7 +205,26 @@ class DecodeSweep:
         self.prev = (out["cpu"].clone(), out["cpu_count"].clone())
         n_cpu, n_delta = int(rec["cpu_count"].sum()), int(rec["delta_count"].sum())
         stats = {"step": t, "cpu_blocks": n_cpu, "delta_blocks": n_delta, "cpu_ratio": n_cpu / (s.k * U),
-                 "recall_blocks": 0, "recall_bytes": 0, "recall_h2d_gbs": None}
+                 "recall_blocks": 0, "recall_bytes": 0, "recall_h2d_gbs": None, "gpu_ms": ev[0].elapsed_time(ev[1])}
+        if self.cpu_pool is not None:
+            # the CPU side of this step's selection (the next layer's partial, one layer ahead)
+            h_q = torch.from_numpy(np.ascontiguousarray(self.ps[t]).view(np.int16)).view(torch.bfloat16)
+            o_cpu = torch.empty((s.B, s.Hq, s.D), dtype=torch.float32)
+            l_cpu = torch.empty((s.B, s.Hq), dtype=torch.float32)
+            c0 = time.perf_counter()
+            self.cpu_pool.submit(h_q, self.hK, self.hV, torch.from_numpy(self.seq.copy()),
+                                 torch.from_numpy(rec["cpu"].reshape(s.B, s.Hkv, s.k).copy()),
+                                 torch.from_numpy(rec["cpu_count"].reshape(s.B, s.Hkv).copy()), s.B, s.Hq, s.Hkv, P,
+                                 s.k, s.scale, o_cpu, l_cpu)
+            if not self.cpu_pool.wait(60.0):
+                raise TimeoutError(f"the CPU side of step {t} took over 60 s")
+            cpu_s = time.perf_counter() - c0
+            rec["O_cpu"], rec["lse_cpu"] = o_cpu.numpy(), l_cpu.numpy()
+            stats["cpu_ms"] = cpu_s * 1e3
+            stats["cpu_gbs"] = n_cpu * 2 * P * s.D * 2 / cpu_s / 1e9
+            # with the CPU partial of layer i+1 made while the GPU runs layer i (Algorithm 1), the GPU
+            # waits for whatever of the CPU time its own step does not cover
+            stats["gpu_idle_frac"] = max(0.0, cpu_s * 1e3 - stats["gpu_ms"]) / max(cpu_s * 1e3, stats["gpu_ms"])
         if self.recall_every > 0 and t % self.recall_every == self.recall_every - 1:
             # the block being written stays on the GPU: the planner sees it as the most important
             # resident block, so it is evicted last, and never (at least k + 1 blocks are resident,
@@ -254,7 +280,7 @@ def profile_recall_intervals(layers: int, steps: int, beta: float = 0.12, shape:
 
 
 def run_layers(layers: int, steps: int, recall_every=16, beta: float = 0.12, shape: W.Shape | None = None,
-               gather: bool = True, pages: bool = False):
+               gather: bool = True, pages: bool = False, cpu_pool=None):
     """The decode sweep over ``layers`` layers, one after another (each its own seeded workload,
     freed before the next, the pinned host copy of its K/V reused): yields (layer, sweep, record)
     for every decode step.  ``recall_every``: a step count, or a sequence of per-layer intervals
@@ -269,7 +295,7 @@ def run_layers(layers: int, steps: int, recall_every=16, beta: float = 0.12, sha
         raise ValueError("one recall interval per layer")
     for layer in range(layers):
         sw = DecodeSweep(dataclasses.replace(base, seed=base.seed + layer), steps, recall_every=every[layer],
-                         host=host, gather=gather, pages=pages)
+                         host=host, gather=gather, pages=pages, cpu_pool=cpu_pool)
         for _ in range(steps):
             yield layer, sw, sw.step()
         del sw
@@ -345,9 +371,17 @@ def main():
     ap.add_argument("--copies", action="store_true", help="recall with cudaMemcpyAsync calls, not the gather kernel")
     ap.add_argument("--pages", action="store_true",
                     help="residency per page (a block of a sequence for all its KV heads), not per block")
+    ap.add_argument("--cpu-side", action="store_true",
+                    help="also compute every step's CPU side on a worker pool of the host's cores and report its "
+                         "time, GB/s and the GPU-idle fraction of the layer-ahead overlap")
     ap.add_argument("--probe-recall", action="store_true",
                     help="instead: host-to-device recall rate at 4 KB, 8 KB and 128 KB granularity")
     a = ap.parse_args()
+    pool = None
+    if a.cpu_side:
+        import os
+
+        pool = bs.CpuPool(len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else 0)
     if a.probe_recall:
         for row in probe_recall_bandwidth():
             print(json.dumps(row), flush=True)
@@ -359,7 +393,7 @@ def main():
             print(json.dumps({"profile_beta": a.beta, "intervals": [int(x) for x in iv],
                               "mean_interval": float(iv.mean())}), flush=True)
             every = iv
-        for layer, sw, rec in run_layers(a.layers, a.steps, every, gather=not a.copies, pages=a.pages):
+        for layer, sw, rec in run_layers(a.layers, a.steps, every, gather=not a.copies, pages=a.pages, cpu_pool=pool):
             print(json.dumps({"layer": layer, **rec["stats"]}), flush=True)
         return
     if a.profile_layers > 0:
@@ -369,7 +403,7 @@ def main():
                               "ratio": [round(float(x), 4) for x in traces[layer]]}), flush=True)
         print(json.dumps({"beta": a.beta, "mean_interval": float(iv.mean())}), flush=True)
         return
-    sw = DecodeSweep(c4_shape(a.steps), a.steps, a.recall_every, gather=not a.copies, pages=a.pages)
+    sw = DecodeSweep(c4_shape(a.steps), a.steps, a.recall_every, gather=not a.copies, pages=a.pages, cpu_pool=pool)
     for _ in range(a.steps):
         print(json.dumps(sw.step()["stats"]), flush=True)
 

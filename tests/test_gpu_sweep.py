@@ -195,3 +195,28 @@ def test_page_granular_residency_sweep():
         tails = (rec["seq"].astype(np.int64) - 1) // P
         assert all(sw.res[u, tails[u // s.Hkv]] for u in range(U)), t  # the page being written stays
     assert n_recalls == steps // every
+
+
+def test_sweep_cpu_side_matches_oracle_and_reports_idle():
+    """The sweep's CPU side (the worker pool over each step's CPU list with Q_pred on the host copy
+    of the K/V) against the oracle's attention over the same blocks, and its report fields."""
+    from block_sparse_kv_pred_gb300.sweep import DecodeSweep
+
+    s = W.Shape("sweep_cpu", B=2, Hq=8, Hkv=2, T=4096, P=32, k=16, resident_frac=0.0, seq_lens=(4000, 3950),
+                hidden=0)
+    with bs.CpuPool(4) as pool:
+        sw = DecodeSweep(s, 3, recall_every=0, cpu_pool=pool)
+        nb, P, D = s.nblk, s.P, s.D
+        for t in range(3):
+            rec = sw.step()
+            st = rec["stats"]
+            assert st["cpu_ms"] > 0 and st["gpu_ms"] > 0 and 0.0 <= st["gpu_idle_frac"] <= 1.0
+            for u in range(s.units):
+                b, kvh = divmod(u, s.Hkv)
+                K = O.bf16_to_f64(sw.hK[u].view(torch.int16).numpy().view(np.uint16).reshape(nb * P, D))
+                V = O.bf16_to_f64(sw.hV[u].view(torch.int16).numpy().view(np.uint16).reshape(nb * P, D))
+                toks = O.block_tokens(rec["cpu"][u, :rec["cpu_count"][u]], P, int(rec["seq"][b]))
+                for h in range(s.G):
+                    hq = kvh * s.G + h
+                    o, l = O.attention_partial(O.bf16_to_f64(sw.ps[t][b, hq]), K[toks], V[toks], s.scale)
+                    check_attention(rec["O_cpu"][b, hq], rec["lse_cpu"][b, hq], o, l, what=(t, u, h))
