@@ -621,8 +621,9 @@ def attention_path(s, nbytes, kern_ms, peak):
             "note": "score_topk + sparse_attn_merge concurrent durations summed (they overlap inside the step)"}
 
 
-def traffic_of(kernel):
-    """DRAM bytes per launch from the committed ncu summary, if the kernel source is unchanged since."""
+def traffic_of(kernel, workload):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on this workload and
+    the kernel source is unchanged since."""
     import hashlib
 
     path = os.path.join(ROOT, "profiles", "dram_traffic_per_launch_qwen3_14b_b40_t32k.txt")
@@ -630,7 +631,7 @@ def traffic_of(kernel):
         return None
     with open(path) as f:
         rec = json.load(f).get(kernel)
-    if not rec:
+    if not rec or not rec.get("workload", "").startswith(workload):
         return None
     h = hashlib.sha256()
     for src in rec.get("sources", []):
@@ -674,7 +675,7 @@ def main():
     ach = kernels[dom]["GB_s"]
     src = f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured" else "fallback 6.8 TB/s"
     roof = {"kernel": dom, "bound": "hbm", "achieved": ach, "peak": peak, "unit": "GB/s", "frac": ach / peak,
-            "peak_source": src, "traffic": traffic_of(dom), "algorithmic_bytes_per_launch": nbytes[dom],
+            "peak_source": src, "traffic": traffic_of(dom, s.name), "algorithmic_bytes_per_launch": nbytes[dom],
             "note": "launch duration measured while the other stream's kernels share the GPU"
             if r["split"] else "serial step"}
     step_bytes = sum(nbytes[k] for k in KERNELS)

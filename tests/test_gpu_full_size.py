@@ -3,6 +3,8 @@ configuration bench.py times (four streams, capped grids), the Qwen3-8B-shaped l
 and the stress shapes (page 16/32/64, budgets 512/2048/8192, min/max and mean digests,
 128K context, plus the dense edge case), each checked against the fp64 oracle on a
 handful of (sequence, KV head) units the oracle finishes in seconds."""
+import functools
+
 import numpy as np
 import pytest
 import torch
@@ -12,7 +14,7 @@ import block_sparse_kv_pred_gb300 as bs
 from block_sparse_kv_pred_gb300 import workload as W
 from block_sparse_kv_pred_gb300.step import EARLY_OF, SPLIT, setup_step
 from block_sparse_kv_pred_gb300.workload import device as WD
-from _parity import bf16_bits, check_attention, check_selection, ensure_built
+from _parity import bf16_bits, check_attention, check_qpred, check_selection, ensure_built, oracle_qpred
 
 pytestmark = pytest.mark.gpu
 
@@ -26,9 +28,16 @@ def _sample(U):
     return sorted({0, 1, U // 3, U // 2, U - 1})
 
 
+@functools.lru_cache(maxsize=None)
+def _oracle_q(cfg):
+    """The oracle's Q_pred of a config's layer (fp64), computed once per module."""
+    return oracle_qpred(W.CONFIGS[cfg]())
+
+
 def _check_unit(wl, u, q_sel_bits, kind, topk, tc, res, rc, cpu, cc, O_out, L_out, o_cpu, l_cpu):
-    """Selection of unit u against the oracle's, then the output over the GPU's own resident
-    list (merged with the CPU partial) against the oracle's attention over that list."""
+    """Selection of unit u against the oracle's (with the oracle's own selection query), then,
+    when the sets agree, the output (merged with the CPU partial) against the oracle's attention
+    over its resident list; at a near-tie only the split of the GPU's own set is checked."""
     s = wl.s
     b, kvh = divmod(u, s.Hkv)
     L = int(wl.seq_len[b])
@@ -40,15 +49,15 @@ def _check_unit(wl, u, q_sel_bits, kind, topk, tc, res, rc, cpu, cc, O_out, L_ou
     else:
         Uref = O.pool_group(O.scores_mean(qs, O.digest_mean(Kb, L, s.P)))
     S_gpu = topk[u, :tc[u]]
-    if check_selection(Uref, s.k, S_gpu, what=u):  # same set: the lists are bit-exact
-        r_ref, c_ref = O.split_residency(O.select_topk(Uref, s.k), wl.resident[u].astype(bool))
-        assert list(res[u, :rc[u]]) == list(r_ref) and list(cpu[u, :cc[u]]) == list(c_ref), u
-    else:  # a near-tie: the split of the GPU's own set must still be exact
-        r_ref, c_ref = O.split_residency(S_gpu, wl.resident[u].astype(bool))
-        assert list(res[u, :rc[u]]) == list(r_ref), u
     assert all(t == -1 for t in topk[u, tc[u]:]) and all(t == -1 for t in res[u, rc[u]:])
+    if not check_selection(Uref, s.k, S_gpu, what=u):  # a near-tie: the split of the GPU's own set is exact
+        r_gpu, _ = O.split_residency(S_gpu, wl.resident[u].astype(bool))
+        assert list(res[u, :rc[u]]) == list(r_gpu), u
+        return
+    r_ref, c_ref = O.split_residency(O.select_topk(Uref, s.k), wl.resident[u].astype(bool))
+    assert list(res[u, :rc[u]]) == list(r_ref) and list(cpu[u, :cc[u]]) == list(c_ref), u
     K, V = O.bf16_to_f64(Kb), O.bf16_to_f64(wl.unit_kv(u, "V"))
-    toks = O.block_tokens(res[u, :rc[u]], s.P, L)
+    toks = O.block_tokens(r_ref, s.P, L)
     for h in range(s.G):
         hq = kvh * s.G + h
         og, lg = O.attention_partial(O.bf16_to_f64(wl.q[b, hq]), K[toks], V[toks], s.scale)
@@ -83,8 +92,10 @@ def test_full_size_step_sampled(cfg, mode, early):
     grab = lambda n: t[f"{n}{par}"].cpu().numpy().reshape(s.units, -1)  # noqa: E731
     topk, res, cpu = grab("topk"), grab("res"), grab("cpu")
     tc, rc, cc = (t[f"{n}_count{par}"].cpu().numpy().reshape(-1) for n in ("topk", "res", "cpu"))
-    qp = bf16_bits(t["Qp0"]).reshape(s.B, s.Hq, s.D)
-    assert np.array_equal(qp.reshape(-1), bf16_bits(t["Qp1"]).reshape(-1))  # same X and W_Q every step
+    assert np.array_equal(bf16_bits(t["Qp0"]), bf16_bits(t["Qp1"]))  # same X and W_Q every step
+    q_ref = _oracle_q(cfg)
+    check_qpred(bf16_bits(t["Qp0"]), q_ref)
+    qp = O.f64_to_bf16(q_ref).reshape(s.B, s.Hq, s.D)  # the oracle selects with its own Q_pred
     last = (step.i - 1) % 2  # output buffer of the last step
     O_out, L_out = t[f"O{last}"].float().cpu().numpy(), t[f"lse{last}"].cpu().numpy()
     o_cpu, l_cpu = wl.cpu_partial()
