@@ -364,10 +364,10 @@ def run_e2e(args, t, step, s, world, device):
             "d2h_bytes_per_step": d2h, "ms_per_step": ms, "steps": reps * GRAPH_STEPS}
 
 
-def cpu_side(s, t, seconds=0.5, max_seqs=8):
+def cpu_side(s, t, seconds=1.0, max_seqs=None):
     """The CPU side of the collaborative attention (scout_cpu_attend) on this host's cores:
     attention over the CPU work list of the last timed step with its Q_pred, for the first
-    ``max_seqs`` sequences (their K/V gathered from the pool into logical block order on the
+    ``max_seqs`` sequences (all by default; their K/V gathered into logical block order on the
     host).  Reported beside the GPU numbers, never part of them; a failure is reported, not
     raised, so that it cannot cost the GPU measurement."""
     import numpy as np
@@ -375,7 +375,7 @@ def cpu_side(s, t, seconds=0.5, max_seqs=8):
     import block_sparse_kv_pred_gb300 as bs
 
     try:
-        Bs = min(s.B, max_seqs)
+        Bs = s.B if max_seqs is None else min(s.B, max_seqs)
         # the whole cache (the step's compact pool holds only the GPU's share of it)
         slots = t.get("page_table_all", t["page_table"])[:Bs].reshape(-1).long()
         if int(slots.min()) < 0:
