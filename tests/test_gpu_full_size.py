@@ -24,8 +24,26 @@ def _built():
     ensure_built()
 
 
-def _sample(U):
-    return sorted({0, 1, U // 3, U // 2, U - 1})
+def _sample(U, extra=0):
+    """Units checked against the oracle: the ends and thirds, plus `extra` seeded others."""
+    base = {0, 1, U // 3, U // 2, U - 1}
+    if extra:
+        base |= set(int(x) for x in np.random.default_rng(U).choice(U, size=min(extra, U), replace=False))
+    return sorted(base)
+
+
+def _check_all_lists(s, wl, topk, tc, res, rc, cpu, cc):
+    """Every unit's lists, without the oracle: k_eff entries of top-k, each list ascending and
+    padded with -1, and res / cpu the resident / non-resident parts of top-k."""
+    nvalid = -(-wl.seq_len.astype(np.int64) // s.P)
+    for u in range(s.units):
+        keff = min(s.k, int(nvalid[u // s.Hkv]))
+        S, R, C = topk[u, :tc[u]], res[u, :rc[u]], cpu[u, :cc[u]]
+        assert tc[u] == keff and rc[u] + cc[u] == keff, u
+        for lst, n in ((topk[u], tc[u]), (res[u], rc[u]), (cpu[u], cc[u])):
+            assert np.all(np.diff(lst[:n]) > 0) and np.all(lst[n:] == -1), u
+        mask = wl.resident[u].astype(bool)
+        assert list(R) == [j for j in S if mask[j]] and list(C) == [j for j in S if not mask[j]], u
 
 
 @functools.lru_cache(maxsize=None)
@@ -71,7 +89,8 @@ def _check_unit(wl, u, q_sel_bits, kind, topk, tc, res, rc, cpu, cc, O_out, L_ou
 def test_full_size_step_sampled(cfg, mode, early):
     """Three steps of the decode step at full size (or, as bench.py times it, a captured CUDA
     graph of two steps replayed twice), with and without early starts; selection with Q_pred,
-    attention with q."""
+    attention with q.  Every unit's lists are checked for consistency; sampled units (32 in the
+    configuration bench.py times) against the oracle."""
     shape = W.CONFIGS[cfg]()
     wl, t, step = setup_step(shape, torch.device("cuda", 0), serial=(mode == "serial"), split=SPLIT, early=early)
     if mode == "graph":
@@ -99,7 +118,9 @@ def test_full_size_step_sampled(cfg, mode, early):
     last = (step.i - 1) % 2  # output buffer of the last step
     O_out, L_out = t[f"O{last}"].float().cpu().numpy(), t[f"lse{last}"].cpu().numpy()
     o_cpu, l_cpu = wl.cpu_partial()
-    for u in _sample(s.units):
+    _check_all_lists(s, wl, topk, tc, res, rc, cpu, cc)
+    # the configuration bench.py times is checked on more units against the oracle
+    for u in _sample(s.units, extra=27 if mode == "graph" and not early else 0):
         b, kvh = divmod(u, s.Hkv)
         _check_unit(wl, u, qp[b, kvh * s.G:(kvh + 1) * s.G], "minmax", topk, tc, res, rc, cpu, cc, O_out, L_out,
                     o_cpu, l_cpu)
