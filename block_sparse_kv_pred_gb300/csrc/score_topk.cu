@@ -375,14 +375,12 @@ __device__ void select_unit(const TopkArgs& a, int u, const uint32_t* keys, int 
       const uint32_t k0 = lane < count ? keys[j0] - base : 0u, k1 = lane + 32 < count ? keys[j1] - base : 0u;
       int r0 = 0, r1 = 0;
       for (int h = 0; h < (count + 31) / 32; ++h) {
-#pragma unroll
-        for (int m = 0; m < 32; ++m) {
+        const int mmax = min(32, count - 32 * h);  // warp-uniform: only the candidates there are
+        for (int m = 0; m < mmax; ++m) {
           const uint32_t km = __shfl_sync(0xffffffffu, h ? k1 : k0, m);
           const int jm = __shfl_sync(0xffffffffu, h ? j1 : j0, m);
-          if (32 * h + m < count) {
-            r0 += (km > k0 || (km == k0 && jm < j0)) ? 1 : 0;
-            r1 += (km > k1 || (km == k1 && jm < j1)) ? 1 : 0;
-          }
+          r0 += (km > k0 || (km == k0 && jm < j0)) ? 1 : 0;
+          r1 += (km > k1 || (km == k1 && jm < j1)) ? 1 : 0;
         }
       }
       if (lane < count && r0 < remaining) atomicOr(&sw.cbits[j0 >> 5], 1u << (j0 & 31));
@@ -428,10 +426,25 @@ __device__ void select_unit(const TopkArgs& a, int u, const uint32_t* keys, int 
     scan_pair(__popc(ms), __popc(mres), lane, et, er, tt, tr);
     scan_pair(__popc(mcpu), __popc(mdel), lane, ec, ed, tc, td);
     const int j0 = g * 1024 + 32 * lane;
-    for (uint32_t m = ms, q = nt + et; m != 0u; m &= m - 1u, ++q) a.topk_idx[lb + q] = j0 + __ffs(m) - 1;
-    for (uint32_t m = mres, q = nr + er; m != 0u; m &= m - 1u, ++q) a.res_list[lb + q] = j0 + __ffs(m) - 1;
-    for (uint32_t m = mcpu, q = nc + ec; m != 0u; m &= m - 1u, ++q) a.cpu_list[lb + q] = j0 + __ffs(m) - 1;
-    for (uint32_t m = mdel, q = nd + ed; m != 0u; m &= m - 1u, ++q) a.delta_list[lb + q] = j0 + __ffs(m) - 1;
+    // one pass over the round's selected blocks in order: every block goes to top-k and to the
+    // resident or the CPU list, and a CPU block that was not on the previous list to delta
+    int32_t* const tl = a.topk_idx + lb;
+    int32_t* const rl = a.res_list + lb;
+    int32_t* const cl = a.cpu_list + lb;
+    int32_t* const dl = a.delta_list + lb;
+    int qt = nt + et, qr = nr + er, qc = nc + ec, qd = nd + ed;
+    for (uint32_t m = ms; m != 0u; m &= m - 1u) {
+      const int bit = __ffs(m) - 1;
+      const uint32_t one = 1u << bit;
+      const int j = j0 + bit;
+      tl[qt++] = j;
+      if (rw & one) {
+        rl[qr++] = j;
+      } else {
+        cl[qc++] = j;
+        if (!(pw & one)) dl[qd++] = j;
+      }
+    }
     nt += tt;
     nr += tr;
     nc += tc;
