@@ -29,12 +29,16 @@
 namespace scout {
 namespace {
 
-// Consumer warps and tokens per stage: four warps (one per scheduler) with 32-token
-// stages, three per warp in a 192 KB ring.  (Measured on GB300: eight warps with 16-token
-// stages are ~15% slower on the Qwen3-14B-shaped residency; the per-page overhead doubles
-// and the combine state no longer leaves room for two slots.)
+// Consumer warps and tokens per stage: six warps with 32-token stages, two per warp in a 192 KB
+// ring.  The warps are latency-bound (each page is a chain of ldmatrix, MMA and softmax steps),
+// so more of them per scheduler hide more of it.  Measured on GB300, Qwen3-14B-shaped step
+// (graph replay, same box, back to back): four warps (three stages each) 58.36 us per step and
+// 33.3 us alone, six 57.78 us and 30.1 us alone, six with two pages per pass 59.08 us; eight
+// warps with 16-token stages were ~15% slower than four (the per-page overhead doubles).  Six
+// warps leave room for one combine slot at G <= 5 with the whole ring; larger groups take the
+// smaller ring (six stages, one per warp).
 #ifndef SCOUT_ATTN_CONSUMERS
-#define SCOUT_ATTN_CONSUMERS 4
+#define SCOUT_ATTN_CONSUMERS 6
 #endif
 #ifndef SCOUT_ATTN_SUBPAGE
 #define SCOUT_ATTN_SUBPAGE 32
