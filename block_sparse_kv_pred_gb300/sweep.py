@@ -184,9 +184,10 @@ class DecodeSweep:
         tail = WD.to_dev(np.array([[u, (int(self.seq[u // s.Hkv]) - 1) // P] for u in range(U)], np.int32), self.dev)
         qp, q = WD.to_dev(self.ps[t], self.dev), WD.to_dev(self.qs[t], self.dev)
         ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
-        if self.cpu_pool is not None:
-            # the GPU spins ~1 ms first, so that the three launches below are queued before it reaches
-            # them and the events time the kernels back to back, not the host's launch gaps
+        if self.cpu_pool is not None and hasattr(torch.cuda, "_sleep"):
+            # the GPU spins ~1 ms first (PyTorch's test helper), so that the three launches below are
+            # queued before it reaches them and the events time the kernels back to back, not the
+            # host's launch gaps (without it the gaps are counted)
             torch.cuda._sleep(2_000_000)
         ev[0].record()  # the step's kernels: digest append, selection, attention
         bs.build_digest("minmax", self.K_pool, self.d_table, self.d_seq, s.B, s.Hkv, P, self.digest, block_list=tail)
