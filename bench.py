@@ -591,7 +591,8 @@ def streams_of(split):
         return "one stream"
     g, sel, att = split if len(split) == 3 else (split[0], split[0], split[1])
     n = lambda c: f"{c} CTAs" if c else "one CTA per SM"  # noqa: E731
-    return (f"GEMM ({n(g)}) after the previous attention || selection ({n(sel)}) after the GEMM || "
+    nsel = f"{sel} CTAs" if sel else "its default grid: ceil(units / ceil(units / SMs)) CTAs, whole units dealt"
+    return (f"GEMM ({n(g)}) after the previous attention || selection ({nsel}) after the GEMM || "
             f"attention ({n(att)}) after the previous selection || digest append")
 
 
