@@ -12,10 +12,11 @@
 // then produced early, and a dedicated split warp publishes them and does the
 // cross-CTA merge (dependent global round trips) while the whole units stream.
 //
-// Inside a CTA: the four consumer warps take the range's sub-pages round-robin.
-// Each warp owns kStages / 4 stages of a shared-memory ring and keeps them
-// filled itself: when it has finished a sub-page it reloads that stage with its
-// sub-page kStages / 4 further on (one 3-D TMA box per K and per V sub-page,
+// Inside a CTA: the NC consumer warps (six, or four when a larger group's combine
+// state needs the room) take the range's sub-pages round-robin.  Each warp owns
+// kStages / NC stages of a shared-memory ring and keeps them filled itself: when
+// it has finished a sub-page it reloads that stage with its sub-page kStages / NC
+// further on (one 3-D TMA box per K and per V sub-page,
 // 128-byte swizzle, completion on an mbarrier), so a stage is never idle while
 // another warp is behind.  The lanes resolve the warp's next 32 sub-pages (list
 // entry, page-table slot, valid tokens) one batch ahead, so the dependent
@@ -35,11 +36,12 @@ namespace {
 // (graph replay, same box, back to back): four warps (three stages each) 58.36 us per step and
 // 33.3 us alone, six 57.78 us and 30.1 us alone, six with two pages per pass 59.08 us; eight
 // warps with 16-token stages were ~15% slower than four (the per-page overhead doubles).  Six
-// warps leave room for one combine slot at G <= 5 with the whole ring; larger groups take the
-// smaller ring (six stages, one per warp).
+// warps' combine state leaves room for the whole ring up to G = 5 at 320 units; past that the
+// launch takes four warps (three stages each, a smaller combine state) before a smaller ring.
 #ifndef SCOUT_ATTN_CONSUMERS
 #define SCOUT_ATTN_CONSUMERS 6
 #endif
+constexpr int kFallbackConsumers = 4;
 #ifndef SCOUT_ATTN_SUBPAGE
 #define SCOUT_ATTN_SUBPAGE 32
 #endif
@@ -47,16 +49,17 @@ namespace {
 #define SCOUT_ATTN_PAIR 1
 #endif
 
-constexpr int kConsumerWarps = SCOUT_ATTN_CONSUMERS;
+constexpr int kConsumers = SCOUT_ATTN_CONSUMERS;  // the preferred count; the kernel takes it as NC
 constexpr int kSubTokens = SCOUT_ATTN_SUBPAGE;
 // pages a consumer warp attends in one pass (1 or 2); measured on GB300 in the graph-replayed
 // Qwen3-14B-shaped step: one 59.55 us per step, two 60.35 (with one, a stage holds a page for
 // less time, so more of the ring is loading)
 constexpr int kPair = SCOUT_ATTN_PAIR;
 
-constexpr int kEpilogueWarp = kConsumerWarps;     // combines the warps' states, writes whole units
-constexpr int kSplitWarp = kConsumerWarps + 1;     // merges the units cut by range boundaries
-constexpr int kThreads = (kConsumerWarps + 2) * 32;
+// warps of a CTA with NC consumer warps: the consumers, then an epilogue warp (combines the
+// warps' states, writes whole units) and a split warp (merges the units cut by range boundaries)
+template <int NC>
+__host__ __device__ constexpr int threads_of() { return (NC + 2) * 32; }
 constexpr int kMaxSplit = 2;  // pieces of cut units per CTA range: its first and its last segment
 constexpr int kPhaseB = 8;   // page of a batch at which the next batch's page-table loads are issued
 constexpr int kPhaseC = 16;  // and at which their values are used
@@ -69,24 +72,24 @@ constexpr float kLn2 = 0.6931471805599453f;
 // A stage holds K and V of one sub-page of PS tokens (a block streams as P / PS
 // sub-pages); the ring has S stages and every consumer warp owns kPerWarp of them.
 constexpr int kRingTarget = 192 * 1024;
-template <int P>
+template <int P, int NC>
 constexpr int big_ring() {  // stages of the 192 KB ring
-  return kRingTarget / (4 * (P < kSubTokens ? P : kSubTokens) * 128) / kConsumerWarps * kConsumerWarps;
+  return kRingTarget / (4 * (P < kSubTokens ? P : kSubTokens) * 128) / NC * NC;
 }
-template <int P>
+template <int P, int NC>
 constexpr int small_ring() {  // two thirds of it, for groups and batches whose combine state is large
-  return big_ring<P>() * 2 / 3 / kConsumerWarps * kConsumerWarps;
+  return big_ring<P, NC>() * 2 / 3 / NC * NC;
 }
-template <int P, int S>
+template <int P, int S, int NC>
 struct Cfg {
   static constexpr int PS = P < kSubTokens ? P : kSubTokens;  // tokens per stage
   static constexpr int kSub = P / PS;                          // stages per block
   static constexpr int kStages = S;
-  static constexpr int kPerWarp = kStages / kConsumerWarps;
+  static constexpr int kPerWarp = kStages / NC;
   static constexpr int kHalfBytes = PS * 128;        // one 64-column half of a sub-page
   static constexpr int kStageBytes = 4 * kHalfBytes; // K (2 halves) + V (2 halves)
   static constexpr int kRingBytes = kStages * kStageBytes;
-  static_assert(kStages % kConsumerWarps == 0 && kPhaseB < kPhaseC && kPhaseC < 32 - kPerWarp - 1,
+  static_assert(kStages % NC == 0 && kPhaseB < kPhaseC && kPhaseC < 32 - kPerWarp - 1,
                 "stage ownership and resolution phases");
 
 };
@@ -260,13 +263,14 @@ __device__ __forceinline__ void attend_values(const uint32_t (&vbase)[NP], float
 // One segment's per-warp softmax states, handed from the consumer warps to the
 // epilogue warp through shared memory.  A slot holds m[warps][8], l[warps][8] and
 // O^T partials o[warps][G][128] (fp32); its size depends on G.
-__host__ __device__ constexpr int slot_floats(int G) { return 2 * kConsumerWarps * kMaxG + kConsumerWarps * G * kD; }
+__host__ __device__ constexpr int slot_floats(int G, int NC) { return 2 * NC * kMaxG + NC * G * kD; }
+template <int NC>
 struct SlotView {
   float* base;
   int G;
   __device__ float& m(int w, int h) const { return base[w * kMaxG + h]; }
-  __device__ float& l(int w, int h) const { return base[(kConsumerWarps + w) * kMaxG + h]; }
-  __device__ float* o(int w, int h) const { return base + 2 * kConsumerWarps * kMaxG + (w * G + h) * kD; }
+  __device__ float& l(int w, int h) const { return base[(NC + w) * kMaxG + h]; }
+  __device__ float* o(int w, int h) const { return base + 2 * NC * kMaxG + (w * G + h) * kD; }
 };
 
 // Walks the unit segments of one CTA's flattened block range in processing order: the
@@ -503,11 +507,12 @@ __device__ void run_split_warp(const AttnArgs& a, const int* prefix, int64_t N, 
   }
 }
 
-template <int P, int S>
-__global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const __grid_constant__ CUtensorMap tmK,
+template <int P, int S, int NC>
+__global__ void __launch_bounds__(threads_of<NC>(), 1) sparse_attn_kernel(const __grid_constant__ CUtensorMap tmK,
                                                                   const __grid_constant__ CUtensorMap tmV,
                                                                   const AttnArgs a) {
-  using C = Cfg<P, S>;
+  using C = Cfg<P, S, NC>;
+  constexpr int kConsumerWarps = NC, kEpilogueWarp = NC, kSplitWarp = NC + 1, kThreads = threads_of<NC>();
   extern __shared__ uint8_t smem_raw[];
   // kfull / vfull: the K / V half of a stage has landed (one phase per fill of the stage)
   __shared__ uint64_t kfull[C::kStages], vfull[C::kStages], cfull[kMaxSlots], cempty[kMaxSlots], sbar[kMaxSplit];
@@ -520,7 +525,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const __grid_c
   const uint32_t raw = smem_u32(smem_raw);
   uint8_t* ring = smem_raw + (((raw + 1023u) & ~1023u) - raw);
   float* cbf = reinterpret_cast<float*>(ring + C::kRingBytes);
-  const int slot_f = slot_floats(a.G);
+  const int slot_f = slot_floats(a.G, NC);
   float* staging = cbf + a.nslots * slot_f;  // [kMaxSplit][stage_floats(G)]
   int* prefix = reinterpret_cast<int*>(staging + kMaxSplit * stage_floats(a.G));  // [units + 1]
 
@@ -601,7 +606,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const __grid_c
       const bool whole = lo == prefix[u] && hi == prefix[u + 1];
       if (whole) load_cpu(a, u, lane, cpu);  // in flight while the unit's pages still stream
       if (!mbar_wait(&cfull[slot], (uint32_t)(sg / a.nslots) & 1u) && lane == 0) report(a.status, SCOUT_DEV_TIMEOUT);
-      const SlotView cs{cbf + slot * slot_f, a.G};
+      const SlotView<NC> cs{cbf + slot * slot_f, a.G};
       // per-head weights of the four warps' states (normalised) and this piece's LSE
       if (lane < a.G) {
         float M = -INFINITY;
@@ -869,7 +874,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const __grid_c
     }
     const int slot = sg % a.nslots;
     if (!mbar_wait(&cempty[slot], ((uint32_t)(sg / a.nslots) & 1u) ^ 1u) && lane == 0) report(a.status, SCOUT_DEV_TIMEOUT);
-    const SlotView cs{cbf + slot * slot_f, a.G};
+    const SlotView<NC> cs{cbf + slot * slot_f, a.G};
     if (g == 0) {
       if (2 * t < a.G) {
         cs.m(warp, 2 * t) = st.m[0];
@@ -910,9 +915,9 @@ inline size_t counters_bytes(int64_t units) { return (size_t)((units * 4 + 255) 
 constexpr size_t kSlotLseBytes = (size_t)kMaxGrid * 2 * kMaxG * sizeof(float);
 constexpr size_t kSlotOBytes = (size_t)kMaxGrid * 2 * kMaxG * kD * sizeof(float);
 
-template <int P, int S>
+template <int P, int S, int NC>
 size_t dyn_smem(int units, int G, int nslots) {
-  return 1024 + Cfg<P, S>::kRingBytes + (size_t)nslots * slot_floats(G) * sizeof(float) +
+  return 1024 + Cfg<P, S, NC>::kRingBytes + (size_t)nslots * slot_floats(G, NC) * sizeof(float) +
          (size_t)kMaxSplit * stage_floats(G) * sizeof(float) + (size_t)(units + 1) * 4;
 }
 constexpr size_t kSmemLimit = 232448 - 1024;  // per-block shared memory minus room for static use
@@ -932,19 +937,18 @@ bool make_page_map(CUtensorMap* map, const void* pool, int64_t n_slots, int P, i
                       CU_TENSOR_MAP_SWIZZLE_128B) == CUDA_SUCCESS;
 }
 
-template <int P, int S>
+template <int P, int S, int NC>
 int launch_ring(const CUtensorMap& tmK, const CUtensorMap& tmV, AttnArgs a, const scout_launch* launch,
                 cudaStream_t stream) {
   const int max_ctas = launch != nullptr ? launch->max_ctas : 0;
-  const size_t smem = dyn_smem<P, S>(a.units, a.G, a.nslots);
-  if (cudaFuncSetAttribute(sparse_attn_kernel<P, S>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
-          cudaSuccess ||
-      cudaFuncSetAttribute(sparse_attn_kernel<P, S>, cudaFuncAttributePreferredSharedMemoryCarveout, 100) !=
-          cudaSuccess)
+  const size_t smem = dyn_smem<P, S, NC>(a.units, a.G, a.nslots);
+  constexpr int kThreads = threads_of<NC>();
+  auto kern = sparse_attn_kernel<P, S, NC>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess ||
+      cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, 100) != cudaSuccess)
     return SCOUT_ERR_CUDA;
   int occ = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, sparse_attn_kernel<P, S>, kThreads, smem) != cudaSuccess ||
-      occ < 1)
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, kThreads, smem) != cudaSuccess || occ < 1)
     return SCOUT_ERR_CUDA;
   const int grid = min(kMaxGrid, max_ctas > 0 ? max_ctas : sm_count() * occ);
   cudaLaunchConfig_t cfg = {};
@@ -955,28 +959,33 @@ int launch_ring(const CUtensorMap& tmK, const CUtensorMap& tmV, AttnArgs a, cons
   cudaLaunchAttribute attr[2];
   cfg.attrs = attr;
   cfg.numAttrs = early_start_attrs(launch, attr, 0);
-  if (cudaLaunchKernelEx(&cfg, sparse_attn_kernel<P, S>, tmK, tmV, a) != cudaSuccess) return SCOUT_ERR_CUDA;
+  if (cudaLaunchKernelEx(&cfg, kern, tmK, tmV, a) != cudaSuccess) return SCOUT_ERR_CUDA;
   return launch_status();
 }
 
-// The biggest ring, then the most combine slots, that fit in shared memory.
+// The most combine slots that fit with ring S and NC consumer warps; 0 if none does.
+template <int P, int S, int NC>
+int slots_fitting(const AttnArgs& a) {
+  for (int ns = kMaxSlots; ns >= 1; --ns)
+    if (dyn_smem<P, S, NC>(a.units, a.G, ns) <= kSmemLimit) return ns;
+  return 0;
+}
+
+// The first configuration that fits in shared memory, with the most combine slots it allows:
+// the preferred consumer warps with the whole ring, then four warps with the whole ring (their
+// combine state is smaller), then four warps with the smaller ring.
 template <int P>
 int launch_attn(const void* K_pool, const void* V_pool, AttnArgs a, const scout_launch* launch, cudaStream_t stream) {
-  constexpr int SB = big_ring<P>(), SS = small_ring<P>();
-  constexpr int PS = Cfg<P, SB>::PS;
+  constexpr int NA = kConsumers, NB = kFallbackConsumers;
+  constexpr int SA = big_ring<P, NA>(), SB = big_ring<P, NB>(), SC = small_ring<P, NB>();
+  constexpr int PS = Cfg<P, SA, NA>::PS;
+  static_assert(Cfg<P, SB, NB>::PS == PS && Cfg<P, SC, NB>::PS == PS, "one stage size for all rings");
   CUtensorMap tmK, tmV;
   if (!make_page_map(&tmK, K_pool, a.n_slots, P, PS) || !make_page_map(&tmV, V_pool, a.n_slots, P, PS))
     return SCOUT_ERR_UNSUPPORTED;
-  for (int ns = kMaxSlots; ns >= 1; --ns)
-    if (dyn_smem<P, SB>(a.units, a.G, ns) <= kSmemLimit) {
-      a.nslots = ns;
-      return launch_ring<P, SB>(tmK, tmV, a, launch, stream);
-    }
-  for (int ns = kMaxSlots; ns >= 1; --ns)
-    if (dyn_smem<P, SS>(a.units, a.G, ns) <= kSmemLimit) {
-      a.nslots = ns;
-      return launch_ring<P, SS>(tmK, tmV, a, launch, stream);
-    }
+  if ((a.nslots = slots_fitting<P, SA, NA>(a)) > 0) return launch_ring<P, SA, NA>(tmK, tmV, a, launch, stream);
+  if ((a.nslots = slots_fitting<P, SB, NB>(a)) > 0) return launch_ring<P, SB, NB>(tmK, tmV, a, launch, stream);
+  if ((a.nslots = slots_fitting<P, SC, NB>(a)) > 0) return launch_ring<P, SC, NB>(tmK, tmV, a, launch, stream);
   return SCOUT_ERR_UNSUPPORTED;
 }
 
