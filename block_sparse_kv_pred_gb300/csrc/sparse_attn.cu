@@ -233,12 +233,15 @@ __device__ __forceinline__ void attend_values(const uint32_t (&vbase)[NP], float
   }
   st.l[0] = st.l[0] * al0 + ps0;
   st.l[1] = st.l[1] * al1 + ps1;
+  // the running sums move only when some head's maximum rose (rarely, after the first pages)
+  if (!__all_sync(0xffffffffu, al0 == 1.f && al1 == 1.f)) {
 #pragma unroll
-  for (int md = 0; md < 8; ++md) {
-    st.o[md][0] *= al0;
-    st.o[md][1] *= al1;
-    st.o[md][2] *= al0;
-    st.o[md][3] *= al1;
+    for (int md = 0; md < 8; ++md) {
+      st.o[md][0] *= al0;
+      st.o[md][1] *= al1;
+      st.o[md][2] *= al0;
+      st.o[md][3] *= al1;
+    }
   }
 #pragma unroll
   for (int tt = 0; tt < T; ++tt) {
