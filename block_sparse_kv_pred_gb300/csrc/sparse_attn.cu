@@ -64,6 +64,9 @@ constexpr int kMaxSplit = 2;  // pieces of cut units per CTA range: its first an
 constexpr int kPhaseB = 8;   // page of a batch at which the next batch's page-table loads are issued
 constexpr int kPhaseC = 16;  // and at which their values are used
 constexpr int kMaxUnits = 4096;
+// resident-list entries (units x k) a launch may address: the prefix over the counts and the
+// per-range sub-page numbers (up to two sub-pages per block) then fit a 32-bit int
+constexpr int64_t kMaxEntries = (int64_t)1 << 28;
 constexpr int kMaxSlots = 2;  // combine slots between the consumer warps and the epilogue warp
 constexpr int kMaxGrid = 1024;
 constexpr float kLog2e = 1.4426950408889634f;
@@ -676,16 +679,17 @@ __global__ void __launch_bounds__(threads_of<NC>(), 1) sparse_attn_kernel(const 
   const int64_t start = range_start(c, N, Gp), end = range_start(c + 1, N, Gp);
   const RangeOrder order = range_order(prefix, a.units, start, end);
   // this warp's pages: sub-page i = warp + 4 k of the range, k = 0 .. n_mine-1, in stage i % kStages
-  const int64_t n_sub = (end - start) * C::kSub;
-  const int64_t n_mine = n_sub > warp ? (n_sub - 1 - warp) / kConsumerWarps + 1 : 0;
+  // sub-page numbers within the range fit 32 bits: the host bounds units * k by 2^28
+  const int n_sub = (int)(end - start) * C::kSub;
+  const int n_mine = n_sub > warp ? (n_sub - 1 - warp) / kConsumerWarps + 1 : 0;
   const uint32_t ring_s = smem_u32(ring);
   // Page kk of this warp, first half of its resolution: its unit, list entry and sequence length.
-  auto resolve_a = [&](int64_t kk, int& ru, int& rj, int& rlen) {
+  auto resolve_a = [&](int kk, int& ru, int& rj, int& rlen) {
     ru = -1;
     rj = -1;
     rlen = 0;
     if (kk < n_mine) {
-      const int64_t x = order.at((warp + (int64_t)kConsumerWarps * kk) / C::kSub);
+      const int64_t x = order.at((warp + kConsumerWarps * kk) / C::kSub);
       ru = unit_of(prefix, a.units, x);
       rj = a.res_list[(int64_t)ru * a.k + (x - prefix[ru])];
       rlen = a.seq_len[ru / a.Hkv];
@@ -701,11 +705,11 @@ __global__ void __launch_bounds__(threads_of<NC>(), 1) sparse_attn_kernel(const 
   };
   // Third: the pool row of the sub-page and its valid tokens (0 = nothing to load).  An entry
   // outside the sequence or the pool is skipped and reported.
-  auto resolve_c = [&](int64_t kk, int ru, int rj, int rlen, int sl, int& row, int& nt) {
+  auto resolve_c = [&](int kk, int ru, int rj, int rlen, int sl, int& row, int& nt) {
     row = 0;
     nt = 0;
     if (ru < 0) return;
-    const int h = (int)((warp + (int64_t)kConsumerWarps * kk) % C::kSub);
+    const int h = (warp + kConsumerWarps * kk) % C::kSub;
     const int nv = rj >= 0 && rj < a.nblk_cap ? min(P, rlen - rj * P) : 0;
     if (nv <= 0 || sl < 0 || sl >= a.n_slots) {
       if (h == 0) report(a.status, SCOUT_DEV_BAD_INDEX);
@@ -716,8 +720,8 @@ __global__ void __launch_bounds__(threads_of<NC>(), 1) sparse_attn_kernel(const 
   };
   // Load the K (which = 0) or V (which = 1) half of page kk (one lane): both 64-column halves
   // in one box.
-  auto issue = [&](int64_t kk, int row, int nt, int which) {
-    const int stage = (int)((warp + (int64_t)kConsumerWarps * kk) % C::kStages);
+  auto issue = [&](int kk, int row, int nt, int which) {
+    const int stage = (warp + kConsumerWarps * kk) % C::kStages;
     uint64_t* bar = which ? &vfull[stage] : &kfull[stage];
     if (nt > 0) {
       uint8_t* sp = ring + stage * C::kStageBytes + which * 2 * C::kHalfBytes;
@@ -733,13 +737,13 @@ __global__ void __launch_bounds__(threads_of<NC>(), 1) sparse_attn_kernel(const 
   resolve_a(lane, pu, pj, plen);
   resolve_b(pu, pj, psl);
   resolve_c(lane, pu, pj, plen, psl, cur_row, cur_nt);
-  auto nt_of = [&](int64_t kk) {
-    return __shfl_sync(0xffffffffu, (kk >> 5) == cur_b ? cur_nt : nxt_nt, (int)(kk & 31));
+  auto nt_of = [&](int kk) {
+    return __shfl_sync(0xffffffffu, (kk >> 5) == cur_b ? cur_nt : nxt_nt, kk & 31);
   };
   // page kk is next in this warp's order: move to its batch when it opens one, and start
   // resolving the batch after it (list entries now, page-table slots kPhaseB pages later)
-  auto advance = [&](int64_t kk) {
-    const int m = (int)(kk & 31);
+  auto advance = [&](int kk) {
+    const int m = kk & 31;
     if (m == 0 && kk > 0) {
       cur_row = nxt_row;
       cur_nt = nxt_nt;
@@ -753,17 +757,17 @@ __global__ void __launch_bounds__(threads_of<NC>(), 1) sparse_attn_kernel(const 
   // further on, the K halves once the scores are computed, the V halves after P V; lane j
   // issues the copy of page kk + j, so the two go out together.  where() gives a lane the
   // pool row and valid tokens of its page (read before the halves are issued).
-  auto where = [&](int64_t kk, int n, int& row, int& nt) {
-    const int64_t kr = kk + C::kPerWarp + (lane < n ? lane : 0);
-    const int src = (int)(kr & 31);
+  auto where = [&](int kk, int n, int& row, int& nt) {
+    const int kr = kk + C::kPerWarp + (lane < n ? lane : 0);
+    const int src = kr & 31;
     const int rc = __shfl_sync(0xffffffffu, cur_row, src), rn = __shfl_sync(0xffffffffu, nxt_row, src);
     const int tc = __shfl_sync(0xffffffffu, cur_nt, src), tn = __shfl_sync(0xffffffffu, nxt_nt, src);
     const bool in_cur = (kr >> 5) == cur_b;
     row = in_cur ? rc : rn;
     nt = in_cur ? tc : tn;
   };
-  auto refill = [&](int64_t kk, int n, int row, int nt, int which) {
-    const int64_t kr = kk + C::kPerWarp + (lane < n ? lane : 0);
+  auto refill = [&](int kk, int n, int row, int nt, int which) {
+    const int kr = kk + C::kPerWarp + (lane < n ? lane : 0);
     if (lane < n && kr < n_mine) issue(kr, row, nt, which);
   };
 
@@ -781,7 +785,7 @@ __global__ void __launch_bounds__(threads_of<NC>(), 1) sparse_attn_kernel(const 
   bool have = it.next(u, lo, hi);
   uint32_t qa[8][2], qn[8][2];
   if (have) load_q(a, u, lane, qa);
-  int64_t i = 0;
+  int i = 0;
   bool ok = true;  // false after a bounded wait ran out
   for (int sg = 0; have; ++sg) {
     // prefetch the next segment's query while this one streams
@@ -796,11 +800,11 @@ __global__ void __launch_bounds__(threads_of<NC>(), 1) sparse_attn_kernel(const 
 #pragma unroll
     for (int d = 0; d < 8; ++d) st.o[d][0] = st.o[d][1] = st.o[d][2] = st.o[d][3] = 0.f;
     // this warp's sub-pages of the segment (global sub-page numbers ii = warp (mod 4)), two at a time
-    const int64_t seg_lo = i, seg_hi = i + (hi - lo) * C::kSub;
-    for (int64_t ii = seg_lo + (warp - seg_lo % kConsumerWarps + kConsumerWarps) % kConsumerWarps; ii < seg_hi;
+    const int seg_lo = i, seg_hi = i + (int)(hi - lo) * C::kSub;
+    for (int ii = seg_lo + (warp - seg_lo % kConsumerWarps + kConsumerWarps) % kConsumerWarps; ii < seg_hi;
          ii += kPair * kConsumerWarps) {
       const bool two = kPair == 2 && ii + kConsumerWarps < seg_hi;
-      const int64_t k = ii / kConsumerWarps;
+      const int k = ii / kConsumerWarps;
       advance(k);
       const int nt0 = nt_of(k);
       int nt1 = 0;
@@ -808,7 +812,7 @@ __global__ void __launch_bounds__(threads_of<NC>(), 1) sparse_attn_kernel(const 
         advance(k + 1);
         nt1 = nt_of(k + 1);
       }
-      const int st0 = (int)(ii % C::kStages), st1 = (int)((ii + kConsumerWarps) % C::kStages);
+      const int st0 = ii % C::kStages, st1 = (ii + kConsumerWarps) % C::kStages;
       const uint32_t ph0 = (uint32_t)(k / C::kPerWarp) & 1u, ph1 = (uint32_t)((k + 1) / C::kPerWarp) & 1u;
       int nrow, nnt;  // the page (of the next ones) whose halves this lane refills
       where(k, two ? 2 : 1, nrow, nnt);
@@ -834,9 +838,9 @@ __global__ void __launch_bounds__(threads_of<NC>(), 1) sparse_attn_kernel(const 
           if (ntx > 0) attend_scores<C::PS, 1>(kbs, nts, qa, a.scale_log2, reinterpret_cast<float(&)[MT][4]>(sc), lane);
         }
       }
-      // the K halves may be reloaded once every lane has read them
+      // the K halves may be reloaded once every lane has read them (ldmatrix only: those reads
+      // returned before the MMAs that use them issued, so no proxy fence is needed)
       if (ok) {
-        fence_proxy_async();
         __syncwarp();
         refill(k, two ? 2 : 1, nrow, nnt, 0);
       }
@@ -848,10 +852,16 @@ __global__ void __launch_bounds__(threads_of<NC>(), 1) sparse_attn_kernel(const 
           ok = false;
         }
       }
+      bool cleared = false;  // generic stores went into a V half (warp-uniform)
       if (got) {
-        if (nt0 > 0 && nt0 < C::PS) clear_tail_rows<C::PS>(ring + st0 * C::kStageBytes + 2 * C::kHalfBytes, nt0, lane);
-        if (two && nt1 > 0 && nt1 < C::PS)
+        if (nt0 > 0 && nt0 < C::PS) {
+          clear_tail_rows<C::PS>(ring + st0 * C::kStageBytes + 2 * C::kHalfBytes, nt0, lane);
+          cleared = true;
+        }
+        if (two && nt1 > 0 && nt1 < C::PS) {
           clear_tail_rows<C::PS>(ring + st1 * C::kStageBytes + 2 * C::kHalfBytes, nt1, lane);
+          cleared = true;
+        }
         if (pair) {
           const uint32_t vbs[2] = {kb0 + 2 * C::kHalfBytes, kb1 + 2 * C::kHalfBytes};
           attend_values<C::PS, 2>(vbs, sc, st, lane);
@@ -860,9 +870,10 @@ __global__ void __launch_bounds__(threads_of<NC>(), 1) sparse_attn_kernel(const 
           attend_values<C::PS, 1>(vbs, reinterpret_cast<float(&)[MT][4]>(sc), st, lane);
         }
       }
-      // and the V halves once P V is done
+      // and the V halves once P V is done; zeroed tail rows are generic writes, which the copy
+      // that overwrites them must be ordered after
       if (ok) {
-        fence_proxy_async();
+        if (cleared) fence_proxy_async();
         __syncwarp();
         refill(k, two ? 2 : 1, nrow, nnt, 1);
       }
@@ -1012,7 +1023,7 @@ int attn_entry(const void* q, const void* K_pool, const void* V_pool, int64_t n_
   const int64_t units = (int64_t)B * Hkv;
   const int G = Hq / Hkv;
   if (D != kD || !valid_P(P) || G > kMaxG || units > kMaxUnits || !aligned16(K_pool) || !aligned16(V_pool) ||
-      (reinterpret_cast<uintptr_t>(q) & 3u) || n_slots * P > (int64_t)0x7fffffff)
+      (reinterpret_cast<uintptr_t>(q) & 3u) || n_slots * P > (int64_t)0x7fffffff || units * k > kMaxEntries)
     return SCOUT_ERR_UNSUPPORTED;
   if (merge && (!aligned16(O_cpu) || (reinterpret_cast<uintptr_t>(O_out) & 7u))) return SCOUT_ERR_UNSUPPORTED;
   if (!merge && !aligned16(O_part)) return SCOUT_ERR_UNSUPPORTED;

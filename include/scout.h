@@ -278,7 +278,8 @@ int scout_resident_list(const uint32_t* resident_bits, const int32_t* seq_len, i
  * the total block count evenly; split units are combined by LSE.
  * workspace: scout_sparse_attn_workspace_bytes() bytes; its first 4 * B * Hkv
  * bytes must be zero before the first use and are left zero by every call.
- * K_pool / V_pool must be 16-byte aligned.  Requires G <= 8, res_count <= k.
+ * K_pool / V_pool must be 16-byte aligned.  Requires G <= 8, res_count <= k,
+ * B * Hkv <= 4096 and B * Hkv * k <= 2^28 (else SCOUT_ERR_UNSUPPORTED).
  * ------------------------------------------------------------------------ */
 size_t scout_sparse_attn_workspace_bytes(int B, int Hq, int Hkv, int D, int P);
 int scout_sparse_attn(const void* q, const void* K_pool, const void* V_pool, int64_t n_slots,
