@@ -517,6 +517,8 @@ __global__ void __launch_bounds__(kThreadsAll, 1) score_topk_kernel(const __grid
       return min(a.nblk_cap, (max(L, 0) + a.P - 1) / a.P);
     };
     int64_t i = 0;  // stages issued
+    int st = 0;     // i % stages, kept running (no division per chunk)
+    uint32_t ph = 0u;  // (i / stages) & 1
     bool q_ready = false, ok = true;
     int u = resolve(atomicAdd(a.counters, 1));
     while (u >= 0) {
@@ -525,9 +527,8 @@ __global__ void __launch_bounds__(kThreadsAll, 1) score_topk_kernel(const __grid
       const int t_next = atomicAdd(a.counters, 1);
       const int nv = nvalid_of(u / a.Hkv);
       const int b = u / a.Hkv, kvh = u - b * a.Hkv;
-      for (int ch = 0; ok && ch < a.nchunk; ++ch, ++i) {
-        const int st = (int)(i % a.stages);
-        if (!mbar_wait(&empty_bar[st], (uint32_t)((i / a.stages) & 1) ^ 1u)) {
+      for (int ch = 0; ok && ch < a.nchunk; ++ch, ++i, st = st + 1 == a.stages ? 0 : st + 1, ph ^= st == 0) {
+        if (!mbar_wait(&empty_bar[st], ph ^ 1u)) {
           report(a.status, SCOUT_DEV_TIMEOUT);
           ok = false;
           break;
@@ -568,8 +569,7 @@ __global__ void __launch_bounds__(kThreadsAll, 1) score_topk_kernel(const __grid
     // this grid's CTAs leave while they finish their last units
     release_dependents();
     if (ok) {  // a stage tagged -1 ends the scoring warps' loop
-      const int st = (int)(i % a.stages);
-      if (mbar_wait(&empty_bar[st], (uint32_t)((i / a.stages) & 1) ^ 1u)) {
+      if (mbar_wait(&empty_bar[st], ph ^ 1u)) {
         stage_unit[st] = -1;
         mbar_arrive(&full_bar[st]);
         ++i;
@@ -615,9 +615,9 @@ __global__ void __launch_bounds__(kThreadsAll, 1) score_topk_kernel(const __grid
   const int g = lane >> 2, t = lane & 3;
   int ucur = -1, kb = 0, e = -1, ch = 0, nvalid = 0;
   uint32_t bmm[16][2], bme[8][2];
-  for (int64_t i = 0;; ++i) {
-    const int st = (int)(i % a.stages);
-    const bool landed = mbar_wait_n(&full_bar[st], (uint32_t)((i / a.stages) & 1), a.score_wait);
+  // stage st of the ring, phase ph, advanced after every chunk (no division per chunk)
+  for (int st = 0, ph = 0;; st = st + 1 == a.stages ? 0 : st + 1, ph ^= st == 0) {
+    const bool landed = mbar_wait_n(&full_bar[st], (uint32_t)ph, a.score_wait);
     if (!landed && lane == 0) report(a.status, SCOUT_DEV_TIMEOUT);
     const int u = landed ? stage_unit[st] : -1;
     if (u < 0) break;
