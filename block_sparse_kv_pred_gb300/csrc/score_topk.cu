@@ -84,32 +84,53 @@ __device__ __forceinline__ void mean_b_frag(const __nv_bfloat16* qs, int G, int 
 // A chunk of 128 digest rows sits in shared memory as four TMA boxes of
 // 128 rows x 128 bytes (row bytes [128 b, 128 b + 128) in box b), each with the
 // 128-byte swizzle: 16-byte chunk c of row r lives at chunk c ^ (r % 8).
-__device__ __forceinline__ uint32_t tile_addr(uint32_t base, int r, int C) {
-  return base + (uint32_t)((C >> 3) * kBoxBytes + r * 128 + (((C & 7) ^ (r & 7)) << 4));
+//   address(r, C) = (C >> 3) * kBoxBytes + r * 128 + (((C & 7) ^ (r & 7)) << 4).
+// A scoring warp reads rows r0 + (lane part) whose r & 7 is a lane constant, at chunks
+// C = c + (a lane part smaller than the step of c) + 8 box, so each address is a per-lane offset
+// (one of four for the min/max digest, two for the mean) plus box * kBoxBytes, computed once.
+struct TileOfs {
+  uint32_t o[4];
+};
+// min/max: ldmatrix rows r0 + 8 ((lane >> 3) & 1) + (lane & 7), chunks 2 s + (lane >> 4):
+// o[i] covers c = 2 i (s & 3 = i), box s >> 2
+__device__ __forceinline__ TileOfs minmax_offsets(int r0, int lane) {
+  TileOfs t;
+  const uint32_t l7 = lane & 7, r = r0 + ((lane >> 3) & 1) * 8 + l7, hb = lane >> 4;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) t.o[i] = r * 128 + (((2u * i) ^ hb ^ l7) << 4);
+  return t;
+}
+// mean: rows r0 + g (and r0 + g + 8, 1024 bytes further), chunks 4 i + t: o[i & 1] covers
+// c = 4 (i & 1), box i >> 1
+__device__ __forceinline__ TileOfs mean_offsets(int r0, int lane) {
+  TileOfs t;
+  const uint32_t g = lane >> 2, tt = lane & 3;
+#pragma unroll
+  for (int i = 0; i < 2; ++i) t.o[i] = (r0 + g) * 128 + (((4u * i) ^ tt ^ g) << 4);
+  t.o[2] = t.o[3] = 0u;
+  return t;
 }
 
 // Scores of the warp's 16 rows (local rows r0 .. r0 + 15): c = rows g, g + 8 x heads 2t, 2t+1.
 template <int KIND>
-__device__ __forceinline__ void score_tile(uint32_t tbase, int r0, int lane, const uint32_t (&bmm)[16][2],
+__device__ __forceinline__ void score_tile(uint32_t tbase, const TileOfs& to, const uint32_t (&bmm)[16][2],
                                            const uint32_t (&bme)[8][2], float (&c)[4]) {
   float acc[4][4];
 #pragma unroll
   for (int j = 0; j < 4; ++j) acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.f;
   if (KIND == SCOUT_DIGEST_MINMAX) {
-    const int r = r0 + ((lane >> 3) & 1) * 8 + (lane & 7);
 #pragma unroll
     for (int s = 0; s < 16; ++s) {  // four independent accumulation chains
       uint32_t a0, a1, a2, a3;
-      ldsm_x4(tile_addr(tbase, r, 2 * s + (lane >> 4)), a0, a1, a2, a3);
+      ldsm_x4(tbase + to.o[s & 3] + (s >> 2) * kBoxBytes, a0, a1, a2, a3);
       mma_bf16(acc[s & 3], a0, a1, a2, a3, bmm[s][0], bmm[s][1]);
     }
   } else {
-    const int g = lane >> 2, t = lane & 3;
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
       // four fp32 channels i*16 + 4t .. +3 of rows g and g + 8, split exactly as hi + mid + lo (bf16)
       uint4 v0, v1;
-      const uint32_t p0 = tile_addr(tbase, r0 + g, i * 4 + t), p1 = tile_addr(tbase, r0 + g + 8, i * 4 + t);
+      const uint32_t p0 = tbase + to.o[i & 1] + (i >> 1) * kBoxBytes, p1 = p0 + 8 * 128;
       asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v0.x), "=r"(v0.y), "=r"(v0.z), "=r"(v0.w) : "r"(p0));
       asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v1.x), "=r"(v1.y), "=r"(v1.z), "=r"(v1.w) : "r"(p1));
       const float x0[4] = {__uint_as_float(v0.x), __uint_as_float(v0.y), __uint_as_float(v0.z), __uint_as_float(v0.w)};
@@ -613,6 +634,7 @@ __global__ void __launch_bounds__(kThreadsAll, 1) score_topk_kernel(const __grid
 
   // ---------------- scoring warps 0..7 -----------------------------------------
   const int g = lane >> 2, t = lane & 3;
+  const TileOfs tofs = KIND == SCOUT_DIGEST_MINMAX ? minmax_offsets(warp * 16, lane) : mean_offsets(warp * 16, lane);
   int ucur = -1, kb = 0, e = -1, ch = 0, nvalid = 0;
   uint32_t bmm[16][2], bme[8][2];
   // stage st of the ring, phase ph, advanced after every chunk (no division per chunk)
@@ -647,7 +669,7 @@ __global__ void __launch_bounds__(kThreadsAll, 1) score_topk_kernel(const __grid
     const int j0 = ch * kChunk + warp * 16;
     if (j0 < a.nblk_cap) {
       float c[4] = {0.f, 0.f, 0.f, 0.f};
-      if (j0 < nvalid) score_tile<KIND>(smem_u32(sp), warp * 16, lane, bmm, bme, c);
+      if (j0 < nvalid) score_tile<KIND>(smem_u32(sp), tofs, bmm, bme, c);
       // pool over the heads of the group (columns 2t, 2t+1 < G), then across t; for the sum the
       // order is ((h0 + h1) + (h2 + h3)) + ((h4 + h5) + (h6 + h7)), the same on every lane
       const float ninf = -INFINITY;
