@@ -189,11 +189,11 @@ def test_score_topk_parity(name):
     assert exact >= s.units - 1
 
 
-def _integer_case(kind, seed=0, k_range=(-3, 4), q_range=(-2, 3)):
+def _integer_case(kind, seed=0, k_range=(-3, 4), q_range=(-2, 3), nblk=301, k=37):
     """Small-integer K and q: every fp32 score is exact, so GPU and fp64 scores agree bit for bit and
     the many ties exercise the lowest-index rule."""
     rng = np.random.default_rng(seed)
-    B, Hq, Hkv, P, T, k = 2, 10, 2, 32, 300 * 32 + 8, 37
+    B, Hq, Hkv, P, T = 2, 10, 2, 32, (nblk - 1) * 32 + 8
     G, D = Hq // Hkv, 128
     nb = -(-T // P)
     seq = np.array([T, 130 * 32 + 1], dtype=np.int32)
@@ -251,6 +251,15 @@ def test_score_topk_ties_beyond_the_candidate_limit(k_range, max_ctas):
     than 64 candidates share the k-th key, and the lowest-index ones are taken."""
     c = _integer_case("minmax", seed=3, k_range=k_range, q_range=(1, 2))
     _check_integer_case(c, "minmax", max_ctas, min_ties=200)
+
+
+@pytest.mark.parametrize("kind,k_range,k", [("minmax", (-3, 4), 37), ("mean", (-3, 4), 200), ("minmax", (0, 2), 64)])
+def test_score_topk_bit_exact_over_several_key_groups(kind, k_range, k):
+    """2,101 blocks per unit: the selection takes the keys 1,024 at a time (three groups, the last
+    ragged) in every counting round; tie-heavy integer scores keep the lists bit-exact."""
+    c = _integer_case(kind, seed=7, k_range=k_range, q_range=(1, 2) if k_range == (0, 2) else (-2, 3),
+                      nblk=2101, k=k)
+    _check_integer_case(c, kind, None, min_ties=500)
 
 
 def _attn_lists(s, rng, force_split=False):
