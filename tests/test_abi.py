@@ -69,6 +69,8 @@ def test_host_validation_rejects_without_launch(L):
                                4, 0.1, fake, fake, fake, 1 << 24, None, None, None) == 2  # misaligned pool
     assert L.scout_sparse_attn(fake, fake, fake, 100, fake, fake, fake, fake, 1, 8, 2, 128, 32, 8, (1 << 27) + 1,
                                0.1, fake, fake, fake, 1 << 24, None, None, None) == 2  # B Hkv k > 2^28 entries
+    assert L.scout_sparse_attn(fake, fake, fake, 100, fake, fake, fake, fake, 2049, 8, 2, 128, 32, 8, 4, 0.1, fake,
+                               fake, fake, 1 << 30, None, None, None) == 2  # B Hkv = 4098 units > 4096
     neg = ctypes.pointer(bs.Launch(-1))
     assert L.scout_predict_q(fake, fake, fake, 8, 128, 64, None, neg, None) == 1  # max_ctas < 0
     assert L.scout_sparse_attn_merge(fake, fake, fake, 100, fake, fake, fake, fake, 1, 8, 2, 128, 32, 8, 4, 0.1,
