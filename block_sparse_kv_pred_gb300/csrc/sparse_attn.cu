@@ -36,8 +36,10 @@ namespace {
 // (graph replay, same box, back to back): four warps (three stages each) 58.36 us per step and
 // 33.3 us alone, six 57.78 us and 30.1 us alone, six with two pages per pass 59.08 us; eight
 // warps with 16-token stages were ~15% slower than four (the per-page overhead doubles).  Six
-// warps' combine state leaves room for the whole ring up to G = 5 at 320 units; past that the
-// launch takes four warps (three stages each, a smaller combine state) before a smaller ring.
+// warps' combine state leaves room for the whole ring and two combine slots up to G = 5 at 320
+// units (with one slot, warps that finish a short segment wait for the epilogue to drain the
+// previous one); past that a launch takes one slot, then four warps (three stages each, a
+// smaller combine state), then a smaller ring.
 #ifndef SCOUT_ATTN_CONSUMERS
 #define SCOUT_ATTN_CONSUMERS 6
 #endif
@@ -357,10 +359,6 @@ __device__ __forceinline__ void load_q(const AttnArgs& a, int u, int lane, uint3
   }
 }
 
-// A piece of a cut unit handed from the epilogue warp to the split warp in shared memory:
-// per-head LSE (natural log) then the normalised output, [G][128] fp32.
-__host__ __device__ constexpr int stage_floats(int G) { return kMaxG + G * kD; }
-
 // The CPU partial of a unit (merge only): lane l holds dims 4l .. 4l+3 of every head and the
 // LSE of head l.  Loaded ahead of its use so that the latency overlaps other work.
 struct CpuPart {
@@ -419,14 +417,11 @@ __device__ __forceinline__ void store4(const AttnArgs& a, int uu, int h, int lan
 }
 
 // The split warp of a CTA: a unit cut by range boundaries has one piece per CTA range it
-// touches (c0 .. c1).  Each piece (staged in shared memory by the CTA's epilogue, signalled on
-// sbar) is published to the workspace and counted; the piece that completes the count (last
-// to arrive) merges all of them by their LSE.  Nothing waits on another CTA.
-__device__ void run_split_warp(const AttnArgs& a, const int* prefix, int64_t N, int Gp, int c, const float* staging,
-                               uint64_t* sbar, float* sfin, float* swg, float* swc, int lane) {
-  // A unit cut by range boundaries has one piece per CTA range it touches (c0 .. c1).  Each
-  // piece is published to the workspace and counted; the piece that completes the count
-  // (last to arrive) merges all of them by their LSE.  Nothing waits on another CTA.
+// touches (c0 .. c1).  Each piece is stored to its workspace slot by the CTA's epilogue warp,
+// which signals it on sbar; the split warp counts it, and the piece that completes the count
+// (last to arrive) merges all of them by their LSE.  Nothing waits on another CTA.
+__device__ void run_split_warp(const AttnArgs& a, const int* prefix, int64_t N, int Gp, int c, uint64_t* sbar,
+                               float* sfin, float* swg, float* swc, int lane) {
   const int64_t start = range_start(c, N, Gp), end = range_start(c + 1, N, Gp);
   SegIter it = seg_iter(prefix, a.units, range_order(prefix, a.units, start, end));
   int u, k = 0;
@@ -436,20 +431,14 @@ __device__ void run_split_warp(const AttnArgs& a, const int* prefix, int64_t N, 
     if (lo == prefix[u] && hi == prefix[u + 1]) continue;  // whole: the epilogue warp's
     if (k >= kMaxSplit) break;  // a range has at most two cut segments
     load_cpu(a, u, lane, cpu);  // used only if this piece completes the unit
+    // the epilogue's stores of the piece happen before its arrive; the fence below makes them
+    // visible, with this warp's, to the CTA that merges the unit
     if (!mbar_wait(&sbar[k], 0u) && lane == 0) report(a.status, SCOUT_DEV_TIMEOUT);
-    const float* stg = staging + k * stage_floats(a.G);
     ++k;
     const int c0 = cta_of(prefix[u], N, Gp), c1 = cta_of(prefix[u + 1] - 1, N, Gp);
     auto piece_slot = [&](int cc) {
       return (int64_t)cc * 2 + (prefix[u] <= range_start(cc, N, Gp) ? 0 : 1);
     };
-    const int64_t msl = piece_slot(c);
-    if (lane < a.G) a.slot_lse[msl * kMaxG + lane] = stg[lane];
-#pragma unroll
-    for (int h = 0; h < kMaxG; ++h)
-      if (h < a.G)
-        *reinterpret_cast<float4*>(a.slot_O + (msl * kMaxG + h) * kD + 4 * lane) =
-            *reinterpret_cast<const float4*>(stg + kMaxG + h * kD + 4 * lane);
     __threadfence();
     __syncwarp();
     int last = 0;
@@ -458,7 +447,7 @@ __device__ void run_split_warp(const AttnArgs& a, const int* prefix, int64_t N, 
     if (!last) continue;
     __threadfence();
     // merge the pieces by their LSE in one pass (running max per head): every load of a
-    // piece is issued at once, this CTA's own piece comes from shared memory
+    // piece is issued at once
     float mx[kMaxG], sm[kMaxG];
     float4 acc[kMaxG];
 #pragma unroll
@@ -474,13 +463,8 @@ __device__ void run_split_warp(const AttnArgs& a, const int* prefix, int64_t N, 
 #pragma unroll
       for (int h = 0; h < kMaxG; ++h) {
         if (h >= a.G) continue;
-        if (cc == c) {
-          pl[h] = stg[h];
-          po[h] = *reinterpret_cast<const float4*>(stg + kMaxG + h * kD + 4 * lane);
-        } else {
-          pl[h] = __ldcg(a.slot_lse + sl * kMaxG + h);
-          po[h] = __ldcg(reinterpret_cast<const float4*>(a.slot_O + (sl * kMaxG + h) * kD + 4 * lane));
-        }
+        pl[h] = __ldcg(a.slot_lse + sl * kMaxG + h);
+        po[h] = __ldcg(reinterpret_cast<const float4*>(a.slot_O + (sl * kMaxG + h) * kD + 4 * lane));
       }
 #pragma unroll
       for (int h = 0; h < kMaxG; ++h) {
@@ -527,13 +511,12 @@ __global__ void __launch_bounds__(threads_of<NC>(), 1) sparse_attn_kernel(const 
   __shared__ float efin[kMaxG], fwg[kMaxG], fwc[kMaxG];     // epilogue final LSE, merge weights
   __shared__ float sfin[kMaxG], swg[kMaxG], swc[kMaxG];    // split warp final LSE, merge weights
 
-  // dynamic shared memory: [ring (1024-aligned)][combine slots][split pieces][unit prefix]
+  // dynamic shared memory: [ring (1024-aligned)][combine slots][unit prefix]
   const uint32_t raw = smem_u32(smem_raw);
   uint8_t* ring = smem_raw + (((raw + 1023u) & ~1023u) - raw);
   float* cbf = reinterpret_cast<float*>(ring + C::kRingBytes);
   const int slot_f = slot_floats(a.G, NC);
-  float* staging = cbf + a.nslots * slot_f;  // [kMaxSplit][stage_floats(G)]
-  int* prefix = reinterpret_cast<int*>(staging + kMaxSplit * stage_floats(a.G));  // [units + 1]
+  int* prefix = reinterpret_cast<int*>(cbf + a.nslots * slot_f);  // [units + 1]
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   if (tid == 0) {
@@ -651,13 +634,14 @@ __global__ void __launch_bounds__(threads_of<NC>(), 1) sparse_attn_kernel(const 
         for (int h = 0; h < kMaxG; ++h)
           if (h < a.G) store4(a, u, h, lane, own4(h), fwg, fwc, cpu);
       } else {
-        // a unit cut by a range boundary: the piece goes to the split warp through shared
-        // memory, so that no global round trip holds the combine slot or this warp
-        float* stg = staging + min(nsplit, kMaxSplit - 1) * stage_floats(a.G);
-        if (lane < a.G) stg[lane] = eown[lane];
+        // a unit cut by a range boundary: the piece is stored to its workspace slot (the range's
+        // first or last segment) and the split warp, signalled through shared memory, counts it;
+        // no global round trip holds the combine slot or this warp
+        const int64_t msl = (int64_t)c * 2 + (prefix[u] <= start ? 0 : 1);
+        if (lane < a.G) a.slot_lse[msl * kMaxG + lane] = eown[lane];
 #pragma unroll
         for (int h = 0; h < kMaxG; ++h)
-          if (h < a.G) *reinterpret_cast<float4*>(stg + kMaxG + h * kD + 4 * lane) = own4(h);
+          if (h < a.G) *reinterpret_cast<float4*>(a.slot_O + (msl * kMaxG + h) * kD + 4 * lane) = own4(h);
         __syncwarp();
         if (lane == 0 && nsplit < kMaxSplit) mbar_arrive(&sbar[nsplit]);
         ++nsplit;
@@ -669,7 +653,7 @@ __global__ void __launch_bounds__(threads_of<NC>(), 1) sparse_attn_kernel(const 
   }
 
   if (warp == kSplitWarp) {
-    if (c < Gp) run_split_warp(a, prefix, N, Gp, c, staging, sbar, sfin, swg, swc, lane);
+    if (c < Gp) run_split_warp(a, prefix, N, Gp, c, sbar, sfin, swg, swc, lane);
     return;
   }
 
@@ -932,7 +916,7 @@ constexpr size_t kSlotOBytes = (size_t)kMaxGrid * 2 * kMaxG * kD * sizeof(float)
 template <int P, int S, int NC>
 size_t dyn_smem(int units, int G, int nslots) {
   return 1024 + Cfg<P, S, NC>::kRingBytes + (size_t)nslots * slot_floats(G, NC) * sizeof(float) +
-         (size_t)kMaxSplit * stage_floats(G) * sizeof(float) + (size_t)(units + 1) * 4;
+         (size_t)(units + 1) * 4;
 }
 constexpr size_t kSmemLimit = 232448 - 1024;  // per-block shared memory minus room for static use
 
