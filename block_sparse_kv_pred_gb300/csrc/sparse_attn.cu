@@ -596,7 +596,7 @@ __global__ void __launch_bounds__(threads_of<NC>(), 1) sparse_attn_kernel(const 
       if (whole) load_cpu(a, u, lane, cpu);  // in flight while the unit's pages still stream
       if (!mbar_wait(&cfull[slot], (uint32_t)(sg / a.nslots) & 1u) && lane == 0) report(a.status, SCOUT_DEV_TIMEOUT);
       const SlotView<NC> cs{cbf + slot * slot_f, a.G};
-      // per-head weights of the four warps' states (normalised) and this piece's LSE
+      // per-head weights of the consumer warps' states (normalised) and this piece's LSE
       if (lane < a.G) {
         float M = -INFINITY;
 #pragma unroll
@@ -657,12 +657,12 @@ __global__ void __launch_bounds__(threads_of<NC>(), 1) sparse_attn_kernel(const 
     return;
   }
 
-  // ---------------- consumer warps 0..3 ----------------------------------------
+  // ---------------- consumer warps 0 .. NC-1 ------------------------------------
   if (c >= Gp) return;
   const int g = lane >> 2, t = lane & 3;
   const int64_t start = range_start(c, N, Gp), end = range_start(c + 1, N, Gp);
   const RangeOrder order = range_order(prefix, a.units, start, end);
-  // this warp's pages: sub-page i = warp + 4 k of the range, k = 0 .. n_mine-1, in stage i % kStages
+  // this warp's pages: sub-page i = warp + NC k of the range, k = 0 .. n_mine-1, in stage i % kStages
   // sub-page numbers within the range fit 32 bits: the host bounds units * k by 2^28
   const int n_sub = (int)(end - start) * C::kSub;
   const int n_mine = n_sub > warp ? (n_sub - 1 - warp) / kConsumerWarps + 1 : 0;
@@ -783,7 +783,7 @@ __global__ void __launch_bounds__(threads_of<NC>(), 1) sparse_attn_kernel(const 
     st.l[0] = st.l[1] = 0.f;
 #pragma unroll
     for (int d = 0; d < 8; ++d) st.o[d][0] = st.o[d][1] = st.o[d][2] = st.o[d][3] = 0.f;
-    // this warp's sub-pages of the segment (global sub-page numbers ii = warp (mod 4)), two at a time
+    // this warp's sub-pages of the segment (sub-page numbers ii = warp mod NC within the range)
     const int seg_lo = i, seg_hi = i + (int)(hi - lo) * C::kSub;
     for (int ii = seg_lo + (warp - seg_lo % kConsumerWarps + kConsumerWarps) % kConsumerWarps; ii < seg_hi;
          ii += kPair * kConsumerWarps) {
