@@ -9,8 +9,12 @@
 // finished by the last of them to arrive (self-resetting counter), which merges
 // the per-CTA partials by their LSE.  Only a range's first and last segment can be
 // cut, and the range is walked last segment first: both of a CTA's cut pieces are
-// then produced early, and a dedicated split warp publishes them and does the
+// then produced early, and a dedicated split warp counts them and does the
 // cross-CTA merge (dependent global round trips) while the whole units stream.
+// When the grid covers every unit and no unit is large (at most kUnitSubPagesPerWarp
+// sub-pages per consumer warp), CTA c takes unit c whole instead: nothing is cut, so
+// no cross-CTA merge (round trips that wait behind the K/V copies in flight) ends
+// the launch, and the longest CTA has one unit's pages.
 //
 // Inside a CTA: the NC consumer warps (six, or four when a larger group's combine
 // state needs the room) take the range's sub-pages round-robin.  Each warp owns
@@ -65,6 +69,9 @@ __host__ __device__ constexpr int threads_of() { return (NC + 2) * 32; }
 constexpr int kMaxSplit = 2;  // pieces of cut units per CTA range: its first and its last segment
 constexpr int kPhaseB = 8;   // page of a batch at which the next batch's page-table loads are issued
 constexpr int kPhaseC = 16;  // and at which their values are used
+// A launch whose grid covers every unit gives each CTA one whole unit when no unit has more than
+// this many sub-pages per consumer warp; otherwise the flattened blocks are split evenly.
+constexpr int kUnitSubPagesPerWarp = 8;
 constexpr int kMaxUnits = 4096;
 // resident-list entries (units x k) a launch may address: the prefix over the counts and the
 // per-range sub-page numbers (up to two sub-pages per block) then fit a 32-bit int
@@ -497,7 +504,9 @@ __device__ void run_split_warp(const AttnArgs& a, const int* prefix, int64_t N, 
   }
 }
 
-template <int P, int S, int NC>
+// UNITS: the launch's grid covers every unit, so the whole-unit partition may be taken (the
+// other instance compiles the flattened split alone).
+template <int P, int S, int NC, bool UNITS>
 __global__ void __launch_bounds__(threads_of<NC>(), 1) sparse_attn_kernel(const __grid_constant__ CUtensorMap tmK,
                                                                   const __grid_constant__ CUtensorMap tmV,
                                                                   const AttnArgs a) {
@@ -506,7 +515,7 @@ __global__ void __launch_bounds__(threads_of<NC>(), 1) sparse_attn_kernel(const 
   extern __shared__ uint8_t smem_raw[];
   // kfull / vfull: the K / V half of a stage has landed (one phase per fill of the stage)
   __shared__ uint64_t kfull[C::kStages], vfull[C::kStages], cfull[kMaxSlots], cempty[kMaxSlots], sbar[kMaxSplit];
-  __shared__ int wtot[kThreads / 32];
+  __shared__ int wtot[kThreads / 32], wmax[kThreads / 32];
   __shared__ float ew[kMaxG][kConsumerWarps], eown[kMaxG];  // epilogue weights
   __shared__ float efin[kMaxG], fwg[kMaxG], fwc[kMaxG];     // epilogue final LSE, merge weights
   __shared__ float sfin[kMaxG], swg[kMaxG], swc[kMaxG];    // split warp final LSE, merge weights
@@ -542,10 +551,15 @@ __global__ void __launch_bounds__(threads_of<NC>(), 1) sparse_attn_kernel(const 
   {
     const int per = (a.units + kThreads - 1) / kThreads;
     const int lo = min(a.units, tid * per), hi = min(a.units, lo + per);
-    int sum = 0;
+    int sum = 0, mx = 0;
     for (int u = lo; u < hi; ++u) {  // the counts are read once, kept in place of the prefix
       prefix[u] = min(max(a.res_count[u], 0), a.k);
       sum += prefix[u];
+      if constexpr (UNITS) mx = max(mx, prefix[u]);
+    }
+    if constexpr (UNITS) {
+      mx = __reduce_max_sync(0xffffffffu, mx);
+      if (lane == 0) wmax[warp] = mx;
     }
     int inc = sum;
 #pragma unroll
@@ -567,7 +581,17 @@ __global__ void __launch_bounds__(threads_of<NC>(), 1) sparse_attn_kernel(const 
     __syncthreads();
   }
   const int64_t N = prefix[a.units];
-  const int Gp = (int)min((int64_t)gridDim.x, N);
+  // With every unit small and the grid covering them, CTA c takes unit c whole: no unit is cut,
+  // so no merge of pieces across CTAs (global round trips behind the K/V copies in flight) ends
+  // the launch.  Otherwise range c is [c N / Gp, (c+1) N / Gp) of the flattened blocks.
+  bool by_unit = false;
+  if constexpr (UNITS) {
+    int maxc = 0;  // the largest clamped count
+    for (int w = 0; w < kThreads / 32; ++w) maxc = max(maxc, wmax[w]);
+    by_unit = a.units <= (int)gridDim.x && maxc * C::kSub <= kUnitSubPagesPerWarp * NC;
+  }
+  const int Gp = by_unit ? a.units : (int)min((int64_t)gridDim.x, N);
+  auto rstart = [&](int cc) -> int64_t { return by_unit ? (int64_t)prefix[cc] : range_start(cc, N, Gp); };
   const int c = blockIdx.x;
 
   if (warp == kEpilogueWarp) {
@@ -586,7 +610,7 @@ __global__ void __launch_bounds__(threads_of<NC>(), 1) sparse_attn_kernel(const 
       __syncwarp();
     }
     if (c >= Gp) return;
-    const int64_t start = range_start(c, N, Gp), end = range_start(c + 1, N, Gp);
+    const int64_t start = rstart(c), end = rstart(c + 1);
     SegIter it = seg_iter(prefix, a.units, range_order(prefix, a.units, start, end));
     int u, nsplit = 0;
     int64_t lo, hi;
@@ -653,14 +677,14 @@ __global__ void __launch_bounds__(threads_of<NC>(), 1) sparse_attn_kernel(const 
   }
 
   if (warp == kSplitWarp) {
-    if (c < Gp) run_split_warp(a, prefix, N, Gp, c, sbar, sfin, swg, swc, lane);
+    if (c < Gp && !by_unit) run_split_warp(a, prefix, N, Gp, c, sbar, sfin, swg, swc, lane);  // no cut unit otherwise
     return;
   }
 
   // ---------------- consumer warps 0 .. NC-1 ------------------------------------
   if (c >= Gp) return;
   const int g = lane >> 2, t = lane & 3;
-  const int64_t start = range_start(c, N, Gp), end = range_start(c + 1, N, Gp);
+  const int64_t start = rstart(c), end = rstart(c + 1);
   const RangeOrder order = range_order(prefix, a.units, start, end);
   // this warp's pages: sub-page i = warp + NC k of the range, k = 0 .. n_mine-1, in stage i % kStages
   // sub-page numbers within the range fit 32 bits: the host bounds units * k by 2^28
@@ -935,20 +959,19 @@ bool make_page_map(CUtensorMap* map, const void* pool, int64_t n_slots, int P, i
                       CU_TENSOR_MAP_SWIZZLE_128B) == CUDA_SUCCESS;
 }
 
-template <int P, int S, int NC>
-int launch_ring(const CUtensorMap& tmK, const CUtensorMap& tmV, AttnArgs a, const scout_launch* launch,
-                cudaStream_t stream) {
-  const int max_ctas = launch != nullptr ? launch->max_ctas : 0;
-  const size_t smem = dyn_smem<P, S, NC>(a.units, a.G, a.nslots);
+template <int P, int S, int NC, bool UNITS>
+bool prepare(size_t smem) {
+  auto kern = sparse_attn_kernel<P, S, NC, UNITS>;
+  return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) == cudaSuccess &&
+         cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, 100) == cudaSuccess;
+}
+
+template <int P, int S, int NC, bool UNITS>
+int launch_grid(const CUtensorMap& tmK, const CUtensorMap& tmV, const AttnArgs& a, const scout_launch* launch,
+                int grid, size_t smem, cudaStream_t stream) {
   constexpr int kThreads = threads_of<NC>();
-  auto kern = sparse_attn_kernel<P, S, NC>;
-  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess ||
-      cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, 100) != cudaSuccess)
-    return SCOUT_ERR_CUDA;
-  int occ = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, kThreads, smem) != cudaSuccess || occ < 1)
-    return SCOUT_ERR_CUDA;
-  const int grid = min(kMaxGrid, max_ctas > 0 ? max_ctas : sm_count() * occ);
+  auto kern = sparse_attn_kernel<P, S, NC, UNITS>;
+  if (UNITS && !prepare<P, S, NC, UNITS>(smem)) return SCOUT_ERR_CUDA;  // the other one was prepared for the query
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)grid);
   cfg.blockDim = dim3(kThreads);
@@ -959,6 +982,24 @@ int launch_ring(const CUtensorMap& tmK, const CUtensorMap& tmV, AttnArgs a, cons
   cfg.numAttrs = early_start_attrs(launch, attr, 0);
   if (cudaLaunchKernelEx(&cfg, kern, tmK, tmV, a) != cudaSuccess) return SCOUT_ERR_CUDA;
   return launch_status();
+}
+
+// One CTA per SM (or the caller's cap); the instance that may take whole units when the grid
+// covers them.
+template <int P, int S, int NC>
+int launch_ring(const CUtensorMap& tmK, const CUtensorMap& tmV, AttnArgs a, const scout_launch* launch,
+                cudaStream_t stream) {
+  const int max_ctas = launch != nullptr ? launch->max_ctas : 0;
+  const size_t smem = dyn_smem<P, S, NC>(a.units, a.G, a.nslots);
+  int occ = 0;
+  if (!prepare<P, S, NC, false>(smem) ||
+      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, sparse_attn_kernel<P, S, NC, false>, threads_of<NC>(),
+                                                    smem) != cudaSuccess ||
+      occ < 1)
+    return SCOUT_ERR_CUDA;
+  const int grid = min(kMaxGrid, max_ctas > 0 ? max_ctas : sm_count() * occ);
+  return a.units <= grid ? launch_grid<P, S, NC, true>(tmK, tmV, a, launch, grid, smem, stream)
+                         : launch_grid<P, S, NC, false>(tmK, tmV, a, launch, grid, smem, stream);
 }
 
 // The most combine slots that fit with ring S and NC consumer warps; 0 if none does.

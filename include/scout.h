@@ -275,7 +275,8 @@ int scout_resident_list(const uint32_t* resident_bits, const int32_t* seq_len, i
  * s_t = scale * q . k_t;  O_part = sum_t softmax(s)_t v_t (normalised, fp32
  * [B][Hq][D]);  lse_part = ln sum_t exp(s_t) (fp32 [B][Hq]).  An empty set
  * gives O = 0 and lse = -inf.  The work is balanced over the SMs by splitting
- * the total block count evenly; split units are combined by LSE.
+ * the total block count evenly, split units being combined by LSE; when the
+ * grid covers every unit and every unit is small, each CTA takes one whole unit.
  * workspace: scout_sparse_attn_workspace_bytes() bytes; its first 4 * B * Hkv
  * bytes must be zero before the first use and are left zero by every call.
  * K_pool / V_pool must be 16-byte aligned.  Requires G <= 8, res_count <= k,
